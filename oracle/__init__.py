@@ -1,0 +1,168 @@
+"""fp64 CPU oracle of the DSA hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never calls it, and it
+shares no code with the CUDA library: the arithmetic lives in ``dsa_oracle.c``
+(plain C, fp64, OpenMP), this module only marshals numpy arrays.
+
+Every function takes tensors/arrays that hold the exact values given to the GPU
+(bf16 or fp32) and widens them to float64 before the call.
+
+Pins (what checks this oracle against something other than itself) live in
+``tests/test_oracle_pins.py``; every oracle function is pinned, none is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dsa_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libdsa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile dsa_oracle.c into a shared library with gcc (-O2, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", _SRC, "-o", tmp, "-lm"]
+        )
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            lib.oracle_packed_metadata.argtypes = [P, I, I, P, P, P, P]
+            lib.oracle_packed_metadata.restype = I
+            lib.oracle_indexer_scores.argtypes = [P, P, P, I, I, P, P, ctypes.c_int64, P, P]
+            lib.oracle_indexer_scores.restype = None
+            lib.oracle_indexer_topk.argtypes = [P, P, P, P, P, I, I, I, I, P, P, P]
+            lib.oracle_indexer_topk.restype = None
+            lib.oracle_sparse_mla_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, P]
+            lib.oracle_sparse_mla_fwd.restype = None
+            lib.oracle_sparse_mla_bwd.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, P, P]
+            lib.oracle_sparse_mla_bwd.restype = None
+            _lib = lib
+    return _lib
+
+
+def _f64(x) -> np.ndarray:
+    """Widen a torch tensor (any float dtype, any device) or array to C-contiguous float64."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _i32(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def _i64(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.ascontiguousarray(x, dtype=np.int64)
+
+
+def _p(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data
+
+
+def packed_metadata(cu_seqlens, total_tokens: int):
+    """cu_seqlens [nseq+1] -> (seq_start[T], causal_len[T], max_seqlen, all_rows_nonempty)."""
+    cu = _i32(cu_seqlens)
+    T = int(total_tokens)
+    start = np.zeros(max(T, 1), np.int32)
+    clen = np.zeros(max(T, 1), np.int32)
+    mx = np.zeros(1, np.int32)
+    ne = np.zeros(1, np.int32)
+    rc = _load().oracle_packed_metadata(_p(cu), len(cu) - 1, T, _p(start), _p(clen), _p(mx), _p(ne))
+    if rc != 0:
+        raise ValueError("cu_seqlens must be a non-decreasing cover of [0, T]")
+    return start[:T], clen[:T], int(mx[0]), int(ne[0])
+
+
+def indexer_scores(q_idx_rows, k_idx, w_rows, pair_row, pair_key, with_magnitude: bool = False):
+    """fp64 indexer scores for explicit pairs (pair_row indexes q_idx_rows/w_rows)."""
+    q = _f64(q_idx_rows)
+    k = _f64(k_idx)
+    w = _f64(w_rows)
+    Hi, Di = q.shape[1], q.shape[2]
+    pr, pk = _i64(pair_row), _i64(pair_key)
+    out = np.zeros(len(pr), np.float64)
+    mag = np.zeros(len(pr), np.float64) if with_magnitude else None
+    _load().oracle_indexer_scores(_p(q), _p(k), _p(w), Hi, Di, _p(pr), _p(pk), len(pr), _p(out), _p(mag))
+    return (out, mag) if with_magnitude else out
+
+
+def indexer_topk(q_idx_rows, k_idx, w_rows, seq_start, row_t, K: int):
+    """Causal top-k for the given rows.
+
+    q_idx_rows [n, Hi, Di] and w_rows [n, Hi] hold only the requested rows,
+    row_t [n] their global token ids, seq_start [T] the per-token sequence
+    start.  Returns (idx [n, K] int32 ascending + -1 suffix, len [n], kth score [n]).
+    """
+    q = _f64(q_idx_rows)
+    k = _f64(k_idx)
+    w = _f64(w_rows)
+    n, Hi, Di = q.shape
+    st = _i32(seq_start)
+    rt = _i64(row_t)
+    idx = np.zeros((n, K), np.int32)
+    ln = np.zeros(n, np.int32)
+    kth = np.zeros(n, np.float64)
+    _load().oracle_indexer_topk(_p(q), _p(k), _p(w), _p(st), _p(rt), n, Hi, Di, int(K), _p(idx), _p(ln), _p(kth))
+    return idx, ln, kth
+
+
+def sparse_mla_fwd(q_rows, kv, idx_rows, scale: float, Dv: int = 512, len_rows=None):
+    """Sparse MLA forward for the given query rows -> (out [n,H,Dv], lse [n,H]) in fp64."""
+    q = _f64(q_rows)
+    kvf = _f64(kv).reshape(kv.shape[0], -1)
+    idx = _i32(idx_rows)
+    ln = None if len_rows is None else _i32(len_rows)
+    n, H, Dqk = q.shape
+    K = idx.shape[1]
+    out = np.zeros((n, H, Dv), np.float64)
+    lse = np.zeros((n, H), np.float64)
+    _load().oracle_sparse_mla_fwd(_p(q), _p(kvf), _p(idx), _p(ln), n, kvf.shape[0], H, Dqk, Dv, K,
+                                  float(scale), _p(out), _p(lse))
+    return out, lse
+
+
+def sparse_mla_bwd(q_rows, kv, idx_rows, dout_rows, scale: float, Dv: int = 512, len_rows=None, dkv=None):
+    """Sparse MLA backward for the given rows -> (dq [n,H,Dqk], dkv [Tk,Dqk]) in fp64.
+
+    dkv accumulates the contributions of exactly these rows (pass an existing
+    array to keep adding, as query chunks do)."""
+    q = _f64(q_rows)
+    kvf = _f64(kv).reshape(kv.shape[0], -1)
+    idx = _i32(idx_rows)
+    ln = None if len_rows is None else _i32(len_rows)
+    do = _f64(dout_rows)
+    n, H, Dqk = q.shape
+    K = idx.shape[1]
+    dq = np.zeros((n, H, Dqk), np.float64)
+    if dkv is None:
+        dkv = np.zeros((kvf.shape[0], Dqk), np.float64)
+    assert dkv.dtype == np.float64 and dkv.flags.c_contiguous
+    _load().oracle_sparse_mla_bwd(_p(q), _p(kvf), _p(idx), _p(ln), n, kvf.shape[0], H, Dqk, Dv, K,
+                                  float(scale), _p(do), _p(dq), _p(dkv))
+    return dq, dkv

@@ -1,0 +1,293 @@
+/*
+ * dsa_oracle.c -- plain, slow, fp64 CPU oracle of the DeepSeek Sparse Attention
+ * hot path.  TEST INFRASTRUCTURE ONLY: it is loaded by the tests, by the smoke
+ * check and by the CPU-baseline leg of the benchmark, never by the product path.
+ * It shares no code, header or constant with the CUDA library.
+ *
+ * Pages followed (cited by title and section):
+ *  [DSA-blog]  "Accelerating GLM-5.2 Long-Context Training with cuDNN Fused DSA
+ *              Kernels ..." (Megatron-Bridge discussion 4957), section "How DSA works".
+ *  [NoPE-PR]   SkyRL PR 2388 "NoPE / unaligned top-k for SparseMLA", sections
+ *              "Why" and "Change".
+ *  [cudnn_dsa] NeMo AutoModel API page glm_moe_dsa.kernels.cudnn_dsa: entries
+ *              cudnn_indexer_topk, cudnn_sparse_attention,
+ *              prepare_cudnn_dsa_packed_metadata, _compact_and_sort_indices.
+ *  [Chunk-PR]  SkyRL PR 2423 "query-chunked sparse attention", section "Summary".
+ *
+ * Every floating-point input arrives already widened to double by the caller,
+ * so the oracle computes in fp64 throughout.  Where the pages leave a step
+ * open, the reading taken is written next to the step.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* THD packing metadata                                                      */
+/* [cudnn_dsa] prepare_cudnn_dsa_packed_metadata: per query, the start of its */
+/* packed sequence and its real causal length.  Reading: with no context      */
+/* parallelism the query coordinates are the identity, so for token t in     */
+/* sequence i, start = cu[i] and causal length = t - cu[i] + 1 (the diagonal  */
+/* is included, "s <= t").                                                    */
+/* Returns 0 on success, -1 if cu_seqlens is not a non-decreasing cover of    */
+/* [0, T].                                                                    */
+/* ------------------------------------------------------------------------ */
+int oracle_packed_metadata(const int32_t *cu_seqlens, int num_seqs, int T,
+                           int32_t *seq_start, int32_t *causal_len,
+                           int32_t *max_seqlen, int32_t *all_rows_nonempty) {
+  if (num_seqs < 1 || cu_seqlens[0] != 0 || cu_seqlens[num_seqs] != T) return -1;
+  int mx = 0;
+  for (int i = 0; i < num_seqs; ++i) {
+    int a = cu_seqlens[i], b = cu_seqlens[i + 1];
+    if (b < a) return -1;
+    if (b - a > mx) mx = b - a;
+    for (int t = a; t < b; ++t) {
+      seq_start[t] = a;
+      causal_len[t] = t - a + 1;
+    }
+  }
+  *max_seqlen = mx;
+  /* every real token sees at least itself, so every row is nonempty */
+  *all_rows_nonempty = (T > 0) ? 1 : 0;
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Lightning-indexer score                                                   */
+/* [cudnn_dsa] cudnn_indexer_topk: index_q [T, H_index, 128], one shared      */
+/* index_k [T_k, 128], already-scaled head weights [T, H_index] ("the caller  */
+/* owns both scalings").  The pages do not print the formula; the reading is  */
+/*   score(t, s) = sum_h w[t,h] * max(0, sum_d q[t,h,d] * k[s,d]).            */
+/* ------------------------------------------------------------------------ */
+static double indexer_score(const double *q_t /*[Hi,Di]*/, const double *k_s /*[Di]*/,
+                            const double *w_t /*[Hi]*/, int Hi, int Di, double *mag) {
+  double score = 0.0, m = 0.0;
+  for (int h = 0; h < Hi; ++h) {
+    double dot = 0.0, adot = 0.0;
+    for (int d = 0; d < Di; ++d) {
+      dot += q_t[(size_t)h * Di + d] * k_s[d];
+      adot += fabs(q_t[(size_t)h * Di + d] * k_s[d]);
+    }
+    double relu = dot > 0.0 ? dot : 0.0;
+    score += w_t[h] * relu;
+    m += fabs(w_t[h]) * adot;
+  }
+  if (mag) *mag = m;
+  return score;
+}
+
+/* Scores for explicit (row, key) pairs.  q_rows holds the query rows named by
+ * pair_row (indices into q_rows), k holds all keys.  mag_out (nullable) gets
+ * sum_h |w| sum_d |q k|, the scale of the rounding error of any fp32
+ * evaluation of the same score. */
+void oracle_indexer_scores(const double *q_rows, const double *k, const double *w_rows,
+                           int Hi, int Di, const int64_t *pair_row, const int64_t *pair_key,
+                           int64_t npairs, double *out, double *mag_out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t p = 0; p < npairs; ++p) {
+    const double *q_t = q_rows + (size_t)pair_row[p] * Hi * Di;
+    const double *w_t = w_rows + (size_t)pair_row[p] * Hi;
+    double mag;
+    out[p] = indexer_score(q_t, k + (size_t)pair_key[p] * Di, w_t, Hi, Di, &mag);
+    if (mag_out) mag_out[p] = mag;
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Per-query causal top-k                                                    */
+/* [DSA-blog] "How DSA works": the indexer emits the top-k key indices per    */
+/* query.  [cudnn_dsa] cudnn_indexer_topk returns int32 global indices; the   */
+/* canonical form (cudnn_sparse_attention, topk_length) is a compact,         */
+/* ascending valid prefix followed by -1.                                     */
+/* Readings: candidates are the causal keys s in [start(t), t]; n = min(K, c);*/
+/* order by score descending, ties to the lower index; the n winners are     */
+/* written ascending, then K - n copies of -1; len[t] = n.                    */
+/* ------------------------------------------------------------------------ */
+typedef struct { double score; int32_t idx; } cand_t;
+
+static int cand_cmp(const void *a, const void *b) {
+  const cand_t *x = (const cand_t *)a, *y = (const cand_t *)b;
+  if (x->score > y->score) return -1;
+  if (x->score < y->score) return 1;
+  return (x->idx < y->idx) ? -1 : (x->idx > y->idx);
+}
+static int int_cmp(const void *a, const void *b) {
+  int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+  return (x > y) - (x < y);
+}
+
+/* q_rows/w_rows hold only the nrows requested rows; row_t[r] is the global
+ * token of row r (its causal window is [seq_start[row_t[r]], row_t[r]]).
+ * kth_out[r] (nullable) receives the score of the n-th winner (-inf if n = 0). */
+void oracle_indexer_topk(const double *q_rows, const double *k, const double *w_rows,
+                         const int32_t *seq_start, const int64_t *row_t, int nrows,
+                         int Hi, int Di, int K, int32_t *idx_out, int32_t *len_out,
+                         double *kth_out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < nrows; ++r) {
+    int64_t t = row_t[r];
+    int64_t b = seq_start[t];
+    int64_t c = t - b + 1;
+    cand_t *cand = (cand_t *)malloc(sizeof(cand_t) * (size_t)(c > 0 ? c : 1));
+    for (int64_t s = b; s <= t; ++s) {
+      cand[s - b].score = indexer_score(q_rows + (size_t)r * Hi * Di, k + (size_t)s * Di,
+                                        w_rows + (size_t)r * Hi, Hi, Di, NULL);
+      cand[s - b].idx = (int32_t)s;
+    }
+    qsort(cand, (size_t)c, sizeof(cand_t), cand_cmp); /* full sort: plain definition */
+    int n = (int)(c < K ? c : K);
+    int32_t *row = idx_out + (size_t)r * K;
+    for (int j = 0; j < n; ++j) row[j] = cand[j].idx;
+    qsort(row, (size_t)n, sizeof(int32_t), int_cmp);
+    for (int j = n; j < K; ++j) row[j] = -1;
+    len_out[r] = n;
+    if (kth_out) kth_out[r] = n > 0 ? cand[n - 1].score : -INFINITY;
+    free(cand);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Slot validity                                                              */
+/* [cudnn_dsa] cudnn_sparse_attention: -1 marks an invalid slot; topk_length  */
+/* (optional) bounds the valid prefix.  [NoPE-PR] "Change": the kernels mask  */
+/* -1 wherever it is.  Reading: a slot j is valid iff j < len (when given)    */
+/* and 0 <= idx < T_k.  Duplicate valid indices count once per slot.          */
+/* ------------------------------------------------------------------------ */
+static int slot_valid(const int32_t *idx_row, const int32_t *len, int64_t r, int j, int Tk) {
+  if (len && j >= len[r]) return 0;
+  int32_t i = idx_row[j];
+  return i >= 0 && i < Tk;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Absorbed sparse MLA forward                                                */
+/* [DSA-blog] "How DSA works" / "Why DSA needs fused kernels": every head of  */
+/* a query attends, as an MQA over one shared latent KV, only to that query's */
+/* selected rows.  [cudnn_dsa] cudnn_sparse_attention: q [T, H, 576],         */
+/* kv_latent [T_k, 1, 576], value = kv[..., :512], explicit softmax_scale,    */
+/* output [T, H, 512].  [NoPE-PR] "Change": value is key[..., :512].          */
+/* Per (t, h), over the valid slot set J:                                     */
+/*   z_j = scale * <q[t,h,:Dqk], kv[idx_j,:Dqk]>                              */
+/*   L   = log sum_j exp(z_j)      (natural log; -inf when J is empty)        */
+/*   O   = sum_j exp(z_j - L) kv[idx_j, :Dv]   (0 when J is empty)            */
+/* ------------------------------------------------------------------------ */
+static void fwd_row(const double *q_r /*[H,Dqk]*/, const double *kv, const int32_t *idx_row,
+                    const int32_t *len, int64_t r, int Tk, int H, int Dqk, int Dv, int K,
+                    double scale, double *o_r /*[H,Dv]*/, double *lse_r /*[H]*/,
+                    double *p_r /*[H,K] nullable: softmax weights per slot*/) {
+  double *z = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+  for (int h = 0; h < H; ++h) {
+    const double *qh = q_r + (size_t)h * Dqk;
+    double m = -INFINITY;
+    for (int j = 0; j < K; ++j) {
+      if (!slot_valid(idx_row, len, r, j, Tk)) { z[j] = -INFINITY; continue; }
+      const double *kr = kv + (size_t)idx_row[j] * Dqk;
+      double dot = 0.0;
+      for (int d = 0; d < Dqk; ++d) dot += qh[d] * kr[d];
+      z[j] = scale * dot;
+      if (z[j] > m) m = z[j];
+    }
+    double *oh = o_r + (size_t)h * Dv;
+    for (int v = 0; v < Dv; ++v) oh[v] = 0.0;
+    if (m == -INFINITY) {
+      lse_r[h] = -INFINITY;
+      if (p_r) for (int j = 0; j < K; ++j) p_r[(size_t)h * K + j] = 0.0;
+      continue;
+    }
+    double sum = 0.0;
+    for (int j = 0; j < K; ++j) if (z[j] != -INFINITY) sum += exp(z[j] - m);
+    double L = m + log(sum);
+    lse_r[h] = L;
+    for (int j = 0; j < K; ++j) {
+      double p = (z[j] == -INFINITY) ? 0.0 : exp(z[j] - L);
+      if (p_r) p_r[(size_t)h * K + j] = p;
+      if (p == 0.0) continue;
+      const double *vr = kv + (size_t)idx_row[j] * Dqk;
+      for (int v = 0; v < Dv; ++v) oh[v] += p * vr[v];
+    }
+  }
+  free(z);
+}
+
+/* q_rows [nrows, H, Dqk], idx_rows [nrows, K], len_rows [nrows] or NULL,
+ * kv [Tk, Dqk].  Outputs out [nrows, H, Dv], lse [nrows, H]. */
+void oracle_sparse_mla_fwd(const double *q_rows, const double *kv, const int32_t *idx_rows,
+                           const int32_t *len_rows, int nrows, int Tk, int H, int Dqk, int Dv,
+                           int K, double scale, double *out, double *lse) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < nrows; ++r)
+    fwd_row(q_rows + (size_t)r * H * Dqk, kv, idx_rows + (size_t)r * K, len_rows, r, Tk, H,
+            Dqk, Dv, K, scale, out + (size_t)r * H * Dv, lse + (size_t)r * H, NULL);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Absorbed sparse MLA backward (analytic gradient of the forward above)      */
+/* [cudnn_dsa] _CudnnSparseAttention.backward: gradients for the query        */
+/* [T, H, 576] and the latent KV, from grad_output [T, H, 512].               */
+/* With P_j = exp(z_j - L), D = <dO, O>, dP_j = <dO, kv[idx_j,:Dv]>,           */
+/* dS_j = P_j (dP_j - D):                                                     */
+/*   dq[t,h,:]        = scale * sum_j dS_j kv[idx_j, :Dqk]                    */
+/*   dkv[idx_j, :Dqk] += scale * sum_h dS_j q[t,h,:]                          */
+/*   dkv[idx_j, :Dv]  += sum_h P_j dO[t,h,:]                                  */
+/* O here is the oracle's own fp64 forward output.  [Chunk-PR] "Summary":     */
+/* query rows are independent and key gradients sum, so dkv accumulates over  */
+/* whatever rows are passed in.  The dkv sum runs over channels in parallel   */
+/* with a fixed (row, slot, head) order, so it is deterministic.             */
+/* ------------------------------------------------------------------------ */
+void oracle_sparse_mla_bwd(const double *q_rows, const double *kv, const int32_t *idx_rows,
+                           const int32_t *len_rows, int nrows, int Tk, int H, int Dqk, int Dv,
+                           int K, double scale, const double *dout_rows /*[nrows,H,Dv]*/,
+                           double *dq /*[nrows,H,Dqk]*/, double *dkv /*[Tk,Dqk], added to*/) {
+  size_t pk = (size_t)nrows * H * K;
+  double *P = (double *)calloc(pk ? pk : 1, sizeof(double));
+  double *dS = (double *)calloc(pk ? pk : 1, sizeof(double));
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < nrows; ++r) {
+    const double *q_r = q_rows + (size_t)r * H * Dqk;
+    const int32_t *idx_row = idx_rows + (size_t)r * K;
+    double *o_r = (double *)malloc(sizeof(double) * (size_t)H * Dv);
+    double *lse_r = (double *)malloc(sizeof(double) * (size_t)H);
+    double *p_r = P + (size_t)r * H * K;
+    double *ds_r = dS + (size_t)r * H * K;
+    fwd_row(q_r, kv, idx_row, len_rows, r, Tk, H, Dqk, Dv, K, scale, o_r, lse_r, p_r);
+    for (int h = 0; h < H; ++h) {
+      const double *dO = dout_rows + ((size_t)r * H + h) * Dv;
+      double D = 0.0;
+      for (int v = 0; v < Dv; ++v) D += dO[v] * o_r[(size_t)h * Dv + v];
+      double *dqh = dq + ((size_t)r * H + h) * Dqk;
+      for (int d = 0; d < Dqk; ++d) dqh[d] = 0.0;
+      for (int j = 0; j < K; ++j) {
+        double p = p_r[(size_t)h * K + j];
+        if (p == 0.0) { ds_r[(size_t)h * K + j] = 0.0; continue; }
+        const double *kr = kv + (size_t)idx_row[j] * Dqk;
+        double dp = 0.0;
+        for (int v = 0; v < Dv; ++v) dp += dO[v] * kr[v];
+        double ds = p * (dp - D);
+        ds_r[(size_t)h * K + j] = ds;
+        for (int d = 0; d < Dqk; ++d) dqh[d] += scale * ds * kr[d];
+      }
+    }
+    free(o_r);
+    free(lse_r);
+  }
+  /* key gradient: parallel over channels, fixed order over (row, slot, head) */
+#pragma omp parallel for schedule(static)
+  for (int d = 0; d < Dqk; ++d) {
+    for (int r = 0; r < nrows; ++r) {
+      const int32_t *idx_row = idx_rows + (size_t)r * K;
+      for (int j = 0; j < K; ++j) {
+        if (!slot_valid(idx_row, len_rows, r, j, Tk)) continue;
+        double acc = 0.0;
+        for (int h = 0; h < H; ++h) {
+          size_t pj = ((size_t)r * H + h) * K + j;
+          acc += scale * dS[pj] * q_rows[((size_t)r * H + h) * Dqk + d];
+          if (d < Dv) acc += P[pj] * dout_rows[((size_t)r * H + h) * Dv + d];
+        }
+        dkv[(size_t)idx_row[j] * Dqk + d] += acc;
+      }
+    }
+  }
+  free(P);
+  free(dS);
+}

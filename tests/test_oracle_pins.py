@@ -1,0 +1,337 @@
+"""Pins of the fp64 CPU oracle against things other than itself.
+
+Each test checks one oracle function against an independent library routine
+(numpy / torch fp64), brute force on tiny inputs, a closed form, a finite
+difference, an invariant stated on the pages, or a hand-derived example.
+All of these run on the CPU (no GPU marker).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_attention_mla_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------
+# helpers (independent re-statements used only as checks)
+# --------------------------------------------------------------------------
+def numpy_indexer_scores(q, k, w):
+    """Library route: einsum -> ReLU -> weighted head sum, all rows x all keys."""
+    dots = np.einsum("thd,sd->ths", q, k)
+    return np.einsum("th,ths->ts", w, np.maximum(dots, 0.0))
+
+
+def dense_masked_attention(q, kv, mask, scale, Dv):
+    """torch fp64 textbook masked softmax attention (MQA over one kv)."""
+    q = torch.as_tensor(q, dtype=torch.float64)
+    kv = torch.as_tensor(kv, dtype=torch.float64)
+    s = scale * torch.einsum("thd,sd->ths", q, kv)  # [T,H,Tk]
+    m = torch.as_tensor(mask)[:, None, :]
+    s = s.masked_fill(~m, float("-inf"))
+    lse = torch.logsumexp(s, dim=-1)
+    p = torch.softmax(s, dim=-1)
+    p = torch.nan_to_num(p, nan=0.0)
+    out = torch.einsum("ths,sv->thv", p, kv[:, :Dv])
+    return out, lse
+
+
+def mask_from_idx(idx, Tk):
+    T, K = idx.shape
+    mask = np.zeros((T, Tk), bool)
+    for t in range(T):
+        for j in range(K):
+            if 0 <= idx[t, j] < Tk:
+                mask[t, idx[t, j]] = True
+    return mask
+
+
+def rand_case(T=24, H=3, Dqk=16, Dv=8, K=6, seed=0, holes=True):
+    g = synth.generator(seed)
+    q = torch.randn(T, H, Dqk, generator=g, dtype=torch.float64)
+    kv = torch.randn(T, Dqk, generator=g, dtype=torch.float64)
+    dout = torch.randn(T, H, Dv, generator=g, dtype=torch.float64)
+    start = torch.zeros(T, dtype=torch.int32)
+    idx = synth.random_causal_topk(start, K, g)
+    if holes:  # move some -1 into the middle of rows (masked wherever they are)
+        idx[K + 3, 1] = -1
+        idx[T - 1, 0] = -1
+    return q.numpy(), kv.numpy(), dout.numpy(), idx.numpy()
+
+
+# --------------------------------------------------------------------------
+# packed THD metadata
+# --------------------------------------------------------------------------
+def test_packed_metadata_by_hand():
+    cu = np.array([0, 3, 3, 7], np.int32)  # includes an empty sequence
+    st, cl, mx, ne = oracle.packed_metadata(cu, 7)
+    assert st.tolist() == [0, 0, 0, 3, 3, 3, 3]
+    assert cl.tolist() == [1, 2, 3, 1, 2, 3, 4]
+    assert mx == 4 and ne == 1
+
+
+def test_packed_metadata_rejects_bad_cover():
+    with pytest.raises(ValueError):
+        oracle.packed_metadata(np.array([0, 5, 3], np.int32), 3)
+    with pytest.raises(ValueError):
+        oracle.packed_metadata(np.array([0, 2, 4], np.int32), 5)
+
+
+# --------------------------------------------------------------------------
+# indexer score
+# --------------------------------------------------------------------------
+def test_indexer_scores_match_numpy_einsum():
+    rng = np.random.default_rng(1)
+    T, Hi, Di = 9, 4, 16
+    q = rng.standard_normal((T, Hi, Di))
+    k = rng.standard_normal((T, Di))
+    w = rng.uniform(-0.5, 1.0, (T, Hi))  # signed weights too
+    pr, pk = np.meshgrid(np.arange(T), np.arange(T), indexing="ij")
+    got = oracle.indexer_scores(q, k, w, pr.ravel(), pk.ravel()).reshape(T, T)
+    ref = numpy_indexer_scores(q, k, w)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_indexer_special_cases():
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((5, 1, 8))
+    k = rng.standard_normal((5, 8))
+    pr, pk = np.meshgrid(np.arange(5), np.arange(5), indexing="ij")
+    got = oracle.indexer_scores(q, k, np.ones((5, 1)), pr.ravel(), pk.ravel()).reshape(5, 5)
+    np.testing.assert_allclose(got, np.maximum(q[:, 0, :] @ k.T, 0.0), rtol=1e-13, atol=1e-13)
+    got0 = oracle.indexer_scores(q, k, np.zeros((5, 1)), pr.ravel(), pk.ravel())
+    assert np.all(got0 == 0.0)
+
+
+# --------------------------------------------------------------------------
+# causal top-k
+# --------------------------------------------------------------------------
+def brute_topk(scores_row, b, t, K):
+    cand = sorted(range(b, t + 1), key=lambda s: (-scores_row[s], s))
+    n = min(K, t - b + 1)
+    sel = sorted(cand[:n])
+    return sel + [-1] * (K - n), n
+
+
+@pytest.mark.parametrize("K", [1, 5, 40])
+def test_topk_brute_force_packed(K):
+    rng = np.random.default_rng(3)
+    cu = np.array([0, 17, 40], np.int32)
+    T, Hi, Di = 40, 3, 8
+    q = rng.standard_normal((T, Hi, Di))
+    k = rng.standard_normal((T, Di))
+    w = rng.uniform(0, 1, (T, Hi))
+    st, _, _, _ = oracle.packed_metadata(cu, T)
+    idx, ln, kth = oracle.indexer_topk(q, k, w, st, np.arange(T), K)
+    S = numpy_indexer_scores(q, k, w)
+    for t in range(T):
+        ref, n = brute_topk(S[t], st[t], t, K)
+        assert idx[t].tolist() == ref, t
+        assert ln[t] == n
+        sel = [s for s in ref if s >= 0]
+        assert kth[t] == pytest.approx(min(S[t, s] for s in sel), rel=1e-12, abs=1e-12)
+
+
+def test_topk_all_ties_take_lowest_indices():
+    rng = np.random.default_rng(4)
+    T, K = 30, 7
+    q = rng.standard_normal((T, 2, 4))
+    k = rng.standard_normal((T, 4))
+    st = np.zeros(T, np.int32)
+    idx, ln, _ = oracle.indexer_topk(q, k, np.zeros((T, 2)), st, np.arange(T), K)
+    for t in range(T):
+        n = min(K, t + 1)
+        assert idx[t, :n].tolist() == list(range(n)) and np.all(idx[t, n:] == -1)
+
+
+def test_topk_strictly_increasing_scores_pick_the_window_end():
+    T, Di, K = 50, 4, 6
+    k = np.zeros((T, Di))
+    k[:, 0] = 0.5 * (np.arange(T) + 1)          # k[s] = alpha (s+1) e0
+    q = np.abs(np.random.default_rng(5).standard_normal((T, 2, Di))) + 0.1  # q[...,0] > 0
+    w = np.full((T, 2), 0.25)
+    st = np.zeros(T, np.int32)
+    idx, ln, _ = oracle.indexer_topk(q, k, w, st, np.arange(T), K)
+    for t in range(T):
+        n = min(K, t + 1)
+        assert idx[t, :n].tolist() == list(range(t - n + 1, t + 1))
+
+
+def test_topk_subset_of_rows_matches_all_rows():
+    rng = np.random.default_rng(6)
+    T, K = 33, 4
+    q = rng.standard_normal((T, 2, 4))
+    k = rng.standard_normal((T, 4))
+    w = rng.uniform(0, 1, (T, 2))
+    st = np.zeros(T, np.int32)
+    full, _, _ = oracle.indexer_topk(q, k, w, st, np.arange(T), K)
+    rows = np.array([32, 0, 17])
+    part, _, _ = oracle.indexer_topk(q[rows], k, w[rows], st, rows, K)
+    assert np.array_equal(part, full[rows])
+
+
+# --------------------------------------------------------------------------
+# sparse MLA forward
+# --------------------------------------------------------------------------
+def test_fwd_golden_two_slot_example():
+    with open(os.path.join(GOLDEN, "fwd_two_slot.json")) as f:
+        gd = json.load(f)
+    out, lse = oracle.sparse_mla_fwd(np.array(gd["q"]), np.array(gd["kv"]), np.array(gd["idx"]),
+                                     gd["scale"], Dv=gd["Dv"])
+    np.testing.assert_allclose(out, np.array(gd["out"]), rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(lse, np.array(gd["lse"]), rtol=1e-14, atol=1e-14)
+
+
+def test_fwd_matches_dense_masked_softmax():
+    q, kv, _, idx = rand_case()
+    scale = 0.37
+    out, lse = oracle.sparse_mla_fwd(q, kv, idx, scale, Dv=8)
+    ref_o, ref_l = dense_masked_attention(q, kv, mask_from_idx(idx, kv.shape[0]), scale, 8)
+    np.testing.assert_allclose(out, ref_o.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_l.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_fwd_full_prefix_equals_causal_sdpa():
+    T, H, Dqk, Dv = 20, 2, 12, 8
+    g = synth.generator(7)
+    q = torch.randn(T, H, Dqk, generator=g, dtype=torch.float64)
+    kv = torch.randn(T, Dqk, generator=g, dtype=torch.float64)
+    idx = synth.random_causal_topk(torch.zeros(T, dtype=torch.int32), T, g)  # K >= c: whole prefix
+    out, _ = oracle.sparse_mla_fwd(q, kv, idx, 0.5, Dv=Dv)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        q.transpose(0, 1), kv[None].expand(H, T, Dqk), kv[None, :, :Dv].expand(H, T, Dv),
+        is_causal=True, scale=0.5).transpose(0, 1)
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_fwd_closed_forms():
+    rng = np.random.default_rng(8)
+    H, Dqk, Dv, Tk = 3, 10, 6, 12
+    q = rng.standard_normal((2, H, Dqk))
+    kv = rng.standard_normal((Tk, Dqk))
+    # one valid slot: O = kv[i, :Dv], LSE = z
+    idx = np.array([[-1, 5, -1], [-1, -1, -1]], np.int32)
+    out, lse = oracle.sparse_mla_fwd(q, kv, idx, 0.3, Dv=Dv)
+    for h in range(H):
+        np.testing.assert_allclose(out[0, h], kv[5, :Dv], rtol=1e-14)
+        assert lse[0, h] == pytest.approx(0.3 * q[0, h] @ kv[5], rel=1e-13)
+    # empty row: O = 0, LSE = -inf
+    assert np.all(out[1] == 0.0) and np.all(np.isneginf(lse[1]))
+    # identical selected rows: O = that row, LSE = z + ln n
+    kv2 = np.tile(kv[3], (Tk, 1))
+    idx2 = np.array([[0, 2, 4, 6, 8]], np.int32)
+    out2, lse2 = oracle.sparse_mla_fwd(q[:1], kv2, idx2, 0.3, Dv=Dv)
+    for h in range(H):
+        np.testing.assert_allclose(out2[0, h], kv[3, :Dv], rtol=1e-13)
+        assert lse2[0, h] == pytest.approx(0.3 * q[0, h] @ kv[3] + math.log(5), rel=1e-13)
+
+
+def test_fwd_invariants_permutation_padding_chunking_length():
+    q, kv, _, idx = rand_case(T=30, K=8, holes=False)
+    scale = 0.21
+    out, lse = oracle.sparse_mla_fwd(q, kv, idx, scale, Dv=8)
+    # slot permutation (moves the -1 suffix into the middle as well)
+    perm = np.random.default_rng(9).permutation(idx.shape[1])
+    o2, l2 = oracle.sparse_mla_fwd(q, kv, idx[:, perm], scale, Dv=8)
+    np.testing.assert_allclose(o2, out, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l2, lse, rtol=1e-12, atol=1e-13)
+    # NoPE: zero-padding q and kv channels (the RoPE slot) changes nothing
+    pad = lambda a: np.concatenate([a, np.zeros(a.shape[:-1] + (8,))], axis=-1)
+    o3, l3 = oracle.sparse_mla_fwd(pad(q), pad(kv), idx, scale, Dv=8)
+    np.testing.assert_allclose(o3, out, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(l3, lse, rtol=1e-13, atol=1e-14)
+    # query chunks are independent
+    o4, _ = oracle.sparse_mla_fwd(q[11:23], kv, idx[11:23], scale, Dv=8)
+    np.testing.assert_allclose(o4, out[11:23], rtol=0, atol=0)
+    # topk_len bounds the prefix: equal to writing -1 after it
+    ln = np.minimum(np.arange(30), 5).astype(np.int32)
+    cut = idx.copy()
+    for t in range(30):
+        cut[t, ln[t]:] = -1
+    o5, l5 = oracle.sparse_mla_fwd(q, kv, idx, scale, Dv=8, len_rows=ln)
+    o6, l6 = oracle.sparse_mla_fwd(q, kv, cut, scale, Dv=8)
+    np.testing.assert_array_equal(o5, o6)
+    np.testing.assert_array_equal(l5, l6)
+
+
+# --------------------------------------------------------------------------
+# sparse MLA backward
+# --------------------------------------------------------------------------
+def test_bwd_central_finite_differences():
+    q, kv, dout, idx = rand_case(T=7, H=2, Dqk=6, Dv=4, K=4, seed=10, holes=False)
+    idx[5, 2] = -1
+    scale = 0.45
+    dq, dkv = oracle.sparse_mla_bwd(q, kv, idx, dout, scale, Dv=4)
+
+    def loss(qq, kk):
+        o, _ = oracle.sparse_mla_fwd(qq, kk, idx, scale, Dv=4)
+        return float(np.sum(o * dout))
+
+    eps = 1e-6
+    fq = np.zeros_like(q)
+    for i in np.ndindex(q.shape):
+        a, b = q.copy(), q.copy()
+        a[i] += eps
+        b[i] -= eps
+        fq[i] = (loss(a, kv) - loss(b, kv)) / (2 * eps)
+    fk = np.zeros_like(kv)
+    for i in np.ndindex(kv.shape):
+        a, b = kv.copy(), kv.copy()
+        a[i] += eps
+        b[i] -= eps
+        fk[i] = (loss(q, a) - loss(q, b)) / (2 * eps)
+    np.testing.assert_allclose(dq, fq, rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(dkv, fk, rtol=1e-6, atol=1e-8)
+
+
+def test_bwd_matches_torch_autograd_dense():
+    q, kv, dout, idx = rand_case(seed=11)
+    scale = 0.3
+    dq, dkv = oracle.sparse_mla_bwd(q, kv, idx, dout, scale, Dv=8)
+    qt = torch.tensor(q, requires_grad=True)
+    kt = torch.tensor(kv, requires_grad=True)
+    o, _ = dense_masked_attention(qt, kt, mask_from_idx(idx, kv.shape[0]), scale, 8)
+    o.backward(torch.tensor(dout))
+    np.testing.assert_allclose(dq, qt.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dkv, kt.grad.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_bwd_dkv_column_sums_property():
+    # sum_j dS_j = 0 and sum_j P_j = 1 per (t, h) give, for every channel c,
+    # sum_k dkv[k, c] = sum_{t,h nonempty} dO[t,h,c] (c < Dv) and 0 (c >= Dv).
+    q, kv, dout, idx = rand_case(T=26, Dqk=12, Dv=8, seed=12)
+    idx[4, :] = -1  # an empty row contributes nothing
+    dq, dkv = oracle.sparse_mla_bwd(q, kv, idx, dout, 0.25, Dv=8)
+    nonempty = (idx >= 0).any(axis=1)
+    colsum = dkv.sum(axis=0)
+    np.testing.assert_allclose(colsum[:8], dout[nonempty].sum(axis=(0, 1)), rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(colsum[8:], 0.0, atol=1e-11)
+    assert np.all(dq[4] == 0.0)
+
+
+def test_bwd_query_chunks_sum_to_one_shot():
+    q, kv, dout, idx = rand_case(T=31, seed=13)
+    dq, dkv = oracle.sparse_mla_bwd(q, kv, idx, dout, 0.2, Dv=8)
+    acc = np.zeros_like(dkv)
+    parts = []
+    for a, b in [(0, 9), (9, 20), (20, 31)]:
+        d, _ = oracle.sparse_mla_bwd(q[a:b], kv, idx[a:b], dout[a:b], 0.2, Dv=8, dkv=acc)
+        parts.append(d)
+    np.testing.assert_allclose(np.concatenate(parts), dq, rtol=0, atol=0)
+    np.testing.assert_allclose(acc, dkv, rtol=1e-12, atol=1e-12)
+
+
+def test_oracle_takes_bf16_tensors_exactly():
+    # bf16 inputs are widened exactly: bf16 -> float64 of the same value
+    x = synth.randn_bf16((3, 2, 8), synth.generator(14))
+    kv = synth.randn_bf16((3, 8), synth.generator(15))
+    idx = torch.tensor([[0, -1], [0, 1], [2, 1]], dtype=torch.int32)
+    o1, _ = oracle.sparse_mla_fwd(x, kv, idx, 0.5, Dv=4)
+    o2, _ = oracle.sparse_mla_fwd(x.double().numpy(), kv.double().numpy(), idx.numpy(), 0.5, Dv=4)
+    np.testing.assert_array_equal(o1, o2)
