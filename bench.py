@@ -1,0 +1,399 @@
+"""Benchmark of the DSA hot path on one GB300 (or N replicas).
+
+Workload (the pages' 32k configuration): one sequence of S = 32768 tokens;
+lightning indexer with 64 heads x 128 (bf16 q_idx [S,64,128], shared k_idx
+[S,128], fp32 head weights ~ U(0,1)/8) and causal top-k K = 2048; the selected
+indices drive absorbed sparse MLA forward + backward with H = 64 heads, width
+576 (512 latent + 64 RoPE), value 512, softmax_scale = 192^-0.5, bf16 N(0,1)
+q / kv / dO.  One step = indexer top-k -> sparse MLA forward -> sparse MLA
+backward on device-resident inputs (the THD metadata is built once, as the
+pages do once per pipeline stage).
+
+Metric: sparse-MLA fwd+bwd TFLOP/s (algorithmic FLOPs over valid slots:
+fwd 2*H*n*(576+512), bwd 2*H*n*(3*576+2*512)) with the indexer's top-k
+tokens/s alongside.  Every input is larger than L2 (q alone is 2.4 GB), so no
+L2 flush is needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+S, HI, DI, K, H, DQK, DV = 32768, 64, 128, 2048, 64, 576, 512
+SCALE = 192 ** -0.5
+METRIC = "sparse-MLA fwd+bwd TFLOP/s (% bf16 peak) and indexer top-k tokens/s at S=32k,K=2048"
+UNIT = "TFLOP/s"
+WORKLOAD = "lightning indexer (64x128) + causal top-k K=2048 -> sparse MLA fwd+bwd H=64 width 576, S=32768, 1 sequence"
+
+
+def mla_flops(n_valid: int) -> tuple[float, float]:
+    return 2.0 * H * n_valid * (DQK + DV), 2.0 * H * n_valid * (3 * DQK + 2 * DV)
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (test infrastructure: the plain fp64 oracle, as it stands)
+# ---------------------------------------------------------------------------
+def oracle_sample(rows: int, seed: int = 0) -> dict:
+    """Time the oracle on a bounded sample of the same workload: the last
+    `rows` query rows (full 32k windows, full K) for indexer top-k and sparse
+    MLA fwd+bwd.  Inputs are drawn with the same recipe, on the CPU."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from sparse_attention_mla_gb300 import synth
+
+    g = synth.generator(seed)
+    k_idx = synth.randn_bf16((S, DI), g)
+    q_idx = synth.randn_bf16((rows, HI, DI), g)
+    w = torch.rand(rows, HI, generator=g) / 8.0
+    kv = synth.randn_bf16((S, DQK), g)
+    q = synth.randn_bf16((rows, H, DQK), g)
+    dout = synth.randn_bf16((rows, H, DV), g)
+    row_t = np.arange(S - rows, S)
+    start = np.zeros(S, np.int32)
+    t0 = time.perf_counter()
+    idx, ln, _ = oracle.indexer_topk(q_idx, k_idx, w, start, row_t, K)
+    t1 = time.perf_counter()
+    oracle.sparse_mla_fwd(q, kv, idx, SCALE)
+    oracle.sparse_mla_bwd(q, kv, idx, dout, SCALE)
+    t2 = time.perf_counter()
+    n_valid = int((idx >= 0).sum())
+    fl = sum(mla_flops(n_valid))
+    return {"mla_s": t2 - t1, "idx_s": t1 - t0, "mla_tflops": fl / (t2 - t1) / 1e12,
+            "idx_tokens_per_s": rows / (t1 - t0), "rows": rows, "cores": os.cpu_count()}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    rows = 2
+    for _ in range(args.warmup):
+        oracle_sample(rows)
+    vals, idx_rates, wall = [], [], []
+    for i in range(args.steps):
+        r = oracle_sample(rows, seed=i)
+        vals.append(r["mla_tflops"])
+        idx_rates.append(r["idx_tokens_per_s"])
+        wall.append(r["mla_s"] + r["idx_s"])
+    v = statistics.median(vals)
+    sample = (f"{rows} query rows (positions {S - rows}..{S - 1}, full 32k causal windows, K=2048) per step: "
+              "indexer top-k + sparse MLA fwd+bwd in the fp64 C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(wall), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "indexer_tokens_per_s": statistics.median(idx_rates),
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# CUDA leg
+# ---------------------------------------------------------------------------
+def run_cuda(args, rank, world, local):
+    import torch
+
+    import sparse_attention_mla_gb300 as dsa
+    from sparse_attention_mla_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dsa.load_library()
+    peaks = load_peaks()
+
+    # ---- inputs (device-resident; drawn on the device with the synth recipe) ----
+    ind = synth.indexer_inputs(S, HI, DI, seed=rank, device=dev)
+    mla = synth.mla_inputs(S, H, DQK, DV, seed=1000 + rank, device=dev)
+    cu = torch.tensor([0, S], dtype=torch.int32, device=dev)
+    seq_start, _, _, _ = dsa.dsa_packed_metadata(cu, S)  # once per stage, as on the pages
+    topk_idx = torch.empty(S, K, dtype=torch.int32, device=dev)
+    topk_len = torch.empty(S, dtype=torch.int32, device=dev)
+    out = torch.empty(S, H, DV, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(S, H, dtype=torch.float32, device=dev)
+    dq = torch.empty(S, H, DQK, dtype=torch.bfloat16, device=dev)
+    dkv = torch.empty(S, DQK, dtype=torch.float32, device=dev)
+    ws_i = torch.zeros(dsa.workspace_size("indexer", S, K), dtype=torch.uint8, device=dev)
+    ws_f = torch.zeros(dsa.workspace_size("fwd", S, H), dtype=torch.uint8, device=dev)
+    ws_b = torch.zeros(dsa.workspace_size("bwd", S, H), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+
+    def step(e=None):
+        if e: e[0].record(stream)
+        dsa.dsa_indexer_topk(ind["q_idx"], ind["k_idx"], ind["w"], seq_start, K, topk_idx=topk_idx,
+                             topk_len=topk_len, workspace=ws_i)
+        if e: e[1].record(stream)
+        dsa.dsa_sparse_mla_fwd(mla["q"], mla["kv"], topk_idx, SCALE, topk_len=topk_len, out=out, lse=lse,
+                               workspace=ws_f)
+        if e: e[2].record(stream)
+        dsa.dsa_sparse_mla_bwd(mla["q"], mla["kv"], topk_idx, SCALE, out, lse, mla["dout"], topk_len=topk_len,
+                               dq=dq, dkv_accum=dkv, workspace=ws_b)
+        if e: e[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    for w_ in (ws_i, ws_f, ws_b):
+        st = dsa.dsa_read_device_status(w_)
+        if st != 0:
+            raise RuntimeError(f"device status {st} after warm-up")
+    n_valid = int(topk_len.sum().item())
+    f_fwd, f_bwd = mla_flops(n_valid)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
+    idx_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    fwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    bwd_ms = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
+    mla_ms_total = sum(e[1].elapsed_time(e[3]) for e in ev)
+    mla_ms_total = max_over_ranks(mla_ms_total, world, dev)
+    value = world * args.steps * (f_fwd + f_bwd) / (mla_ms_total * 1e-3) / 1e12
+    idx_tok_s = world * S / (idx_ms * 1e-3)
+
+    # ---- roofline of the dominant kernel (the backward: most FLOPs and time) ----
+    bwd_tflops = f_bwd / (bwd_ms * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            tr = json.load(f).get("sparse_mla_bwd_kernel")
+        if tr and tr.get("kernel_rev") == kernel_rev("dsa_bwd.cu"):
+            traffic = tr["bytes_per_valid_slot"] * n_valid
+    roofline = {"bound": "tensor", "kernel": "sparse_mla_bwd_kernel", "achieved": round(bwd_tflops, 2),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_tflops / peak, 4), "traffic": traffic,
+                "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)"}
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, f_fwd + f_bwd, world)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "S": S, "K": K, "H": H, "width": DQK, "indexer_heads": HI,
+                   "indexer_dim": DI, "global_batch": S * world, "seq_len": S,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (q 2.4 GB), no flush"},
+        "mla_pct_bf16_peak": round(100 * value / world / peak, 2),
+        "indexer_tokens_per_s": round(idx_tok_s, 1),
+        "components_ms": {"indexer_topk": round(idx_ms, 3), "sparse_mla_fwd": round(fwd_ms, 3),
+                          "sparse_mla_bwd": round(bwd_ms, 3)},
+        "n_valid_slots": n_valid,
+        "roofline": roofline,
+        "clocks": clocks,
+        "gpu_launches": 4 * args.steps,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        r = oracle_sample(16)
+        line["cpu_baseline"] = {"value": round(r["mla_tflops"], 6), "unit": UNIT, "cores": r["cores"],
+                                "kind": "oracle",
+                                "sample": "16 query rows (positions 32752..32767, full windows, K=2048): indexer "
+                                          "top-k then sparse MLA fwd+bwd in the fp64 C oracle; value = MLA fwd+bwd "
+                                          f"TFLOP/s; indexer {r['idx_tokens_per_s']:.2f} tokens/s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, flops_per_step, world):
+    """Same metric through the public API with pinned host buffers: every step
+    copies its inputs host->device and reads its results device->host."""
+    host_in = {k: v.to("cpu").pin_memory() for k, v in list(ind.items()) + list(mla.items())}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    res_shapes = {"topk_idx": ((S, K), torch.int32), "topk_len": ((S,), torch.int32),
+                  "out": ((S, H, DV), torch.bfloat16), "lse": ((S, H), torch.float32),
+                  "dq": ((S, H, DQK), torch.bfloat16), "dkv": ((S, DQK), torch.float32)}
+    dres = {k: torch.empty(*s, dtype=d, device=dev) for k, (s, d) in res_shapes.items()}
+    hres = {k: torch.empty(*s, dtype=d).pin_memory() for k, (s, d) in res_shapes.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in hres.values())
+
+    def step():
+        for k in host_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        dsa.dsa_indexer_topk(dev_in["q_idx"], dev_in["k_idx"], dev_in["w"], seq_start, K, topk_idx=dres["topk_idx"],
+                             topk_len=dres["topk_len"])
+        dsa.dsa_sparse_mla_fwd(dev_in["q"], dev_in["kv"], dres["topk_idx"], SCALE, topk_len=dres["topk_len"],
+                               out=dres["out"], lse=dres["lse"])
+        dsa.dsa_sparse_mla_bwd(dev_in["q"], dev_in["kv"], dres["topk_idx"], SCALE, dres["out"], dres["lse"],
+                               dev_in["dout"], topk_len=dres["topk_len"], dq=dres["dq"], dkv_accum=dres["dkv"])
+        for k in hres:
+            hres[k].copy_(dres[k], non_blocking=True)
+
+    steps = max(1, min(args.steps, 3))
+    step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    return {"value": round(world * steps * flops_per_step / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "note": "MLA fwd+bwd FLOPs over the whole step incl. indexer and host copies"}
+
+
+def kernel_rev(src_name: str) -> str:
+    """Content hash of a kernel source: ncu counters are reused only for the same code."""
+    import hashlib
+
+    with open(os.path.join(ROOT, "sparse_attention_mla_gb300", "csrc", src_name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seq", type=int, default=32768,
+                    help="sequence length; only for small-case profiler captures (the benchmark is 32768)")
+    args = ap.parse_args()
+    global S
+    S = args.seq
+    if args.warmup < 3 and args.impl == "cuda":
+        args.warmup = 3
+    rank, world, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_cuda(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

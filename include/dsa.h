@@ -1,0 +1,166 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DeepSeek Sparse Attention hot path.
+ *
+ * Conventions for every entry point:
+ *  - Tensor arguments are caller-owned DEVICE pointers to contiguous row-major
+ *    storage (innermost dimension last); host pointers are named *_host.
+ *  - bf16 tensors are passed as dsa_bf16_t (the raw 16-bit pattern).
+ *  - Calls are asynchronous on the caller's CUDA stream (NULL = legacy default
+ *    stream); only dsa_packed_metadata and dsa_read_device_status synchronise.
+ *  - The library never allocates device memory.  Scratch comes from the
+ *    caller's `workspace` (at least dsa_*_workspace_size() bytes, 256-byte
+ *    aligned); its first 4 bytes are the device error word (see
+ *    dsa_read_device_status).
+ *  - Every call returns a dsa_status_t; argument errors are detected on the
+ *    host before anything is launched and leave all outputs untouched.
+ *    dsa_last_error_message() describes the most recent failure of the calling
+ *    thread.
+ *
+ * Pages cited (title, then section or API entry):
+ *  [DSA-blog]  "Accelerating GLM-5.2 Long-Context Training with cuDNN Fused DSA
+ *              Kernels and THD-Packed Context Parallelism using Megatron Bridge"
+ *  [NoPE-PR]   SkyRL pull request 2388 (NoPE / unaligned top-k SparseMLA)
+ *  [cudnn_dsa] NeMo AutoModel API: glm_moe_dsa.kernels.cudnn_dsa
+ *  [Chunk-PR]  SkyRL pull request 2423 (query-chunked sparse attention)
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* dsa_stream_t; /* same type as cudaStream_t */
+typedef uint16_t dsa_bf16_t;              /* bfloat16 bit pattern */
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_UNSUPPORTED = 1,      /* no CUDA device, or the device is not sm_103 */
+  DSA_ERR_DTYPE = 2,            /* reserved: the ABI fixes every dtype */
+  DSA_ERR_INVALID_ARGUMENT = 3, /* null pointer, bad shape, K or scale */
+  DSA_ERR_WORKSPACE = 4,        /* workspace missing, too small or misaligned */
+  DSA_ERR_CUDA = 5,             /* a CUDA runtime call or launch failed */
+  DSA_ERR_DEVICE_INDEX = 6,     /* device saw an index outside [-1, T_k) (slot masked) */
+  DSA_ERR_TIMEOUT = 7           /* a bounded device-side wait gave up (CTA exited) */
+} dsa_status_t;
+
+/* Text for a status code (static storage). */
+const char* dsa_status_string(dsa_status_t status);
+/* Message of the calling thread's most recent failed call ("" if none). */
+const char* dsa_last_error_message(void);
+/* ABI version: 1. */
+int32_t dsa_abi_version(void);
+
+/*
+ * dsa_packed_metadata -- THD packing metadata, no context parallelism.
+ * Source: [cudnn_dsa] prepare_cudnn_dsa_packed_metadata and
+ * CudnnDsaPackedMetadata (starts, causal_lengths, max_seqlen,
+ * all_rows_nonempty): per query token t of sequence i,
+ *   seq_start[t] = cu_seqlens[i],  causal_len[t] = t - cu_seqlens[i] + 1.
+ *  cu_seqlens   device int32 [num_seqs + 1], cu[0] = 0, non-decreasing, cu[num_seqs] = total_tokens
+ *  seq_start    device int32 [total_tokens] (out)
+ *  causal_len   device int32 [total_tokens] (out)
+ *  max_seqlen_host, all_rows_nonempty_host: host int32 scalars (out), may be NULL
+ * Like the pages' routine it performs one device-to-host synchronisation (to
+ * validate cu_seqlens and return max_seqlen).  Returns
+ * DSA_ERR_INVALID_ARGUMENT if cu_seqlens is not a valid cover of [0, T).
+ */
+dsa_status_t dsa_packed_metadata(const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                                 int32_t* seq_start, int32_t* causal_len, int32_t* max_seqlen_host,
+                                 int32_t* all_rows_nonempty_host, dsa_stream_t stream);
+
+/*
+ * dsa_indexer_topk -- lightning-indexer score fused with per-query causal top-k.
+ * Source: [DSA-blog] "How DSA works" (the indexer scores query-key relevance
+ * and emits the top-k indices per query); [cudnn_dsa] cudnn_indexer_topk
+ * (index_q [T, H_index, 128], index_k [T_k, 128], already-scaled head weights,
+ * output int32 global indices, K in [1, 2048]); canonical output form from
+ * cudnn_sparse_attention's topk_length (compact ascending prefix).
+ *   score(t, s) = sum_h w[t,h] * max(0, <q_idx[t,h,:], k_idx[s,:]>),  s in [seq_start[t], t]
+ * For each t the n = min(K, causal_len[t]) highest-scoring keys (ties to the
+ * lower index) are written ascending to topk_idx[t, 0:n], then -1 up to K.
+ * The [T, T_k] score matrix is never written to memory.
+ *  q_idx        device bf16 [T, Hi, Di]; Hi in [1, 64], Di = 128
+ *  k_idx        device bf16 [T_k, Di]
+ *  head_weights device fp32 [T, Hi] (caller applies any scaling)
+ *  seq_start    device int32 [T] from dsa_packed_metadata (window start; the
+ *               window end is the token itself, so T_k >= T is required)
+ *  topk_idx     device int32 [T, K] (out);  topk_len device int32 [T] (out) or NULL
+ *  workspace    >= dsa_indexer_topk_workspace_size() bytes
+ */
+size_t dsa_indexer_topk_workspace_size(int32_t T, int32_t K);
+dsa_status_t dsa_indexer_topk(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
+                              const int32_t* seq_start, int32_t T, int32_t T_k, int32_t Hi, int32_t Di, int32_t K,
+                              int32_t* topk_idx, int32_t* topk_len, void* workspace, size_t workspace_bytes,
+                              dsa_stream_t stream);
+
+/*
+ * dsa_sparse_mla_fwd -- absorbed sparse MLA forward (MQA over one latent KV).
+ * Source: [DSA-blog] "How DSA works" and "Why DSA needs fused kernels";
+ * [cudnn_dsa] cudnn_sparse_attention / _CudnnSparseAttention.forward (q
+ * [T, H, 576], kv_latent [T_k, 1, 576], int32 indices with -1 invalid, optional
+ * topk_length, explicit softmax_scale, output [T, H, 512]); [NoPE-PR] "Change"
+ * (value = kv[..., :512], NoPE width 512, unaligned top-k widths).
+ * Slot j of row t is valid iff topk_idx[t,j] >= 0 and (topk_len == NULL or
+ * j < topk_len[t]); per (t, h):
+ *   z_j = softmax_scale * <q[t,h,:], kv[idx_j,:]>,  lse[t,h] = ln sum_j exp(z_j),
+ *   out[t,h,:] = sum_j exp(z_j - lse) * kv[idx_j, 0:Dv].
+ * A row with no valid slot gets out = 0 and lse = -inf.  Indices >= T_k or
+ * < -1 are masked and reported through the device error word.
+ *  q        device bf16 [T, H, Dqk], Dqk in {512, 576};  kv device bf16 [T_k, Dqk]
+ *  topk_idx device int32 [T, K], any K >= 1;  topk_len device int32 [T] or NULL
+ *  out      device bf16 [T, H, Dv] (out), Dv = 512;  lse device fp32 [T, H] (out)
+ *  workspace >= dsa_sparse_mla_fwd_workspace_size() bytes
+ * Query chunking ([Chunk-PR] "Summary"): rows are independent, so a chunk is a
+ * call on row-offset pointers of q/topk_idx/out/lse with the full kv.
+ */
+size_t dsa_sparse_mla_fwd_workspace_size(int32_t T, int32_t H);
+dsa_status_t dsa_sparse_mla_fwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
+                                const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
+                                int32_t Dv, int32_t K, float softmax_scale, dsa_bf16_t* out, float* lse,
+                                void* workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+/*
+ * dsa_sparse_mla_bwd -- analytic backward of dsa_sparse_mla_fwd.
+ * Source: [cudnn_dsa] _CudnnSparseAttention.backward (gradients for the query
+ * [T, H, 576] and the latent KV from grad_output [T, H, 512]); [Chunk-PR]
+ * "Summary" (query chunks are independent, key gradients sum).
+ * With P_j = exp(z_j - lse), D = <dout, out>, dP_j = <dout, kv[idx_j,:Dv]>,
+ * dS_j = P_j (dP_j - D):
+ *   dq[t,h,:]         = softmax_scale * sum_j dS_j kv[idx_j, :]
+ *   dkv_accum[idx_j,:] += softmax_scale * sum_h dS_j q[t,h,:]
+ *   dkv_accum[idx_j,0:Dv] += sum_h P_j dout[t,h,:]
+ *  q, kv, topk_idx, topk_len, sizes, softmax_scale: as in the forward call
+ *  out, lse       device: the forward's outputs for these rows
+ *  dout           device bf16 [T, H, Dv]
+ *  dq             device bf16 [T, H, Dqk] (out)
+ *  dkv_accum      device fp32 [T_k, Dqk]: zeroed first when accumulate == 0,
+ *                 added to when accumulate == 1 (query chunks)
+ *  dkv_bf16       device bf16 [T_k, Dqk] (out, rounded copy of dkv_accum) or NULL
+ *  workspace      >= dsa_sparse_mla_bwd_workspace_size(T, H) bytes
+ * Summation order of dkv_accum across rows is not deterministic (fp32 atomics).
+ */
+size_t dsa_sparse_mla_bwd_workspace_size(int32_t T, int32_t H);
+dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
+                                const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
+                                int32_t Dv, int32_t K, float softmax_scale, const dsa_bf16_t* out,
+                                const float* lse, const dsa_bf16_t* dout, dsa_bf16_t* dq, float* dkv_accum,
+                                int32_t accumulate, dsa_bf16_t* dkv_bf16, void* workspace,
+                                size_t workspace_bytes, dsa_stream_t stream);
+
+/*
+ * dsa_read_device_status -- synchronise `stream`, read and clear the device
+ * error word at the start of `workspace`, and store it in *status_host
+ * (DSA_OK, DSA_ERR_DEVICE_INDEX or DSA_ERR_TIMEOUT).  Library addition with no
+ * counterpart on the pages: it surfaces the bounded-wait and index checks.
+ */
+dsa_status_t dsa_read_device_status(void* workspace, dsa_stream_t stream, int32_t* status_host);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H_ */

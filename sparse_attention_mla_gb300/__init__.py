@@ -1,0 +1,256 @@
+"""GB300-native (sm_103a) DeepSeek Sparse Attention hot path.
+
+Thin Python binding over the C ABI of ``libdsa.so`` (see ``include/dsa.h``).
+The functions carry the C entry points' names and only marshal arguments:
+torch supplies device memory and the current CUDA stream; every step of the
+computation runs in the library's CUDA kernels.  There is no CPU fallback: if
+the library is missing or the device is not sm_103, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+import threading
+
+import torch
+
+from .build_ext import LIB as _LIB_PATH
+from .build_ext import INCLUDE as _INCLUDE
+
+__all__ = [
+    "DsaError",
+    "load_library",
+    "declared_symbols",
+    "dsa_packed_metadata",
+    "dsa_indexer_topk",
+    "dsa_sparse_mla_fwd",
+    "dsa_sparse_mla_bwd",
+    "dsa_read_device_status",
+    "workspace_size",
+]
+
+DSA_OK = 0
+STATUS_NAMES = {
+    0: "DSA_OK",
+    1: "DSA_ERR_UNSUPPORTED",
+    2: "DSA_ERR_DTYPE",
+    3: "DSA_ERR_INVALID_ARGUMENT",
+    4: "DSA_ERR_WORKSPACE",
+    5: "DSA_ERR_CUDA",
+    6: "DSA_ERR_DEVICE_INDEX",
+    7: "DSA_ERR_TIMEOUT",
+}
+
+
+class DsaError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {message}")
+
+
+_lib = None
+_lock = threading.Lock()
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_SZ = ctypes.c_size_t
+_F = ctypes.c_float
+
+
+def declared_symbols() -> list[str]:
+    """Function names declared in include/*.h (the ABI surface)."""
+    names = []
+    for fn in sorted(os.listdir(_INCLUDE)):
+        if fn.endswith(".h"):
+            text = open(os.path.join(_INCLUDE, fn)).read()
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(dsa_[a-z0-9_]+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+def load_library(path: str | None = None):
+    """Load libdsa.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or _LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} not found: build the CUDA library first "
+                "(python -m sparse_attention_mla_gb300.build_ext, or __graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        lib.dsa_status_string.restype = ctypes.c_char_p
+        lib.dsa_status_string.argtypes = [ctypes.c_int]
+        lib.dsa_last_error_message.restype = ctypes.c_char_p
+        lib.dsa_last_error_message.argtypes = []
+        lib.dsa_abi_version.restype = _I
+        lib.dsa_packed_metadata.argtypes = [_P, _I, _I, _P, _P, _P, _P, _P]
+        lib.dsa_indexer_topk_workspace_size.argtypes = [_I, _I]
+        lib.dsa_indexer_topk_workspace_size.restype = _SZ
+        lib.dsa_indexer_topk.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]
+        lib.dsa_sparse_mla_fwd_workspace_size.argtypes = [_I, _I]
+        lib.dsa_sparse_mla_fwd_workspace_size.restype = _SZ
+        lib.dsa_sparse_mla_fwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]
+        lib.dsa_sparse_mla_bwd_workspace_size.argtypes = [_I, _I]
+        lib.dsa_sparse_mla_bwd_workspace_size.restype = _SZ
+        lib.dsa_sparse_mla_bwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I,
+                                           _P, _P, _SZ, _P]
+        lib.dsa_read_device_status.argtypes = [_P, _P, _P]
+        for name in ("dsa_packed_metadata", "dsa_indexer_topk", "dsa_sparse_mla_fwd", "dsa_sparse_mla_bwd",
+                     "dsa_read_device_status"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(status: int, where: str):
+    if status != DSA_OK:
+        lib = load_library()
+        raise DsaError(status, where, lib.dsa_last_error_message().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, name, dtype, ndim=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def workspace_size(kind: str, T: int, H_or_K: int) -> int:
+    lib = load_library()
+    fn = {"fwd": lib.dsa_sparse_mla_fwd_workspace_size, "bwd": lib.dsa_sparse_mla_bwd_workspace_size,
+          "indexer": lib.dsa_indexer_topk_workspace_size}[kind]
+    return int(fn(int(T), int(H_or_K)))
+
+
+def _workspace(kind, T, x, device, workspace):
+    need = workspace_size(kind, T, x)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    return workspace, workspace.numel()
+
+
+def dsa_packed_metadata(cu_seqlens: torch.Tensor, total_tokens: int):
+    """cu_seqlens int32 [nseq+1] (CUDA) -> (seq_start [T], causal_len [T], max_seqlen, all_rows_nonempty)."""
+    lib = load_library()
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    dev = cu_seqlens.device
+    T = int(total_tokens)
+    start = torch.empty(T, dtype=torch.int32, device=dev)
+    clen = torch.empty(T, dtype=torch.int32, device=dev)
+    mx = ctypes.c_int32(0)
+    ne = ctypes.c_int32(0)
+    _check(lib.dsa_packed_metadata(_ptr(cu_seqlens), cu_seqlens.numel() - 1, T, _ptr(start), _ptr(clen),
+                                   ctypes.byref(mx), ctypes.byref(ne), _stream(dev)), "dsa_packed_metadata")
+    return start, clen, mx.value, ne.value
+
+
+def dsa_indexer_topk(q_idx, k_idx, head_weights, seq_start, K: int, topk_idx=None, topk_len=None,
+                     workspace=None, with_len: bool = True):
+    """Fused indexer score + causal top-k -> (topk_idx int32 [T,K], topk_len int32 [T] or None)."""
+    lib = load_library()
+    _need(q_idx, "q_idx", torch.bfloat16, 3)
+    dev = q_idx.device
+    _need(k_idx, "k_idx", torch.bfloat16, 2, dev)
+    _need(head_weights, "head_weights", torch.float32, 2, dev)
+    _need(seq_start, "seq_start", torch.int32, 1, dev)
+    T, Hi, Di = q_idx.shape
+    Tk = k_idx.shape[0]
+    if topk_idx is None:
+        topk_idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+    if topk_len is None and with_len:
+        topk_len = torch.empty(T, dtype=torch.int32, device=dev)
+    ws, wsb = _workspace("indexer", T, K, dev, workspace)
+    _check(lib.dsa_indexer_topk(_ptr(q_idx), _ptr(k_idx), _ptr(head_weights), _ptr(seq_start), T, Tk, Hi, Di,
+                                int(K), _ptr(topk_idx), _ptr(topk_len), _ptr(ws), wsb, _stream(dev)),
+           "dsa_indexer_topk")
+    return topk_idx, topk_len
+
+
+def dsa_sparse_mla_fwd(q, kv, topk_idx, softmax_scale: float, topk_len=None, out=None, lse=None,
+                       workspace=None, Dv: int = 512):
+    """Sparse MLA forward -> (out bf16 [T,H,Dv], lse fp32 [T,H]).  kv may be [T_k, Dqk] or [T_k, 1, Dqk]."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    if kv.dim() == 3:
+        kv = kv.reshape(kv.shape[0], kv.shape[2])
+    _need(kv, "kv", torch.bfloat16, 2, dev)
+    if topk_idx.dim() == 3:
+        topk_idx = topk_idx.reshape(topk_idx.shape[0], topk_idx.shape[2])
+    _need(topk_idx, "topk_idx", torch.int32, 2, dev)
+    if topk_len is not None:
+        _need(topk_len, "topk_len", torch.int32, 1, dev)
+    T, H, Dqk = q.shape
+    K = topk_idx.shape[1]
+    if out is None:
+        out = torch.empty(T, H, Dv, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+    ws, wsb = _workspace("fwd", T, H, dev, workspace)
+    _check(lib.dsa_sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(topk_idx), _ptr(topk_len), T, kv.shape[0], H, Dqk, Dv,
+                                  K, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(ws), wsb, _stream(dev)),
+           "dsa_sparse_mla_fwd")
+    return out, lse
+
+
+def dsa_sparse_mla_bwd(q, kv, topk_idx, softmax_scale: float, out, lse, dout, topk_len=None, dq=None,
+                       dkv_accum=None, accumulate: bool = False, dkv_bf16=None, workspace=None):
+    """Sparse MLA backward -> (dq bf16 [T,H,Dqk], dkv_accum fp32 [T_k,Dqk], dkv_bf16 or None)."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    if kv.dim() == 3:
+        kv = kv.reshape(kv.shape[0], kv.shape[2])
+    _need(kv, "kv", torch.bfloat16, 2, dev)
+    if topk_idx.dim() == 3:
+        topk_idx = topk_idx.reshape(topk_idx.shape[0], topk_idx.shape[2])
+    _need(topk_idx, "topk_idx", torch.int32, 2, dev)
+    _need(out, "out", torch.bfloat16, 3, dev)
+    _need(lse, "lse", torch.float32, 2, dev)
+    _need(dout, "dout", torch.bfloat16, 3, dev)
+    if topk_len is not None:
+        _need(topk_len, "topk_len", torch.int32, 1, dev)
+    T, H, Dqk = q.shape
+    Dv = out.shape[2]
+    K = topk_idx.shape[1]
+    Tk = kv.shape[0]
+    if dq is None:
+        dq = torch.empty(T, H, Dqk, dtype=torch.bfloat16, device=dev)
+    if dkv_accum is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs an existing dkv_accum")
+        dkv_accum = torch.empty(Tk, Dqk, dtype=torch.float32, device=dev)
+    _need(dkv_accum, "dkv_accum", torch.float32, 2, dev)
+    ws, wsb = _workspace("bwd", T, H, dev, workspace)
+    _check(lib.dsa_sparse_mla_bwd(_ptr(q), _ptr(kv), _ptr(topk_idx), _ptr(topk_len), T, Tk, H, Dqk, Dv, K,
+                                  float(softmax_scale), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dkv_accum),
+                                  1 if accumulate else 0, _ptr(dkv_bf16), _ptr(ws), wsb, _stream(dev)),
+           "dsa_sparse_mla_bwd")
+    return dq, dkv_accum, dkv_bf16
+
+
+def dsa_read_device_status(workspace: torch.Tensor) -> int:
+    """Synchronise the current stream, read and clear the device error word of ``workspace``."""
+    lib = load_library()
+    st = ctypes.c_int32(0)
+    _check(lib.dsa_read_device_status(_ptr(workspace), _stream(workspace.device), ctypes.byref(st)),
+           "dsa_read_device_status")
+    return st.value

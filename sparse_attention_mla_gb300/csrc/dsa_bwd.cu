@@ -1,0 +1,505 @@
+// dsa_bwd.cu -- absorbed sparse MLA backward on sm_103a (tcgen05 + TMEM + TMA).
+//
+// For one query token t and a group of 64 heads per CTA, with P_j =
+// exp(z_j - lse), D = <dO, O>, dP_j = <dO, kv[idx_j, :512]>, dS_j = P_j(dP_j - D):
+//   dq[t,h,:]          = scale sum_j dS_j kv[idx_j, :]
+//   dkv[idx_j, :]     += scale sum_h dS_j q[t,h,:]
+//   dkv[idx_j, :512]  += sum_h P_j dO[t,h,:]
+// Source: NeMo AutoModel glm_moe_dsa.kernels.cudnn_dsa,
+// _CudnnSparseAttention.backward (query gradient [T, H, 576] and latent-KV
+// gradient from grad_output [T, H, 512]); SkyRL PR 2423, "Summary" (query
+// rows independent, key gradients sum); the forward it differentiates is
+// described in "Accelerating GLM-5.2 Long-Context Training with cuDNN Fused
+// DSA Kernels ...", "How DSA works".
+//
+// Design (sm_103a):
+//  * P is recomputed from the saved lse (no running max), D comes from a
+//    small preprocessing kernel.
+//  * All MMAs use M = 128 (keys of the tile, or channels) and N = 64 heads or
+//    64 channels:  S^T = KV Q^T and dP^T = V dO^T (keys on M), dQ^T += KV^T dS^T
+//    (channels on M), dKV = dS^T Q + P^T dO (keys on M, 64-channel groups).
+//  * Q [64 x Dqk] and dO [64 x 512] stay resident in shared memory for the
+//    token; the gathered tile streams twice through a 2-slot ring of
+//    128-channel pairs (once for S^T/dP^T, once for dQ^T).
+//  * P^T (bf16) goes to TMEM and is the A operand of the P^T dO product; dS^T
+//    (bf16, pre-multiplied by scale) goes to shared memory where it is both
+//    the B operand of dQ^T and the A operand of dS^T Q.
+//  * dKV of a tile is produced 64 channels at a time into two TMEM buffers
+//    (aliasing S^T / dP^T, which are dead by then) and flushed by the softmax
+//    warps with red.global.add.v4.f32 on the gathered rows of the fp32
+//    accumulator (L2 reductions).
+#include <cmath>
+
+#include "dsa_device.cuh"
+#include "dsa_host.h"
+
+namespace dsa {
+namespace bwd {
+
+constexpr int kThreads = 320;
+constexpr int kTile = 128;
+constexpr int kHeads = 64;
+constexpr int kDv = 512;
+
+template <int DQK>
+struct Smem {
+  static constexpr int NCH = DQK / 64;         // channel chunks of kv / q
+  static constexpr int NP = (NCH + 1) / 2;     // channel pairs (128 channels)
+  static constexpr int Q_CHUNK = kHeads * 128; // 8 KiB
+  static constexpr int KV_CHUNK = kTile * 128; // 16 KiB
+  static constexpr int SLOT = 2 * KV_CHUNK;    // ring slot: one pair
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = OFF_Q + NCH * Q_CHUNK;
+  static constexpr int OFF_RING = OFF_DO + 8 * Q_CHUNK;
+  static constexpr int OFF_DS = OFF_RING + 2 * SLOT;
+  static constexpr int OFF_MISC = OFF_DS + KV_CHUNK;
+  static constexpr int MISC = 1024;
+  static constexpr int TOTAL = OFF_MISC + MISC + 1024;
+};
+
+// misc layout
+constexpr int M_FULL = 0, M_EMPTY = 16, M_SDP = 32, M_DS = 40, M_KVF = 48, M_KVE = 64, M_DQ = 80, M_FIN = 88;
+constexpr int M_TMEM = 128, M_NEFF = 132, M_ABORT = 136;
+
+// TMEM columns
+constexpr uint32_t C_S = 0, C_DP = 64, C_DQ = 128, C_P = 448;
+
+// D[t,h] = <dO[t,h,:], O[t,h,:]> in fp32; one warp per (t, h).
+__global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
+                                 float* __restrict__ delta, long long rows) {
+  const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= rows) return;
+  const uint4* o = reinterpret_cast<const uint4*>(out + w * kDv);
+  const uint4* d = reinterpret_cast<const uint4*>(dout + w * kDv);
+  float acc = 0.f;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    uint4 a = __ldg(o + lane + 32 * k), b = __ldg(d + lane + 32 * k);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float2 fa = __bfloat1622float2(a2[e]), fb = __bfloat1622float2(b2[e]);
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+  }
+#pragma unroll
+  for (int o2 = 16; o2 >= 1; o2 >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o2);
+  if (lane == 0) delta[w] = acc;
+}
+
+__global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, long long n4) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+    float4 v = reinterpret_cast<const float4*>(src)[i];
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t*>(&lo);
+    o.y = *reinterpret_cast<uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(dst)[i] = o;
+  }
+}
+
+template <int DQK>
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_bwd_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16* __restrict__ q,
+                          const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ topk_len,
+                          const float* __restrict__ lse, const float* __restrict__ delta,
+                          const __nv_bfloat16* __restrict__ dout, int T, int Tk, int H, int K, float scale,
+                          __nv_bfloat16* __restrict__ dq, float* __restrict__ dkv, int* __restrict__ err) {
+  using L = Smem<DQK>;
+  constexpr int NCH = L::NCH;
+  constexpr int NP = L::NP;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sQ = smem_u32(smem + L::OFF_Q);
+  const uint32_t sDO = smem_u32(smem + L::OFF_DO);
+  const uint32_t sRing = smem_u32(smem + L::OFF_RING);
+  const uint32_t sDS = smem_u32(smem + L::OFF_DS);
+  uint8_t* misc = smem + L::OFF_MISC;
+  const uint32_t bar_full = smem_u32(misc + M_FULL), bar_empty = smem_u32(misc + M_EMPTY);
+  const uint32_t bar_sdp = smem_u32(misc + M_SDP), bar_ds = smem_u32(misc + M_DS);
+  const uint32_t bar_kvf = smem_u32(misc + M_KVF), bar_kve = smem_u32(misc + M_KVE);
+  const uint32_t bar_dq = smem_u32(misc + M_DQ), bar_fin = smem_u32(misc + M_FIN);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + M_TMEM);
+  int* s_neff = reinterpret_cast<int*>(misc + M_NEFF);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(misc + M_ABORT);
+
+  const int t = blockIdx.x;
+  const int hg = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t* idx_row = topk_idx + (size_t)t * K;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_kvf + 8 * s, 1);
+      mbar_init(bar_kve + 8 * s, 8);
+    }
+    mbar_init(bar_sdp, 1);
+    mbar_init(bar_ds, 8);
+    mbar_init(bar_dq, 1);
+    mbar_init(bar_fin, 1);
+    *s_neff = 0;
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(s_tmem), 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+
+  if (warp >= 2) {
+    const int tid = threadIdx.x - 64;
+    if (topk_len != nullptr) {
+      if (tid == 0) {
+        int n = topk_len[t];
+        *s_neff = n < 0 ? 0 : (n > K ? K : n);
+      }
+    } else {
+      int last = 0;
+      for (int j = tid; j < K; j += 256)
+        if (idx_row[j] >= 0) last = j + 1;
+      if (last) atomicMax(s_neff, last);
+    }
+    // Q [64 x DQK] and dO [64 x 512] -> 128B-swizzled chunks (rows = heads); heads >= H are zero.
+    for (int u = tid; u < kHeads * NCH * 8; u += 256) {
+      const int hh = u / (NCH * 8), rem = u - hh * (NCH * 8), c = rem >> 3, uc = rem & 7;
+      const int h = hg * kHeads + hh;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (h < H) v = __ldg(reinterpret_cast<const uint4*>(q + ((size_t)t * H + h) * DQK + c * 64 + uc * 8));
+      st_shared_v4(sQ + c * L::Q_CHUNK + sw128_off(hh, uc), v.x, v.y, v.z, v.w);
+    }
+    for (int u = tid; u < kHeads * 8 * 8; u += 256) {
+      const int hh = u >> 6, rem = u & 63, c = rem >> 3, uc = rem & 7;
+      const int h = hg * kHeads + hh;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (h < H) v = __ldg(reinterpret_cast<const uint4*>(dout + ((size_t)t * H + h) * kDv + c * 64 + uc * 8));
+      st_shared_v4(sDO + c * L::Q_CHUNK + sw128_off(hh, uc), v.x, v.y, v.z, v.w);
+    }
+    // Ring rows that are never gathered must stay finite: zero the ring once.
+    for (int u = tid; u < 2 * L::SLOT / 16; u += 256) st_shared_v4(sRing + u * 16, 0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  const int n_eff = *s_neff;
+  const int ntiles = (n_eff + kTile - 1) / kTile;
+  const uint32_t tmem = *s_tmem;
+
+  if (warp == 0) {
+    // ======================= producer =======================
+    int L_cnt = 0;  // pair loads issued so far
+    bool stop = false;
+    for (int i = 0; i < ntiles && !stop; ++i) {
+      const int base = i * kTile;
+      const int ngroups = min(32, (n_eff - base + 3) >> 2);
+      int r[4] = {0, 0, 0, 0};
+      if (lane < ngroups) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = base + 4 * lane + e;
+          int ix = -1;
+          if (j < n_eff) ix = __ldg(idx_row + j);
+          if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
+          r[e] = (ix >= 0 && ix < Tk) ? ix : 0;
+        }
+      }
+      for (int pass = 0; pass < 2 && !stop; ++pass) {
+        for (int p = 0; p < NP; ++p, ++L_cnt) {
+          const int slot = L_cnt & 1;
+          const uint32_t ph = ((L_cnt >> 1) & 1) ^ 1;
+          if (!mbar_wait(bar_empty + 8 * slot, ph, s_abort, err)) { stop = true; break; }
+          const int nch = (2 * p + 1 < NCH) ? 2 : 1;
+          if (lane == 0) mbar_expect_tx(bar_full + 8 * slot, (uint32_t)(ngroups * 4 * 128 * nch));
+          __syncwarp();
+          if (lane < ngroups) {
+            const uint32_t dst = sRing + slot * L::SLOT + (4 * lane) * 128;
+            for (int cc = 0; cc < nch; ++cc)
+              tma_gather4(dst + cc * L::KV_CHUNK, &kv_map, (2 * p + cc) * 64, r[0], r[1], r[2], r[3],
+                          bar_full + 8 * slot);
+          }
+        }
+      }
+    }
+    if (*s_abort && L_cnt > 0 && lane == 0) {
+      volatile int dummy = 0;
+      const int last = L_cnt - 1;
+      mbar_wait(bar_full + 8 * (last & 1), (last >> 1) & 1, &dummy, err);
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t kIdKK = idesc_bf16(128, 64, false, false);  // A K-major, B K-major
+      constexpr uint32_t kIdMM = idesc_bf16(128, 64, true, true);    // A MN-major, B MN-major
+      constexpr uint32_t kIdKM = idesc_bf16(128, 64, false, true);   // A K-major (smem or tmem), B MN-major
+      int L_cnt = 0, G = 0;
+      bool stop = false;
+      for (int i = 0; i < ntiles && !stop; ++i) {
+        // S^T / dP^T alias the dKV staging buffers: both must be flushed.
+        if (i > 0) {
+          if (!mbar_wait(bar_kve + 8 * (G & 1), (((G >> 1) & 1) ^ 1), s_abort, err)) break;
+          if (!mbar_wait(bar_kve + 8 * ((G + 1) & 1), ((((G + 1) >> 1) & 1) ^ 1), s_abort, err)) break;
+        }
+        // ---- pass A: S^T = KV Q^T, dP^T = V dO^T ----
+        for (int p = 0; p < NP; ++p, ++L_cnt) {
+          const int slot = L_cnt & 1;
+          if (!mbar_wait(bar_full + 8 * slot, (L_cnt >> 1) & 1, s_abort, err)) { stop = true; break; }
+          tc_fence_after();
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * p + cc;
+            if (c >= NCH) break;
+            const uint32_t a0 = sRing + slot * L::SLOT + cc * L::KV_CHUNK;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ss(tmem + C_S, sdesc_sw128(a0 + k * 32, 16, 1024), sdesc_sw128(sQ + c * L::Q_CHUNK + k * 32, 16, 1024),
+                     kIdKK, (c | k) != 0);
+            if (c < 8) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_ss(tmem + C_DP, sdesc_sw128(a0 + k * 32, 16, 1024),
+                       sdesc_sw128(sDO + c * L::Q_CHUNK + k * 32, 16, 1024), kIdKK, (c | k) != 0);
+            }
+          }
+          mma_commit(bar_empty + 8 * slot);
+        }
+        if (stop) break;
+        mma_commit(bar_sdp);
+        if (!mbar_wait(bar_ds, i & 1, s_abort, err)) break;
+        tc_fence_after();
+        // ---- pass B: dQ^T[pair p] += KV^T dS'^T ----
+        for (int p = 0; p < NP; ++p, ++L_cnt) {
+          const int slot = L_cnt & 1;
+          if (!mbar_wait(bar_full + 8 * slot, (L_cnt >> 1) & 1, s_abort, err)) { stop = true; break; }
+          tc_fence_after();
+          const uint32_t a0 = sRing + slot * L::SLOT;
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k)
+            mma_ss(tmem + C_DQ + p * 64, sdesc_sw128(a0 + k * 2048, L::KV_CHUNK, 1024),
+                   sdesc_sw128(sDS + k * 2048, L::KV_CHUNK, 1024), kIdMM, (i > 0 || k > 0) ? 1u : 0u);
+          mma_commit(bar_empty + 8 * slot);
+        }
+        if (stop) break;
+        // ---- dKV = dS'^T Q (+ P^T dO), 64 channels at a time ----
+        for (int g = 0; g < NCH; ++g, ++G) {
+          const int b = G & 1;
+          if (!mbar_wait(bar_kve + 8 * b, ((G >> 1) & 1) ^ 1, s_abort, err)) { stop = true; break; }
+          tc_fence_after();
+          const uint32_t d = tmem + 64 * b;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(d, sdesc_sw128(sDS + k * 32, 16, 1024), sdesc_sw128(sQ + g * L::Q_CHUNK + k * 2048, 16, 1024),
+                   kIdKM, k > 0);
+          if (g < 8) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ts(d, tmem + C_P + 8 * k, sdesc_sw128(sDO + g * L::Q_CHUNK + k * 2048, 16, 1024), kIdKM, 1u);
+          }
+          mma_commit(bar_kvf + 8 * b);
+        }
+      }
+      mma_commit(bar_dq);
+      mma_commit(bar_fin);
+      volatile int dummy = 0;
+      mbar_wait(bar_fin, 0, &dummy, err);
+    }
+    __syncwarp();
+  } else {
+    // ======================= softmax-backward, dKV flush, dQ epilogue =======================
+    const int sw = warp - 2;
+    const int qd = warp & 3;
+    const int ch = sw >> 2;           // heads ch*32 .. ch*32+31 / channel half of a 64-channel group
+    const int r = qd * 32 + lane;     // key row of the tile
+    const int bar_id = 1 + ch;
+    const float sl2e = scale * 1.4426950408889634f;
+    float lse2[32], dl[32];
+#pragma unroll
+    for (int h = 0; h < 32; ++h) {
+      const int hh = hg * kHeads + ch * 32 + h;
+      lse2[h] = (hh < H) ? lse[(size_t)t * H + hh] * 1.4426950408889634f : INFINITY;  // padded heads: P = 0
+      dl[h] = (hh < H) ? delta[(size_t)t * H + hh] : 0.f;
+    }
+    int G = 0;
+    bool aborted = false;
+    for (int i = 0; i < ntiles && !aborted; ++i) {
+      const bool got = mbar_wait(bar_sdp, i & 1, s_abort, err);
+      if (named_bar_or(bar_id, 128, !got)) { aborted = true; break; }
+      tc_fence_after();
+      uint32_t sv[32], dv[32];
+      tmem_ld32(tmem_addr(tmem + C_S, qd * 32, ch * 32), sv);
+      tmem_ld32(tmem_addr(tmem + C_DP, qd * 32, ch * 32), dv);
+      tmem_ld_wait();
+      const int j = i * kTile + r;
+      int ix = -1;
+      if (j < n_eff) ix = __ldg(idx_row + j);
+      const bool valid = ix >= 0 && ix < Tk;
+      uint32_t pk[16], dk[16];
+#pragma unroll
+      for (int h = 0; h < 32; h += 2) {
+        float p0 = 0.f, p1 = 0.f, s0 = 0.f, s1 = 0.f;
+        if (valid) {
+          p0 = exp2f(__uint_as_float(sv[h]) * sl2e - lse2[h]);
+          p1 = exp2f(__uint_as_float(sv[h + 1]) * sl2e - lse2[h + 1]);
+          s0 = scale * p0 * (__uint_as_float(dv[h]) - dl[h]);
+          s1 = scale * p1 * (__uint_as_float(dv[h + 1]) - dl[h + 1]);
+        }
+        pk[h >> 1] = pack_bf16x2(p0, p1);
+        dk[h >> 1] = pack_bf16x2(s0, s1);
+      }
+#pragma unroll
+      for (int uu = 0; uu < 4; ++uu)
+        st_shared_v4(sDS + sw128_off(r, ch * 4 + uu), dk[4 * uu], dk[4 * uu + 1], dk[4 * uu + 2], dk[4 * uu + 3]);
+      tmem_st16(tmem_addr(tmem + C_P, qd * 32, ch * 16), pk);
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ds);
+      // ---- flush dKV groups of this tile ----
+      for (int g = 0; g < NCH; ++g, ++G) {
+        const int b = G & 1;
+        const bool ok = mbar_wait(bar_kvf + 8 * b, (G >> 1) & 1, s_abort, err);
+        if (!ok) { aborted = true; }
+        tc_fence_after();
+        if (ok) {
+          uint32_t v[32];
+          tmem_ld32(tmem_addr(tmem + 64 * b, qd * 32, ch * 32), v);
+          tmem_ld_wait();
+          if (valid) {
+            float* dst = dkv + (size_t)ix * DQK + g * 64 + ch * 32;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              red_add_v4(dst + 4 * e, __uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                         __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_kve + 8 * b);
+        if (!ok) break;
+      }
+      aborted = named_bar_or(bar_id, 128, aborted);
+    }
+    // ---- dQ epilogue ----
+    bool have = false;
+    if (!aborted && ntiles > 0) {
+      const bool got = mbar_wait(bar_dq, 0, s_abort, err);
+      have = !named_bar_or(bar_id, 128, !got);
+      tc_fence_after();
+    }
+    const int hbase = hg * kHeads + ch * 32;
+    const int hcount = min(32, H - hbase);
+#pragma unroll 1
+    for (int p = 0; p < NP; ++p) {
+      uint32_t v[32];
+      if (have) {
+        tmem_ld32(tmem_addr(tmem + C_DQ + p * 64, qd * 32, ch * 32), v);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int h = 0; h < 32; ++h) v[h] = 0u;
+      }
+      const int c = p * 128 + qd * 32 + lane;
+      if (c < DQK) {
+        __nv_bfloat16* dp = dq + ((size_t)t * H + hbase) * DQK + c;
+#pragma unroll
+        for (int h = 0; h < 32; ++h)
+          if (h < hcount) dp[(size_t)h * DQK] = __float2bfloat16_rn(__uint_as_float(v[h]));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DQK>
+dsa_status_t launch(const CUtensorMap& map, const void* q, const int32_t* idx, const int32_t* len, const float* lse,
+                    const float* delta, const void* dout, int T, int Tk, int H, int K, float scale, void* dq,
+                    float* dkv, int* err, cudaStream_t s) {
+  using L = Smem<DQK>;
+  static bool configured = false;
+  if (!configured) {
+    dsa_status_t st = cuda_check(cudaFuncSetAttribute(sparse_mla_bwd_kernel<DQK>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL),
+                                 "configuring sparse_mla_bwd_kernel");
+    if (st != DSA_OK) return st;
+    configured = true;
+  }
+  dim3 grid(T, (H + kHeads - 1) / kHeads);
+  sparse_mla_bwd_kernel<DQK><<<grid, kThreads, L::TOTAL, s>>>(
+      map, reinterpret_cast<const __nv_bfloat16*>(q), idx, len, lse, delta,
+      reinterpret_cast<const __nv_bfloat16*>(dout), T, Tk, H, K, scale, reinterpret_cast<__nv_bfloat16*>(dq), dkv,
+      err);
+  return cuda_check(cudaGetLastError(), "launching sparse_mla_bwd_kernel");
+}
+
+}  // namespace bwd
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" size_t dsa_sparse_mla_bwd_workspace_size(int32_t T, int32_t H) {
+  const size_t delta = (size_t)(T > 0 ? T : 0) * (size_t)(H > 0 ? H : 0) * sizeof(float);
+  return kErrorWordBytes + ((delta + 255) & ~size_t(255));
+}
+
+extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
+                                           const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
+                                           int32_t Dv, int32_t K, float softmax_scale, const dsa_bf16_t* out,
+                                           const float* lse, const dsa_bf16_t* dout, dsa_bf16_t* dq,
+                                           float* dkv_accum, int32_t accumulate, dsa_bf16_t* dkv_bf16,
+                                           void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
+  const char* who = "dsa_sparse_mla_bwd";
+  if (T < 0 || T_k < 1 || H < 1 || K < 1)
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: need T >= 0, T_k >= 1, H >= 1, K >= 1 (got %d, %d, %d, %d)", who, T,
+                T_k, H, K);
+  if (Dqk != 576 && Dqk != 512) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: Dqk must be 576 or 512 (got %d)", who, Dqk);
+  if (Dv != 512) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: Dv must be 512 (got %d)", who, Dv);
+  if (accumulate != 0 && accumulate != 1) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: accumulate must be 0 or 1", who);
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f))
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: softmax_scale must be finite and > 0", who);
+  if (!kv || !dkv_accum) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: kv / dkv_accum is NULL", who);
+  if (T > 0 && (!q || !topk_idx || !out || !lse || !dout || !dq))
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: null tensor pointer", who);
+  if (!aligned16(kv) || !aligned16(dkv_accum) || (T > 0 && (!aligned16(q) || !aligned16(out) || !aligned16(dout))))
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: q, kv, out, dout and dkv_accum must be 16-byte aligned", who);
+  if (dkv_bf16 && (reinterpret_cast<uintptr_t>(dkv_bf16) & 7u))
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: dkv_bf16 must be 8-byte aligned", who);
+  dsa_status_t st = check_workspace(workspace, workspace_bytes, dsa_sparse_mla_bwd_workspace_size(T, H), who);
+  if (st != DSA_OK) return st;
+  if ((st = check_device()) != DSA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = clear_error_word(workspace, s)) != DSA_OK) return st;
+  if (!accumulate &&
+      (st = cuda_check(cudaMemsetAsync(dkv_accum, 0, (size_t)T_k * Dqk * sizeof(float), s), "zeroing dkv_accum")))
+    return st;
+  int* err = reinterpret_cast<int*>(workspace);
+  float* delta = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + kErrorWordBytes);
+  if (T > 0) {
+    const long long rows = (long long)T * H;
+    bwd::bwd_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(out),
+                                                                     reinterpret_cast<const __nv_bfloat16*>(dout),
+                                                                     delta, rows);
+    if ((st = cuda_check(cudaGetLastError(), "launching bwd_delta_kernel"))) return st;
+    CUtensorMap map;
+    if ((st = make_map_2d_bf16(&map, kv, (uint64_t)T_k, (uint64_t)Dqk, (uint64_t)Dqk, 64, 1)) != DSA_OK) return st;
+    st = (Dqk == 576) ? bwd::launch<576>(map, q, topk_idx, topk_len, lse, delta, dout, T, T_k, H, K, softmax_scale,
+                                         dq, dkv_accum, err, s)
+                      : bwd::launch<512>(map, q, topk_idx, topk_len, lse, delta, dout, T, T_k, H, K, softmax_scale,
+                                         dq, dkv_accum, err, s);
+    if (st != DSA_OK) return st;
+  }
+  if (dkv_bf16) {
+    const long long n4 = (long long)T_k * Dqk / 4;
+    bwd::f32_to_bf16_kernel<<<152 * 4, 256, 0, s>>>(dkv_accum, reinterpret_cast<__nv_bfloat16*>(dkv_bf16), n4);
+    if ((st = cuda_check(cudaGetLastError(), "launching f32_to_bf16_kernel"))) return st;
+  }
+  return ok();
+}

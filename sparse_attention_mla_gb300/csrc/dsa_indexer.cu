@@ -1,0 +1,433 @@
+// dsa_indexer.cu -- lightning-indexer score fused with per-query causal top-k
+// on sm_103a (tcgen05 + TMEM + TMA).
+//
+//   score(t, s) = sum_h w[t,h] * max(0, <q_idx[t,h,:], k_idx[s,:]>),  s in [seq_start[t], t]
+// and for each t the n = min(K, causal length) best keys (score descending,
+// ties to the lower index), written ascending with a -1 suffix.
+// Source: "Accelerating GLM-5.2 Long-Context Training with cuDNN Fused DSA
+// Kernels ...", "How DSA works" (the indexer scores query-key relevance and
+// emits the top-k per query) and "Why DSA needs fused kernels" (the S x S
+// score matrix must stay on chip); NeMo AutoModel
+// glm_moe_dsa.kernels.cudnn_indexer_topk (index_q [T, H_index, 128], one
+// shared index_k [T_k, 128], pre-scaled fp32 head weights, K in [1, 2048]);
+// the canonical ascending/-1 form from cudnn_sparse_attention (topk_length).
+//
+// Design (sm_103a):
+//  * One CTA owns 4 consecutive query tokens.  Their 4 x 64 index heads form
+//    the N = 256 side of the MMA; keys are the M = 128 side:
+//    D[key, (token, head)] = K_tile . Q^T, fp32 in TMEM, double-buffered
+//    (2 x 256 columns).  k_idx tiles arrive by TMA (2 boxes of 64 channels).
+//  * The epilogue warps (one TMEM lane = one key) apply ReLU and the fp32
+//    head-weighted sum, so scores exist only in registers.
+//  * Selection: each token keeps a shared-memory buffer of candidates
+//    (score, index) that beat its running threshold.  Candidates are appended
+//    in ascending key order (a block-wide scan, not atomics), and a full
+//    buffer is compacted to the best K by an 8-bit radix select on the
+//    order-preserving integer image of the score; ties at the threshold keep
+//    the earliest (= lowest-index) entries, and the compaction is stable, so
+//    the buffer stays sorted by index and the output needs no sort.
+#include <climits>
+#include <cmath>
+
+#include "dsa_device.cuh"
+#include "dsa_host.h"
+
+namespace dsa {
+namespace idx {
+
+constexpr int kThreads = 320;
+constexpr int kTokens = 4;     // query tokens per CTA
+constexpr int kHeads = 64;     // index heads (padded)
+constexpr int kDi = 128;       // index head dim
+constexpr int kTile = 128;     // keys per tile
+constexpr int kN = kTokens * kHeads;
+constexpr int kMaxK = 2048;
+
+constexpr int OFF_Q = 0;                       // 2 chunks x [256 rows x 128 B]
+constexpr int Q_CHUNK = kN * 128;              // 32 KiB
+constexpr int OFF_K = OFF_Q + 2 * Q_CHUNK;     // 2 stages x 2 chunks x [128 rows x 128 B]
+constexpr int K_CHUNK = kTile * 128;           // 16 KiB
+constexpr int K_STAGE = 2 * K_CHUNK;
+constexpr int OFF_MISC = OFF_K + 2 * K_STAGE;  // 128 KiB
+constexpr int MISC = 4096;
+constexpr int OFF_CAND = OFF_MISC + MISC;
+constexpr int CAP = 2944;                      // candidates per token
+constexpr int TOTAL = OFF_CAND + kTokens * CAP * 8 + 1024;
+static_assert(TOTAL <= 232448, "shared memory budget");
+static_assert(CAP >= kMaxK + kTile + 128, "candidate buffer must hold K + one tile");
+
+// misc layout
+constexpr int M_KF = 0, M_KE = 16, M_DF = 32, M_DE = 48, M_FIN = 64;
+constexpr int M_TMEM = 128, M_ABORT = 132;
+constexpr int M_W = 256;                // float [4][64]
+constexpr int M_WCNT = M_W + 1024;      // int [2 halves][2 parity][4 warps]
+constexpr int M_HIST = M_WCNT + 64;     // int [2 halves][256]
+constexpr int M_SEL = M_HIST + 2048;    // int [2 halves][4]
+
+__device__ __forceinline__ uint32_t ordered(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unordered(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Per-half context: 4 warps (128 threads), one named barrier.
+struct Half {
+  int bar;     // named barrier id
+  int tid;     // 0..127 within the half (ordered by key row)
+  int wq;      // warp position 0..3 by key row (lane quadrant)
+  int lane;
+  int* wcnt;   // [2 parity][4]
+  int* hist;   // [256]
+  int* sel;    // [4]
+};
+
+// Exclusive block scan of a predicate over the 128 threads of a half in
+// key-row order; returns (exclusive prefix, total).  Uses wcnt[par].
+__device__ __forceinline__ int2 half_scan(const Half& hf, bool pred, int par) {
+  const uint32_t ball = __ballot_sync(0xffffffffu, pred);
+  if (hf.lane == 0) hf.wcnt[par * 4 + hf.wq] = __popc(ball);
+  named_bar(hf.bar, 128);
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int c = hf.wcnt[par * 4 + w];
+    before += (w < hf.wq) ? c : 0;
+    total += c;
+  }
+  before += __popc(ball & ((1u << hf.lane) - 1u));
+  return make_int2(before, total);
+}
+
+// Keep the best `target` of the cnt candidates (score desc, index asc),
+// stably, in place.  Returns the new threshold image (accept iff key > thr).
+__device__ uint32_t compact(const Half& hf, float* cs, int* ci, int cnt, int target, int& parity) {
+  // radix select: find the target-th largest key image v
+  uint32_t prefix = 0, pmask = 0;
+  int kk = target;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    hf.hist[hf.tid] = 0;
+    hf.hist[hf.tid + 128] = 0;
+    named_bar(hf.bar, 128);
+    for (int e = hf.tid; e < cnt; e += 128) {
+      const uint32_t key = ordered(cs[e]);
+      if ((key & pmask) == prefix) atomicAdd(&hf.hist[(key >> shift) & 255], 1);
+    }
+    named_bar(hf.bar, 128);
+    if (hf.wq == 0) {
+      // lane l owns bins 255-8l .. 248-8l (descending)
+      int c[8], s = 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        c[b] = hf.hist[255 - 8 * hf.lane - b];
+        s += c[b];
+      }
+      int incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (hf.lane >= o) incl += v;
+      }
+      int above = incl - s;  // count in bins above this lane's first bin
+      if (above < kk && kk <= incl) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if (above < kk && kk <= above + c[b]) {
+            hf.sel[0] = 255 - 8 * hf.lane - b;
+            hf.sel[1] = above;
+          }
+          above += c[b];
+        }
+      }
+    }
+    named_bar(hf.bar, 128);
+    const int d = hf.sel[0];
+    kk -= hf.sel[1];
+    prefix |= (uint32_t)d << shift;
+    pmask |= 255u << shift;
+    named_bar(hf.bar, 128);  // sel is rewritten by the next pass
+  }
+  const uint32_t v = prefix;  // kk >= 1 ties at v are kept (the earliest ones)
+  int kept = 0, ties = 0;
+  for (int base = 0; base < cnt; base += 128) {
+    const int e = base + hf.tid;
+    float s = 0.f;
+    int ix = 0;
+    uint32_t key = 0;
+    if (e < cnt) {
+      s = cs[e];
+      ix = ci[e];
+      key = ordered(s);
+    }
+    const bool eq = (e < cnt) && key == v;
+    const int2 te = half_scan(hf, eq, parity);
+    parity ^= 1;
+    const bool keep = (e < cnt) && (key > v || (eq && ties + te.x < kk));
+    const int2 ke = half_scan(hf, keep, parity);
+    parity ^= 1;
+    // every thread has read its element (before the scans' barriers) -> safe to write
+    if (keep) {
+      cs[kept + ke.x] = s;
+      ci[kept + ke.x] = ix;
+    }
+    kept += ke.y;
+    ties += te.y;
+  }
+  named_bar(hf.bar, 128);
+  return v;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_topk_kernel(const __grid_constant__ CUtensorMap k_map, const __nv_bfloat16* __restrict__ q_idx,
+                        const float* __restrict__ w, const int32_t* __restrict__ seq_start, int T, int Tk, int Hi,
+                        int K, int32_t* __restrict__ topk_idx, int32_t* __restrict__ topk_len,
+                        int* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sQ = smem_u32(smem + OFF_Q);
+  const uint32_t sK = smem_u32(smem + OFF_K);
+  uint8_t* misc = smem + OFF_MISC;
+  const uint32_t bar_kf = smem_u32(misc + M_KF), bar_ke = smem_u32(misc + M_KE);
+  const uint32_t bar_df = smem_u32(misc + M_DF), bar_de = smem_u32(misc + M_DE);
+  const uint32_t bar_fin = smem_u32(misc + M_FIN);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + M_TMEM);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(misc + M_ABORT);
+  float* s_w = reinterpret_cast<float*>(misc + M_W);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // heaviest (latest) token blocks first
+  const int nblk = (T + kTokens - 1) / kTokens;
+  const int t0 = (nblk - 1 - (int)blockIdx.x) * kTokens;
+  const int nt = min(kTokens, T - t0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_kf + 8 * s, 1);
+      mbar_init(bar_ke + 8 * s, 1);
+      mbar_init(bar_df + 8 * s, 1);
+      mbar_init(bar_de + 8 * s, 8);
+    }
+    mbar_init(bar_fin, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(s_tmem), 512);
+    tmem_relinquish();
+  }
+  // key-tile range covering every token's causal window
+  int lo = INT_MAX, hi = -1;
+  for (int k = 0; k < nt; ++k) {
+    lo = min(lo, __ldg(seq_start + t0 + k));
+    hi = max(hi, t0 + k);
+  }
+  hi = min(hi, Tk - 1);
+  const int kt0 = lo / kTile, kt1 = hi / kTile;
+  const int ntiles = (hi >= lo) ? kt1 - kt0 + 1 : 0;
+
+  if (warp >= 2) {
+    const int tid = threadIdx.x - 64;
+    // Q rows (token k, head h) -> 2 chunks of [256 rows x 128 B], swizzled; padding rows zero
+    for (int u = tid; u < kN * 16; u += 256) {
+      const int row = u >> 4, c = (u >> 3) & 1, uc = u & 7;
+      const int k = row / kHeads, h = row - k * kHeads;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (k < nt && h < Hi)
+        v = __ldg(reinterpret_cast<const uint4*>(q_idx + ((size_t)(t0 + k) * Hi + h) * kDi + c * 64 + uc * 8));
+      st_shared_v4(sQ + c * Q_CHUNK + sw128_off(row, uc), v.x, v.y, v.z, v.w);
+    }
+    for (int u = tid; u < kTokens * kHeads; u += 256) {
+      const int k = u / kHeads, h = u - k * kHeads;
+      s_w[u] = (k < nt && h < Hi) ? __ldg(w + (size_t)(t0 + k) * Hi + h) : 0.f;
+    }
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  const uint32_t tmem = *s_tmem;
+
+  if (warp == 0) {
+    // ======================= producer: k_idx tiles =======================
+    if (lane == 0) {
+      int i = 0;
+      for (; i < ntiles; ++i) {
+        const int s = i & 1;
+        if (!mbar_wait(bar_ke + 8 * s, ((i >> 1) & 1) ^ 1, s_abort, err)) break;
+        mbar_expect_tx(bar_kf + 8 * s, K_STAGE);
+        const int row = (kt0 + i) * kTile;
+        tma_load_2d(sK + s * K_STAGE, &k_map, 0, row, bar_kf + 8 * s);
+        tma_load_2d(sK + s * K_STAGE + K_CHUNK, &k_map, 64, row, bar_kf + 8 * s);
+      }
+      if (*s_abort && i > 0) {
+        volatile int dummy = 0;
+        mbar_wait(bar_kf + 8 * ((i - 1) & 1), ((i - 1) >> 1) & 1, &dummy, err);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t kId = idesc_bf16(128, kN, false, false);
+      for (int i = 0; i < ntiles; ++i) {
+        const int s = i & 1, b = i & 1;
+        if (!mbar_wait(bar_kf + 8 * s, (i >> 1) & 1, s_abort, err)) break;
+        if (!mbar_wait(bar_de + 8 * b, ((i >> 1) & 1) ^ 1, s_abort, err)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + b * kN, sdesc_sw128(sK + s * K_STAGE + c * K_CHUNK + k * 32, 16, 1024),
+                   sdesc_sw128(sQ + c * Q_CHUNK + k * 32, 16, 1024), kId, (c | k) != 0);
+        mma_commit(bar_ke + 8 * s);
+        mma_commit(bar_df + 8 * b);
+      }
+      mma_commit(bar_fin);
+      volatile int dummy = 0;
+      mbar_wait(bar_fin, 0, &dummy, err);
+    }
+    __syncwarp();
+  } else {
+    // ======================= score epilogue + selection =======================
+    const int sw = warp - 2;
+    const int qd = warp & 3;
+    const int half = sw >> 2;  // tokens 2*half, 2*half+1
+    Half hf;
+    hf.bar = 1 + half;
+    hf.wq = qd;
+    hf.lane = lane;
+    hf.tid = qd * 32 + lane;
+    hf.wcnt = reinterpret_cast<int*>(misc + M_WCNT) + half * 8;
+    hf.hist = reinterpret_cast<int*>(misc + M_HIST) + half * 256;
+    hf.sel = reinterpret_cast<int*>(misc + M_SEL) + half * 4;
+    float* cs[2];
+    int* ci[2];
+    int win_lo[2], win_hi[2], cnt[2] = {0, 0};
+    uint32_t thr[2] = {0u, 0u};
+    for (int u = 0; u < 2; ++u) {
+      const int k = 2 * half + u;
+      cs[u] = reinterpret_cast<float*>(smem + OFF_CAND + k * CAP * 8);
+      ci[u] = reinterpret_cast<int*>(smem + OFF_CAND + k * CAP * 8 + CAP * 4);
+      win_lo[u] = (k < nt) ? __ldg(seq_start + t0 + k) : 1;
+      win_hi[u] = (k < nt) ? t0 + k : 0;  // empty window for inactive tokens
+    }
+    int parity = 0;
+    bool aborted = false;
+    for (int i = 0; i < ntiles; ++i) {
+      const int b = i & 1;
+      const bool got = mbar_wait(bar_df + 8 * b, (i >> 1) & 1, s_abort, err);
+      if (named_bar_or(hf.bar, 128, !got)) { aborted = true; break; }
+      tc_fence_after();
+      uint32_t v[2][64];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t col = b * kN + (2 * half + u) * kHeads;
+        tmem_ld32(tmem_addr(tmem + col, qd * 32, 0), *reinterpret_cast<uint32_t(*)[32]>(&v[u][0]));
+        tmem_ld32(tmem_addr(tmem + col + 32, qd * 32, 0), *reinterpret_cast<uint32_t(*)[32]>(&v[u][32]));
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_de + 8 * b);
+      const int key = (kt0 + i) * kTile + hf.tid;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float* wr = s_w + (2 * half + u) * kHeads;
+        float sc = 0.f;
+#pragma unroll
+        for (int h = 0; h < kHeads; ++h) sc = fmaf(wr[h], fmaxf(__uint_as_float(v[u][h]), 0.f), sc);
+        const bool in = key >= win_lo[u] && key <= win_hi[u];
+        const bool acc = in && ordered(sc) > thr[u];
+        const int2 pos = half_scan(hf, acc, parity);
+        parity ^= 1;
+        if (acc) {
+          cs[u][cnt[u] + pos.x] = sc;
+          ci[u][cnt[u] + pos.x] = key;
+        }
+        cnt[u] += pos.y;
+        if (cnt[u] > CAP - kTile) {
+          named_bar(hf.bar, 128);
+          thr[u] = compact(hf, cs[u], ci[u], cnt[u], K, parity);
+          cnt[u] = K;
+        }
+      }
+    }
+    // ---- final selection and output (ascending, -1 suffix) ----
+    if (!aborted) named_bar(hf.bar, 128);
+    for (int u = 0; u < 2; ++u) {
+      const int k = 2 * half + u;
+      if (k >= nt) continue;
+      const int t = t0 + k;
+      const int c = win_hi[u] - win_lo[u] + 1;
+      const int n = min(K, c);
+      if (!aborted && cnt[u] > n) {
+        compact(hf, cs[u], ci[u], cnt[u], n, parity);
+        cnt[u] = n;
+      }
+      const int have = aborted ? 0 : min(cnt[u], n);
+      int32_t* row = topk_idx + (size_t)t * K;
+      for (int j = hf.tid; j < K; j += 128) row[j] = (j < have) ? ci[u][j] : -1;
+      if (topk_len != nullptr && hf.tid == 0) topk_len[t] = have;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace idx
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" size_t dsa_indexer_topk_workspace_size(int32_t T, int32_t K) {
+  (void)T;
+  (void)K;
+  return kErrorWordBytes;
+}
+
+extern "C" dsa_status_t dsa_indexer_topk(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
+                                         const int32_t* seq_start, int32_t T, int32_t T_k, int32_t Hi, int32_t Di,
+                                         int32_t K, int32_t* topk_idx, int32_t* topk_len, void* workspace,
+                                         size_t workspace_bytes, dsa_stream_t stream) {
+  const char* who = "dsa_indexer_topk";
+  if (T < 0 || T_k < 1) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: need T >= 0 and T_k >= 1", who);
+  if (T_k < T) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: T_k (%d) must be >= T (%d)", who, T_k, T);
+  if (Hi < 1 || Hi > idx::kHeads) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: Hi must be in [1, 64] (got %d)", who, Hi);
+  if (Di != idx::kDi) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: Di must be 128 (got %d)", who, Di);
+  if (K < 1 || K > idx::kMaxK) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: K must be in [1, 2048] (got %d)", who, K);
+  if (!k_idx) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: k_idx is NULL", who);
+  if (T > 0 && (!q_idx || !head_weights || !seq_start || !topk_idx))
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: null tensor pointer", who);
+  if (!aligned16(k_idx) || (T > 0 && !aligned16(q_idx)))
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: q_idx and k_idx must be 16-byte aligned", who);
+  dsa_status_t st = check_workspace(workspace, workspace_bytes, dsa_indexer_topk_workspace_size(T, K), who);
+  if (st != DSA_OK) return st;
+  if ((st = check_device()) != DSA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = clear_error_word(workspace, s)) != DSA_OK) return st;
+  if (T == 0) return ok();
+  CUtensorMap map;
+  if ((st = make_map_2d_bf16(&map, k_idx, (uint64_t)T_k, (uint64_t)idx::kDi, (uint64_t)idx::kDi, 64, idx::kTile)) !=
+      DSA_OK)
+    return st;
+  static bool configured = false;
+  if (!configured) {
+    if ((st = cuda_check(cudaFuncSetAttribute(idx::indexer_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              idx::TOTAL),
+                         "configuring indexer_topk_kernel")))
+      return st;
+    configured = true;
+  }
+  const int nblk = (T + idx::kTokens - 1) / idx::kTokens;
+  idx::indexer_topk_kernel<<<nblk, idx::kThreads, idx::TOTAL, s>>>(
+      map, reinterpret_cast<const __nv_bfloat16*>(q_idx), head_weights, seq_start, T, T_k, Hi, K, topk_idx, topk_len,
+      reinterpret_cast<int*>(workspace));
+  if ((st = cuda_check(cudaGetLastError(), "launching indexer_topk_kernel"))) return st;
+  return ok();
+}
