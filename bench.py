@@ -216,6 +216,7 @@ def run_cuda(args, rank, world, local):
     topk_idx = torch.empty(S, K, dtype=torch.int32, device=dev)
     topk_len = torch.empty(S, dtype=torch.int32, device=dev)
     out = torch.empty(S, H, DV, dtype=torch.bfloat16, device=dev)
+    out_lo = torch.empty(S, H, DV, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(S, H, dtype=torch.float32, device=dev)
     dq = torch.empty(S, H, DQK, dtype=torch.bfloat16, device=dev)
     dkv = torch.empty(S, DQK, dtype=torch.float32, device=dev)
@@ -232,10 +233,10 @@ def run_cuda(args, rank, world, local):
                              topk_len=topk_len, workspace=ws_i)
         if e: e[1].record(stream)
         dsa.dsa_sparse_mla_fwd(mla["q"], mla["kv"], topk_idx, SCALE, topk_len=topk_len, out=out, lse=lse,
-                               workspace=ws_f)
+                               workspace=ws_f, out_lo=out_lo)
         if e: e[2].record(stream)
         dsa.dsa_sparse_mla_bwd(mla["q"], mla["kv"], topk_idx, SCALE, out, lse, mla["dout"], topk_len=topk_len,
-                               dq=dq, dkv_accum=dkv, workspace=ws_b)
+                               dq=dq, dkv_accum=dkv, workspace=ws_b, out_lo=out_lo)
         if e: e[3].record(stream)
 
     for _ in range(args.warmup):
@@ -325,7 +326,8 @@ def run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, flops_per_step, 
     host_in = {k: v.to("cpu").pin_memory() for k, v in list(ind.items()) + list(mla.items())}
     dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
     res_shapes = {"topk_idx": ((S, K), torch.int32), "topk_len": ((S,), torch.int32),
-                  "out": ((S, H, DV), torch.bfloat16), "lse": ((S, H), torch.float32),
+                  "out": ((S, H, DV), torch.bfloat16), "out_lo": ((S, H, DV), torch.bfloat16),
+                  "lse": ((S, H), torch.float32),
                   "dq": ((S, H, DQK), torch.bfloat16), "dkv": ((S, DQK), torch.float32)}
     dres = {k: torch.empty(*s, dtype=d, device=dev) for k, (s, d) in res_shapes.items()}
     hres = {k: torch.empty(*s, dtype=d).pin_memory() for k, (s, d) in res_shapes.items()}
@@ -338,9 +340,10 @@ def run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, flops_per_step, 
         dsa.dsa_indexer_topk(dev_in["q_idx"], dev_in["k_idx"], dev_in["w"], seq_start, K, topk_idx=dres["topk_idx"],
                              topk_len=dres["topk_len"])
         dsa.dsa_sparse_mla_fwd(dev_in["q"], dev_in["kv"], dres["topk_idx"], SCALE, topk_len=dres["topk_len"],
-                               out=dres["out"], lse=dres["lse"])
+                               out=dres["out"], lse=dres["lse"], out_lo=dres["out_lo"])
         dsa.dsa_sparse_mla_bwd(dev_in["q"], dev_in["kv"], dres["topk_idx"], SCALE, dres["out"], dres["lse"],
-                               dev_in["dout"], topk_len=dres["topk_len"], dq=dres["dq"], dkv_accum=dres["dkv"])
+                               dev_in["dout"], topk_len=dres["topk_len"], dq=dres["dq"], dkv_accum=dres["dkv"],
+                               out_lo=dres["out_lo"])
         for k in hres:
             hres[k].copy_(dres[k], non_blocking=True)
 

@@ -114,6 +114,10 @@ dsa_status_t dsa_indexer_topk(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, 
  *  q        device bf16 [T, H, Dqk], Dqk in {512, 576};  kv device bf16 [T_k, Dqk]
  *  topk_idx device int32 [T, K], any K >= 1;  topk_len device int32 [T] or NULL
  *  out      device bf16 [T, H, Dv] (out), Dv = 512;  lse device fp32 [T, H] (out)
+ *  out_lo   device bf16 [T, H, Dv] (out) or NULL: the rounding residual
+ *           bf16(O - out) of the fp32 result O.  Passing it on to the backward
+ *           makes D = <dout, O> use the unrounded O (library addition; the
+ *           pages' interface returns out only).
  *  workspace >= dsa_sparse_mla_fwd_workspace_size() bytes
  * Query chunking ([Chunk-PR] "Summary"): rows are independent, so a chunk is a
  * call on row-offset pointers of q/topk_idx/out/lse with the full kv.
@@ -121,8 +125,8 @@ dsa_status_t dsa_indexer_topk(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, 
 size_t dsa_sparse_mla_fwd_workspace_size(int32_t T, int32_t H);
 dsa_status_t dsa_sparse_mla_fwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
                                 const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
-                                int32_t Dv, int32_t K, float softmax_scale, dsa_bf16_t* out, float* lse,
-                                void* workspace, size_t workspace_bytes, dsa_stream_t stream);
+                                int32_t Dv, int32_t K, float softmax_scale, dsa_bf16_t* out, dsa_bf16_t* out_lo,
+                                float* lse, void* workspace, size_t workspace_bytes, dsa_stream_t stream);
 
 /*
  * dsa_sparse_mla_bwd -- analytic backward of dsa_sparse_mla_fwd.
@@ -136,6 +140,8 @@ dsa_status_t dsa_sparse_mla_fwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const
  *   dkv_accum[idx_j,0:Dv] += sum_h P_j dout[t,h,:]
  *  q, kv, topk_idx, topk_len, sizes, softmax_scale: as in the forward call
  *  out, lse       device: the forward's outputs for these rows
+ *  out_lo         device bf16 [T, H, Dv]: the forward's residual, or NULL (then D
+ *                 is computed from the rounded out)
  *  dout           device bf16 [T, H, Dv]
  *  dq             device bf16 [T, H, Dqk] (out)
  *  dkv_accum      device fp32 [T_k, Dqk]: zeroed first when accumulate == 0,
@@ -148,7 +154,8 @@ size_t dsa_sparse_mla_bwd_workspace_size(int32_t T, int32_t H);
 dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
                                 const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
                                 int32_t Dv, int32_t K, float softmax_scale, const dsa_bf16_t* out,
-                                const float* lse, const dsa_bf16_t* dout, dsa_bf16_t* dq, float* dkv_accum,
+                                const dsa_bf16_t* out_lo, const float* lse, const dsa_bf16_t* dout, dsa_bf16_t* dq,
+                                float* dkv_accum,
                                 int32_t accumulate, dsa_bf16_t* dkv_bf16, void* workspace,
                                 size_t workspace_bytes, dsa_stream_t stream);
 

@@ -91,11 +91,11 @@ def load_library(path: str | None = None):
         lib.dsa_indexer_topk.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]
         lib.dsa_sparse_mla_fwd_workspace_size.argtypes = [_I, _I]
         lib.dsa_sparse_mla_fwd_workspace_size.restype = _SZ
-        lib.dsa_sparse_mla_fwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]
+        lib.dsa_sparse_mla_fwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _SZ, _P]
         lib.dsa_sparse_mla_bwd_workspace_size.argtypes = [_I, _I]
         lib.dsa_sparse_mla_bwd_workspace_size.restype = _SZ
-        lib.dsa_sparse_mla_bwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I,
-                                           _P, _P, _SZ, _P]
+        lib.dsa_sparse_mla_bwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P,
+                                           _I, _P, _P, _SZ, _P]
         lib.dsa_read_device_status.argtypes = [_P, _P, _P]
         for name in ("dsa_packed_metadata", "dsa_indexer_topk", "dsa_sparse_mla_fwd", "dsa_sparse_mla_bwd",
                      "dsa_read_device_status"):
@@ -185,8 +185,10 @@ def dsa_indexer_topk(q_idx, k_idx, head_weights, seq_start, K: int, topk_idx=Non
 
 
 def dsa_sparse_mla_fwd(q, kv, topk_idx, softmax_scale: float, topk_len=None, out=None, lse=None,
-                       workspace=None, Dv: int = 512):
-    """Sparse MLA forward -> (out bf16 [T,H,Dv], lse fp32 [T,H]).  kv may be [T_k, Dqk] or [T_k, 1, Dqk]."""
+                       workspace=None, Dv: int = 512, out_lo=None):
+    """Sparse MLA forward -> (out bf16 [T,H,Dv], lse fp32 [T,H]), or (out, lse, out_lo) when
+    out_lo is a tensor or True (the bf16 rounding residual of out, for an exact backward D).
+    kv may be [T_k, Dqk] or [T_k, 1, Dqk]."""
     lib = load_library()
     _need(q, "q", torch.bfloat16, 3)
     dev = q.device
@@ -204,16 +206,22 @@ def dsa_sparse_mla_fwd(q, kv, topk_idx, softmax_scale: float, topk_len=None, out
         out = torch.empty(T, H, Dv, dtype=torch.bfloat16, device=dev)
     if lse is None:
         lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+    want_lo = out_lo is not None and out_lo is not False
+    if out_lo is True:
+        out_lo = torch.empty(T, H, Dv, dtype=torch.bfloat16, device=dev)
+    lo = out_lo if want_lo else None
     ws, wsb = _workspace("fwd", T, H, dev, workspace)
     _check(lib.dsa_sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(topk_idx), _ptr(topk_len), T, kv.shape[0], H, Dqk, Dv,
-                                  K, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(ws), wsb, _stream(dev)),
+                                  K, float(softmax_scale), _ptr(out), _ptr(lo), _ptr(lse), _ptr(ws), wsb,
+                                  _stream(dev)),
            "dsa_sparse_mla_fwd")
-    return out, lse
+    return (out, lse, lo) if want_lo else (out, lse)
 
 
 def dsa_sparse_mla_bwd(q, kv, topk_idx, softmax_scale: float, out, lse, dout, topk_len=None, dq=None,
-                       dkv_accum=None, accumulate: bool = False, dkv_bf16=None, workspace=None):
-    """Sparse MLA backward -> (dq bf16 [T,H,Dqk], dkv_accum fp32 [T_k,Dqk], dkv_bf16 or None)."""
+                       dkv_accum=None, accumulate: bool = False, dkv_bf16=None, workspace=None, out_lo=None):
+    """Sparse MLA backward -> (dq bf16 [T,H,Dqk], dkv_accum fp32 [T_k,Dqk], dkv_bf16 or None).
+    out_lo: the forward's residual (recommended; D then uses the unrounded output)."""
     lib = load_library()
     _need(q, "q", torch.bfloat16, 3)
     dev = q.device
@@ -228,6 +236,8 @@ def dsa_sparse_mla_bwd(q, kv, topk_idx, softmax_scale: float, out, lse, dout, to
     _need(dout, "dout", torch.bfloat16, 3, dev)
     if topk_len is not None:
         _need(topk_len, "topk_len", torch.int32, 1, dev)
+    if out_lo is not None:
+        _need(out_lo, "out_lo", torch.bfloat16, 3, dev)
     T, H, Dqk = q.shape
     Dv = out.shape[2]
     K = topk_idx.shape[1]
@@ -241,7 +251,8 @@ def dsa_sparse_mla_bwd(q, kv, topk_idx, softmax_scale: float, out, lse, dout, to
     _need(dkv_accum, "dkv_accum", torch.float32, 2, dev)
     ws, wsb = _workspace("bwd", T, H, dev, workspace)
     _check(lib.dsa_sparse_mla_bwd(_ptr(q), _ptr(kv), _ptr(topk_idx), _ptr(topk_len), T, Tk, H, Dqk, Dv, K,
-                                  float(softmax_scale), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dkv_accum),
+                                  float(softmax_scale), _ptr(out), _ptr(out_lo), _ptr(lse), _ptr(dout), _ptr(dq),
+                                  _ptr(dkv_accum),
                                   1 if accumulate else 0, _ptr(dkv_bf16), _ptr(ws), wsb, _stream(dev)),
            "dsa_sparse_mla_bwd")
     return dq, dkv_accum, dkv_bf16

@@ -1,4 +1,4 @@
-// dsa_bwd.cu -- absorbed sparse MLA backward on sm_103a (tcgen05 + TMEM + TMA).
+// dsa_bwd.cu -- absorbed sparse MLA backward on sm_103a (tcgen05 + TMEM).
 //
 // For one query token t and a group of 64 heads per CTA, with P_j =
 // exp(z_j - lse), D = <dO, O>, dP_j = <dO, kv[idx_j, :512]>, dS_j = P_j(dP_j - D):
@@ -13,21 +13,26 @@
 // DSA Kernels ...", "How DSA works".
 //
 // Design (sm_103a):
-//  * P is recomputed from the saved lse (no running max), D comes from a
-//    small preprocessing kernel.
-//  * All MMAs use M = 128 (keys of the tile, or channels) and N = 64 heads or
-//    64 channels:  S^T = KV Q^T and dP^T = V dO^T (keys on M), dQ^T += KV^T dS^T
-//    (channels on M), dKV = dS^T Q + P^T dO (keys on M, 64-channel groups).
-//  * Q [64 x Dqk] and dO [64 x 512] stay resident in shared memory for the
-//    token; the gathered tile streams twice through a 2-slot ring of
-//    128-channel pairs (once for S^T/dP^T, once for dQ^T).
-//  * P^T (bf16) goes to TMEM and is the A operand of the P^T dO product; dS^T
-//    (bf16, pre-multiplied by scale) goes to shared memory where it is both
-//    the B operand of dQ^T and the A operand of dS^T Q.
-//  * dKV of a tile is produced 64 channels at a time into two TMEM buffers
-//    (aliasing S^T / dP^T, which are dead by then) and flushed by the softmax
-//    warps with red.global.add.v4.f32 on the gathered rows of the fp32
-//    accumulator (L2 reductions).
+//  * P is recomputed from the saved lse (no running max).  D comes from a
+//    small kernel; when the forward's bf16 residual of O is given, D uses the
+//    unrounded O, so that sum_j dS_j = 0 holds to fp32 accuracy.
+//  * All MMAs have M = 128: S^T = KV Q^T and dP^T = V dO^T (keys on M, N = 64
+//    heads), dQ^T += KV^T dS^T (channels on M), dKV = dS^T Q + P^T dO (keys on
+//    M, 32-channel groups).
+//  * Q [64 x Dqk] and dO [64 x 512] stay in shared memory for the token; the
+//    gathered tile streams twice through a 2-slot ring of 128-channel pairs
+//    (once for S^T / dP^T, once for dQ^T).  The gather is 16-byte cp.async
+//    issued by the 256 worker threads.
+//  * dS (x scale) and P are split into bf16 hi + lo parts in TMEM and feed the
+//    dKV products as A operands, so dkv is accurate to about fp32 even for
+//    keys shared by many rows; dS hi also goes to shared memory as the B
+//    operand of dQ^T.
+//  * dKV of a tile is produced 32 channels at a time into two TMEM buffers and
+//    flushed by the workers with red.global.add.v4.f32 on the gathered rows of
+//    the fp32 accumulator (reductions in L2).
+//
+// Warp roles: warp 0 issues MMAs (one thread) and owns TMEM; warps 1..8 gather,
+// run the softmax backward, flush dKV and write dq.
 #include <cmath>
 
 #include "dsa_device.cuh"
@@ -36,15 +41,18 @@
 namespace dsa {
 namespace bwd {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 288;
+constexpr int kWorkers = 256;
 constexpr int kTile = 128;
 constexpr int kHeads = 64;
 constexpr int kDv = 512;
+constexpr int kGroup = 32;  // dKV channels per staging buffer
 
 template <int DQK>
 struct Smem {
   static constexpr int NCH = DQK / 64;         // channel chunks of kv / q
   static constexpr int NP = (NCH + 1) / 2;     // channel pairs (128 channels)
+  static constexpr int NG = DQK / kGroup;      // dKV groups
   static constexpr int Q_CHUNK = kHeads * 128; // 8 KiB
   static constexpr int KV_CHUNK = kTile * 128; // 16 KiB
   static constexpr int SLOT = 2 * KV_CHUNK;    // ring slot: one pair
@@ -55,34 +63,41 @@ struct Smem {
   static constexpr int OFF_MISC = OFF_DS + KV_CHUNK;
   static constexpr int MISC = 1024;
   static constexpr int TOTAL = OFF_MISC + MISC + 1024;
+  static_assert(TOTAL <= 232448, "shared memory budget");
+  static_assert(2 * SLOT + KV_CHUNK >= kHeads * DQK * 2, "dq staging fits ring + dS");
 };
 
 // misc layout
-constexpr int M_FULL = 0, M_EMPTY = 16, M_SDP = 32, M_DS = 40, M_KVF = 48, M_KVE = 64, M_DQ = 80, M_FIN = 88;
+constexpr int M_FULL = 0, M_EMPTY = 16, M_SDP = 32, M_DS = 40, M_STF = 48, M_STE = 64, M_DQ = 80, M_KVD = 88,
+              M_FIN = 96;
 constexpr int M_TMEM = 128, M_NEFF = 132, M_ABORT = 136;
+constexpr int M_LSE = 256, M_DL = 512;  // float [64] each
 
 // TMEM columns
-constexpr uint32_t C_S = 0, C_DP = 64, C_DQ = 128, C_P = 448;
+constexpr uint32_t C_DQ = 0, C_S = 320, C_DP = 384, C_STG = 448;
 
-// D[t,h] = <dO[t,h,:], O[t,h,:]> in fp32; one warp per (t, h).
-__global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
-                                 float* __restrict__ delta, long long rows) {
+// D[t,h] = <dO[t,h,:], O[t,h,:] (+ O_lo[t,h,:])> in fp32; one warp per (t, h).
+__global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ out_lo,
+                                 const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta, long long rows) {
   const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (w >= rows) return;
   const uint4* o = reinterpret_cast<const uint4*>(out + w * kDv);
+  const uint4* ol = out_lo ? reinterpret_cast<const uint4*>(out_lo + w * kDv) : nullptr;
   const uint4* d = reinterpret_cast<const uint4*>(dout + w * kDv);
   float acc = 0.f;
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     uint4 a = __ldg(o + lane + 32 * k), b = __ldg(d + lane + 32 * k);
+    uint4 c = ol ? __ldg(ol + lane + 32 * k) : make_uint4(0, 0, 0, 0);
     const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
     const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+    const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      float2 fa = __bfloat1622float2(a2[e]), fb = __bfloat1622float2(b2[e]);
-      acc = fmaf(fa.x, fb.x, acc);
-      acc = fmaf(fa.y, fb.y, acc);
+      float2 fa = __bfloat1622float2(a2[e]), fb = __bfloat1622float2(b2[e]), fc = __bfloat1622float2(c2[e]);
+      acc = fmaf(fa.x + fc.x, fb.x, acc);
+      acc = fmaf(fa.y + fc.y, fb.y, acc);
     }
   }
 #pragma unroll
@@ -101,9 +116,31 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16*
   }
 }
 
+// Gather channel pair p of the tile into a ring slot (see the forward's
+// gather: 16-byte units, zero-fill for invalid / beyond-prefix rows).
+template <int DQK>
+__device__ __forceinline__ void gather_pair(uint32_t slot, const __nv_bfloat16* __restrict__ kv, int p, int tid,
+                                            const int (&rix)[4], uint32_t bar) {
+  constexpr int NCH = DQK / 64;
+  const int uc = tid & 7;
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    const int c = 2 * p + cc;
+    if (c >= NCH) break;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int r = (tid >> 3) + 32 * e;
+      const bool ok = rix[e] >= 0;
+      const __nv_bfloat16* src = kv + (ok ? (size_t)rix[e] * DQK + c * 64 + uc * 8 : 0);
+      cp_async16(slot + cc * (kTile * 128) + sw128_off(r, uc), src, ok ? 16u : 0u);
+    }
+  }
+  cp_async_arrive(bar);
+}
+
 template <int DQK>
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_bwd_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16* __restrict__ q,
+    sparse_mla_bwd_kernel(const __nv_bfloat16* __restrict__ kv, const __nv_bfloat16* __restrict__ q,
                           const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ topk_len,
                           const float* __restrict__ lse, const float* __restrict__ delta,
                           const __nv_bfloat16* __restrict__ dout, int T, int Tk, int H, int K, float scale,
@@ -111,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = Smem<DQK>;
   constexpr int NCH = L::NCH;
   constexpr int NP = L::NP;
+  constexpr int NG = L::NG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(smem + L::OFF_Q);
@@ -120,8 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* misc = smem + L::OFF_MISC;
   const uint32_t bar_full = smem_u32(misc + M_FULL), bar_empty = smem_u32(misc + M_EMPTY);
   const uint32_t bar_sdp = smem_u32(misc + M_SDP), bar_ds = smem_u32(misc + M_DS);
-  const uint32_t bar_kvf = smem_u32(misc + M_KVF), bar_kve = smem_u32(misc + M_KVE);
-  const uint32_t bar_dq = smem_u32(misc + M_DQ), bar_fin = smem_u32(misc + M_FIN);
+  const uint32_t bar_stf = smem_u32(misc + M_STF), bar_ste = smem_u32(misc + M_STE);
+  const uint32_t bar_dq = smem_u32(misc + M_DQ), bar_kvd = smem_u32(misc + M_KVD), bar_fin = smem_u32(misc + M_FIN);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + M_TMEM);
   int* s_neff = reinterpret_cast<int*>(misc + M_NEFF);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + M_ABORT);
@@ -133,27 +171,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_full + 8 * s, kWorkers);
       mbar_init(bar_empty + 8 * s, 1);
-      mbar_init(bar_kvf + 8 * s, 1);
-      mbar_init(bar_kve + 8 * s, 8);
+      mbar_init(bar_stf + 8 * s, 1);
+      mbar_init(bar_ste + 8 * s, 8);
     }
     mbar_init(bar_sdp, 1);
     mbar_init(bar_ds, 8);
     mbar_init(bar_dq, 1);
+    mbar_init(bar_kvd, 1);
     mbar_init(bar_fin, 1);
     *s_neff = 0;
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 0) {
     tmem_alloc(smem_u32(s_tmem), 512);
     tmem_relinquish();
   }
   __syncthreads();
 
-  if (warp >= 2) {
-    const int tid = threadIdx.x - 64;
+  const int tid = threadIdx.x - 32;  // worker id 0..255
+  if (warp >= 1) {
     if (topk_len != nullptr) {
       if (tid == 0) {
         int n = topk_len[t];
@@ -161,27 +200,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       int last = 0;
-      for (int j = tid; j < K; j += 256)
+      for (int j = tid; j < K; j += kWorkers)
         if (idx_row[j] >= 0) last = j + 1;
       if (last) atomicMax(s_neff, last);
     }
     // Q [64 x DQK] and dO [64 x 512] -> 128B-swizzled chunks (rows = heads); heads >= H are zero.
-    for (int u = tid; u < kHeads * NCH * 8; u += 256) {
+    for (int u = tid; u < kHeads * NCH * 8; u += kWorkers) {
       const int hh = u / (NCH * 8), rem = u - hh * (NCH * 8), c = rem >> 3, uc = rem & 7;
       const int h = hg * kHeads + hh;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (h < H) v = __ldg(reinterpret_cast<const uint4*>(q + ((size_t)t * H + h) * DQK + c * 64 + uc * 8));
       st_shared_v4(sQ + c * L::Q_CHUNK + sw128_off(hh, uc), v.x, v.y, v.z, v.w);
     }
-    for (int u = tid; u < kHeads * 8 * 8; u += 256) {
+    for (int u = tid; u < kHeads * 8 * 8; u += kWorkers) {
       const int hh = u >> 6, rem = u & 63, c = rem >> 3, uc = rem & 7;
       const int h = hg * kHeads + hh;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (h < H) v = __ldg(reinterpret_cast<const uint4*>(dout + ((size_t)t * H + h) * kDv + c * 64 + uc * 8));
       st_shared_v4(sDO + c * L::Q_CHUNK + sw128_off(hh, uc), v.x, v.y, v.z, v.w);
     }
-    // Ring rows that are never gathered must stay finite: zero the ring once.
-    for (int u = tid; u < 2 * L::SLOT / 16; u += 256) st_shared_v4(sRing + u * 16, 0, 0, 0, 0);
     fence_proxy_async_smem();
   }
   __syncthreads();
@@ -190,63 +227,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *s_tmem;
 
   if (warp == 0) {
-    // ======================= producer =======================
-    int L_cnt = 0;  // pair loads issued so far
-    bool stop = false;
-    for (int i = 0; i < ntiles && !stop; ++i) {
-      const int base = i * kTile;
-      const int ngroups = min(32, (n_eff - base + 3) >> 2);
-      int r[4] = {0, 0, 0, 0};
-      if (lane < ngroups) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = base + 4 * lane + e;
-          int ix = -1;
-          if (j < n_eff) ix = __ldg(idx_row + j);
-          if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
-          r[e] = (ix >= 0 && ix < Tk) ? ix : 0;
-        }
-      }
-      for (int pass = 0; pass < 2 && !stop; ++pass) {
-        for (int p = 0; p < NP; ++p, ++L_cnt) {
-          const int slot = L_cnt & 1;
-          const uint32_t ph = ((L_cnt >> 1) & 1) ^ 1;
-          if (!mbar_wait(bar_empty + 8 * slot, ph, s_abort, err)) { stop = true; break; }
-          const int nch = (2 * p + 1 < NCH) ? 2 : 1;
-          if (lane == 0) mbar_expect_tx(bar_full + 8 * slot, (uint32_t)(ngroups * 4 * 128 * nch));
-          __syncwarp();
-          if (lane < ngroups) {
-            const uint32_t dst = sRing + slot * L::SLOT + (4 * lane) * 128;
-            for (int cc = 0; cc < nch; ++cc)
-              tma_gather4(dst + cc * L::KV_CHUNK, &kv_map, (2 * p + cc) * 64, r[0], r[1], r[2], r[3],
-                          bar_full + 8 * slot);
-          }
-        }
-      }
-    }
-    if (*s_abort && L_cnt > 0 && lane == 0) {
-      volatile int dummy = 0;
-      const int last = L_cnt - 1;
-      mbar_wait(bar_full + 8 * (last & 1), (last >> 1) & 1, &dummy, err);
-    }
-  } else if (warp == 1) {
     // ======================= MMA issuer =======================
     if (lane == 0) {
-      constexpr uint32_t kIdKK = idesc_bf16(128, 64, false, false);  // A K-major, B K-major
-      constexpr uint32_t kIdMM = idesc_bf16(128, 64, true, true);    // A MN-major, B MN-major
-      constexpr uint32_t kIdKM = idesc_bf16(128, 64, false, true);   // A K-major (smem or tmem), B MN-major
+      constexpr uint32_t kIdKK = idesc_bf16(128, 64, false, false);      // S^T, dP^T
+      constexpr uint32_t kIdMM = idesc_bf16(128, 64, true, true);        // dQ^T
+      constexpr uint32_t kIdKM = idesc_bf16(128, kGroup, false, true);   // dKV: A (TMEM) x B MN-major
       int L_cnt = 0, G = 0;
       bool stop = false;
       for (int i = 0; i < ntiles && !stop; ++i) {
-        // S^T / dP^T alias the dKV staging buffers: both must be flushed.
-        if (i > 0) {
-          if (!mbar_wait(bar_kve + 8 * (G & 1), (((G >> 1) & 1) ^ 1), s_abort, err)) break;
-          if (!mbar_wait(bar_kve + 8 * ((G + 1) & 1), ((((G + 1) >> 1) & 1) ^ 1), s_abort, err)) break;
+        if (i > 0) {  // the previous tile's dKV reads its A operands from the S^T / dP^T columns
+          if (!mbar_wait(bar_kvd, (i - 1) & 1, s_abort, err)) break;
         }
         // ---- pass A: S^T = KV Q^T, dP^T = V dO^T ----
         for (int p = 0; p < NP; ++p, ++L_cnt) {
           const int slot = L_cnt & 1;
           if (!mbar_wait(bar_full + 8 * slot, (L_cnt >> 1) & 1, s_abort, err)) { stop = true; break; }
+          fence_proxy_async_smem();
           tc_fence_after();
           for (int cc = 0; cc < 2; ++cc) {
             const int c = 2 * p + cc;
@@ -269,10 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar_sdp);
         if (!mbar_wait(bar_ds, i & 1, s_abort, err)) break;
         tc_fence_after();
-        // ---- pass B: dQ^T[pair p] += KV^T dS'^T ----
+        // ---- pass B: dQ^T[pair p] += KV^T dS^T ----
         for (int p = 0; p < NP; ++p, ++L_cnt) {
           const int slot = L_cnt & 1;
           if (!mbar_wait(bar_full + 8 * slot, (L_cnt >> 1) & 1, s_abort, err)) { stop = true; break; }
+          fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t a0 = sRing + slot * L::SLOT;
 #pragma unroll
@@ -282,23 +279,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(bar_empty + 8 * slot);
         }
         if (stop) break;
-        // ---- dKV = dS'^T Q (+ P^T dO), 64 channels at a time ----
-        for (int g = 0; g < NCH; ++g, ++G) {
+        // ---- dKV = (dS_hi + dS_lo)^T Q + (P_hi + P_lo)^T dO, 32 channels at a time ----
+        for (int g = 0; g < NG; ++g, ++G) {
           const int b = G & 1;
-          if (!mbar_wait(bar_kve + 8 * b, ((G >> 1) & 1) ^ 1, s_abort, err)) { stop = true; break; }
+          if (!mbar_wait(bar_ste + 8 * b, ((G >> 1) & 1) ^ 1, s_abort, err)) { stop = true; break; }
           tc_fence_after();
-          const uint32_t d = tmem + 64 * b;
+          const uint32_t d = tmem + C_STG + kGroup * b;
+          const uint32_t qb = sQ + (g >> 1) * L::Q_CHUNK + (g & 1) * 64;
+          const uint32_t ob = sDO + (g >> 1) * L::Q_CHUNK + (g & 1) * 64;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(d, sdesc_sw128(sDS + k * 32, 16, 1024), sdesc_sw128(sQ + g * L::Q_CHUNK + k * 2048, 16, 1024),
-                   kIdKM, k > 0);
-          if (g < 8) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ts(d, tmem + C_P + 8 * k, sdesc_sw128(sDO + g * L::Q_CHUNK + k * 2048, 16, 1024), kIdKM, 1u);
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t acol = (k >> 1) * 32 + (k & 1) * 8;
+            const uint64_t bq = sdesc_sw128(qb + k * 2048, 16, 1024);
+            mma_ts(d, tmem + C_S + acol, bq, kIdKM, k > 0);        // dS hi
+            mma_ts(d, tmem + C_S + 16 + acol, bq, kIdKM, 1u);      // dS lo
+            if (g * kGroup < kDv) {
+              const uint64_t bo = sdesc_sw128(ob + k * 2048, 16, 1024);
+              mma_ts(d, tmem + C_DP + acol, bo, kIdKM, 1u);        // P hi
+              mma_ts(d, tmem + C_DP + 16 + acol, bo, kIdKM, 1u);   // P lo
+            }
           }
-          mma_commit(bar_kvf + 8 * b);
+          mma_commit(bar_stf + 8 * b);
         }
+        mma_commit(bar_kvd);
       }
       mma_commit(bar_dq);
       mma_commit(bar_fin);
@@ -307,35 +310,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ======================= softmax-backward, dKV flush, dQ epilogue =======================
-    const int sw = warp - 2;
+    // ======================= workers =======================
+    const int wk = warp - 1;
     const int qd = warp & 3;
-    const int ch = sw >> 2;           // heads ch*32 .. ch*32+31 / channel half of a 64-channel group
+    const int ch = wk >> 2;           // heads ch*32 .. ch*32+31 / column half of a dKV group
     const int r = qd * 32 + lane;     // key row of the tile
     const int bar_id = 1 + ch;
     const float sl2e = scale * 1.4426950408889634f;
-    float lse2[32], dl[32];
-#pragma unroll
-    for (int h = 0; h < 32; ++h) {
-      const int hh = hg * kHeads + ch * 32 + h;
-      lse2[h] = (hh < H) ? lse[(size_t)t * H + hh] * 1.4426950408889634f : INFINITY;  // padded heads: P = 0
-      dl[h] = (hh < H) ? delta[(size_t)t * H + hh] : 0.f;
+    // per-head lse (log2 units) and D, shared by every key row: kept in shared memory
+    float* s_lse2 = reinterpret_cast<float*>(misc + M_LSE);
+    float* s_dl = reinterpret_cast<float*>(misc + M_DL);
+    if (tid < kHeads) {
+      const int hh = hg * kHeads + tid;
+      s_lse2[tid] = (hh < H) ? lse[(size_t)t * H + hh] * 1.4426950408889634f : INFINITY;  // padded heads: P = 0
+      s_dl[tid] = (hh < H) ? delta[(size_t)t * H + hh] : 0.f;
     }
-    int G = 0;
+    named_bar(3, kWorkers);
+    const float* lse2 = s_lse2 + ch * 32;
+    const float* dl = s_dl + ch * 32;
+    auto load_rows = [&](int i, int (&rix)[4]) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = i * kTile + (tid >> 3) + 32 * e;
+        int v = -1;
+        if (j < n_eff) {
+          const int ix = __ldg(idx_row + j);
+          v = (ix >= 0 && ix < Tk) ? ix : -1;
+          if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
+        }
+        rix[e] = v;
+      }
+    };
+    int L_cnt = 0, G = 0;
     bool aborted = false;
+    auto gather_pass = [&](const int (&rix)[4]) {
+      for (int p = 0; p < NP; ++p, ++L_cnt) {
+        const int slot = L_cnt & 1;
+        if (!mbar_wait(bar_empty + 8 * slot, ((L_cnt >> 1) & 1) ^ 1, s_abort, err)) return false;
+        gather_pair<DQK>(sRing + slot * L::SLOT, kv, p, tid, rix, bar_full + 8 * slot);
+      }
+      return true;
+    };
     for (int i = 0; i < ntiles && !aborted; ++i) {
+      int rix[4];
+      load_rows(i, rix);
+      bool ok = gather_pass(rix);                       // pass A data
+      if (named_bar_or(bar_id, 128, !ok)) { aborted = true; break; }
       const bool got = mbar_wait(bar_sdp, i & 1, s_abort, err);
       if (named_bar_or(bar_id, 128, !got)) { aborted = true; break; }
       tc_fence_after();
       uint32_t sv[32], dv[32];
-      tmem_ld32(tmem_addr(tmem + C_S, qd * 32, ch * 32), sv);
-      tmem_ld32(tmem_addr(tmem + C_DP, qd * 32, ch * 32), dv);
+      tmem_ld32(tmem_addr(tmem + C_S + ch * 32, qd * 32, 0), sv);
+      tmem_ld32(tmem_addr(tmem + C_DP + ch * 32, qd * 32, 0), dv);
       tmem_ld_wait();
       const int j = i * kTile + r;
       int ix = -1;
       if (j < n_eff) ix = __ldg(idx_row + j);
       const bool valid = ix >= 0 && ix < Tk;
-      uint32_t pk[16], dk[16];
+      uint32_t ph[16], pl[16], sh[16], sl[16], dsb[16];
 #pragma unroll
       for (int h = 0; h < 32; h += 2) {
         float p0 = 0.f, p1 = 0.f, s0 = 0.f, s1 = 0.f;
@@ -345,57 +377,69 @@ __global__ void __launch_bounds__(kThreads, 1)
           s0 = scale * p0 * (__uint_as_float(dv[h]) - dl[h]);
           s1 = scale * p1 * (__uint_as_float(dv[h + 1]) - dl[h + 1]);
         }
-        pk[h >> 1] = pack_bf16x2(p0, p1);
-        dk[h >> 1] = pack_bf16x2(s0, s1);
+        const __nv_bfloat162 phi = __floats2bfloat162_rn(p0, p1);
+        const __nv_bfloat162 shi = __floats2bfloat162_rn(s0, s1);
+        const float2 phf = __bfloat1622float2(phi), shf = __bfloat1622float2(shi);
+        ph[h >> 1] = *reinterpret_cast<const uint32_t*>(&phi);
+        sh[h >> 1] = *reinterpret_cast<const uint32_t*>(&shi);
+        pl[h >> 1] = pack_bf16x2(p0 - phf.x, p1 - phf.y);
+        sl[h >> 1] = pack_bf16x2(s0 - shf.x, s1 - shf.y);
+        dsb[h >> 1] = sh[h >> 1];
       }
 #pragma unroll
       for (int uu = 0; uu < 4; ++uu)
-        st_shared_v4(sDS + sw128_off(r, ch * 4 + uu), dk[4 * uu], dk[4 * uu + 1], dk[4 * uu + 2], dk[4 * uu + 3]);
-      tmem_st16(tmem_addr(tmem + C_P, qd * 32, ch * 16), pk);
+        st_shared_v4(sDS + sw128_off(r, ch * 4 + uu), dsb[4 * uu], dsb[4 * uu + 1], dsb[4 * uu + 2], dsb[4 * uu + 3]);
+      // A operands of the dKV products, over this thread's own S^T / dP^T columns
+      tmem_st16(tmem_addr(tmem + C_S + ch * 32, qd * 32, 0), sh);
+      tmem_st16(tmem_addr(tmem + C_S + ch * 32 + 16, qd * 32, 0), sl);
+      tmem_st16(tmem_addr(tmem + C_DP + ch * 32, qd * 32, 0), ph);
+      tmem_st16(tmem_addr(tmem + C_DP + ch * 32 + 16, qd * 32, 0), pl);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
+      ok = gather_pass(rix);                            // pass B data
+      if (named_bar_or(bar_id, 128, !ok)) { aborted = true; break; }
       // ---- flush dKV groups of this tile ----
-      for (int g = 0; g < NCH; ++g, ++G) {
+      for (int g = 0; g < NG; ++g, ++G) {
         const int b = G & 1;
-        const bool ok = mbar_wait(bar_kvf + 8 * b, (G >> 1) & 1, s_abort, err);
-        if (!ok) { aborted = true; }
+        const bool okw = mbar_wait(bar_stf + 8 * b, (G >> 1) & 1, s_abort, err);
+        if (!okw) aborted = true;
         tc_fence_after();
-        if (ok) {
-          uint32_t v[32];
-          tmem_ld32(tmem_addr(tmem + 64 * b, qd * 32, ch * 32), v);
+        if (okw) {
+          uint32_t v[16];
+          tmem_ld16(tmem_addr(tmem + C_STG + kGroup * b + ch * 16, qd * 32, 0), v);
           tmem_ld_wait();
           if (valid) {
-            float* dst = dkv + (size_t)ix * DQK + g * 64 + ch * 32;
+            float* dst = dkv + (size_t)ix * DQK + g * kGroup + ch * 16;
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
+            for (int e = 0; e < 4; ++e)
               red_add_v4(dst + 4 * e, __uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
                          __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_kve + 8 * b);
-        if (!ok) break;
+        if (lane == 0) mbar_arrive(bar_ste + 8 * b);
+        if (!okw) break;
       }
       aborted = named_bar_or(bar_id, 128, aborted);
     }
-    // ---- dQ epilogue ----
+    // ---- dq epilogue: dQ^T (lanes = channels) -> staged [64 heads][DQK] bf16 -> coalesced stores ----
     bool have = false;
     if (!aborted && ntiles > 0) {
       const bool got = mbar_wait(bar_dq, 0, s_abort, err);
       have = !named_bar_or(bar_id, 128, !got);
       tc_fence_after();
     }
-    const int hbase = hg * kHeads + ch * 32;
-    const int hcount = min(32, H - hbase);
+    named_bar(3, kWorkers);  // both halves are done with the ring before it becomes the staging area
+    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + L::OFF_RING);
 #pragma unroll 1
     for (int p = 0; p < NP; ++p) {
       uint32_t v[32];
       if (have) {
-        tmem_ld32(tmem_addr(tmem + C_DQ + p * 64, qd * 32, ch * 32), v);
+        tmem_ld32(tmem_addr(tmem + C_DQ + p * 64 + ch * 32, qd * 32, 0), v);
         tmem_ld_wait();
       } else {
 #pragma unroll
@@ -403,24 +447,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int c = p * 128 + qd * 32 + lane;
       if (c < DQK) {
-        __nv_bfloat16* dp = dq + ((size_t)t * H + hbase) * DQK + c;
 #pragma unroll
-        for (int h = 0; h < 32; ++h)
-          if (h < hcount) dp[(size_t)h * DQK] = __float2bfloat16_rn(__uint_as_float(v[h]));
+        for (int h = 0; h < 32; ++h) stage[(ch * 32 + h) * DQK + c] = __float2bfloat16_rn(__uint_as_float(v[h]));
       }
     }
+    named_bar(3, kWorkers);
+    const int hcount = min(kHeads, H - hg * kHeads);
+    uint4* dst = reinterpret_cast<uint4*>(dq + ((size_t)t * H + hg * kHeads) * DQK);
+    for (int u = tid; u < hcount * (DQK / 8); u += kWorkers) dst[u] = reinterpret_cast<const uint4*>(stage)[u];
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
 template <int DQK>
-dsa_status_t launch(const CUtensorMap& map, const void* q, const int32_t* idx, const int32_t* len, const float* lse,
+dsa_status_t launch(const void* kv, const void* q, const int32_t* idx, const int32_t* len, const float* lse,
                     const float* delta, const void* dout, int T, int Tk, int H, int K, float scale, void* dq,
                     float* dkv, int* err, cudaStream_t s) {
   using L = Smem<DQK>;
@@ -434,7 +480,7 @@ dsa_status_t launch(const CUtensorMap& map, const void* q, const int32_t* idx, c
   }
   dim3 grid(T, (H + kHeads - 1) / kHeads);
   sparse_mla_bwd_kernel<DQK><<<grid, kThreads, L::TOTAL, s>>>(
-      map, reinterpret_cast<const __nv_bfloat16*>(q), idx, len, lse, delta,
+      reinterpret_cast<const __nv_bfloat16*>(kv), reinterpret_cast<const __nv_bfloat16*>(q), idx, len, lse, delta,
       reinterpret_cast<const __nv_bfloat16*>(dout), T, Tk, H, K, scale, reinterpret_cast<__nv_bfloat16*>(dq), dkv,
       err);
   return cuda_check(cudaGetLastError(), "launching sparse_mla_bwd_kernel");
@@ -453,8 +499,8 @@ extern "C" size_t dsa_sparse_mla_bwd_workspace_size(int32_t T, int32_t H) {
 extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
                                            const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
                                            int32_t Dv, int32_t K, float softmax_scale, const dsa_bf16_t* out,
-                                           const float* lse, const dsa_bf16_t* dout, dsa_bf16_t* dq,
-                                           float* dkv_accum, int32_t accumulate, dsa_bf16_t* dkv_bf16,
+                                           const dsa_bf16_t* out_lo, const float* lse, const dsa_bf16_t* dout,
+                                           dsa_bf16_t* dq, float* dkv_accum, int32_t accumulate, dsa_bf16_t* dkv_bf16,
                                            void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
   const char* who = "dsa_sparse_mla_bwd";
   if (T < 0 || T_k < 1 || H < 1 || K < 1)
@@ -468,8 +514,11 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t
   if (!kv || !dkv_accum) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: kv / dkv_accum is NULL", who);
   if (T > 0 && (!q || !topk_idx || !out || !lse || !dout || !dq))
     return fail(DSA_ERR_INVALID_ARGUMENT, "%s: null tensor pointer", who);
-  if (!aligned16(kv) || !aligned16(dkv_accum) || (T > 0 && (!aligned16(q) || !aligned16(out) || !aligned16(dout))))
-    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: q, kv, out, dout and dkv_accum must be 16-byte aligned", who);
+  if (!aligned16(kv) || !aligned16(dkv_accum) ||
+      (T > 0 && (!aligned16(q) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) ||
+                 (out_lo && !aligned16(out_lo)))))
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: q, kv, out, out_lo, dout, dq and dkv_accum must be 16-byte aligned",
+                who);
   if (dkv_bf16 && (reinterpret_cast<uintptr_t>(dkv_bf16) & 7u))
     return fail(DSA_ERR_INVALID_ARGUMENT, "%s: dkv_bf16 must be 8-byte aligned", who);
   dsa_status_t st = check_workspace(workspace, workspace_bytes, dsa_sparse_mla_bwd_workspace_size(T, H), who);
@@ -484,16 +533,14 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t
   float* delta = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + kErrorWordBytes);
   if (T > 0) {
     const long long rows = (long long)T * H;
-    bwd::bwd_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(out),
-                                                                     reinterpret_cast<const __nv_bfloat16*>(dout),
-                                                                     delta, rows);
+    bwd::bwd_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(out), reinterpret_cast<const __nv_bfloat16*>(out_lo),
+        reinterpret_cast<const __nv_bfloat16*>(dout), delta, rows);
     if ((st = cuda_check(cudaGetLastError(), "launching bwd_delta_kernel"))) return st;
-    CUtensorMap map;
-    if ((st = make_map_2d_bf16(&map, kv, (uint64_t)T_k, (uint64_t)Dqk, (uint64_t)Dqk, 64, 1)) != DSA_OK) return st;
-    st = (Dqk == 576) ? bwd::launch<576>(map, q, topk_idx, topk_len, lse, delta, dout, T, T_k, H, K, softmax_scale,
-                                         dq, dkv_accum, err, s)
-                      : bwd::launch<512>(map, q, topk_idx, topk_len, lse, delta, dout, T, T_k, H, K, softmax_scale,
-                                         dq, dkv_accum, err, s);
+    st = (Dqk == 576) ? bwd::launch<576>(kv, q, topk_idx, topk_len, lse, delta, dout, T, T_k, H, K, softmax_scale, dq,
+                                         dkv_accum, err, s)
+                      : bwd::launch<512>(kv, q, topk_idx, topk_len, lse, delta, dout, T, T_k, H, K, softmax_scale, dq,
+                                         dkv_accum, err, s);
     if (st != DSA_OK) return st;
   }
   if (dkv_bf16) {

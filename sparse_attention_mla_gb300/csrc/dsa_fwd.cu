@@ -1,4 +1,4 @@
-// dsa_fwd.cu -- absorbed sparse MLA forward on sm_103a (tcgen05 + TMEM + TMA).
+// dsa_fwd.cu -- absorbed sparse MLA forward on sm_103a (tcgen05 + TMEM).
 //
 // Computes, for one query token t and one group of 64 heads per CTA,
 //   z_j = scale <q[t,h,:], kv[idx_j,:]>,  lse = ln sum_j e^{z_j},
@@ -14,24 +14,33 @@
 //
 // Design (sm_103a):
 //  * The selected kv rows of a 128-slot tile are gathered ONCE into shared
-//    memory with TMA tile::gather4 (4 rows x 64 channels per instruction,
-//    128-byte swizzle) and used by all 64 heads of the CTA.
-//  * Scores are computed transposed, S^T[key, head] = KV_tile . Q^T, so the
+//    memory (128-byte swizzled, 9 chunks of 64 channels) and used by all 64
+//    heads of the CTA.  The gather is 16-byte cp.async issued by the 256
+//    softmax threads (many requests in flight; a per-chunk mbarrier counts the
+//    landings), so the tensor core starts on chunk 0 while later chunks land.
+//  * Scores are computed transposed, S^T[key, head] = KV_tile . Q^T: the
 //    tensor-core M axis is the 128 keys of the tile and N = 64 heads
-//    (M = 128 is the full-rate tcgen05 shape; the 64 heads are the shared
+//    (M = 128 is the full-rate tcgen05 shape; the heads are the shared
 //    operand).  Output is accumulated transposed too, O^T[ch, head] +=
 //    V^T . P^T, as four M = 128 channel tiles.  TMEM holds S^T (64 columns)
-//    and O^T (256 columns); the 576-wide O of 64 heads would not fit TMEM in
-//    the heads-on-M orientation.
+//    and O^T (256 columns); 64 x 512 fp32 O in the heads-on-M orientation
+//    would need M = 64 tiles that leave half of each TMEM lane quadrant idle.
+//  * Each channel tile of the P.V product signals its own barrier, so the
+//    gather of the next tile's chunks starts while the rest of P.V runs.
 //  * Online softmax with the running max per head; a rescale of O^T happens
 //    only when some score exceeds the running max by more than 2^8 (lazy
 //    rescale), otherwise P uses the stale max.
-//  * P^T (bf16) is written into the shared-memory slot of the tile's RoPE
-//    channels (no longer needed once S^T is done), which keeps the whole
-//    working set (Q 72 KiB + tile 144 KiB) inside one SM's shared memory.
+//  * P^T is written into the shared-memory slot of the tile's RoPE channels
+//    (no longer needed once S^T is done), which keeps the working set
+//    (Q 72 KiB + tile 144 KiB) inside one SM's shared memory.  P is split into
+//    bf16 hi + lo parts that go through the same slot one after the other
+//    (P_hi . V, then P_lo . V), so O carries P to about fp32 accuracy and the
+//    backward's D = <dO, O> is consistent with the exact softmax.
+//  * The epilogue stages O (and, on request, the bf16 residual O - bf16(O))
+//    through shared memory for coalesced 16-byte stores.
 //
-// Warp roles: warp 0 gathers (TMA), warp 1 issues MMAs (one thread) and owns
-// TMEM, warps 2..9 run the softmax and the epilogue.
+// Warp roles: warp 0 issues MMAs (one thread) and owns TMEM; warps 1..8 run
+// the gather, the softmax and the epilogue.
 #include <cmath>
 
 #include "dsa_device.cuh"
@@ -40,7 +49,8 @@
 namespace dsa {
 namespace fwd {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 288;
+constexpr int kWorkers = 256;
 constexpr int kTile = 128;   // top-k slots per tile (MMA M)
 constexpr int kHeads = 64;   // heads per CTA (MMA N)
 constexpr int kDv = 512;
@@ -58,14 +68,17 @@ struct Smem {
   static constexpr int OFF_MISC = (DQK == 576) ? OFF_KV + NCH * KV_CHUNK : OFF_P + KV_CHUNK;
   static constexpr int MISC = 2048;
   static constexpr int TOTAL = OFF_MISC + MISC + 1024;  // + alignment slack
+  static_assert(TOTAL <= 232448, "shared memory budget");
 };
 
 // misc layout (bytes)
-constexpr int M_BAR_KV = 0, M_BAR_S = 8, M_BAR_P = 16, M_BAR_O = 24, M_BAR_FIN = 32;
-constexpr int M_TMEM = 64, M_NEFF = 68, M_ABORT = 72;
-constexpr int M_RED = 128;         // float [4][64]
-constexpr int M_STAT = 128 + 1024; // float [64]: running max per head
-constexpr int M_LSUM = M_STAT + 256;  // float [64]: softmax denominator per head
+constexpr int M_BAR_KV = 0;    // [9] chunk landed
+constexpr int M_BAR_PV = 80;   // [4] P.V channel tile done
+constexpr int M_BAR_S = 112, M_BAR_P = 120, M_BAR_FIN = 128, M_BAR_PLO = 136, M_BAR_PVH = 144;
+constexpr int M_TMEM = 192, M_NEFF = 196, M_ABORT = 200;
+constexpr int M_RED = 256;             // float [4][64]
+constexpr int M_STAT = M_RED + 1024;   // float [64]: running max per head
+constexpr int M_LSUM = M_STAT + 256;   // float [64]: softmax denominator per head
 
 // Transposing butterfly: v[0..31] per lane (lane = key, index = head) ->
 // lane l returns the reduction over the warp's 32 keys of head l.
@@ -85,12 +98,30 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
   return v[0];
 }
 
+// Gather channels [64c, 64c+64) of the tile's rows into chunk slot c.  Thread
+// `tid` copies 16-byte unit (tid & 7) of rows r_e = (tid >> 3) + 32 e.  Rows
+// whose slot is invalid or beyond the valid prefix are zero-filled (no global
+// read), so every row of the tile is finite and P = 0 times it stays 0.
+template <int DQK>
+__device__ __forceinline__ void gather_chunk(uint32_t dst_chunk, const __nv_bfloat16* __restrict__ kv, int c, int tid,
+                                             const int (&rix)[4], uint32_t bar) {
+  const int uc = tid & 7;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int r = (tid >> 3) + 32 * e;
+    const bool ok = rix[e] >= 0;
+    const __nv_bfloat16* src = kv + (ok ? (size_t)rix[e] * DQK + c * 64 + uc * 8 : 0);
+    cp_async16(dst_chunk + sw128_off(r, uc), src, ok ? 16u : 0u);
+  }
+  cp_async_arrive(bar);
+}
+
 template <int DQK>
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_fwd_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16* __restrict__ q,
+    sparse_mla_fwd_kernel(const __nv_bfloat16* __restrict__ kv, const __nv_bfloat16* __restrict__ q,
                           const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ topk_len, int T, int Tk,
-                          int H, int K, float sl2e, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
-                          int* __restrict__ err) {
+                          int H, int K, float sl2e, __nv_bfloat16* __restrict__ out,
+                          __nv_bfloat16* __restrict__ out_lo, float* __restrict__ lse, int* __restrict__ err) {
   using L = Smem<DQK>;
   constexpr int NCH = L::NCH;
   extern __shared__ uint8_t smem_raw[];
@@ -99,9 +130,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sKV = smem_u32(smem + L::OFF_KV);
   const uint32_t sP = smem_u32(smem + L::OFF_P);
   uint8_t* misc = smem + L::OFF_MISC;
-  const uint32_t bar_kv = smem_u32(misc + M_BAR_KV), bar_s = smem_u32(misc + M_BAR_S);
-  const uint32_t bar_p = smem_u32(misc + M_BAR_P), bar_o = smem_u32(misc + M_BAR_O);
+  const uint32_t bar_kv = smem_u32(misc + M_BAR_KV), bar_pv = smem_u32(misc + M_BAR_PV);
+  const uint32_t bar_s = smem_u32(misc + M_BAR_S), bar_p = smem_u32(misc + M_BAR_P);
   const uint32_t bar_fin = smem_u32(misc + M_BAR_FIN);
+  const uint32_t bar_plo = smem_u32(misc + M_BAR_PLO), bar_pvh = smem_u32(misc + M_BAR_PVH);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + M_TMEM);
   int* s_neff = reinterpret_cast<int*>(misc + M_NEFF);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + M_ABORT);
@@ -115,24 +147,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t* idx_row = topk_idx + (size_t)t * K;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_kv, 1);
+    for (int c = 0; c < NCH; ++c) mbar_init(bar_kv + 8 * c, kWorkers);
+    for (int m = 0; m < 4; ++m) mbar_init(bar_pv + 8 * m, 1);
     mbar_init(bar_s, 1);
     mbar_init(bar_p, 8);
-    mbar_init(bar_o, 1);
+    mbar_init(bar_plo, 8);
+    mbar_init(bar_pvh, 1);
     mbar_init(bar_fin, 1);
     *s_neff = 0;
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 0) {
     tmem_alloc(smem_u32(s_tmem), 512);
     tmem_relinquish();
   }
   __syncthreads();
 
-  // ---- valid prefix length and Q staging (softmax warps) ----
-  if (warp >= 2) {
-    const int tid = threadIdx.x - 64;  // 0..255
+  const int tid = threadIdx.x - 32;  // worker id 0..255 (negative for warp 0)
+  // ---- valid prefix length and Q staging (workers) ----
+  if (warp >= 1) {
     if (topk_len != nullptr) {
       if (tid == 0) {
         int n = topk_len[t];
@@ -140,14 +174,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       int last = 0;
-      for (int j = tid; j < K; j += 256)
+      for (int j = tid; j < K; j += kWorkers)
         if (idx_row[j] >= 0) last = j + 1;
       if (last) atomicMax(s_neff, last);
     }
     if (tid < kHeads) s_stat[tid] = -INFINITY;  // running max per head (log2 units)
     // Q [64 heads, DQK] -> NCH chunks of [64 rows x 128 B], 128B swizzle; heads >= H are zero.
     constexpr int UNITS = kHeads * NCH * 8;
-    for (int u = tid; u < UNITS; u += 256) {
+    for (int u = tid; u < UNITS; u += kWorkers) {
       const int hh = u / (NCH * 8);
       const int rem = u - hh * (NCH * 8);
       const int c = rem >> 3, uc = rem & 7;
@@ -161,64 +195,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   const int n_eff = *s_neff;
   const int ntiles = (n_eff + kTile - 1) / kTile;
-  // A single partial tile leaves rows it never gathers: make them finite (zero)
-  // so that P = 0 times V stays 0.  Later tiles only hold stale gathered rows.
-  if (ntiles == 1 && warp >= 2) {
-    const int tid = threadIdx.x - 64;
-    const int r0 = ((n_eff + 3) >> 2) << 2;
-    const int units = (kTile - r0) * 8;
-    for (int c = 0; c < NCH; ++c)
-      for (int u = tid; u < units; u += 256)
-        st_shared_v4(sKV + c * L::KV_CHUNK + (r0 + (u >> 3)) * 128 + ((u & 7) << 4), 0, 0, 0, 0);
-    fence_proxy_async_smem();
-  }
-  __syncthreads();
   const uint32_t tmem = *s_tmem;
   const uint32_t tS = tmem;        // S^T: 128 lanes x 64 columns
   const uint32_t tO = tmem + 64;   // O^T: 4 channel tiles x 64 columns
 
   if (warp == 0) {
-    // ======================= producer: TMA gather =======================
-    int issued = 0;
-    for (int i = 0; i < ntiles; ++i) {
-      if (i > 0 && !mbar_wait(bar_o, (i - 1) & 1, s_abort, err)) break;
-      const int base = i * kTile;
-      const int rem = n_eff - base;
-      const int ngroups = min(32, (rem + 3) >> 2);
-      if (lane == 0) mbar_expect_tx(bar_kv, (uint32_t)(ngroups * 4 * DQK * 2));
-      __syncwarp();
-      if (lane < ngroups) {
-        int r[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = base + 4 * lane + e;
-          int ix = -1;
-          if (j < n_eff) ix = __ldg(idx_row + j);
-          if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
-          r[e] = (ix >= 0 && ix < Tk) ? ix : 0;
-        }
-        const uint32_t dst = sKV + (4 * lane) * 128;
-#pragma unroll 1
-        for (int c = 0; c < NCH; ++c)
-          tma_gather4(dst + c * L::KV_CHUNK, &kv_map, c * 64, r[0], r[1], r[2], r[3], bar_kv);
-      }
-      issued = i + 1;
-    }
-    // On abort, wait (bounded) for our own copies still in flight.
-    if (*s_abort && issued > 0 && lane == 0) {
-      volatile int dummy = 0;
-      mbar_wait(bar_kv, (issued - 1) & 1, &dummy, err);
-    }
-  } else if (warp == 1) {
     // ======================= MMA issuer =======================
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, kHeads, false, false);  // A = KV (K-major), B = Q (K-major)
       constexpr uint32_t kIdPV = idesc_bf16(128, kHeads, true, true);   // A = V^T (MN-major), B = P^T (MN-major)
       for (int i = 0; i < ntiles; ++i) {
-        if (!mbar_wait(bar_kv, i & 1, s_abort, err)) break;
-        tc_fence_after();
+        bool stop = false;
 #pragma unroll 1
         for (int c = 0; c < NCH; ++c) {
+          if (!mbar_wait(bar_kv + 8 * c, i & 1, s_abort, err)) { stop = true; break; }
+          fence_proxy_async_smem();  // cp.async landings -> visible to the tensor core
+          tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t a = sdesc_sw128(sKV + c * L::KV_CHUNK + k * 32, 16, 1024);
@@ -226,7 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(tS, a, b, kIdS, (c | k) != 0);
           }
         }
+        if (stop) break;
         mma_commit(bar_s);
+        // O^T += V^T P_hi^T, then (P_lo in the same slot) O^T += V^T P_lo^T
         if (!mbar_wait(bar_p, i & 1, s_abort, err)) break;
         tc_fence_after();
 #pragma unroll 1
@@ -238,7 +232,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(tO + m * kHeads, a, b, kIdPV, (i > 0 || k > 0) ? 1u : 0u);
           }
         }
-        mma_commit(bar_o);
+        mma_commit(bar_pvh);
+        if (!mbar_wait(bar_plo, i & 1, s_abort, err)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int m = 0; m < kDv / 128; ++m) {
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k) {
+            const uint64_t a = sdesc_sw128(sKV + (2 * m) * L::KV_CHUNK + k * 2048, L::KV_CHUNK, 1024);
+            const uint64_t b = sdesc_sw128(sP + k * 2048, L::KV_CHUNK, 1024);
+            mma_ss(tO + m * kHeads, a, b, kIdPV, 1u);
+          }
+          mma_commit(bar_pv + 8 * m);
+        }
       }
       // every MMA of this CTA completes before the teardown frees TMEM
       mma_commit(bar_fin);
@@ -247,18 +253,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ======================= softmax + epilogue =======================
-    const int sw = warp - 2;          // 0..7
+    // ======================= gather + softmax + epilogue =======================
+    const int wk = warp - 1;          // 0..7
     const int qd = warp & 3;          // TMEM lane quadrant this warp may access
-    const int ch = sw >> 2;           // head half: heads ch*32 .. ch*32+31
+    const int ch = wk >> 2;           // head half: heads ch*32 .. ch*32+31
     const int r = qd * 32 + lane;     // key row of the tile / channel row of an O^T tile
     const int bar_id = 1 + ch;        // named barrier of the 128 threads of this half
-    float m_run[32], l_part[32];
+    // row indices this thread gathers for tile i: -1 = zero-fill (invalid or beyond the prefix)
+    auto load_rows = [&](int i, int (&rix)[4]) {
 #pragma unroll
-    for (int h = 0; h < 32; ++h) {
-      m_run[h] = -INFINITY;
-      l_part[h] = 0.f;
+      for (int e = 0; e < 4; ++e) {
+        const int j = i * kTile + (tid >> 3) + 32 * e;
+        int v = -1;
+        if (j < n_eff) {
+          const int ix = __ldg(idx_row + j);
+          v = (ix >= 0 && ix < Tk) ? ix : -1;
+          if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
+        }
+        rix[e] = v;
+      }
+    };
+    if (ntiles > 0) {
+      int rix[4];
+      load_rows(0, rix);
+      for (int c = 0; c < NCH; ++c) gather_chunk<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, bar_kv + 8 * c);
     }
+    // running max per head lives in s_stat (identical for all threads of a half)
+    const float* m_run = s_stat + ch * 32;
+    float l_part[32];
+#pragma unroll
+    for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
     bool aborted = false;
     for (int i = 0; i < ntiles; ++i) {
       const bool got = mbar_wait(bar_s, i & 1, s_abort, err);
@@ -294,18 +318,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float bm = fmaxf(fmaxf(s_red[ch * 32 + lane], s_red[64 + ch * 32 + lane]),
                                fmaxf(s_red[128 + ch * 32 + lane], s_red[192 + ch * 32 + lane]));
         const float mn = fmaxf(s_stat[ch * 32 + lane], bm);
+        // old max (mo) of every head of this half, then publish the new one
+        float alpha[32];
+        bool any = false;
+        const float mo_lane = s_stat[ch * 32 + lane];
         named_bar(bar_id, 128);
         if (qd == 0) s_stat[ch * 32 + lane] = mn;
         named_bar(bar_id, 128);
-        float alpha[32];
-        bool any = false;
 #pragma unroll
         for (int h = 0; h < 32; ++h) {
-          const float mnew = s_stat[ch * 32 + h];
-          alpha[h] = (m_run[h] == -INFINITY) ? 0.f : exp2f(m_run[h] - mnew);
+          const float mo = __shfl_sync(0xffffffffu, mo_lane, h);
+          const float mnew = m_run[h];
+          alpha[h] = (mo == -INFINITY) ? 0.f : exp2f(mo - mnew);
           any |= (i > 0) && (alpha[h] != 1.f);
           l_part[h] *= alpha[h];
-          m_run[h] = mnew;
         }
         if (any) {
           // O^T is complete for the previous tile: bar_s of this tile was
@@ -323,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_wait();
         }
       }
-      uint32_t pk[16];
+      uint32_t pk[16], pl[16];
 #pragma unroll
       for (int h = 0; h < 32; h += 2) {
         const float mu0 = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
@@ -332,7 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float p1 = (z[h + 1] == -INFINITY) ? 0.f : exp2f(z[h + 1] - mu1);
         l_part[h] += p0;
         l_part[h + 1] += p1;
-        pk[h >> 1] = pack_bf16x2(p0, p1);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
+        const float2 hf = __bfloat1622float2(hi);
+        pk[h >> 1] = *reinterpret_cast<const uint32_t*>(&hi);
+        pl[h >> 1] = pack_bf16x2(p0 - hf.x, p1 - hf.y);
       }
       // P^T row r: 64 heads x bf16 = 128 B; this half owns units ch*4 .. ch*4+3.
 #pragma unroll
@@ -342,9 +371,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p);
+      // the lo part goes into the same slot once V^T P_hi^T has read it
+      {
+        const bool okh = mbar_wait(bar_pvh, i & 1, s_abort, err);
+        if (okh) {
+#pragma unroll
+          for (int uu = 0; uu < 4; ++uu)
+            st_shared_v4(sP + sw128_off(r, ch * 4 + uu), pl[4 * uu], pl[4 * uu + 1], pl[4 * uu + 2], pl[4 * uu + 3]);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_plo);
+        if (named_bar_or(bar_id, 128, !okh)) { aborted = true; break; }
+      }
+      // ---- gather the next tile, chunk pair by chunk pair as P.V frees them ----
+      if (i + 1 < ntiles) {
+        int rix[4];
+        load_rows(i + 1, rix);
+        for (int m = 0; m < 4 && !aborted; ++m) {
+          if (!mbar_wait(bar_pv + 8 * m, i & 1, s_abort, err)) { aborted = true; break; }
+          gather_chunk<DQK>(sKV + (2 * m) * L::KV_CHUNK, kv, 2 * m, tid, rix, bar_kv + 8 * (2 * m));
+          gather_chunk<DQK>(sKV + (2 * m + 1) * L::KV_CHUNK, kv, 2 * m + 1, tid, rix, bar_kv + 8 * (2 * m + 1));
+        }
+        if (NCH == 9 && !aborted) gather_chunk<DQK>(sKV + 8 * L::KV_CHUNK, kv, 8, tid, rix, bar_kv + 8 * 8);
+        if (named_bar_or(bar_id, 128, aborted)) { aborted = true; break; }
+      }
     }
     if (!aborted && ntiles > 0) {
-      const bool got = mbar_wait(bar_o, (ntiles - 1) & 1, s_abort, err);
+      const bool got = mbar_wait(bar_pv + 8 * 3, (ntiles - 1) & 1, s_abort, err);
       aborted = named_bar_or(bar_id, 128, !got);
       tc_fence_after();
     }
@@ -358,7 +412,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float mh = s_stat[ch * 32 + lane];
     const int hl = hg * kHeads + ch * 32 + lane;
     if (qd == 0 && hl < H) lse[(size_t)t * H + hl] = (lt > 0.f) ? (mh * 0.69314718055994531f + logf(lt)) : -INFINITY;
-    named_bar(bar_id, 128);
     if (qd == 0) s_lsum[ch * 32 + lane] = lt;
     named_bar(bar_id, 128);
     float inv[32];
@@ -367,8 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float l = s_lsum[ch * 32 + h];
       inv[h] = (l > 0.f) ? 1.f / l : 0.f;
     }
-    const int hbase = hg * kHeads + ch * 32;
-    const int hcount = min(32, H - hbase);
+    // stage out (and its residual) as [64 heads][512] bf16 in the free tile region
+    uint8_t* stage = smem + L::OFF_KV;
+    uint8_t* stage_lo = stage + kHeads * kDv * 2;
 #pragma unroll 1
     for (int mt = 0; mt < kDv / 128; ++mt) {
       uint32_t ov[32];
@@ -380,24 +434,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < 32; ++h) ov[h] = 0u;
       }
       const int c = mt * 128 + qd * 32 + lane;
-      __nv_bfloat16* op = out + ((size_t)t * H + hbase) * kDv + c;
 #pragma unroll
-      for (int h = 0; h < 32; ++h)
-        if (h < hcount) op[(size_t)h * kDv] = __float2bfloat16_rn(__uint_as_float(ov[h]) * inv[h]);
+      for (int h = 0; h < 32; ++h) {
+        const float o = __uint_as_float(ov[h]) * inv[h];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(o);
+        reinterpret_cast<__nv_bfloat16*>(stage)[(ch * 32 + h) * kDv + c] = hi;
+        if (out_lo) reinterpret_cast<__nv_bfloat16*>(stage_lo)[(ch * 32 + h) * kDv + c] =
+            __float2bfloat16_rn(o - __bfloat162float(hi));
+      }
+    }
+    named_bar(3, kWorkers);
+    const int hcount = min(kHeads, H - hg * kHeads);
+    const size_t gbase = ((size_t)t * H + hg * kHeads) * kDv;
+    for (int u = tid; u < hcount * (kDv / 8); u += kWorkers) {
+      reinterpret_cast<uint4*>(out + gbase)[u] = reinterpret_cast<const uint4*>(stage)[u];
+      if (out_lo) reinterpret_cast<uint4*>(out_lo + gbase)[u] = reinterpret_cast<const uint4*>(stage_lo)[u];
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
 template <int DQK>
-dsa_status_t launch(const CUtensorMap& map, const void* q, const int32_t* idx, const int32_t* len, int T, int Tk,
-                    int H, int K, float scale, void* out, float* lse, int* err, cudaStream_t s) {
+dsa_status_t launch(const void* kv, const void* q, const int32_t* idx, const int32_t* len, int T, int Tk, int H,
+                    int K, float scale, void* out, void* out_lo, float* lse, int* err, cudaStream_t s) {
   using L = Smem<DQK>;
   static bool configured = false;
   if (!configured) {
@@ -410,8 +475,8 @@ dsa_status_t launch(const CUtensorMap& map, const void* q, const int32_t* idx, c
   dim3 grid(T, (H + kHeads - 1) / kHeads);
   const float sl2e = scale * 1.4426950408889634f;
   sparse_mla_fwd_kernel<DQK><<<grid, kThreads, L::TOTAL, s>>>(
-      map, reinterpret_cast<const __nv_bfloat16*>(q), idx, len, T, Tk, H, K, sl2e,
-      reinterpret_cast<__nv_bfloat16*>(out), lse, err);
+      reinterpret_cast<const __nv_bfloat16*>(kv), reinterpret_cast<const __nv_bfloat16*>(q), idx, len, T, Tk, H, K,
+      sl2e, reinterpret_cast<__nv_bfloat16*>(out), reinterpret_cast<__nv_bfloat16*>(out_lo), lse, err);
   return cuda_check(cudaGetLastError(), "launching sparse_mla_fwd_kernel");
 }
 
@@ -428,8 +493,9 @@ extern "C" size_t dsa_sparse_mla_fwd_workspace_size(int32_t T, int32_t H) {
 
 extern "C" dsa_status_t dsa_sparse_mla_fwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
                                            const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
-                                           int32_t Dv, int32_t K, float softmax_scale, dsa_bf16_t* out, float* lse,
-                                           void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
+                                           int32_t Dv, int32_t K, float softmax_scale, dsa_bf16_t* out,
+                                           dsa_bf16_t* out_lo, float* lse, void* workspace, size_t workspace_bytes,
+                                           dsa_stream_t stream) {
   const char* who = "dsa_sparse_mla_fwd";
   if (T < 0 || T_k < 1 || H < 1 || K < 1)
     return fail(DSA_ERR_INVALID_ARGUMENT, "%s: need T >= 0, T_k >= 1, H >= 1, K >= 1 (got %d, %d, %d, %d)", who, T,
@@ -441,18 +507,17 @@ extern "C" dsa_status_t dsa_sparse_mla_fwd(const dsa_bf16_t* q, const dsa_bf16_t
   if (T > 0 && (!q || !kv || !topk_idx || !out || !lse))
     return fail(DSA_ERR_INVALID_ARGUMENT, "%s: null tensor pointer", who);
   if (!kv) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: kv is NULL", who);
-  if (T > 0 && (!aligned16(q) || !aligned16(kv)))
-    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: q and kv must be 16-byte aligned", who);
+  if (T > 0 && (!aligned16(q) || !aligned16(kv) || !aligned16(out) || (out_lo && !aligned16(out_lo))))
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: q, kv, out and out_lo must be 16-byte aligned", who);
   dsa_status_t st = check_workspace(workspace, workspace_bytes, dsa_sparse_mla_fwd_workspace_size(T, H), who);
   if (st != DSA_OK) return st;
   if ((st = check_device()) != DSA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = clear_error_word(workspace, s)) != DSA_OK) return st;
   if (T == 0) return ok();
-  CUtensorMap map;
-  if ((st = make_map_2d_bf16(&map, kv, (uint64_t)T_k, (uint64_t)Dqk, (uint64_t)Dqk, 64, 1)) != DSA_OK) return st;
   int* err = reinterpret_cast<int*>(workspace);
-  st = (Dqk == 576) ? fwd::launch<576>(map, q, topk_idx, topk_len, T, T_k, H, K, softmax_scale, out, lse, err, s)
-                    : fwd::launch<512>(map, q, topk_idx, topk_len, T, T_k, H, K, softmax_scale, out, lse, err, s);
+  st = (Dqk == 576)
+           ? fwd::launch<576>(kv, q, topk_idx, topk_len, T, T_k, H, K, softmax_scale, out, out_lo, lse, err, s)
+           : fwd::launch<512>(kv, q, topk_idx, topk_len, T, T_k, H, K, softmax_scale, out, out_lo, lse, err, s);
   return st == DSA_OK ? ok() : st;
 }

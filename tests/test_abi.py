@@ -39,7 +39,7 @@ def fwd(lib, **kw):
              lse=FAKE, ws=P(0x100000), wsb=1 << 20, stream=None)
     a.update(kw)
     return lib.dsa_sparse_mla_fwd(a["q"], a["kv"], a["idx"], a["ln"], a["T"], a["Tk"], a["H"], a["Dqk"], a["Dv"],
-                                  a["K"], ctypes.c_float(a["scale"]), a["out"], a["lse"], a["ws"], a["wsb"],
+                                  a["K"], ctypes.c_float(a["scale"]), a["out"], None, a["lse"], a["ws"], a["wsb"],
                                   a["stream"])
 
 
