@@ -160,6 +160,32 @@ dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const
                                 size_t workspace_bytes, dsa_stream_t stream);
 
 /*
+ * dsa_sparse_mla_bwd_noalloc -- dsa_sparse_mla_bwd without a caller workspace.
+ * The pages have no counterpart: this is a library addition for callers that
+ * cannot allocate device memory (runtimes that reserve all device memory in
+ * their own pool and forbid other allocations, or plug-ins whose host program
+ * owns every allocation) and so cannot supply the workspace.  Arguments,
+ * semantics and results are those of dsa_sparse_mla_bwd.
+ *  - Scratch is a fixed 16 MiB + 256 B device array built into the library,
+ *    held by every GPU that loads it until the process exits; T * H must not
+ *    exceed dsa_sparse_mla_bwd_noalloc_max_rows() (4 Mi), else
+ *    DSA_ERR_WORKSPACE is returned and nothing is launched.
+ *  - The call allocates nothing.  The first call on a device looks up the
+ *    array's device address (cudaGetSymbolAddress) with that device current;
+ *    make that first call before any stream capture.
+ *  - Every call uses the same array: calls whose executions overlap on the
+ *    GPU race on it and must be ordered by the caller (same stream or events).
+ *    Each call clears the error word and rewrites the D values it reads.
+ */
+size_t dsa_sparse_mla_bwd_noalloc_max_rows(void);
+dsa_status_t dsa_sparse_mla_bwd_noalloc(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
+                                        const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
+                                        int32_t Dv, int32_t K, float softmax_scale, const dsa_bf16_t* out,
+                                        const dsa_bf16_t* out_lo, const float* lse, const dsa_bf16_t* dout,
+                                        dsa_bf16_t* dq, float* dkv_accum, int32_t accumulate, dsa_bf16_t* dkv_bf16,
+                                        dsa_stream_t stream);
+
+/*
  * dsa_read_device_status -- synchronise `stream`, read and clear the device
  * error word at the start of `workspace`, and store it in *status_host
  * (DSA_OK, DSA_ERR_DEVICE_INDEX or DSA_ERR_TIMEOUT).  Library addition with no

@@ -97,6 +97,11 @@ def load_library(path: str | None = None):
         lib.dsa_sparse_mla_bwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P,
                                            _I, _P, _P, _SZ, _P]
         lib.dsa_read_device_status.argtypes = [_P, _P, _P]
+        lib.dsa_sparse_mla_bwd_noalloc_max_rows.restype = _SZ
+        lib.dsa_sparse_mla_bwd_noalloc_max_rows.argtypes = []
+        lib.dsa_sparse_mla_bwd_noalloc.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P,
+                                                   _P, _I, _P, _P]
+        lib.dsa_sparse_mla_bwd_noalloc.restype = ctypes.c_int
         for name in ("dsa_packed_metadata", "dsa_indexer_topk", "dsa_sparse_mla_fwd", "dsa_sparse_mla_bwd",
                      "dsa_read_device_status"):
             getattr(lib, name).restype = ctypes.c_int

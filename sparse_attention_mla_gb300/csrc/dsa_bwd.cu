@@ -550,3 +550,74 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t
   }
   return ok();
 }
+
+// ---------------------------------------------------------------------------
+// dsa_sparse_mla_bwd_noalloc: the backward for callers that cannot allocate.
+//
+// Some callers cannot call cudaMalloc: runtimes that reserve all device memory
+// up front in their own pool and forbid any other allocation, or plug-ins
+// loaded into a host program that owns every allocation.  They cannot provide
+// the workspace dsa_sparse_mla_bwd needs (the device error word and the
+// per-(row, head) D array).  This entry point takes its scratch from the
+// file-scope device array below instead, so it allocates nothing.
+//
+// The array is a fixed 16 MiB + 256 B that every GPU which loads this library
+// holds until the process exits.  Its name is only a host-side stand-in for
+// the device array, so the host looks up the array's real device address with
+// cudaGetSymbolAddress, once per device, on the first call made with that
+// device current; that first call should therefore come before any stream
+// capture.  All calls share the one array: two calls whose executions overlap
+// on the GPU race on it, so callers must order them (one stream, or events).
+// Each call clears the error word it uses and overwrites the D array it
+// reads, so stale contents from an earlier call do not leak into the result.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace dsa {
+namespace bwd {
+constexpr size_t kNoAllocDeltaBytes = size_t(16) << 20;  // D for up to 4 Mi (row, head) pairs
+constexpr size_t kNoAllocScratchBytes = kErrorWordBytes + kNoAllocDeltaBytes;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device (looked up once per device).
+static dsa_status_t noalloc_scratch(void** ptr) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  dsa_status_t st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != DSA_OK) return st;
+  if (dev < 0 || dev >= 64) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if ((st = cuda_check(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress(scratch)")) != DSA_OK)
+      return st;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return DSA_OK;
+}
+}  // namespace bwd
+}  // namespace dsa
+
+extern "C" size_t dsa_sparse_mla_bwd_noalloc_max_rows(void) { return bwd::kNoAllocDeltaBytes / sizeof(float); }
+
+extern "C" dsa_status_t dsa_sparse_mla_bwd_noalloc(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
+                                                   const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H,
+                                                   int32_t Dqk, int32_t Dv, int32_t K, float softmax_scale,
+                                                   const dsa_bf16_t* out, const dsa_bf16_t* out_lo, const float* lse,
+                                                   const dsa_bf16_t* dout, dsa_bf16_t* dq, float* dkv_accum,
+                                                   int32_t accumulate, dsa_bf16_t* dkv_bf16, dsa_stream_t stream) {
+  const size_t need = dsa_sparse_mla_bwd_workspace_size(T, H);
+  if (need > bwd::kNoAllocScratchBytes)
+    return fail(DSA_ERR_WORKSPACE,
+                "dsa_sparse_mla_bwd_noalloc: T*H = %lld rows x heads exceeds the built-in scratch limit of %zu "
+                "(use dsa_sparse_mla_bwd with a caller workspace, or split the rows into chunks)",
+                (long long)T * H, dsa_sparse_mla_bwd_noalloc_max_rows());
+  dsa_status_t st = check_device();
+  if (st != DSA_OK) return st;
+  void* scratch = nullptr;
+  if ((st = bwd::noalloc_scratch(&scratch)) != DSA_OK) return st;
+  return dsa_sparse_mla_bwd(q, kv, topk_idx, topk_len, T, T_k, H, Dqk, Dv, K, softmax_scale, out, out_lo, lse, dout,
+                            dq, dkv_accum, accumulate, dkv_bf16, scratch, bwd::kNoAllocScratchBytes, stream);
+}
