@@ -23,16 +23,21 @@
 //    gathered tile streams twice through a 2-slot ring of 128-channel pairs
 //    (once for S^T / dP^T, once for dQ^T).  The gather is 16-byte cp.async
 //    issued by the 256 worker threads.
-//  * dS (x scale) and P are split into bf16 hi + lo parts in TMEM and feed the
-//    dKV products as A operands, so dkv is accurate to about fp32 even for
-//    keys shared by many rows; dS hi also goes to shared memory as the B
-//    operand of dQ^T.
-//  * dKV of a tile is produced 32 channels at a time into two TMEM buffers and
-//    flushed by the workers with red.global.add.v4.f32 on the gathered rows of
-//    the fp32 accumulator (reductions in L2).
+//  * dS (x scale) and P are split into bf16 hi + lo parts so that dkv is
+//    accurate to about fp32 even for keys shared by many rows.  dS hi sits in
+//    shared memory (B operand of dQ^T, A operand of dS^T Q); dS lo, P hi and
+//    P lo are written into TMEM over the thread's own S^T / dP^T columns and
+//    are A operands of the dKV products.
+//  * dKV of a tile is produced 64 channels at a time into one TMEM staging
+//    buffer and flushed by the workers with red.global.add.v4.f32 on the
+//    gathered rows of the fp32 accumulator (reductions in L2).  While the
+//    tensor core works on dKV, the workers have already issued the gather of
+//    the next tile's first channel pairs.
 //
-// Warp roles: warp 0 issues MMAs (one thread) and owns TMEM; warps 1..8 gather,
-// run the softmax backward, flush dKV and write dq.
+// Warp roles (4 warpgroups): warp 0 issues MMAs (one thread) and owns TMEM;
+// warpgroups 1-2 gather, run the softmax backward and write dq; warpgroup 3
+// copies each dKV group out of TMEM, releases it and issues the L2
+// reductions, so that the reductions overlap everything else.
 #include <cmath>
 
 #include "dsa_device.cuh"
@@ -41,12 +46,12 @@
 namespace dsa {
 namespace bwd {
 
-constexpr int kThreads = 288;
-constexpr int kWorkers = 256;
+constexpr int kThreads = 512;  // 4 warpgroups: MMA / math / math / flush
+constexpr int kMath = 256;    // math threads (warpgroups 1 and 2)
 constexpr int kTile = 128;
 constexpr int kHeads = 64;
 constexpr int kDv = 512;
-constexpr int kGroup = 32;  // dKV channels per staging buffer
+constexpr int kGroup = 64;  // dKV channels per staging group (one 64-channel chunk)
 
 template <int DQK>
 struct Smem {
@@ -73,7 +78,7 @@ constexpr int M_FULL = 0, M_EMPTY = 16, M_SDP = 32, M_DS = 40, M_STF = 48, M_STE
 constexpr int M_TMEM = 128, M_NEFF = 132, M_ABORT = 136;
 constexpr int M_LSE = 256, M_DL = 512;  // float [64] each
 
-// TMEM columns
+// TMEM columns: dQ^T (5 x 64), S^T, dP^T, dKV staging (64)
 constexpr uint32_t C_DQ = 0, C_S = 320, C_DP = 384, C_STG = 448;
 
 // D[t,h] = <dO[t,h,:], O[t,h,:] (+ O_lo[t,h,:])> in fp32; one warp per (t, h).
@@ -163,19 +168,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + M_TMEM);
   int* s_neff = reinterpret_cast<int*>(misc + M_NEFF);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + M_ABORT);
+  float* s_lse2 = reinterpret_cast<float*>(misc + M_LSE);
+  float* s_dl = reinterpret_cast<float*>(misc + M_DL);
 
   const int t = blockIdx.x;
   const int hg = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t* idx_row = topk_idx + (size_t)t * K;
+  const bool is_math = warp >= 4 && warp < 12;   // warpgroups 1, 2
+  const bool is_flush = warp >= 12;              // warpgroup 3
+  const int tid = threadIdx.x - 128;             // math thread id 0..255
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar_full + 8 * s, kWorkers);
+      mbar_init(bar_full + 8 * s, kMath);
       mbar_init(bar_empty + 8 * s, 1);
-      mbar_init(bar_stf + 8 * s, 1);
-      mbar_init(bar_ste + 8 * s, 8);
     }
+    mbar_init(bar_stf, 1);
+    mbar_init(bar_ste, 4);
     mbar_init(bar_sdp, 1);
     mbar_init(bar_ds, 8);
     mbar_init(bar_dq, 1);
@@ -191,8 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  const int tid = threadIdx.x - 32;  // worker id 0..255
-  if (warp >= 1) {
+  if (is_math) {
     if (topk_len != nullptr) {
       if (tid == 0) {
         int n = topk_len[t];
@@ -200,24 +209,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       int last = 0;
-      for (int j = tid; j < K; j += kWorkers)
+      for (int j = tid; j < K; j += kMath)
         if (idx_row[j] >= 0) last = j + 1;
       if (last) atomicMax(s_neff, last);
     }
     // Q [64 x DQK] and dO [64 x 512] -> 128B-swizzled chunks (rows = heads); heads >= H are zero.
-    for (int u = tid; u < kHeads * NCH * 8; u += kWorkers) {
+    for (int u = tid; u < kHeads * NCH * 8; u += kMath) {
       const int hh = u / (NCH * 8), rem = u - hh * (NCH * 8), c = rem >> 3, uc = rem & 7;
       const int h = hg * kHeads + hh;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (h < H) v = __ldg(reinterpret_cast<const uint4*>(q + ((size_t)t * H + h) * DQK + c * 64 + uc * 8));
       st_shared_v4(sQ + c * L::Q_CHUNK + sw128_off(hh, uc), v.x, v.y, v.z, v.w);
     }
-    for (int u = tid; u < kHeads * 8 * 8; u += kWorkers) {
+    for (int u = tid; u < kHeads * 8 * 8; u += kMath) {
       const int hh = u >> 6, rem = u & 63, c = rem >> 3, uc = rem & 7;
       const int h = hg * kHeads + hh;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (h < H) v = __ldg(reinterpret_cast<const uint4*>(dout + ((size_t)t * H + h) * kDv + c * 64 + uc * 8));
       st_shared_v4(sDO + c * L::Q_CHUNK + sw128_off(hh, uc), v.x, v.y, v.z, v.w);
+    }
+    // per-head lse (log2 units) and D, shared by every key row
+    if (tid < kHeads) {
+      const int hh = hg * kHeads + tid;
+      s_lse2[tid] = (hh < H) ? lse[(size_t)t * H + hh] * 1.4426950408889634f : INFINITY;  // padded heads: P = 0
+      s_dl[tid] = (hh < H) ? delta[(size_t)t * H + hh] : 0.f;
     }
     fence_proxy_async_smem();
   }
@@ -226,12 +241,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = (n_eff + kTile - 1) / kTile;
   const uint32_t tmem = *s_tmem;
 
-  if (warp == 0) {
-    // ======================= MMA issuer =======================
-    if (lane == 0) {
+  if (warp < 4) {
+    if (warp == 0 && lane == 0) {
+      // ======================= MMA issuer =======================
       constexpr uint32_t kIdKK = idesc_bf16(128, 64, false, false);      // S^T, dP^T
       constexpr uint32_t kIdMM = idesc_bf16(128, 64, true, true);        // dQ^T
-      constexpr uint32_t kIdKM = idesc_bf16(128, kGroup, false, true);   // dKV: A (TMEM) x B MN-major
+      constexpr uint32_t kIdKM = idesc_bf16(128, kGroup, false, true);   // dKV: A (smem/TMEM) x B MN-major
       int L_cnt = 0, G = 0;
       bool stop = false;
       for (int i = 0; i < ntiles && !stop; ++i) {
@@ -279,27 +294,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(bar_empty + 8 * slot);
         }
         if (stop) break;
-        // ---- dKV = (dS_hi + dS_lo)^T Q + (P_hi + P_lo)^T dO, 32 channels at a time ----
+        // ---- dKV = (dS_hi + dS_lo)^T Q + (P_hi + P_lo)^T dO, one 64-channel chunk at a time ----
         for (int g = 0; g < NG; ++g, ++G) {
-          const int b = G & 1;
-          if (!mbar_wait(bar_ste + 8 * b, ((G >> 1) & 1) ^ 1, s_abort, err)) { stop = true; break; }
+          if (!mbar_wait(bar_ste, (G & 1) ^ 1, s_abort, err)) { stop = true; break; }
           tc_fence_after();
-          const uint32_t d = tmem + C_STG + kGroup * b;
-          const uint32_t qb = sQ + (g >> 1) * L::Q_CHUNK + (g & 1) * 64;
-          const uint32_t ob = sDO + (g >> 1) * L::Q_CHUNK + (g & 1) * 64;
+          const uint32_t d = tmem + C_STG;
+          const uint32_t qb = sQ + g * L::Q_CHUNK;
+          const uint32_t ob = sDO + g * L::Q_CHUNK;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint32_t acol = (k >> 1) * 32 + (k & 1) * 8;
+            const uint32_t acol = (k >> 1) * 32 + (k & 1) * 8;  // heads 16k..16k+15 of a thread-half region
             const uint64_t bq = sdesc_sw128(qb + k * 2048, 16, 1024);
-            mma_ts(d, tmem + C_S + acol, bq, kIdKM, k > 0);        // dS hi
-            mma_ts(d, tmem + C_S + 16 + acol, bq, kIdKM, 1u);      // dS lo
-            if (g * kGroup < kDv) {
+            mma_ss(d, sdesc_sw128(sDS + k * 32, 16, 1024), bq, kIdKM, k > 0);  // dS hi (shared memory)
+            mma_ts(d, tmem + C_S + acol, bq, kIdKM, 1u);                      // dS lo
+            if (g < 8) {
               const uint64_t bo = sdesc_sw128(ob + k * 2048, 16, 1024);
-              mma_ts(d, tmem + C_DP + acol, bo, kIdKM, 1u);        // P hi
-              mma_ts(d, tmem + C_DP + 16 + acol, bo, kIdKM, 1u);   // P lo
+              mma_ts(d, tmem + C_DP + acol, bo, kIdKM, 1u);                   // P hi
+              mma_ts(d, tmem + C_DP + 16 + acol, bo, kIdKM, 1u);              // P lo
             }
           }
-          mma_commit(bar_stf + 8 * b);
+          mma_commit(bar_stf);
         }
         mma_commit(bar_kvd);
       }
@@ -309,23 +323,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar_fin, 0, &dummy, err);
     }
     __syncwarp();
-  } else {
-    // ======================= workers =======================
-    const int wk = warp - 1;
+  } else if (is_flush) {
+    // ======================= dKV flush: TMEM staging -> registers -> L2 reductions =======================
     const int qd = warp & 3;
-    const int ch = wk >> 2;           // heads ch*32 .. ch*32+31 / column half of a dKV group
+    const int r = qd * 32 + lane;  // key row of the tile
+    int G = 0;
+    for (int i = 0; i < ntiles; ++i) {
+      const int j = i * kTile + r;
+      int ix = -1;
+      if (j < n_eff) ix = __ldg(idx_row + j);
+      const bool valid = ix >= 0 && ix < Tk;
+      float* rowp = dkv + (size_t)(valid ? ix : 0) * DQK;
+      bool stop = false;
+      for (int g = 0; g < NG; ++g, ++G) {
+        if (!mbar_wait(bar_stf, G & 1, s_abort, err)) { stop = true; break; }
+        tc_fence_after();
+        uint32_t v[4][16];
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) tmem_ld16(tmem_addr(tmem + C_STG + 16 * qq, qd * 32, 0), v[qq]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_ste);  // staging free: the next group's MMAs may start
+        if (valid) {
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              red_add_v4(rowp + g * kGroup + 16 * qq + 4 * e, __uint_as_float(v[qq][4 * e]),
+                         __uint_as_float(v[qq][4 * e + 1]), __uint_as_float(v[qq][4 * e + 2]),
+                         __uint_as_float(v[qq][4 * e + 3]));
+        }
+      }
+      if (stop) break;
+    }
+  } else {
+    // ======================= math warps: gather, softmax backward, dq epilogue =======================
+    const int mw = warp - 4;          // 0..7
+    const int qd = warp & 3;
+    const int ch = mw >> 2;           // heads ch*32 .. ch*32+31
     const int r = qd * 32 + lane;     // key row of the tile
     const int bar_id = 1 + ch;
     const float sl2e = scale * 1.4426950408889634f;
-    // per-head lse (log2 units) and D, shared by every key row: kept in shared memory
-    float* s_lse2 = reinterpret_cast<float*>(misc + M_LSE);
-    float* s_dl = reinterpret_cast<float*>(misc + M_DL);
-    if (tid < kHeads) {
-      const int hh = hg * kHeads + tid;
-      s_lse2[tid] = (hh < H) ? lse[(size_t)t * H + hh] * 1.4426950408889634f : INFINITY;  // padded heads: P = 0
-      s_dl[tid] = (hh < H) ? delta[(size_t)t * H + hh] : 0.f;
-    }
-    named_bar(3, kWorkers);
     const float* lse2 = s_lse2 + ch * 32;
     const float* dl = s_dl + ch * 32;
     auto load_rows = [&](int i, int (&rix)[4]) {
@@ -341,21 +380,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         rix[e] = v;
       }
     };
-    int L_cnt = 0, G = 0;
+    int L_cnt = 0;
     bool aborted = false;
-    auto gather_pass = [&](const int (&rix)[4]) {
-      for (int p = 0; p < NP; ++p, ++L_cnt) {
+    auto gather_pairs = [&](const int (&rix)[4], int p0, int p1) {
+      for (int p = p0; p < p1; ++p, ++L_cnt) {
         const int slot = L_cnt & 1;
         if (!mbar_wait(bar_empty + 8 * slot, ((L_cnt >> 1) & 1) ^ 1, s_abort, err)) return false;
         gather_pair<DQK>(sRing + slot * L::SLOT, kv, p, tid, rix, bar_full + 8 * slot);
       }
       return true;
     };
+    int rix[4], rix_next[4];
+    if (ntiles > 0) {
+      load_rows(0, rix);
+      aborted = named_bar_or(bar_id, 128, !gather_pairs(rix, 0, NP));
+    }
     for (int i = 0; i < ntiles && !aborted; ++i) {
-      int rix[4];
-      load_rows(i, rix);
-      bool ok = gather_pass(rix);                       // pass A data
-      if (named_bar_or(bar_id, 128, !ok)) { aborted = true; break; }
       const bool got = mbar_wait(bar_sdp, i & 1, s_abort, err);
       if (named_bar_or(bar_id, 128, !got)) { aborted = true; break; }
       tc_fence_after();
@@ -367,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ix = -1;
       if (j < n_eff) ix = __ldg(idx_row + j);
       const bool valid = ix >= 0 && ix < Tk;
-      uint32_t ph[16], pl[16], sh[16], sl[16], dsb[16];
+      uint32_t ph[16], pl[16], sh[16], sl[16];
 #pragma unroll
       for (int h = 0; h < 32; h += 2) {
         float p0 = 0.f, p1 = 0.f, s0 = 0.f, s1 = 0.f;
@@ -384,14 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         sh[h >> 1] = *reinterpret_cast<const uint32_t*>(&shi);
         pl[h >> 1] = pack_bf16x2(p0 - phf.x, p1 - phf.y);
         sl[h >> 1] = pack_bf16x2(s0 - shf.x, s1 - shf.y);
-        dsb[h >> 1] = sh[h >> 1];
       }
 #pragma unroll
       for (int uu = 0; uu < 4; ++uu)
-        st_shared_v4(sDS + sw128_off(r, ch * 4 + uu), dsb[4 * uu], dsb[4 * uu + 1], dsb[4 * uu + 2], dsb[4 * uu + 3]);
-      // A operands of the dKV products, over this thread's own S^T / dP^T columns
-      tmem_st16(tmem_addr(tmem + C_S + ch * 32, qd * 32, 0), sh);
-      tmem_st16(tmem_addr(tmem + C_S + ch * 32 + 16, qd * 32, 0), sl);
+        st_shared_v4(sDS + sw128_off(r, ch * 4 + uu), sh[4 * uu], sh[4 * uu + 1], sh[4 * uu + 2], sh[4 * uu + 3]);
+      // TMEM A operands of the dKV products, over this thread's own S^T / dP^T columns
+      tmem_st16(tmem_addr(tmem + C_S + ch * 32, qd * 32, 0), sl);
       tmem_st16(tmem_addr(tmem + C_DP + ch * 32, qd * 32, 0), ph);
       tmem_st16(tmem_addr(tmem + C_DP + ch * 32 + 16, qd * 32, 0), pl);
       tmem_st_wait();
@@ -399,32 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
-      ok = gather_pass(rix);                            // pass B data
-      if (named_bar_or(bar_id, 128, !ok)) { aborted = true; break; }
-      // ---- flush dKV groups of this tile ----
-      for (int g = 0; g < NG; ++g, ++G) {
-        const int b = G & 1;
-        const bool okw = mbar_wait(bar_stf + 8 * b, (G >> 1) & 1, s_abort, err);
-        if (!okw) aborted = true;
-        tc_fence_after();
-        if (okw) {
-          uint32_t v[16];
-          tmem_ld16(tmem_addr(tmem + C_STG + kGroup * b + ch * 16, qd * 32, 0), v);
-          tmem_ld_wait();
-          if (valid) {
-            float* dst = dkv + (size_t)ix * DQK + g * kGroup + ch * 16;
+      bool ok = gather_pairs(rix, 0, NP);                 // pass B data
+      if (ok && i + 1 < ntiles) {                         // the next tile's pass A data
+        load_rows(i + 1, rix_next);
+        ok = gather_pairs(rix_next, 0, NP);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              red_add_v4(dst + 4 * e, __uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                         __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_ste + 8 * b);
-        if (!okw) break;
+        for (int e = 0; e < 4; ++e) rix[e] = rix_next[e];
       }
-      aborted = named_bar_or(bar_id, 128, aborted);
+      aborted = named_bar_or(bar_id, 128, !ok);
     }
     // ---- dq epilogue: dQ^T (lanes = channels) -> staged [64 heads][DQK] bf16 -> coalesced stores ----
     bool have = false;
@@ -433,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       have = !named_bar_or(bar_id, 128, !got);
       tc_fence_after();
     }
-    named_bar(3, kWorkers);  // both halves are done with the ring before it becomes the staging area
+    named_bar(3, kMath);  // both halves are done with the ring before it becomes the staging area
     __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + L::OFF_RING);
 #pragma unroll 1
     for (int p = 0; p < NP; ++p) {
@@ -451,10 +471,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < 32; ++h) stage[(ch * 32 + h) * DQK + c] = __float2bfloat16_rn(__uint_as_float(v[h]));
       }
     }
-    named_bar(3, kWorkers);
+    named_bar(3, kMath);
     const int hcount = min(kHeads, H - hg * kHeads);
     uint4* dst = reinterpret_cast<uint4*>(dq + ((size_t)t * H + hg * kHeads) * DQK);
-    for (int u = tid; u < hcount * (DQK / 8); u += kWorkers) dst[u] = reinterpret_cast<const uint4*>(stage)[u];
+    for (int u = tid; u < hcount * (DQK / 8); u += kMath) dst[u] = reinterpret_cast<const uint4*>(stage)[u];
   }
 
   tc_fence_before();
