@@ -17,8 +17,10 @@
 //    the N = 256 side of the MMA; keys are the M = 128 side:
 //    D[key, (token, head)] = K_tile . Q^T, fp32 in TMEM, double-buffered
 //    (2 x 256 columns).  k_idx tiles arrive by TMA (2 boxes of 64 channels).
-//  * The epilogue warps (one TMEM lane = one key) apply ReLU and the fp32
-//    head-weighted sum, so scores exist only in registers.
+//  * 16 epilogue warps, 4 per token (one TMEM lane = one key), apply ReLU and
+//    the fp32 head-weighted sum, so scores exist only in registers; each token
+//    has its own warp group, named barrier and candidate buffer, so the four
+//    tokens' selections run in parallel.
 //  * Selection: each token keeps a shared-memory buffer of candidates
 //    (score, index) that beat its running threshold.  Candidates are appended
 //    in ascending key order (a block-wide scan, not atomics), and a full
@@ -35,7 +37,8 @@
 namespace dsa {
 namespace idx {
 
-constexpr int kThreads = 320;
+constexpr int kEpi = 512;                 // 16 epilogue warps: 4 per query token
+constexpr int kThreads = 64 + kEpi;       // + producer warp + MMA warp
 constexpr int kTokens = 4;     // query tokens per CTA
 constexpr int kHeads = 64;     // index heads (padded)
 constexpr int kDi = 128;       // index head dim
@@ -49,7 +52,7 @@ constexpr int OFF_K = OFF_Q + 2 * Q_CHUNK;     // 2 stages x 2 chunks x [128 row
 constexpr int K_CHUNK = kTile * 128;           // 16 KiB
 constexpr int K_STAGE = 2 * K_CHUNK;
 constexpr int OFF_MISC = OFF_K + 2 * K_STAGE;  // 128 KiB
-constexpr int MISC = 4096;
+constexpr int MISC = 6144;
 constexpr int OFF_CAND = OFF_MISC + MISC;
 constexpr int CAP = 2944;                      // candidates per token
 constexpr int TOTAL = OFF_CAND + kTokens * CAP * 8 + 1024;
@@ -60,9 +63,10 @@ static_assert(CAP >= kMaxK + kTile + 128, "candidate buffer must hold K + one ti
 constexpr int M_KF = 0, M_KE = 16, M_DF = 32, M_DE = 48, M_FIN = 64;
 constexpr int M_TMEM = 128, M_ABORT = 132;
 constexpr int M_W = 256;                // float [4][64]
-constexpr int M_WCNT = M_W + 1024;      // int [2 halves][2 parity][4 warps]
-constexpr int M_HIST = M_WCNT + 64;     // int [2 halves][256]
-constexpr int M_SEL = M_HIST + 2048;    // int [2 halves][4]
+constexpr int M_WCNT = M_W + 1024;      // int [4 tokens][2 parity][4 warps]
+constexpr int M_HIST = M_WCNT + 128;    // int [4 tokens][256]
+constexpr int M_SEL = M_HIST + 4096;    // int [4 tokens][4]
+static_assert(M_SEL + 64 <= MISC, "misc layout");
 
 __device__ __forceinline__ uint32_t ordered(float f) {
   const uint32_t u = __float_as_uint(f);
@@ -72,7 +76,7 @@ __device__ __forceinline__ float unordered(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Per-half context: 4 warps (128 threads), one named barrier.
+// Per-token context: 4 warps (128 threads, one per TMEM lane quadrant), one named barrier.
 struct Half {
   int bar;     // named barrier id
   int tid;     // 0..127 within the half (ordered by key row)
@@ -207,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_kf + 8 * s, 1);
       mbar_init(bar_ke + 8 * s, 1);
       mbar_init(bar_df + 8 * s, 1);
-      mbar_init(bar_de + 8 * s, 8);
+      mbar_init(bar_de + 8 * s, kEpi / 32);
     }
     mbar_init(bar_fin, 1);
     *s_abort = 0;
@@ -230,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 2) {
     const int tid = threadIdx.x - 64;
     // Q rows (token k, head h) -> 2 chunks of [256 rows x 128 B], swizzled; padding rows zero
-    for (int u = tid; u < kN * 16; u += 256) {
+    for (int u = tid; u < kN * 16; u += kEpi) {
       const int row = u >> 4, c = (u >> 3) & 1, uc = u & 7;
       const int k = row / kHeads, h = row - k * kHeads;
       uint4 v = make_uint4(0, 0, 0, 0);
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         v = __ldg(reinterpret_cast<const uint4*>(q_idx + ((size_t)(t0 + k) * Hi + h) * kDi + c * 64 + uc * 8));
       st_shared_v4(sQ + c * Q_CHUNK + sw128_off(row, uc), v.x, v.y, v.z, v.w);
     }
-    for (int u = tid; u < kTokens * kHeads; u += 256) {
+    for (int u = tid; u < kTokens * kHeads; u += kEpi) {
       const int k = u / kHeads, h = u - k * kHeads;
       s_w[u] = (k < nt && h < Hi) ? __ldg(w + (size_t)(t0 + k) * Hi + h) : 0.f;
     }
@@ -289,29 +293,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ======================= score epilogue + selection =======================
-    const int sw = warp - 2;
+    // ======================= score epilogue + selection (one 4-warp group per token) =======================
+    const int ew = warp - 2;
     const int qd = warp & 3;
-    const int half = sw >> 2;  // tokens 2*half, 2*half+1
+    const int k = ew >> 2;  // this group's token
     Half hf;
-    hf.bar = 1 + half;
+    hf.bar = 1 + k;
     hf.wq = qd;
     hf.lane = lane;
     hf.tid = qd * 32 + lane;
-    hf.wcnt = reinterpret_cast<int*>(misc + M_WCNT) + half * 8;
-    hf.hist = reinterpret_cast<int*>(misc + M_HIST) + half * 256;
-    hf.sel = reinterpret_cast<int*>(misc + M_SEL) + half * 4;
-    float* cs[2];
-    int* ci[2];
-    int win_lo[2], win_hi[2], cnt[2] = {0, 0};
-    uint32_t thr[2] = {0u, 0u};
-    for (int u = 0; u < 2; ++u) {
-      const int k = 2 * half + u;
-      cs[u] = reinterpret_cast<float*>(smem + OFF_CAND + k * CAP * 8);
-      ci[u] = reinterpret_cast<int*>(smem + OFF_CAND + k * CAP * 8 + CAP * 4);
-      win_lo[u] = (k < nt) ? __ldg(seq_start + t0 + k) : 1;
-      win_hi[u] = (k < nt) ? t0 + k : 0;  // empty window for inactive tokens
-    }
+    hf.wcnt = reinterpret_cast<int*>(misc + M_WCNT) + k * 8;
+    hf.hist = reinterpret_cast<int*>(misc + M_HIST) + k * 256;
+    hf.sel = reinterpret_cast<int*>(misc + M_SEL) + k * 4;
+    float* cs = reinterpret_cast<float*>(smem + OFF_CAND + k * CAP * 8);
+    int* ci = reinterpret_cast<int*>(smem + OFF_CAND + k * CAP * 8 + CAP * 4);
+    const int win_lo = (k < nt) ? __ldg(seq_start + t0 + k) : 1;
+    const int win_hi = (k < nt) ? t0 + k : 0;  // empty window for an inactive token
+    const float* wr = s_w + k * kHeads;
+    int cnt = 0;
+    uint32_t thr = 0u;
     int parity = 0;
     bool aborted = false;
     for (int i = 0; i < ntiles; ++i) {
@@ -319,55 +319,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool got = mbar_wait(bar_df + 8 * b, (i >> 1) & 1, s_abort, err);
       if (named_bar_or(hf.bar, 128, !got)) { aborted = true; break; }
       tc_fence_after();
-      uint32_t v[2][64];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint32_t col = b * kN + (2 * half + u) * kHeads;
-        tmem_ld32(tmem_addr(tmem + col, qd * 32, 0), *reinterpret_cast<uint32_t(*)[32]>(&v[u][0]));
-        tmem_ld32(tmem_addr(tmem + col + 32, qd * 32, 0), *reinterpret_cast<uint32_t(*)[32]>(&v[u][32]));
-      }
+      uint32_t v[64];
+      const uint32_t col = b * kN + k * kHeads;
+      tmem_ld32(tmem_addr(tmem + col, qd * 32, 0), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(tmem_addr(tmem + col + 32, qd * 32, 0), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_de + 8 * b);
-      const int key = (kt0 + i) * kTile + hf.tid;
+      const int tile0 = (kt0 + i) * kTile;
+      if (tile0 > win_hi || tile0 + kTile <= win_lo) continue;  // whole tile outside this token's window (uniform)
+      const int key = tile0 + hf.tid;
+      float sc = 0.f;
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const float* wr = s_w + (2 * half + u) * kHeads;
-        float sc = 0.f;
-#pragma unroll
-        for (int h = 0; h < kHeads; ++h) sc = fmaf(wr[h], fmaxf(__uint_as_float(v[u][h]), 0.f), sc);
-        const bool in = key >= win_lo[u] && key <= win_hi[u];
-        const bool acc = in && ordered(sc) > thr[u];
-        const int2 pos = half_scan(hf, acc, parity);
-        parity ^= 1;
-        if (acc) {
-          cs[u][cnt[u] + pos.x] = sc;
-          ci[u][cnt[u] + pos.x] = key;
-        }
-        cnt[u] += pos.y;
-        if (cnt[u] > CAP - kTile) {
-          named_bar(hf.bar, 128);
-          thr[u] = compact(hf, cs[u], ci[u], cnt[u], K, parity);
-          cnt[u] = K;
-        }
+      for (int h = 0; h < kHeads; ++h) sc = fmaf(wr[h], fmaxf(__uint_as_float(v[h]), 0.f), sc);
+      const bool in = key >= win_lo && key <= win_hi;
+      const bool acc = in && ordered(sc) > thr;
+      const int2 pos = half_scan(hf, acc, parity);
+      parity ^= 1;
+      if (acc) {
+        cs[cnt + pos.x] = sc;
+        ci[cnt + pos.x] = key;
+      }
+      cnt += pos.y;
+      if (cnt > CAP - kTile) {
+        named_bar(hf.bar, 128);
+        thr = compact(hf, cs, ci, cnt, K, parity);
+        cnt = K;
       }
     }
     // ---- final selection and output (ascending, -1 suffix) ----
     if (!aborted) named_bar(hf.bar, 128);
-    for (int u = 0; u < 2; ++u) {
-      const int k = 2 * half + u;
-      if (k >= nt) continue;
+    if (k < nt) {
       const int t = t0 + k;
-      const int c = win_hi[u] - win_lo[u] + 1;
+      const int c = win_hi - win_lo + 1;
       const int n = min(K, c);
-      if (!aborted && cnt[u] > n) {
-        compact(hf, cs[u], ci[u], cnt[u], n, parity);
-        cnt[u] = n;
+      if (!aborted && cnt > n) {
+        compact(hf, cs, ci, cnt, n, parity);
+        cnt = n;
       }
-      const int have = aborted ? 0 : min(cnt[u], n);
+      const int have = aborted ? 0 : min(cnt, n);
       int32_t* row = topk_idx + (size_t)t * K;
-      for (int j = hf.tid; j < K; j += 128) row[j] = (j < have) ? ci[u][j] : -1;
+      for (int j = hf.tid; j < K; j += 128) row[j] = (j < have) ? ci[j] : -1;
       if (topk_len != nullptr && hf.tid == 0) topk_len[t] = have;
     }
   }
