@@ -67,7 +67,8 @@ struct Smem {
   static constexpr int OFF_DS = OFF_RING + 2 * SLOT;
   static constexpr int OFF_MISC = OFF_DS + KV_CHUNK;
   static constexpr int MISC = 1024;
-  static constexpr int TOTAL = OFF_MISC + MISC + 1024;
+  static constexpr int OFF_FST = OFF_MISC + MISC;  // flush transpose buffers: 4 warps x 32 rows x 64 B
+  static constexpr int TOTAL = OFF_FST + 4 * 2048 + 1024;
   static_assert(TOTAL <= 232448, "shared memory budget");
   static_assert(2 * SLOT + KV_CHUNK >= kHeads * DQK * 2, "dq staging fits ring + dS");
 };
@@ -327,13 +328,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================= dKV flush: TMEM staging -> registers -> L2 reductions =======================
     const int qd = warp & 3;
     const int r = qd * 32 + lane;  // key row of the tile
+    const uint32_t fst = smem_u32(smem + L::OFF_FST + qd * 2048);
     int G = 0;
     for (int i = 0; i < ntiles; ++i) {
       const int j = i * kTile + r;
       int ix = -1;
       if (j < n_eff) ix = __ldg(idx_row + j);
       const bool valid = ix >= 0 && ix < Tk;
-      float* rowp = dkv + (size_t)(valid ? ix : 0) * DQK;
       bool stop = false;
       for (int g = 0; g < NG; ++g, ++G) {
         if (!mbar_wait(bar_stf, G & 1, s_abort, err)) { stop = true; break; }
@@ -345,14 +346,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_ste);  // staging free: the next group's MMAs may start
-        if (valid) {
+        // Transpose 16 channels at a time through this warp's 2 KB buffer so that 4
+        // lanes cover one row's 64 contiguous bytes: each reduction instruction then
+        // touches 8 rows x 64 B instead of 32 rows x 16 B.
 #pragma unroll
-          for (int qq = 0; qq < 4; ++qq)
+        for (int qq = 0; qq < 4; ++qq) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              red_add_v4(rowp + g * kGroup + 16 * qq + 4 * e, __uint_as_float(v[qq][4 * e]),
-                         __uint_as_float(v[qq][4 * e + 1]), __uint_as_float(v[qq][4 * e + 2]),
-                         __uint_as_float(v[qq][4 * e + 3]));
+          for (int k = 0; k < 4; ++k)
+            st_shared_v4(fst + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4), v[qq][4 * k], v[qq][4 * k + 1],
+                         v[qq][4 * k + 2], v[qq][4 * k + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int st = 0; st < 4; ++st) {
+            const int rl = 8 * st + (lane >> 2), u = lane & 3;
+            const int ixr = __shfl_sync(0xffffffffu, valid ? ix : -1, rl);
+            float4 f;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+                         : "r"(fst + rl * 64 + ((u ^ ((rl >> 1) & 3)) << 4))
+                         : "memory");
+            if (ixr >= 0) red_add_v4(dkv + (size_t)ixr * DQK + g * kGroup + 16 * qq + 4 * u, f.x, f.y, f.z, f.w);
+          }
+          __syncwarp();
         }
       }
       if (stop) break;
