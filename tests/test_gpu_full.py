@@ -1,0 +1,175 @@
+"""Full-size checks: the pages' workloads at their full sizes, in the launch
+configuration the benchmark times, against the fp64 oracle.
+
+Large outputs are compared on sampled rows the oracle computes one by one
+(query rows are independent), plus properties that hold at any size:
+  * dkv column sums: sum_k dkv[k,c] = sum_{t,h nonempty} dO[t,h,c] (c < 512), 0 for RoPE channels;
+  * dkv restricted to a chunk of rows (a call on row-offset pointers) equals
+    the oracle's dkv of exactly those rows, at full T_k and K;
+  * query chunks give the same outputs as one shot.
+Inputs are drawn on the GPU with the seeded recipe (sparse_attention_mla_gb300.synth).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_mla_gb300 as dsa
+from sparse_attention_mla_gb300 import synth
+
+from _cmp import assert_close, assert_lse
+from test_gpu_indexer import check_rows
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def causal_idx_gpu(seq_start, K, seed, T):
+    """Random causal index sets drawn on the GPU: uniform n-subset of [start, t], ascending, -1 suffix."""
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    st = seq_start.to(DEV).long()
+    idx = torch.full((T, K), -1, dtype=torch.int32, device=DEV)
+    for a in range(0, T, 1024):
+        b = min(T, a + 1024)
+        t = torch.arange(a, b, device=DEV)
+        c = t - st[a:b] + 1
+        cmax = int(c.max())
+        r = torch.rand(b - a, cmax, generator=g, device=DEV)
+        r.masked_fill_(torch.arange(cmax, device=DEV)[None, :] >= c[:, None], -1.0)
+        kk = min(K, cmax)
+        v, i = r.topk(kk, dim=1)
+        i = torch.where(v >= 0, i + st[a:b, None], torch.full_like(i, 1 << 30)).sort(dim=1).values
+        i = torch.where(i == (1 << 30), torch.full_like(i, -1), i)
+        idx[a:b, :kk] = i.to(torch.int32)
+    return idx
+
+
+def sample_rows(T, starts_of_interest, n_random=12, seed=0):
+    g = np.random.default_rng(seed)
+    rows = set(int(x) for x in starts_of_interest if 0 <= x < T)
+    rows |= set(g.integers(0, T, n_random).tolist())
+    return np.array(sorted(rows))
+
+
+def mla_full_check(q, kv, dout, idx, scale, ln=None, rows=None, chunk=(0, 64), Dv=512):
+    """fwd+bwd of the whole problem, then row samples, column sums and one exact dkv chunk."""
+    T, H = q.shape[0], q.shape[1]
+    wf = torch.zeros(dsa.workspace_size("fwd", T, H), dtype=torch.uint8, device=DEV)
+    wb = torch.zeros(dsa.workspace_size("bwd", T, H), dtype=torch.uint8, device=DEV)
+    out, lse, lo = dsa.dsa_sparse_mla_fwd(q, kv, idx, scale, topk_len=ln, out_lo=True, workspace=wf)
+    dq, dkv, _ = dsa.dsa_sparse_mla_bwd(q, kv, idx, scale, out, lse, dout, topk_len=ln, out_lo=lo, workspace=wb)
+    assert dsa.dsa_read_device_status(wf) == 0 and dsa.dsa_read_device_status(wb) == 0
+    del wb
+    kvc = kv.cpu()
+    r = torch.as_tensor(rows)
+    ln_r = None if ln is None else ln[r].cpu()
+    ref_o, ref_l = oracle.sparse_mla_fwd(q[r].cpu(), kvc, idx[r].cpu(), scale, len_rows=ln_r)
+    assert_close(out[r].cpu(), ref_o, "out (sampled rows)")
+    assert_lse(lse[r].cpu(), ref_l)
+    ref_dq, _ = oracle.sparse_mla_bwd(q[r].cpu(), kvc, idx[r].cpu(), dout[r].cpu(), scale, len_rows=ln_r)
+    assert_close(dq[r].cpu(), ref_dq, "dq (sampled rows)")
+    # column sums of the full dkv
+    valid = (idx >= 0) if ln is None else ((idx >= 0) & (torch.arange(idx.shape[1], device=DEV)[None, :] < ln[:, None]))
+    nonempty = valid.any(dim=1)
+    col = dkv.double().sum(0).cpu().numpy()
+    ref = torch.zeros(dout.shape[-1], dtype=torch.float64, device=DEV)
+    for a in range(0, dout.shape[0], 4096):
+        ref += dout[a:a + 4096][nonempty[a:a + 4096]].double().sum((0, 1))
+    ref = ref.cpu().numpy()
+    scale_ref = max(1.0, float(np.abs(ref).max()))
+    assert np.max(np.abs(col[:Dv] - ref)) <= 2e-2 * scale_ref, "dkv column sums (value channels)"
+    assert np.max(np.abs(col[Dv:])) <= 2e-2 * scale_ref if col.shape[0] > Dv else True
+    # exact dkv of a chunk of rows, at full T_k and K
+    a, b = chunk
+    _, dkv_c, _ = dsa.dsa_sparse_mla_bwd(q[a:b], kv, idx[a:b], scale, out[a:b], lse[a:b], dout[a:b],
+                                         topk_len=None if ln is None else ln[a:b], out_lo=lo[a:b])
+    _, ref_c = oracle.sparse_mla_bwd(q[a:b].cpu(), kvc, idx[a:b].cpu(), dout[a:b].cpu(), scale,
+                                     len_rows=None if ln is None else ln[a:b].cpu())
+    assert_close(dkv_c.cpu(), ref_c, f"dkv of rows {a}:{b}")
+    return out, lse, lo, dq, dkv
+
+
+def test_full_v32_layout_S4096_H128_K2048():
+    # DeepSeek-V3.2 layout: 1 sequence, S=4096, H=128, width 576, K=2048 random causal, scale 192^-0.5
+    c = synth.CONFIGS["v32"]
+    T = c["T"]
+    x = synth.mla_inputs(T, c["H"], c["Dqk"], c["Dv"], seed=2, device=DEV)
+    idx = causal_idx_gpu(torch.zeros(T, dtype=torch.int32), c["K"], 2, T)
+    rows = sample_rows(T, [0, 1, 2, 63, 2047, 2048, 2049, T - 1])
+    mla_full_check(x["q"], x["kv"], x["dout"], idx, c["scale"], rows=rows, chunk=(T - 48, T))
+
+
+def test_full_indexer_32k_then_sparse_mla_H64():
+    # the benchmark's workload: S=32768, indexer 64x128, K=2048, then H=64 sparse MLA fwd+bwd at width 576
+    c = synth.CONFIGS["idx32k"]
+    T, K = c["T"], c["K"]
+    ind = synth.indexer_inputs(T, c["Hi"], c["Di"], seed=3, device=DEV)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=DEV)
+    start, _, _, _ = dsa.dsa_packed_metadata(cu, T)
+    ws = torch.zeros(dsa.workspace_size("indexer", T, K), dtype=torch.uint8, device=DEV)
+    idx, ln = dsa.dsa_indexer_topk(ind["q_idx"], ind["k_idx"], ind["w"], start, K, workspace=ws)
+    assert dsa.dsa_read_device_status(ws) == 0
+    rows = sample_rows(T, [0, 1, 2047, 2048, 2049, 16383, T - 2, T - 1], n_random=8, seed=3)
+    qi = ind["q_idx"].cpu()
+    check_rows(idx.cpu().numpy(), ln.cpu().numpy(), qi, ind["k_idx"].cpu(), ind["w"].cpu(),
+               start.cpu().numpy(), rows, K)
+    x = synth.mla_inputs(T, c["H"], c["Dqk"], c["Dv"], seed=4, device=DEV)
+    mla_full_check(x["q"], x["kv"], x["dout"], idx, c["scale"], ln=ln, rows=rows, chunk=(T - 32, T))
+
+
+def test_full_nope_S16384_H8_K2051_and_query_chunks():
+    # GLM-5.3-Flash NoPE: S=16384, H=8, width 512, unaligned K=2051, scale 512^-0.5; 4096-token chunks = one shot
+    c = synth.CONFIGS["nope"]
+    T, K = c["T"], c["K"]
+    x = synth.mla_inputs(T, c["H"], c["Dqk"], c["Dv"], seed=5, device=DEV)
+    idx = causal_idx_gpu(torch.zeros(T, dtype=torch.int32), K, 5, T)
+    rows = sample_rows(T, [0, 1, 2050, 2051, 2052, T - 1], seed=5)
+    out, lse, lo, dq, dkv = mla_full_check(x["q"], x["kv"], x["dout"], idx, c["scale"], rows=rows,
+                                           chunk=(8000, 8064))
+    acc = None
+    for a in range(0, T, 4096):
+        b = min(T, a + 4096)
+        o_c, l_c, lo_c = dsa.dsa_sparse_mla_fwd(x["q"][a:b], x["kv"], idx[a:b], c["scale"], out_lo=True)
+        assert torch.equal(o_c, out[a:b]) and torch.equal(l_c, lse[a:b])
+        dq_c, acc, _ = dsa.dsa_sparse_mla_bwd(x["q"][a:b], x["kv"], idx[a:b], c["scale"], o_c, l_c, x["dout"][a:b],
+                                              dkv_accum=acc, accumulate=acc is not None, out_lo=lo_c)
+        assert torch.equal(dq_c, dq[a:b])
+    assert_close(acc.cpu(), dkv.cpu().double(), "chunked dkv", max_abs=1e-3, rel_fro=1e-5)
+
+
+def test_full_thd_packed_indexshare_4_layers():
+    # 8 sequences, lengths U[4096, 32768] rescaled to 131072 tokens; indexer once, its top-k reused by 4 layers
+    c = synth.CONFIGS["thd"]
+    T, K = c["T"], c["K"]
+    lens = synth.thd_lengths(c["nseq"], c["lo"], c["hi"], T, synth.generator(6))
+    cu = synth.cu_seqlens_from_lengths(lens)
+    start, clen, mx, ne = dsa.dsa_packed_metadata(cu.to(DEV), T)
+    st_ref, cl_ref, mx_ref, _ = oracle.packed_metadata(cu.numpy(), T)
+    assert np.array_equal(start.cpu().numpy(), st_ref) and np.array_equal(clen.cpu().numpy(), cl_ref)
+    assert mx == mx_ref == max(lens) and ne == 1
+    ind = synth.indexer_inputs(T, c["Hi"], c["Di"], seed=6, device=DEV)
+    ws = torch.zeros(dsa.workspace_size("indexer", T, K), dtype=torch.uint8, device=DEV)
+    idx, ln = dsa.dsa_indexer_topk(ind["q_idx"], ind["k_idx"], ind["w"], start, K, workspace=ws)
+    assert dsa.dsa_read_device_status(ws) == 0
+    cuts = cu.tolist()
+    rows = sample_rows(T, [cuts[1] - 1, cuts[1], cuts[1] + 1, cuts[4] + 2047, cuts[4] + 2048, T - 1], n_random=6,
+                       seed=6)
+    check_rows(idx.cpu().numpy(), ln.cpu().numpy(), ind["q_idx"].cpu(), ind["k_idx"].cpu(), ind["w"].cpu(),
+               st_ref, rows, K)
+    # packing is exact: one sequence run alone gives the same indices (shifted by its offset)
+    a, b = cuts[2], cuts[3]
+    cu1 = torch.tensor([0, b - a], dtype=torch.int32, device=DEV)
+    s1, _, _, _ = dsa.dsa_packed_metadata(cu1, b - a)
+    idx1, ln1 = dsa.dsa_indexer_topk(ind["q_idx"][a:b], ind["k_idx"][a:b], ind["w"][a:b], s1, K)
+    shifted = torch.where(idx1 >= 0, idx1 + a, idx1)
+    assert torch.equal(shifted, idx[a:b]) and torch.equal(ln1, ln[a:b])
+    # IndexShare: the same index tensor drives 4 layers with independent q / kv / dO
+    idx_before = idx.clone()
+    for layer in range(c["layers"]):
+        x = synth.mla_inputs(T, c["H"], c["Dqk"], 512, seed=100 + layer, device=DEV)
+        mla_full_check(x["q"], x["kv"], x["dout"], idx, c["scale"], ln=ln, rows=rows[::3],
+                       chunk=(cuts[5] - 16, cuts[5] + 16))
+        del x
+        torch.cuda.empty_cache()
+    assert torch.equal(idx, idx_before)
