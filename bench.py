@@ -222,7 +222,7 @@ def run_cuda(args, rank, world, local):
     dkv = torch.empty(S, DQK, dtype=torch.float32, device=dev)
     ws_i = torch.zeros(dsa.workspace_size("indexer", S, K), dtype=torch.uint8, device=dev)
     ws_f = torch.zeros(dsa.workspace_size("fwd", S, H), dtype=torch.uint8, device=dev)
-    ws_b = torch.zeros(dsa.workspace_size("bwd", S, H), dtype=torch.uint8, device=dev)
+    ws_b = torch.zeros(dsa.workspace_size("bwd", S, H, K), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]

@@ -147,10 +147,12 @@ dsa_status_t dsa_sparse_mla_fwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const
  *  dkv_accum      device fp32 [T_k, Dqk]: zeroed first when accumulate == 0,
  *                 added to when accumulate == 1 (query chunks)
  *  dkv_bf16       device bf16 [T_k, Dqk] (out, rounded copy of dkv_accum) or NULL
- *  workspace      >= dsa_sparse_mla_bwd_workspace_size(T, H) bytes
+ *  workspace      >= dsa_sparse_mla_bwd_workspace_size(T, H, K) bytes: the
+ *                 error word, D (T*H fp32) and a per-SM scratch for the bf16
+ *                 dS of one row's tiles (256 slots x ceil(K/128) x 16 KiB)
  * Summation order of dkv_accum across rows is not deterministic (fp32 atomics).
  */
-size_t dsa_sparse_mla_bwd_workspace_size(int32_t T, int32_t H);
+size_t dsa_sparse_mla_bwd_workspace_size(int32_t T, int32_t H, int32_t K);
 dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
                                 const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
                                 int32_t Dv, int32_t K, float softmax_scale, const dsa_bf16_t* out,
@@ -166,9 +168,10 @@ dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const
  * their own pool and forbid other allocations, or plug-ins whose host program
  * owns every allocation) and so cannot supply the workspace.  Arguments,
  * semantics and results are those of dsa_sparse_mla_bwd.
- *  - Scratch is a fixed 16 MiB + 256 B device array built into the library,
+ *  - Scratch is a fixed 84 MiB + 256 B device array built into the library,
  *    held by every GPU that loads it until the process exits; T * H must not
- *    exceed dsa_sparse_mla_bwd_noalloc_max_rows() (4 Mi), else
+ *    exceed dsa_sparse_mla_bwd_noalloc_max_rows() (4 Mi) and K must not
+ *    exceed dsa_sparse_mla_bwd_noalloc_max_topk() (2176), else
  *    DSA_ERR_WORKSPACE is returned and nothing is launched.
  *  - The call allocates nothing.  The first call on a device looks up the
  *    array's device address (cudaGetSymbolAddress) with that device current;
@@ -178,6 +181,7 @@ dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const
  *    Each call clears the error word and rewrites the D values it reads.
  */
 size_t dsa_sparse_mla_bwd_noalloc_max_rows(void);
+int32_t dsa_sparse_mla_bwd_noalloc_max_topk(void);
 dsa_status_t dsa_sparse_mla_bwd_noalloc(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
                                         const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
                                         int32_t Dv, int32_t K, float softmax_scale, const dsa_bf16_t* out,

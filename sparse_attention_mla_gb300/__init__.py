@@ -92,13 +92,15 @@ def load_library(path: str | None = None):
         lib.dsa_sparse_mla_fwd_workspace_size.argtypes = [_I, _I]
         lib.dsa_sparse_mla_fwd_workspace_size.restype = _SZ
         lib.dsa_sparse_mla_fwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _SZ, _P]
-        lib.dsa_sparse_mla_bwd_workspace_size.argtypes = [_I, _I]
+        lib.dsa_sparse_mla_bwd_workspace_size.argtypes = [_I, _I, _I]
         lib.dsa_sparse_mla_bwd_workspace_size.restype = _SZ
         lib.dsa_sparse_mla_bwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P,
                                            _I, _P, _P, _SZ, _P]
         lib.dsa_read_device_status.argtypes = [_P, _P, _P]
         lib.dsa_sparse_mla_bwd_noalloc_max_rows.restype = _SZ
         lib.dsa_sparse_mla_bwd_noalloc_max_rows.argtypes = []
+        lib.dsa_sparse_mla_bwd_noalloc_max_topk.restype = _I
+        lib.dsa_sparse_mla_bwd_noalloc_max_topk.argtypes = []
         lib.dsa_sparse_mla_bwd_noalloc.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P,
                                                    _P, _I, _P, _P]
         lib.dsa_sparse_mla_bwd_noalloc.restype = ctypes.c_int
@@ -138,15 +140,19 @@ def _need(t, name, dtype, ndim=None, device=None):
         raise ValueError(f"{name} must be contiguous")
 
 
-def workspace_size(kind: str, T: int, H_or_K: int) -> int:
+def workspace_size(kind: str, T: int, H_or_K: int, K: int | None = None) -> int:
+    """Workspace bytes: ("fwd", T, H), ("indexer", T, K) or ("bwd", T, H, K)."""
     lib = load_library()
-    fn = {"fwd": lib.dsa_sparse_mla_fwd_workspace_size, "bwd": lib.dsa_sparse_mla_bwd_workspace_size,
-          "indexer": lib.dsa_indexer_topk_workspace_size}[kind]
+    if kind == "bwd":
+        if K is None:
+            raise ValueError('workspace_size("bwd", T, H, K) needs the top-k width K')
+        return int(lib.dsa_sparse_mla_bwd_workspace_size(int(T), int(H_or_K), int(K)))
+    fn = {"fwd": lib.dsa_sparse_mla_fwd_workspace_size, "indexer": lib.dsa_indexer_topk_workspace_size}[kind]
     return int(fn(int(T), int(H_or_K)))
 
 
-def _workspace(kind, T, x, device, workspace):
-    need = workspace_size(kind, T, x)
+def _workspace(kind, T, x, device, workspace, K=None):
+    need = workspace_size(kind, T, x, K)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
     return workspace, workspace.numel()
@@ -254,7 +260,7 @@ def dsa_sparse_mla_bwd(q, kv, topk_idx, softmax_scale: float, out, lse, dout, to
             raise ValueError("accumulate=True needs an existing dkv_accum")
         dkv_accum = torch.empty(Tk, Dqk, dtype=torch.float32, device=dev)
     _need(dkv_accum, "dkv_accum", torch.float32, 2, dev)
-    ws, wsb = _workspace("bwd", T, H, dev, workspace)
+    ws, wsb = _workspace("bwd", T, H, dev, workspace, K)
     _check(lib.dsa_sparse_mla_bwd(_ptr(q), _ptr(kv), _ptr(topk_idx), _ptr(topk_len), T, Tk, H, Dqk, Dv, K,
                                   float(softmax_scale), _ptr(out), _ptr(out_lo), _ptr(lse), _ptr(dout), _ptr(dq),
                                   _ptr(dkv_accum),

@@ -12,32 +12,38 @@
 // described in "Accelerating GLM-5.2 Long-Context Training with cuDNN Fused
 // DSA Kernels ...", "How DSA works".
 //
-// Design (sm_103a):
+// Design (sm_103a).  The key gradient is scattered into an fp32 accumulator
+// with L2 reductions (red.global.add), one 2304-byte row per selected key and
+// token; those reductions bound the kernel, so everything else is arranged
+// to keep them running back to back:
 //  * P is recomputed from the saved lse (no running max).  D comes from a
 //    small kernel; when the forward's bf16 residual of O is given, D uses the
 //    unrounded O, so that sum_j dS_j = 0 holds to fp32 accuracy.
-//  * All MMAs have M = 128: S^T = KV Q^T and dP^T = V dO^T (keys on M, N = 64
-//    heads), dQ^T += KV^T dS^T (channels on M), dKV = dS^T Q + P^T dO (keys on
-//    M, 32-channel groups).
-//  * Q [64 x Dqk] and dO [64 x 512] stay in shared memory for the token; the
-//    gathered tile streams twice through a 2-slot ring of 128-channel pairs
-//    (once for S^T / dP^T, once for dQ^T).  The gather is 16-byte cp.async
-//    issued by the 256 worker threads.
-//  * dS (x scale) and P are split into bf16 hi + lo parts so that dkv is
-//    accurate to about fp32 even for keys shared by many rows.  dS hi sits in
-//    shared memory (B operand of dQ^T, A operand of dS^T Q); dS lo, P hi and
-//    P lo are written into TMEM over the thread's own S^T / dP^T columns and
-//    are A operands of the dKV products.
-//  * dKV of a tile is produced 64 channels at a time into one TMEM staging
-//    buffer and flushed by the workers with red.global.add.v4.f32 on the
-//    gathered rows of the fp32 accumulator (reductions in L2).  While the
-//    tensor core works on dKV, the workers have already issued the gather of
-//    the next tile's first channel pairs.
+//  * Main loop, per 128-slot tile: S^T = KV Q^T and dP^T = V dO^T (keys on
+//    the MMA M axis, N = 64 heads) into one of TWO TMEM buffers; the softmax
+//    backward turns them, in place, into dS (x scale) and P, each split into
+//    bf16 hi + lo parts (dkv accurate to about fp32 even for keys shared by
+//    many rows); dKV = dS^T Q + P^T dO is then formed 64 channels at a time
+//    with all four A operands read from TMEM, into one of FOUR TMEM staging
+//    slots that the flush warps drain into L2 reductions.  With two S/dP
+//    buffers and four staging slots, the next tile's S^T / dP^T and softmax
+//    run while the reductions of this tile are still in flight.
+//  * dq needs dS for every tile of the token but the main loop has no TMEM
+//    left for its accumulator, so dS hi of each tile is also written to a
+//    per-SM scratch in global memory (L2-resident) and dQ^T = KV^T dS^T is
+//    formed in an end phase per token, when Q and dO are dead and their
+//    shared memory becomes a deep gather ring.
+//  * The gathered rows stream through shared memory in 64-channel chunks
+//    (128-byte swizzle) loaded by 16-byte cp.async (zero-fill for invalid or
+//    beyond-prefix rows).
+//  * One thread issues every MMA.  It polls its inputs (ring chunks landed,
+//    dS ready, staging slot free, buffer free) and issues whichever unit of
+//    work is ready, dKV groups first, so that the tensor core follows the
+//    reductions instead of a fixed program order.
 //
-// Warp roles (4 warpgroups): warp 0 issues MMAs (one thread) and owns TMEM;
-// warpgroups 1-2 gather, run the softmax backward and write dq; warpgroup 3
-// copies each dKV group out of TMEM, releases it and issues the L2
-// reductions, so that the reductions overlap everything else.
+// Warp roles: warp 0 issues MMAs and owns TMEM; warps 1-3 gather; warps 4-11
+// run the softmax backward and the dq epilogue; warps 12-15 drain the dKV
+// staging slots into L2 reductions.
 #include <cmath>
 
 #include "dsa_device.cuh"
@@ -46,41 +52,56 @@
 namespace dsa {
 namespace bwd {
 
-constexpr int kThreads = 512;  // 4 warpgroups: MMA / math / math / flush
-constexpr int kMath = 256;    // math threads (warpgroups 1 and 2)
-constexpr int kTile = 128;
-constexpr int kHeads = 64;
+constexpr int kThreads = 512;
+constexpr int kGather = 96;    // warps 1-3
+constexpr int kMath = 256;     // warps 4-11
+constexpr int kTile = 128;     // top-k slots per tile (MMA M)
+constexpr int kHeads = 64;     // heads per CTA (MMA N)
 constexpr int kDv = 512;
-constexpr int kGroup = 64;  // dKV channels per staging group (one 64-channel chunk)
+constexpr int kGroup = 128;    // dKV channels per staging slot (MMA N)
+constexpr int kRing = 5;       // main-loop ring: 16 KiB chunk slots
+constexpr int kERing = 6;      // end-phase ring: 32 KiB slots (a dS tile or a 128-channel pair)
+constexpr int kStage = 2;      // dKV staging slots
+constexpr int kMaxSmSlots = 256;                  // dS scratch slots, indexed by SM id
+constexpr int kDsTileBytes = kTile * kHeads * 2;  // bf16 dS of one tile: 16 KiB
+constexpr int kUnits = kTile * 8;                 // 16-byte units of one 64-channel chunk
 
 template <int DQK>
 struct Smem {
-  static constexpr int NCH = DQK / 64;         // channel chunks of kv / q
-  static constexpr int NP = (NCH + 1) / 2;     // channel pairs (128 channels)
-  static constexpr int NG = DQK / kGroup;      // dKV groups
-  static constexpr int Q_CHUNK = kHeads * 128; // 8 KiB
-  static constexpr int KV_CHUNK = kTile * 128; // 16 KiB
-  static constexpr int SLOT = 2 * KV_CHUNK;    // ring slot: one pair
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_DO = OFF_Q + NCH * Q_CHUNK;
-  static constexpr int OFF_RING = OFF_DO + 8 * Q_CHUNK;
-  static constexpr int OFF_DS = OFF_RING + 2 * SLOT;
-  static constexpr int OFF_MISC = OFF_DS + KV_CHUNK;
+  static constexpr int NCH = DQK / 64;          // channel chunks of kv / q
+  static constexpr int NP = (NCH + 1) / 2;      // channel pairs (128 channels)
+  static constexpr int NG = (DQK + kGroup - 1) / kGroup;  // dKV groups (the last may be 64 channels)
+  static constexpr int Q_CHUNK = kHeads * 128;  // 8 KiB: 64 heads x 64 channels
+  static constexpr int QDO = 2 * Q_CHUNK;       // chunk c of Q followed by chunk c of dO
+  static constexpr int KV_CHUNK = kTile * 128;  // 16 KiB
+  static constexpr int ESLOT = 2 * KV_CHUNK;    // end-phase slot
+  // Q and dO, chunk-interleaved: [Q_0 dO_0][Q_1 dO_1]...[Q_7 dO_7][Q_8].  One K-major
+  // operand of N = 128 rows then covers the 64 heads of Q_c and of dO_c, so that a
+  // single MMA forms S^T and dP^T; two consecutive chunks of Q (or of dO) form an
+  // MN-major operand of N = 128 channels with LBO = QDO.
+  static constexpr int OFF_QDO = 0;
+  static constexpr int OFF_RING = OFF_QDO + 8 * QDO + (NCH - 8) * Q_CHUNK;
+  static constexpr int OFF_FST = OFF_RING + kRing * KV_CHUNK;  // flush transposes: 4 warps x 16 rows x 128 B
+  static constexpr int OFF_MISC = OFF_FST + 4 * 2048;
   static constexpr int MISC = 1024;
-  static constexpr int OFF_FST = OFF_MISC + MISC;  // flush transpose buffers: 4 warps x 32 rows x 64 B
-  static constexpr int TOTAL = OFF_FST + 4 * 2048 + 1024;
+  static constexpr int TOTAL = OFF_MISC + MISC + 1024;  // + alignment slack
+  static constexpr int OFF_ERING = 0;                   // end phase: over Q, dO and the main ring
   static_assert(TOTAL <= 232448, "shared memory budget");
-  static_assert(2 * SLOT + KV_CHUNK >= kHeads * DQK * 2, "dq staging fits ring + dS");
+  static_assert(kERing * ESLOT <= OFF_FST, "end-phase ring fits below the flush buffers");
+  static_assert(kHeads * DQK * 2 <= OFF_FST, "dq staging fits below the flush buffers");
 };
 
-// misc layout
-constexpr int M_FULL = 0, M_EMPTY = 16, M_SDP = 32, M_DS = 40, M_STF = 48, M_STE = 64, M_DQ = 80, M_KVD = 88,
-              M_FIN = 96;
-constexpr int M_TMEM = 128, M_NEFF = 132, M_ABORT = 136;
-constexpr int M_LSE = 256, M_DL = 512;  // float [64] each
+// misc layout: mbarriers (8 bytes each), then scalars and per-head vectors
+constexpr int B_FULL = 0, B_EMPTY = 5, B_EFULL = 10, B_EEMPTY = 16, B_SDP = 22, B_DS = 24, B_KVD = 26, B_STF = 28,
+              B_STE = 32, B_DSDONE = 36, B_ENDGO = 37, B_DQ = 38, B_FIN = 39, B_COUNT = 40;
+constexpr int M_TMEM = 384, M_NEFF = 388, M_ABORT = 392;
+constexpr int M_LSE = 512, M_DL = 768;  // float [64] each
+static_assert(B_COUNT * 8 <= M_TMEM, "barriers fit");
 
-// TMEM columns: dQ^T (5 x 64), S^T, dP^T, dKV staging (64)
-constexpr uint32_t C_DQ = 0, C_S = 320, C_DP = 384, C_STG = 448;
+// TMEM columns.  Main loop: buffer b holds S^T at 128b and dP^T at 128b + 64;
+// staging slot s at 256 + 128s.  End phase: dQ^T channel tile p at 64p.
+constexpr uint32_t C_BUF = 128, C_STG = 256;
+static_assert(C_STG + kStage * kGroup <= 512, "TMEM budget");
 
 // D[t,h] = <dO[t,h,:], O[t,h,:] (+ O_lo[t,h,:])> in fp32; one warp per (t, h).
 __global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ out_lo,
@@ -122,27 +143,41 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16*
   }
 }
 
-// Gather channel pair p of the tile into a ring slot (see the forward's
-// gather: 16-byte units, zero-fill for invalid / beyond-prefix rows).
-template <int DQK>
-__device__ __forceinline__ void gather_pair(uint32_t slot, const __nv_bfloat16* __restrict__ kv, int p, int tid,
-                                            const int (&rix)[4], uint32_t bar) {
-  constexpr int NCH = DQK / 64;
-  const int uc = tid & 7;
+// One thread's share of gathering a tile's rows, 64 channels at a time, with
+// NT threads: per unit (row, 16-byte column) the source pointer of channel 0
+// and the swizzled destination offset are computed once per tile, so that a
+// chunk costs one cp.async per unit.  Invalid or beyond-prefix rows are
+// zero-filled (src-size 0; the pointer stays inside kv and is not read).
+template <int DQK, int NT>
+struct TileGather {
+  static constexpr int KU = (kUnits + NT - 1) / NT;
+  const __nv_bfloat16* src[KU];
+  uint32_t dst[KU];
+  uint32_t okm;
+  __device__ __forceinline__ void rows(const __nv_bfloat16* __restrict__ kv, const int32_t* __restrict__ idx_row,
+                                       int i, int n_eff, int Tk, int et, int* err) {
+    okm = 0;
 #pragma unroll
-  for (int cc = 0; cc < 2; ++cc) {
-    const int c = 2 * p + cc;
-    if (c >= NCH) break;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int r = (tid >> 3) + 32 * e;
-      const bool ok = rix[e] >= 0;
-      const __nv_bfloat16* src = kv + (ok ? (size_t)rix[e] * DQK + c * 64 + uc * 8 : 0);
-      cp_async16(slot + cc * (kTile * 128) + sw128_off(r, uc), src, ok ? 16u : 0u);
+    for (int k = 0; k < KU; ++k) {
+      const int u = et + NT * k;
+      const int j = i * kTile + (u >> 3);
+      int v = -1;
+      if (u < kUnits && j < n_eff) {
+        const int ix = __ldg(idx_row + j);
+        v = (ix >= 0 && ix < Tk) ? ix : -1;
+        if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
+      }
+      src[k] = kv + (v >= 0 ? (size_t)v * DQK : 0) + (u & 7) * 8;
+      dst[k] = sw128_off((u >> 3) & (kTile - 1), u & 7);
+      okm |= (v >= 0 ? 1u : 0u) << k;
     }
   }
-  cp_async_arrive(bar);
-}
+  __device__ __forceinline__ void chunk(uint32_t base, int c, int et) const {
+#pragma unroll
+    for (int k = 0; k < KU; ++k)
+      if (et + NT * k < kUnits) cp_async16(base + dst[k], src[k] + c * 64, ((okm >> k) & 1u) ? 16u : 0u);
+  }
+};
 
 template <int DQK>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -150,22 +185,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ topk_len,
                           const float* __restrict__ lse, const float* __restrict__ delta,
                           const __nv_bfloat16* __restrict__ dout, int T, int Tk, int H, int K, float scale,
-                          __nv_bfloat16* __restrict__ dq, float* __restrict__ dkv, int* __restrict__ err) {
+                          __nv_bfloat16* __restrict__ dq, float* __restrict__ dkv, uint8_t* __restrict__ ds_scratch,
+                          int tiles_per_slot, int* __restrict__ err) {
   using L = Smem<DQK>;
   constexpr int NCH = L::NCH;
   constexpr int NP = L::NP;
   constexpr int NG = L::NG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sQ = smem_u32(smem + L::OFF_Q);
-  const uint32_t sDO = smem_u32(smem + L::OFF_DO);
+  const uint32_t sQDO = smem_u32(smem + L::OFF_QDO);
   const uint32_t sRing = smem_u32(smem + L::OFF_RING);
-  const uint32_t sDS = smem_u32(smem + L::OFF_DS);
+  const uint32_t sERing = smem_u32(smem + L::OFF_ERING);
   uint8_t* misc = smem + L::OFF_MISC;
-  const uint32_t bar_full = smem_u32(misc + M_FULL), bar_empty = smem_u32(misc + M_EMPTY);
-  const uint32_t bar_sdp = smem_u32(misc + M_SDP), bar_ds = smem_u32(misc + M_DS);
-  const uint32_t bar_stf = smem_u32(misc + M_STF), bar_ste = smem_u32(misc + M_STE);
-  const uint32_t bar_dq = smem_u32(misc + M_DQ), bar_kvd = smem_u32(misc + M_KVD), bar_fin = smem_u32(misc + M_FIN);
+  const uint32_t bars = smem_u32(misc);
+  auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + M_TMEM);
   int* s_neff = reinterpret_cast<int*>(misc + M_NEFF);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + M_ABORT);
@@ -176,22 +209,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hg = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t* idx_row = topk_idx + (size_t)t * K;
-  const bool is_math = warp >= 4 && warp < 12;   // warpgroups 1, 2
-  const bool is_flush = warp >= 12;              // warpgroup 3
-  const int tid = threadIdx.x - 128;             // math thread id 0..255
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar_full + 8 * s, kMath);
-      mbar_init(bar_empty + 8 * s, 1);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(bar(B_FULL + i), kGather);
+      mbar_init(bar(B_EMPTY + i), 1);
     }
-    mbar_init(bar_stf, 1);
-    mbar_init(bar_ste, 4);
-    mbar_init(bar_sdp, 1);
-    mbar_init(bar_ds, 8);
-    mbar_init(bar_dq, 1);
-    mbar_init(bar_kvd, 1);
-    mbar_init(bar_fin, 1);
+    for (int i = 0; i < kERing; ++i) {
+      mbar_init(bar(B_EFULL + i), kGather + kMath);  // the math warps join the end-phase gathers
+      mbar_init(bar(B_EEMPTY + i), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_SDP + b), 1);
+      mbar_init(bar(B_DS + b), kMath / 32);
+      mbar_init(bar(B_KVD + b), 1);
+    }
+    for (int s = 0; s < kStage; ++s) {
+      mbar_init(bar(B_STF + s), 1);
+      mbar_init(bar(B_STE + s), 4);
+    }
+    mbar_init(bar(B_DSDONE), kMath);
+    mbar_init(bar(B_ENDGO), 1);
+    mbar_init(bar(B_DQ), 1);
+    mbar_init(bar(B_FIN), 1);
     *s_neff = 0;
     *s_abort = 0;
     fence_mbar_init();
@@ -202,7 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
+  const bool is_gather = warp >= 1 && warp < 4;
+  const bool is_math = warp >= 4 && warp < 12;
+  const bool is_flush = warp >= 12;
   if (is_math) {
+    const int tid = threadIdx.x - 128;
     if (topk_len != nullptr) {
       if (tid == 0) {
         int n = topk_len[t];
@@ -220,14 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int h = hg * kHeads + hh;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (h < H) v = __ldg(reinterpret_cast<const uint4*>(q + ((size_t)t * H + h) * DQK + c * 64 + uc * 8));
-      st_shared_v4(sQ + c * L::Q_CHUNK + sw128_off(hh, uc), v.x, v.y, v.z, v.w);
+      st_shared_v4(sQDO + c * L::QDO + sw128_off(hh, uc), v.x, v.y, v.z, v.w);
     }
     for (int u = tid; u < kHeads * 8 * 8; u += kMath) {
       const int hh = u >> 6, rem = u & 63, c = rem >> 3, uc = rem & 7;
       const int h = hg * kHeads + hh;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (h < H) v = __ldg(reinterpret_cast<const uint4*>(dout + ((size_t)t * H + h) * kDv + c * 64 + uc * 8));
-      st_shared_v4(sDO + c * L::Q_CHUNK + sw128_off(hh, uc), v.x, v.y, v.z, v.w);
+      st_shared_v4(sQDO + c * L::QDO + L::Q_CHUNK + sw128_off(hh, uc), v.x, v.y, v.z, v.w);
     }
     // per-head lse (log2 units) and D, shared by every key row
     if (tid < kHeads) {
@@ -238,92 +282,207 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
   }
   __syncthreads();
+  int ntiles = (*s_neff + kTile - 1) / kTile;
   const int n_eff = *s_neff;
-  const int ntiles = (n_eff + kTile - 1) / kTile;
   const uint32_t tmem = *s_tmem;
+  // this SM's dS scratch (one CTA per SM at a time: the shared-memory footprint admits no second)
+  const uint32_t smid = sm_id();
+  if (smid >= (uint32_t)kMaxSmSlots || ntiles > tiles_per_slot) {
+    if (threadIdx.x == 0) record_error(err, DSA_ERR_UNSUPPORTED);
+    ntiles = 0;
+  }
+  uint8_t* ds_slot = ds_scratch + (size_t)smid * tiles_per_slot * kDsTileBytes;
 
-  if (warp < 4) {
-    if (warp == 0 && lane == 0) {
-      // ======================= MMA issuer =======================
-      constexpr uint32_t kIdKK = idesc_bf16(128, 64, false, false);      // S^T, dP^T
-      constexpr uint32_t kIdMM = idesc_bf16(128, 64, true, true);        // dQ^T
-      constexpr uint32_t kIdKM = idesc_bf16(128, kGroup, false, true);   // dKV: A (smem/TMEM) x B MN-major
-      int L_cnt = 0, G = 0;
-      bool stop = false;
-      for (int i = 0; i < ntiles && !stop; ++i) {
-        if (i > 0) {  // the previous tile's dKV reads its A operands from the S^T / dP^T columns
-          if (!mbar_wait(bar_kvd, (i - 1) & 1, s_abort, err)) break;
-        }
-        // ---- pass A: S^T = KV Q^T, dP^T = V dO^T ----
-        for (int p = 0; p < NP; ++p, ++L_cnt) {
-          const int slot = L_cnt & 1;
-          if (!mbar_wait(bar_full + 8 * slot, (L_cnt >> 1) & 1, s_abort, err)) { stop = true; break; }
-          fence_proxy_async_smem();
-          tc_fence_after();
-          for (int cc = 0; cc < 2; ++cc) {
-            const int c = 2 * p + cc;
-            if (c >= NCH) break;
-            const uint32_t a0 = sRing + slot * L::SLOT + cc * L::KV_CHUNK;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ss(tmem + C_S, sdesc_sw128(a0 + k * 32, 16, 1024), sdesc_sw128(sQ + c * L::Q_CHUNK + k * 32, 16, 1024),
-                     kIdKK, (c | k) != 0);
-            if (c < 8) {
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_ss(tmem + C_DP, sdesc_sw128(a0 + k * 32, 16, 1024),
-                       sdesc_sw128(sDO + c * L::Q_CHUNK + k * 32, 16, 1024), kIdKK, (c | k) != 0);
-            }
-          }
-          mma_commit(bar_empty + 8 * slot);
-        }
-        if (stop) break;
-        mma_commit(bar_sdp);
-        if (!mbar_wait(bar_ds, i & 1, s_abort, err)) break;
-        tc_fence_after();
-        // ---- pass B: dQ^T[pair p] += KV^T dS^T ----
-        for (int p = 0; p < NP; ++p, ++L_cnt) {
-          const int slot = L_cnt & 1;
-          if (!mbar_wait(bar_full + 8 * slot, (L_cnt >> 1) & 1, s_abort, err)) { stop = true; break; }
-          fence_proxy_async_smem();
-          tc_fence_after();
-          const uint32_t a0 = sRing + slot * L::SLOT;
-#pragma unroll
-          for (int k = 0; k < kTile / 16; ++k)
-            mma_ss(tmem + C_DQ + p * 64, sdesc_sw128(a0 + k * 2048, L::KV_CHUNK, 1024),
-                   sdesc_sw128(sDS + k * 2048, L::KV_CHUNK, 1024), kIdMM, (i > 0 || k > 0) ? 1u : 0u);
-          mma_commit(bar_empty + 8 * slot);
-        }
-        if (stop) break;
-        // ---- dKV = (dS_hi + dS_lo)^T Q + (P_hi + P_lo)^T dO, one 64-channel chunk at a time ----
-        for (int g = 0; g < NG; ++g, ++G) {
-          if (!mbar_wait(bar_ste, (G & 1) ^ 1, s_abort, err)) { stop = true; break; }
-          tc_fence_after();
-          const uint32_t d = tmem + C_STG;
-          const uint32_t qb = sQ + g * L::Q_CHUNK;
-          const uint32_t ob = sDO + g * L::Q_CHUNK;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t acol = (k >> 1) * 32 + (k & 1) * 8;  // heads 16k..16k+15 of a thread-half region
-            const uint64_t bq = sdesc_sw128(qb + k * 2048, 16, 1024);
-            mma_ss(d, sdesc_sw128(sDS + k * 32, 16, 1024), bq, kIdKM, k > 0);  // dS hi (shared memory)
-            mma_ts(d, tmem + C_S + acol, bq, kIdKM, 1u);                      // dS lo
-            if (g < 8) {
-              const uint64_t bo = sdesc_sw128(ob + k * 2048, 16, 1024);
-              mma_ts(d, tmem + C_DP + acol, bo, kIdKM, 1u);                   // P hi
-              mma_ts(d, tmem + C_DP + 16 + acol, bo, kIdKM, 1u);              // P lo
-            }
-          }
-          mma_commit(bar_stf);
-        }
-        mma_commit(bar_kvd);
+  // End-phase gathers, shared by the gather and the math warps (et = 0..351):
+  // per tile the swizzled dS image from the scratch, then the channel pairs.
+  auto end_gathers = [&](int et) {
+    constexpr int NT = kGather + kMath;
+    if (!mbar_wait(bar(B_ENDGO), 0, s_abort, err) || !mbar_wait(bar(B_DSDONE), 0, s_abort, err)) return;
+    TileGather<DQK, NT> tg;
+    int Le = 0;
+    for (int i = 0; i < ntiles; ++i) {
+      int slot = Le % kERing;
+      if (Le >= kERing && !mbar_wait(bar(B_EEMPTY + slot), ((Le / kERing) - 1) & 1, s_abort, err)) return;
+      const uint8_t* src = ds_slot + (size_t)i * kDsTileBytes;
+      for (int u = et; u < kDsTileBytes / 16; u += NT) cp_async16(sERing + slot * L::ESLOT + 16 * u, src + 16 * u, 16u);
+      cp_async_arrive(bar(B_EFULL + slot));
+      ++Le;
+      tg.rows(kv, idx_row, i, n_eff, Tk, et, err);
+      for (int p = 0; p < NP; ++p, ++Le) {
+        slot = Le % kERing;
+        if (Le >= kERing && !mbar_wait(bar(B_EEMPTY + slot), ((Le / kERing) - 1) & 1, s_abort, err)) return;
+        tg.chunk(sERing + slot * L::ESLOT, 2 * p, et);
+        if (2 * p + 1 < NCH) tg.chunk(sERing + slot * L::ESLOT + L::KV_CHUNK, 2 * p + 1, et);
+        cp_async_arrive(bar(B_EFULL + slot));
       }
-      mma_commit(bar_dq);
-      mma_commit(bar_fin);
+    }
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ======================= MMA issuer =======================
+      constexpr uint32_t kIdSP = idesc_bf16(128, 128, false, false);  // [S^T | dP^T] = KV [Q | dO]^T
+      constexpr uint32_t kIdS = idesc_bf16(128, 64, false, false);    // S^T only (RoPE chunk)
+      constexpr uint32_t kIdMM = idesc_bf16(128, 64, true, true);     // dQ^T
+      constexpr uint32_t kIdKM = idesc_bf16(128, 128, false, true);   // dKV, 128 channels: A (TMEM) x B MN-major
+      constexpr uint32_t kIdKM64 = idesc_bf16(128, 64, false, true);  // dKV, last 64 channels
+      int ia = 0, ca = 0, La = 0;  // S^T / dP^T stream: next (tile, chunk), ring item
+      int id = 0, gd = 0, G = 0;   // dKV stream: next (tile, group), staging item
+      bool ds_seen = false, buf_seen = false, idle = false, stop = false;
+      long long idle_t0 = 0;
+      while (id < ntiles) {
+        bool progressed = false;
+        // ---- dKV group gd of tile id: needs dS/P of tile id in TMEM and a free staging slot ----
+        if (id < ia) {
+          if (!ds_seen) ds_seen = mbar_test(bar(B_DS + (id & 1)), (id >> 1) & 1);
+          const int s = G & (kStage - 1), n = G / kStage;
+          if (ds_seen && (n == 0 || mbar_test(bar(B_STE + s), (n - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t bS = tmem + C_BUF * (id & 1), bP = bS + 64;
+            const uint32_t d = tmem + C_STG + kGroup * s;
+            const uint32_t qb = sQDO + 2 * gd * L::QDO;  // chunks 2gd, 2gd+1 of Q (and of dO at + Q_CHUNK)
+            if (gd * kGroup + kGroup <= DQK) {
+              const uint64_t bq0 = sdesc_sw128(qb, L::QDO, 1024), bo0 = sdesc_sw128(qb + L::Q_CHUNK, L::QDO, 1024);
+              const bool with_p = gd * kGroup + kGroup <= kDv;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint32_t acol = (k >> 1) * 32 + (k & 1) * 8;  // heads 16k..16k+15 in a thread-half region
+                const uint64_t bq = bq0 + (uint64_t)(k * 128), bo = bo0 + (uint64_t)(k * 128);  // + 16 head rows
+                mma_ts(d, bS + 16 + acol, bq, kIdKM, k > 0);  // dS hi
+                mma_ts(d, bS + acol, bq, kIdKM, 1u);          // dS lo
+                if (with_p) {
+                  mma_ts(d, bP + acol, bo, kIdKM, 1u);        // P hi
+                  mma_ts(d, bP + 16 + acol, bo, kIdKM, 1u);   // P lo
+                }
+              }
+            } else {  // the RoPE channels 512..575: dS terms only
+              const uint64_t bq0 = sdesc_sw128(qb, 16, 1024);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint32_t acol = (k >> 1) * 32 + (k & 1) * 8;
+                const uint64_t bq = bq0 + (uint64_t)(k * 128);
+                mma_ts(d, bS + 16 + acol, bq, kIdKM64, k > 0);
+                mma_ts(d, bS + acol, bq, kIdKM64, 1u);
+              }
+            }
+            mma_commit(bar(B_STF + s));
+            ++G;
+            progressed = true;
+            if (++gd == NG) {
+              mma_commit(bar(B_KVD + (id & 1)));  // buffer id & 1 may be overwritten once this lands
+              gd = 0;
+              ++id;
+              ds_seen = false;
+            }
+          }
+        }
+        // ---- chunk ca of tile ia: S^T (+ dP^T) into buffer ia & 1 ----
+        if (ia < ntiles) {
+          if (!buf_seen) buf_seen = (ia < 2) || mbar_test(bar(B_KVD + (ia & 1)), ((ia - 2) >> 1) & 1);
+          const int slot = La % kRing;
+          if (buf_seen && mbar_test(bar(B_FULL + slot), (La / kRing) & 1)) {
+            fence_proxy_async_smem();  // cp.async landings -> visible to the tensor core
+            tc_fence_after();
+            const uint32_t bS = tmem + C_BUF * (ia & 1);
+            const uint64_t a0 = sdesc_sw128(sRing + slot * L::KV_CHUNK, 16, 1024);
+            const uint64_t b0 = sdesc_sw128(sQDO + ca * L::QDO, 16, 1024);  // rows: 64 heads of Q_c, then of dO_c
+            const uint32_t idn = (ca < 8) ? kIdSP : kIdS;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // + 16 channels = + 32 bytes per row
+              mma_ss(bS, a0 + (uint64_t)(k * 2), b0 + (uint64_t)(k * 2), idn, (ca | k) != 0);
+            mma_commit(bar(B_EMPTY + slot));
+            ++La;
+            progressed = true;
+            if (++ca == NCH) {
+              mma_commit(bar(B_SDP + (ia & 1)));
+              ca = 0;
+              ++ia;
+              buf_seen = false;
+            }
+          }
+        }
+        if (progressed) {
+          idle = false;
+          continue;
+        }
+        __nanosleep(32);  // leave the issue slots to the math and flush warps of this sub-partition
+        if (!idle) {
+          idle = true;
+          idle_t0 = clock64();
+        } else if (*s_abort) {
+          stop = true;
+          break;
+        } else if (clock64() - idle_t0 > kWaitLimitCycles) {
+          *s_abort = 1;
+          record_error(err, DSA_ERR_TIMEOUT);
+          stop = true;
+          break;
+        }
+      }
+      // ---- end phase: dQ^T[pair p] += KV^T dS^T over every tile of the token ----
+      if (!stop && ntiles > 0) {
+        // every dKV MMA has landed: Q, dO, the main ring and the S/dP buffers are dead
+        stop = !mbar_wait(bar(B_KVD + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, s_abort, err);
+        if (!stop) mbar_arrive(bar(B_ENDGO));
+        // the rope tile of dQ^T overlaps staging slot 0: wait for its last drain
+        bool rope_free = (NP * 64 <= (int)C_STG);
+        const int uses0 = (G + kStage - 1) / kStage;
+        int Le = 0;
+        for (int i = 0; i < ntiles && !stop; ++i) {
+          const int sds = Le % kERing;
+          if (!mbar_wait(bar(B_EFULL + sds), (Le / kERing) & 1, s_abort, err)) { stop = true; break; }
+          const uint32_t dsb = sERing + sds * L::ESLOT;
+          ++Le;
+          for (int p = 0; p < NP; ++p, ++Le) {
+            const int sl = Le % kERing;
+            if (!mbar_wait(bar(B_EFULL + sl), (Le / kERing) & 1, s_abort, err)) { stop = true; break; }
+            if (p * 64 + 64 > (int)C_STG && !rope_free) {
+              if (uses0 > 0 && !mbar_wait(bar(B_STE), (uses0 - 1) & 1, s_abort, err)) { stop = true; break; }
+              rope_free = true;
+            }
+            fence_proxy_async_smem();
+            tc_fence_after();
+            const uint64_t a0 = sdesc_sw128(sERing + sl * L::ESLOT, L::KV_CHUNK, 1024);
+            const uint64_t b0 = sdesc_sw128(dsb, L::KV_CHUNK, 1024);
+#pragma unroll
+            for (int k = 0; k < kTile / 16; ++k)  // + 16 key rows = + 2048 bytes
+              mma_ss(tmem + 64 * p, a0 + (uint64_t)(k * 128), b0 + (uint64_t)(k * 128), kIdMM, (i > 0 || k > 0) ? 1u : 0u);
+            mma_commit(bar(B_EEMPTY + sl));
+          }
+          if (stop) break;
+          mma_commit(bar(B_EEMPTY + sds));
+        }
+      }
+      if (stop) *s_abort = 1;
+      mma_commit(bar(B_DQ));
+      // every MMA of this CTA completes before the teardown frees TMEM
+      mma_commit(bar(B_FIN));
       volatile int dummy = 0;
-      mbar_wait(bar_fin, 0, &dummy, err);
+      mbar_wait(bar(B_FIN), 0, &dummy, err);
     }
     __syncwarp();
+  } else if (is_gather) {
+    // ======================= gathers (cp.async, 16-byte units) =======================
+    const int gt = threadIdx.x - 32;  // 0..95
+    TileGather<DQK, kGather> tg;
+    bool aborted = false;
+    int La = 0;
+    for (int i = 0; i < ntiles && !aborted; ++i) {
+      tg.rows(kv, idx_row, i, n_eff, Tk, gt, err);
+      for (int c = 0; c < NCH; ++c, ++La) {
+        const int slot = La % kRing;
+        if (La >= kRing && !mbar_wait(bar(B_EMPTY + slot), ((La / kRing) - 1) & 1, s_abort, err)) {
+          aborted = true;
+          break;
+        }
+        tg.chunk(sRing + slot * L::KV_CHUNK, c, gt);
+        cp_async_arrive(bar(B_FULL + slot));
+      }
+    }
+    // the end phase overwrites Q, dO and the main ring, and reads the dS scratch
+    if (!aborted && ntiles > 0) end_gathers(gt);
+    // no copy may still be landing in this CTA's shared memory when it exits
+    asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (is_flush) {
     // ======================= dKV flush: TMEM staging -> registers -> L2 reductions =======================
     const int qd = warp & 3;
@@ -334,89 +493,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = i * kTile + r;
       int ix = -1;
       if (j < n_eff) ix = __ldg(idx_row + j);
-      const bool valid = ix >= 0 && ix < Tk;
+      if (!(ix >= 0 && ix < Tk)) ix = -1;
       bool stop = false;
       for (int g = 0; g < NG; ++g, ++G) {
-        if (!mbar_wait(bar_stf, G & 1, s_abort, err)) { stop = true; break; }
+        const int s = G & (kStage - 1), n = G / kStage;
+        if (!mbar_wait(bar(B_STF + s), n & 1, s_abort, err)) { stop = true; break; }
         tc_fence_after();
-        uint32_t v[4][16];
+        const int halves = (g * kGroup + kGroup <= DQK) ? 2 : 1;
+        for (int hf = 0; hf < halves; ++hf) {
+          uint32_t v[4][16];
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) tmem_ld16(tmem_addr(tmem + C_STG + 16 * qq, qd * 32, 0), v[qq]);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_ste);  // staging free: the next group's MMAs may start
-        // Transpose 16 channels at a time through this warp's 2 KB buffer so that 4
-        // lanes cover one row's 64 contiguous bytes: each reduction instruction then
-        // touches 8 rows x 64 B instead of 32 rows x 16 B.
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            st_shared_v4(fst + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4), v[qq][4 * k], v[qq][4 * k + 1],
-                         v[qq][4 * k + 2], v[qq][4 * k + 3]);
-          __syncwarp();
-#pragma unroll
-          for (int st = 0; st < 4; ++st) {
-            const int rl = 8 * st + (lane >> 2), u = lane & 3;
-            const int ixr = __shfl_sync(0xffffffffu, valid ? ix : -1, rl);
-            float4 f;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
-                         : "r"(fst + rl * 64 + ((u ^ ((rl >> 1) & 3)) << 4))
-                         : "memory");
-            if (ixr >= 0) red_add_v4(dkv + (size_t)ixr * DQK + g * kGroup + 16 * qq + 4 * u, f.x, f.y, f.z, f.w);
+          for (int qq = 0; qq < 4; ++qq)
+            tmem_ld16(tmem_addr(tmem + C_STG + kGroup * s + 64 * hf + 16 * qq, qd * 32, 0), v[qq]);
+          tmem_ld_wait();
+          if (hf == halves - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_STE + s));  // the slot may be refilled
           }
-          __syncwarp();
+          float* dst_row = dkv + g * kGroup + 64 * hf;
+          // Transpose through this warp's 2 KB buffer, 16 rows x 32 channels at a time, so
+          // that 8 lanes cover one row's 128 contiguous bytes: each reduction instruction
+          // then touches 4 rows x 128 B.
+#pragma unroll
+          for (int bc = 0; bc < 2; ++bc) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              if ((lane >> 4) == hh) {
+                const int rl = lane & 15;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  const uint32_t(&w)[16] = v[2 * bc + (u >> 2)];
+                  st_shared_v4(fst + rl * 128 + ((u ^ (rl & 7)) << 4), w[4 * (u & 3)], w[4 * (u & 3) + 1],
+                               w[4 * (u & 3) + 2], w[4 * (u & 3) + 3]);
+                }
+              }
+              __syncwarp();
+#pragma unroll
+              for (int st = 0; st < 4; ++st) {
+                const int rl = 4 * st + (lane >> 3), u = lane & 7;
+                const int ixr = __shfl_sync(0xffffffffu, ix, 16 * hh + rl);
+                float4 f;
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+                             : "r"(fst + rl * 128 + ((u ^ (rl & 7)) << 4))
+                             : "memory");
+                if (ixr >= 0) red_add_v4(dst_row + (size_t)ixr * DQK + 32 * bc + 4 * u, f.x, f.y, f.z, f.w);
+              }
+              __syncwarp();
+            }
+          }
         }
       }
       if (stop) break;
     }
   } else {
-    // ======================= math warps: gather, softmax backward, dq epilogue =======================
-    const int mw = warp - 4;          // 0..7
+    // ======================= math warps: softmax backward, dS scratch, dq epilogue =======================
+    const int mw = warp - 4;  // 0..7
     const int qd = warp & 3;
-    const int ch = mw >> 2;           // heads ch*32 .. ch*32+31
-    const int r = qd * 32 + lane;     // key row of the tile
-    const int bar_id = 1 + ch;
+    const int ch = mw >> 2;        // heads ch*32 .. ch*32+31
+    const int r = qd * 32 + lane;  // key row of the tile
     const float sl2e = scale * 1.4426950408889634f;
     const float* lse2 = s_lse2 + ch * 32;
     const float* dl = s_dl + ch * 32;
-    auto load_rows = [&](int i, int (&rix)[4]) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = i * kTile + (tid >> 3) + 32 * e;
-        int v = -1;
-        if (j < n_eff) {
-          const int ix = __ldg(idx_row + j);
-          v = (ix >= 0 && ix < Tk) ? ix : -1;
-          if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
-        }
-        rix[e] = v;
-      }
-    };
-    int L_cnt = 0;
     bool aborted = false;
-    auto gather_pairs = [&](const int (&rix)[4], int p0, int p1) {
-      for (int p = p0; p < p1; ++p, ++L_cnt) {
-        const int slot = L_cnt & 1;
-        if (!mbar_wait(bar_empty + 8 * slot, ((L_cnt >> 1) & 1) ^ 1, s_abort, err)) return false;
-        gather_pair<DQK>(sRing + slot * L::SLOT, kv, p, tid, rix, bar_full + 8 * slot);
-      }
-      return true;
-    };
-    int rix[4], rix_next[4];
-    if (ntiles > 0) {
-      load_rows(0, rix);
-      aborted = named_bar_or(bar_id, 128, !gather_pairs(rix, 0, NP));
-    }
-    for (int i = 0; i < ntiles && !aborted; ++i) {
-      const bool got = mbar_wait(bar_sdp, i & 1, s_abort, err);
-      if (named_bar_or(bar_id, 128, !got)) { aborted = true; break; }
+    for (int i = 0; i < ntiles; ++i) {
+      const int b = i & 1;
+      if (!mbar_wait(bar(B_SDP + b), (i >> 1) & 1, s_abort, err)) { aborted = true; break; }
       tc_fence_after();
+      const uint32_t tS = tmem_addr(tmem + C_BUF * b + ch * 32, qd * 32, 0);
+      const uint32_t tP = tS + 64;
       uint32_t sv[32], dv[32];
-      tmem_ld32(tmem_addr(tmem + C_S + ch * 32, qd * 32, 0), sv);
-      tmem_ld32(tmem_addr(tmem + C_DP + ch * 32, qd * 32, 0), dv);
+      tmem_ld32(tS, sv);
+      tmem_ld32(tP, dv);
       tmem_ld_wait();
       const int j = i * kTile + r;
       int ix = -1;
@@ -440,41 +589,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         pl[h >> 1] = pack_bf16x2(p0 - phf.x, p1 - phf.y);
         sl[h >> 1] = pack_bf16x2(s0 - shf.x, s1 - shf.y);
       }
+      // A operands of the dKV products, in place over this thread's S^T / dP^T columns
+      tmem_st16(tS, sl);
+      tmem_st16(tS + 16, sh);
+      tmem_st16(tP, ph);
+      tmem_st16(tP + 16, pl);
+      // dS hi of the tile in the swizzled [128 keys][64 heads] layout the end phase feeds to the tensor core
+      uint4* img = reinterpret_cast<uint4*>(ds_slot + (size_t)i * kDsTileBytes);
 #pragma unroll
       for (int uu = 0; uu < 4; ++uu)
-        st_shared_v4(sDS + sw128_off(r, ch * 4 + uu), sh[4 * uu], sh[4 * uu + 1], sh[4 * uu + 2], sh[4 * uu + 3]);
-      // TMEM A operands of the dKV products, over this thread's own S^T / dP^T columns
-      tmem_st16(tmem_addr(tmem + C_S + ch * 32, qd * 32, 0), sl);
-      tmem_st16(tmem_addr(tmem + C_DP + ch * 32, qd * 32, 0), ph);
-      tmem_st16(tmem_addr(tmem + C_DP + ch * 32 + 16, qd * 32, 0), pl);
+        img[sw128_off(r, ch * 4 + uu) >> 4] = make_uint4(sh[4 * uu], sh[4 * uu + 1], sh[4 * uu + 2], sh[4 * uu + 3]);
       tmem_st_wait();
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_ds);
-      bool ok = gather_pairs(rix, 0, NP);                 // pass B data
-      if (ok && i + 1 < ntiles) {                         // the next tile's pass A data
-        load_rows(i + 1, rix_next);
-        ok = gather_pairs(rix_next, 0, NP);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) rix[e] = rix_next[e];
-      }
-      aborted = named_bar_or(bar_id, 128, !ok);
+      if (lane == 0) mbar_arrive(bar(B_DS + b));
     }
+    mbar_arrive(bar(B_DSDONE));  // this thread's dS scratch stores precede the end-phase gathers
+    if (!aborted && ntiles > 0) end_gathers(threadIdx.x - 32);
+    asm volatile("cp.async.wait_all;" ::: "memory");
     // ---- dq epilogue: dQ^T (lanes = channels) -> staged [64 heads][DQK] bf16 -> coalesced stores ----
+    const int bar_id = 1 + ch;
     bool have = false;
     if (!aborted && ntiles > 0) {
-      const bool got = mbar_wait(bar_dq, 0, s_abort, err);
+      const bool got = mbar_wait(bar(B_DQ), 0, s_abort, err);
       have = !named_bar_or(bar_id, 128, !got);
       tc_fence_after();
     }
-    named_bar(3, kMath);  // both halves are done with the ring before it becomes the staging area
-    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + L::OFF_RING);
+    named_bar(3, kMath);  // both halves have left the loop before the staging area is written
+    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + L::OFF_ERING);
 #pragma unroll 1
     for (int p = 0; p < NP; ++p) {
       uint32_t v[32];
       if (have) {
-        tmem_ld32(tmem_addr(tmem + C_DQ + p * 64 + ch * 32, qd * 32, 0), v);
+        tmem_ld32(tmem_addr(tmem + 64 * p + ch * 32, qd * 32, 0), v);
         tmem_ld_wait();
       } else {
 #pragma unroll
@@ -489,7 +636,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar(3, kMath);
     const int hcount = min(kHeads, H - hg * kHeads);
     uint4* dst = reinterpret_cast<uint4*>(dq + ((size_t)t * H + hg * kHeads) * DQK);
-    for (int u = tid; u < hcount * (DQK / 8); u += kMath) dst[u] = reinterpret_cast<const uint4*>(stage)[u];
+    for (int u = threadIdx.x - 128; u < hcount * (DQK / 8); u += kMath)
+      dst[u] = reinterpret_cast<const uint4*>(stage)[u];
   }
 
   tc_fence_before();
@@ -503,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int DQK>
 dsa_status_t launch(const void* kv, const void* q, const int32_t* idx, const int32_t* len, const float* lse,
                     const float* delta, const void* dout, int T, int Tk, int H, int K, float scale, void* dq,
-                    float* dkv, int* err, cudaStream_t s) {
+                    float* dkv, uint8_t* ds_scratch, int* err, cudaStream_t s) {
   using L = Smem<DQK>;
   static bool configured = false;
   if (!configured) {
@@ -517,7 +665,7 @@ dsa_status_t launch(const void* kv, const void* q, const int32_t* idx, const int
   sparse_mla_bwd_kernel<DQK><<<grid, kThreads, L::TOTAL, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(kv), reinterpret_cast<const __nv_bfloat16*>(q), idx, len, lse, delta,
       reinterpret_cast<const __nv_bfloat16*>(dout), T, Tk, H, K, scale, reinterpret_cast<__nv_bfloat16*>(dq), dkv,
-      err);
+      ds_scratch, (K + kTile - 1) / kTile, err);
   return cuda_check(cudaGetLastError(), "launching sparse_mla_bwd_kernel");
 }
 
@@ -526,9 +674,22 @@ dsa_status_t launch(const void* kv, const void* q, const int32_t* idx, const int
 
 using namespace dsa;
 
-extern "C" size_t dsa_sparse_mla_bwd_workspace_size(int32_t T, int32_t H) {
-  const size_t delta = (size_t)(T > 0 ? T : 0) * (size_t)(H > 0 ? H : 0) * sizeof(float);
-  return kErrorWordBytes + ((delta + 255) & ~size_t(255));
+namespace dsa {
+namespace bwd {
+// Workspace layout: [error word][D: T*H fp32][dS scratch: kMaxSmSlots x ceil(K/128) x 16 KiB]
+static size_t delta_bytes(int32_t T, int32_t H) {
+  const size_t d = (size_t)(T > 0 ? T : 0) * (size_t)(H > 0 ? H : 0) * sizeof(float);
+  return (d + 255) & ~size_t(255);
+}
+static size_t scratch_bytes(int32_t K) {
+  const size_t tiles = (size_t)((K > 0 ? K : 1) + kTile - 1) / kTile;
+  return (size_t)kMaxSmSlots * tiles * kDsTileBytes;
+}
+}  // namespace bwd
+}  // namespace dsa
+
+extern "C" size_t dsa_sparse_mla_bwd_workspace_size(int32_t T, int32_t H, int32_t K) {
+  return kErrorWordBytes + bwd::delta_bytes(T, H) + bwd::scratch_bytes(K);
 }
 
 extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
@@ -556,7 +717,7 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t
                 who);
   if (dkv_bf16 && (reinterpret_cast<uintptr_t>(dkv_bf16) & 7u))
     return fail(DSA_ERR_INVALID_ARGUMENT, "%s: dkv_bf16 must be 8-byte aligned", who);
-  dsa_status_t st = check_workspace(workspace, workspace_bytes, dsa_sparse_mla_bwd_workspace_size(T, H), who);
+  dsa_status_t st = check_workspace(workspace, workspace_bytes, dsa_sparse_mla_bwd_workspace_size(T, H, K), who);
   if (st != DSA_OK) return st;
   if ((st = check_device()) != DSA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -566,6 +727,7 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t
     return st;
   int* err = reinterpret_cast<int*>(workspace);
   float* delta = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + kErrorWordBytes);
+  uint8_t* ds_scratch = reinterpret_cast<uint8_t*>(workspace) + kErrorWordBytes + bwd::delta_bytes(T, H);
   if (T > 0) {
     const long long rows = (long long)T * H;
     bwd::bwd_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
@@ -573,9 +735,9 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t
         reinterpret_cast<const __nv_bfloat16*>(dout), delta, rows);
     if ((st = cuda_check(cudaGetLastError(), "launching bwd_delta_kernel"))) return st;
     st = (Dqk == 576) ? bwd::launch<576>(kv, q, topk_idx, topk_len, lse, delta, dout, T, T_k, H, K, softmax_scale, dq,
-                                         dkv_accum, err, s)
+                                         dkv_accum, ds_scratch, err, s)
                       : bwd::launch<512>(kv, q, topk_idx, topk_len, lse, delta, dout, T, T_k, H, K, softmax_scale, dq,
-                                         dkv_accum, err, s);
+                                         dkv_accum, ds_scratch, err, s);
     if (st != DSA_OK) return st;
   }
   if (dkv_bf16) {
@@ -596,8 +758,9 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t
 // per-(row, head) D array).  This entry point takes its scratch from the
 // file-scope device array below instead, so it allocates nothing.
 //
-// The array is a fixed 16 MiB + 256 B that every GPU which loads this library
-// holds until the process exits.  Its name is only a host-side stand-in for
+// The array is a fixed 84 MiB + 256 B (error word, D for up to 4 Mi (row,
+// head) pairs, dS scratch for top-k up to 2176) that every GPU which loads
+// this library holds until the process exits.  Its name is only a host-side stand-in for
 // the device array, so the host looks up the array's real device address with
 // cudaGetSymbolAddress, once per device, on the first call made with that
 // device current; that first call should therefore come before any stream
@@ -611,7 +774,9 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t
 namespace dsa {
 namespace bwd {
 constexpr size_t kNoAllocDeltaBytes = size_t(16) << 20;  // D for up to 4 Mi (row, head) pairs
-constexpr size_t kNoAllocScratchBytes = kErrorWordBytes + kNoAllocDeltaBytes;
+constexpr int kNoAllocMaxTopk = 17 * kTile;               // dS scratch for up to 17 tiles per row
+constexpr size_t kNoAllocScratchBytes =
+    kErrorWordBytes + kNoAllocDeltaBytes + (size_t)kMaxSmSlots * (kNoAllocMaxTopk / kTile) * kDsTileBytes;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of g_noalloc_scratch on the current device (looked up once per device).
@@ -636,6 +801,7 @@ static dsa_status_t noalloc_scratch(void** ptr) {
 }  // namespace dsa
 
 extern "C" size_t dsa_sparse_mla_bwd_noalloc_max_rows(void) { return bwd::kNoAllocDeltaBytes / sizeof(float); }
+extern "C" int32_t dsa_sparse_mla_bwd_noalloc_max_topk(void) { return bwd::kNoAllocMaxTopk; }
 
 extern "C" dsa_status_t dsa_sparse_mla_bwd_noalloc(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
                                                    const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H,
@@ -643,12 +809,16 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd_noalloc(const dsa_bf16_t* q, const ds
                                                    const dsa_bf16_t* out, const dsa_bf16_t* out_lo, const float* lse,
                                                    const dsa_bf16_t* dout, dsa_bf16_t* dq, float* dkv_accum,
                                                    int32_t accumulate, dsa_bf16_t* dkv_bf16, dsa_stream_t stream) {
-  const size_t need = dsa_sparse_mla_bwd_workspace_size(T, H);
-  if (need > bwd::kNoAllocScratchBytes)
+  if ((size_t)(T > 0 ? T : 0) * (size_t)(H > 0 ? H : 0) > dsa_sparse_mla_bwd_noalloc_max_rows())
     return fail(DSA_ERR_WORKSPACE,
                 "dsa_sparse_mla_bwd_noalloc: T*H = %lld rows x heads exceeds the built-in scratch limit of %zu "
                 "(use dsa_sparse_mla_bwd with a caller workspace, or split the rows into chunks)",
                 (long long)T * H, dsa_sparse_mla_bwd_noalloc_max_rows());
+  if (K > bwd::kNoAllocMaxTopk)
+    return fail(DSA_ERR_WORKSPACE,
+                "dsa_sparse_mla_bwd_noalloc: top-k K = %d exceeds the built-in scratch limit of %d (use "
+                "dsa_sparse_mla_bwd with a caller workspace)",
+                K, bwd::kNoAllocMaxTopk);
   dsa_status_t st = check_device();
   if (st != DSA_OK) return st;
   void* scratch = nullptr;

@@ -49,13 +49,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity (no suspend).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Id of the SM this thread runs on.
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
+  return v;
+}
+
 // Bounded wait.  Gives up after ~2^31 SM cycles (about one second at the
 // GB300 clock) or as soon as another role of the CTA has given up (*abort
 // set); on give-up it records DSA_ERR_TIMEOUT and returns false so that the
 // caller can leave its loop and reach the CTA teardown.
 constexpr long long kWaitLimitCycles = 1ll << 31;
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+  // Fast path: a non-blocking test.  try_wait costs a few hundred cycles even
+  // when the phase has already completed, which would stall a thread that
+  // issues MMAs after each satisfied wait.
+  if (mbar_test(bar, parity)) return true;
   long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;

@@ -17,7 +17,7 @@ DEV = "cuda:0"
 def gpu_fwd_bwd(q, kv, dout, idx, scale, ln=None, dkv=None, accumulate=False, want_bf16=False, use_lo=True):
     dq_, kv_, i_, do_ = q.to(DEV), kv.to(DEV), idx.to(DEV), dout.to(DEV)
     ln_ = None if ln is None else ln.to(DEV)
-    ws = torch.zeros(dsa.workspace_size("bwd", q.shape[0], q.shape[1]) + 256, dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(dsa.workspace_size("bwd", q.shape[0], q.shape[1], idx.shape[1]) + 256, dtype=torch.uint8, device=DEV)
     out, lse, lo = dsa.dsa_sparse_mla_fwd(dq_, kv_, i_, scale, topk_len=ln_, out_lo=True)
     kb = torch.empty_like(kv_) if want_bf16 else None
     dq, dkv, kb = dsa.dsa_sparse_mla_bwd(dq_, kv_, i_, scale, out, lse, do_, topk_len=ln_, dkv_accum=dkv,

@@ -56,7 +56,7 @@ def mla_full_check(q, kv, dout, idx, scale, ln=None, rows=None, chunk=(0, 64), D
     """fwd+bwd of the whole problem, then row samples, column sums and one exact dkv chunk."""
     T, H = q.shape[0], q.shape[1]
     wf = torch.zeros(dsa.workspace_size("fwd", T, H), dtype=torch.uint8, device=DEV)
-    wb = torch.zeros(dsa.workspace_size("bwd", T, H), dtype=torch.uint8, device=DEV)
+    wb = torch.zeros(dsa.workspace_size("bwd", T, H, idx.shape[1]), dtype=torch.uint8, device=DEV)
     out, lse, lo = dsa.dsa_sparse_mla_fwd(q, kv, idx, scale, topk_len=ln, out_lo=True, workspace=wf)
     dq, dkv, _ = dsa.dsa_sparse_mla_bwd(q, kv, idx, scale, out, lse, dout, topk_len=ln, out_lo=lo, workspace=wb)
     assert dsa.dsa_read_device_status(wf) == 0 and dsa.dsa_read_device_status(wb) == 0

@@ -70,3 +70,13 @@ def test_noalloc_bwd_rejects_rows_beyond_its_scratch():
                                         None, fake, fake, fake, fake, 0, None, None)
     assert st == 4  # DSA_ERR_WORKSPACE
     assert "scratch limit" in lib.dsa_last_error_message().decode()
+
+
+def test_noalloc_bwd_rejects_topk_beyond_its_scratch():
+    lib = dsa.load_library()
+    K = lib.dsa_sparse_mla_bwd_noalloc_max_topk() + 1  # rejected on the host before any launch
+    fake = ctypes.c_void_p(0x10000)
+    st = lib.dsa_sparse_mla_bwd_noalloc(fake, fake, fake, None, 4, 4, 64, 576, 512, K, ctypes.c_float(0.1), fake,
+                                        None, fake, fake, fake, fake, 0, None, None)
+    assert st == 4  # DSA_ERR_WORKSPACE
+    assert "scratch limit" in lib.dsa_last_error_message().decode()
