@@ -59,7 +59,7 @@ constexpr int kTile = 128;     // top-k slots per tile (MMA M)
 constexpr int kHeads = 64;     // heads per CTA (MMA N)
 constexpr int kDv = 512;
 constexpr int kGroup = 128;    // dKV channels per staging slot (MMA N)
-constexpr int kRing = 5;       // main-loop ring: 16 KiB chunk slots
+constexpr int kRing = 4;       // main-loop ring: 16 KiB chunk slots
 constexpr int kERing = 6;      // end-phase ring: 32 KiB slots (a dS tile or a 128-channel pair)
 constexpr int kStage = 2;      // dKV staging slots
 constexpr int kMaxSmSlots = 256;                  // dS scratch slots, indexed by SM id
@@ -81,8 +81,8 @@ struct Smem {
   // MN-major operand of N = 128 channels with LBO = QDO.
   static constexpr int OFF_QDO = 0;
   static constexpr int OFF_RING = OFF_QDO + 8 * QDO + (NCH - 8) * Q_CHUNK;
-  static constexpr int OFF_FST = OFF_RING + kRing * KV_CHUNK;  // flush transposes: 4 warps x 16 rows x 128 B
-  static constexpr int OFF_MISC = OFF_FST + 4 * 2048;
+  static constexpr int OFF_FST = OFF_RING + kRing * KV_CHUNK;  // flush transposes: 12 warps x 16 rows x 128 B
+  static constexpr int OFF_MISC = OFF_FST + 12 * 2048;
   static constexpr int MISC = 1024;
   static constexpr int TOTAL = OFF_MISC + MISC + 1024;  // + alignment slack
   static constexpr int OFF_ERING = 0;                   // end phase: over Q, dO and the main ring
@@ -140,6 +140,44 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16*
     o.x = *reinterpret_cast<uint32_t*>(&lo);
     o.y = *reinterpret_cast<uint32_t*>(&hi);
     reinterpret_cast<uint2*>(dst)[i] = o;
+  }
+}
+
+// Drain 64 staged dKV channels of this warp's 32 key rows into L2 reductions.
+// v holds the warp's TMEM load (lane = key row, 64 consecutive channels); the
+// rows are transposed through the warp's 2 KB buffer, 16 rows x 32 channels at
+// a time, so that 8 lanes cover one row's 128 contiguous bytes and each
+// reduction instruction touches 4 rows x 128 B.  ix: this lane's key (-1 = skip).
+template <int DQK>
+__device__ __forceinline__ void reduce_rows64(const uint32_t (&v)[4][16], uint32_t fst, int lane, int ix,
+                                              float* dst_col) {
+#pragma unroll
+  for (int bc = 0; bc < 2; ++bc) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      if ((lane >> 4) == hh) {
+        const int rl = lane & 15;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t(&w)[16] = v[2 * bc + (u >> 2)];
+          st_shared_v4(fst + rl * 128 + ((u ^ (rl & 7)) << 4), w[4 * (u & 3)], w[4 * (u & 3) + 1], w[4 * (u & 3) + 2],
+                       w[4 * (u & 3) + 3]);
+        }
+      }
+      __syncwarp();
+#pragma unroll
+      for (int st = 0; st < 4; ++st) {
+        const int rl = 4 * st + (lane >> 3), u = lane & 7;
+        const int ixr = __shfl_sync(0xffffffffu, ix, 16 * hh + rl);
+        float4 f;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+                     : "r"(fst + rl * 128 + ((u ^ (rl & 7)) << 4))
+                     : "memory");
+        if (ixr >= 0) red_add_v4(dst_col + (size_t)ixr * DQK + 32 * bc + 4 * u, f.x, f.y, f.z, f.w);
+      }
+      __syncwarp();
+    }
   }
 }
 
@@ -226,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kStage; ++s) {
       mbar_init(bar(B_STF + s), 1);
-      mbar_init(bar(B_STE + s), 4);
+      mbar_init(bar(B_STE + s), s == 0 ? kMath / 32 : 4);  // slot 0: the math warps drain it; slot 1: the flush warps
     }
     mbar_init(bar(B_DSDONE), kMath);
     mbar_init(bar(B_ENDGO), 1);
@@ -484,65 +522,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     // no copy may still be landing in this CTA's shared memory when it exits
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (is_flush) {
-    // ======================= dKV flush: TMEM staging -> registers -> L2 reductions =======================
+    // ======================= dKV flush: staging slot 1 (odd groups) -> L2 reductions =======================
     const int qd = warp & 3;
     const int r = qd * 32 + lane;  // key row of the tile
     const uint32_t fst = smem_u32(smem + L::OFF_FST + qd * 2048);
-    int G = 0;
     for (int i = 0; i < ntiles; ++i) {
       const int j = i * kTile + r;
       int ix = -1;
       if (j < n_eff) ix = __ldg(idx_row + j);
       if (!(ix >= 0 && ix < Tk)) ix = -1;
       bool stop = false;
-      for (int g = 0; g < NG; ++g, ++G) {
-        const int s = G & (kStage - 1), n = G / kStage;
-        if (!mbar_wait(bar(B_STF + s), n & 1, s_abort, err)) { stop = true; break; }
+      for (int g = 0; g < NG; ++g) {
+        const int G = i * NG + g;
+        if ((G & 1) == 0) continue;  // slot 0: the math warps
+        const int n = G >> 1;
+        if (!mbar_wait(bar(B_STF + 1), n & 1, s_abort, err)) { stop = true; break; }
         tc_fence_after();
         const int halves = (g * kGroup + kGroup <= DQK) ? 2 : 1;
         for (int hf = 0; hf < halves; ++hf) {
           uint32_t v[4][16];
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq)
-            tmem_ld16(tmem_addr(tmem + C_STG + kGroup * s + 64 * hf + 16 * qq, qd * 32, 0), v[qq]);
+            tmem_ld16(tmem_addr(tmem + C_STG + kGroup + 64 * hf + 16 * qq, qd * 32, 0), v[qq]);
           tmem_ld_wait();
           if (hf == halves - 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_STE + s));  // the slot may be refilled
+            if (lane == 0) mbar_arrive(bar(B_STE + 1));  // the slot may be refilled
           }
-          float* dst_row = dkv + g * kGroup + 64 * hf;
-          // Transpose through this warp's 2 KB buffer, 16 rows x 32 channels at a time, so
-          // that 8 lanes cover one row's 128 contiguous bytes: each reduction instruction
-          // then touches 4 rows x 128 B.
-#pragma unroll
-          for (int bc = 0; bc < 2; ++bc) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              if ((lane >> 4) == hh) {
-                const int rl = lane & 15;
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                  const uint32_t(&w)[16] = v[2 * bc + (u >> 2)];
-                  st_shared_v4(fst + rl * 128 + ((u ^ (rl & 7)) << 4), w[4 * (u & 3)], w[4 * (u & 3) + 1],
-                               w[4 * (u & 3) + 2], w[4 * (u & 3) + 3]);
-                }
-              }
-              __syncwarp();
-#pragma unroll
-              for (int st = 0; st < 4; ++st) {
-                const int rl = 4 * st + (lane >> 3), u = lane & 7;
-                const int ixr = __shfl_sync(0xffffffffu, ix, 16 * hh + rl);
-                float4 f;
-                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                             : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
-                             : "r"(fst + rl * 128 + ((u ^ (rl & 7)) << 4))
-                             : "memory");
-                if (ixr >= 0) red_add_v4(dst_row + (size_t)ixr * DQK + 32 * bc + 4 * u, f.x, f.y, f.z, f.w);
-              }
-              __syncwarp();
-            }
-          }
+          reduce_rows64<DQK>(v, fst, lane, ix, dkv + g * kGroup + 64 * hf);
         }
       }
       if (stop) break;
@@ -556,6 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2e = scale * 1.4426950408889634f;
     const float* lse2 = s_lse2 + ch * 32;
     const float* dl = s_dl + ch * 32;
+    const uint32_t fst_m = smem_u32(smem + L::OFF_FST + (4 + mw) * 2048);  // this warp's transpose buffer
     bool aborted = false;
     for (int i = 0; i < ntiles; ++i) {
       const int b = i & 1;
@@ -603,6 +612,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DS + b));
+      // ---- drain this tile's even dKV groups (staging slot 0): this warp's rows, channel half ch ----
+      const int kix = valid ? ix : -1;
+      for (int g = 0; g < NG; ++g) {
+        const int G = i * NG + g;
+        if (G & 1) continue;  // slot 1: the flush warps
+        if (!mbar_wait(bar(B_STF), (G >> 1) & 1, s_abort, err)) { aborted = true; break; }
+        const bool mine = g * kGroup + 64 * ch < DQK;  // the last group may hold 64 channels only
+        if (mine) {
+          tc_fence_after();
+          uint32_t v[4][16];
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) tmem_ld16(tmem_addr(tmem + C_STG + 64 * ch + 16 * qq, qd * 32, 0), v[qq]);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_STE));
+          reduce_rows64<DQK>(v, fst_m, lane, kix, dkv + g * kGroup + 64 * ch);
+        } else {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_STE));
+        }
+      }
+      if (aborted) break;
     }
     mbar_arrive(bar(B_DSDONE));  // this thread's dS scratch stores precede the end-phase gathers
     if (!aborted && ntiles > 0) end_gathers(threadIdx.x - 32);
