@@ -300,16 +300,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = tid; u < kHeads * NCH * 8; u += kMath) {
       const int hh = u / (NCH * 8), rem = u - hh * (NCH * 8), c = rem >> 3, uc = rem & 7;
       const int h = hg * kHeads + hh;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (h < H) v = __ldg(reinterpret_cast<const uint4*>(q + ((size_t)t * H + h) * DQK + c * 64 + uc * 8));
-      st_shared_v4(sQDO + c * L::QDO + sw128_off(hh, uc), v.x, v.y, v.z, v.w);
+      const bool ok = h < H;  // padded heads are zero-filled without a read
+      cp_async16(sQDO + c * L::QDO + sw128_off(hh, uc), q + (ok ? ((size_t)t * H + h) * DQK + c * 64 + uc * 8 : 0),
+                 ok ? 16u : 0u);
     }
     for (int u = tid; u < kHeads * 8 * 8; u += kMath) {
       const int hh = u >> 6, rem = u & 63, c = rem >> 3, uc = rem & 7;
       const int h = hg * kHeads + hh;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (h < H) v = __ldg(reinterpret_cast<const uint4*>(dout + ((size_t)t * H + h) * kDv + c * 64 + uc * 8));
-      st_shared_v4(sQDO + c * L::QDO + L::Q_CHUNK + sw128_off(hh, uc), v.x, v.y, v.z, v.w);
+      const bool ok = h < H;
+      cp_async16(sQDO + c * L::QDO + L::Q_CHUNK + sw128_off(hh, uc),
+                 dout + (ok ? ((size_t)t * H + h) * kDv + c * 64 + uc * 8 : 0), ok ? 16u : 0u);
     }
     // per-head lse (log2 units) and D, shared by every key row
     if (tid < kHeads) {
@@ -317,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_lse2[tid] = (hh < H) ? lse[(size_t)t * H + hh] * 1.4426950408889634f : INFINITY;  // padded heads: P = 0
       s_dl[tid] = (hh < H) ? delta[(size_t)t * H + hh] : 0.f;
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // all copies in flight at once, one wait
     fence_proxy_async_smem();
   }
   __syncthreads();

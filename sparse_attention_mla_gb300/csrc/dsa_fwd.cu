@@ -186,10 +186,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rem = u - hh * (NCH * 8);
       const int c = rem >> 3, uc = rem & 7;
       const int h = hg * kHeads + hh;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (h < H) v = __ldg(reinterpret_cast<const uint4*>(q + ((size_t)t * H + h) * DQK + c * 64 + uc * 8));
-      st_shared_v4(sQ + c * L::Q_CHUNK + sw128_off(hh, uc), v.x, v.y, v.z, v.w);
+      const bool ok = h < H;  // padded heads are zero-filled without a read
+      cp_async16(sQ + c * L::Q_CHUNK + sw128_off(hh, uc), q + (ok ? ((size_t)t * H + h) * DQK + c * 64 + uc * 8 : 0),
+                 ok ? 16u : 0u);
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // all copies in flight at once, one wait
     fence_proxy_async_smem();
   }
   __syncthreads();
