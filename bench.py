@@ -368,8 +368,11 @@ def kernel_rev(src_name: str) -> str:
     """Content hash of a kernel source: ncu counters are reused only for the same code."""
     import hashlib
 
-    with open(os.path.join(ROOT, "sparse_attention_mla_gb300", "csrc", src_name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in (src_name, "dsa_device.cuh"):  # the kernel source and the device helpers it inlines
+        with open(os.path.join(ROOT, "sparse_attention_mla_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def main():
