@@ -212,38 +212,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar_kv + 8 * c, i & 1, s_abort, err)) { stop = true; break; }
           fence_proxy_async_smem();  // cp.async landings -> visible to the tensor core
           tc_fence_after();
+          const uint64_t a0 = sdesc_sw128(sKV + c * L::KV_CHUNK, 16, 1024);
+          const uint64_t b0 = sdesc_sw128(sQ + c * L::Q_CHUNK, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t a = sdesc_sw128(sKV + c * L::KV_CHUNK + k * 32, 16, 1024);
-            const uint64_t b = sdesc_sw128(sQ + c * L::Q_CHUNK + k * 32, 16, 1024);
-            mma_ss(tS, a, b, kIdS, (c | k) != 0);
-          }
+          for (int k = 0; k < 4; ++k)  // + 16 channels = + 32 bytes per row
+            mma_ss(tS, a0 + (uint64_t)(k * 2), b0 + (uint64_t)(k * 2), kIdS, (c | k) != 0);
         }
         if (stop) break;
         mma_commit(bar_s);
         // O^T += V^T P_hi^T, then (P_lo in the same slot) O^T += V^T P_lo^T
         if (!mbar_wait(bar_p, i & 1, s_abort, err)) break;
         tc_fence_after();
-#pragma unroll 1
+        const uint64_t pb0 = sdesc_sw128(sP, L::KV_CHUNK, 1024);
+        const uint64_t va0 = sdesc_sw128(sKV, L::KV_CHUNK, 1024);
+        constexpr uint64_t kPair = (2 * L::KV_CHUNK) >> 4;  // descriptor step between channel pairs
+#pragma unroll
         for (int m = 0; m < kDv / 128; ++m) {
 #pragma unroll
-          for (int k = 0; k < kTile / 16; ++k) {
-            const uint64_t a = sdesc_sw128(sKV + (2 * m) * L::KV_CHUNK + k * 2048, L::KV_CHUNK, 1024);
-            const uint64_t b = sdesc_sw128(sP + k * 2048, L::KV_CHUNK, 1024);
-            mma_ss(tO + m * kHeads, a, b, kIdPV, (i > 0 || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < kTile / 16; ++k)  // + 16 key rows = + 2048 bytes
+            mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV,
+                   (i > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(bar_pvh);
         if (!mbar_wait(bar_plo, i & 1, s_abort, err)) break;
         tc_fence_after();
-#pragma unroll 1
+#pragma unroll
         for (int m = 0; m < kDv / 128; ++m) {
 #pragma unroll
-          for (int k = 0; k < kTile / 16; ++k) {
-            const uint64_t a = sdesc_sw128(sKV + (2 * m) * L::KV_CHUNK + k * 2048, L::KV_CHUNK, 1024);
-            const uint64_t b = sdesc_sw128(sP + k * 2048, L::KV_CHUNK, 1024);
-            mma_ss(tO + m * kHeads, a, b, kIdPV, 1u);
-          }
+          for (int k = 0; k < kTile / 16; ++k)
+            mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV, 1u);
           mma_commit(bar_pv + 8 * m);
         }
       }
