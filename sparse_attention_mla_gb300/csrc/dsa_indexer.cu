@@ -104,13 +104,19 @@ __device__ __forceinline__ int2 half_scan(const Half& hf, bool pred, int par) {
   return make_int2(before, total);
 }
 
-// Keep the best `target` of the cnt candidates (score desc, index asc),
-// stably, in place.  Returns the new threshold image (accept iff key > thr).
-__device__ uint32_t compact(const Half& hf, float* cs, int* ci, int cnt, int target, int& parity) {
-  // radix select: find the target-th largest key image v
+// Exact (passes = 4): keep the best `target` of the cnt candidates (score
+// desc, index asc), stably, in place; returns v with "accept iff key > v".
+// Approximate (passes = 2): find the 16-bit key bucket that holds the
+// target-th best and keep every candidate at or above that bucket, stably: a
+// superset of the best `target` (so the final exact selection is unchanged)
+// in half the passes; returns the bucket floor minus one, again "accept iff
+// key > v".  *kept_out receives the number kept.
+__device__ uint32_t compact(const Half& hf, float* cs, int* ci, int cnt, int target, int& parity, int passes,
+                            int* kept_out) {
+  // radix select: find the target-th largest key image (its top 8*passes bits)
   uint32_t prefix = 0, pmask = 0;
   int kk = target;
-  for (int pass = 0; pass < 4; ++pass) {
+  for (int pass = 0; pass < passes; ++pass) {
     const int shift = 24 - 8 * pass;
     hf.hist[hf.tid] = 0;
     hf.hist[hf.tid + 128] = 0;
@@ -153,6 +159,31 @@ __device__ uint32_t compact(const Half& hf, float* cs, int* ci, int cnt, int tar
     pmask |= 255u << shift;
     named_bar(hf.bar, 128);  // sel is rewritten by the next pass
   }
+  if (passes < 4) {
+    // keep every key >= prefix (the bucket floor): one scan per chunk
+    int kept = 0;
+    for (int base = 0; base < cnt; base += 128) {
+      const int e = base + hf.tid;
+      float s = 0.f;
+      int ix = 0;
+      bool keep = false;
+      if (e < cnt) {
+        s = cs[e];
+        ix = ci[e];
+        keep = ordered(s) >= prefix;
+      }
+      const int2 ke = half_scan(hf, keep, parity);
+      parity ^= 1;
+      if (keep) {
+        cs[kept + ke.x] = s;
+        ci[kept + ke.x] = ix;
+      }
+      kept += ke.y;
+    }
+    named_bar(hf.bar, 128);
+    *kept_out = kept;
+    return prefix - 1u;  // prefix >= 1: the target-th best has key >= prefix > 0
+  }
   const uint32_t v = prefix;  // kk >= 1 ties at v are kept (the earliest ones)
   int kept = 0, ties = 0;
   for (int base = 0; base < cnt; base += 128) {
@@ -180,6 +211,7 @@ __device__ uint32_t compact(const Half& hf, float* cs, int* ci, int cnt, int tar
     ties += te.y;
   }
   named_bar(hf.bar, 128);
+  *kept_out = kept;
   return v;
 }
 
@@ -331,8 +363,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tile0 > win_hi || tile0 + kTile <= win_lo) continue;  // whole tile outside this token's window (uniform)
       const int key = tile0 + hf.tid;
       float sc = 0.f;
+      const float4* wr4 = reinterpret_cast<const float4*>(wr);
 #pragma unroll
-      for (int h = 0; h < kHeads; ++h) sc = fmaf(wr[h], fmaxf(__uint_as_float(v[h]), 0.f), sc);
+      for (int h4 = 0; h4 < kHeads / 4; ++h4) {
+        const float4 wv = wr4[h4];
+        sc = fmaf(wv.x, fmaxf(__uint_as_float(v[4 * h4]), 0.f), sc);
+        sc = fmaf(wv.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), sc);
+        sc = fmaf(wv.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), sc);
+        sc = fmaf(wv.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), sc);
+      }
       const bool in = key >= win_lo && key <= win_hi;
       const bool acc = in && ordered(sc) > thr;
       const int2 pos = half_scan(hf, acc, parity);
@@ -344,8 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       cnt += pos.y;
       if (cnt > CAP - kTile) {
         named_bar(hf.bar, 128);
-        thr = compact(hf, cs, ci, cnt, K, parity);
-        cnt = K;
+        int kept = 0;
+        thr = compact(hf, cs, ci, cnt, K, parity, 2, &kept);
+        if (kept > CAP - 2 * kTile) thr = compact(hf, cs, ci, kept, K, parity, 4, &kept);  // a crowded bucket
+        cnt = kept;
       }
     }
     // ---- final selection and output (ascending, -1 suffix) ----
@@ -355,7 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int c = win_hi - win_lo + 1;
       const int n = min(K, c);
       if (!aborted && cnt > n) {
-        compact(hf, cs, ci, cnt, n, parity);
+        int kept = 0;
+        compact(hf, cs, ci, cnt, n, parity, 4, &kept);
         cnt = n;
       }
       const int have = aborted ? 0 : min(cnt, n);
