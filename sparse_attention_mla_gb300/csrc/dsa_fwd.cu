@@ -208,15 +208,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < ntiles; ++i) {
         bool stop = false;
 #pragma unroll 1
-        for (int c = 0; c < NCH; ++c) {
+        // one burst per group of landed chunks: wait for the next chunk, then take every
+        // later chunk that has landed too (fewer fences and waits between MMAs)
+        const uint64_t a00 = sdesc_sw128(sKV, 16, 1024), b00 = sdesc_sw128(sQ, 16, 1024);
+        for (int c = 0; c < NCH && !stop;) {
           if (!mbar_wait(bar_kv + 8 * c, i & 1, s_abort, err)) { stop = true; break; }
+          int ce = c + 1;
+          while (ce < NCH && mbar_test(bar_kv + 8 * ce, i & 1)) ++ce;
           fence_proxy_async_smem();  // cp.async landings -> visible to the tensor core
           tc_fence_after();
-          const uint64_t a0 = sdesc_sw128(sKV + c * L::KV_CHUNK, 16, 1024);
-          const uint64_t b0 = sdesc_sw128(sQ + c * L::Q_CHUNK, 16, 1024);
+          for (; c < ce; ++c) {
+            const uint64_t a0 = a00 + (uint64_t)((c * L::KV_CHUNK) >> 4), b0 = b00 + (uint64_t)((c * L::Q_CHUNK) >> 4);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)  // + 16 channels = + 32 bytes per row
-            mma_ss(tS, a0 + (uint64_t)(k * 2), b0 + (uint64_t)(k * 2), kIdS, (c | k) != 0);
+            for (int k = 0; k < 4; ++k)  // + 16 channels = + 32 bytes per row
+              mma_ss(tS, a0 + (uint64_t)(k * 2), b0 + (uint64_t)(k * 2), kIdS, (c | k) != 0);
+          }
         }
         if (stop) break;
         mma_commit(bar_s);
