@@ -53,3 +53,4 @@ def assert_lse(got, ref, name="lse", tol=LSE_ABS):
     if fin.any():
         err = float(np.max(np.abs(g[fin] - r[fin])))
         assert err <= tol, f"{name}: max |d| = {err:.3e} > {tol}"
+

@@ -59,3 +59,52 @@ def test_fwd_rejects_bad_workspace(lib, bad):
 def test_metadata_rejects_invalid_arguments(lib):
     assert lib.dsa_packed_metadata(None, 1, 4, FAKE, FAKE, None, None, None) == 3
     assert lib.dsa_packed_metadata(FAKE, 0, 4, FAKE, FAKE, None, None, None) == 3
+
+
+def bwd(lib, **kw):
+    a = dict(q=FAKE, kv=FAKE, idx=FAKE, ln=None, T=4, Tk=8, H=16, Dqk=576, Dv=512, K=64, scale=0.1, out=FAKE,
+             out_lo=None, lse=FAKE, dout=FAKE, dq=FAKE, dkv=FAKE, acc=0, dkv_bf16=None, ws=P(0x100000), wsb=1 << 30,
+             stream=None)
+    a.update(kw)
+    return lib.dsa_sparse_mla_bwd(a["q"], a["kv"], a["idx"], a["ln"], a["T"], a["Tk"], a["H"], a["Dqk"], a["Dv"],
+                                  a["K"], ctypes.c_float(a["scale"]), a["out"], a["out_lo"], a["lse"], a["dout"],
+                                  a["dq"], a["dkv"], a["acc"], a["dkv_bf16"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("bad", [dict(Dqk=500), dict(Dv=256), dict(K=0), dict(H=0), dict(Tk=0), dict(T=-1),
+                                 dict(acc=2), dict(scale=0.0), dict(scale=float("inf")), dict(kv=None),
+                                 dict(dkv=None), dict(dq=None), dict(q=P(0x10002)), dict(out_lo=P(0x10008)),
+                                 dict(dkv_bf16=P(0x10002))])
+def test_bwd_rejects_invalid_arguments(lib, bad):
+    assert bwd(lib, **bad) == 3  # DSA_ERR_INVALID_ARGUMENT
+    assert lib.dsa_last_error_message().decode().startswith("dsa_sparse_mla_bwd")
+
+
+def test_bwd_workspace_grows_with_rows_heads_and_topk(lib):
+    lib.dsa_sparse_mla_bwd_workspace_size.restype = ctypes.c_size_t
+    base = lib.dsa_sparse_mla_bwd_workspace_size(4, 16, 64)
+    assert lib.dsa_sparse_mla_bwd_workspace_size(4096, 16, 64) > base          # D per (row, head)
+    assert lib.dsa_sparse_mla_bwd_workspace_size(4, 16, 2051) > base           # dS scratch per 128-slot tile
+    assert bwd(lib, wsb=base - 256) == 4                                         # DSA_ERR_WORKSPACE
+    assert bwd(lib, ws=P(0x100010)) == 4                                         # not 256-byte aligned
+
+
+def idxr(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, w=FAKE, st=FAKE, T=4, Tk=8, Hi=64, Di=128, K=64, idx=FAKE, ln=None, ws=P(0x100000),
+             wsb=1 << 20, stream=None)
+    a.update(kw)
+    return lib.dsa_indexer_topk(a["q"], a["k"], a["w"], a["st"], a["T"], a["Tk"], a["Hi"], a["Di"], a["K"], a["idx"],
+                                a["ln"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("bad", [dict(Tk=3), dict(T=-1), dict(Hi=0), dict(Hi=65), dict(Di=64), dict(K=0),
+                                 dict(K=2049), dict(k=None), dict(w=None), dict(st=None), dict(idx=None),
+                                 dict(q=P(0x10002))])
+def test_indexer_rejects_invalid_arguments(lib, bad):
+    assert idxr(lib, **bad) == 3  # DSA_ERR_INVALID_ARGUMENT
+    assert lib.dsa_last_error_message().decode().startswith("dsa_indexer_topk")
+
+
+def test_indexer_rejects_bad_workspace(lib):
+    assert idxr(lib, ws=None) == 4
+    assert idxr(lib, wsb=16) == 4

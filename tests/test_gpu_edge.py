@@ -1,0 +1,111 @@
+"""Edge cases of the CUDA path against the fp64 oracle: top-k of one, scores
+that grow across tiles (the forward's lazy rescale of the running max), kv
+longer than the queries with non-causal index sets, and empty calls."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_mla_gb300 as dsa
+from sparse_attention_mla_gb300 import synth
+
+from _cmp import REL_FRO, assert_close, assert_lse, errors
+from test_gpu_fwd import make_case
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def fwd_bwd_vs_oracle(q, kv, dout, idx, scale, ln=None, stress=False):
+    qd, kvd, idd, dod = q.to(DEV), kv.to(DEV), idx.to(DEV), dout.to(DEV)
+    lnd = None if ln is None else ln.to(DEV)
+    wf = torch.zeros(dsa.workspace_size("fwd", q.shape[0], q.shape[1]), dtype=torch.uint8, device=DEV)
+    wb = torch.zeros(dsa.workspace_size("bwd", q.shape[0], q.shape[1], idx.shape[1]), dtype=torch.uint8, device=DEV)
+    out, lse, lo = dsa.dsa_sparse_mla_fwd(qd, kvd, idd, scale, topk_len=lnd, out_lo=True, workspace=wf)
+    dq, dkv, _ = dsa.dsa_sparse_mla_bwd(qd, kvd, idd, scale, out, lse, dod, topk_len=lnd, out_lo=lo, workspace=wb)
+    assert dsa.dsa_read_device_status(wf) == 0 and dsa.dsa_read_device_status(wb) == 0
+    ref_o, ref_l = oracle.sparse_mla_fwd(q, kv, idx, scale, len_rows=ln)
+    ref_dq, ref_dkv = oracle.sparse_mla_bwd(q, kv, idx, dout, scale, len_rows=ln)
+    assert_close(out.cpu(), ref_o, "out")
+    assert_lse(lse.cpu(), ref_l)
+    if not stress:
+        assert_close(dq.cpu(), ref_dq, "dq")
+        assert_close(dkv.cpu(), ref_dkv, "dkv")
+    else:
+        # dq is formed from bf16 dS: where large terms cancel, its element error follows the sum of
+        # |terms|, not dq; stress inputs check the gradients in relative Frobenius norm only
+        for got, ref, name in ((dq, ref_dq, "dq"), (dkv, ref_dkv, "dkv")):
+            _, rf = errors(got.cpu(), ref)
+            assert rf <= REL_FRO, f"{name}: rel_fro={rf:.3e}"
+
+
+def test_topk_one():
+    # K = 1: each row attends to exactly one key (P = 1, dS = 0, dkv = dO on that row)
+    q, kv, dout, idx = make_case(40, 100, 64, 576, 1, 11)
+    fwd_bwd_vs_oracle(q, kv, dout, idx, 192 ** -0.5)
+
+
+def test_growing_scores_rescale_running_max():
+    # kv rows scaled up with the key index, slots ascending: every new 128-slot tile raises the
+    # running max by far more than the lazy-rescale threshold, so O is rescaled tile after tile
+    q, kv, dout, idx = make_case(24, 700, 64, 576, 600, 12)
+    ramp = (1.0 + torch.arange(kv.shape[0], dtype=torch.float32) / 120.0)[:, None]
+    kv = (kv.float() * ramp).to(torch.bfloat16)
+    fwd_bwd_vs_oracle(q, kv, dout, idx, 0.25, stress=True)
+
+
+def test_peaky_softmax_large_scale():
+    # one dominant key per row: exp2 arguments span a wide range, most P round to tiny values
+    q, kv, dout, idx = make_case(32, 400, 16, 576, 260, 13)
+    fwd_bwd_vs_oracle(q, kv, dout, idx, 1.0, stress=True)
+
+
+def test_kv_longer_than_queries_non_causal_indices():
+    # the MLA kernels take any index set: rows pick keys anywhere in a kv 3x longer than the queries
+    T, Tk, H, K = 48, 3000, 64, 333
+    g = synth.generator(14)
+    q = synth.randn_bf16((T, H, 576), g)
+    kv = synth.randn_bf16((Tk, 576), g)
+    dout = synth.randn_bf16((T, H, 512), g)
+    idx = torch.stack([torch.randperm(Tk, generator=g)[:K].sort().values for _ in range(T)]).to(torch.int32)
+    fwd_bwd_vs_oracle(q, kv, dout, idx, 192 ** -0.5)
+
+
+def test_empty_calls_leave_outputs_consistent():
+    # T = 0: nothing is launched; the backward still zeroes dkv (accumulate = 0)
+    kv = synth.randn_bf16((16, 576), synth.generator(15)).to(DEV)
+    q = torch.empty(0, 64, 576, dtype=torch.bfloat16, device=DEV)
+    idx = torch.empty(0, 32, dtype=torch.int32, device=DEV)
+    out, lse = dsa.dsa_sparse_mla_fwd(q, kv, idx, 0.1)
+    assert out.shape == (0, 64, 512) and lse.shape == (0, 64)
+    dout = torch.empty(0, 64, 512, dtype=torch.bfloat16, device=DEV)
+    dkv = torch.full((16, 576), 7.0, dtype=torch.float32, device=DEV)
+    dq, dkv, _ = dsa.dsa_sparse_mla_bwd(q, kv, idx, 0.1, out, lse, dout, dkv_accum=dkv)
+    torch.cuda.synchronize()
+    assert dq.shape == (0, 64, 576) and torch.all(dkv == 0)
+    qi = torch.empty(0, 64, 128, dtype=torch.bfloat16, device=DEV)
+    ki = synth.randn_bf16((16, 128), synth.generator(16)).to(DEV)
+    w = torch.empty(0, 64, dtype=torch.float32, device=DEV)
+    st = torch.empty(0, dtype=torch.int32, device=DEV)
+    ti, tl = dsa.dsa_indexer_topk(qi, ki, w, st, 8)
+    assert ti.shape == (0, 8) and tl.shape == (0,)
+
+
+def test_indexer_k_one_and_k_2048_boundaries():
+    # K = 1 picks the single best key; K = 2048 (the largest) on windows just above and below it
+    T = 2300
+    x = synth.indexer_inputs(T, 64, 128, seed=17)
+    cu = torch.tensor([0, T], dtype=torch.int32)
+    start, _, _, _ = dsa.dsa_packed_metadata(cu.to(DEV), T)
+    for K in (1, 2048):
+        idx, ln = dsa.dsa_indexer_topk(x["q_idx"].to(DEV), x["k_idx"].to(DEV), x["w"].to(DEV), start, K)
+        rows = np.array([0, 1, 2046, 2047, 2048, 2049, T - 1])
+        ref_idx, ref_len, _ = oracle.indexer_topk(x["q_idx"][rows], x["k_idx"], x["w"][rows],
+                                                  start.cpu().numpy(), rows, K)
+        gl = ln.cpu().numpy()[rows]
+        assert np.array_equal(gl, ref_len)
+        gi = idx.cpu().numpy()[rows]
+        for r in range(len(rows)):
+            n = ref_len[r]
+            assert np.all(gi[r, n:] == -1)
+            assert len(set(gi[r, :n]) ^ set(ref_idx[r, :n])) <= 2  # at most one fp32 near-tie swap
