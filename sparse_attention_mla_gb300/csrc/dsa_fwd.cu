@@ -207,7 +207,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdPV = idesc_bf16(128, kHeads, true, true);   // A = V^T (MN-major), B = P^T (MN-major)
       for (int i = 0; i < ntiles; ++i) {
         bool stop = false;
-#pragma unroll 1
         // one burst per group of landed chunks: wait for the next chunk, then take every
         // later chunk that has landed too (fewer fences and waits between MMAs)
         const uint64_t a00 = sdesc_sw128(sKV, 16, 1024), b00 = sdesc_sw128(sQ, 16, 1024);
