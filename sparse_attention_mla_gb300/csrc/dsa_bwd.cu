@@ -181,6 +181,12 @@ __device__ __forceinline__ void reduce_rows64(const uint32_t (&v)[4][16], uint32
   }
 }
 
+// Drain warps of a quadrant: the flush warp (role 0) and the two math warps
+// (roles 1, 2 = head halves).  The flush warp drains the first half (64
+// channels) of every dKV group; the second halves alternate between the math
+// warps, which also run the softmax on the critical path.
+__device__ __forceinline__ int drain_role(int g, int hf) { return hf == 0 ? 0 : 1 + (g & 1); }
+
 // One thread's share of gathering a tile's rows, 64 channels at a time, with
 // NT threads: per unit (row, 16-byte column) the source pointer of channel 0
 // and the swizzled destination offset are computed once per tile, so that a
@@ -264,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kStage; ++s) {
       mbar_init(bar(B_STF + s), 1);
-      mbar_init(bar(B_STE + s), s == 0 ? kMath / 32 : 4);  // slot 0: the math warps drain it; slot 1: the flush warps
+      mbar_init(bar(B_STE + s), kMath / 32 + 4);  // every drain warp (8 math + 4 flush) releases every use
     }
     mbar_init(bar(B_DSDONE), kMath);
     mbar_init(bar(B_ENDGO), 1);
@@ -355,6 +361,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         cp_async_arrive(bar(B_EFULL + slot));
       }
     }
+  };
+
+  // A drain warp's part of staged dKV group G (group g of its tile): wait for it (every drain warp
+  // waits for every group, in order, so that each slot barrier is read phase by phase), load the
+  // halves this warp owns, release the slot, then reduce them into dkv.
+  auto drain_group = [&](int G, int g, int role, int ix, uint32_t fst) -> bool {
+    const int s = G & (kStage - 1);
+    if (!mbar_wait(bar(B_STF + s), (G / kStage) & 1, s_abort, err)) return false;
+    const int halves = (g * kGroup + kGroup <= DQK) ? 2 : 1;
+    int mine = -1;  // the half this warp owns, if any (drain_role gives a warp at most one per group)
+    for (int hf = 0; hf < halves; ++hf)
+      if (drain_role(g, hf) == role) mine = hf;
+    if (mine >= 0) {
+      tc_fence_after();
+      uint32_t v[4][16];
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq)
+        tmem_ld16(tmem_addr(tmem + C_STG + kGroup * s + 64 * mine + 16 * qq, (warp & 3) * 32, 0), v[qq]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_STE + s));  // the slot may be refilled
+      reduce_rows64<DQK>(v, fst, lane, ix, dkv + g * kGroup + 64 * mine);
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_STE + s));
+    }
+    return true;
   };
 
   if (warp == 0) {
@@ -523,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // no copy may still be landing in this CTA's shared memory when it exits
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (is_flush) {
-    // ======================= dKV flush: staging slot 1 (odd groups) -> L2 reductions =======================
+    // ======================= dKV flush: its share of every staged group -> L2 reductions =======================
     const int qd = warp & 3;
     const int r = qd * 32 + lane;  // key row of the tile
     const uint32_t fst = smem_u32(smem + L::OFF_FST + qd * 2048);
@@ -533,27 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j < n_eff) ix = __ldg(idx_row + j);
       if (!(ix >= 0 && ix < Tk)) ix = -1;
       bool stop = false;
-      for (int g = 0; g < NG; ++g) {
-        const int G = i * NG + g;
-        if ((G & 1) == 0) continue;  // slot 0: the math warps
-        const int n = G >> 1;
-        if (!mbar_wait(bar(B_STF + 1), n & 1, s_abort, err)) { stop = true; break; }
-        tc_fence_after();
-        const int halves = (g * kGroup + kGroup <= DQK) ? 2 : 1;
-        for (int hf = 0; hf < halves; ++hf) {
-          uint32_t v[4][16];
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq)
-            tmem_ld16(tmem_addr(tmem + C_STG + kGroup + 64 * hf + 16 * qq, qd * 32, 0), v[qq]);
-          tmem_ld_wait();
-          if (hf == halves - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_STE + 1));  // the slot may be refilled
-          }
-          reduce_rows64<DQK>(v, fst, lane, ix, dkv + g * kGroup + 64 * hf);
-        }
-      }
+      for (int g = 0; g < NG; ++g)
+        if (!drain_group(i * NG + g, g, 0, ix, fst)) { stop = true; break; }
       if (stop) break;
     }
   } else {
@@ -613,28 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DS + b));
-      // ---- drain this tile's even dKV groups (staging slot 0): this warp's rows, channel half ch ----
+      // ---- this warp's share of the tile's staged dKV groups (role 1 + ch) ----
       const int kix = valid ? ix : -1;
-      for (int g = 0; g < NG; ++g) {
-        const int G = i * NG + g;
-        if (G & 1) continue;  // slot 1: the flush warps
-        if (!mbar_wait(bar(B_STF), (G >> 1) & 1, s_abort, err)) { aborted = true; break; }
-        const bool mine = g * kGroup + 64 * ch < DQK;  // the last group may hold 64 channels only
-        if (mine) {
-          tc_fence_after();
-          uint32_t v[4][16];
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) tmem_ld16(tmem_addr(tmem + C_STG + 64 * ch + 16 * qq, qd * 32, 0), v[qq]);
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_STE));
-          reduce_rows64<DQK>(v, fst_m, lane, kix, dkv + g * kGroup + 64 * ch);
-        } else {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_STE));
-        }
-      }
+      for (int g = 0; g < NG && !aborted; ++g)
+        if (!drain_group(i * NG + g, g, 1 + ch, kix, fst_m)) aborted = true;
       if (aborted) break;
     }
     mbar_arrive(bar(B_DSDONE));  // this thread's dS scratch stores precede the end-phase gathers
