@@ -601,10 +601,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h = 0; h < 32; h += 2) {
         float p0 = 0.f, p1 = 0.f, s0 = 0.f, s1 = 0.f;
         if (valid) {
-          p0 = exp2f(__uint_as_float(sv[h]) * sl2e - lse2[h]);
-          p1 = exp2f(__uint_as_float(sv[h + 1]) * sl2e - lse2[h + 1]);
-          s0 = scale * p0 * (__uint_as_float(dv[h]) - dl[h]);
-          s1 = scale * p1 * (__uint_as_float(dv[h + 1]) - dl[h + 1]);
+          // per-head lse and D as 16-byte loads (4 heads), picked apart per pair
+          const float4 L4 = reinterpret_cast<const float4*>(lse2)[h >> 2];
+          const float4 D4 = reinterpret_cast<const float4*>(dl)[h >> 2];
+          const float l0 = (h & 2) ? L4.z : L4.x, l1 = (h & 2) ? L4.w : L4.y;
+          const float d0 = (h & 2) ? D4.z : D4.x, d1 = (h & 2) ? D4.w : D4.y;
+          p0 = exp2f(__uint_as_float(sv[h]) * sl2e - l0);
+          p1 = exp2f(__uint_as_float(sv[h + 1]) * sl2e - l1);
+          s0 = scale * p0 * (__uint_as_float(dv[h]) - d0);
+          s1 = scale * p1 * (__uint_as_float(dv[h + 1]) - d1);
         }
         const __nv_bfloat162 phi = __floats2bfloat162_rn(p0, p1);
         const __nv_bfloat162 shi = __floats2bfloat162_rn(s0, s1);

@@ -308,7 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!need) {
         bool mine = false;
 #pragma unroll
-        for (int h = 0; h < 32; ++h) mine |= z[h] > m_run[h] + kRescaleThreshold;
+        for (int h4 = 0; h4 < 8; ++h4) {  // running max as 16-byte loads (4 heads)
+          const float4 m4 = reinterpret_cast<const float4*>(m_run)[h4];
+          mine |= (z[4 * h4] > m4.x + kRescaleThreshold) | (z[4 * h4 + 1] > m4.y + kRescaleThreshold) |
+                  (z[4 * h4 + 2] > m4.z + kRescaleThreshold) | (z[4 * h4 + 3] > m4.w + kRescaleThreshold);
+        }
         need = named_bar_or(bar_id, 128, mine);
       }
       if (need) {
@@ -355,8 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pk[16], pl[16];
 #pragma unroll
       for (int h = 0; h < 32; h += 2) {
-        const float mu0 = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
-        const float mu1 = (m_run[h + 1] == -INFINITY) ? 0.f : m_run[h + 1];
+        const float4 m4 = reinterpret_cast<const float4*>(m_run)[h >> 2];
+        const float ma = (h & 2) ? m4.z : m4.x, mb = (h & 2) ? m4.w : m4.y;
+        const float mu0 = (ma == -INFINITY) ? 0.f : ma;
+        const float mu1 = (mb == -INFINITY) ? 0.f : mb;
         const float p0 = (z[h] == -INFINITY) ? 0.f : exp2f(z[h] - mu0);
         const float p1 = (z[h + 1] == -INFINITY) ? 0.f : exp2f(z[h + 1] - mu1);
         l_part[h] += p0;
