@@ -584,6 +584,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool aborted = false;
     for (int i = 0; i < ntiles; ++i) {
       const int b = i & 1;
+      // this key row's index does not depend on the MMA: its load overlaps the wait
+      const int j = i * kTile + r;
+      const int ix = (j < n_eff) ? __ldg(idx_row + j) : -1;
       if (!mbar_wait(bar(B_SDP + b), (i >> 1) & 1, s_abort, err)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t tS = tmem_addr(tmem + C_BUF * b + ch * 32, qd * 32, 0);
@@ -592,9 +595,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tS, sv);
       tmem_ld32(tP, dv);
       tmem_ld_wait();
-      const int j = i * kTile + r;
-      int ix = -1;
-      if (j < n_eff) ix = __ldg(idx_row + j);
       const bool valid = ix >= 0 && ix < Tk;
       uint32_t ph[16], pl[16], sh[16], sl[16];
 #pragma unroll

@@ -288,6 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
     bool aborted = false;
     for (int i = 0; i < ntiles; ++i) {
+      // this key row's index does not depend on the MMA: its load overlaps the wait
+      const int j = i * kTile + r;
+      const int ixw = (j < n_eff) ? __ldg(idx_row + j) : -1;
       const bool got = mbar_wait(bar_s, i & 1, s_abort, err);
       // every thread of the half leaves together, or none does (named barriers follow)
       if (named_bar_or(bar_id, 128, !got)) { aborted = true; break; }
@@ -295,12 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sv[32];
       tmem_ld32(tmem_addr(tS, qd * 32, ch * 32), sv);
       tmem_ld_wait();
-      const int j = i * kTile + r;
-      bool valid = false;
-      if (j < n_eff) {
-        const int ix = __ldg(idx_row + j);
-        valid = ix >= 0 && ix < Tk;
-      }
+      const bool valid = ixw >= 0 && ixw < Tk;
       float z[32];
 #pragma unroll
       for (int h = 0; h < 32; ++h) z[h] = valid ? __uint_as_float(sv[h]) * sl2e : -INFINITY;
