@@ -108,9 +108,11 @@ def dist_init():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
+        import torch
         import torch.distributed as dist
 
-        backend = "nccl"
+        # one process per GPU over NCCL; gloo where no GPU is visible (host-side tests of the replica path)
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
         dist.init_process_group(backend=backend)
     return rank, world, local
 
