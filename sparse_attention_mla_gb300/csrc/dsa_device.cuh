@@ -1,5 +1,5 @@
 // dsa_device.cuh -- sm_103a device helpers: mbarriers with bounded waits, TMA
-// (tiled and gather4), tcgen05 (TMEM alloc, MMA, commit, ld/st) and the
+// tiled loads, cp.async, tcgen05 (TMEM alloc, MMA, commit, ld/st) and the
 // shared-memory / instruction descriptors used by the DSA kernels.
 #pragma once
 #include <cuda.h>
@@ -128,16 +128,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           dst),
       "l"(map), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-// Gather of four rows (r0..r3) of one column box starting at inner coordinate
-// col; the map's box is one row high.  Writes 4 consecutive box rows at dst.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int32_t col, int32_t r0,
-                                            int32_t r1, int32_t r2, int32_t r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
       : "memory");
 }
 

@@ -23,11 +23,14 @@
 //    tokens' selections run in parallel.
 //  * Selection: each token keeps a shared-memory buffer of candidates
 //    (score, index) that beat its running threshold.  Candidates are appended
-//    in ascending key order (a block-wide scan, not atomics), and a full
-//    buffer is compacted to the best K by an 8-bit radix select on the
-//    order-preserving integer image of the score; ties at the threshold keep
-//    the earliest (= lowest-index) entries, and the compaction is stable, so
-//    the buffer stays sorted by index and the output needs no sort.
+//    in ascending key order (a block-wide scan, not atomics).  A full buffer
+//    is compacted by a two-pass (16-bit) radix select on the order-preserving
+//    integer image of the score: every candidate at or above the bucket that
+//    holds the K-th best is kept, a superset of the final top-K, and the
+//    threshold rises to that bucket.  The final selection is an exact
+//    four-pass select where ties at the threshold keep the earliest
+//    (= lowest-index) entries.  Every compaction is stable, so the buffer
+//    stays sorted by index and the output needs no sort.
 #include <climits>
 #include <cmath>
 
