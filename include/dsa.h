@@ -99,6 +99,25 @@ dsa_status_t dsa_indexer_topk(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, 
                               dsa_stream_t stream);
 
 /*
+ * dsa_indexer_topk_with_scores -- diagnostic form of dsa_indexer_topk: the same
+ * kernel code and the same results (topk_idx, topk_len), and in addition the
+ * fp32 score of every key of the window of rows [score_row0, score_row0 +
+ * score_rows), stored at scores[(t - score_row0) * T_k + key] (device fp32
+ * [score_rows, T_k], caller-owned; entries outside a row's window are left
+ * untouched).  These are exactly the values the selection ranked, so a test
+ * can check the selection itself (order by score descending, ties to the
+ * lower index) independently of fp32 rounding.  The pages have no
+ * counterpart; this entry is for tests and diagnostics.  Errors as for
+ * dsa_indexer_topk, plus DSA_ERR_INVALID_ARGUMENT unless 0 <= score_row0,
+ * score_row0 + score_rows <= T and scores != NULL when score_rows > 0.
+ */
+dsa_status_t dsa_indexer_topk_with_scores(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
+                                          const int32_t* seq_start, int32_t T, int32_t T_k, int32_t Hi, int32_t Di,
+                                          int32_t K, int32_t* topk_idx, int32_t* topk_len, float* scores,
+                                          int32_t score_row0, int32_t score_rows, void* workspace,
+                                          size_t workspace_bytes, dsa_stream_t stream);
+
+/*
  * dsa_sparse_mla_fwd -- absorbed sparse MLA forward (MQA over one latent KV).
  * Source: [DSA-blog] "How DSA works" and "Why DSA needs fused kernels";
  * [cudnn_dsa] cudnn_sparse_attention / _CudnnSparseAttention.forward (q

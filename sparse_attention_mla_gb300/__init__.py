@@ -25,6 +25,7 @@ __all__ = [
     "declared_symbols",
     "dsa_packed_metadata",
     "dsa_indexer_topk",
+    "dsa_indexer_topk_with_scores",
     "dsa_sparse_mla_fwd",
     "dsa_sparse_mla_bwd",
     "dsa_read_device_status",
@@ -89,6 +90,8 @@ def load_library(path: str | None = None):
         lib.dsa_indexer_topk_workspace_size.argtypes = [_I, _I]
         lib.dsa_indexer_topk_workspace_size.restype = _SZ
         lib.dsa_indexer_topk.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]
+        lib.dsa_indexer_topk_with_scores.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _I, _I, _P,
+                                                     _SZ, _P]
         lib.dsa_sparse_mla_fwd_workspace_size.argtypes = [_I, _I]
         lib.dsa_sparse_mla_fwd_workspace_size.restype = _SZ
         lib.dsa_sparse_mla_fwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _SZ, _P]
@@ -104,8 +107,8 @@ def load_library(path: str | None = None):
         lib.dsa_sparse_mla_bwd_noalloc.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P,
                                                    _P, _I, _P, _P]
         lib.dsa_sparse_mla_bwd_noalloc.restype = ctypes.c_int
-        for name in ("dsa_packed_metadata", "dsa_indexer_topk", "dsa_sparse_mla_fwd", "dsa_sparse_mla_bwd",
-                     "dsa_read_device_status"):
+        for name in ("dsa_packed_metadata", "dsa_indexer_topk", "dsa_indexer_topk_with_scores",
+                     "dsa_sparse_mla_fwd", "dsa_sparse_mla_bwd", "dsa_read_device_status"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -193,6 +196,29 @@ def dsa_indexer_topk(q_idx, k_idx, head_weights, seq_start, K: int, topk_idx=Non
                                 int(K), _ptr(topk_idx), _ptr(topk_len), _ptr(ws), wsb, _stream(dev)),
            "dsa_indexer_topk")
     return topk_idx, topk_len
+
+
+def dsa_indexer_topk_with_scores(q_idx, k_idx, head_weights, seq_start, K: int, score_row0: int,
+                                 score_rows: int, workspace=None):
+    """Diagnostic form of dsa_indexer_topk -> (topk_idx, topk_len, scores fp32 [score_rows, T_k]): the
+    fp32 score of every window key of rows score_row0 .. score_row0 + score_rows - 1 (NaN elsewhere)."""
+    lib = load_library()
+    _need(q_idx, "q_idx", torch.bfloat16, 3)
+    dev = q_idx.device
+    _need(k_idx, "k_idx", torch.bfloat16, 2, dev)
+    _need(head_weights, "head_weights", torch.float32, 2, dev)
+    _need(seq_start, "seq_start", torch.int32, 1, dev)
+    T, Hi, Di = q_idx.shape
+    Tk = k_idx.shape[0]
+    topk_idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+    topk_len = torch.empty(T, dtype=torch.int32, device=dev)
+    scores = torch.full((score_rows, Tk), float("nan"), dtype=torch.float32, device=dev)
+    ws, wsb = _workspace("indexer", T, K, dev, workspace)
+    _check(lib.dsa_indexer_topk_with_scores(_ptr(q_idx), _ptr(k_idx), _ptr(head_weights), _ptr(seq_start), T, Tk,
+                                            Hi, Di, int(K), _ptr(topk_idx), _ptr(topk_len), _ptr(scores),
+                                            int(score_row0), int(score_rows), _ptr(ws), wsb, _stream(dev)),
+           "dsa_indexer_topk_with_scores")
+    return topk_idx, topk_len, scores
 
 
 def dsa_sparse_mla_fwd(q, kv, topk_idx, softmax_scale: float, topk_len=None, out=None, lse=None,

@@ -218,11 +218,15 @@ __device__ uint32_t compact(const Half& hf, float* cs, int* ci, int cnt, int tar
   return v;
 }
 
+// kScores: the diagnostic variant that also stores, for rows [score_row0,
+// score_row0 + score_rows), the fp32 score of every key of the row's window
+// (scores[(t - score_row0) * Tk + key]), i.e. exactly the values it selects from.
+template <bool kScores>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_topk_kernel(const __grid_constant__ CUtensorMap k_map, const __nv_bfloat16* __restrict__ q_idx,
                         const float* __restrict__ w, const int32_t* __restrict__ seq_start, int T, int Tk, int Hi,
                         int K, int32_t* __restrict__ topk_idx, int32_t* __restrict__ topk_len,
-                        int* __restrict__ err) {
+                        int* __restrict__ err, float* __restrict__ scores, int score_row0, int score_rows) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(smem + OFF_Q);
@@ -376,6 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         sc = fmaf(wv.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), sc);
       }
       const bool in = key >= win_lo && key <= win_hi;
+      if (kScores && in) {
+        const int rr = t0 + k - score_row0;
+        if (rr >= 0 && rr < score_rows) scores[(size_t)rr * Tk + key] = sc;
+      }
       const bool acc = in && ordered(sc) > thr;
       const int2 pos = half_scan(hf, acc, parity);
       parity ^= 1;
@@ -429,21 +437,25 @@ extern "C" size_t dsa_indexer_topk_workspace_size(int32_t T, int32_t K) {
   return kErrorWordBytes;
 }
 
-extern "C" dsa_status_t dsa_indexer_topk(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
-                                         const int32_t* seq_start, int32_t T, int32_t T_k, int32_t Hi, int32_t Di,
-                                         int32_t K, int32_t* topk_idx, int32_t* topk_len, void* workspace,
-                                         size_t workspace_bytes, dsa_stream_t stream) {
-  const char* who = "dsa_indexer_topk";
+namespace dsa {
+namespace idx {
+template <bool kScores>
+static dsa_status_t run(const char* who, const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
+                        const int32_t* seq_start, int32_t T, int32_t T_k, int32_t Hi, int32_t Di, int32_t K,
+                        int32_t* topk_idx, int32_t* topk_len, float* scores, int32_t score_row0, int32_t score_rows,
+                        void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
   if (T < 0 || T_k < 1) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: need T >= 0 and T_k >= 1", who);
   if (T_k < T) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: T_k (%d) must be >= T (%d)", who, T_k, T);
-  if (Hi < 1 || Hi > idx::kHeads) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: Hi must be in [1, 64] (got %d)", who, Hi);
-  if (Di != idx::kDi) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: Di must be 128 (got %d)", who, Di);
-  if (K < 1 || K > idx::kMaxK) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: K must be in [1, 2048] (got %d)", who, K);
+  if (Hi < 1 || Hi > kHeads) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: Hi must be in [1, 64] (got %d)", who, Hi);
+  if (Di != kDi) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: Di must be 128 (got %d)", who, Di);
+  if (K < 1 || K > kMaxK) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: K must be in [1, 2048] (got %d)", who, K);
   if (!k_idx) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: k_idx is NULL", who);
   if (T > 0 && (!q_idx || !head_weights || !seq_start || !topk_idx))
     return fail(DSA_ERR_INVALID_ARGUMENT, "%s: null tensor pointer", who);
   if (!aligned16(k_idx) || (T > 0 && !aligned16(q_idx)))
     return fail(DSA_ERR_INVALID_ARGUMENT, "%s: q_idx and k_idx must be 16-byte aligned", who);
+  if (kScores && (score_rows < 0 || score_row0 < 0 || score_row0 + score_rows > T || (score_rows > 0 && !scores)))
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: need 0 <= score_row0, score_row0 + score_rows <= T and scores", who);
   dsa_status_t st = check_workspace(workspace, workspace_bytes, dsa_indexer_topk_workspace_size(T, K), who);
   if (st != DSA_OK) return st;
   if ((st = check_device()) != DSA_OK) return st;
@@ -451,21 +463,39 @@ extern "C" dsa_status_t dsa_indexer_topk(const dsa_bf16_t* q_idx, const dsa_bf16
   if ((st = clear_error_word(workspace, s)) != DSA_OK) return st;
   if (T == 0) return ok();
   CUtensorMap map;
-  if ((st = make_map_2d_bf16(&map, k_idx, (uint64_t)T_k, (uint64_t)idx::kDi, (uint64_t)idx::kDi, 64, idx::kTile)) !=
-      DSA_OK)
-    return st;
+  if ((st = make_map_2d_bf16(&map, k_idx, (uint64_t)T_k, (uint64_t)kDi, (uint64_t)kDi, 64, kTile)) != DSA_OK) return st;
   static bool configured = false;
   if (!configured) {
-    if ((st = cuda_check(cudaFuncSetAttribute(idx::indexer_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              idx::TOTAL),
+    if ((st = cuda_check(cudaFuncSetAttribute(indexer_topk_kernel<kScores>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, TOTAL),
                          "configuring indexer_topk_kernel")))
       return st;
     configured = true;
   }
-  const int nblk = (T + idx::kTokens - 1) / idx::kTokens;
-  idx::indexer_topk_kernel<<<nblk, idx::kThreads, idx::TOTAL, s>>>(
+  const int nblk = (T + kTokens - 1) / kTokens;
+  indexer_topk_kernel<kScores><<<nblk, kThreads, TOTAL, s>>>(
       map, reinterpret_cast<const __nv_bfloat16*>(q_idx), head_weights, seq_start, T, T_k, Hi, K, topk_idx, topk_len,
-      reinterpret_cast<int*>(workspace));
+      reinterpret_cast<int*>(workspace), scores, score_row0, score_rows);
   if ((st = cuda_check(cudaGetLastError(), "launching indexer_topk_kernel"))) return st;
   return ok();
+}
+}  // namespace idx
+}  // namespace dsa
+
+extern "C" dsa_status_t dsa_indexer_topk(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
+                                         const int32_t* seq_start, int32_t T, int32_t T_k, int32_t Hi, int32_t Di,
+                                         int32_t K, int32_t* topk_idx, int32_t* topk_len, void* workspace,
+                                         size_t workspace_bytes, dsa_stream_t stream) {
+  return idx::run<false>("dsa_indexer_topk", q_idx, k_idx, head_weights, seq_start, T, T_k, Hi, Di, K, topk_idx,
+                         topk_len, nullptr, 0, 0, workspace, workspace_bytes, stream);
+}
+
+extern "C" dsa_status_t dsa_indexer_topk_with_scores(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx,
+                                                     const float* head_weights, const int32_t* seq_start, int32_t T,
+                                                     int32_t T_k, int32_t Hi, int32_t Di, int32_t K, int32_t* topk_idx,
+                                                     int32_t* topk_len, float* scores, int32_t score_row0,
+                                                     int32_t score_rows, void* workspace, size_t workspace_bytes,
+                                                     dsa_stream_t stream) {
+  return idx::run<true>("dsa_indexer_topk_with_scores", q_idx, k_idx, head_weights, seq_start, T, T_k, Hi, Di, K,
+                        topk_idx, topk_len, scores, score_row0, score_rows, workspace, workspace_bytes, stream);
 }

@@ -117,3 +117,38 @@ def test_indexer_increasing_scores_pick_window_end():
     for t in range(T):
         n = min(K, t + 1)
         assert gidx[t, :n].tolist() == list(range(t - n + 1, t + 1))
+
+
+def _exact_topk(scores_row, lo, hi, K):
+    """The selection rule on given fp32 values: score descending, ties to the lower index; ascending output."""
+    keys = np.arange(lo, hi + 1)
+    sc = scores_row[lo:hi + 1].astype(np.float64)  # fp32 values, widened exactly
+    order = np.lexsort((keys, -sc))
+    return np.sort(keys[order[:min(K, len(keys))]])
+
+
+@pytest.mark.parametrize("T,K,cut,row0,nrows", [(700, 200, [0, 100, 350, 353, 700], 0, 700),
+                                                (5000, 2048, [0, 5000], 3800, 1200)])
+def test_indexer_selection_is_exact_on_its_own_scores(T, K, cut, row0, nrows):
+    # Consistency of the selection stage: the kernel's own fp32 scores, ranked by the rule, give
+    # exactly its indices (candidate buffer, approximate and exact compactions, tie-breaking).
+    # Independent of fp32 rounding; the set parity against the fp64 oracle is checked above.
+    x = synth.indexer_inputs(T, 64, 128, seed=21)
+    x["w"][:, 7] = 0.0  # a zero-weight head: its ReLU terms drop out exactly
+    cu = torch.tensor(cut, dtype=torch.int32)
+    start, _, _, _ = dsa.dsa_packed_metadata(cu.to(DEV), T)
+    q, k, w = x["q_idx"].to(DEV), x["k_idx"].to(DEV), x["w"].to(DEV)
+    ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
+    idx, ln, sc = dsa.dsa_indexer_topk_with_scores(q, k, w, start, K, row0, nrows, workspace=ws)
+    assert dsa.dsa_read_device_status(ws) == 0
+    idx0, ln0 = dsa.dsa_indexer_topk(q, k, w, start, K)  # the production kernel selects the same
+    assert torch.equal(idx0, idx) and torch.equal(ln0, ln)
+    idx, ln, sc, st = idx.cpu().numpy(), ln.cpu().numpy(), sc.cpu().numpy(), start.cpu().numpy()
+    for r in range(nrows):
+        t = row0 + r
+        want = _exact_topk(sc[r], st[t], t, K)
+        n = len(want)
+        assert ln[t] == n
+        assert np.array_equal(idx[t, :n], want), f"row {t}"
+        assert np.all(idx[t, n:] == -1)
+        assert np.all(np.isfinite(sc[r, st[t]:t + 1]))  # every window key was scored
