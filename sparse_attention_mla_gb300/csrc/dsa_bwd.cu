@@ -19,14 +19,17 @@
 //  * P is recomputed from the saved lse (no running max).  D comes from a
 //    small kernel; when the forward's bf16 residual of O is given, D uses the
 //    unrounded O, so that sum_j dS_j = 0 holds to fp32 accuracy.
-//  * Main loop, per 128-slot tile: S^T = KV Q^T and dP^T = V dO^T (keys on
-//    the MMA M axis, N = 64 heads) into one of TWO TMEM buffers; the softmax
-//    backward turns them, in place, into dS (x scale) and P, each split into
-//    bf16 hi + lo parts (dkv accurate to about fp32 even for keys shared by
-//    many rows); dKV = dS^T Q + P^T dO is then formed 64 channels at a time
-//    with all four A operands read from TMEM, into one of FOUR TMEM staging
-//    slots that the flush warps drain into L2 reductions.  With two S/dP
-//    buffers and four staging slots, the next tile's S^T / dP^T and softmax
+//  * Main loop, per 128-slot tile: [S^T | dP^T] = KV [Q | dO]^T (keys on the
+//    MMA M axis; Q and dO chunks side by side give N = 128) into one of TWO
+//    TMEM buffers; the softmax backward turns them, in place, into dS (x
+//    scale) and P, each split into bf16 hi + lo parts (dkv accurate to about
+//    fp32 even for keys shared by many rows); dKV = dS^T Q + P^T dO is then
+//    formed 128 channels at a time (N = 128) with all four A operands read
+//    from TMEM, into one of TWO TMEM staging slots.  The slots are drained
+//    into L2 reductions by the flush warps and the math warps (64 channels
+//    each, read out of TMEM and released at once, then transposed so that
+//    every reduction instruction covers 4 rows x 128 bytes).  With two S/dP
+//    buffers and two staging slots, the next tile's S^T / dP^T and softmax
 //    run while the reductions of this tile are still in flight.
 //  * dq needs dS for every tile of the token but the main loop has no TMEM
 //    left for its accumulator, so dS hi of each tile is also written to a
@@ -41,9 +44,10 @@
 //    work is ready, dKV groups first, so that the tensor core follows the
 //    reductions instead of a fixed program order.
 //
-// Warp roles: warp 0 issues MMAs and owns TMEM; warps 1-3 gather; warps 4-11
-// run the softmax backward and the dq epilogue; warps 12-15 drain the dKV
-// staging slots into L2 reductions.
+// Warp roles: warp 0 issues MMAs and owns TMEM; warps 1-3 gather (with warps
+// 4-11 in the end phase); warps 4-11 run the softmax backward, drain their
+// share of the dKV groups and write dq; warps 12-15 drain the rest of the dKV
+// groups.
 #include <cmath>
 
 #include "dsa_device.cuh"
@@ -365,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // A drain warp's part of staged dKV group G (group g of its tile): wait for it (every drain warp
   // waits for every group, in order, so that each slot barrier is read phase by phase), load the
-  // halves this warp owns, release the slot, then reduce them into dkv.
+  // half this warp owns if any, release the slot, then reduce it into dkv.
   auto drain_group = [&](int G, int g, int role, int ix, uint32_t fst) -> bool {
     const int s = G & (kStage - 1);
     if (!mbar_wait(bar(B_STF + s), (G / kStage) & 1, s_abort, err)) return false;
