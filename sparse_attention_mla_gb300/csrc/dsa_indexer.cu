@@ -71,6 +71,16 @@ constexpr int M_HIST = M_WCNT + 128;    // int [4 tokens][256]
 constexpr int M_SEL = M_HIST + 4096;    // int [4 tokens][4]
 static_assert(M_SEL + 64 <= MISC, "misc layout");
 
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+// d = a * b + c on two fp32 lanes at once (round to nearest, as fmaf per lane).
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t ordered(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -369,16 +379,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tile0 = (kt0 + i) * kTile;
       if (tile0 > win_hi || tile0 + kTile <= win_lo) continue;  // whole tile outside this token's window (uniform)
       const int key = tile0 + hf.tid;
-      float sc = 0.f;
+      // sum_h w_h * ReLU(s_h) with packed fp32 pairs: two running sums (even / odd heads)
+      uint64_t acc2 = 0;
       const float4* wr4 = reinterpret_cast<const float4*>(wr);
 #pragma unroll
       for (int h4 = 0; h4 < kHeads / 4; ++h4) {
         const float4 wv = wr4[h4];
-        sc = fmaf(wv.x, fmaxf(__uint_as_float(v[4 * h4]), 0.f), sc);
-        sc = fmaf(wv.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), sc);
-        sc = fmaf(wv.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), sc);
-        sc = fmaf(wv.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), sc);
+        const uint64_t w01 = pack_f32x2(wv.x, wv.y), w23 = pack_f32x2(wv.z, wv.w);
+        const uint64_t r01 = pack_f32x2(fmaxf(__uint_as_float(v[4 * h4]), 0.f), fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f));
+        const uint64_t r23 =
+            pack_f32x2(fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f));
+        acc2 = fma_f32x2(w01, r01, acc2);
+        acc2 = fma_f32x2(w23, r23, acc2);
       }
+      const float sc = __uint_as_float((uint32_t)acc2) + __uint_as_float((uint32_t)(acc2 >> 32));
       const bool in = key >= win_lo && key <= win_hi;
       if (kScores && in) {
         const int rr = t0 + k - score_row0;
