@@ -80,6 +80,24 @@ constexpr int M_RED = 256;             // float [4][64]
 constexpr int M_STAT = M_RED + 1024;   // float [64]: running max per head
 constexpr int M_LSUM = M_STAT + 256;   // float [64]: softmax denominator per head
 
+// Element-wise fp32 on two lanes at once (add.f32x2 / sub.f32x2, round to nearest as the scalar ops).
+__device__ __forceinline__ float2 f32x2_add(float2 a, float2 b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(r)
+      : "l"((uint64_t)__float_as_uint(a.x) | ((uint64_t)__float_as_uint(a.y) << 32)),
+        "l"((uint64_t)__float_as_uint(b.x) | ((uint64_t)__float_as_uint(b.y) << 32)));
+  return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
+}
+__device__ __forceinline__ float2 f32x2_sub(float2 a, float2 b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;"
+      : "=l"(r)
+      : "l"((uint64_t)__float_as_uint(a.x) | ((uint64_t)__float_as_uint(a.y) << 32)),
+        "l"((uint64_t)__float_as_uint(b.x) | ((uint64_t)__float_as_uint(b.y) << 32)));
+  return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
+}
+
 // Transposing butterfly: v[0..31] per lane (lane = key, index = head) ->
 // lane l returns the reduction over the warp's 32 keys of head l.
 template <bool MAX>
@@ -359,16 +377,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h = 0; h < 32; h += 2) {
         const float4 m4 = reinterpret_cast<const float4*>(m_run)[h >> 2];
         const float ma = (h & 2) ? m4.z : m4.x, mb = (h & 2) ? m4.w : m4.y;
-        const float mu0 = (ma == -INFINITY) ? 0.f : ma;
+        const float mu0 = (ma == -INFINITY) ? 0.f : ma;  // a head with no valid slot yet: keep z - mu = -inf
         const float mu1 = (mb == -INFINITY) ? 0.f : mb;
-        const float p0 = (z[h] == -INFINITY) ? 0.f : exp2f(z[h] - mu0);
-        const float p1 = (z[h + 1] == -INFINITY) ? 0.f : exp2f(z[h + 1] - mu1);
-        l_part[h] += p0;
-        l_part[h + 1] += p1;
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
-        const float2 hf = __bfloat1622float2(hi);
+        // masked slots have z = -inf, so exp2 gives +0 without a test; pairs of lanes in packed fp32
+        const float2 e = f32x2_sub(make_float2(z[h], z[h + 1]), make_float2(mu0, mu1));
+        const float2 pp = make_float2(exp2f(e.x), exp2f(e.y));
+        const float2 ls = f32x2_add(make_float2(l_part[h], l_part[h + 1]), pp);
+        l_part[h] = ls.x;
+        l_part[h + 1] = ls.y;
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(pp.x, pp.y);
+        const float2 lo = f32x2_sub(pp, __bfloat1622float2(hi));
         pk[h >> 1] = *reinterpret_cast<const uint32_t*>(&hi);
-        pl[h >> 1] = pack_bf16x2(p0 - hf.x, p1 - hf.y);
+        pl[h >> 1] = pack_bf16x2(lo.x, lo.y);
       }
       // P^T row r: 64 heads x bf16 = 128 B; this half owns units ch*4 .. ch*4+3.
 #pragma unroll
