@@ -33,9 +33,11 @@
 //  * P^T is written into the shared-memory slot of the tile's RoPE channels
 //    (no longer needed once S^T is done), which keeps the working set
 //    (Q 72 KiB + tile 144 KiB) inside one SM's shared memory.  P is split into
-//    bf16 hi + lo parts that go through the same slot one after the other
-//    (P_hi . V, then P_lo . V), so O carries P to about fp32 accuracy and the
-//    backward's D = <dO, O> is consistent with the exact softmax.
+//    bf16 hi + lo parts, so O carries P to about fp32 accuracy and the
+//    backward's D = <dO, O> is consistent with the exact softmax.  The lo part
+//    of key rows 0..63 has an 8 KiB slot of its own and is written with the hi
+//    part; the lo part of rows 64..127 goes into the P slot once P_hi . V has
+//    read it, while the tensor core runs the first half of P_lo . V.
 //  * The epilogue stages O (and, on request, the bf16 residual O - bf16(O))
 //    through shared memory for coalesced 16-byte stores.
 //
@@ -67,7 +69,10 @@ struct Smem {
   static constexpr int OFF_P = (DQK == 576) ? OFF_KV + 8 * KV_CHUNK : OFF_KV + NCH * KV_CHUNK;
   static constexpr int OFF_MISC = (DQK == 576) ? OFF_KV + NCH * KV_CHUNK : OFF_P + KV_CHUNK;
   static constexpr int MISC = 2048;
-  static constexpr int TOTAL = OFF_MISC + MISC + 1024;  // + alignment slack
+  // P_lo^T of key rows 0..63 (8 KiB, same layout as the first half of the P slot); rows 64..127
+  // follow the hi part through the P slot
+  static constexpr int OFF_PLO = OFF_MISC + MISC;
+  static constexpr int TOTAL = OFF_PLO + KV_CHUNK / 2 + 1024;  // + alignment slack
   static_assert(TOTAL <= 232448, "shared memory budget");
 };
 
@@ -147,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + L::OFF_Q);
   const uint32_t sKV = smem_u32(smem + L::OFF_KV);
   const uint32_t sP = smem_u32(smem + L::OFF_P);
+  const uint32_t sPlo = smem_u32(smem + L::OFF_PLO);
   uint8_t* misc = smem + L::OFF_MISC;
   const uint32_t bar_kv = smem_u32(misc + M_BAR_KV), bar_pv = smem_u32(misc + M_BAR_PV);
   const uint32_t bar_s = smem_u32(misc + M_BAR_S), bar_p = smem_u32(misc + M_BAR_P);
@@ -169,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int m = 0; m < 4; ++m) mbar_init(bar_pv + 8 * m, 1);
     mbar_init(bar_s, 1);
     mbar_init(bar_p, 8);
-    mbar_init(bar_plo, 8);
+    mbar_init(bar_plo, 4);  // the warps of key rows 64..127 (lane quadrants 2, 3)
     mbar_init(bar_pvh, 1);
     mbar_init(bar_fin, 1);
     *s_neff = 0;
@@ -243,10 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (stop) break;
         mma_commit(bar_s);
-        // O^T += V^T P_hi^T, then (P_lo in the same slot) O^T += V^T P_lo^T
+        // O^T += V^T P_hi^T, then O^T += V^T P_lo^T: key rows 0..63 from their own slot while
+        // the workers move rows 64..127 into the P slot
         if (!mbar_wait(bar_p, i & 1, s_abort, err)) break;
         tc_fence_after();
         const uint64_t pb0 = sdesc_sw128(sP, L::KV_CHUNK, 1024);
+        const uint64_t lb0 = sdesc_sw128(sPlo, L::KV_CHUNK, 1024);
         const uint64_t va0 = sdesc_sw128(sKV, L::KV_CHUNK, 1024);
         constexpr uint64_t kPair = (2 * L::KV_CHUNK) >> 4;  // descriptor step between channel pairs
 #pragma unroll
@@ -257,12 +265,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                    (i > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(bar_pvh);
+#pragma unroll
+        for (int m = 0; m < kDv / 128; ++m) {
+#pragma unroll
+          for (int k = 0; k < kTile / 32; ++k)
+            mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), lb0 + (uint64_t)(k * 128), kIdPV, 1u);
+        }
         if (!mbar_wait(bar_plo, i & 1, s_abort, err)) break;
         tc_fence_after();
 #pragma unroll
         for (int m = 0; m < kDv / 128; ++m) {
 #pragma unroll
-          for (int k = 0; k < kTile / 16; ++k)
+          for (int k = kTile / 32; k < kTile / 16; ++k)
             mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV, 1u);
           mma_commit(bar_pv + 8 * m);
         }
@@ -394,21 +408,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int uu = 0; uu < 4; ++uu)
         st_shared_v4(sP + sw128_off(r, ch * 4 + uu), pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2], pk[4 * uu + 3]);
+      if (qd < 2) {  // key rows 0..63: the lo part has its own slot
+#pragma unroll
+        for (int uu = 0; uu < 4; ++uu)
+          st_shared_v4(sPlo + sw128_off(r, ch * 4 + uu), pl[4 * uu], pl[4 * uu + 1], pl[4 * uu + 2], pl[4 * uu + 3]);
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p);
-      // the lo part goes into the same slot once V^T P_hi^T has read it
+      // key rows 64..127: the lo part goes into the P slot once V^T P_hi^T has read it
       {
-        const bool okh = mbar_wait(bar_pvh, i & 1, s_abort, err);
-        if (okh) {
+        bool okh = true;
+        if (qd >= 2) {
+          okh = mbar_wait(bar_pvh, i & 1, s_abort, err);
+          if (okh) {
 #pragma unroll
-          for (int uu = 0; uu < 4; ++uu)
-            st_shared_v4(sP + sw128_off(r, ch * 4 + uu), pl[4 * uu], pl[4 * uu + 1], pl[4 * uu + 2], pl[4 * uu + 3]);
-          fence_proxy_async_smem();
+            for (int uu = 0; uu < 4; ++uu)
+              st_shared_v4(sP + sw128_off(r, ch * 4 + uu), pl[4 * uu], pl[4 * uu + 1], pl[4 * uu + 2], pl[4 * uu + 3]);
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_plo);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_plo);
         if (named_bar_or(bar_id, 128, !okh)) { aborted = true; break; }
       }
       // ---- gather the next tile, chunk pair by chunk pair as P.V frees them ----
