@@ -41,6 +41,31 @@ def mla_flops(n_valid: int) -> tuple[float, float]:
     return 2.0 * H * n_valid * (DQK + DV), 2.0 * H * n_valid * (3 * DQK + 2 * DV)
 
 
+# L2 rates of this GPU for the two access patterns the MLA kernels live on, measured by
+# standalone microbenchmarks on a GB300 (all SMs, clocks at 2070 MHz): fp32 reductions of
+# 4-row x 128-byte segments at the selected rows (red.global.add.v4.f32, the backward's
+# pattern) and 16-byte cp.async gathers of selected 1152-byte rows.
+L2_RED_TBS = 6.9
+L2_GATHER_TBS = 8.9
+
+
+def l2_model(n_valid: int, n_tiles: int, fwd_ms: float, bwd_ms: float) -> dict:
+    """Time the MLA kernels would take if their L2 traffic alone ran at the rates above.
+
+    Backward per valid slot: one fp32 dKV row reduced (4 * DQK bytes) and the kv row gathered
+    twice (2 * 2 * DQK); per 128-slot tile, the bf16 dS tile written to and read back from the
+    scratch (2 * 128 * 64 * 2 bytes).  Forward: the kv row gathered once (2 * DQK)."""
+    red = 4.0 * DQK * n_valid
+    gat_b = 2.0 * 2 * DQK * n_valid + 2.0 * n_tiles * 128 * 64 * 2
+    gat_f = 2.0 * DQK * n_valid
+    t_b = (red / (L2_RED_TBS * 1e12) + gat_b / (L2_GATHER_TBS * 1e12)) * 1e3
+    t_f = gat_f / (L2_GATHER_TBS * 1e12) * 1e3
+    return {"rates_tbs": {"reduction": L2_RED_TBS, "gather": L2_GATHER_TBS},
+            "bwd": {"reduction_gb": round(red / 1e9, 2), "gather_gb": round(gat_b / 1e9, 2),
+                    "model_ms": round(t_b, 3), "frac": round(t_b / bwd_ms, 4)},
+            "fwd": {"gather_gb": round(gat_f / 1e9, 2), "model_ms": round(t_f, 3), "frac": round(t_f / fwd_ms, 4)}}
+
+
 def load_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -249,6 +274,7 @@ def run_cuda(args, rank, world, local):
         if st != 0:
             raise RuntimeError(f"device status {st} after warm-up")
     n_valid = int(topk_len.sum().item())
+    n_tiles = int(((topk_len + 127) // 128).sum().item()) * ((H + 63) // 64)
     f_fwd, f_bwd = mla_flops(n_valid)
 
     sampler = ClockSampler(local)
@@ -307,6 +333,7 @@ def run_cuda(args, rank, world, local):
                           "sparse_mla_bwd": round(bwd_ms, 3)},
         "n_valid_slots": n_valid,
         "roofline": roofline,
+        "l2_model": l2_model(n_valid, n_tiles, fwd_ms, bwd_ms),
         "clocks": clocks,
         "gpu_launches": 4 * args.steps,
         "e2e": e2e,

@@ -282,19 +282,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= 2) {
     const int tid = threadIdx.x - 64;
-    // Q rows (token k, head h) -> 2 chunks of [256 rows x 128 B], swizzled; padding rows zero
+    // Q rows (token k, head h) -> 2 chunks of [256 rows x 128 B], swizzled; padding rows are
+    // zero-filled without a read.  All copies are in flight at once (cp.async), one wait.
     for (int u = tid; u < kN * 16; u += kEpi) {
       const int row = u >> 4, c = (u >> 3) & 1, uc = u & 7;
       const int k = row / kHeads, h = row - k * kHeads;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (k < nt && h < Hi)
-        v = __ldg(reinterpret_cast<const uint4*>(q_idx + ((size_t)(t0 + k) * Hi + h) * kDi + c * 64 + uc * 8));
-      st_shared_v4(sQ + c * Q_CHUNK + sw128_off(row, uc), v.x, v.y, v.z, v.w);
+      const bool ok = k < nt && h < Hi;
+      cp_async16(sQ + c * Q_CHUNK + sw128_off(row, uc),
+                 q_idx + (ok ? ((size_t)(t0 + k) * Hi + h) * kDi + c * 64 + uc * 8 : 0), ok ? 16u : 0u);
     }
     for (int u = tid; u < kTokens * kHeads; u += kEpi) {
       const int k = u / kHeads, h = u - k * kHeads;
       s_w[u] = (k < nt && h < Hi) ? __ldg(w + (size_t)(t0 + k) * Hi + h) : 0.f;
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     fence_proxy_async_smem();
   }
   __syncthreads();
