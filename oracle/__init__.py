@@ -50,10 +50,14 @@ def _load():
             I = ctypes.c_int
             lib.oracle_packed_metadata.argtypes = [P, I, I, P, P, P, P]
             lib.oracle_packed_metadata.restype = I
+            lib.oracle_packed_metadata_cp.argtypes = [P, P, I, I, P, P, I, P, P, P, P]
+            lib.oracle_packed_metadata_cp.restype = I
             lib.oracle_indexer_scores.argtypes = [P, P, P, I, I, P, P, ctypes.c_int64, P, P]
             lib.oracle_indexer_scores.restype = None
             lib.oracle_indexer_topk.argtypes = [P, P, P, P, P, I, I, I, I, P, P, P]
             lib.oracle_indexer_topk.restype = None
+            lib.oracle_indexer_topk_window.argtypes = [P, P, P, P, P, I, I, I, I, P, P, P]
+            lib.oracle_indexer_topk_window.restype = None
             lib.oracle_sparse_mla_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, P]
             lib.oracle_sparse_mla_fwd.restype = None
             lib.oracle_sparse_mla_bwd.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, P, P]
@@ -99,6 +103,30 @@ def packed_metadata(cu_seqlens, total_tokens: int):
     return start[:T], clen[:T], int(mx[0]), int(ne[0])
 
 
+def packed_metadata_cp(cu_seqlens, total_key_tokens: int, query_indices=None, cu_seqlens_padded=None,
+                       padding_mask=None, T_q: int | None = None):
+    """Context-parallel form: local query rows (global padded coordinates `query_indices`,
+    identity when absent) against gathered global keys.  Returns (seq_start[T_q],
+    causal_len[T_q], max_seqlen, all_rows_nonempty); raises ValueError on invalid input."""
+    cu = _i32(cu_seqlens)
+    cp = None if cu_seqlens_padded is None else _i32(cu_seqlens_padded)
+    qi = None if query_indices is None else _i32(query_indices)
+    pm = None if padding_mask is None else np.ascontiguousarray(
+        padding_mask.detach().to("cpu").numpy() if hasattr(padding_mask, "detach") else padding_mask, dtype=np.uint8)
+    if T_q is None:
+        T_q = len(qi) if qi is not None else int(total_key_tokens)
+    n = int(T_q)
+    start = np.zeros(max(n, 1), np.int32)
+    clen = np.zeros(max(n, 1), np.int32)
+    mx = np.zeros(1, np.int32)
+    ne = np.zeros(1, np.int32)
+    rc = _load().oracle_packed_metadata_cp(_p(cu), _p(cp), len(cu) - 1, int(total_key_tokens), _p(qi), _p(pm), n,
+                                           _p(start), _p(clen), _p(mx), _p(ne))
+    if rc != 0:
+        raise ValueError("invalid sequence boundaries or query coordinates")
+    return start[:n], clen[:n], int(mx[0]), int(ne[0])
+
+
 def indexer_scores(q_idx_rows, k_idx, w_rows, pair_row, pair_key, with_magnitude: bool = False):
     """fp64 indexer scores for explicit pairs (pair_row indexes q_idx_rows/w_rows)."""
     q = _f64(q_idx_rows)
@@ -129,6 +157,22 @@ def indexer_topk(q_idx_rows, k_idx, w_rows, seq_start, row_t, K: int):
     ln = np.zeros(n, np.int32)
     kth = np.zeros(n, np.float64)
     _load().oracle_indexer_topk(_p(q), _p(k), _p(w), _p(st), _p(rt), n, Hi, Di, int(K), _p(idx), _p(ln), _p(kth))
+    return idx, ln, kth
+
+
+def indexer_topk_window(q_idx_rows, k_idx, w_rows, win_start, win_len, K: int):
+    """Top-k of each given row over its explicit key window [win_start, win_start + win_len - 1]
+    (none when win_len = 0).  Returns (idx [n, K], len [n], kth score [n]) as indexer_topk."""
+    q = _f64(q_idx_rows)
+    k = _f64(k_idx)
+    w = _f64(w_rows)
+    n, Hi, Di = q.shape
+    ws, wl = _i32(win_start), _i32(win_len)
+    idx = np.zeros((n, K), np.int32)
+    ln = np.zeros(n, np.int32)
+    kth = np.zeros(n, np.float64)
+    _load().oracle_indexer_topk_window(_p(q), _p(k), _p(w), _p(ws), _p(wl), n, Hi, Di, int(K), _p(idx), _p(ln),
+                                       _p(kth))
     return idx, ln, kth
 
 

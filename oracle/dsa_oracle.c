@@ -54,6 +54,59 @@ int oracle_packed_metadata(const int32_t *cu_seqlens, int num_seqs, int T,
 }
 
 /* ------------------------------------------------------------------------ */
+/* THD packing metadata with context parallelism                              */
+/* [cudnn_dsa] prepare_cudnn_dsa_packed_metadata: metadata for rank-local     */
+/* queries and gathered global keys.  query_indices holds the global padded-  */
+/* storage coordinate of each local query row (absent: the identity, i.e. the */
+/* queries cover every global key token); cu_seqlens_padded holds the padded  */
+/* storage boundaries (absent: cu_seqlens is also the storage); padding_mask  */
+/* marks local padding rows and stays authoritative; the result holds, per    */
+/* query, the global padded-storage start and the real causal length.         */
+/* Readings: with P the storage boundaries and L_i = cu[i+1] - cu[i], a row   */
+/* with coordinate g lies in sequence i when P[i] <= g < P[i+1]; its position */
+/* is p = g - P[i]; start = P[i] and causal length = p + 1 when p < L_i and   */
+/* the row is not masked, else 0 (a padding row).  A row outside every        */
+/* sequence's storage gets start = g and length 0.  A nonzero mask byte marks */
+/* padding.  max_seqlen = max_i L_i; all_rows_nonempty = every length > 0.    */
+/* Returns 0, or -1 when cu_seqlens / cu_seqlens_padded are not non-decreasing*/
+/* from 0, a sequence's real length exceeds its storage, the storage exceeds  */
+/* total_key_tokens, or a coordinate lies outside [0, total_key_tokens).      */
+/* ------------------------------------------------------------------------ */
+int oracle_packed_metadata_cp(const int32_t *cu_seqlens, const int32_t *cu_padded, int num_seqs,
+                              int total_key_tokens, const int32_t *query_idx, const uint8_t *pad_mask,
+                              int Tq, int32_t *seq_start, int32_t *causal_len, int32_t *max_seqlen,
+                              int32_t *all_rows_nonempty) {
+  const int32_t *P = cu_padded ? cu_padded : cu_seqlens;
+  if (num_seqs < 1 || cu_seqlens[0] != 0 || P[0] != 0 || P[num_seqs] > total_key_tokens) return -1;
+  int mx = 0;
+  for (int i = 0; i < num_seqs; ++i) {
+    int L = cu_seqlens[i + 1] - cu_seqlens[i];
+    if (L < 0 || P[i + 1] < P[i] || L > P[i + 1] - P[i]) return -1;
+    if (L > mx) mx = L;
+  }
+  int nonempty = 1;
+  for (int r = 0; r < Tq; ++r) {
+    int g = query_idx ? query_idx[r] : r;
+    if (g < 0 || g >= total_key_tokens) return -1;
+    int start = g, len = 0;
+    for (int i = 0; i < num_seqs; ++i) {
+      if (P[i] <= g && g < P[i + 1]) {
+        int pos = g - P[i];
+        start = P[i];
+        if (pos < cu_seqlens[i + 1] - cu_seqlens[i] && !(pad_mask && pad_mask[r])) len = pos + 1;
+        break;
+      }
+    }
+    seq_start[r] = start;
+    causal_len[r] = len;
+    if (len == 0) nonempty = 0;
+  }
+  *max_seqlen = mx;
+  *all_rows_nonempty = (Tq > 0) ? nonempty : 0;
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Lightning-indexer score                                                   */
 /* [cudnn_dsa] cudnn_indexer_topk: index_q [T, H_index, 128], one shared      */
 /* index_k [T_k, 128], already-scaled head weights [T, H_index] ("the caller  */
@@ -117,6 +170,25 @@ static int int_cmp(const void *a, const void *b) {
   return (x > y) - (x < y);
 }
 
+/* Top-k of one query row over the window [b, b + c - 1] of keys. */
+static void topk_window(const double *q_row, const double *k, const double *w_row, int64_t b, int64_t c,
+                        int Hi, int Di, int K, int32_t *row, int32_t *len_out, double *kth_out) {
+  cand_t *cand = (cand_t *)malloc(sizeof(cand_t) * (size_t)(c > 0 ? c : 1));
+  for (int64_t s = b; s < b + c; ++s) {
+    cand[s - b].score = indexer_score(q_row, k + (size_t)s * Di, w_row, Hi, Di, NULL);
+    cand[s - b].idx = (int32_t)s;
+  }
+  qsort(cand, (size_t)(c > 0 ? c : 0), sizeof(cand_t), cand_cmp); /* full sort: plain definition */
+  int n = (int)(c < K ? c : K);
+  if (n < 0) n = 0;
+  for (int j = 0; j < n; ++j) row[j] = cand[j].idx;
+  qsort(row, (size_t)n, sizeof(int32_t), int_cmp);
+  for (int j = n; j < K; ++j) row[j] = -1;
+  *len_out = n;
+  if (kth_out) *kth_out = n > 0 ? cand[n - 1].score : -INFINITY;
+  free(cand);
+}
+
 /* q_rows/w_rows hold only the nrows requested rows; row_t[r] is the global
  * token of row r (its causal window is [seq_start[row_t[r]], row_t[r]]).
  * kth_out[r] (nullable) receives the score of the n-th winner (-inf if n = 0). */
@@ -128,23 +200,21 @@ void oracle_indexer_topk(const double *q_rows, const double *k, const double *w_
   for (int r = 0; r < nrows; ++r) {
     int64_t t = row_t[r];
     int64_t b = seq_start[t];
-    int64_t c = t - b + 1;
-    cand_t *cand = (cand_t *)malloc(sizeof(cand_t) * (size_t)(c > 0 ? c : 1));
-    for (int64_t s = b; s <= t; ++s) {
-      cand[s - b].score = indexer_score(q_rows + (size_t)r * Hi * Di, k + (size_t)s * Di,
-                                        w_rows + (size_t)r * Hi, Hi, Di, NULL);
-      cand[s - b].idx = (int32_t)s;
-    }
-    qsort(cand, (size_t)c, sizeof(cand_t), cand_cmp); /* full sort: plain definition */
-    int n = (int)(c < K ? c : K);
-    int32_t *row = idx_out + (size_t)r * K;
-    for (int j = 0; j < n; ++j) row[j] = cand[j].idx;
-    qsort(row, (size_t)n, sizeof(int32_t), int_cmp);
-    for (int j = n; j < K; ++j) row[j] = -1;
-    len_out[r] = n;
-    if (kth_out) kth_out[r] = n > 0 ? cand[n - 1].score : -INFINITY;
-    free(cand);
+    topk_window(q_rows + (size_t)r * Hi * Di, k, w_rows + (size_t)r * Hi, b, t - b + 1, Hi, Di, K,
+                idx_out + (size_t)r * K, len_out + r, kth_out ? kth_out + r : NULL);
   }
+}
+
+/* The same over explicit windows, the form the context-parallel metadata
+ * gives: row r's candidates are the keys [win_start[r], win_start[r] +
+ * win_len[r] - 1], none when win_len[r] = 0. */
+void oracle_indexer_topk_window(const double *q_rows, const double *k, const double *w_rows,
+                                const int32_t *win_start, const int32_t *win_len, int nrows, int Hi, int Di,
+                                int K, int32_t *idx_out, int32_t *len_out, double *kth_out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < nrows; ++r)
+    topk_window(q_rows + (size_t)r * Hi * Di, k, w_rows + (size_t)r * Hi, win_start[r], win_len[r], Hi, Di, K,
+                idx_out + (size_t)r * K, len_out + r, kth_out ? kth_out + r : NULL);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -84,6 +84,82 @@ def test_packed_metadata_rejects_bad_cover():
 
 
 # --------------------------------------------------------------------------
+# packed THD metadata with context parallelism (local queries, global keys)
+# --------------------------------------------------------------------------
+def cp_split(total, ranks, rank):
+    """Load-balanced contiguous chunks: 2 * ranks chunks, rank r holds chunks r and 2R-1-r."""
+    edges = np.linspace(0, total, 2 * ranks + 1).astype(np.int64)
+    a, b = rank, 2 * ranks - 1 - rank
+    return np.concatenate([np.arange(edges[a], edges[a + 1]), np.arange(edges[b], edges[b + 1])]).astype(np.int32)
+
+
+def test_packed_metadata_cp_golden_two_ranks():
+    with open(os.path.join(GOLDEN, "cp_metadata_two_ranks.json")) as f:
+        g = json.load(f)
+    for rk in g["ranks"]:
+        st, cl, mx, ne = oracle.packed_metadata_cp(
+            np.array(g["cu_seqlens"]), g["total_key_tokens"], query_indices=np.array(rk["query_indices"]),
+            cu_seqlens_padded=np.array(g["cu_seqlens_padded"]), padding_mask=np.array(rk["padding_mask"]))
+        assert st.tolist() == rk["seq_start"] and cl.tolist() == rk["causal_len"]
+        assert mx == g["max_seqlen"] and ne == g["all_rows_nonempty"]
+
+
+def test_packed_metadata_cp_identity_is_the_cp1_form():
+    rng = np.random.default_rng(21)
+    for _ in range(20):
+        lens = rng.integers(0, 9, rng.integers(1, 6))
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        T = int(cu[-1])
+        a = oracle.packed_metadata_cp(cu, T)
+        b = oracle.packed_metadata(cu, T)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and a[2:] == b[2:]
+
+
+@pytest.mark.parametrize("ranks", [1, 2, 3])
+def test_packed_metadata_cp_shards_keep_every_real_token(ranks):
+    # Padded storage with a random pad after every sequence, split over CP ranks: every real
+    # token shows up on exactly one rank, with the start of its sequence's storage and the
+    # causal length the CP=1 metadata gives it in the compact layout; padding rows get length 0.
+    rng = np.random.default_rng(22 + ranks)
+    lens = rng.integers(0, 12, 5)
+    pads = rng.integers(0, 4, 5)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    P = np.concatenate([[0], np.cumsum(lens + pads)]).astype(np.int32)
+    total = int(P[-1]) + 2  # two rows of trailing pack padding
+    _, ref_len, ref_mx, _ = oracle.packed_metadata(cu, int(cu[-1]))
+    seen = {}
+    for r in range(ranks):
+        qi = cp_split(total, ranks, r)
+        st, cl, mx, _ = oracle.packed_metadata_cp(cu, total, query_indices=qi, cu_seqlens_padded=P)
+        assert mx == ref_mx
+        for g, s, c in zip(qi.tolist(), st.tolist(), cl.tolist()):
+            assert g not in seen
+            seen[g] = (s, c)
+    assert sorted(seen) == list(range(total))
+    for i in range(len(lens)):
+        for p in range(int(P[i + 1] - P[i])):
+            s, c = seen[int(P[i]) + p]
+            assert s == P[i]
+            assert c == (ref_len[cu[i] + p] if p < lens[i] else 0)
+    for g in range(int(P[-1]), total):
+        assert seen[g][1] == 0
+
+
+def test_packed_metadata_cp_mask_is_authoritative_and_bad_input_rejected():
+    cu, P = np.array([0, 4], np.int32), np.array([0, 4], np.int32)
+    qi = np.array([0, 1, 2, 3], np.int32)
+    _, cl, _, ne = oracle.packed_metadata_cp(cu, 4, query_indices=qi, cu_seqlens_padded=P,
+                                             padding_mask=np.array([0, 0, 1, 1]))
+    assert cl.tolist() == [1, 2, 0, 0] and ne == 0
+    with pytest.raises(ValueError):  # a real length larger than its storage
+        oracle.packed_metadata_cp(np.array([0, 5]), 8, cu_seqlens_padded=np.array([0, 4]), T_q=4)
+    with pytest.raises(ValueError):  # a coordinate outside the key tokens
+        oracle.packed_metadata_cp(cu, 4, query_indices=np.array([0, 4]))
+    with pytest.raises(ValueError):  # storage beyond the key tokens
+        oracle.packed_metadata_cp(cu, 3, query_indices=np.array([0]))
+
+
+# --------------------------------------------------------------------------
 # indexer score
 # --------------------------------------------------------------------------
 def test_indexer_scores_match_numpy_einsum():
@@ -174,6 +250,38 @@ def test_topk_subset_of_rows_matches_all_rows():
     rows = np.array([32, 0, 17])
     part, _, _ = oracle.indexer_topk(q[rows], k, w[rows], st, rows, K)
     assert np.array_equal(part, full[rows])
+
+
+def test_topk_window_is_the_causal_form_on_causal_windows():
+    rng = np.random.default_rng(7)
+    cu = np.array([0, 11, 30], np.int32)
+    T, K = 30, 5
+    q = rng.standard_normal((T, 2, 4))
+    k = rng.standard_normal((T, 4))
+    w = rng.uniform(0, 1, (T, 2))
+    st, cl, _, _ = oracle.packed_metadata(cu, T)
+    a = oracle.indexer_topk(q, k, w, st, np.arange(T), K)
+    b = oracle.indexer_topk_window(q, k, w, st, cl, K)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
+
+
+def test_topk_window_brute_force_arbitrary_and_empty_windows():
+    rng = np.random.default_rng(8)
+    n, Tk, K = 12, 25, 6
+    q = rng.standard_normal((n, 3, 5))
+    k = rng.standard_normal((Tk, 5))
+    w = rng.uniform(-0.2, 1, (n, 3))
+    ws = rng.integers(0, Tk, n).astype(np.int32)
+    wl = np.minimum(rng.integers(0, 12, n), Tk - ws).astype(np.int32)
+    wl[3] = 0
+    idx, ln, _ = oracle.indexer_topk_window(q, k, w, ws, wl, K)
+    S = numpy_indexer_scores(q, k, w)
+    for r in range(n):
+        if wl[r] == 0:
+            assert ln[r] == 0 and np.all(idx[r] == -1)
+            continue
+        ref, m = brute_topk(S[r], ws[r], ws[r] + wl[r] - 1, K)
+        assert idx[r].tolist() == ref and ln[r] == m
 
 
 # --------------------------------------------------------------------------
