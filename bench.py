@@ -318,6 +318,7 @@ def run_cuda(args, rank, world, local):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, f_fwd + f_bwd, world)
+    cp = None if args.no_cp else run_cp_indexer(args, dsa, torch, dev, stream, ind, topk_idx, topk_len)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -337,6 +338,7 @@ def run_cuda(args, rank, world, local):
         "clocks": clocks,
         "gpu_launches": 4 * args.steps,
         "e2e": e2e,
+        "cp_indexer": cp,
     }
     if rank == 0 and not args.no_cpu_baseline:
         r = oracle_sample(16)
@@ -347,6 +349,35 @@ def run_cuda(args, rank, world, local):
                                           f"TFLOP/s; indexer {r['idx_tokens_per_s']:.2f} tokens/s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_cp_indexer(args, dsa, torch, dev, stream, ind, topk_idx, topk_len, ranks=2):
+    """The indexer in its context-parallel form: rank 0 of `ranks`, holding the load-balanced
+    chunks 0 and 2R-1 of the sequence's query rows, against all keys.  Its rows must equal the
+    same rows of the one-shot indexer; timed with CUDA events over K steps."""
+    S_ = ind["q_idx"].shape[0]
+    edges = [S_ * i // (2 * ranks) for i in range(2 * ranks + 1)]
+    qi = torch.cat([torch.arange(edges[0], edges[1]), torch.arange(edges[-2], edges[-1])]).to(dev)
+    q_loc, w_loc = ind["q_idx"][qi].contiguous(), ind["w"][qi].contiguous()
+    cu = torch.tensor([0, S_], dtype=torch.int32, device=dev)
+    st, cl, _, _ = dsa.dsa_packed_metadata_cp(cu, S_, query_indices=qi.to(torch.int32))
+    ws = torch.zeros(dsa.workspace_size("indexer", q_loc.shape[0], K), dtype=torch.uint8, device=dev)
+    run = lambda: dsa.dsa_indexer_topk_cp(q_loc, ind["k_idx"], w_loc, st, cl, K, workspace=ws)
+    for _ in range(args.warmup):
+        idx, ln = run()
+    torch.cuda.synchronize(dev)
+    same = bool(torch.equal(idx, topk_idx[qi]) and torch.equal(ln, topk_len[qi]))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev:
+        a.record(stream)
+        run()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    if dsa.dsa_read_device_status(ws) != 0:
+        raise RuntimeError("device status after the context-parallel indexer")
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    return {"ranks": ranks, "rank": 0, "local_rows": int(q_loc.shape[0]), "ms": round(ms, 3),
+            "tokens_per_s": round(q_loc.shape[0] / (ms * 1e-3), 1), "matches_one_shot_rows": same}
 
 
 def run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, flops_per_step, world):
@@ -460,6 +491,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cp", action="store_true", help="skip the context-parallel indexer line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seq", type=int, default=32768,
                     help="sequence length; only for small-case profiler captures (the benchmark is 32768)")

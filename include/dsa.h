@@ -74,6 +74,39 @@ dsa_status_t dsa_packed_metadata(const int32_t* cu_seqlens, int32_t num_seqs, in
                                  int32_t* all_rows_nonempty_host, dsa_stream_t stream);
 
 /*
+ * dsa_packed_metadata_cp -- THD packing metadata for rank-local queries and
+ * gathered global keys (context parallelism).
+ * Source: [cudnn_dsa] prepare_cudnn_dsa_packed_metadata (query_indices,
+ * cu_seqlens_padded, padding_mask; per-query global padded-storage starts and
+ * real causal lengths) and cudnn_indexer_topk (rank-local index_q, gathered
+ * global index_k).  With P = cu_seqlens_padded (or cu_seqlens when NULL) and
+ * L_i = cu_seqlens[i+1] - cu_seqlens[i], local row r has global coordinate
+ * g = query_indices[r] (r when NULL); when P[i] <= g < P[i+1]:
+ *   seq_start[r] = P[i],  causal_len[r] = g - P[i] + 1 if g - P[i] < L_i and
+ *   padding_mask[r] == 0, else 0 (a padding row);
+ * a row outside every sequence's storage gets seq_start[r] = g, causal_len 0.
+ *  cu_seqlens         device int32 [num_seqs + 1], from 0, non-decreasing (real tokens)
+ *  cu_seqlens_padded  device int32 [num_seqs + 1] or NULL, from 0, non-decreasing,
+ *                     P[i+1] - P[i] >= L_i, P[num_seqs] <= total_key_tokens
+ *  query_indices      device int32 [T_q] or NULL (then row r is coordinate r and
+ *                     T_q <= total_key_tokens), each in [0, total_key_tokens)
+ *  padding_mask       device uint8 [T_q] or NULL; nonzero marks a padding row
+ *  seq_start, causal_len  device int32 [T_q] (out)
+ *  max_seqlen_host    host int32 (out) = max_i L_i, may be NULL
+ *  all_rows_nonempty_host  host int32 (out) = 1 iff T_q > 0 and every
+ *                     causal_len > 0, may be NULL
+ * Performs one device-to-host synchronisation (to validate the inputs and
+ * compute the host scalars) and returns DSA_ERR_INVALID_ARGUMENT when any rule
+ * above is broken; the outputs are then untouched.  With no optional input it
+ * equals dsa_packed_metadata.
+ */
+dsa_status_t dsa_packed_metadata_cp(const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded, int32_t num_seqs,
+                                    int32_t total_key_tokens, const int32_t* query_indices,
+                                    const uint8_t* padding_mask, int32_t T_q, int32_t* seq_start,
+                                    int32_t* causal_len, int32_t* max_seqlen_host, int32_t* all_rows_nonempty_host,
+                                    dsa_stream_t stream);
+
+/*
  * dsa_indexer_topk -- lightning-indexer score fused with per-query causal top-k.
  * Source: [DSA-blog] "How DSA works" (the indexer scores query-key relevance
  * and emits the top-k indices per query); [cudnn_dsa] cudnn_indexer_topk
@@ -97,6 +130,27 @@ dsa_status_t dsa_indexer_topk(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, 
                               const int32_t* seq_start, int32_t T, int32_t T_k, int32_t Hi, int32_t Di, int32_t K,
                               int32_t* topk_idx, int32_t* topk_len, void* workspace, size_t workspace_bytes,
                               dsa_stream_t stream);
+
+/*
+ * dsa_indexer_topk_cp -- the same kernel for rank-local query rows against the
+ * gathered global keys (context parallelism).
+ * Source: [cudnn_dsa] cudnn_indexer_topk (rank-local index_q [T_q, H_index,
+ * 128], gathered global index_k [T_k, 128], query_indices / packed_metadata).
+ * Row r's candidates are the keys [seq_start[r], seq_start[r] + causal_len[r]
+ * - 1] (none when causal_len[r] = 0), clipped to [0, T_k); otherwise as
+ * dsa_indexer_topk: n = min(K, window size) best keys, ascending, -1 suffix.
+ *  q_idx        device bf16 [T_q, Hi, Di] (local rows)
+ *  k_idx        device bf16 [T_k, Di] (global keys; no relation between T_k and T_q)
+ *  head_weights device fp32 [T_q, Hi]
+ *  seq_start, causal_len  device int32 [T_q] from dsa_packed_metadata_cp
+ *  topk_idx, topk_len, workspace  as dsa_indexer_topk
+ * Errors as dsa_indexer_topk (without the T_k >= T rule), plus
+ * DSA_ERR_INVALID_ARGUMENT when causal_len is NULL and T_q > 0.
+ */
+dsa_status_t dsa_indexer_topk_cp(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
+                                 const int32_t* seq_start, const int32_t* causal_len, int32_t T_q, int32_t T_k,
+                                 int32_t Hi, int32_t Di, int32_t K, int32_t* topk_idx, int32_t* topk_len,
+                                 void* workspace, size_t workspace_bytes, dsa_stream_t stream);
 
 /*
  * dsa_indexer_topk_with_scores -- diagnostic form of dsa_indexer_topk: the same

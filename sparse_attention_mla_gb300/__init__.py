@@ -24,7 +24,9 @@ __all__ = [
     "load_library",
     "declared_symbols",
     "dsa_packed_metadata",
+    "dsa_packed_metadata_cp",
     "dsa_indexer_topk",
+    "dsa_indexer_topk_cp",
     "dsa_indexer_topk_with_scores",
     "dsa_sparse_mla_fwd",
     "dsa_sparse_mla_bwd",
@@ -87,9 +89,11 @@ def load_library(path: str | None = None):
         lib.dsa_last_error_message.argtypes = []
         lib.dsa_abi_version.restype = _I
         lib.dsa_packed_metadata.argtypes = [_P, _I, _I, _P, _P, _P, _P, _P]
+        lib.dsa_packed_metadata_cp.argtypes = [_P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]
         lib.dsa_indexer_topk_workspace_size.argtypes = [_I, _I]
         lib.dsa_indexer_topk_workspace_size.restype = _SZ
         lib.dsa_indexer_topk.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]
+        lib.dsa_indexer_topk_cp.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]
         lib.dsa_indexer_topk_with_scores.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _I, _I, _P,
                                                      _SZ, _P]
         lib.dsa_sparse_mla_fwd_workspace_size.argtypes = [_I, _I]
@@ -174,6 +178,67 @@ def dsa_packed_metadata(cu_seqlens: torch.Tensor, total_tokens: int):
     _check(lib.dsa_packed_metadata(_ptr(cu_seqlens), cu_seqlens.numel() - 1, T, _ptr(start), _ptr(clen),
                                    ctypes.byref(mx), ctypes.byref(ne), _stream(dev)), "dsa_packed_metadata")
     return start, clen, mx.value, ne.value
+
+
+def dsa_packed_metadata_cp(cu_seqlens: torch.Tensor, total_key_tokens: int, query_indices=None,
+                           cu_seqlens_padded=None, padding_mask=None, T_q: int | None = None):
+    """Context-parallel metadata: rank-local query rows (global padded coordinates `query_indices`,
+    identity when None) against gathered global keys -> (seq_start [T_q], causal_len [T_q],
+    max_seqlen, all_rows_nonempty).  padding_mask: bool/uint8 [T_q], True marks a padding row."""
+    lib = load_library()
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    dev = cu_seqlens.device
+    if cu_seqlens_padded is not None:
+        _need(cu_seqlens_padded, "cu_seqlens_padded", torch.int32, 1, dev)
+        if cu_seqlens_padded.numel() != cu_seqlens.numel():
+            raise ValueError("cu_seqlens_padded must have as many entries as cu_seqlens")
+    if query_indices is not None:
+        _need(query_indices, "query_indices", torch.int32, 1, dev)
+    if T_q is None:
+        T_q = query_indices.numel() if query_indices is not None else int(total_key_tokens)
+    T_q = int(T_q)
+    if query_indices is not None and query_indices.numel() != T_q:
+        raise ValueError("query_indices must have T_q entries")
+    if padding_mask is not None:
+        if padding_mask.dtype == torch.bool:
+            padding_mask = padding_mask.view(torch.uint8)
+        _need(padding_mask, "padding_mask", torch.uint8, 1, dev)
+        if padding_mask.numel() != T_q:
+            raise ValueError("padding_mask must have T_q entries")
+    start = torch.empty(T_q, dtype=torch.int32, device=dev)
+    clen = torch.empty(T_q, dtype=torch.int32, device=dev)
+    mx = ctypes.c_int32(0)
+    ne = ctypes.c_int32(0)
+    _check(lib.dsa_packed_metadata_cp(_ptr(cu_seqlens), _ptr(cu_seqlens_padded), cu_seqlens.numel() - 1,
+                                      int(total_key_tokens), _ptr(query_indices), _ptr(padding_mask), T_q, _ptr(start),
+                                      _ptr(clen), ctypes.byref(mx), ctypes.byref(ne), _stream(dev)),
+           "dsa_packed_metadata_cp")
+    return start, clen, mx.value, ne.value
+
+
+def dsa_indexer_topk_cp(q_idx, k_idx, head_weights, seq_start, causal_len, K: int, topk_idx=None, topk_len=None,
+                        workspace=None):
+    """Indexer top-k for rank-local rows against gathered global keys: row r's window is
+    [seq_start[r], seq_start[r] + causal_len[r] - 1] -> (topk_idx int32 [T_q, K], topk_len int32 [T_q])."""
+    lib = load_library()
+    _need(q_idx, "q_idx", torch.bfloat16, 3)
+    dev = q_idx.device
+    _need(k_idx, "k_idx", torch.bfloat16, 2, dev)
+    _need(head_weights, "head_weights", torch.float32, 2, dev)
+    _need(seq_start, "seq_start", torch.int32, 1, dev)
+    _need(causal_len, "causal_len", torch.int32, 1, dev)
+    T, Hi, Di = q_idx.shape
+    Tk = k_idx.shape[0]
+    if topk_idx is None:
+        topk_idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+    if topk_len is None:
+        topk_len = torch.empty(T, dtype=torch.int32, device=dev)
+    ws, wsb = _workspace("indexer", T, K, dev, workspace)
+    _check(lib.dsa_indexer_topk_cp(_ptr(q_idx), _ptr(k_idx), _ptr(head_weights), _ptr(seq_start), _ptr(causal_len),
+                                   T, Tk, Hi, Di, int(K), _ptr(topk_idx), _ptr(topk_len), _ptr(ws), wsb,
+                                   _stream(dev)),
+           "dsa_indexer_topk_cp")
+    return topk_idx, topk_len
 
 
 def dsa_indexer_topk(q_idx, k_idx, head_weights, seq_start, K: int, topk_idx=None, topk_len=None,

@@ -1,5 +1,6 @@
 // dsa_api.cu -- status reporting, device checks, tensor maps, workspace sizes,
 // the device error word, and dsa_packed_metadata.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -118,6 +119,30 @@ __global__ void packed_metadata_kernel(const int32_t* __restrict__ cu, int nseq,
   }
 }
 
+// Context-parallel form: row r has global padded-storage coordinate g (query_idx[r], or r);
+// with P the storage boundaries, the last i with P[i] <= g is its sequence when g < P[nseq].
+__global__ void packed_metadata_cp_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ P, int nseq,
+                                          const int32_t* __restrict__ qidx, const uint8_t* __restrict__ mask, int Tq,
+                                          int32_t* __restrict__ start, int32_t* __restrict__ clen) {
+  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < Tq; r += gridDim.x * blockDim.x) {
+    const int g = qidx ? __ldg(qidx + r) : r;
+    int s = g, len = 0;
+    if (g < __ldg(P + nseq)) {
+      int lo = 0, hi = nseq;  // invariant: P[lo] <= g < P[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(P + mid) <= g) lo = mid; else hi = mid;
+      }
+      s = __ldg(P + lo);
+      const int pos = g - s;
+      const bool pad = mask != nullptr && __ldg(mask + r) != 0;
+      if (pos < __ldg(cu + lo + 1) - __ldg(cu + lo) && !pad) len = pos + 1;
+    }
+    start[r] = s;
+    clen[r] = len;
+  }
+}
+
 }  // namespace dsa
 
 using namespace dsa;
@@ -192,6 +217,81 @@ dsa_status_t dsa_packed_metadata(const int32_t* cu_seqlens, int32_t num_seqs, in
   }
   if (max_seqlen_host) *max_seqlen_host = mx;
   if (all_rows_nonempty_host) *all_rows_nonempty_host = total_tokens > 0 ? 1 : 0;
+  return ok();
+}
+
+dsa_status_t dsa_packed_metadata_cp(const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded, int32_t num_seqs,
+                                    int32_t total_key_tokens, const int32_t* query_indices,
+                                    const uint8_t* padding_mask, int32_t T_q, int32_t* seq_start,
+                                    int32_t* causal_len, int32_t* max_seqlen_host, int32_t* all_rows_nonempty_host,
+                                    dsa_stream_t stream) {
+  const char* who = "dsa_packed_metadata_cp";
+  if (!cu_seqlens) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: cu_seqlens is NULL", who);
+  if (num_seqs < 1) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: num_seqs must be >= 1", who);
+  if (T_q < 0 || total_key_tokens < 0) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: T_q and total_key_tokens must be >= 0", who);
+  if (!query_indices && T_q > total_key_tokens)
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: without query_indices, T_q (%d) must be <= total_key_tokens (%d)", who,
+                T_q, total_key_tokens);
+  if (T_q > 0 && (!seq_start || !causal_len)) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: output pointer is NULL", who);
+  dsa_status_t st = check_device();
+  if (st != DSA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // one device-to-host synchronisation: boundaries, coordinates and mask for validation
+  std::vector<int32_t> cu(num_seqs + 1), P(num_seqs + 1), qi(query_indices ? T_q : 0);
+  std::vector<uint8_t> pm(padding_mask ? T_q : 0);
+  const size_t nb = sizeof(int32_t) * (num_seqs + 1);
+  if ((st = cuda_check(cudaMemcpyAsync(cu.data(), cu_seqlens, nb, cudaMemcpyDeviceToHost, s), "copying cu_seqlens")))
+    return st;
+  if (cu_seqlens_padded &&
+      (st = cuda_check(cudaMemcpyAsync(P.data(), cu_seqlens_padded, nb, cudaMemcpyDeviceToHost, s),
+                       "copying cu_seqlens_padded")))
+    return st;
+  if (!qi.empty() && (st = cuda_check(cudaMemcpyAsync(qi.data(), query_indices, sizeof(int32_t) * qi.size(),
+                                                      cudaMemcpyDeviceToHost, s),
+                                      "copying query_indices")))
+    return st;
+  if (!pm.empty() &&
+      (st = cuda_check(cudaMemcpyAsync(pm.data(), padding_mask, pm.size(), cudaMemcpyDeviceToHost, s),
+                       "copying padding_mask")))
+    return st;
+  if ((st = cuda_check(cudaStreamSynchronize(s), "synchronising the stream"))) return st;
+  if (!cu_seqlens_padded) P = cu;
+  if (cu[0] != 0 || P[0] != 0)
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: cu_seqlens[0] and cu_seqlens_padded[0] must be 0", who);
+  if (P[num_seqs] > total_key_tokens)
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: the padded storage (%d rows) exceeds total_key_tokens (%d)", who,
+                P[num_seqs], total_key_tokens);
+  int32_t mx = 0;
+  for (int i = 0; i < num_seqs; ++i) {
+    const int32_t L = cu[i + 1] - cu[i];
+    if (L < 0 || P[i + 1] < P[i])
+      return fail(DSA_ERR_INVALID_ARGUMENT, "%s: sequence boundaries decrease at %d", who, i);
+    if (L > P[i + 1] - P[i])
+      return fail(DSA_ERR_INVALID_ARGUMENT, "%s: sequence %d has %d real tokens but %d storage rows", who, i, L,
+                  P[i + 1] - P[i]);
+    if (L > mx) mx = L;
+  }
+  // every coordinate inside the key tokens; a row is nonempty when it is a real, unmasked token
+  int nonempty = T_q > 0 ? 1 : 0;
+  for (int32_t r = 0; r < T_q; ++r) {
+    const int32_t g = qi.empty() ? r : qi[r];
+    if (g < 0 || g >= total_key_tokens)
+      return fail(DSA_ERR_INVALID_ARGUMENT, "%s: query_indices[%d] = %d outside [0, %d)", who, r, g, total_key_tokens);
+    if (!nonempty) continue;
+    const int i = (int)(std::upper_bound(P.begin(), P.begin() + num_seqs, g) - P.begin()) - 1;
+    if (g >= P[num_seqs] || g - P[i] >= cu[i + 1] - cu[i] || (!pm.empty() && pm[r])) nonempty = 0;
+  }
+  if (T_q > 0) {
+    const int threads = 256;
+    int blocks = (T_q + threads - 1) / threads;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    packed_metadata_cp_kernel<<<blocks, threads, 0, s>>>(cu_seqlens, cu_seqlens_padded ? cu_seqlens_padded : cu_seqlens,
+                                                         num_seqs, query_indices, padding_mask, T_q, seq_start,
+                                                         causal_len);
+    if ((st = cuda_check(cudaGetLastError(), "launching packed_metadata_cp_kernel"))) return st;
+  }
+  if (max_seqlen_host) *max_seqlen_host = mx;
+  if (all_rows_nonempty_host) *all_rows_nonempty_host = nonempty;
   return ok();
 }
 

@@ -3,7 +3,10 @@
 //
 //   score(t, s) = sum_h w[t,h] * max(0, <q_idx[t,h,:], k_idx[s,:]>),  s in [seq_start[t], t]
 // and for each t the n = min(K, causal length) best keys (score descending,
-// ties to the lower index), written ascending with a -1 suffix.
+// ties to the lower index), written ascending with a -1 suffix.  With context
+// parallelism the rows are rank-local queries against the gathered global
+// keys, and each row's window [seq_start, seq_start + causal_len - 1] comes
+// from the context-parallel metadata (empty for padding rows).
 // Source: "Accelerating GLM-5.2 Long-Context Training with cuDNN Fused DSA
 // Kernels ...", "How DSA works" (the indexer scores query-key relevance and
 // emits the top-k per query) and "Why DSA needs fused kernels" (the S x S
@@ -234,7 +237,8 @@ __device__ uint32_t compact(const Half& hf, float* cs, int* ci, int cnt, int tar
 template <bool kScores>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_topk_kernel(const __grid_constant__ CUtensorMap k_map, const __nv_bfloat16* __restrict__ q_idx,
-                        const float* __restrict__ w, const int32_t* __restrict__ seq_start, int T, int Tk, int Hi,
+                        const float* __restrict__ w, const int32_t* __restrict__ seq_start,
+                        const int32_t* __restrict__ causal_len, int T, int Tk, int Hi,
                         int K, int32_t* __restrict__ topk_idx, int32_t* __restrict__ topk_len,
                         int* __restrict__ err, float* __restrict__ scores, int score_row0, int score_rows) {
   extern __shared__ uint8_t smem_raw[];
@@ -270,13 +274,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(s_tmem), 512);
     tmem_relinquish();
   }
-  // key-tile range covering every token's causal window
+  // Key window of token t: [seq_start[t], seq_start[t] + causal_len[t] - 1] when the
+  // lengths are given (context-parallel rows, possibly empty), else [seq_start[t], t];
+  // clipped to the keys [0, Tk).  Empty: (1, 0).
+  auto window = [&](int t, int& a, int& b) {
+    a = __ldg(seq_start + t);
+    b = causal_len ? a + __ldg(causal_len + t) - 1 : t;
+    a = max(a, 0);
+    b = min(b, Tk - 1);
+    if (b < a) a = 1, b = 0;
+  };
+  // key-tile range covering every token's window
   int lo = INT_MAX, hi = -1;
   for (int k = 0; k < nt; ++k) {
-    lo = min(lo, __ldg(seq_start + t0 + k));
-    hi = max(hi, t0 + k);
+    int a, b;
+    window(t0 + k, a, b);
+    if (b >= a) {
+      lo = min(lo, a);
+      hi = max(hi, b);
+    }
   }
-  hi = min(hi, Tk - 1);
   const int kt0 = lo / kTile, kt1 = hi / kTile;
   const int ntiles = (hi >= lo) ? kt1 - kt0 + 1 : 0;
 
@@ -357,8 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     hf.sel = reinterpret_cast<int*>(misc + M_SEL) + k * 4;
     float* cs = reinterpret_cast<float*>(smem + OFF_CAND + k * CAP * 8);
     int* ci = reinterpret_cast<int*>(smem + OFF_CAND + k * CAP * 8 + CAP * 4);
-    const int win_lo = (k < nt) ? __ldg(seq_start + t0 + k) : 1;
-    const int win_hi = (k < nt) ? t0 + k : 0;  // empty window for an inactive token
+    int win_lo = 1, win_hi = 0;  // empty window for an inactive token
+    if (k < nt) window(t0 + k, win_lo, win_hi);
     const float* wr = s_w + k * kHeads;
     int cnt = 0;
     uint32_t thr = 0u;
@@ -456,11 +473,12 @@ namespace dsa {
 namespace idx {
 template <bool kScores>
 static dsa_status_t run(const char* who, const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
-                        const int32_t* seq_start, int32_t T, int32_t T_k, int32_t Hi, int32_t Di, int32_t K,
+                        const int32_t* seq_start, const int32_t* causal_len, int32_t T, int32_t T_k, int32_t Hi,
+                        int32_t Di, int32_t K,
                         int32_t* topk_idx, int32_t* topk_len, float* scores, int32_t score_row0, int32_t score_rows,
                         void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
   if (T < 0 || T_k < 1) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: need T >= 0 and T_k >= 1", who);
-  if (T_k < T) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: T_k (%d) must be >= T (%d)", who, T_k, T);
+  if (!causal_len && T_k < T) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: T_k (%d) must be >= T (%d)", who, T_k, T);
   if (Hi < 1 || Hi > kHeads) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: Hi must be in [1, 64] (got %d)", who, Hi);
   if (Di != kDi) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: Di must be 128 (got %d)", who, Di);
   if (K < 1 || K > kMaxK) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: K must be in [1, 2048] (got %d)", who, K);
@@ -489,8 +507,8 @@ static dsa_status_t run(const char* who, const dsa_bf16_t* q_idx, const dsa_bf16
   }
   const int nblk = (T + kTokens - 1) / kTokens;
   indexer_topk_kernel<kScores><<<nblk, kThreads, TOTAL, s>>>(
-      map, reinterpret_cast<const __nv_bfloat16*>(q_idx), head_weights, seq_start, T, T_k, Hi, K, topk_idx, topk_len,
-      reinterpret_cast<int*>(workspace), scores, score_row0, score_rows);
+      map, reinterpret_cast<const __nv_bfloat16*>(q_idx), head_weights, seq_start, causal_len, T, T_k, Hi, K, topk_idx,
+      topk_len, reinterpret_cast<int*>(workspace), scores, score_row0, score_rows);
   if ((st = cuda_check(cudaGetLastError(), "launching indexer_topk_kernel"))) return st;
   return ok();
 }
@@ -501,8 +519,18 @@ extern "C" dsa_status_t dsa_indexer_topk(const dsa_bf16_t* q_idx, const dsa_bf16
                                          const int32_t* seq_start, int32_t T, int32_t T_k, int32_t Hi, int32_t Di,
                                          int32_t K, int32_t* topk_idx, int32_t* topk_len, void* workspace,
                                          size_t workspace_bytes, dsa_stream_t stream) {
-  return idx::run<false>("dsa_indexer_topk", q_idx, k_idx, head_weights, seq_start, T, T_k, Hi, Di, K, topk_idx,
-                         topk_len, nullptr, 0, 0, workspace, workspace_bytes, stream);
+  return idx::run<false>("dsa_indexer_topk", q_idx, k_idx, head_weights, seq_start, nullptr, T, T_k, Hi, Di, K,
+                         topk_idx, topk_len, nullptr, 0, 0, workspace, workspace_bytes, stream);
+}
+
+extern "C" dsa_status_t dsa_indexer_topk_cp(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
+                                            const int32_t* seq_start, const int32_t* causal_len, int32_t T_q,
+                                            int32_t T_k, int32_t Hi, int32_t Di, int32_t K, int32_t* topk_idx,
+                                            int32_t* topk_len, void* workspace, size_t workspace_bytes,
+                                            dsa_stream_t stream) {
+  if (T_q > 0 && !causal_len) return fail(DSA_ERR_INVALID_ARGUMENT, "dsa_indexer_topk_cp: causal_len is NULL");
+  return idx::run<false>("dsa_indexer_topk_cp", q_idx, k_idx, head_weights, seq_start, causal_len, T_q, T_k, Hi, Di,
+                         K, topk_idx, topk_len, nullptr, 0, 0, workspace, workspace_bytes, stream);
 }
 
 extern "C" dsa_status_t dsa_indexer_topk_with_scores(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx,
@@ -511,6 +539,6 @@ extern "C" dsa_status_t dsa_indexer_topk_with_scores(const dsa_bf16_t* q_idx, co
                                                      int32_t* topk_len, float* scores, int32_t score_row0,
                                                      int32_t score_rows, void* workspace, size_t workspace_bytes,
                                                      dsa_stream_t stream) {
-  return idx::run<true>("dsa_indexer_topk_with_scores", q_idx, k_idx, head_weights, seq_start, T, T_k, Hi, Di, K,
-                        topk_idx, topk_len, scores, score_row0, score_rows, workspace, workspace_bytes, stream);
+  return idx::run<true>("dsa_indexer_topk_with_scores", q_idx, k_idx, head_weights, seq_start, nullptr, T, T_k, Hi, Di,
+                        K, topk_idx, topk_len, scores, score_row0, score_rows, workspace, workspace_bytes, stream);
 }

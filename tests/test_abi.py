@@ -16,7 +16,8 @@ def lib():
 
 def test_every_declared_symbol_is_exported(lib):
     names = dsa.declared_symbols()
-    expected = {"dsa_packed_metadata", "dsa_indexer_topk", "dsa_sparse_mla_fwd", "dsa_sparse_mla_bwd",
+    expected = {"dsa_packed_metadata", "dsa_packed_metadata_cp", "dsa_indexer_topk", "dsa_indexer_topk_cp",
+                "dsa_sparse_mla_fwd", "dsa_sparse_mla_bwd",
                 "dsa_status_string", "dsa_last_error_message", "dsa_read_device_status"}
     assert expected <= set(names)
     for n in names:
@@ -61,6 +62,20 @@ def test_metadata_rejects_invalid_arguments(lib):
     assert lib.dsa_packed_metadata(FAKE, 0, 4, FAKE, FAKE, None, None, None) == 3
 
 
+def meta_cp(lib, **kw):
+    a = dict(cu=FAKE, cup=None, n=2, Tk=16, qi=FAKE, pm=None, Tq=4, st=FAKE, cl=FAKE)
+    a.update(kw)
+    return lib.dsa_packed_metadata_cp(a["cu"], a["cup"], a["n"], a["Tk"], a["qi"], a["pm"], a["Tq"], a["st"], a["cl"],
+                                      None, None, None)
+
+
+@pytest.mark.parametrize("bad", [dict(cu=None), dict(n=0), dict(Tq=-1), dict(Tk=-1), dict(st=None), dict(cl=None),
+                                 dict(qi=None, Tq=17)])
+def test_metadata_cp_rejects_invalid_arguments(lib, bad):
+    assert meta_cp(lib, **bad) == 3  # DSA_ERR_INVALID_ARGUMENT, before any device access
+    assert lib.dsa_last_error_message().decode().startswith("dsa_packed_metadata_cp")
+
+
 def bwd(lib, **kw):
     a = dict(q=FAKE, kv=FAKE, idx=FAKE, ln=None, T=4, Tk=8, H=16, Dqk=576, Dv=512, K=64, scale=0.1, out=FAKE,
              out_lo=None, lse=FAKE, dout=FAKE, dq=FAKE, dkv=FAKE, acc=0, dkv_bf16=None, ws=P(0x100000), wsb=1 << 30,
@@ -103,6 +118,21 @@ def idxr(lib, **kw):
 def test_indexer_rejects_invalid_arguments(lib, bad):
     assert idxr(lib, **bad) == 3  # DSA_ERR_INVALID_ARGUMENT
     assert lib.dsa_last_error_message().decode().startswith("dsa_indexer_topk")
+
+
+def idxr_cp(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, w=FAKE, st=FAKE, cl=FAKE, T=4, Tk=8, Hi=64, Di=128, K=64, idx=FAKE, ln=None,
+             ws=P(0x100000), wsb=1 << 20, stream=None)
+    a.update(kw)
+    return lib.dsa_indexer_topk_cp(a["q"], a["k"], a["w"], a["st"], a["cl"], a["T"], a["Tk"], a["Hi"], a["Di"],
+                                   a["K"], a["idx"], a["ln"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("bad", [dict(cl=None), dict(T=-1), dict(Hi=65), dict(Di=64), dict(K=2049), dict(k=None),
+                                 dict(st=None), dict(q=P(0x10002))])
+def test_indexer_cp_rejects_invalid_arguments(lib, bad):
+    assert idxr_cp(lib, **bad) == 3
+    assert lib.dsa_last_error_message().decode().startswith("dsa_indexer_topk_cp")
 
 
 def test_indexer_rejects_bad_workspace(lib):

@@ -1,0 +1,143 @@
+"""Context-parallel metadata and indexer (rank-local queries, gathered global keys): CUDA path
+through the C ABI vs the fp64 oracle, and vs the CP=1 path on the compact layout.
+
+The layout is padded THD storage: every sequence's real tokens followed by padding rows, plus
+trailing pack padding; ranks hold load-balanced contiguous chunks of the storage rows
+(2R chunks, rank r holds chunks r and 2R-1-r), as the cuDNN DSA API page describes
+query_indices ("global padded-storage coordinates for the local query rows").
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_mla_gb300 as dsa
+from sparse_attention_mla_gb300 import synth
+
+from test_gpu_indexer import GAMMA
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def layout(lens, pads, trailing):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    P = np.concatenate([[0], np.cumsum(np.asarray(lens) + np.asarray(pads))]).astype(np.int32)
+    return cu, P, int(P[-1]) + int(trailing)
+
+
+def cp_split(total, ranks, rank):
+    edges = np.linspace(0, total, 2 * ranks + 1).astype(np.int64)
+    a, b = rank, 2 * ranks - 1 - rank
+    return np.concatenate([np.arange(edges[a], edges[a + 1]), np.arange(edges[b], edges[b + 1])]).astype(np.int32)
+
+
+def t32(a):
+    return torch.as_tensor(np.asarray(a, dtype=np.int32)).to(DEV)
+
+
+@pytest.mark.parametrize("ranks,padded,masked", [(1, False, False), (2, True, False), (3, True, True), (4, True, True)])
+def test_metadata_cp_matches_oracle(ranks, padded, masked):
+    rng = np.random.default_rng(40 + ranks)
+    lens = rng.integers(0, 700, 7)
+    lens[2] = 0  # an empty sequence
+    pads = rng.integers(0, 50, 7) if padded else np.zeros(7, np.int64)
+    cu, P, total = layout(lens, pads, 33 if padded else 0)
+    for r in range(ranks):
+        qi = cp_split(total, ranks, r)
+        pm = (rng.random(len(qi)) < 0.05).astype(np.uint8) if masked else None
+        got = dsa.dsa_packed_metadata_cp(t32(cu), total, query_indices=t32(qi),
+                                         cu_seqlens_padded=t32(P) if padded else None,
+                                         padding_mask=None if pm is None else torch.as_tensor(pm).to(DEV))
+        ref = oracle.packed_metadata_cp(cu, total, query_indices=qi, cu_seqlens_padded=P if padded else None,
+                                        padding_mask=pm)
+        assert np.array_equal(got[0].cpu().numpy(), ref[0]) and np.array_equal(got[1].cpu().numpy(), ref[1])
+        assert got[2:] == ref[2:]
+
+
+def test_metadata_cp_identity_and_bool_mask():
+    cu = np.array([0, 5, 5, 12], np.int32)
+    st, cl, mx, ne = dsa.dsa_packed_metadata_cp(t32(cu), 12)
+    ref = oracle.packed_metadata(cu, 12)
+    assert np.array_equal(st.cpu().numpy(), ref[0]) and np.array_equal(cl.cpu().numpy(), ref[1])
+    assert (mx, ne) == ref[2:]
+    mask = torch.zeros(12, dtype=torch.bool, device=DEV)
+    mask[7] = True
+    _, cl, _, ne = dsa.dsa_packed_metadata_cp(t32(cu), 12, padding_mask=mask)
+    assert cl[7].item() == 0 and ne == 0
+
+
+def test_metadata_cp_rejects_inconsistent_layouts():
+    cu = t32([0, 6, 9])
+    with pytest.raises(dsa.DsaError):  # sequence 0 has 6 real tokens in 4 storage rows
+        dsa.dsa_packed_metadata_cp(cu, 16, query_indices=t32([0, 1]), cu_seqlens_padded=t32([0, 4, 9]))
+    with pytest.raises(dsa.DsaError):  # a coordinate outside the key tokens
+        dsa.dsa_packed_metadata_cp(cu, 9, query_indices=t32([0, 9]))
+    with pytest.raises(dsa.DsaError):  # storage beyond the key tokens
+        dsa.dsa_packed_metadata_cp(cu, 8, query_indices=t32([0]))
+
+
+def check_window_rows(gidx, glen, q_rows, k, w_rows, ws, wl, K):
+    """Rows vs the oracle's top-k over the same windows: lengths exact; index sets equal except
+    where keys sit inside the fp32 tie band of the n-th best score."""
+    ref_idx, ref_len, kth = oracle.indexer_topk_window(q_rows, k, w_rows, ws, wl, K)
+    for r in range(len(ws)):
+        n = int(ref_len[r])
+        assert glen[r] == n, (r, glen[r], n)
+        assert np.all(gidx[r, n:] == -1)
+        sel = gidx[r, :n]
+        assert np.all(np.diff(sel) > 0)
+        if n:
+            assert sel.min() >= ws[r] and sel.max() <= ws[r] + wl[r] - 1
+        diff = sorted(set(sel.tolist()) ^ set(ref_idx[r, :n].tolist()))
+        if diff:
+            sc, mag = oracle.indexer_scores(q_rows, k, w_rows, np.full(len(diff), r), np.array(diff),
+                                            with_magnitude=True)
+            ksc, kmag = oracle.indexer_scores(q_rows, k, w_rows, np.full(n, r), ref_idx[r, :n], with_magnitude=True)
+            j = int(np.argmin(ksc))
+            for d in range(len(diff)):
+                assert abs(sc[d] - kth[r]) <= GAMMA * (mag[d] + kmag[j]), f"row {r}: key {diff[d]}"
+
+
+def test_indexer_cp_ranks_equal_cp1_and_oracle():
+    # three sequences in padded storage (one long enough for candidate compactions at K = 2048),
+    # two CP ranks, a few real rows masked as padding on each rank
+    lens, pads, K = [5000, 300, 1300], [37, 0, 91], 2048
+    cu, P, total = layout(lens, pads, 40)
+    x = synth.indexer_inputs(total, 64, 128, seed=44)  # every storage row, padding included
+    q_all, k_all, w_all = x["q_idx"], x["k_idx"], x["w"]
+    # CP=1 reference on the compact layout (real rows only), mapped back to storage coordinates
+    real = np.concatenate([np.arange(P[i], P[i] + lens[i]) for i in range(len(lens))]).astype(np.int64)
+    seq_of = np.concatenate([np.full(lens[i], i) for i in range(len(lens))])
+    shift = (P[:-1] - cu[:-1])[seq_of]  # storage = compact + shift
+    st_c, _, _, _ = dsa.dsa_packed_metadata(t32(cu), int(cu[-1]))
+    ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
+    idx_c, len_c = dsa.dsa_indexer_topk(q_all[real].to(DEV), k_all[real].to(DEV), w_all[real].to(DEV), st_c, K,
+                                        workspace=ws)
+    assert dsa.dsa_read_device_status(ws) == 0
+    idx_c, len_c = idx_c.cpu().numpy(), len_c.cpu().numpy()
+    ref_storage = np.where(idx_c >= 0, idx_c + shift[np.clip(idx_c, 0, None)], -1)
+    compact_of = {int(g): c for c, g in enumerate(real)}
+    rng = np.random.default_rng(45)
+    k_dev = k_all.to(DEV)
+    for r in range(2):
+        qi = cp_split(total, 2, r)
+        pm = np.zeros(len(qi), np.uint8)
+        pm[rng.choice(len(qi), 5, replace=False)] = 1
+        st, cl, _, ne = dsa.dsa_packed_metadata_cp(t32(cu), total, query_indices=t32(qi), cu_seqlens_padded=t32(P),
+                                                   padding_mask=torch.as_tensor(pm).to(DEV))
+        assert ne == 0
+        qi64 = qi.astype(np.int64)
+        idx, ln = dsa.dsa_indexer_topk_cp(q_all[qi64].to(DEV), k_dev, w_all[qi64].to(DEV), st, cl, K, workspace=ws)
+        assert dsa.dsa_read_device_status(ws) == 0
+        idx, ln, st, cl = idx.cpu().numpy(), ln.cpu().numpy(), st.cpu().numpy(), cl.cpu().numpy()
+        for j, g in enumerate(qi.tolist()):
+            c = compact_of.get(g)
+            if c is None or pm[j]:  # a padding row: empty window, empty selection
+                assert cl[j] == 0 and ln[j] == 0 and np.all(idx[j] == -1), (r, g)
+                continue
+            assert ln[j] == len_c[c] and np.array_equal(idx[j], ref_storage[c]), (r, g)
+        # oracle on sampled rows: both chunk boundaries, the sequence ends, random rows
+        pick = np.unique(np.concatenate([[0, len(qi) // 2 - 1, len(qi) // 2, len(qi) - 1],
+                                         rng.choice(len(qi), 40, replace=False)]))
+        check_window_rows(idx[pick], ln[pick], q_all[qi64[pick]], k_all, w_all[qi64[pick]], st[pick], cl[pick], K)
