@@ -98,7 +98,7 @@ def indexer_inputs(T: int, Hi: int, Di: int, seed: int, device="cpu", Tk: int | 
 
 
 # Workloads of the pages (shapes only).  Sizes: T tokens, H heads, Dqk/Dv widths, K top-k.
-CONFIGS = {
+WORKLOADS = {
     "tiny": dict(T=256, H=16, Dqk=576, Dv=512, K=64, scale=192 ** -0.5),
     "v32": dict(T=4096, H=128, Dqk=576, Dv=512, K=2048, scale=192 ** -0.5),
     "idx32k": dict(T=32768, H=64, Dqk=576, Dv=512, K=2048, scale=192 ** -0.5, Hi=64, Di=128),

@@ -36,7 +36,7 @@ def check(q, kv, dout, idx, scale, ln=None, use_lo=True):
 
 
 def test_bwd_tiny_config():
-    c = synth.CONFIGS["tiny"]
+    c = synth.WORKLOADS["tiny"]
     q, kv, dout, idx = make_case(c["T"], 0, c["H"], c["Dqk"], c["K"], 0)
     check(q, kv, dout, idx, c["scale"])
 

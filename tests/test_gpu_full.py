@@ -92,7 +92,7 @@ def mla_full_check(q, kv, dout, idx, scale, ln=None, rows=None, chunk=(0, 64), D
 
 def test_full_v32_layout_S4096_H128_K2048():
     # DeepSeek-V3.2 layout: 1 sequence, S=4096, H=128, width 576, K=2048 random causal, scale 192^-0.5
-    c = synth.CONFIGS["v32"]
+    c = synth.WORKLOADS["v32"]
     T = c["T"]
     x = synth.mla_inputs(T, c["H"], c["Dqk"], c["Dv"], seed=2, device=DEV)
     idx = causal_idx_gpu(torch.zeros(T, dtype=torch.int32), c["K"], 2, T)
@@ -103,7 +103,7 @@ def test_full_v32_layout_S4096_H128_K2048():
 
 def test_full_indexer_32k_then_sparse_mla_H64():
     # the benchmark's workload: S=32768, indexer 64x128, K=2048, then H=64 sparse MLA fwd+bwd at width 576
-    c = synth.CONFIGS["idx32k"]
+    c = synth.WORKLOADS["idx32k"]
     T, K = c["T"], c["K"]
     ind = synth.indexer_inputs(T, c["Hi"], c["Di"], seed=3, device=DEV)
     cu = torch.tensor([0, T], dtype=torch.int32, device=DEV)
@@ -122,7 +122,7 @@ def test_full_indexer_32k_then_sparse_mla_H64():
 
 def test_full_nope_S16384_H8_K2051_and_query_chunks():
     # GLM-5.3-Flash NoPE: S=16384, H=8, width 512, unaligned K=2051, scale 512^-0.5; 4096-token chunks = one shot
-    c = synth.CONFIGS["nope"]
+    c = synth.WORKLOADS["nope"]
     T, K = c["T"], c["K"]
     x = synth.mla_inputs(T, c["H"], c["Dqk"], c["Dv"], seed=5, device=DEV)
     idx = causal_idx_gpu(torch.zeros(T, dtype=torch.int32), K, 5, T)
@@ -143,7 +143,7 @@ def test_full_nope_S16384_H8_K2051_and_query_chunks():
 
 def test_full_thd_packed_indexshare_4_layers():
     # 8 sequences, lengths U[4096, 32768] rescaled to 131072 tokens; indexer once, its top-k reused by 4 layers
-    c = synth.CONFIGS["thd"]
+    c = synth.WORKLOADS["thd"]
     T, K = c["T"], c["K"]
     lens = synth.thd_lengths(c["nseq"], c["lo"], c["hi"], T, synth.generator(6))
     cu = synth.cu_seqlens_from_lengths(lens)

@@ -44,7 +44,7 @@ def check(q, kv, idx, scale, ln=None, expect_status=0):
 
 def test_fwd_tiny_config():
     # 1 sequence, T=256, H=16, width 576, K=64, random causal indices, seed 0
-    c = synth.CONFIGS["tiny"]
+    c = synth.WORKLOADS["tiny"]
     q, kv, _, idx = make_case(c["T"], 0, c["H"], c["Dqk"], c["K"], 0)
     check(q, kv, idx, c["scale"])
 
