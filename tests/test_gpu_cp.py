@@ -141,3 +141,48 @@ def test_indexer_cp_ranks_equal_cp1_and_oracle():
         pick = np.unique(np.concatenate([[0, len(qi) // 2 - 1, len(qi) // 2, len(qi) - 1],
                                          rng.choice(len(qi), 40, replace=False)]))
         check_window_rows(idx[pick], ln[pick], q_all[qi64[pick]], k_all, w_all[qi64[pick]], st[pick], cl[pick], K)
+
+
+def test_cp_ranks_through_fwd_bwd_equal_one_shot():
+    # One rank's half of context parallelism end to end: metadata -> indexer -> sparse MLA forward ->
+    # backward on the rank's local rows against all keys, the key gradient accumulated over the ranks.
+    # Rows (indices, out, lse, dq) equal the one-shot run's rows; the summed dkv equals its dkv up to
+    # the order of the fp32 reductions.
+    lens, pads, K, H = [1500, 700], [20, 12], 256, 16
+    cu, P, total = layout(lens, pads, 8)
+    ind = synth.indexer_inputs(total, 64, 128, seed=46)
+    x = synth.mla_inputs(total, H, 576, 512, seed=47)
+    q, kv, dout = x["q"].to(DEV), x["kv"].to(DEV), x["dout"].to(DEV)
+    qx, kx, wx = ind["q_idx"].to(DEV), ind["k_idx"].to(DEV), ind["w"].to(DEV)
+    scale = 192 ** -0.5
+    wi = torch.zeros(4096, dtype=torch.uint8, device=DEV)
+    wf = torch.zeros(dsa.workspace_size("fwd", total, H), dtype=torch.uint8, device=DEV)
+    wb = torch.zeros(dsa.workspace_size("bwd", total, H, K), dtype=torch.uint8, device=DEV)
+
+    def rank_pass(rows, dkv, accumulate):
+        st, cl, _, _ = dsa.dsa_packed_metadata_cp(t32(cu), total, query_indices=rows, cu_seqlens_padded=t32(P))
+        r64 = rows.long()
+        idx, ln = dsa.dsa_indexer_topk_cp(qx[r64].contiguous(), kx, wx[r64].contiguous(), st, cl, K, workspace=wi)
+        out, lse, lo = dsa.dsa_sparse_mla_fwd(q[r64].contiguous(), kv, idx, scale, topk_len=ln, out_lo=True,
+                                              workspace=wf)
+        dq, dkv, _ = dsa.dsa_sparse_mla_bwd(q[r64].contiguous(), kv, idx, scale, out, lse, dout[r64].contiguous(),
+                                            topk_len=ln, out_lo=lo, dkv_accum=dkv, accumulate=accumulate,
+                                            workspace=wb)
+        for w_ in (wi, wf, wb):
+            assert dsa.dsa_read_device_status(w_) == 0
+        return idx, ln, out, lse, dq, dkv
+
+    one = rank_pass(t32(np.arange(total)), torch.empty(total, 576, dtype=torch.float32, device=DEV), False)
+    dkv = torch.empty(total, 576, dtype=torch.float32, device=DEV)
+    for r in range(2):
+        rows = t32(cp_split(total, 2, r))
+        idx, ln, out, lse, dq, dkv = rank_pass(rows, dkv, r > 0)
+        r64 = rows.long()
+        assert torch.equal(idx, one[0][r64]) and torch.equal(ln, one[1][r64])
+        assert torch.equal(out, one[2][r64]) and torch.equal(lse, one[3][r64]) and torch.equal(dq, one[4][r64])
+    err = (dkv - one[5]).norm() / one[5].norm()
+    assert err.item() <= 1e-6, err.item()
+    # padding rows (storage slots past a sequence's real tokens, trailing pack padding) are empty
+    pad = np.setdiff1d(np.arange(total), np.concatenate([np.arange(P[i], P[i] + lens[i]) for i in range(2)]))
+    assert torch.all(one[1][torch.as_tensor(pad).to(DEV)] == 0)
+    assert torch.all(one[2][torch.as_tensor(pad).to(DEV)] == 0)
