@@ -25,8 +25,10 @@
 //    V^T . P^T, as four M = 128 channel tiles.  TMEM holds S^T (64 columns)
 //    and O^T (256 columns); 64 x 512 fp32 O in the heads-on-M orientation
 //    would need M = 64 tiles that leave half of each TMEM lane quadrant idle.
-//  * Each channel tile of the P.V product signals its own barrier, so the
-//    gather of the next tile's chunks starts while the rest of P.V runs.
+//  * P.V runs key rows 0..63 first (P_hi and P_lo for every channel tile),
+//    then rows 64..127, and signals after the first half: the next tile's
+//    rows 0..63 of every value chunk are gathered while the tensor core works
+//    on rows 64..127.
 //  * Online softmax with the running max per head; a rescale of O^T happens
 //    only when some score exceeds the running max by more than 2^8 (lazy
 //    rescale), otherwise P uses the stale max.
@@ -36,8 +38,9 @@
 //    bf16 hi + lo parts, so O carries P to about fp32 accuracy and the
 //    backward's D = <dO, O> is consistent with the exact softmax.  The lo part
 //    of key rows 0..63 has an 8 KiB slot of its own and is written with the hi
-//    part; the lo part of rows 64..127 goes into the P slot once P_hi . V has
-//    read it, while the tensor core runs the first half of P_lo . V.
+//    part; the lo part of rows 64..127 goes into the P slot's rows 0..63 once
+//    the first key half of P.V has read them, while the tensor core runs P_hi
+//    of rows 64..127.
 //  * The epilogue stages O (and, on request, the bf16 residual O - bf16(O))
 //    through shared memory for coalesced 16-byte stores.
 //
@@ -78,7 +81,7 @@ struct Smem {
 
 // misc layout (bytes)
 constexpr int M_BAR_KV = 0;    // [9] chunk landed
-constexpr int M_BAR_PV = 80;   // [4] P.V channel tile done
+constexpr int M_BAR_PV = 80;   // P.V of the tile done
 constexpr int M_BAR_S = 112, M_BAR_P = 120, M_BAR_FIN = 128, M_BAR_PLO = 136, M_BAR_PVH = 144;
 constexpr int M_TMEM = 192, M_NEFF = 196, M_ABORT = 200;
 constexpr int M_RED = 256;             // float [4][64]
@@ -139,6 +142,20 @@ __device__ __forceinline__ void gather_chunk(uint32_t dst_chunk, const __nv_bflo
   cp_async_arrive(bar);
 }
 
+// Rows 0..63 (half 0) or 64..127 (half 1) of the same copy, without the arrive.
+template <int DQK>
+__device__ __forceinline__ void gather_half(uint32_t dst_chunk, const __nv_bfloat16* __restrict__ kv, int c, int tid,
+                                            const int (&rix)[4], int half) {
+  const int uc = tid & 7;
+#pragma unroll
+  for (int e = 2 * half; e < 2 * half + 2; ++e) {
+    const int r = (tid >> 3) + 32 * e;
+    const bool ok = rix[e] >= 0;
+    const __nv_bfloat16* src = kv + (ok ? (size_t)rix[e] * DQK + c * 64 + uc * 8 : 0);
+    cp_async16(dst_chunk + sw128_off(r, uc), src, ok ? 16u : 0u);
+  }
+}
+
 template <int DQK>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_fwd_kernel(const __nv_bfloat16* __restrict__ kv, const __nv_bfloat16* __restrict__ q,
@@ -172,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int c = 0; c < NCH; ++c) mbar_init(bar_kv + 8 * c, kWorkers);
-    for (int m = 0; m < 4; ++m) mbar_init(bar_pv + 8 * m, 1);
+    mbar_init(bar_pv, 1);
     mbar_init(bar_s, 1);
     mbar_init(bar_p, 8);
     mbar_init(bar_plo, 4);  // the warps of key rows 64..127 (lane quadrants 2, 3)
@@ -249,37 +266,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (stop) break;
         mma_commit(bar_s);
-        // O^T += V^T P_hi^T, then O^T += V^T P_lo^T: key rows 0..63 from their own slot while
-        // the workers move rows 64..127 into the P slot
+        // O^T += V^T (P_hi + P_lo)^T, key rows 0..63 first (P_lo of those rows has its own
+        // slot), so that rows 0..63 of every chunk slot are free while rows 64..127 are multiplied
         if (!mbar_wait(bar_p, i & 1, s_abort, err)) break;
         tc_fence_after();
         const uint64_t pb0 = sdesc_sw128(sP, L::KV_CHUNK, 1024);
         const uint64_t lb0 = sdesc_sw128(sPlo, L::KV_CHUNK, 1024);
         const uint64_t va0 = sdesc_sw128(sKV, L::KV_CHUNK, 1024);
         constexpr uint64_t kPair = (2 * L::KV_CHUNK) >> 4;  // descriptor step between channel pairs
+        constexpr int kHalf = kTile / 32;                   // 16-key steps per 64-key half
 #pragma unroll
         for (int m = 0; m < kDv / 128; ++m) {
 #pragma unroll
-          for (int k = 0; k < kTile / 16; ++k)  // + 16 key rows = + 2048 bytes
+          for (int k = 0; k < kHalf; ++k)  // + 16 key rows = + 2048 bytes
             mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV,
                    (i > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < kHalf; ++k)
+            mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), lb0 + (uint64_t)(k * 128), kIdPV, 1u);
         }
-        mma_commit(bar_pvh);
+        mma_commit(bar_pvh);  // rows 0..63 of the chunk slots and of the P slot are read
 #pragma unroll
         for (int m = 0; m < kDv / 128; ++m) {
 #pragma unroll
-          for (int k = 0; k < kTile / 32; ++k)
-            mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), lb0 + (uint64_t)(k * 128), kIdPV, 1u);
+          for (int k = kHalf; k < 2 * kHalf; ++k)
+            mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV, 1u);
         }
+        // P_lo of rows 64..127, moved by the workers into the P slot's rows 0..63
         if (!mbar_wait(bar_plo, i & 1, s_abort, err)) break;
         tc_fence_after();
 #pragma unroll
         for (int m = 0; m < kDv / 128; ++m) {
 #pragma unroll
-          for (int k = kTile / 32; k < kTile / 16; ++k)
-            mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV, 1u);
-          mma_commit(bar_pv + 8 * m);
+          for (int k = kHalf; k < 2 * kHalf; ++k)
+            mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)((k - kHalf) * 128), kIdPV,
+                   1u);
         }
+        mma_commit(bar_pv);  // P.V of this tile is complete
       }
       // every MMA of this CTA completes before the teardown frees TMEM
       mma_commit(bar_fin);
@@ -417,15 +440,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p);
-      // key rows 64..127: the lo part goes into the P slot once V^T P_hi^T has read it
+      // rows 0..63 of every slot are free once bar_pvh completes: the lo part of key rows
+      // 64..127 goes into the P slot's rows 0..63, and the next tile's rows 0..63 are gathered
+      const bool more = i + 1 < ntiles;
+      int rix[4];
+      if (more) load_rows(i + 1, rix);
       {
-        bool okh = true;
+        const bool okh = mbar_wait(bar_pvh, i & 1, s_abort, err);
         if (qd >= 2) {
-          okh = mbar_wait(bar_pvh, i & 1, s_abort, err);
           if (okh) {
 #pragma unroll
             for (int uu = 0; uu < 4; ++uu)
-              st_shared_v4(sP + sw128_off(r, ch * 4 + uu), pl[4 * uu], pl[4 * uu + 1], pl[4 * uu + 2], pl[4 * uu + 3]);
+              st_shared_v4(sP + sw128_off(r - 64, ch * 4 + uu), pl[4 * uu], pl[4 * uu + 1], pl[4 * uu + 2],
+                           pl[4 * uu + 3]);
             fence_proxy_async_smem();
           }
           __syncwarp();
@@ -433,21 +460,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (named_bar_or(bar_id, 128, !okh)) { aborted = true; break; }
       }
-      // ---- gather the next tile, chunk pair by chunk pair as P.V frees them ----
-      if (i + 1 < ntiles) {
-        int rix[4];
-        load_rows(i + 1, rix);
-        for (int m = 0; m < 4 && !aborted; ++m) {
-          if (!mbar_wait(bar_pv + 8 * m, i & 1, s_abort, err)) { aborted = true; break; }
-          gather_chunk<DQK>(sKV + (2 * m) * L::KV_CHUNK, kv, 2 * m, tid, rix, bar_kv + 8 * (2 * m));
-          gather_chunk<DQK>(sKV + (2 * m + 1) * L::KV_CHUNK, kv, 2 * m + 1, tid, rix, bar_kv + 8 * (2 * m + 1));
+      if (more) {
+        for (int c = 0; c < kDv / 64; ++c) gather_half<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, 0);
+        // rows 64..127 (and the RoPE chunk, which holds P) once P.V is complete
+        if (!mbar_wait(bar_pv, i & 1, s_abort, err)) {
+          aborted = true;
+        } else {
+          for (int c = 0; c < kDv / 64; ++c) {
+            gather_half<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, 1);
+            cp_async_arrive(bar_kv + 8 * c);  // covers this thread's copies of both halves
+          }
+          if (NCH == 9) gather_chunk<DQK>(sKV + 8 * L::KV_CHUNK, kv, 8, tid, rix, bar_kv + 8 * 8);
         }
-        if (NCH == 9 && !aborted) gather_chunk<DQK>(sKV + 8 * L::KV_CHUNK, kv, 8, tid, rix, bar_kv + 8 * 8);
         if (named_bar_or(bar_id, 128, aborted)) { aborted = true; break; }
       }
     }
     if (!aborted && ntiles > 0) {
-      const bool got = mbar_wait(bar_pv + 8 * 3, (ntiles - 1) & 1, s_abort, err);
+      const bool got = mbar_wait(bar_pv, (ntiles - 1) & 1, s_abort, err);
       aborted = named_bar_or(bar_id, 128, !got);
       tc_fence_after();
     }
