@@ -473,6 +473,95 @@ def run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, flops_per_step, 
                     "with copies overlapping compute on two copy streams"}
 
 
+def run_workloads(args, local):
+    """Each workload of the pages' table on one GPU (not the benchmark line): MLA fwd+bwd TFLOP/s
+    and % of the sustained bf16 peak, and the indexer's tokens/s where the workload has one.
+    Indices come from the indexer (32k path, THD packing with IndexShare over its layers) or are
+    random causal sets (the others), drawn with the same seeded recipe as the tests."""
+    import statistics
+    import torch
+
+    import sparse_attention_mla_gb300 as dsa
+    from sparse_attention_mla_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    peak = load_peaks().get("bf16_tflops_sustained")
+    for name in args.workloads.split(","):
+        c = synth.WORKLOADS[name]
+        T, H, Dqk, Dv, Kw, scale = c["T"], c["H"], c["Dqk"], c["Dv"], c["K"], c["scale"]
+        layers = c.get("layers", 1)
+        g = synth.generator(0)
+        if "nseq" in c:
+            cu = synth.cu_seqlens_from_lengths(synth.thd_lengths(c["nseq"], c["lo"], c["hi"], T, g))
+        else:
+            cu = torch.tensor([0, T], dtype=torch.int32)
+        st, _, _, _ = dsa.dsa_packed_metadata(cu.to(dev), T)
+        idx_ms = None
+        if "Hi" in c:
+            ind = synth.indexer_inputs(T, c["Hi"], c["Di"], seed=0, device=dev)
+            run_idx = lambda: dsa.dsa_indexer_topk(ind["q_idx"], ind["k_idx"], ind["w"], st, Kw)
+            for _ in range(args.warmup):
+                idx, ln = run_idx()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+            for a, b in ev:
+                a.record(stream)
+                idx, ln = run_idx()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            idx_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+            del ind
+        else:
+            idx = synth.random_causal_topk(st.cpu(), Kw, g).to(dev)
+            ln = (idx >= 0).sum(1).to(torch.int32)
+        x = synth.mla_inputs(T, H, Dqk, Dv, seed=1000, device=dev)
+        wf = torch.zeros(dsa.workspace_size("fwd", T, H), dtype=torch.uint8, device=dev)
+        wb = torch.zeros(dsa.workspace_size("bwd", T, H, Kw), dtype=torch.uint8, device=dev)
+        out = torch.empty(T, H, Dv, dtype=torch.bfloat16, device=dev)
+        lo = torch.empty_like(out)
+        lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+        dq = torch.empty(T, H, Dqk, dtype=torch.bfloat16, device=dev)
+        dkv = torch.empty(T, Dqk, dtype=torch.float32, device=dev)
+        evs = []
+
+        def step(rec):
+            for _ in range(layers):  # IndexShare: every layer reuses the one selection
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)] if rec else None
+                if e: e[0].record(stream)
+                dsa.dsa_sparse_mla_fwd(x["q"], x["kv"], idx, scale, topk_len=ln, out=out, lse=lse, workspace=wf,
+                                       out_lo=lo, Dv=Dv)
+                if e: e[1].record(stream)
+                dsa.dsa_sparse_mla_bwd(x["q"], x["kv"], idx, scale, out, lse, x["dout"], topk_len=ln, dq=dq,
+                                       dkv_accum=dkv, workspace=wb, out_lo=lo)
+                if e: e[2].record(stream)
+                if e: evs.append(e)
+
+        for _ in range(args.warmup):
+            step(False)
+        for _ in range(args.steps):
+            step(True)
+        torch.cuda.synchronize(dev)
+        for w_ in (wf, wb):
+            if dsa.dsa_read_device_status(w_) != 0:
+                raise RuntimeError(f"device status after workload {name}")
+        n = int(ln.sum().item())
+        fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+        bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
+        ff = 2.0 * H * n * (Dqk + Dv)
+        fb = 2.0 * H * n * (3 * Dqk + 2 * Dv)
+        tf = (ff + fb) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12
+        line = {"workload": name, "T": T, "H": H, "Dqk": Dqk, "K": Kw, "layers": layers, "n_valid_slots": n,
+                "mla_fwd_ms": round(fwd_ms, 3), "mla_bwd_ms": round(bwd_ms, 3), "mla_tflops": round(tf, 2),
+                "mla_pct_bf16_sustained": round(100 * tf / peak, 2) if peak else None,
+                "fwd_tflops": round(ff / (fwd_ms * 1e-3) / 1e12, 2), "bwd_tflops": round(fb / (bwd_ms * 1e-3) / 1e12, 2)}
+        if idx_ms is not None:
+            line.update({"indexer_ms": round(idx_ms, 3), "indexer_tokens_per_s": round(T / (idx_ms * 1e-3), 1)})
+        print(json.dumps(line), flush=True)
+        del x, out, lo, dq, dkv, idx, ln
+        torch.cuda.empty_cache()
+
+
 def kernel_rev(src_name: str) -> str:
     """Content hash of a kernel source: ncu counters are reused only for the same code."""
     import hashlib
@@ -493,6 +582,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cp", action="store_true", help="skip the context-parallel indexer line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workloads", default=None,
+                    help="comma-separated workload names (tiny,v32,idx32k,nope,thd): one line per workload "
+                         "instead of the benchmark line")
     ap.add_argument("--seq", type=int, default=32768,
                     help="sequence length; only for small-case profiler captures (the benchmark is 32768)")
     args = ap.parse_args()
@@ -500,6 +592,9 @@ def main():
     S = args.seq
     if args.warmup < 3 and args.impl == "cuda":
         args.warmup = 3
+    if args.workloads:
+        run_workloads(args, int(os.environ.get("LOCAL_RANK", "0")))
+        return
     rank, world, local = dist_init()
     if args.impl == "reference":
         run_reference(args, rank, world)
