@@ -176,25 +176,57 @@ __device__ uint32_t compact(const Half& hf, float* cs, int* ci, int cnt, int tar
     named_bar(hf.bar, 128);  // sel is rewritten by the next pass
   }
   if (passes < 4) {
-    // keep every key >= prefix (the bucket floor): one scan per chunk
+    // keep every key >= prefix (the bucket floor), stably, in place: blocks of 512 candidates,
+    // 4 consecutive ones per thread (16-byte loads), one scan and one barrier per block.  Every
+    // thread has read its 4 before the barrier, and the block's writes land below its end.
     int kept = 0;
-    for (int base = 0; base < cnt; base += 128) {
-      const int e = base + hf.tid;
-      float s = 0.f;
-      int ix = 0;
-      bool keep = false;
-      if (e < cnt) {
-        s = cs[e];
-        ix = ci[e];
-        keep = ordered(s) >= prefix;
+    for (int base = 0; base < cnt; base += 512) {
+      const int e0 = base + 4 * hf.tid;
+      float sv[4] = {0.f, 0.f, 0.f, 0.f};
+      int iv[4] = {0, 0, 0, 0};
+      if (e0 + 3 < cnt) {
+        const float4 a = *reinterpret_cast<const float4*>(cs + e0);
+        const int4 b = *reinterpret_cast<const int4*>(ci + e0);
+        sv[0] = a.x, sv[1] = a.y, sv[2] = a.z, sv[3] = a.w;
+        iv[0] = b.x, iv[1] = b.y, iv[2] = b.z, iv[3] = b.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (e0 + j < cnt) sv[j] = cs[e0 + j], iv[j] = ci[e0 + j];
       }
-      const int2 ke = half_scan(hf, keep, parity);
+      bool keep[4];
+      int m = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        keep[j] = (e0 + j < cnt) && ordered(sv[j]) >= prefix;
+        m += keep[j];
+      }
+      // exclusive scan of m over the 128 threads of the half, in candidate order
+      int incl = m;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (hf.lane >= o) incl += v;
+      }
+      if (hf.lane == 31) hf.wcnt[parity * 4 + hf.wq] = incl;
+      named_bar(hf.bar, 128);
+      int before = 0, total = 0;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int c = hf.wcnt[parity * 4 + w];
+        before += (w < hf.wq) ? c : 0;
+        total += c;
+      }
       parity ^= 1;
-      if (keep) {
-        cs[kept + ke.x] = s;
-        ci[kept + ke.x] = ix;
-      }
-      kept += ke.y;
+      int pos = kept + before + incl - m;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (keep[j]) {
+          cs[pos] = sv[j];
+          ci[pos] = iv[j];
+          ++pos;
+        }
+      kept += total;
     }
     named_bar(hf.bar, 128);
     *kept_out = kept;
