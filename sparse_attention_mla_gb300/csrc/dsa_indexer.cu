@@ -120,6 +120,27 @@ __device__ __forceinline__ int2 half_scan(const Half& hf, bool pred, int par) {
   return make_int2(before, total);
 }
 
+// Exclusive block scan of per-thread counts over the 128 threads of a half, in
+// thread order; returns (exclusive prefix, total).  Uses wcnt[par].
+__device__ __forceinline__ int2 half_scan_count(const Half& hf, int n, int par) {
+  int incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (hf.lane >= o) incl += v;
+  }
+  if (hf.lane == 31) hf.wcnt[par * 4 + hf.wq] = incl;
+  named_bar(hf.bar, 128);
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int c = hf.wcnt[par * 4 + w];
+    before += (w < hf.wq) ? c : 0;
+    total += c;
+  }
+  return make_int2(before + incl - n, total);
+}
+
 // Exact (passes = 4): keep the best `target` of the cnt candidates (score
 // desc, index asc), stably, in place; returns v with "accept iff key > v".
 // Approximate (passes = 2): find the 16-bit key bucket that holds the
@@ -201,24 +222,9 @@ __device__ uint32_t compact(const Half& hf, float* cs, int* ci, int cnt, int tar
         keep[j] = (e0 + j < cnt) && ordered(sv[j]) >= prefix;
         m += keep[j];
       }
-      // exclusive scan of m over the 128 threads of the half, in candidate order
-      int incl = m;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (hf.lane >= o) incl += v;
-      }
-      if (hf.lane == 31) hf.wcnt[parity * 4 + hf.wq] = incl;
-      named_bar(hf.bar, 128);
-      int before = 0, total = 0;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const int c = hf.wcnt[parity * 4 + w];
-        before += (w < hf.wq) ? c : 0;
-        total += c;
-      }
+      const int2 ke = half_scan_count(hf, m, parity);
       parity ^= 1;
-      int pos = kept + before + incl - m;
+      int pos = kept + ke.x;
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         if (keep[j]) {
@@ -226,7 +232,7 @@ __device__ uint32_t compact(const Half& hf, float* cs, int* ci, int cnt, int tar
           ci[pos] = iv[j];
           ++pos;
         }
-      kept += total;
+      kept += ke.y;
     }
     named_bar(hf.bar, 128);
     *kept_out = kept;
@@ -234,27 +240,53 @@ __device__ uint32_t compact(const Half& hf, float* cs, int* ci, int cnt, int tar
   }
   const uint32_t v = prefix;  // kk >= 1 ties at v are kept (the earliest ones)
   int kept = 0, ties = 0;
-  for (int base = 0; base < cnt; base += 128) {
-    const int e = base + hf.tid;
-    float s = 0.f;
-    int ix = 0;
-    uint32_t key = 0;
-    if (e < cnt) {
-      s = cs[e];
-      ix = ci[e];
-      key = ordered(s);
+  // blocks of 512 candidates, 4 consecutive ones per thread; per block one scan of the ties at v
+  // (earlier ties win) and one of the kept, in candidate order.  Every thread has read its 4
+  // before the first barrier, and the block's writes land below its end.
+  for (int base = 0; base < cnt; base += 512) {
+    const int e0 = base + 4 * hf.tid;
+    float sv[4] = {0.f, 0.f, 0.f, 0.f};
+    int iv[4] = {0, 0, 0, 0};
+    if (e0 + 3 < cnt) {
+      const float4 a = *reinterpret_cast<const float4*>(cs + e0);
+      const int4 b = *reinterpret_cast<const int4*>(ci + e0);
+      sv[0] = a.x, sv[1] = a.y, sv[2] = a.z, sv[3] = a.w;
+      iv[0] = b.x, iv[1] = b.y, iv[2] = b.z, iv[3] = b.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (e0 + j < cnt) sv[j] = cs[e0 + j], iv[j] = ci[e0 + j];
     }
-    const bool eq = (e < cnt) && key == v;
-    const int2 te = half_scan(hf, eq, parity);
-    parity ^= 1;
-    const bool keep = (e < cnt) && (key > v || (eq && ties + te.x < kk));
-    const int2 ke = half_scan(hf, keep, parity);
-    parity ^= 1;
-    // every thread has read its element (before the scans' barriers) -> safe to write
-    if (keep) {
-      cs[kept + ke.x] = s;
-      ci[kept + ke.x] = ix;
+    uint32_t key[4];
+    bool eq[4];
+    int neq = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      key[j] = ordered(sv[j]);
+      eq[j] = (e0 + j < cnt) && key[j] == v;
+      neq += eq[j];
     }
+    const int2 te = half_scan_count(hf, neq, parity);
+    parity ^= 1;
+    int tie_rank = ties + te.x;  // ties at v before this thread's candidates
+    bool keep[4];
+    int nkeep = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      keep[j] = (e0 + j < cnt) && (key[j] > v || (eq[j] && tie_rank < kk));
+      tie_rank += eq[j];
+      nkeep += keep[j];
+    }
+    const int2 ke = half_scan_count(hf, nkeep, parity);
+    parity ^= 1;
+    int pos = kept + ke.x;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (keep[j]) {
+        cs[pos] = sv[j];
+        ci[pos] = iv[j];
+        ++pos;
+      }
     kept += ke.y;
     ties += te.y;
   }
