@@ -58,9 +58,9 @@ def _load():
             lib.oracle_indexer_topk.restype = None
             lib.oracle_indexer_topk_window.argtypes = [P, P, P, P, P, I, I, I, I, P, P, P]
             lib.oracle_indexer_topk_window.restype = None
-            lib.oracle_sparse_mla_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, P]
+            lib.oracle_sparse_mla_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, P, P]
             lib.oracle_sparse_mla_fwd.restype = None
-            lib.oracle_sparse_mla_bwd.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, P, P]
+            lib.oracle_sparse_mla_bwd.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, P, P, P, P, P]
             lib.oracle_sparse_mla_bwd.restype = None
             _lib = lib
     return _lib
@@ -176,8 +176,9 @@ def indexer_topk_window(q_idx_rows, k_idx, w_rows, win_start, win_len, K: int):
     return idx, ln, kth
 
 
-def sparse_mla_fwd(q_rows, kv, idx_rows, scale: float, Dv: int = 512, len_rows=None):
-    """Sparse MLA forward for the given query rows -> (out [n,H,Dv], lse [n,H]) in fp64."""
+def sparse_mla_fwd(q_rows, kv, idx_rows, scale: float, Dv: int = 512, len_rows=None, sink=None):
+    """Sparse MLA forward for the given query rows -> (out [n,H,Dv], lse [n,H]) in fp64.
+    sink: per-head sink logits [H] (one more logit per row with no value row), or None."""
     q = _f64(q_rows)
     kvf = _f64(kv).reshape(kv.shape[0], -1)
     idx = _i32(idx_rows)
@@ -186,13 +187,18 @@ def sparse_mla_fwd(q_rows, kv, idx_rows, scale: float, Dv: int = 512, len_rows=N
     K = idx.shape[1]
     out = np.zeros((n, H, Dv), np.float64)
     lse = np.zeros((n, H), np.float64)
+    sk = None if sink is None else _f64(sink).reshape(H)
     _load().oracle_sparse_mla_fwd(_p(q), _p(kvf), _p(idx), _p(ln), n, kvf.shape[0], H, Dqk, Dv, K,
-                                  float(scale), _p(out), _p(lse))
+                                  float(scale), _p(sk), _p(out), _p(lse))
     return out, lse
 
 
-def sparse_mla_bwd(q_rows, kv, idx_rows, dout_rows, scale: float, Dv: int = 512, len_rows=None, dkv=None):
-    """Sparse MLA backward for the given rows -> (dq [n,H,Dqk], dkv [Tk,Dqk]) in fp64.
+def sparse_mla_bwd(q_rows, kv, idx_rows, dout_rows, scale: float, Dv: int = 512, len_rows=None, dkv=None,
+                   with_dq_magnitude: bool = False, sink=None, d_sink=None):
+    """Sparse MLA backward for the given rows -> (dq [n,H,Dqk], dkv [Tk,Dqk]) in fp64, and with
+    with_dq_magnitude also dq_mag [n,H,Dqk] = scale * sum_j |dS_j| |kv[idx_j, :]| (the scale of
+    the error of a dq formed from dS rounded to a 16-bit float).  With a sink [H], d_sink [H] (fp64,
+    created when None) receives -sum_t P_sink D and is returned after dkv.
 
     dkv accumulates the contributions of exactly these rows (pass an existing
     array to keep adding, as query chunks do)."""
@@ -204,9 +210,15 @@ def sparse_mla_bwd(q_rows, kv, idx_rows, dout_rows, scale: float, Dv: int = 512,
     n, H, Dqk = q.shape
     K = idx.shape[1]
     dq = np.zeros((n, H, Dqk), np.float64)
+    mag = np.zeros((n, H, Dqk), np.float64) if with_dq_magnitude else None
+    sk = None if sink is None else _f64(sink).reshape(H)
+    if sk is not None and d_sink is None:
+        d_sink = np.zeros(H, np.float64)
     if dkv is None:
         dkv = np.zeros((kvf.shape[0], Dqk), np.float64)
     assert dkv.dtype == np.float64 and dkv.flags.c_contiguous
     _load().oracle_sparse_mla_bwd(_p(q), _p(kvf), _p(idx), _p(ln), n, kvf.shape[0], H, Dqk, Dv, K,
-                                  float(scale), _p(do), _p(dq), _p(dkv))
-    return dq, dkv
+                                  float(scale), _p(sk), _p(do), _p(dq), _p(dkv), _p(None if sk is None else d_sink),
+                                  _p(mag))
+    res = (dq, dkv) + ((d_sink,) if sk is not None else ()) + ((mag,) if with_dq_magnitude else ())
+    return res

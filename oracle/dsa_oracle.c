@@ -19,6 +19,9 @@
  * open, the reading taken is written next to the step.
  */
 #include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -241,11 +244,16 @@ static int slot_valid(const int32_t *idx_row, const int32_t *len, int64_t r, int
 /*   z_j = scale * <q[t,h,:Dqk], kv[idx_j,:Dqk]>                              */
 /*   L   = log sum_j exp(z_j)      (natural log; -inf when J is empty)        */
 /*   O   = sum_j exp(z_j - L) kv[idx_j, :Dv]   (0 when J is empty)            */
+/* Attention sink ([cudnn_dsa] _pad_attention_heads pads a sink [H] together  */
+/* with q; the pages print no formula).  Reading: sink[h] is one more logit   */
+/* of every row of head h, in the units of z, with no value row:              */
+/*   L = log(sum_j exp(z_j) + exp(sink[h])),  O = sum_j exp(z_j - L) kv_j     */
+/* so an empty row gets L = sink[h] and O = 0.  sink == NULL: no sink.        */
 /* ------------------------------------------------------------------------ */
 static void fwd_row(const double *q_r /*[H,Dqk]*/, const double *kv, const int32_t *idx_row,
                     const int32_t *len, int64_t r, int Tk, int H, int Dqk, int Dv, int K,
-                    double scale, double *o_r /*[H,Dv]*/, double *lse_r /*[H]*/,
-                    double *p_r /*[H,K] nullable: softmax weights per slot*/) {
+                    double scale, const double *sink /*[H] or NULL*/, double *o_r /*[H,Dv]*/,
+                    double *lse_r /*[H]*/, double *p_r /*[H,K] nullable: softmax weights per slot*/) {
   double *z = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
   for (int h = 0; h < H; ++h) {
     const double *qh = q_r + (size_t)h * Dqk;
@@ -258,6 +266,7 @@ static void fwd_row(const double *q_r /*[H,Dqk]*/, const double *kv, const int32
       z[j] = scale * dot;
       if (z[j] > m) m = z[j];
     }
+    if (sink && sink[h] > m) m = sink[h];
     double *oh = o_r + (size_t)h * Dv;
     for (int v = 0; v < Dv; ++v) oh[v] = 0.0;
     if (m == -INFINITY) {
@@ -267,6 +276,7 @@ static void fwd_row(const double *q_r /*[H,Dqk]*/, const double *kv, const int32
     }
     double sum = 0.0;
     for (int j = 0; j < K; ++j) if (z[j] != -INFINITY) sum += exp(z[j] - m);
+    if (sink) sum += exp(sink[h] - m);
     double L = m + log(sum);
     lse_r[h] = L;
     for (int j = 0; j < K; ++j) {
@@ -284,11 +294,11 @@ static void fwd_row(const double *q_r /*[H,Dqk]*/, const double *kv, const int32
  * kv [Tk, Dqk].  Outputs out [nrows, H, Dv], lse [nrows, H]. */
 void oracle_sparse_mla_fwd(const double *q_rows, const double *kv, const int32_t *idx_rows,
                            const int32_t *len_rows, int nrows, int Tk, int H, int Dqk, int Dv,
-                           int K, double scale, double *out, double *lse) {
+                           int K, double scale, const double *sink, double *out, double *lse) {
 #pragma omp parallel for schedule(dynamic, 1)
   for (int r = 0; r < nrows; ++r)
     fwd_row(q_rows + (size_t)r * H * Dqk, kv, idx_rows + (size_t)r * K, len_rows, r, Tk, H,
-            Dqk, Dv, K, scale, out + (size_t)r * H * Dv, lse + (size_t)r * H, NULL);
+            Dqk, Dv, K, scale, sink, out + (size_t)r * H * Dv, lse + (size_t)r * H, NULL);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -304,14 +314,26 @@ void oracle_sparse_mla_fwd(const double *q_rows, const double *kv, const int32_t
 /* query rows are independent and key gradients sum, so dkv accumulates over  */
 /* whatever rows are passed in.  The dkv sum runs over channels in parallel   */
 /* with a fixed (row, slot, head) order, so it is deterministic.             */
+/* With a sink, P and O are those of the forward above; O is sum_j P_j kv_j  */
+/* with P_sink = exp(sink[h] - L) left out, so dO/dsink = -P_sink O and      */
+/*   d_sink[h] += -sum_t P_sink[t,h] D[t,h]                                   */
+/* (d_sink nullable; added to, like dkv).                                     */
+/* dq_mag (nullable) receives scale * sum_j |dS_j| |kv[idx_j, d]| per         */
+/* (row, head, channel): the scale of the error that rounding each dS_j to a  */
+/* 16-bit float before the dq sum can cause.                                  */
 /* ------------------------------------------------------------------------ */
 void oracle_sparse_mla_bwd(const double *q_rows, const double *kv, const int32_t *idx_rows,
                            const int32_t *len_rows, int nrows, int Tk, int H, int Dqk, int Dv,
-                           int K, double scale, const double *dout_rows /*[nrows,H,Dv]*/,
-                           double *dq /*[nrows,H,Dqk]*/, double *dkv /*[Tk,Dqk], added to*/) {
+                           int K, double scale, const double *sink /*[H] or NULL*/,
+                           const double *dout_rows /*[nrows,H,Dv]*/,
+                           double *dq /*[nrows,H,Dqk]*/, double *dkv /*[Tk,Dqk], added to*/,
+                           double *d_sink /*[H] or NULL, added to*/,
+                           double *dq_mag /*[nrows,H,Dqk] or NULL*/) {
   size_t pk = (size_t)nrows * H * K;
   double *P = (double *)calloc(pk ? pk : 1, sizeof(double));
   double *dS = (double *)calloc(pk ? pk : 1, sizeof(double));
+  /* per-row sink gradient terms, summed in row order after the parallel loop */
+  double *gs = (sink && d_sink) ? (double *)calloc((size_t)nrows * H + 1, sizeof(double)) : NULL;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int r = 0; r < nrows; ++r) {
     const double *q_r = q_rows + (size_t)r * H * Dqk;
@@ -320,13 +342,16 @@ void oracle_sparse_mla_bwd(const double *q_rows, const double *kv, const int32_t
     double *lse_r = (double *)malloc(sizeof(double) * (size_t)H);
     double *p_r = P + (size_t)r * H * K;
     double *ds_r = dS + (size_t)r * H * K;
-    fwd_row(q_r, kv, idx_row, len_rows, r, Tk, H, Dqk, Dv, K, scale, o_r, lse_r, p_r);
+    fwd_row(q_r, kv, idx_row, len_rows, r, Tk, H, Dqk, Dv, K, scale, sink, o_r, lse_r, p_r);
     for (int h = 0; h < H; ++h) {
       const double *dO = dout_rows + ((size_t)r * H + h) * Dv;
       double D = 0.0;
       for (int v = 0; v < Dv; ++v) D += dO[v] * o_r[(size_t)h * Dv + v];
+      if (gs && lse_r[h] != -INFINITY) gs[(size_t)r * H + h] = -exp(sink[h] - lse_r[h]) * D;
       double *dqh = dq + ((size_t)r * H + h) * Dqk;
+      double *mgh = dq_mag ? dq_mag + ((size_t)r * H + h) * Dqk : NULL;
       for (int d = 0; d < Dqk; ++d) dqh[d] = 0.0;
+      if (mgh) for (int d = 0; d < Dqk; ++d) mgh[d] = 0.0;
       for (int j = 0; j < K; ++j) {
         double p = p_r[(size_t)h * K + j];
         if (p == 0.0) { ds_r[(size_t)h * K + j] = 0.0; continue; }
@@ -336,27 +361,49 @@ void oracle_sparse_mla_bwd(const double *q_rows, const double *kv, const int32_t
         double ds = p * (dp - D);
         ds_r[(size_t)h * K + j] = ds;
         for (int d = 0; d < Dqk; ++d) dqh[d] += scale * ds * kr[d];
+        if (mgh) for (int d = 0; d < Dqk; ++d) mgh[d] += scale * fabs(ds) * fabs(kr[d]);
       }
     }
     free(o_r);
     free(lse_r);
   }
-  /* key gradient: parallel over channels, fixed order over (row, slot, head) */
-#pragma omp parallel for schedule(static)
-  for (int d = 0; d < Dqk; ++d) {
+  if (gs) {
+    for (int r = 0; r < nrows; ++r)
+      for (int h = 0; h < H; ++h) d_sink[h] += gs[(size_t)r * H + h];
+    free(gs);
+  }
+  /* key gradient: each thread owns a contiguous range of channels and walks the
+   * (row, slot, head) triples in a fixed order, so every element sees the same
+   * summation order whatever the thread count: per (row, slot) the head terms
+   * are summed first (dS term, then P term, head by head), then added to dkv. */
+#pragma omp parallel
+  {
+    int nth = 1, id = 0;
+#ifdef _OPENMP
+    nth = omp_get_num_threads();
+    id = omp_get_thread_num();
+#endif
+    const int d0 = (int)((int64_t)Dqk * id / nth), d1 = (int)((int64_t)Dqk * (id + 1) / nth);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)(d1 > d0 ? d1 - d0 : 1));
     for (int r = 0; r < nrows; ++r) {
       const int32_t *idx_row = idx_rows + (size_t)r * K;
       for (int j = 0; j < K; ++j) {
         if (!slot_valid(idx_row, len_rows, r, j, Tk)) continue;
-        double acc = 0.0;
+        for (int d = d0; d < d1; ++d) acc[d - d0] = 0.0;
         for (int h = 0; h < H; ++h) {
           size_t pj = ((size_t)r * H + h) * K + j;
-          acc += scale * dS[pj] * q_rows[((size_t)r * H + h) * Dqk + d];
-          if (d < Dv) acc += P[pj] * dout_rows[((size_t)r * H + h) * Dv + d];
+          const double *qh = q_rows + ((size_t)r * H + h) * Dqk;
+          const double *doh = dout_rows + ((size_t)r * H + h) * Dv;
+          for (int d = d0; d < d1; ++d) {
+            acc[d - d0] += scale * dS[pj] * qh[d];
+            if (d < Dv) acc[d - d0] += P[pj] * doh[d];
+          }
         }
-        dkv[(size_t)idx_row[j] * Dqk + d] += acc;
+        double *dst = dkv + (size_t)idx_row[j] * Dqk;
+        for (int d = d0; d < d1; ++d) dst[d] += acc[d - d0];
       }
     }
+    free(acc);
   }
   free(P);
   free(dS);

@@ -185,6 +185,24 @@ def test_indexer_special_cases():
     assert np.all(got0 == 0.0)
 
 
+def test_indexer_score_magnitude_matches_numpy():
+    # the magnitude the tie band is built from: sum_h |w[t,h]| sum_d |q[t,h,d] k[s,d]| (library route,
+    # numpy), and a closed form: with q, k, w all positive no ReLU cuts and no term cancels, so the
+    # magnitude equals the score itself
+    rng = np.random.default_rng(21)
+    T, Hi, Di = 7, 5, 12
+    q = rng.standard_normal((T, Hi, Di))
+    k = rng.standard_normal((T, Di))
+    w = rng.uniform(-0.5, 1.0, (T, Hi))
+    pr, pk = np.meshgrid(np.arange(T), np.arange(T), indexing="ij")
+    _, mag = oracle.indexer_scores(q, k, w, pr.ravel(), pk.ravel(), with_magnitude=True)
+    ref = np.einsum("th,thsd->ts", np.abs(w), np.abs(np.einsum("thd,sd->thsd", q, k)))
+    np.testing.assert_allclose(mag.reshape(T, T), ref, rtol=1e-13, atol=1e-13)
+    qp, kp, wp = np.abs(q), np.abs(k), np.abs(w)
+    sc, magp = oracle.indexer_scores(qp, kp, wp, pr.ravel(), pk.ravel(), with_magnitude=True)
+    np.testing.assert_allclose(magp, sc, rtol=1e-13, atol=0)
+
+
 # --------------------------------------------------------------------------
 # causal top-k
 # --------------------------------------------------------------------------
@@ -435,6 +453,26 @@ def test_bwd_query_chunks_sum_to_one_shot():
     np.testing.assert_allclose(acc, dkv, rtol=1e-12, atol=1e-12)
 
 
+def test_bwd_dq_magnitude_bounds_dq_and_is_tight_on_two_mirrored_slots():
+    # dq_mag = scale sum_j |dS_j| |kv[idx_j]| bounds |dq| (triangle inequality) on any input; with two
+    # valid slots whose kv rows are negatives of each other dS_2 = -dS_1 (sum_j dS_j = 0) and
+    # dq = scale dS_1 (kv_1 - kv_2) = 2 scale dS_1 kv_1, so |dq| equals the magnitude exactly
+    q, kv, dout, idx = rand_case(T=20, seed=16)
+    dq, _, mag = oracle.sparse_mla_bwd(q, kv, idx, dout, 0.3, Dv=8, with_dq_magnitude=True)
+    assert np.all(np.abs(dq) <= mag * (1 + 1e-12) + 1e-300)
+    rng = np.random.default_rng(17)
+    H, Dqk, Dv = 3, 10, 6
+    kv2 = np.zeros((2, Dqk))
+    kv2[0] = rng.uniform(0.5, 2.0, Dqk)
+    kv2[1] = -kv2[0]
+    q2 = rng.standard_normal((1, H, Dqk))
+    do2 = rng.standard_normal((1, H, Dv))
+    idx2 = np.array([[0, 1]], dtype=np.int32)
+    dq2, _, mag2 = oracle.sparse_mla_bwd(q2, kv2, idx2, do2, 0.7, Dv=Dv, with_dq_magnitude=True)
+    assert np.all(mag2 > 0)
+    np.testing.assert_allclose(np.abs(dq2), mag2, rtol=1e-12, atol=0)
+
+
 def test_oracle_takes_bf16_tensors_exactly():
     # bf16 inputs are widened exactly: bf16 -> float64 of the same value
     x = synth.randn_bf16((3, 2, 8), synth.generator(14))
@@ -443,3 +481,76 @@ def test_oracle_takes_bf16_tensors_exactly():
     o1, _ = oracle.sparse_mla_fwd(x, kv, idx, 0.5, Dv=4)
     o2, _ = oracle.sparse_mla_fwd(x.double().numpy(), kv.double().numpy(), idx.numpy(), 0.5, Dv=4)
     np.testing.assert_array_equal(o1, o2)
+
+
+# --------------------------------------------------------------------------
+# attention sink (per-head logit with no value row)
+# --------------------------------------------------------------------------
+def dense_attention_with_sink(q, kv, mask, scale, Dv, sink):
+    """torch fp64: the masked score matrix with one more column per head holding the sink logit,
+    softmax over keys + sink, the sink's weight multiplying a zero value row."""
+    s = scale * torch.einsum("thd,sd->ths", q, kv)
+    s = s.masked_fill(~torch.as_tensor(mask)[:, None, :], float("-inf"))
+    col = sink[None, :, None].expand(s.shape[0], s.shape[1], 1)
+    s = torch.cat([s, col], dim=-1)
+    lse = torch.logsumexp(s, dim=-1)
+    p = torch.softmax(s, dim=-1)[..., :-1]
+    return torch.einsum("ths,sv->thv", p, kv[:, :Dv]), lse
+
+
+def test_sink_matches_dense_softmax_with_a_sink_column_and_autograd():
+    q, kv, dout, idx = rand_case(seed=31)
+    idx[2, :] = -1  # an empty row: only the sink remains
+    sink = np.array([0.7, -1.3, 2.1])
+    scale = 0.35
+    out, lse = oracle.sparse_mla_fwd(q, kv, idx, scale, Dv=8, sink=sink)
+    dq, dkv, dsink = oracle.sparse_mla_bwd(q, kv, idx, dout, scale, Dv=8, sink=sink)
+    qt = torch.tensor(q, requires_grad=True)
+    kt = torch.tensor(kv, requires_grad=True)
+    st = torch.tensor(sink, requires_grad=True)
+    o, l = dense_attention_with_sink(qt, kt, mask_from_idx(idx, kv.shape[0]), scale, 8, st)
+    np.testing.assert_allclose(out, o.detach().numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, l.detach().numpy(), rtol=1e-12, atol=1e-13)
+    o.backward(torch.tensor(dout))
+    np.testing.assert_allclose(dq, qt.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dkv, kt.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dsink, st.grad.numpy(), rtol=1e-11, atol=1e-12)
+    assert np.all(out[2] == 0.0) and np.allclose(lse[2], sink, rtol=0, atol=0)
+
+
+def test_sink_closed_forms_and_minus_infinity():
+    # one valid slot with score z: lse = log(e^z + e^s), O = sigmoid(z - s) kv_row
+    rng = np.random.default_rng(32)
+    q = rng.standard_normal((1, 2, 6))
+    kv = rng.standard_normal((3, 6))
+    idx = np.array([[1, -1, -1]], dtype=np.int32)
+    sink = np.array([0.4, -0.9])
+    out, lse = oracle.sparse_mla_fwd(q, kv, idx, 0.5, Dv=4, sink=sink)
+    z = 0.5 * q[0] @ kv[1]
+    np.testing.assert_allclose(lse[0], np.logaddexp(z, sink), rtol=1e-14)
+    np.testing.assert_allclose(out[0], (1.0 / (1.0 + np.exp(sink - z)))[:, None] * kv[1, :4][None, :], rtol=1e-13)
+    # a sink of -inf is no sink at all, gradients included
+    q, kv, dout, idx = rand_case(seed=33)
+    o0, l0 = oracle.sparse_mla_fwd(q, kv, idx, 0.3, Dv=8)
+    o1, l1 = oracle.sparse_mla_fwd(q, kv, idx, 0.3, Dv=8, sink=np.full(3, -np.inf))
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
+    dq0, dkv0 = oracle.sparse_mla_bwd(q, kv, idx, dout, 0.3, Dv=8)
+    dq1, dkv1, ds1 = oracle.sparse_mla_bwd(q, kv, idx, dout, 0.3, Dv=8, sink=np.full(3, -np.inf))
+    np.testing.assert_array_equal(dq0, dq1)
+    np.testing.assert_array_equal(dkv0, dkv1)
+    assert np.all(ds1 == 0.0)
+
+
+def test_sink_gradient_central_finite_differences():
+    q, kv, dout, idx = rand_case(T=9, H=3, Dqk=6, Dv=4, K=4, seed=34, holes=False)
+    sink = np.array([0.2, -0.5, 1.1])
+    _, _, dsink = oracle.sparse_mla_bwd(q, kv, idx, dout, 0.45, Dv=4, sink=sink)
+    eps = 1e-6
+    for h in range(3):
+        a, b = sink.copy(), sink.copy()
+        a[h] += eps
+        b[h] -= eps
+        fa = np.sum(oracle.sparse_mla_fwd(q, kv, idx, 0.45, Dv=4, sink=a)[0] * dout)
+        fb = np.sum(oracle.sparse_mla_fwd(q, kv, idx, 0.45, Dv=4, sink=b)[0] * dout)
+        np.testing.assert_allclose(dsink[h], (fa - fb) / (2 * eps), rtol=1e-6, atol=1e-9)
