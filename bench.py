@@ -197,7 +197,7 @@ def oracle_sample(rows: int, seed: int = 0) -> dict:
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    rows = 2
+    rows = os.cpu_count() or 1  # one query row per host core (the oracle is parallel over rows)
     for _ in range(args.warmup):
         oracle_sample(rows)
     vals, idx_rates, wall = [], [], []
@@ -300,25 +300,40 @@ def run_cuda(args, rank, world, local):
     value = world * args.steps * (f_fwd + f_bwd) / (mla_ms_total * 1e-3) / 1e12
     idx_tok_s = world * S / (idx_ms * 1e-3)
 
-    # ---- roofline of the dominant kernel (the backward: most FLOPs and time) ----
-    bwd_tflops = f_bwd / (bwd_ms * 1e-3) / 1e12
+    # ---- rooflines: each kernel's algorithmic work over its CUDA-event time; the dominant kernel
+    # (the backward: most FLOPs and time) is `roofline` ----
     peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-    traffic = None
-    tfile = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tfile):
-        with open(tfile) as f:
-            tr = json.load(f).get("sparse_mla_bwd_kernel")
-        if tr and tr.get("kernel_rev") == kernel_rev("dsa_bwd.cu"):
-            traffic = tr["bytes_per_valid_slot"] * n_valid
-    roofline = {"bound": "tensor", "kernel": "sparse_mla_bwd_kernel", "achieved": round(bwd_tflops, 2),
-                "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_tflops / peak, 4), "traffic": traffic,
-                "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)"}
+    src = f"{peaks['source']} bf16 sustained (kernels timed inside a long step)"
+    n_pairs = int((torch.arange(S, device=dev) - seq_start + 1).clamp(min=0).sum().item())
+    f_idx = 2.0 * HI * DI * n_pairs
+    idx_bytes = S * HI * DI * 2 + S * DI * 2 + S * HI * 4 + S * K * 4 + S * 4  # q_idx, k_idx, w, idx, len
+    units = {"sparse_mla_bwd_kernel": n_valid, "sparse_mla_fwd_kernel": n_valid, "indexer_topk_kernel": S}
+    per_kernel = {}
+    for name, flops, ms, src_file in (("sparse_mla_bwd_kernel", f_bwd, bwd_ms, "dsa_bwd.cu"),
+                                      ("sparse_mla_fwd_kernel", f_fwd, fwd_ms, "dsa_fwd.cu"),
+                                      ("indexer_topk_kernel", f_idx, idx_ms, "dsa_indexer.cu")):
+        ach = flops / (ms * 1e-3) / 1e12
+        per_kernel[name] = {"bound": "tensor", "kernel": name, "achieved": round(ach, 2), "peak": peak,
+                            "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                            "traffic": traffic_per_launch(name, src_file, units[name]), "ms": round(ms, 3),
+                            "peak_source": src}
+    hbm = peaks.get("hbm_gbs")
+    idx_gbs = idx_bytes / (idx_ms * 1e-3) / 1e9
+    per_kernel["indexer_topk_kernel"].update({"causal_pairs": n_pairs, "hbm_algorithmic_bytes": idx_bytes,
+                                              "hbm_achieved_gbs": round(idx_gbs, 1),
+                                              "hbm_frac": round(idx_gbs / hbm, 4) if hbm else None})
+    roofline = per_kernel["sparse_mla_bwd_kernel"]
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, f_fwd + f_bwd, world)
     cp = None if args.no_cp else run_cp_indexer(args, dsa, torch, dev, stream, ind, topk_idx, topk_len)
+    workloads = None
+    if not args.no_workloads:
+        del ws_b
+        torch.cuda.empty_cache()
+        workloads = {name: time_workload(name, args, dev, stream) for name in ("v32", "nope")}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -334,11 +349,13 @@ def run_cuda(args, rank, world, local):
                           "sparse_mla_bwd": round(bwd_ms, 3)},
         "n_valid_slots": n_valid,
         "roofline": roofline,
+        "roofline_kernels": per_kernel,
         "l2_model": l2_model(n_valid, n_tiles, fwd_ms, bwd_ms),
         "clocks": clocks,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 3 * args.steps,  # indexer, forward, backward per step
         "e2e": e2e,
         "cp_indexer": cp,
+        "workloads": workloads,
     }
     if rank == 0 and not args.no_cpu_baseline:
         r = oracle_sample(16)
@@ -402,6 +419,9 @@ def run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, flops_per_step, 
     CH = 4096
     chunks = [(a, min(S, a + CH)) for a in range(0, S, CH)]
     comp, cin, cout = stream, torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    # every workspace is allocated once, before the timed steps
+    ws_i = torch.empty(dsa.workspace_size("indexer", S, K), dtype=torch.uint8, device=dev)
+    ws_f = torch.empty(dsa.workspace_size("fwd", CH, H), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(dsa.workspace_size("bwd", CH, H, K), dtype=torch.uint8, device=dev)
     whole = ("k_idx", "kv", "q_idx", "w")           # the indexer's inputs and the keys: copied first
     per_chunk_in = ("q", "dout")                    # copied per query chunk
@@ -426,7 +446,7 @@ def run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, flops_per_step, 
         with torch.cuda.stream(comp):
             comp.wait_event(ev_whole)
             dsa.dsa_indexer_topk(dev_in["q_idx"], dev_in["k_idx"], dev_in["w"], seq_start, K,
-                                 topk_idx=dres["topk_idx"], topk_len=dres["topk_len"])
+                                 topk_idx=dres["topk_idx"], topk_len=dres["topk_len"], workspace=ws_i)
             ev_idx = torch.cuda.Event()
             ev_idx.record(comp)
         with torch.cuda.stream(cout):
@@ -438,7 +458,7 @@ def run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, flops_per_step, 
                 comp.wait_event(ev_in[c])
                 dsa.dsa_sparse_mla_fwd(dev_in["q"][a:b], dev_in["kv"], dres["topk_idx"][a:b], SCALE,
                                        topk_len=dres["topk_len"][a:b], out=dres["out"][a:b], lse=dres["lse"][a:b],
-                                       out_lo=dres["out_lo"][a:b])
+                                       out_lo=dres["out_lo"][a:b], workspace=ws_f)
                 dsa.dsa_sparse_mla_bwd(dev_in["q"][a:b], dev_in["kv"], dres["topk_idx"][a:b], SCALE,
                                        dres["out"][a:b], dres["lse"][a:b], dev_in["dout"][a:b],
                                        topk_len=dres["topk_len"][a:b], dq=dres["dq"][a:b], dkv_accum=dres["dkv"],
@@ -473,93 +493,117 @@ def run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, flops_per_step, 
                     "with copies overlapping compute on two copy streams"}
 
 
-def run_workloads(args, local):
-    """Each workload of the pages' table on one GPU (not the benchmark line): MLA fwd+bwd TFLOP/s
-    and % of the sustained bf16 peak, and the indexer's tokens/s where the workload has one.
-    Indices come from the indexer (32k path, THD packing with IndexShare over its layers) or are
-    random causal sets (the others), drawn with the same seeded recipe as the tests."""
-    import statistics
+def time_workload(name, args, dev, stream) -> dict:
+    """One workload of the pages' table on this GPU: MLA fwd+bwd TFLOP/s and % of the sustained bf16
+    peak (CUDA events on the launching stream, median over the timed steps), and the indexer's
+    tokens/s where the workload has one.  Indices come from the indexer (32k path, THD packing with
+    IndexShare over its layers) or are random causal sets (the others), drawn with the same seeded
+    recipe as the tests; the backward gets the forward's residual of O, as in the benchmark step."""
     import torch
 
     import sparse_attention_mla_gb300 as dsa
     from sparse_attention_mla_gb300 import synth
 
+    peak = load_peaks().get("bf16_tflops_sustained")
+    c = synth.WORKLOADS[name]
+    T, Hh, Dqk, Dv, Kw, scale = c["T"], c["H"], c["Dqk"], c["Dv"], c["K"], c["scale"]
+    layers = c.get("layers", 1)
+    g = synth.generator(0)
+    if "nseq" in c:
+        cu = synth.cu_seqlens_from_lengths(synth.thd_lengths(c["nseq"], c["lo"], c["hi"], T, g))
+    else:
+        cu = torch.tensor([0, T], dtype=torch.int32)
+    st, _, _, _ = dsa.dsa_packed_metadata(cu.to(dev), T)
+    idx_ms = None
+    if "Hi" in c:
+        ind = synth.indexer_inputs(T, c["Hi"], c["Di"], seed=0, device=dev)
+        wi = torch.zeros(dsa.workspace_size("indexer", T, Kw), dtype=torch.uint8, device=dev)
+        run_idx = lambda: dsa.dsa_indexer_topk(ind["q_idx"], ind["k_idx"], ind["w"], st, Kw, workspace=wi)
+        for _ in range(args.warmup):
+            idx, ln = run_idx()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in ev:
+            a.record(stream)
+            idx, ln = run_idx()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        idx_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        del ind
+    else:
+        idx = synth.random_causal_topk(st.cpu(), Kw, g).to(dev)
+        ln = (idx >= 0).sum(1).to(torch.int32)
+    x = synth.mla_inputs(T, Hh, Dqk, Dv, seed=1000, device=dev)
+    wf = torch.zeros(dsa.workspace_size("fwd", T, Hh), dtype=torch.uint8, device=dev)
+    wb = torch.zeros(dsa.workspace_size("bwd", T, Hh, Kw), dtype=torch.uint8, device=dev)
+    out = torch.empty(T, Hh, Dv, dtype=torch.bfloat16, device=dev)
+    lo = torch.empty_like(out)
+    lse = torch.empty(T, Hh, dtype=torch.float32, device=dev)
+    dq = torch.empty(T, Hh, Dqk, dtype=torch.bfloat16, device=dev)
+    dkv = torch.empty(T, Dqk, dtype=torch.float32, device=dev)
+    evs = []
+
+    def step(rec):
+        for _ in range(layers):  # IndexShare: every layer reuses the one selection
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)] if rec else None
+            if e: e[0].record(stream)
+            dsa.dsa_sparse_mla_fwd(x["q"], x["kv"], idx, scale, topk_len=ln, out=out, lse=lse, workspace=wf,
+                                   out_lo=lo, Dv=Dv)
+            if e: e[1].record(stream)
+            dsa.dsa_sparse_mla_bwd(x["q"], x["kv"], idx, scale, out, lse, x["dout"], topk_len=ln, dq=dq,
+                                   dkv_accum=dkv, workspace=wb, out_lo=lo)
+            if e: e[2].record(stream)
+            if e: evs.append(e)
+
+    for _ in range(args.warmup):
+        step(False)
+    for _ in range(args.steps):
+        step(True)
+    torch.cuda.synchronize(dev)
+    for w_ in (wf, wb):
+        if dsa.dsa_read_device_status(w_) != 0:
+            raise RuntimeError(f"device status after workload {name}")
+    n = int(ln.sum().item())
+    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
+    ff = 2.0 * Hh * n * (Dqk + Dv)
+    fb = 2.0 * Hh * n * (3 * Dqk + 2 * Dv)
+    tf = (ff + fb) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12
+    line = {"workload": name, "T": T, "H": Hh, "Dqk": Dqk, "K": Kw, "layers": layers, "n_valid_slots": n,
+            "mla_fwd_ms": round(fwd_ms, 3), "mla_bwd_ms": round(bwd_ms, 3), "mla_tflops": round(tf, 2),
+            "mla_pct_bf16_sustained": round(100 * tf / peak, 2) if peak else None,
+            "fwd_tflops": round(ff / (fwd_ms * 1e-3) / 1e12, 2), "bwd_tflops": round(fb / (bwd_ms * 1e-3) / 1e12, 2),
+            "timing": f"CUDA events, {args.warmup} warm-up and {args.steps} timed steps, median"}
+    if idx_ms is not None:
+        line.update({"indexer_ms": round(idx_ms, 3), "indexer_tokens_per_s": round(T / (idx_ms * 1e-3), 1)})
+    del x, out, lo, dq, dkv, idx, ln, wf, wb
+    torch.cuda.empty_cache()
+    return line
+
+
+def run_workloads(args, local):
+    """Each named workload of the pages' table on one GPU, one JSON line each (not the benchmark line)."""
+    import torch
+
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
-    peak = load_peaks().get("bf16_tflops_sustained")
     for name in args.workloads.split(","):
-        c = synth.WORKLOADS[name]
-        T, H, Dqk, Dv, Kw, scale = c["T"], c["H"], c["Dqk"], c["Dv"], c["K"], c["scale"]
-        layers = c.get("layers", 1)
-        g = synth.generator(0)
-        if "nseq" in c:
-            cu = synth.cu_seqlens_from_lengths(synth.thd_lengths(c["nseq"], c["lo"], c["hi"], T, g))
-        else:
-            cu = torch.tensor([0, T], dtype=torch.int32)
-        st, _, _, _ = dsa.dsa_packed_metadata(cu.to(dev), T)
-        idx_ms = None
-        if "Hi" in c:
-            ind = synth.indexer_inputs(T, c["Hi"], c["Di"], seed=0, device=dev)
-            run_idx = lambda: dsa.dsa_indexer_topk(ind["q_idx"], ind["k_idx"], ind["w"], st, Kw)
-            for _ in range(args.warmup):
-                idx, ln = run_idx()
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-            for a, b in ev:
-                a.record(stream)
-                idx, ln = run_idx()
-                b.record(stream)
-            torch.cuda.synchronize(dev)
-            idx_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
-            del ind
-        else:
-            idx = synth.random_causal_topk(st.cpu(), Kw, g).to(dev)
-            ln = (idx >= 0).sum(1).to(torch.int32)
-        x = synth.mla_inputs(T, H, Dqk, Dv, seed=1000, device=dev)
-        wf = torch.zeros(dsa.workspace_size("fwd", T, H), dtype=torch.uint8, device=dev)
-        wb = torch.zeros(dsa.workspace_size("bwd", T, H, Kw), dtype=torch.uint8, device=dev)
-        out = torch.empty(T, H, Dv, dtype=torch.bfloat16, device=dev)
-        lo = torch.empty_like(out)
-        lse = torch.empty(T, H, dtype=torch.float32, device=dev)
-        dq = torch.empty(T, H, Dqk, dtype=torch.bfloat16, device=dev)
-        dkv = torch.empty(T, Dqk, dtype=torch.float32, device=dev)
-        evs = []
+        print(json.dumps(time_workload(name, args, dev, stream)), flush=True)
 
-        def step(rec):
-            for _ in range(layers):  # IndexShare: every layer reuses the one selection
-                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)] if rec else None
-                if e: e[0].record(stream)
-                dsa.dsa_sparse_mla_fwd(x["q"], x["kv"], idx, scale, topk_len=ln, out=out, lse=lse, workspace=wf,
-                                       out_lo=lo, Dv=Dv)
-                if e: e[1].record(stream)
-                dsa.dsa_sparse_mla_bwd(x["q"], x["kv"], idx, scale, out, lse, x["dout"], topk_len=ln, dq=dq,
-                                       dkv_accum=dkv, workspace=wb, out_lo=lo)
-                if e: e[2].record(stream)
-                if e: evs.append(e)
 
-        for _ in range(args.warmup):
-            step(False)
-        for _ in range(args.steps):
-            step(True)
-        torch.cuda.synchronize(dev)
-        for w_ in (wf, wb):
-            if dsa.dsa_read_device_status(w_) != 0:
-                raise RuntimeError(f"device status after workload {name}")
-        n = int(ln.sum().item())
-        fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
-        bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
-        ff = 2.0 * H * n * (Dqk + Dv)
-        fb = 2.0 * H * n * (3 * Dqk + 2 * Dv)
-        tf = (ff + fb) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12
-        line = {"workload": name, "T": T, "H": H, "Dqk": Dqk, "K": Kw, "layers": layers, "n_valid_slots": n,
-                "mla_fwd_ms": round(fwd_ms, 3), "mla_bwd_ms": round(bwd_ms, 3), "mla_tflops": round(tf, 2),
-                "mla_pct_bf16_sustained": round(100 * tf / peak, 2) if peak else None,
-                "fwd_tflops": round(ff / (fwd_ms * 1e-3) / 1e12, 2), "bwd_tflops": round(fb / (bwd_ms * 1e-3) / 1e12, 2)}
-        if idx_ms is not None:
-            line.update({"indexer_ms": round(idx_ms, 3), "indexer_tokens_per_s": round(T / (idx_ms * 1e-3), 1)})
-        print(json.dumps(line), flush=True)
-        del x, out, lo, dq, dkv, idx, ln
-        torch.cuda.empty_cache()
+def traffic_per_launch(kernel: str, src_file: str, units: int):
+    """DRAM bytes of one launch from the committed ncu capture (profiles/traffic.json), scaled from the
+    captured launch by the units processed (valid slots, or tokens for the indexer); None when the
+    capture was taken on different kernel source."""
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tfile):
+        return None
+    with open(tfile) as f:
+        tr = json.load(f).get(kernel)
+    if not tr or tr.get("kernel_rev") != kernel_rev(src_file):
+        return None
+    per = tr.get("bytes_per_valid_slot", tr.get("bytes_per_token"))
+    return None if per is None else per * units
 
 
 def kernel_rev(src_name: str) -> str:
@@ -582,6 +626,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cp", action="store_true", help="skip the context-parallel indexer line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the V3.2 and NoPE workload timings")
     ap.add_argument("--workloads", default=None,
                     help="comma-separated workload names (tiny,v32,idx32k,nope,thd): one line per workload "
                          "instead of the benchmark line")

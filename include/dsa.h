@@ -52,7 +52,7 @@ typedef enum {
 const char* dsa_status_string(dsa_status_t status);
 /* Message of the calling thread's most recent failed call ("" if none). */
 const char* dsa_last_error_message(void);
-/* ABI version: 1. */
+/* ABI version: 2 (attention sink arguments of the sparse MLA calls). */
 int32_t dsa_abi_version(void);
 
 /*
@@ -184,13 +184,21 @@ dsa_status_t dsa_indexer_topk_with_scores(const dsa_bf16_t* q_idx, const dsa_bf1
  *   out[t,h,:] = sum_j exp(z_j - lse) * kv[idx_j, 0:Dv].
  * A row with no valid slot gets out = 0 and lse = -inf.  Indices >= T_k or
  * < -1 are masked and reported through the device error word.
+ * Attention sink ([cudnn_dsa] _pad_attention_heads pads a sink [H] with q;
+ * the pages print no formula; reading taken): attn_sink[h] is one more logit
+ * of every row of head h, in the units of z, with no value row:
+ *   lse[t,h] = ln(sum_j exp(z_j) + exp(attn_sink[h])),  out as above,
+ * so a row with no valid slot gets out = 0 and lse = attn_sink[h].  A sink of
+ * -inf is no sink; NaN or +inf sinks are outside the contract.
  *  q        device bf16 [T, H, Dqk], Dqk in {512, 576};  kv device bf16 [T_k, Dqk]
  *  topk_idx device int32 [T, K], any K >= 1;  topk_len device int32 [T] or NULL
+ *  attn_sink device fp32 [H] or NULL (no sink)
  *  out      device bf16 [T, H, Dv] (out), Dv = 512;  lse device fp32 [T, H] (out)
  *  out_lo   device bf16 [T, H, Dv] (out) or NULL: the rounding residual
- *           bf16(O - out) of the fp32 result O.  Passing it on to the backward
- *           makes D = <dout, O> use the unrounded O (library addition; the
- *           pages' interface returns out only).
+ *           bf16(O - out) of the fp32 result O (P.V runs on bf16 hi + lo parts
+ *           of P, so O is accurate to about fp32).  Passing it on to the
+ *           backward makes D = <dout, O> use that O instead of the rounded out
+ *           (library addition; the pages' interface returns out only).
  *  workspace >= dsa_sparse_mla_fwd_workspace_size() bytes
  * Query chunking ([Chunk-PR] "Summary"): rows are independent, so a chunk is a
  * call on row-offset pointers of q/topk_idx/out/lse with the full kv.
@@ -198,8 +206,9 @@ dsa_status_t dsa_indexer_topk_with_scores(const dsa_bf16_t* q_idx, const dsa_bf1
 size_t dsa_sparse_mla_fwd_workspace_size(int32_t T, int32_t H);
 dsa_status_t dsa_sparse_mla_fwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
                                 const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
-                                int32_t Dv, int32_t K, float softmax_scale, dsa_bf16_t* out, dsa_bf16_t* out_lo,
-                                float* lse, void* workspace, size_t workspace_bytes, dsa_stream_t stream);
+                                int32_t Dv, int32_t K, float softmax_scale, const float* attn_sink, dsa_bf16_t* out,
+                                dsa_bf16_t* out_lo, float* lse, void* workspace, size_t workspace_bytes,
+                                dsa_stream_t stream);
 
 /*
  * dsa_sparse_mla_bwd -- analytic backward of dsa_sparse_mla_fwd.
@@ -211,7 +220,9 @@ dsa_status_t dsa_sparse_mla_fwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const
  *   dq[t,h,:]         = softmax_scale * sum_j dS_j kv[idx_j, :]
  *   dkv_accum[idx_j,:] += softmax_scale * sum_h dS_j q[t,h,:]
  *   dkv_accum[idx_j,0:Dv] += sum_h P_j dout[t,h,:]
- *  q, kv, topk_idx, topk_len, sizes, softmax_scale: as in the forward call
+ * and with a sink, P_sink = exp(attn_sink[h] - lse[t,h]):
+ *   d_sink[h] += -sum_t P_sink[t,h] D[t,h]
+ *  q, kv, topk_idx, topk_len, sizes, softmax_scale, attn_sink: as in the forward call
  *  out, lse       device: the forward's outputs for these rows
  *  out_lo         device bf16 [T, H, Dv]: the forward's residual, or NULL (then D
  *                 is computed from the rounded out)
@@ -219,20 +230,26 @@ dsa_status_t dsa_sparse_mla_fwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const
  *  dq             device bf16 [T, H, Dqk] (out)
  *  dkv_accum      device fp32 [T_k, Dqk]: zeroed first when accumulate == 0,
  *                 added to when accumulate == 1 (query chunks)
+ *  d_sink         device fp32 [H] or NULL (needs attn_sink): zeroed first when
+ *                 accumulate == 0, added to when accumulate == 1
  *  dkv_bf16       device bf16 [T_k, Dqk] (out, rounded copy of dkv_accum) or NULL
  *  workspace      >= dsa_sparse_mla_bwd_workspace_size(T, H, K) bytes: the
- *                 error word, D (T*H fp32) and a per-SM scratch for the bf16
- *                 dS of one row's tiles (256 slots x ceil(K/128) x 16 KiB)
- * Summation order of dkv_accum across rows is not deterministic (fp32 atomics).
+ *                 error word, 256 scratch-slot flags, D (T*H fp32) and the
+ *                 scratch slots for the bf16 dS of one row's tiles (256 slots
+ *                 x ceil(K/128) x 16 KiB; a CTA claims a free slot and
+ *                 releases it on exit).  One workspace serves one call at a
+ *                 time: calls whose executions overlap must not share it.
+ * Summation order of dkv_accum (and d_sink) across rows is not deterministic
+ * (fp32 atomics).
  */
 size_t dsa_sparse_mla_bwd_workspace_size(int32_t T, int32_t H, int32_t K);
 dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
                                 const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
-                                int32_t Dv, int32_t K, float softmax_scale, const dsa_bf16_t* out,
-                                const dsa_bf16_t* out_lo, const float* lse, const dsa_bf16_t* dout, dsa_bf16_t* dq,
-                                float* dkv_accum,
-                                int32_t accumulate, dsa_bf16_t* dkv_bf16, void* workspace,
-                                size_t workspace_bytes, dsa_stream_t stream);
+                                int32_t Dv, int32_t K, float softmax_scale, const float* attn_sink,
+                                const dsa_bf16_t* out, const dsa_bf16_t* out_lo, const float* lse,
+                                const dsa_bf16_t* dout, dsa_bf16_t* dq, float* dkv_accum, float* d_sink,
+                                int32_t accumulate, dsa_bf16_t* dkv_bf16, void* workspace, size_t workspace_bytes,
+                                dsa_stream_t stream);
 
 /*
  * dsa_sparse_mla_bwd_noalloc -- dsa_sparse_mla_bwd without a caller workspace.
@@ -241,26 +258,49 @@ dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const
  * their own pool and forbid other allocations, or plug-ins whose host program
  * owns every allocation) and so cannot supply the workspace.  Arguments,
  * semantics and results are those of dsa_sparse_mla_bwd.
- *  - Scratch is a fixed 84 MiB + 256 B device array built into the library,
- *    held by every GPU that loads it until the process exits; T * H must not
- *    exceed dsa_sparse_mla_bwd_noalloc_max_rows() (4 Mi) and K must not
+ *  - Scratch is a fixed 84 MiB + 1280 B device array built into the library,
+ *    held by every GPU that loads it until the process exits; K must not
  *    exceed dsa_sparse_mla_bwd_noalloc_max_topk() (2176), else
- *    DSA_ERR_WORKSPACE is returned and nothing is launched.
- *  - The call allocates nothing.  The first call on a device looks up the
- *    array's device address (cudaGetSymbolAddress) with that device current;
- *    make that first call before any stream capture.
+ *    DSA_ERR_WORKSPACE is returned and nothing is launched.  Its D part holds
+ *    4 Mi (row, head) pairs: longer calls run in row chunks of
+ *    floor(4 Mi / H) rows, one after the other on `stream`, with dkv_accum
+ *    and d_sink accumulating over the chunks.
+ *  - The call allocates nothing.  The first call on a device (and again after
+ *    the device's context is replaced) looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
  *  - Every call uses the same array: calls whose executions overlap on the
  *    GPU race on it and must be ordered by the caller (same stream or events).
- *    Each call clears the error word and rewrites the D values it reads.
+ *    Each call clears the array's error word and slot flags; the device error
+ *    word is read with dsa_sparse_mla_bwd_noalloc_read_status.
  */
-size_t dsa_sparse_mla_bwd_noalloc_max_rows(void);
 int32_t dsa_sparse_mla_bwd_noalloc_max_topk(void);
 dsa_status_t dsa_sparse_mla_bwd_noalloc(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
                                         const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
-                                        int32_t Dv, int32_t K, float softmax_scale, const dsa_bf16_t* out,
-                                        const dsa_bf16_t* out_lo, const float* lse, const dsa_bf16_t* dout,
-                                        dsa_bf16_t* dq, float* dkv_accum, int32_t accumulate, dsa_bf16_t* dkv_bf16,
-                                        dsa_stream_t stream);
+                                        int32_t Dv, int32_t K, float softmax_scale, const float* attn_sink,
+                                        const dsa_bf16_t* out, const dsa_bf16_t* out_lo, const float* lse,
+                                        const dsa_bf16_t* dout, dsa_bf16_t* dq, float* dkv_accum, float* d_sink,
+                                        int32_t accumulate, dsa_bf16_t* dkv_bf16, dsa_stream_t stream);
+/*
+ * dsa_sparse_mla_bwd_noalloc_read_status -- the no-alloc backward's device
+ * error word: synchronise `stream`, read and clear the word in the built-in
+ * array and store it in *status_host (DSA_OK, DSA_ERR_DEVICE_INDEX or
+ * DSA_ERR_TIMEOUT), as dsa_read_device_status does for a workspace.  No
+ * counterpart on the pages (library addition).
+ */
+dsa_status_t dsa_sparse_mla_bwd_noalloc_read_status(dsa_stream_t stream, int32_t* status_host);
+
+/*
+ * dsa_set_wait_limit_cycles -- the cycle limit of every bounded device-side
+ * wait of the kernels launched after the call (process-wide; the default is
+ * 2^31 SM cycles, about one second).  A wait that runs past it records
+ * DSA_ERR_TIMEOUT in the device error word and its CTA leaves its work and
+ * exits cleanly; 0 gives up at the first wait whose phase has not completed,
+ * which lets a test drive every timeout path on purpose.  A negative value
+ * restores the default.  Returns the previous limit.  Library addition with
+ * no counterpart on the pages.
+ */
+int64_t dsa_set_wait_limit_cycles(int64_t cycles);
 
 /*
  * dsa_read_device_status -- synchronise `stream`, read and clear the device

@@ -30,7 +30,10 @@ __all__ = [
     "dsa_indexer_topk_with_scores",
     "dsa_sparse_mla_fwd",
     "dsa_sparse_mla_bwd",
+    "dsa_sparse_mla_bwd_noalloc",
+    "dsa_sparse_mla_bwd_noalloc_read_status",
     "dsa_read_device_status",
+    "dsa_set_wait_limit_cycles",
     "workspace_size",
 ]
 
@@ -98,19 +101,21 @@ def load_library(path: str | None = None):
                                                      _SZ, _P]
         lib.dsa_sparse_mla_fwd_workspace_size.argtypes = [_I, _I]
         lib.dsa_sparse_mla_fwd_workspace_size.restype = _SZ
-        lib.dsa_sparse_mla_fwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _SZ, _P]
+        lib.dsa_sparse_mla_fwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _SZ, _P]
         lib.dsa_sparse_mla_bwd_workspace_size.argtypes = [_I, _I, _I]
         lib.dsa_sparse_mla_bwd_workspace_size.restype = _SZ
-        lib.dsa_sparse_mla_bwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P,
-                                           _I, _P, _P, _SZ, _P]
+        lib.dsa_sparse_mla_bwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P,
+                                           _P, _I, _P, _P, _SZ, _P]
         lib.dsa_read_device_status.argtypes = [_P, _P, _P]
-        lib.dsa_sparse_mla_bwd_noalloc_max_rows.restype = _SZ
-        lib.dsa_sparse_mla_bwd_noalloc_max_rows.argtypes = []
+        lib.dsa_set_wait_limit_cycles.argtypes = [ctypes.c_int64]
+        lib.dsa_set_wait_limit_cycles.restype = ctypes.c_int64
         lib.dsa_sparse_mla_bwd_noalloc_max_topk.restype = _I
         lib.dsa_sparse_mla_bwd_noalloc_max_topk.argtypes = []
         lib.dsa_sparse_mla_bwd_noalloc.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P,
-                                                   _P, _I, _P, _P]
+                                                   _P, _P, _P, _I, _P, _P]
         lib.dsa_sparse_mla_bwd_noalloc.restype = ctypes.c_int
+        lib.dsa_sparse_mla_bwd_noalloc_read_status.argtypes = [_P, _P]
+        lib.dsa_sparse_mla_bwd_noalloc_read_status.restype = ctypes.c_int
         for name in ("dsa_packed_metadata", "dsa_indexer_topk", "dsa_indexer_topk_with_scores",
                      "dsa_sparse_mla_fwd", "dsa_sparse_mla_bwd", "dsa_read_device_status"):
             getattr(lib, name).restype = ctypes.c_int
@@ -287,10 +292,10 @@ def dsa_indexer_topk_with_scores(q_idx, k_idx, head_weights, seq_start, K: int, 
 
 
 def dsa_sparse_mla_fwd(q, kv, topk_idx, softmax_scale: float, topk_len=None, out=None, lse=None,
-                       workspace=None, Dv: int = 512, out_lo=None):
+                       workspace=None, Dv: int = 512, out_lo=None, attn_sink=None):
     """Sparse MLA forward -> (out bf16 [T,H,Dv], lse fp32 [T,H]), or (out, lse, out_lo) when
     out_lo is a tensor or True (the bf16 rounding residual of out, for an exact backward D).
-    kv may be [T_k, Dqk] or [T_k, 1, Dqk]."""
+    kv may be [T_k, Dqk] or [T_k, 1, Dqk]; attn_sink: fp32 [H] per-head sink logits or None."""
     lib = load_library()
     _need(q, "q", torch.bfloat16, 3)
     dev = q.device
@@ -304,6 +309,10 @@ def dsa_sparse_mla_fwd(q, kv, topk_idx, softmax_scale: float, topk_len=None, out
         _need(topk_len, "topk_len", torch.int32, 1, dev)
     T, H, Dqk = q.shape
     K = topk_idx.shape[1]
+    if attn_sink is not None:
+        _need(attn_sink, "attn_sink", torch.float32, 1, dev)
+        if attn_sink.numel() != H:
+            raise ValueError(f"attn_sink must have H = {H} entries")
     if out is None:
         out = torch.empty(T, H, Dv, dtype=torch.bfloat16, device=dev)
     if lse is None:
@@ -314,16 +323,19 @@ def dsa_sparse_mla_fwd(q, kv, topk_idx, softmax_scale: float, topk_len=None, out
     lo = out_lo if want_lo else None
     ws, wsb = _workspace("fwd", T, H, dev, workspace)
     _check(lib.dsa_sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(topk_idx), _ptr(topk_len), T, kv.shape[0], H, Dqk, Dv,
-                                  K, float(softmax_scale), _ptr(out), _ptr(lo), _ptr(lse), _ptr(ws), wsb,
-                                  _stream(dev)),
+                                  K, float(softmax_scale), _ptr(attn_sink), _ptr(out), _ptr(lo), _ptr(lse), _ptr(ws),
+                                  wsb, _stream(dev)),
            "dsa_sparse_mla_fwd")
     return (out, lse, lo) if want_lo else (out, lse)
 
 
 def dsa_sparse_mla_bwd(q, kv, topk_idx, softmax_scale: float, out, lse, dout, topk_len=None, dq=None,
-                       dkv_accum=None, accumulate: bool = False, dkv_bf16=None, workspace=None, out_lo=None):
-    """Sparse MLA backward -> (dq bf16 [T,H,Dqk], dkv_accum fp32 [T_k,Dqk], dkv_bf16 or None).
-    out_lo: the forward's residual (recommended; D then uses the unrounded output)."""
+                       dkv_accum=None, accumulate: bool = False, dkv_bf16=None, workspace=None, out_lo=None,
+                       attn_sink=None, d_sink=None):
+    """Sparse MLA backward -> (dq bf16 [T,H,Dqk], dkv_accum fp32 [T_k,Dqk], dkv_bf16 or None), and
+    d_sink fp32 [H] as a fourth result when attn_sink is given (d_sink: an existing tensor to fill,
+    or to add to with accumulate=True).
+    out_lo: the precise forward's residual (D then uses the fp32 output)."""
     lib = load_library()
     _need(q, "q", torch.bfloat16, 3)
     dev = q.device
@@ -351,13 +363,72 @@ def dsa_sparse_mla_bwd(q, kv, topk_idx, softmax_scale: float, out, lse, dout, to
             raise ValueError("accumulate=True needs an existing dkv_accum")
         dkv_accum = torch.empty(Tk, Dqk, dtype=torch.float32, device=dev)
     _need(dkv_accum, "dkv_accum", torch.float32, 2, dev)
+    if attn_sink is not None:
+        _need(attn_sink, "attn_sink", torch.float32, 1, dev)
+        if d_sink is None:
+            if accumulate:
+                raise ValueError("accumulate=True needs an existing d_sink")
+            d_sink = torch.empty(H, dtype=torch.float32, device=dev)
+        _need(d_sink, "d_sink", torch.float32, 1, dev)
     ws, wsb = _workspace("bwd", T, H, dev, workspace, K)
     _check(lib.dsa_sparse_mla_bwd(_ptr(q), _ptr(kv), _ptr(topk_idx), _ptr(topk_len), T, Tk, H, Dqk, Dv, K,
-                                  float(softmax_scale), _ptr(out), _ptr(out_lo), _ptr(lse), _ptr(dout), _ptr(dq),
-                                  _ptr(dkv_accum),
+                                  float(softmax_scale), _ptr(attn_sink), _ptr(out), _ptr(out_lo), _ptr(lse),
+                                  _ptr(dout), _ptr(dq), _ptr(dkv_accum), _ptr(d_sink),
                                   1 if accumulate else 0, _ptr(dkv_bf16), _ptr(ws), wsb, _stream(dev)),
            "dsa_sparse_mla_bwd")
+    return (dq, dkv_accum, dkv_bf16) if attn_sink is None else (dq, dkv_accum, dkv_bf16, d_sink)
+
+
+def dsa_sparse_mla_bwd_noalloc(q, kv, topk_idx, softmax_scale: float, out, lse, dout, topk_len=None, dq=None,
+                               dkv_accum=None, accumulate: bool = False, dkv_bf16=None, out_lo=None):
+    """dsa_sparse_mla_bwd with the library's built-in scratch instead of a workspace (for callers
+    that cannot allocate device memory; see include/dsa.h) -> (dq, dkv_accum, dkv_bf16).
+    Output tensors the caller does not pass are allocated here by torch, as in the other calls."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    if kv.dim() == 3:
+        kv = kv.reshape(kv.shape[0], kv.shape[2])
+    _need(kv, "kv", torch.bfloat16, 2, dev)
+    _need(topk_idx, "topk_idx", torch.int32, 2, dev)
+    _need(out, "out", torch.bfloat16, 3, dev)
+    _need(lse, "lse", torch.float32, 2, dev)
+    _need(dout, "dout", torch.bfloat16, 3, dev)
+    if topk_len is not None:
+        _need(topk_len, "topk_len", torch.int32, 1, dev)
+    if out_lo is not None:
+        _need(out_lo, "out_lo", torch.bfloat16, 3, dev)
+    T, H, Dqk = q.shape
+    Tk = kv.shape[0]
+    if dq is None:
+        dq = torch.empty(T, H, Dqk, dtype=torch.bfloat16, device=dev)
+    if dkv_accum is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs an existing dkv_accum")
+        dkv_accum = torch.empty(Tk, Dqk, dtype=torch.float32, device=dev)
+    _need(dkv_accum, "dkv_accum", torch.float32, 2, dev)
+    _check(lib.dsa_sparse_mla_bwd_noalloc(_ptr(q), _ptr(kv), _ptr(topk_idx), _ptr(topk_len), T, Tk, H, Dqk,
+                                          out.shape[2], topk_idx.shape[1], float(softmax_scale), None, _ptr(out),
+                                          _ptr(out_lo), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dkv_accum), None,
+                                          1 if accumulate else 0, _ptr(dkv_bf16), _stream(dev)),
+           "dsa_sparse_mla_bwd_noalloc")
     return dq, dkv_accum, dkv_bf16
+
+
+def dsa_sparse_mla_bwd_noalloc_read_status(device=None) -> int:
+    """Synchronise the current stream, read and clear the no-alloc backward's device error word."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    st = ctypes.c_int32(0)
+    _check(lib.dsa_sparse_mla_bwd_noalloc_read_status(_stream(dev), ctypes.byref(st)),
+           "dsa_sparse_mla_bwd_noalloc_read_status")
+    return st.value
+
+
+def dsa_set_wait_limit_cycles(cycles: int) -> int:
+    """Cycle limit of the kernels' bounded waits for later launches (negative: the default, 2^31);
+    returns the previous limit."""
+    return int(load_library().dsa_set_wait_limit_cycles(int(cycles)))
 
 
 def dsa_read_device_status(workspace: torch.Tensor) -> int:

@@ -1,6 +1,7 @@
 // dsa_api.cu -- status reporting, device checks, tensor maps, workspace sizes,
 // the device error word, and dsa_packed_metadata.
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -8,6 +9,7 @@
 #include <vector>
 
 #include "dsa_host.h"
+#include "dsa_once.h"
 
 namespace dsa {
 
@@ -101,6 +103,21 @@ dsa_status_t clear_error_word(void* ws, cudaStream_t stream) {
   return cuda_check(cudaMemsetAsync(ws, 0, sizeof(int), stream), "clearing the device error word");
 }
 
+static std::atomic<long long> g_wait_limit{1ll << 31};
+long long wait_limit_cycles() { return g_wait_limit.load(std::memory_order_relaxed); }
+
+dsa_status_t configure_kernel_smem(const void* func, int bytes, const char* what) {
+  static PerDeviceOnce table;
+  int dev = 0;
+  dsa_status_t st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != DSA_OK) return st;
+  table.run(func, dev, [&] {
+    st = cuda_check(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes), what);
+    return st == DSA_OK;
+  });
+  return st;
+}
+
 // ---------------------------------------------------------------------------
 // THD metadata: per token, start of its sequence and causal length.
 // ---------------------------------------------------------------------------
@@ -165,7 +182,11 @@ const char* dsa_status_string(dsa_status_t s) {
 
 const char* dsa_last_error_message(void) { return g_msg; }
 
-int32_t dsa_abi_version(void) { return 1; }
+int32_t dsa_abi_version(void) { return 2; }
+
+int64_t dsa_set_wait_limit_cycles(int64_t cycles) {
+  return g_wait_limit.exchange(cycles < 0 ? (1ll << 31) : cycles);
+}
 
 dsa_status_t dsa_read_device_status(void* workspace, dsa_stream_t stream, int32_t* status_host) {
   if (!workspace || !status_host) return fail(DSA_ERR_INVALID_ARGUMENT, "dsa_read_device_status: null pointer");

@@ -16,9 +16,13 @@
 // with L2 reductions (red.global.add), one 2304-byte row per selected key and
 // token; those reductions bound the kernel, so everything else is arranged
 // to keep them running back to back:
-//  * P is recomputed from the saved lse (no running max).  D comes from a
-//    small kernel; when the forward's bf16 residual of O is given, D uses the
-//    unrounded O, so that sum_j dS_j = 0 holds to fp32 accuracy.
+//  * P is recomputed from the saved lse (no running max; an attention sink of
+//    the forward is inside lse, so P needs nothing more).  D = <dO, O> comes
+//    from a small kernel that streams O and dO at full memory bandwidth
+//    before the main kernel starts (every CTA then finds D ready); when the
+//    forward's bf16 residual of O is given, D uses O + residual, so that
+//    sum_j dS_j = 0 holds to fp32 accuracy.  With a sink, the same kernel
+//    adds the sink gradient -exp(sink - lse) D of each (token, head) to d_sink.
 //  * Main loop, per 128-slot tile: [S^T | dP^T] = KV [Q | dO]^T (keys on the
 //    MMA M axis; Q and dO chunks side by side give N = 128) into one of TWO
 //    TMEM buffers; the softmax backward turns them, in place, into dS (x
@@ -33,9 +37,12 @@
 //    run while the reductions of this tile are still in flight.
 //  * dq needs dS for every tile of the token but the main loop has no TMEM
 //    left for its accumulator, so dS hi of each tile is also written to a
-//    per-SM scratch in global memory (L2-resident) and dQ^T = KV^T dS^T is
+//    scratch slot in global memory (L2-resident) and dQ^T = KV^T dS^T is
 //    formed in an end phase per token, when Q and dO are dead and their
-//    shared memory becomes a deep gather ring.
+//    shared memory becomes a deep gather ring.  A CTA claims its scratch slot
+//    from a table of slot flags in the workspace (compare-and-swap, starting
+//    at the SM id as a hint) and frees it when it exits, so two CTAs never
+//    share a slot whatever SMs they run on.
 //  * The gathered rows stream through shared memory in 64-channel chunks
 //    (128-byte swizzle) loaded by 16-byte cp.async (zero-fill for invalid or
 //    beyond-prefix rows).
@@ -66,7 +73,8 @@ constexpr int kGroup = 128;    // dKV channels per staging slot (MMA N)
 constexpr int kRing = 4;       // main-loop ring: 16 KiB chunk slots
 constexpr int kERing = 6;      // end-phase ring: 32 KiB slots (a dS tile or a 128-channel pair)
 constexpr int kStage = 2;      // dKV staging slots
-constexpr int kMaxSmSlots = 256;                  // dS scratch slots, indexed by SM id
+constexpr int kMaxSlots = 256;                    // dS scratch slots (more than the resident CTAs)
+constexpr long long kHintRetryCycles = 8192;      // retries of the SM's own slot before scanning
 constexpr int kDsTileBytes = kTile * kHeads * 2;  // bf16 dS of one tile: 16 KiB
 constexpr int kUnits = kTile * 8;                 // 16-byte units of one 64-channel chunk
 
@@ -98,7 +106,7 @@ struct Smem {
 // misc layout: mbarriers (8 bytes each), then scalars and per-head vectors
 constexpr int B_FULL = 0, B_EMPTY = 5, B_EFULL = 10, B_EEMPTY = 16, B_SDP = 22, B_DS = 24, B_KVD = 26, B_STF = 28,
               B_STE = 32, B_DSDONE = 36, B_ENDGO = 37, B_DQ = 38, B_FIN = 39, B_COUNT = 40;
-constexpr int M_TMEM = 384, M_NEFF = 388, M_ABORT = 392;
+constexpr int M_TMEM = 384, M_NEFF = 388, M_ABORT = 392, M_SLOT = 396;
 constexpr int M_LSE = 512, M_DL = 768;  // float [64] each
 static_assert(B_COUNT * 8 <= M_TMEM, "barriers fit");
 
@@ -107,9 +115,12 @@ static_assert(B_COUNT * 8 <= M_TMEM, "barriers fit");
 constexpr uint32_t C_BUF = 128, C_STG = 256;
 static_assert(C_STG + kStage * kGroup <= 512, "TMEM budget");
 
-// D[t,h] = <dO[t,h,:], O[t,h,:] (+ O_lo[t,h,:])> in fp32; one warp per (t, h).
+// D[t,h] = <dO[t,h,:], O[t,h,:] (+ O_lo[t,h,:])> in fp32; one warp per (t, h).  With a sink,
+// d_sink[h] += -exp(sink[h] - lse[t,h]) D[t,h] (nothing for an empty row, lse = -inf).
 __global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ out_lo,
-                                 const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta, long long rows) {
+                                 const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta, long long rows,
+                                 const float* __restrict__ lse, const float* __restrict__ sink,
+                                 float* __restrict__ d_sink, int H) {
   const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (w >= rows) return;
@@ -133,7 +144,14 @@ __global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ out, const __
   }
 #pragma unroll
   for (int o2 = 16; o2 >= 1; o2 >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o2);
-  if (lane == 0) delta[w] = acc;
+  if (lane == 0) {
+    delta[w] = acc;
+    if (d_sink != nullptr) {
+      const int h = (int)(w % H);
+      const float l = __ldg(lse + w), sk = __ldg(sink + h);
+      if (sk > -INFINITY && l > -INFINITY) atomicAdd(d_sink + h, -expf(sk - l) * acc);
+    }
+  }
 }
 
 __global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, long long n4) {
@@ -233,8 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ topk_len,
                           const float* __restrict__ lse, const float* __restrict__ delta,
                           const __nv_bfloat16* __restrict__ dout, int T, int Tk, int H, int K, float scale,
-                          __nv_bfloat16* __restrict__ dq, float* __restrict__ dkv, uint8_t* __restrict__ ds_scratch,
-                          int tiles_per_slot, int* __restrict__ err) {
+                          __nv_bfloat16* __restrict__ dq, float* __restrict__ dkv,
+                          int* __restrict__ slot_flags, uint8_t* __restrict__ ds_scratch, int tiles_per_slot,
+                          int* __restrict__ err, long long wait_limit) {
   using L = Smem<DQK>;
   constexpr int NCH = L::NCH;
   constexpr int NP = L::NP;
@@ -250,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + M_TMEM);
   int* s_neff = reinterpret_cast<int*>(misc + M_NEFF);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + M_ABORT);
+  int* s_slot = reinterpret_cast<int*>(misc + M_SLOT);
   float* s_lse2 = reinterpret_cast<float*>(misc + M_LSE);
   float* s_dl = reinterpret_cast<float*>(misc + M_DL);
 
@@ -288,6 +308,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(s_tmem), 512);
     tmem_relinquish();
   }
+  if (threadIdx.x == 32) {
+    // claim a free dS scratch slot by compare-and-swap over the slot flags.  The SM id is a hint
+    // (slots are owned by CTAs, not SMs): the CTA that ran here before frees that slot as it
+    // exits, and its release may still be on its way to L2, so the hint is retried for a short
+    // while before the other slots are scanned; reusing it keeps the scratch footprint at one
+    // slot per SM in L2.  Gives up (DSA_ERR_TIMEOUT) after the wait limit.
+    const int hint = (int)(sm_id() % (uint32_t)kMaxSlots);
+    int slot = -1;
+    const long long c0 = clock64();
+    while (slot < 0 && clock64() - c0 < kHintRetryCycles)
+      if (atomicCAS(slot_flags + hint, 0, 1) == 0) slot = hint;
+    for (int k = 1; slot < 0; ++k) {
+      const int sl = (hint + k) % kMaxSlots;
+      if (atomicCAS(slot_flags + sl, 0, 1) == 0) {
+        slot = sl;
+      } else if (k >= kMaxSlots && clock64() - c0 > wait_limit) {
+        record_error(err, DSA_ERR_TIMEOUT);
+        break;
+      }
+    }
+    __threadfence();  // the previous owner's scratch accesses precede this CTA's
+    *s_slot = slot;
+  }
   __syncthreads();
 
   const bool is_gather = warp >= 1 && warp < 4;
@@ -307,19 +350,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (last) atomicMax(s_neff, last);
     }
     // Q [64 x DQK] and dO [64 x 512] -> 128B-swizzled chunks (rows = heads); heads >= H are zero.
+    // Read once per CTA: evicted from L2 first (the scratch, dkv and kv rows stay)
+    const uint64_t pol = l2_evict_first_policy();
     for (int u = tid; u < kHeads * NCH * 8; u += kMath) {
       const int hh = u / (NCH * 8), rem = u - hh * (NCH * 8), c = rem >> 3, uc = rem & 7;
       const int h = hg * kHeads + hh;
       const bool ok = h < H;  // padded heads are zero-filled without a read
-      cp_async16(sQDO + c * L::QDO + sw128_off(hh, uc), q + (ok ? ((size_t)t * H + h) * DQK + c * 64 + uc * 8 : 0),
-                 ok ? 16u : 0u);
+      cp_async16_hint(sQDO + c * L::QDO + sw128_off(hh, uc),
+                      q + (ok ? ((size_t)t * H + h) * DQK + c * 64 + uc * 8 : 0), ok ? 16u : 0u, pol);
     }
     for (int u = tid; u < kHeads * 8 * 8; u += kMath) {
       const int hh = u >> 6, rem = u & 63, c = rem >> 3, uc = rem & 7;
       const int h = hg * kHeads + hh;
       const bool ok = h < H;
-      cp_async16(sQDO + c * L::QDO + L::Q_CHUNK + sw128_off(hh, uc),
-                 dout + (ok ? ((size_t)t * H + h) * kDv + c * 64 + uc * 8 : 0), ok ? 16u : 0u);
+      cp_async16_hint(sQDO + c * L::QDO + L::Q_CHUNK + sw128_off(hh, uc),
+                      dout + (ok ? ((size_t)t * H + h) * kDv + c * 64 + uc * 8 : 0), ok ? 16u : 0u, pol);
     }
     // per-head lse (log2 units) and D, shared by every key row
     if (tid < kHeads) {
@@ -334,24 +379,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   int ntiles = (*s_neff + kTile - 1) / kTile;
   const int n_eff = *s_neff;
   const uint32_t tmem = *s_tmem;
-  // this SM's dS scratch (one CTA per SM at a time: the shared-memory footprint admits no second)
-  const uint32_t smid = sm_id();
-  if (smid >= (uint32_t)kMaxSmSlots || ntiles > tiles_per_slot) {
-    if (threadIdx.x == 0) record_error(err, DSA_ERR_UNSUPPORTED);
+  // this CTA's dS scratch slot (none: the claim timed out, and the CTA computes nothing)
+  const int slot = *s_slot;
+  if (slot < 0 || ntiles > tiles_per_slot) {
+    if (threadIdx.x == 0 && slot >= 0) record_error(err, DSA_ERR_UNSUPPORTED);
     ntiles = 0;
   }
-  uint8_t* ds_slot = ds_scratch + (size_t)smid * tiles_per_slot * kDsTileBytes;
+  uint8_t* ds_slot = ds_scratch + (size_t)(slot < 0 ? 0 : slot) * tiles_per_slot * kDsTileBytes;
 
   // End-phase gathers, shared by the gather and the math warps (et = 0..351):
   // per tile the swizzled dS image from the scratch, then the channel pairs.
   auto end_gathers = [&](int et) {
     constexpr int NT = kGather + kMath;
-    if (!mbar_wait(bar(B_ENDGO), 0, s_abort, err) || !mbar_wait(bar(B_DSDONE), 0, s_abort, err)) return;
+    if (!mbar_wait(bar(B_ENDGO), 0, s_abort, err, wait_limit) || !mbar_wait(bar(B_DSDONE), 0, s_abort, err, wait_limit)) return;
     TileGather<DQK, NT> tg;
     int Le = 0;
     for (int i = 0; i < ntiles; ++i) {
       int slot = Le % kERing;
-      if (Le >= kERing && !mbar_wait(bar(B_EEMPTY + slot), ((Le / kERing) - 1) & 1, s_abort, err)) return;
+      if (Le >= kERing && !mbar_wait(bar(B_EEMPTY + slot), ((Le / kERing) - 1) & 1, s_abort, err, wait_limit)) return;
       const uint8_t* src = ds_slot + (size_t)i * kDsTileBytes;
       for (int u = et; u < kDsTileBytes / 16; u += NT) cp_async16(sERing + slot * L::ESLOT + 16 * u, src + 16 * u, 16u);
       cp_async_arrive(bar(B_EFULL + slot));
@@ -359,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tg.rows(kv, idx_row, i, n_eff, Tk, et, err);
       for (int p = 0; p < NP; ++p, ++Le) {
         slot = Le % kERing;
-        if (Le >= kERing && !mbar_wait(bar(B_EEMPTY + slot), ((Le / kERing) - 1) & 1, s_abort, err)) return;
+        if (Le >= kERing && !mbar_wait(bar(B_EEMPTY + slot), ((Le / kERing) - 1) & 1, s_abort, err, wait_limit)) return;
         tg.chunk(sERing + slot * L::ESLOT, 2 * p, et);
         if (2 * p + 1 < NCH) tg.chunk(sERing + slot * L::ESLOT + L::KV_CHUNK, 2 * p + 1, et);
         cp_async_arrive(bar(B_EFULL + slot));
@@ -372,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // half this warp owns if any, release the slot, then reduce it into dkv.
   auto drain_group = [&](int G, int g, int role, int ix, uint32_t fst) -> bool {
     const int s = G & (kStage - 1);
-    if (!mbar_wait(bar(B_STF + s), (G / kStage) & 1, s_abort, err)) return false;
+    if (!mbar_wait(bar(B_STF + s), (G / kStage) & 1, s_abort, err, wait_limit)) return false;
     const int halves = (g * kGroup + kGroup <= DQK) ? 2 : 1;
     int mine = -1;  // the half this warp owns, if any (drain_role gives a warp at most one per group)
     for (int hf = 0; hf < halves; ++hf)
@@ -489,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (*s_abort) {
           stop = true;
           break;
-        } else if (clock64() - idle_t0 > kWaitLimitCycles) {
+        } else if (clock64() - idle_t0 > wait_limit) {
           *s_abort = 1;
           record_error(err, DSA_ERR_TIMEOUT);
           stop = true;
@@ -499,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- end phase: dQ^T[pair p] += KV^T dS^T over every tile of the token ----
       if (!stop && ntiles > 0) {
         // every dKV MMA has landed: Q, dO, the main ring and the S/dP buffers are dead
-        stop = !mbar_wait(bar(B_KVD + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, s_abort, err);
+        stop = !mbar_wait(bar(B_KVD + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, s_abort, err, wait_limit);
         if (!stop) mbar_arrive(bar(B_ENDGO));
         // the rope tile of dQ^T overlaps staging slot 0: wait for its last drain
         bool rope_free = (NP * 64 <= (int)C_STG);
@@ -507,14 +552,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         int Le = 0;
         for (int i = 0; i < ntiles && !stop; ++i) {
           const int sds = Le % kERing;
-          if (!mbar_wait(bar(B_EFULL + sds), (Le / kERing) & 1, s_abort, err)) { stop = true; break; }
+          if (!mbar_wait(bar(B_EFULL + sds), (Le / kERing) & 1, s_abort, err, wait_limit)) { stop = true; break; }
           const uint32_t dsb = sERing + sds * L::ESLOT;
           ++Le;
           for (int p = 0; p < NP; ++p, ++Le) {
             const int sl = Le % kERing;
-            if (!mbar_wait(bar(B_EFULL + sl), (Le / kERing) & 1, s_abort, err)) { stop = true; break; }
+            if (!mbar_wait(bar(B_EFULL + sl), (Le / kERing) & 1, s_abort, err, wait_limit)) { stop = true; break; }
             if (p * 64 + 64 > (int)C_STG && !rope_free) {
-              if (uses0 > 0 && !mbar_wait(bar(B_STE), (uses0 - 1) & 1, s_abort, err)) { stop = true; break; }
+              if (uses0 > 0 && !mbar_wait(bar(B_STE), (uses0 - 1) & 1, s_abort, err, wait_limit)) { stop = true; break; }
               rope_free = true;
             }
             fence_proxy_async_smem();
@@ -548,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tg.rows(kv, idx_row, i, n_eff, Tk, gt, err);
       for (int c = 0; c < NCH; ++c, ++La) {
         const int slot = La % kRing;
-        if (La >= kRing && !mbar_wait(bar(B_EMPTY + slot), ((La / kRing) - 1) & 1, s_abort, err)) {
+        if (La >= kRing && !mbar_wait(bar(B_EMPTY + slot), ((La / kRing) - 1) & 1, s_abort, err, wait_limit)) {
           aborted = true;
           break;
         }
@@ -591,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this key row's index does not depend on the MMA: its load overlaps the wait
       const int j = i * kTile + r;
       const int ix = (j < n_eff) ? __ldg(idx_row + j) : -1;
-      if (!mbar_wait(bar(B_SDP + b), (i >> 1) & 1, s_abort, err)) { aborted = true; break; }
+      if (!mbar_wait(bar(B_SDP + b), (i >> 1) & 1, s_abort, err, wait_limit)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t tS = tmem_addr(tmem + C_BUF * b + ch * 32, qd * 32, 0);
       const uint32_t tP = tS + 64;
@@ -648,12 +693,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("cp.async.wait_all;" ::: "memory");
     // ---- dq epilogue: dQ^T (lanes = channels) -> staged [64 heads][DQK] bf16 -> coalesced stores ----
     const int bar_id = 1 + ch;
-    bool have = false;
-    if (!aborted && ntiles > 0) {
-      const bool got = mbar_wait(bar(B_DQ), 0, s_abort, err);
-      have = !named_bar_or(bar_id, 128, !got);
-      tc_fence_after();
-    }
+    // every thread of the half joins the barrier, whether or not its warp left the loop early
+    // (`aborted` is per warp here: the drains fail warp by warp)
+    bool ok = !aborted && ntiles > 0;
+    if (ok) ok = mbar_wait(bar(B_DQ), 0, s_abort, err, wait_limit);
+    const bool have = !named_bar_or(bar_id, 128, !ok);
+    if (have) tc_fence_after();
     named_bar(3, kMath);  // both halves have left the loop before the staging area is written
     __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + L::OFF_ERING);
 #pragma unroll 1
@@ -675,8 +720,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar(3, kMath);
     const int hcount = min(kHeads, H - hg * kHeads);
     uint4* dst = reinterpret_cast<uint4*>(dq + ((size_t)t * H + hg * kHeads) * DQK);
+    const uint64_t pol = l2_evict_first_policy();  // dq is written once
     for (int u = threadIdx.x - 128; u < hcount * (DQK / 8); u += kMath)
-      dst[u] = reinterpret_cast<const uint4*>(stage)[u];
+      stg16_hint(dst + u, reinterpret_cast<const uint4*>(stage)[u], pol);
   }
 
   tc_fence_before();
@@ -685,27 +731,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (threadIdx.x == 32) {
+    const int held = *s_slot;
+    if (held >= 0) {
+      __threadfence();  // every access of this CTA to the slot precedes its release
+      atomicExch(slot_flags + held, 0);
+    }
+  }
 }
 
 template <int DQK>
 dsa_status_t launch(const void* kv, const void* q, const int32_t* idx, const int32_t* len, const float* lse,
                     const float* delta, const void* dout, int T, int Tk, int H, int K, float scale, void* dq,
-                    float* dkv, uint8_t* ds_scratch, int* err, cudaStream_t s) {
+                    float* dkv, int* slot_flags, uint8_t* ds_scratch, int* err, cudaStream_t s) {
   using L = Smem<DQK>;
-  static bool configured = false;
-  if (!configured) {
-    dsa_status_t st = cuda_check(cudaFuncSetAttribute(sparse_mla_bwd_kernel<DQK>,
-                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL),
-                                 "configuring sparse_mla_bwd_kernel");
-    if (st != DSA_OK) return st;
-    configured = true;
-  }
+  dsa_status_t st = configure_kernel_smem(reinterpret_cast<const void*>(sparse_mla_bwd_kernel<DQK>), L::TOTAL,
+                                          "configuring sparse_mla_bwd_kernel");
+  if (st != DSA_OK) return st;
   dim3 grid(T, (H + kHeads - 1) / kHeads);
   sparse_mla_bwd_kernel<DQK><<<grid, kThreads, L::TOTAL, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(kv), reinterpret_cast<const __nv_bfloat16*>(q), idx, len, lse, delta,
       reinterpret_cast<const __nv_bfloat16*>(dout), T, Tk, H, K, scale, reinterpret_cast<__nv_bfloat16*>(dq), dkv,
-      ds_scratch, (K + kTile - 1) / kTile, err);
+      slot_flags, ds_scratch, (K + kTile - 1) / kTile, err, wait_limit_cycles());
   return cuda_check(cudaGetLastError(), "launching sparse_mla_bwd_kernel");
+}
+
+// Workspace layout: [error word, 256 B][slot flags: kMaxSlots int32][D: T*H fp32]
+//                   [dS scratch: kMaxSlots x ceil(K/128) x 16 KiB]
+constexpr size_t kFlagBytes = kMaxSlots * sizeof(int);
+constexpr size_t kHeadBytes = kErrorWordBytes + kFlagBytes;  // cleared at every call
+static size_t delta_bytes(int32_t T, int32_t H) {
+  const size_t d = (size_t)(T > 0 ? T : 0) * (size_t)(H > 0 ? H : 0) * sizeof(float);
+  return (d + 255) & ~size_t(255);
+}
+static size_t scratch_bytes(int32_t K) {
+  const size_t tiles = (size_t)((K > 0 ? K : 1) + kTile - 1) / kTile;
+  return (size_t)kMaxSlots * tiles * kDsTileBytes;
 }
 
 }  // namespace bwd
@@ -713,31 +774,21 @@ dsa_status_t launch(const void* kv, const void* q, const int32_t* idx, const int
 
 using namespace dsa;
 
+extern "C" size_t dsa_sparse_mla_bwd_workspace_size(int32_t T, int32_t H, int32_t K) {
+  return bwd::kHeadBytes + bwd::delta_bytes(T, H) + bwd::scratch_bytes(K);
+}
+
 namespace dsa {
 namespace bwd {
-// Workspace layout: [error word][D: T*H fp32][dS scratch: kMaxSmSlots x ceil(K/128) x 16 KiB]
-static size_t delta_bytes(int32_t T, int32_t H) {
-  const size_t d = (size_t)(T > 0 ? T : 0) * (size_t)(H > 0 ? H : 0) * sizeof(float);
-  return (d + 255) & ~size_t(255);
-}
-static size_t scratch_bytes(int32_t K) {
-  const size_t tiles = (size_t)((K > 0 ? K : 1) + kTile - 1) / kTile;
-  return (size_t)kMaxSmSlots * tiles * kDsTileBytes;
-}
-}  // namespace bwd
-}  // namespace dsa
-
-extern "C" size_t dsa_sparse_mla_bwd_workspace_size(int32_t T, int32_t H, int32_t K) {
-  return kErrorWordBytes + bwd::delta_bytes(T, H) + bwd::scratch_bytes(K);
-}
-
-extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
-                                           const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
-                                           int32_t Dv, int32_t K, float softmax_scale, const dsa_bf16_t* out,
-                                           const dsa_bf16_t* out_lo, const float* lse, const dsa_bf16_t* dout,
-                                           dsa_bf16_t* dq, float* dkv_accum, int32_t accumulate, dsa_bf16_t* dkv_bf16,
-                                           void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
-  const char* who = "dsa_sparse_mla_bwd";
+// The backward proper, on a scratch region of `workspace_bytes` bytes laid out as above.  A call
+// split into row chunks passes first = false after its first chunk (the device error word keeps
+// what earlier chunks recorded) and last = false before its last one (dkv is rounded to bf16 once).
+static dsa_status_t run(const char* who, const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
+                        const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk, int32_t Dv,
+                        int32_t K, float softmax_scale, const float* attn_sink, const dsa_bf16_t* out,
+                        const dsa_bf16_t* out_lo, const float* lse, const dsa_bf16_t* dout, dsa_bf16_t* dq,
+                        float* dkv_accum, float* d_sink, int32_t accumulate, dsa_bf16_t* dkv_bf16, void* workspace,
+                        size_t workspace_bytes, dsa_stream_t stream, bool first = true, bool last = true) {
   if (T < 0 || T_k < 1 || H < 1 || K < 1)
     return fail(DSA_ERR_INVALID_ARGUMENT, "%s: need T >= 0, T_k >= 1, H >= 1, K >= 1 (got %d, %d, %d, %d)", who, T,
                 T_k, H, K);
@@ -756,35 +807,58 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t
                 who);
   if (dkv_bf16 && (reinterpret_cast<uintptr_t>(dkv_bf16) & 7u))
     return fail(DSA_ERR_INVALID_ARGUMENT, "%s: dkv_bf16 must be 8-byte aligned", who);
-  dsa_status_t st = check_workspace(workspace, workspace_bytes, dsa_sparse_mla_bwd_workspace_size(T, H, K), who);
+  if (d_sink && !attn_sink) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: d_sink needs attn_sink", who);
+  dsa_status_t st = check_workspace(workspace, workspace_bytes, kHeadBytes + delta_bytes(T, H) + scratch_bytes(K), who);
   if (st != DSA_OK) return st;
   if ((st = check_device()) != DSA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = clear_error_word(workspace, s)) != DSA_OK) return st;
+  // the error word (on a call's first chunk) and every slot flag start at zero
+  uint8_t* clear_from = reinterpret_cast<uint8_t*>(workspace) + (first ? 0 : kErrorWordBytes);
+  if ((st = cuda_check(cudaMemsetAsync(clear_from, 0, first ? kHeadBytes : kFlagBytes, s),
+                       "clearing the error word and slot flags")))
+    return st;
   if (!accumulate &&
       (st = cuda_check(cudaMemsetAsync(dkv_accum, 0, (size_t)T_k * Dqk * sizeof(float), s), "zeroing dkv_accum")))
     return st;
+  if (!accumulate && d_sink &&
+      (st = cuda_check(cudaMemsetAsync(d_sink, 0, (size_t)H * sizeof(float), s), "zeroing d_sink")))
+    return st;
   int* err = reinterpret_cast<int*>(workspace);
-  float* delta = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + kErrorWordBytes);
-  uint8_t* ds_scratch = reinterpret_cast<uint8_t*>(workspace) + kErrorWordBytes + bwd::delta_bytes(T, H);
+  int* flags = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(workspace) + kErrorWordBytes);
+  float* delta = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + kHeadBytes);
+  uint8_t* ds_scratch = reinterpret_cast<uint8_t*>(workspace) + kHeadBytes + delta_bytes(T, H);
   if (T > 0) {
     const long long rows = (long long)T * H;
-    bwd::bwd_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+    bwd_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
         reinterpret_cast<const __nv_bfloat16*>(out), reinterpret_cast<const __nv_bfloat16*>(out_lo),
-        reinterpret_cast<const __nv_bfloat16*>(dout), delta, rows);
+        reinterpret_cast<const __nv_bfloat16*>(dout), delta, rows, lse, attn_sink, d_sink, H);
     if ((st = cuda_check(cudaGetLastError(), "launching bwd_delta_kernel"))) return st;
-    st = (Dqk == 576) ? bwd::launch<576>(kv, q, topk_idx, topk_len, lse, delta, dout, T, T_k, H, K, softmax_scale, dq,
-                                         dkv_accum, ds_scratch, err, s)
-                      : bwd::launch<512>(kv, q, topk_idx, topk_len, lse, delta, dout, T, T_k, H, K, softmax_scale, dq,
-                                         dkv_accum, ds_scratch, err, s);
+    st = (Dqk == 576) ? launch<576>(kv, q, topk_idx, topk_len, lse, delta, dout, T, T_k, H, K, softmax_scale, dq,
+                                    dkv_accum, flags, ds_scratch, err, s)
+                      : launch<512>(kv, q, topk_idx, topk_len, lse, delta, dout, T, T_k, H, K, softmax_scale, dq,
+                                    dkv_accum, flags, ds_scratch, err, s);
     if (st != DSA_OK) return st;
   }
-  if (dkv_bf16) {
+  if (dkv_bf16 && last) {
     const long long n4 = (long long)T_k * Dqk / 4;
-    bwd::f32_to_bf16_kernel<<<152 * 4, 256, 0, s>>>(dkv_accum, reinterpret_cast<__nv_bfloat16*>(dkv_bf16), n4);
+    f32_to_bf16_kernel<<<152 * 4, 256, 0, s>>>(dkv_accum, reinterpret_cast<__nv_bfloat16*>(dkv_bf16), n4);
     if ((st = cuda_check(cudaGetLastError(), "launching f32_to_bf16_kernel"))) return st;
   }
   return ok();
+}
+}  // namespace bwd
+}  // namespace dsa
+
+extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
+                                           const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
+                                           int32_t Dv, int32_t K, float softmax_scale, const float* attn_sink,
+                                           const dsa_bf16_t* out, const dsa_bf16_t* out_lo, const float* lse,
+                                           const dsa_bf16_t* dout, dsa_bf16_t* dq, float* dkv_accum, float* d_sink,
+                                           int32_t accumulate, dsa_bf16_t* dkv_bf16, void* workspace,
+                                           size_t workspace_bytes, dsa_stream_t stream) {
+  return bwd::run("dsa_sparse_mla_bwd", q, kv, topk_idx, topk_len, T, T_k, H, Dqk, Dv, K, softmax_scale, attn_sink,
+                  out, out_lo, lse, dout, dq, dkv_accum, d_sink, accumulate, dkv_bf16, workspace, workspace_bytes,
+                  stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -793,45 +867,82 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t
 // Some callers cannot call cudaMalloc: runtimes that reserve all device memory
 // up front in their own pool and forbid any other allocation, or plug-ins
 // loaded into a host program that owns every allocation.  They cannot provide
-// the workspace dsa_sparse_mla_bwd needs (the device error word and the
-// per-(row, head) D array).  This entry point takes its scratch from the
+// the workspace dsa_sparse_mla_bwd needs (the device error word, the scratch
+// slot flags and the dS scratch).  This entry point takes its scratch from the
 // file-scope device array below instead, so it allocates nothing.
 //
-// The array is a fixed 84 MiB + 256 B (error word, D for up to 4 Mi (row,
-// head) pairs, dS scratch for top-k up to 2176) that every GPU which loads
-// this library holds until the process exits.  Its name is only a host-side stand-in for
-// the device array, so the host looks up the array's real device address with
-// cudaGetSymbolAddress, once per device, on the first call made with that
-// device current; that first call should therefore come before any stream
-// capture.  All calls share the one array: two calls whose executions overlap
-// on the GPU race on it, so callers must order them (one stream, or events).
-// Each call clears the error word it uses and overwrites the D array it
-// reads, so stale contents from an earlier call do not leak into the result.
+// The array is a fixed 84 MiB + 1280 B (error word, slot flags, D for 4 Mi
+// (row, head) pairs, dS scratch for top-k up to 2176) that every GPU which
+// loads this library holds until the process exits.  Query rows beyond what
+// its D part holds are processed in chunks (rows are independent and key
+// gradients sum, so dkv and d_sink accumulate over the chunks).  Its name is only a host-side stand-in for the device array,
+// so the host looks up the array's real device address with
+// cudaGetSymbolAddress, once per device and CUDA context, on the first call
+// made there; that first call should therefore come before any stream capture.
+// All calls share the one array: two calls whose executions overlap on the GPU
+// race on it, so callers must order them (one stream, or events).  Each call
+// clears the error word and the slot flags it uses, and its dS scratch is
+// written before it is read, so stale contents from an earlier call do not
+// leak into the result.  dsa_sparse_mla_bwd_noalloc_read_status reads the
+// array's error word, as dsa_read_device_status does for a workspace.
 // ---------------------------------------------------------------------------
+#include <algorithm>
+#include <climits>
 #include <mutex>
 
 namespace dsa {
 namespace bwd {
-constexpr size_t kNoAllocDeltaBytes = size_t(16) << 20;  // D for up to 4 Mi (row, head) pairs
-constexpr int kNoAllocMaxTopk = 17 * kTile;               // dS scratch for up to 17 tiles per row
+constexpr int kNoAllocMaxTopk = 17 * kTile;                   // dS scratch for up to 17 tiles per row
+constexpr size_t kNoAllocDeltaBytes = size_t(16) << 20;        // D for up to 4 Mi (row, head) pairs per chunk
 constexpr size_t kNoAllocScratchBytes =
-    kErrorWordBytes + kNoAllocDeltaBytes + (size_t)kMaxSmSlots * (kNoAllocMaxTopk / kTile) * kDsTileBytes;
+    kHeadBytes + kNoAllocDeltaBytes + (size_t)kMaxSlots * (kNoAllocMaxTopk / kTile) * kDsTileBytes;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on the current device (looked up once per device).
+typedef int (*CtxGetCurrentFn)(void** ctx);
+typedef int (*CtxGetIdFn)(void* ctx, unsigned long long* id);
+
+// Id of the calling thread's current CUDA context (0 if the driver cannot say).
+static unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_ctx = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_ctx = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    cudaGetLastError();
+  });
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_ctx && get_id && get_ctx(&ctx) == 0 && ctx && get_id(ctx, &id) == 0) return id;
+  return 0;
+}
+
+// Device address of g_noalloc_scratch in the current device's context.  It is looked up once per
+// (device, context): a reset of the device's primary context reloads the module, and the array may
+// then sit elsewhere, so a new context id means a new lookup.  (A thread with no context bound yet
+// reads id 0 and looks the address up again; the lookup binds the context.)
 static dsa_status_t noalloc_scratch(void** ptr) {
   static std::mutex mu;
   static void* addr[64] = {};
+  static unsigned long long ctx_of[64] = {};
   int dev = 0;
   dsa_status_t st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
   if (st != DSA_OK) return st;
   if (dev < 0 || dev >= 64) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lk(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || ctx == 0 || ctx != ctx_of[dev]) {
     void* p = nullptr;
     if ((st = cuda_check(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress(scratch)")) != DSA_OK)
       return st;
     addr[dev] = p;
+    ctx_of[dev] = current_context_id();
   }
   *ptr = addr[dev];
   return DSA_OK;
@@ -839,29 +950,52 @@ static dsa_status_t noalloc_scratch(void** ptr) {
 }  // namespace bwd
 }  // namespace dsa
 
-extern "C" size_t dsa_sparse_mla_bwd_noalloc_max_rows(void) { return bwd::kNoAllocDeltaBytes / sizeof(float); }
 extern "C" int32_t dsa_sparse_mla_bwd_noalloc_max_topk(void) { return bwd::kNoAllocMaxTopk; }
 
 extern "C" dsa_status_t dsa_sparse_mla_bwd_noalloc(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
                                                    const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H,
                                                    int32_t Dqk, int32_t Dv, int32_t K, float softmax_scale,
-                                                   const dsa_bf16_t* out, const dsa_bf16_t* out_lo, const float* lse,
-                                                   const dsa_bf16_t* dout, dsa_bf16_t* dq, float* dkv_accum,
-                                                   int32_t accumulate, dsa_bf16_t* dkv_bf16, dsa_stream_t stream) {
-  if ((size_t)(T > 0 ? T : 0) * (size_t)(H > 0 ? H : 0) > dsa_sparse_mla_bwd_noalloc_max_rows())
-    return fail(DSA_ERR_WORKSPACE,
-                "dsa_sparse_mla_bwd_noalloc: T*H = %lld rows x heads exceeds the built-in scratch limit of %zu "
-                "(use dsa_sparse_mla_bwd with a caller workspace, or split the rows into chunks)",
-                (long long)T * H, dsa_sparse_mla_bwd_noalloc_max_rows());
+                                                   const float* attn_sink, const dsa_bf16_t* out,
+                                                   const dsa_bf16_t* out_lo, const float* lse, const dsa_bf16_t* dout,
+                                                   dsa_bf16_t* dq, float* dkv_accum, float* d_sink, int32_t accumulate,
+                                                   dsa_bf16_t* dkv_bf16, dsa_stream_t stream) {
   if (K > bwd::kNoAllocMaxTopk)
     return fail(DSA_ERR_WORKSPACE,
                 "dsa_sparse_mla_bwd_noalloc: top-k K = %d exceeds the built-in scratch limit of %d (use "
                 "dsa_sparse_mla_bwd with a caller workspace)",
                 K, bwd::kNoAllocMaxTopk);
+  const size_t max_pairs = bwd::kNoAllocDeltaBytes / sizeof(float);
+  if (H < 1 || (size_t)H > max_pairs)
+    return fail(DSA_ERR_INVALID_ARGUMENT, "dsa_sparse_mla_bwd_noalloc: H must be in [1, %zu] (got %d)", max_pairs, H);
   dsa_status_t st = check_device();
   if (st != DSA_OK) return st;
   void* scratch = nullptr;
   if ((st = bwd::noalloc_scratch(&scratch)) != DSA_OK) return st;
-  return dsa_sparse_mla_bwd(q, kv, topk_idx, topk_len, T, T_k, H, Dqk, Dv, K, softmax_scale, out, out_lo, lse, dout,
-                            dq, dkv_accum, accumulate, dkv_bf16, scratch, bwd::kNoAllocScratchBytes, stream);
+  const char* who = "dsa_sparse_mla_bwd_noalloc";
+  // rows in chunks whose D fits the array (one chunk for T * H <= 4 Mi)
+  const int32_t per = (int32_t)std::min<size_t>(max_pairs / (size_t)H, (size_t)INT32_MAX);
+  if (T <= 0)
+    return bwd::run(who, q, kv, topk_idx, topk_len, T, T_k, H, Dqk, Dv, K, softmax_scale, attn_sink, out, out_lo, lse,
+                    dout, dq, dkv_accum, d_sink, accumulate, dkv_bf16, scratch, bwd::kNoAllocScratchBytes, stream);
+  for (int32_t r0 = 0; r0 < T; r0 += per) {
+    const int32_t n = std::min(per, T - r0);
+    const size_t rh = (size_t)r0 * H;
+    st = bwd::run(who, q ? q + rh * Dqk : q, kv, topk_idx ? topk_idx + (size_t)r0 * K : topk_idx,
+                  topk_len ? topk_len + r0 : nullptr, n, T_k, H, Dqk, Dv, K, softmax_scale, attn_sink,
+                  out ? out + rh * Dv : out, out_lo ? out_lo + rh * Dv : nullptr, lse ? lse + rh : lse,
+                  dout ? dout + rh * Dv : dout, dq ? dq + rh * Dqk : dq, dkv_accum, d_sink,
+                  (r0 > 0) ? 1 : accumulate, dkv_bf16, scratch, bwd::kNoAllocScratchBytes, stream, r0 == 0,
+                  r0 + n >= T);
+    if (st != DSA_OK) return st;
+  }
+  return ok();
+}
+
+extern "C" dsa_status_t dsa_sparse_mla_bwd_noalloc_read_status(dsa_stream_t stream, int32_t* status_host) {
+  if (!status_host) return fail(DSA_ERR_INVALID_ARGUMENT, "dsa_sparse_mla_bwd_noalloc_read_status: null pointer");
+  dsa_status_t st = check_device();
+  if (st != DSA_OK) return st;
+  void* scratch = nullptr;
+  if ((st = bwd::noalloc_scratch(&scratch)) != DSA_OK) return st;
+  return dsa_read_device_status(scratch, stream, status_host);
 }

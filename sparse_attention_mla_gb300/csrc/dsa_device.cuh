@@ -69,25 +69,30 @@ __device__ __forceinline__ uint32_t sm_id() {
   return v;
 }
 
-// Bounded wait.  Gives up after ~2^31 SM cycles (about one second at the
-// GB300 clock) or as soon as another role of the CTA has given up (*abort
-// set); on give-up it records DSA_ERR_TIMEOUT and returns false so that the
-// caller can leave its loop and reach the CTA teardown.
+// Bounded wait.  Gives up once `limit` SM cycles have passed since the first
+// failed test (the default, 2^31 cycles, is about one second at the GB300
+// clock; the launch passes the limit set by dsa_set_wait_limit_cycles) or as
+// soon as another role of the CTA has given up (*abort set); on give-up it
+// records DSA_ERR_TIMEOUT and returns false so that the caller can leave its
+// loop and reach the CTA teardown.  The limit is checked before each blocking
+// try, so a limit of 0 gives up at the first phase that has not completed.
+// Waits that drain a CTA's own work in flight before teardown use the default.
 constexpr long long kWaitLimitCycles = 1ll << 31;
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* err) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* err,
+                                          long long limit = kWaitLimitCycles) {
   // Fast path: a non-blocking test.  try_wait costs a few hundred cycles even
   // when the phase has already completed, which would stall a thread that
   // issues MMAs after each satisfied wait.
   if (mbar_test(bar, parity)) return true;
   long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 >= limit) {
       *abort = 1;
       record_error(err, DSA_ERR_TIMEOUT);
       return false;
     }
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
   }
 }
 
@@ -282,6 +287,34 @@ namespace dsa {
 // = 0 writes 16 zero bytes without reading src.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// L2 cache policy for data read or written once per CTA (q, dO, O, out, dq):
+// evicted first, so that it does not push out the lines a kernel keeps
+// reusing (gathered kv rows, the fp32 dkv accumulator, the dS scratch).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// cp_async16 with an L2 cache policy.
+__device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src),
+               "r"(src_bytes), "l"(pol)
+               : "memory");
+}
+// 16-byte read-only global load with an L2 cache policy (not kept in L1).
+__device__ __forceinline__ uint4 ldg16_hint(const void* src, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(src), "l"(pol));
+  return v;
+}
+// 16-byte global store with an L2 cache policy.
+__device__ __forceinline__ void stg16_hint(void* dst, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
 }
 // Arrive on bar once every cp.async issued so far by this thread has landed
 // (the barrier's count includes this arrival).

@@ -25,22 +25,27 @@
 //    V^T . P^T, as four M = 128 channel tiles.  TMEM holds S^T (64 columns)
 //    and O^T (256 columns); 64 x 512 fp32 O in the heads-on-M orientation
 //    would need M = 64 tiles that leave half of each TMEM lane quadrant idle.
-//  * P.V runs key rows 0..63 first (P_hi and P_lo for every channel tile),
-//    then rows 64..127, and signals after the first half: the next tile's
-//    rows 0..63 of every value chunk are gathered while the tensor core works
-//    on rows 64..127.
+//  * P.V runs key rows 0..63 first, then rows 64..127, and signals after the
+//    first half: the next tile's rows 0..63 of every value chunk are
+//    gathered while the tensor core works on rows 64..127.
 //  * Online softmax with the running max per head; a rescale of O^T happens
 //    only when some score exceeds the running max by more than 2^8 (lazy
 //    rescale), otherwise P uses the stale max.
 //  * P^T is written into the shared-memory slot of the tile's RoPE channels
 //    (no longer needed once S^T is done), which keeps the working set
-//    (Q 72 KiB + tile 144 KiB) inside one SM's shared memory.  P is split into
-//    bf16 hi + lo parts, so O carries P to about fp32 accuracy and the
-//    backward's D = <dO, O> is consistent with the exact softmax.  The lo part
-//    of key rows 0..63 has an 8 KiB slot of its own and is written with the hi
-//    part; the lo part of rows 64..127 goes into the P slot's rows 0..63 once
-//    the first key half of P.V has read them, while the tensor core runs P_hi
-//    of rows 64..127.
+//    (Q 72 KiB + tile 144 KiB) inside one SM's shared memory.  P is split
+//    into bf16 hi + lo parts and P.V runs on both, so O is accurate to about
+//    fp32 and the backward's D = <dO, O> matches the exact softmax: with P in
+//    bf16 alone (the operand precision of the pages' kernels) D is off by
+//    about 2^-8 of its terms, and dq / dkv miss the 2e-2 max-abs target on
+//    unit-scale inputs.  The lo part of key rows 0..63 has an 8 KiB slot of
+//    its own; the lo part of rows 64..127 goes into the P slot's rows 0..63
+//    once the first key half of P.V has read them, while the tensor core runs
+//    P_hi of rows 64..127.
+//  * An attention sink (optional, one logit per head: NeMo AutoModel
+//    glm_moe_dsa.kernels.cudnn_dsa, _pad_attention_heads) starts the running
+//    max of its head and adds its own term to the denominator at the end; it
+//    has no value row.
 //  * The epilogue stages O (and, on request, the bf16 residual O - bf16(O))
 //    through shared memory for coalesced 16-byte stores.
 //
@@ -72,8 +77,7 @@ struct Smem {
   static constexpr int OFF_P = (DQK == 576) ? OFF_KV + 8 * KV_CHUNK : OFF_KV + NCH * KV_CHUNK;
   static constexpr int OFF_MISC = (DQK == 576) ? OFF_KV + NCH * KV_CHUNK : OFF_P + KV_CHUNK;
   static constexpr int MISC = 2048;
-  // P_lo^T of key rows 0..63 (8 KiB, same layout as the first half of the P slot); rows 64..127
-  // follow the hi part through the P slot
+  // P_lo^T of key rows 0..63 (8 KiB, the layout of the first half of the P slot)
   static constexpr int OFF_PLO = OFF_MISC + MISC;
   static constexpr int TOTAL = OFF_PLO + KV_CHUNK / 2 + 1024;  // + alignment slack
   static_assert(TOTAL <= 232448, "shared memory budget");
@@ -160,8 +164,9 @@ template <int DQK>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_fwd_kernel(const __nv_bfloat16* __restrict__ kv, const __nv_bfloat16* __restrict__ q,
                           const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ topk_len, int T, int Tk,
-                          int H, int K, float sl2e, __nv_bfloat16* __restrict__ out,
-                          __nv_bfloat16* __restrict__ out_lo, float* __restrict__ lse, int* __restrict__ err) {
+                          int H, int K, float sl2e, const float* __restrict__ sink, __nv_bfloat16* __restrict__ out,
+                          __nv_bfloat16* __restrict__ out_lo, float* __restrict__ lse, int* __restrict__ err,
+                          long long wait_limit) {
   using L = Smem<DQK>;
   constexpr int NCH = L::NCH;
   extern __shared__ uint8_t smem_raw[];
@@ -192,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_pv, 1);
     mbar_init(bar_s, 1);
     mbar_init(bar_p, 8);
-    mbar_init(bar_plo, 4);  // the warps of key rows 64..127 (lane quadrants 2, 3)
     mbar_init(bar_pvh, 1);
+    mbar_init(bar_plo, 4);  // the warps of key rows 64..127 (lane quadrants 2, 3)
     mbar_init(bar_fin, 1);
     *s_neff = 0;
     *s_abort = 0;
@@ -219,17 +224,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (idx_row[j] >= 0) last = j + 1;
       if (last) atomicMax(s_neff, last);
     }
-    if (tid < kHeads) s_stat[tid] = -INFINITY;  // running max per head (log2 units)
+    if (tid < kHeads) {  // running max per head (log2 units), from the sink logit when there is one
+      const int h = hg * kHeads + tid;
+      s_stat[tid] = (sink != nullptr && h < H) ? __ldg(sink + h) * 1.4426950408889634f : -INFINITY;
+    }
     // Q [64 heads, DQK] -> NCH chunks of [64 rows x 128 B], 128B swizzle; heads >= H are zero.
     constexpr int UNITS = kHeads * NCH * 8;
+    const uint64_t pol = l2_evict_first_policy();  // q is read once: evicted first, the kv rows stay
     for (int u = tid; u < UNITS; u += kWorkers) {
       const int hh = u / (NCH * 8);
       const int rem = u - hh * (NCH * 8);
       const int c = rem >> 3, uc = rem & 7;
       const int h = hg * kHeads + hh;
       const bool ok = h < H;  // padded heads are zero-filled without a read
-      cp_async16(sQ + c * L::Q_CHUNK + sw128_off(hh, uc), q + (ok ? ((size_t)t * H + h) * DQK + c * 64 + uc * 8 : 0),
-                 ok ? 16u : 0u);
+      cp_async16_hint(sQ + c * L::Q_CHUNK + sw128_off(hh, uc),
+                      q + (ok ? ((size_t)t * H + h) * DQK + c * 64 + uc * 8 : 0), ok ? 16u : 0u, pol);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");  // all copies in flight at once, one wait
     fence_proxy_async_smem();
@@ -252,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // later chunk that has landed too (fewer fences and waits between MMAs)
         const uint64_t a00 = sdesc_sw128(sKV, 16, 1024), b00 = sdesc_sw128(sQ, 16, 1024);
         for (int c = 0; c < NCH && !stop;) {
-          if (!mbar_wait(bar_kv + 8 * c, i & 1, s_abort, err)) { stop = true; break; }
+          if (!mbar_wait(bar_kv + 8 * c, i & 1, s_abort, err, wait_limit)) { stop = true; break; }
           int ce = c + 1;
           while (ce < NCH && mbar_test(bar_kv + 8 * ce, i & 1)) ++ce;
           fence_proxy_async_smem();  // cp.async landings -> visible to the tensor core
@@ -266,9 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (stop) break;
         mma_commit(bar_s);
-        // O^T += V^T (P_hi + P_lo)^T, key rows 0..63 first (P_lo of those rows has its own
-        // slot), so that rows 0..63 of every chunk slot are free while rows 64..127 are multiplied
-        if (!mbar_wait(bar_p, i & 1, s_abort, err)) break;
+        // O^T += V^T (P_hi + P_lo)^T, key rows 0..63 first (P_lo of those rows has its own slot),
+        // so that rows 0..63 of every chunk slot are free while rows 64..127 are multiplied
+        if (!mbar_wait(bar_p, i & 1, s_abort, err, wait_limit)) break;
         tc_fence_after();
         const uint64_t pb0 = sdesc_sw128(sP, L::KV_CHUNK, 1024);
         const uint64_t lb0 = sdesc_sw128(sPlo, L::KV_CHUNK, 1024);
@@ -285,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kHalf; ++k)
             mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), lb0 + (uint64_t)(k * 128), kIdPV, 1u);
         }
-        mma_commit(bar_pvh);  // rows 0..63 of the chunk slots and of the P slot are read
+        mma_commit(bar_pvh);  // rows 0..63 of the chunk slots (and of the P slot) are read
 #pragma unroll
         for (int m = 0; m < kDv / 128; ++m) {
 #pragma unroll
@@ -293,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV, 1u);
         }
         // P_lo of rows 64..127, moved by the workers into the P slot's rows 0..63
-        if (!mbar_wait(bar_plo, i & 1, s_abort, err)) break;
+        if (!mbar_wait(bar_plo, i & 1, s_abort, err, wait_limit)) break;
         tc_fence_after();
 #pragma unroll
         for (int m = 0; m < kDv / 128; ++m) {
@@ -346,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this key row's index does not depend on the MMA: its load overlaps the wait
       const int j = i * kTile + r;
       const int ixw = (j < n_eff) ? __ldg(idx_row + j) : -1;
-      const bool got = mbar_wait(bar_s, i & 1, s_abort, err);
+      const bool got = mbar_wait(bar_s, i & 1, s_abort, err, wait_limit);
       // every thread of the half leaves together, or none does (named barriers follow)
       if (named_bar_or(bar_id, 128, !got)) { aborted = true; break; }
       tc_fence_after();
@@ -446,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int rix[4];
       if (more) load_rows(i + 1, rix);
       {
-        const bool okh = mbar_wait(bar_pvh, i & 1, s_abort, err);
+        const bool okh = mbar_wait(bar_pvh, i & 1, s_abort, err, wait_limit);
         if (qd >= 2) {
           if (okh) {
 #pragma unroll
@@ -463,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (more) {
         for (int c = 0; c < kDv / 64; ++c) gather_half<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, 0);
         // rows 64..127 (and the RoPE chunk, which holds P) once P.V is complete
-        if (!mbar_wait(bar_pv, i & 1, s_abort, err)) {
+        if (!mbar_wait(bar_pv, i & 1, s_abort, err, wait_limit)) {
           aborted = true;
         } else {
           for (int c = 0; c < kDv / 64; ++c) {
@@ -476,19 +485,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (!aborted && ntiles > 0) {
-      const bool got = mbar_wait(bar_pv, (ntiles - 1) & 1, s_abort, err);
+      const bool got = mbar_wait(bar_pv, (ntiles - 1) & 1, s_abort, err, wait_limit);
       aborted = named_bar_or(bar_id, 128, !got);
       tc_fence_after();
     }
+    // after an abort some gathers may still be landing: none may land once the epilogue reuses the tile
+    asm volatile("cp.async.wait_all;" ::: "memory");
     // ---- epilogue: l per head, lse, out = O^T / l ----
     const float lsum = warp_transpose_reduce<false>(l_part, lane);
     named_bar(bar_id, 128);  // everyone is done reading s_red / s_stat of the loop
     s_red[qd * 64 + ch * 32 + lane] = lsum;
     named_bar(bar_id, 128);
-    const float lt = s_red[ch * 32 + lane] + s_red[64 + ch * 32 + lane] + s_red[128 + ch * 32 + lane] +
-                     s_red[192 + ch * 32 + lane];
     const float mh = s_stat[ch * 32 + lane];
     const int hl = hg * kHeads + ch * 32 + lane;
+    // the sink's own term, relative to the final running max (which started at the sink)
+    const float s2 = (sink != nullptr && hl < H) ? __ldg(sink + hl) * 1.4426950408889634f : -INFINITY;
+    const float lsink = (s2 > -INFINITY) ? exp2f(s2 - mh) : 0.f;  // a -inf sink is no sink
+    const float lt = s_red[ch * 32 + lane] + s_red[64 + ch * 32 + lane] + s_red[128 + ch * 32 + lane] +
+                     s_red[192 + ch * 32 + lane] + lsink;
     if (qd == 0 && hl < H) lse[(size_t)t * H + hl] = (lt > 0.f) ? (mh * 0.69314718055994531f + logf(lt)) : -INFINITY;
     if (qd == 0) s_lsum[ch * 32 + lane] = lt;
     named_bar(bar_id, 128);
@@ -524,9 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar(3, kWorkers);
     const int hcount = min(kHeads, H - hg * kHeads);
     const size_t gbase = ((size_t)t * H + hg * kHeads) * kDv;
+    const uint64_t pol = l2_evict_first_policy();  // out and out_lo are written once
     for (int u = tid; u < hcount * (kDv / 8); u += kWorkers) {
-      reinterpret_cast<uint4*>(out + gbase)[u] = reinterpret_cast<const uint4*>(stage)[u];
-      if (out_lo) reinterpret_cast<uint4*>(out_lo + gbase)[u] = reinterpret_cast<const uint4*>(stage_lo)[u];
+      stg16_hint(reinterpret_cast<uint4*>(out + gbase) + u, reinterpret_cast<const uint4*>(stage)[u], pol);
+      if (out_lo) stg16_hint(reinterpret_cast<uint4*>(out_lo + gbase) + u, reinterpret_cast<const uint4*>(stage_lo)[u], pol);
     }
   }
 
@@ -540,21 +555,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int DQK>
 dsa_status_t launch(const void* kv, const void* q, const int32_t* idx, const int32_t* len, int T, int Tk, int H,
-                    int K, float scale, void* out, void* out_lo, float* lse, int* err, cudaStream_t s) {
+                    int K, float scale, const float* sink, void* out, void* out_lo, float* lse, int* err,
+                    cudaStream_t s) {
   using L = Smem<DQK>;
-  static bool configured = false;
-  if (!configured) {
-    dsa_status_t st = cuda_check(cudaFuncSetAttribute(sparse_mla_fwd_kernel<DQK>,
-                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL),
-                                 "configuring sparse_mla_fwd_kernel");
-    if (st != DSA_OK) return st;
-    configured = true;
-  }
+  dsa_status_t st = configure_kernel_smem(reinterpret_cast<const void*>(sparse_mla_fwd_kernel<DQK>), L::TOTAL,
+                                          "configuring sparse_mla_fwd_kernel");
+  if (st != DSA_OK) return st;
   dim3 grid(T, (H + kHeads - 1) / kHeads);
   const float sl2e = scale * 1.4426950408889634f;
   sparse_mla_fwd_kernel<DQK><<<grid, kThreads, L::TOTAL, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(kv), reinterpret_cast<const __nv_bfloat16*>(q), idx, len, T, Tk, H, K,
-      sl2e, reinterpret_cast<__nv_bfloat16*>(out), reinterpret_cast<__nv_bfloat16*>(out_lo), lse, err);
+      sl2e, sink, reinterpret_cast<__nv_bfloat16*>(out), reinterpret_cast<__nv_bfloat16*>(out_lo), lse, err,
+      wait_limit_cycles());
   return cuda_check(cudaGetLastError(), "launching sparse_mla_fwd_kernel");
 }
 
@@ -571,9 +583,9 @@ extern "C" size_t dsa_sparse_mla_fwd_workspace_size(int32_t T, int32_t H) {
 
 extern "C" dsa_status_t dsa_sparse_mla_fwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const int32_t* topk_idx,
                                            const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk,
-                                           int32_t Dv, int32_t K, float softmax_scale, dsa_bf16_t* out,
-                                           dsa_bf16_t* out_lo, float* lse, void* workspace, size_t workspace_bytes,
-                                           dsa_stream_t stream) {
+                                           int32_t Dv, int32_t K, float softmax_scale, const float* attn_sink,
+                                           dsa_bf16_t* out, dsa_bf16_t* out_lo, float* lse, void* workspace,
+                                           size_t workspace_bytes, dsa_stream_t stream) {
   const char* who = "dsa_sparse_mla_fwd";
   if (T < 0 || T_k < 1 || H < 1 || K < 1)
     return fail(DSA_ERR_INVALID_ARGUMENT, "%s: need T >= 0, T_k >= 1, H >= 1, K >= 1 (got %d, %d, %d, %d)", who, T,
@@ -594,8 +606,9 @@ extern "C" dsa_status_t dsa_sparse_mla_fwd(const dsa_bf16_t* q, const dsa_bf16_t
   if ((st = clear_error_word(workspace, s)) != DSA_OK) return st;
   if (T == 0) return ok();
   int* err = reinterpret_cast<int*>(workspace);
-  st = (Dqk == 576)
-           ? fwd::launch<576>(kv, q, topk_idx, topk_len, T, T_k, H, K, softmax_scale, out, out_lo, lse, err, s)
-           : fwd::launch<512>(kv, q, topk_idx, topk_len, T, T_k, H, K, softmax_scale, out, out_lo, lse, err, s);
+  st = (Dqk == 576) ? fwd::launch<576>(kv, q, topk_idx, topk_len, T, T_k, H, K, softmax_scale, attn_sink, out, out_lo,
+                                      lse, err, s)
+                    : fwd::launch<512>(kv, q, topk_idx, topk_len, T, T_k, H, K, softmax_scale, attn_sink, out, out_lo,
+                                      lse, err, s);
   return st == DSA_OK ? ok() : st;
 }

@@ -24,6 +24,11 @@ dsa_status_t make_map_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows,
 dsa_status_t check_workspace(const void* ws, size_t bytes, size_t need, const char* who);
 // Zeroes the device error word at the start of the workspace.
 dsa_status_t clear_error_word(void* ws, cudaStream_t stream);
+// Cycle limit of the kernels' bounded waits (dsa_set_wait_limit_cycles; default 2^31).
+long long wait_limit_cycles();
+// Sets the kernel's dynamic shared-memory limit to `bytes` once per (kernel, device),
+// on the current device; thread-safe.
+dsa_status_t configure_kernel_smem(const void* func, int bytes, const char* what);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -305,7 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float* __restrict__ w, const int32_t* __restrict__ seq_start,
                         const int32_t* __restrict__ causal_len, int T, int Tk, int Hi,
                         int K, int32_t* __restrict__ topk_idx, int32_t* __restrict__ topk_len,
-                        int* __restrict__ err, float* __restrict__ scores, int score_row0, int score_rows) {
+                        int* __restrict__ err, float* __restrict__ scores, int score_row0, int score_rows,
+                        long long wait_limit) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(smem + OFF_Q);
@@ -366,12 +367,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x - 64;
     // Q rows (token k, head h) -> 2 chunks of [256 rows x 128 B], swizzled; padding rows are
     // zero-filled without a read.  All copies are in flight at once (cp.async), one wait.
+    const uint64_t pol = l2_evict_first_policy();  // q_idx is read once: evicted first, k_idx stays
     for (int u = tid; u < kN * 16; u += kEpi) {
       const int row = u >> 4, c = (u >> 3) & 1, uc = u & 7;
       const int k = row / kHeads, h = row - k * kHeads;
       const bool ok = k < nt && h < Hi;
-      cp_async16(sQ + c * Q_CHUNK + sw128_off(row, uc),
-                 q_idx + (ok ? ((size_t)(t0 + k) * Hi + h) * kDi + c * 64 + uc * 8 : 0), ok ? 16u : 0u);
+      cp_async16_hint(sQ + c * Q_CHUNK + sw128_off(row, uc),
+                      q_idx + (ok ? ((size_t)(t0 + k) * Hi + h) * kDi + c * 64 + uc * 8 : 0), ok ? 16u : 0u, pol);
     }
     for (int u = tid; u < kTokens * kHeads; u += kEpi) {
       const int k = u / kHeads, h = u - k * kHeads;
@@ -389,15 +391,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       int i = 0;
       for (; i < ntiles; ++i) {
         const int s = i & 1;
-        if (!mbar_wait(bar_ke + 8 * s, ((i >> 1) & 1) ^ 1, s_abort, err)) break;
+        if (!mbar_wait(bar_ke + 8 * s, ((i >> 1) & 1) ^ 1, s_abort, err, wait_limit)) break;
         mbar_expect_tx(bar_kf + 8 * s, K_STAGE);
         const int row = (kt0 + i) * kTile;
         tma_load_2d(sK + s * K_STAGE, &k_map, 0, row, bar_kf + 8 * s);
         tma_load_2d(sK + s * K_STAGE + K_CHUNK, &k_map, 64, row, bar_kf + 8 * s);
       }
-      if (*s_abort && i > 0) {
+      if (*s_abort) {
+        // tiles i-2 and i-1 may both be in flight (two stages): both land before the CTA exits
         volatile int dummy = 0;
-        mbar_wait(bar_kf + 8 * ((i - 1) & 1), ((i - 1) >> 1) & 1, &dummy, err);
+        for (int j = (i >= 2 ? i - 2 : 0); j < i; ++j) mbar_wait(bar_kf + 8 * (j & 1), (j >> 1) & 1, &dummy, err);
       }
     }
     __syncwarp();
@@ -407,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kId = idesc_bf16(128, kN, false, false);
       for (int i = 0; i < ntiles; ++i) {
         const int s = i & 1, b = i & 1;
-        if (!mbar_wait(bar_kf + 8 * s, (i >> 1) & 1, s_abort, err)) break;
-        if (!mbar_wait(bar_de + 8 * b, ((i >> 1) & 1) ^ 1, s_abort, err)) break;
+        if (!mbar_wait(bar_kf + 8 * s, (i >> 1) & 1, s_abort, err, wait_limit)) break;
+        if (!mbar_wait(bar_de + 8 * b, ((i >> 1) & 1) ^ 1, s_abort, err, wait_limit)) break;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 2; ++c)
@@ -448,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool aborted = false;
     for (int i = 0; i < ntiles; ++i) {
       const int b = i & 1;
-      const bool got = mbar_wait(bar_df + 8 * b, (i >> 1) & 1, s_abort, err);
+      const bool got = mbar_wait(bar_df + 8 * b, (i >> 1) & 1, s_abort, err, wait_limit);
       if (named_bar_or(hf.bar, 128, !got)) { aborted = true; break; }
       tc_fence_after();
       uint32_t v[64];
@@ -562,18 +565,13 @@ static dsa_status_t run(const char* who, const dsa_bf16_t* q_idx, const dsa_bf16
   if (T == 0) return ok();
   CUtensorMap map;
   if ((st = make_map_2d_bf16(&map, k_idx, (uint64_t)T_k, (uint64_t)kDi, (uint64_t)kDi, 64, kTile)) != DSA_OK) return st;
-  static bool configured = false;
-  if (!configured) {
-    if ((st = cuda_check(cudaFuncSetAttribute(indexer_topk_kernel<kScores>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, TOTAL),
-                         "configuring indexer_topk_kernel")))
-      return st;
-    configured = true;
-  }
+  if ((st = configure_kernel_smem(reinterpret_cast<const void*>(indexer_topk_kernel<kScores>), TOTAL,
+                                  "configuring indexer_topk_kernel")))
+    return st;
   const int nblk = (T + kTokens - 1) / kTokens;
   indexer_topk_kernel<kScores><<<nblk, kThreads, TOTAL, s>>>(
       map, reinterpret_cast<const __nv_bfloat16*>(q_idx), head_weights, seq_start, causal_len, T, T_k, Hi, K, topk_idx,
-      topk_len, reinterpret_cast<int*>(workspace), scores, score_row0, score_rows);
+      topk_len, reinterpret_cast<int*>(workspace), scores, score_row0, score_rows, wait_limit_cycles());
   if ((st = cuda_check(cudaGetLastError(), "launching indexer_topk_kernel"))) return st;
   return ok();
 }

@@ -17,7 +17,8 @@ def lib():
 def test_every_declared_symbol_is_exported(lib):
     names = dsa.declared_symbols()
     expected = {"dsa_packed_metadata", "dsa_packed_metadata_cp", "dsa_indexer_topk", "dsa_indexer_topk_cp",
-                "dsa_sparse_mla_fwd", "dsa_sparse_mla_bwd",
+                "dsa_sparse_mla_fwd", "dsa_sparse_mla_bwd", "dsa_sparse_mla_bwd_noalloc",
+                "dsa_sparse_mla_bwd_noalloc_read_status", "dsa_sparse_mla_bwd_noalloc_max_topk",
                 "dsa_status_string", "dsa_last_error_message", "dsa_read_device_status"}
     assert expected <= set(names)
     for n in names:
@@ -25,7 +26,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dsa_abi_version() == 1
+    assert lib.dsa_abi_version() == 2
     for code in range(8):
         s = lib.dsa_status_string(code).decode()
         assert s.startswith(dsa.STATUS_NAMES[code])
@@ -36,12 +37,12 @@ FAKE = P(0x10000)  # never dereferenced: validation fails before any device use
 
 
 def fwd(lib, **kw):
-    a = dict(q=FAKE, kv=FAKE, idx=FAKE, ln=None, T=4, Tk=8, H=16, Dqk=576, Dv=512, K=64, scale=0.1, out=FAKE,
-             lse=FAKE, ws=P(0x100000), wsb=1 << 20, stream=None)
+    a = dict(q=FAKE, kv=FAKE, idx=FAKE, ln=None, T=4, Tk=8, H=16, Dqk=576, Dv=512, K=64, scale=0.1, sink=None,
+             out=FAKE, lse=FAKE, ws=P(0x100000), wsb=1 << 20, stream=None)
     a.update(kw)
     return lib.dsa_sparse_mla_fwd(a["q"], a["kv"], a["idx"], a["ln"], a["T"], a["Tk"], a["H"], a["Dqk"], a["Dv"],
-                                  a["K"], ctypes.c_float(a["scale"]), a["out"], None, a["lse"], a["ws"], a["wsb"],
-                                  a["stream"])
+                                  a["K"], ctypes.c_float(a["scale"]), a["sink"], a["out"], None, a["lse"], a["ws"],
+                                  a["wsb"], a["stream"])
 
 
 @pytest.mark.parametrize("bad", [dict(Dqk=500), dict(Dv=256), dict(K=0), dict(H=0), dict(Tk=0), dict(T=-1),
@@ -77,19 +78,20 @@ def test_metadata_cp_rejects_invalid_arguments(lib, bad):
 
 
 def bwd(lib, **kw):
-    a = dict(q=FAKE, kv=FAKE, idx=FAKE, ln=None, T=4, Tk=8, H=16, Dqk=576, Dv=512, K=64, scale=0.1, out=FAKE,
-             out_lo=None, lse=FAKE, dout=FAKE, dq=FAKE, dkv=FAKE, acc=0, dkv_bf16=None, ws=P(0x100000), wsb=1 << 30,
-             stream=None)
+    a = dict(q=FAKE, kv=FAKE, idx=FAKE, ln=None, T=4, Tk=8, H=16, Dqk=576, Dv=512, K=64, scale=0.1, sink=None,
+             out=FAKE, out_lo=None, lse=FAKE, dout=FAKE, dq=FAKE, dkv=FAKE, dsink=None, acc=0, dkv_bf16=None,
+             ws=P(0x100000), wsb=1 << 30, stream=None)
     a.update(kw)
     return lib.dsa_sparse_mla_bwd(a["q"], a["kv"], a["idx"], a["ln"], a["T"], a["Tk"], a["H"], a["Dqk"], a["Dv"],
-                                  a["K"], ctypes.c_float(a["scale"]), a["out"], a["out_lo"], a["lse"], a["dout"],
-                                  a["dq"], a["dkv"], a["acc"], a["dkv_bf16"], a["ws"], a["wsb"], a["stream"])
+                                  a["K"], ctypes.c_float(a["scale"]), a["sink"], a["out"], a["out_lo"], a["lse"],
+                                  a["dout"], a["dq"], a["dkv"], a["dsink"], a["acc"], a["dkv_bf16"], a["ws"], a["wsb"],
+                                  a["stream"])
 
 
 @pytest.mark.parametrize("bad", [dict(Dqk=500), dict(Dv=256), dict(K=0), dict(H=0), dict(Tk=0), dict(T=-1),
                                  dict(acc=2), dict(scale=0.0), dict(scale=float("inf")), dict(kv=None),
                                  dict(dkv=None), dict(dq=None), dict(q=P(0x10002)), dict(out_lo=P(0x10008)),
-                                 dict(dkv_bf16=P(0x10002))])
+                                 dict(dkv_bf16=P(0x10002)), dict(dsink=FAKE)])
 def test_bwd_rejects_invalid_arguments(lib, bad):
     assert bwd(lib, **bad) == 3  # DSA_ERR_INVALID_ARGUMENT
     assert lib.dsa_last_error_message().decode().startswith("dsa_sparse_mla_bwd")
@@ -138,3 +140,14 @@ def test_indexer_cp_rejects_invalid_arguments(lib, bad):
 def test_indexer_rejects_bad_workspace(lib):
     assert idxr(lib, ws=None) == 4
     assert idxr(lib, wsb=16) == 4
+
+
+def test_wait_limit_setter_returns_the_previous_value(lib):
+    lib.dsa_set_wait_limit_cycles.argtypes = [ctypes.c_int64]
+    lib.dsa_set_wait_limit_cycles.restype = ctypes.c_int64
+    prev = lib.dsa_set_wait_limit_cycles(12345)
+    try:
+        assert lib.dsa_set_wait_limit_cycles(-1) == 12345
+        assert lib.dsa_set_wait_limit_cycles(-1) == 1 << 31  # negative: the default
+    finally:
+        lib.dsa_set_wait_limit_cycles(prev)

@@ -1,4 +1,7 @@
-"""Sparse MLA backward: CUDA path (through the C ABI) vs the fp64 oracle."""
+"""Sparse MLA backward: CUDA path (through the C ABI) vs the fp64 oracle.
+
+The backward gets the forward's residual of O (as the benchmark runs it), so
+that D = <dO, O> uses the fp32 O; one case takes D from the rounded output."""
 import numpy as np
 import pytest
 import torch
@@ -19,10 +22,10 @@ def gpu_fwd_bwd(q, kv, dout, idx, scale, ln=None, dkv=None, accumulate=False, wa
     ln_ = None if ln is None else ln.to(DEV)
     ws = torch.zeros(dsa.workspace_size("bwd", q.shape[0], q.shape[1], idx.shape[1]) + 256, dtype=torch.uint8, device=DEV)
     out, lse, lo = dsa.dsa_sparse_mla_fwd(dq_, kv_, i_, scale, topk_len=ln_, out_lo=True)
+    lo = lo if use_lo else None
     kb = torch.empty_like(kv_) if want_bf16 else None
     dq, dkv, kb = dsa.dsa_sparse_mla_bwd(dq_, kv_, i_, scale, out, lse, do_, topk_len=ln_, dkv_accum=dkv,
-                                         accumulate=accumulate, dkv_bf16=kb, workspace=ws,
-                                         out_lo=lo if use_lo else None)
+                                         accumulate=accumulate, dkv_bf16=kb, workspace=ws, out_lo=lo)
     assert dsa.dsa_read_device_status(ws) == 0
     return dq, dkv, kb
 
@@ -95,7 +98,8 @@ def test_bwd_dkv_bf16_copy_is_rounded_accumulator():
 
 
 def test_bwd_dkv_column_sums_equal_dout_sums():
-    # property at any size: sum_k dkv[k, c] = sum_{t,h nonempty} dO[t,h,c] (c < 512), 0 for RoPE channels
+    # property at any size: sum_k dkv[k, c] = sum_{t,h nonempty} dO[t,h,c] (c < 512), 0 for RoPE channels.
+    # It rests on sum_j dS_j = 0, i.e. on D = <dO, O> with the fp32 O (the forward's residual)
     q, kv, dout, idx = make_case(256, 1000, 64, 576, 700, 10)
     _, dkv, _ = gpu_fwd_bwd(q, kv, dout, idx, 192 ** -0.5)
     col = dkv.double().sum(0).cpu().numpy()

@@ -1,6 +1,15 @@
 """Edge cases of the CUDA path against the fp64 oracle: top-k of one, scores
 that grow across tiles (the forward's lazy rescale of the running max), kv
-longer than the queries with non-causal index sets, and empty calls."""
+longer than the queries with non-causal index sets, empty calls, and the
+indexer at the smallest and largest K.
+
+Every case passes the forward's residual of O to the backward, so D is
+accurate to about fp32.  On stress inputs (far outside unit scale) out, lse
+and dkv meet the pages' bounds element by element.  dq is formed from dS rounded to bf16 (unit
+roundoff 2^-8) before the dq product, so where large terms cancel its error
+is bounded by 2^-8 scale sum_j |dS_j| |kv[idx_j, c]| (the oracle's dq
+magnitude), not by |dq|: dq is checked against that bound plus the pages'
+2e-2, and in relative Frobenius norm."""
 import numpy as np
 import pytest
 import torch
@@ -9,8 +18,9 @@ import oracle
 import sparse_attention_mla_gb300 as dsa
 from sparse_attention_mla_gb300 import synth
 
-from _cmp import REL_FRO, assert_close, assert_lse, errors
+from _cmp import MAX_ABS, REL_FRO, assert_close, assert_lse, errors, storage_half_ulp, to64
 from test_gpu_fwd import make_case
+from test_gpu_indexer import check_rows
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -25,18 +35,18 @@ def fwd_bwd_vs_oracle(q, kv, dout, idx, scale, ln=None, stress=False):
     dq, dkv, _ = dsa.dsa_sparse_mla_bwd(qd, kvd, idd, scale, out, lse, dod, topk_len=lnd, out_lo=lo, workspace=wb)
     assert dsa.dsa_read_device_status(wf) == 0 and dsa.dsa_read_device_status(wb) == 0
     ref_o, ref_l = oracle.sparse_mla_fwd(q, kv, idx, scale, len_rows=ln)
-    ref_dq, ref_dkv = oracle.sparse_mla_bwd(q, kv, idx, dout, scale, len_rows=ln)
+    ref_dq, ref_dkv, dq_mag = oracle.sparse_mla_bwd(q, kv, idx, dout, scale, len_rows=ln, with_dq_magnitude=True)
     assert_close(out.cpu(), ref_o, "out")
     assert_lse(lse.cpu(), ref_l)
+    assert_close(dkv.cpu(), ref_dkv, "dkv")
     if not stress:
         assert_close(dq.cpu(), ref_dq, "dq")
-        assert_close(dkv.cpu(), ref_dkv, "dkv")
     else:
-        # dq is formed from bf16 dS: where large terms cancel, its element error follows the sum of
-        # |terms|, not dq; stress inputs check the gradients in relative Frobenius norm only
-        for got, ref, name in ((dq, ref_dq, "dq"), (dkv, ref_dkv, "dkv")):
-            _, rf = errors(got.cpu(), ref)
-            assert rf <= REL_FRO, f"{name}: rel_fro={rf:.3e}"
+        g = dq.cpu()
+        excess = np.abs(to64(g) - ref_dq) - storage_half_ulp(g) - 2.0 ** -8 * dq_mag
+        assert float(np.max(excess)) <= MAX_ABS, f"dq: {float(np.max(excess)):.3e} beyond the bf16-dS bound"
+        _, rf = errors(g, ref_dq)
+        assert rf <= REL_FRO, f"dq: rel_fro={rf:.3e}"
 
 
 def test_topk_one():
@@ -92,20 +102,15 @@ def test_empty_calls_leave_outputs_consistent():
 
 
 def test_indexer_k_one_and_k_2048_boundaries():
-    # K = 1 picks the single best key; K = 2048 (the largest) on windows just above and below it
+    # K = 1 picks the single best key; K = 2048 (the largest) on windows just above and below it;
+    # sets equal the oracle's except inside the fp32 tie band (check_rows)
     T = 2300
     x = synth.indexer_inputs(T, 64, 128, seed=17)
     cu = torch.tensor([0, T], dtype=torch.int32)
     start, _, _, _ = dsa.dsa_packed_metadata(cu.to(DEV), T)
+    rows = np.array([0, 1, 2, 1000, 2046, 2047, 2048, 2049, 2050, T - 2, T - 1])
     for K in (1, 2048):
-        idx, ln = dsa.dsa_indexer_topk(x["q_idx"].to(DEV), x["k_idx"].to(DEV), x["w"].to(DEV), start, K)
-        rows = np.array([0, 1, 2046, 2047, 2048, 2049, T - 1])
-        ref_idx, ref_len, _ = oracle.indexer_topk(x["q_idx"][rows], x["k_idx"], x["w"][rows],
-                                                  start.cpu().numpy(), rows, K)
-        gl = ln.cpu().numpy()[rows]
-        assert np.array_equal(gl, ref_len)
-        gi = idx.cpu().numpy()[rows]
-        for r in range(len(rows)):
-            n = ref_len[r]
-            assert np.all(gi[r, n:] == -1)
-            assert len(set(gi[r, :n]) ^ set(ref_idx[r, :n])) <= 2  # at most one fp32 near-tie swap
+        ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
+        idx, ln = dsa.dsa_indexer_topk(x["q_idx"].to(DEV), x["k_idx"].to(DEV), x["w"].to(DEV), start, K, workspace=ws)
+        assert dsa.dsa_read_device_status(ws) == 0
+        check_rows(idx.cpu().numpy(), ln.cpu().numpy(), x["q_idx"], x["k_idx"], x["w"], start.cpu().numpy(), rows, K)

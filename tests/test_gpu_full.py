@@ -1,11 +1,16 @@
 """Full-size checks: the pages' workloads at their full sizes, in the launch
-configuration the benchmark times, against the fp64 oracle.
+configuration the benchmark times (the forward's residual of O passed to the
+backward), against the fp64 oracle.
 
-Large outputs are compared on sampled rows the oracle computes one by one
-(query rows are independent), plus properties that hold at any size:
-  * dkv column sums: sum_k dkv[k,c] = sum_{t,h nonempty} dO[t,h,c] (c < 512), 0 for RoPE channels;
-  * dkv restricted to a chunk of rows (a call on row-offset pointers) equals
-    the oracle's dkv of exactly those rows, at full T_k and K;
+  * V3.2 layout and NoPE: dq of every query row and dkv of every key row,
+    element by element (the oracle runs every row, in chunks whose key
+    gradients accumulate, as query chunks do);
+  * the 32k indexer -> MLA path and the THD IndexShare layers, where the
+    oracle cannot run every row: out / lse / dq on sampled rows the oracle
+    computes one by one (query rows are independent), dkv restricted to a
+    chunk of rows (a call on row-offset pointers) against the oracle's dkv of
+    exactly those rows at full T_k and K, and the dkv column sums
+    sum_k dkv[k,c] = sum_{t,h nonempty} dO[t,h,c] (c < 512), 0 for RoPE;
   * query chunks give the same outputs as one shot.
 Inputs are drawn on the GPU with the seeded recipe (sparse_attention_mla_gb300.synth).
 """
@@ -22,6 +27,7 @@ from test_gpu_indexer import check_rows
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
+ORACLE_CHUNK_BYTES = 6e8  # the oracle keeps P and dS (fp64) of the rows of one chunk
 
 
 def causal_idx_gpu(seq_start, K, seed, T):
@@ -52,25 +58,37 @@ def sample_rows(T, starts_of_interest, n_random=12, seed=0):
     return np.array(sorted(rows))
 
 
-def mla_full_check(q, kv, dout, idx, scale, ln=None, rows=None, chunk=(0, 64), Dv=512):
-    """fwd+bwd of the whole problem, then row samples, column sums and one exact dkv chunk."""
+def mla_full_check(q, kv, dout, idx, scale, ln=None, rows=None, chunk=(0, 64), Dv=512, every_row=False):
+    """fwd+bwd of the whole problem as the benchmark runs it, then out/lse on the sampled rows and
+    either (every_row) dq of every row and the whole dkv element by element, or dq on the sampled
+    rows, the dkv column sums and the exact dkv of one chunk of rows."""
     T, H = q.shape[0], q.shape[1]
+    K = idx.shape[1]
     wf = torch.zeros(dsa.workspace_size("fwd", T, H), dtype=torch.uint8, device=DEV)
-    wb = torch.zeros(dsa.workspace_size("bwd", T, H, idx.shape[1]), dtype=torch.uint8, device=DEV)
+    wb = torch.zeros(dsa.workspace_size("bwd", T, H, K), dtype=torch.uint8, device=DEV)
     out, lse, lo = dsa.dsa_sparse_mla_fwd(q, kv, idx, scale, topk_len=ln, out_lo=True, workspace=wf)
     dq, dkv, _ = dsa.dsa_sparse_mla_bwd(q, kv, idx, scale, out, lse, dout, topk_len=ln, out_lo=lo, workspace=wb)
     assert dsa.dsa_read_device_status(wf) == 0 and dsa.dsa_read_device_status(wb) == 0
-    del wb
     kvc = kv.cpu()
     r = torch.as_tensor(rows)
     ln_r = None if ln is None else ln[r].cpu()
     ref_o, ref_l = oracle.sparse_mla_fwd(q[r].cpu(), kvc, idx[r].cpu(), scale, len_rows=ln_r)
     assert_close(out[r].cpu(), ref_o, "out (sampled rows)")
     assert_lse(lse[r].cpu(), ref_l)
+    if every_row:
+        ref_dkv = np.zeros((kv.shape[0], kv.shape[1]), np.float64)
+        step = max(1, int(ORACLE_CHUNK_BYTES // (H * K * 16)))
+        for a in range(0, T, step):
+            b = min(T, a + step)
+            ref_dq, _ = oracle.sparse_mla_bwd(q[a:b].cpu(), kvc, idx[a:b].cpu(), dout[a:b].cpu(), scale,
+                                              len_rows=None if ln is None else ln[a:b].cpu(), dkv=ref_dkv)
+            assert_close(dq[a:b].cpu(), ref_dq, f"dq rows {a}:{b}")
+        assert_close(dkv.cpu(), ref_dkv, "dkv (every key row)")
+        return out, lse, lo, dq, dkv
     ref_dq, _ = oracle.sparse_mla_bwd(q[r].cpu(), kvc, idx[r].cpu(), dout[r].cpu(), scale, len_rows=ln_r)
     assert_close(dq[r].cpu(), ref_dq, "dq (sampled rows)")
     # column sums of the full dkv
-    valid = (idx >= 0) if ln is None else ((idx >= 0) & (torch.arange(idx.shape[1], device=DEV)[None, :] < ln[:, None]))
+    valid = (idx >= 0) if ln is None else ((idx >= 0) & (torch.arange(K, device=DEV)[None, :] < ln[:, None]))
     nonempty = valid.any(dim=1)
     col = dkv.double().sum(0).cpu().numpy()
     ref = torch.zeros(dout.shape[-1], dtype=torch.float64, device=DEV)
@@ -83,7 +101,8 @@ def mla_full_check(q, kv, dout, idx, scale, ln=None, rows=None, chunk=(0, 64), D
     # exact dkv of a chunk of rows, at full T_k and K
     a, b = chunk
     _, dkv_c, _ = dsa.dsa_sparse_mla_bwd(q[a:b], kv, idx[a:b], scale, out[a:b], lse[a:b], dout[a:b],
-                                         topk_len=None if ln is None else ln[a:b], out_lo=lo[a:b])
+                                         topk_len=None if ln is None else ln[a:b], out_lo=lo[a:b], workspace=wb)
+    assert dsa.dsa_read_device_status(wb) == 0
     _, ref_c = oracle.sparse_mla_bwd(q[a:b].cpu(), kvc, idx[a:b].cpu(), dout[a:b].cpu(), scale,
                                      len_rows=None if ln is None else ln[a:b].cpu())
     assert_close(dkv_c.cpu(), ref_c, f"dkv of rows {a}:{b}")
@@ -98,7 +117,7 @@ def test_full_v32_layout_S4096_H128_K2048():
     idx = causal_idx_gpu(torch.zeros(T, dtype=torch.int32), c["K"], 2, T)
     rows = np.union1d(sample_rows(T, [0, 1, 2, 63, 2047, 2048, 2049, T - 1], n_random=0, seed=2),
                       np.random.default_rng(2).choice(T, 2048, replace=False))  # >= 2048 distinct rows
-    mla_full_check(x["q"], x["kv"], x["dout"], idx, c["scale"], rows=rows, chunk=(T - 48, T))
+    mla_full_check(x["q"], x["kv"], x["dout"], idx, c["scale"], rows=rows, every_row=True)
 
 
 def test_full_indexer_32k_then_sparse_mla_H64():
@@ -111,10 +130,13 @@ def test_full_indexer_32k_then_sparse_mla_H64():
     ws = torch.zeros(dsa.workspace_size("indexer", T, K), dtype=torch.uint8, device=DEV)
     idx, ln = dsa.dsa_indexer_topk(ind["q_idx"], ind["k_idx"], ind["w"], start, K, workspace=ws)
     assert dsa.dsa_read_device_status(ws) == 0
-    rows = sample_rows(T, [0, 1, 2047, 2048, 2049, 16383, T - 2, T - 1], n_random=24, seed=3)
+    # >= 2048 distinct rows of the indexer against the oracle's full-window top-k
+    rows = np.union1d(sample_rows(T, [0, 1, 2047, 2048, 2049, 16383, T - 2, T - 1], n_random=0, seed=3),
+                      np.random.default_rng(3).choice(T, 2048, replace=False))
     qi = ind["q_idx"].cpu()
     check_rows(idx.cpu().numpy(), ln.cpu().numpy(), qi, ind["k_idx"].cpu(), ind["w"].cpu(),
                start.cpu().numpy(), rows, K)
+    rows = sample_rows(T, [0, 1, 2047, 2048, 2049, 16383, T - 2, T - 1], n_random=24, seed=3)
     x = synth.mla_inputs(T, c["H"], c["Dqk"], c["Dv"], seed=4, device=DEV)
     mla_rows = np.union1d(rows, np.random.default_rng(33).choice(T, 512, replace=False))  # oracle time bounds this
     mla_full_check(x["q"], x["kv"], x["dout"], idx, c["scale"], ln=ln, rows=mla_rows, chunk=(T - 32, T))
@@ -128,8 +150,7 @@ def test_full_nope_S16384_H8_K2051_and_query_chunks():
     idx = causal_idx_gpu(torch.zeros(T, dtype=torch.int32), K, 5, T)
     rows = np.union1d(sample_rows(T, [0, 1, 2050, 2051, 2052, T - 1], n_random=0, seed=5),
                       np.random.default_rng(5).choice(T, 2048, replace=False))
-    out, lse, lo, dq, dkv = mla_full_check(x["q"], x["kv"], x["dout"], idx, c["scale"], rows=rows,
-                                           chunk=(8000, 8064))
+    out, lse, lo, dq, dkv = mla_full_check(x["q"], x["kv"], x["dout"], idx, c["scale"], rows=rows, every_row=True)
     acc = None
     for a in range(0, T, 4096):
         b = min(T, a + 4096)

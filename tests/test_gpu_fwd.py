@@ -1,4 +1,7 @@
-"""Sparse MLA forward: CUDA path (through the C ABI) vs the fp64 oracle."""
+"""Sparse MLA forward: CUDA path (through the C ABI) vs the fp64 oracle.
+
+Every case runs with and without the request for O's residual (out_lo);
+the residual request must not change out or lse."""
 import numpy as np
 import pytest
 import torch
@@ -25,20 +28,25 @@ def make_case(nrows, pos0, H, Dqk, K, seed, Tk=None):
     return q, kv, dout, idx
 
 
-def run_fwd(q, kv, idx, scale, ln=None):
+def run_fwd(q, kv, idx, scale, ln=None, with_lo=False):
     ws = torch.zeros(1 << 12, dtype=torch.uint8, device=DEV)
-    out, lse = dsa.dsa_sparse_mla_fwd(q.to(DEV), kv.to(DEV), idx.to(DEV), scale,
-                                      topk_len=None if ln is None else ln.to(DEV), workspace=ws)
+    res = dsa.dsa_sparse_mla_fwd(q.to(DEV), kv.to(DEV), idx.to(DEV), scale,
+                                 topk_len=None if ln is None else ln.to(DEV), workspace=ws,
+                                 out_lo=True if with_lo else None)
     status = dsa.dsa_read_device_status(ws)
-    return out.cpu(), lse.cpu(), status
+    return res[0].cpu(), res[1].cpu(), status
 
 
 def check(q, kv, idx, scale, ln=None, expect_status=0):
-    out, lse, status = run_fwd(q, kv, idx, scale, ln)
-    assert status == expect_status
     ref_o, ref_l = oracle.sparse_mla_fwd(q, kv, idx, scale, len_rows=ln)
-    assert_close(out, ref_o, "out")
-    assert_lse(lse, ref_l)
+    res = []
+    for with_lo in (False, True):
+        out, lse, status = run_fwd(q, kv, idx, scale, ln, with_lo)
+        assert status == expect_status
+        assert_close(out, ref_o, f"out (with_lo={with_lo})")
+        assert_lse(lse, ref_l)
+        res.append((out, lse))
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
     return out, lse
 
 

@@ -43,13 +43,13 @@ def check_rows(gidx, glen, q_idx, k_idx, w, start, rows, K):
         diff = sorted(set(sel.tolist()) ^ set(ref_idx[r, :n].tolist()))
         if diff:
             swaps += len(diff) // 2
-            pr = np.full(len(diff) + 1, r)
-            pk = np.array(diff + [int(ref_idx[r, :n][0])])
-            sc, mag = oracle.indexer_scores(q_idx[rows], k_idx, w[rows], pr, pk, with_magnitude=True)
-            # magnitude of the n-th best key's score
-            kth_key = [s for s in ref_idx[r, :n] if True]
-            kth_sc, kth_mag = oracle.indexer_scores(q_idx[rows], k_idx, w[rows], np.full(n, r),
-                                                    np.array(kth_key), with_magnitude=True)
+            qt, wt = q_idx[[t]], w[[t]]  # this row only
+            sc, mag = oracle.indexer_scores(qt, k_idx, wt, np.zeros(len(diff), np.int64), np.array(diff),
+                                            with_magnitude=True)
+            # magnitude of the n-th best key's score (the lowest-scoring key the oracle selects)
+            sel_ref = np.asarray(ref_idx[r, :n])
+            kth_sc, kth_mag = oracle.indexer_scores(qt, k_idx, wt, np.zeros(n, np.int64), sel_ref,
+                                                    with_magnitude=True)
             j = int(np.argmin(kth_sc))
             for d in range(len(diff)):
                 assert abs(sc[d] - kth[r]) <= GAMMA * (mag[d] + kth_mag[j]), \
