@@ -62,6 +62,10 @@ def _load():
             lib.oracle_sparse_mla_fwd.restype = None
             lib.oracle_sparse_mla_bwd.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, P, P, P, P, P]
             lib.oracle_sparse_mla_bwd.restype = None
+            lib.oracle_attn_slot_prob.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, P]
+            lib.oracle_attn_slot_prob.restype = None
+            lib.oracle_indexer_kl.argtypes = [P, P, P, P, P, P, I, I, I, I, I, ctypes.c_double, P, P, P, P]
+            lib.oracle_indexer_kl.restype = None
             _lib = lib
     return _lib
 
@@ -222,3 +226,41 @@ def sparse_mla_bwd(q_rows, kv, idx_rows, dout_rows, scale: float, Dv: int = 512,
                                   _p(mag))
     res = (dq, dkv) + ((d_sink,) if sk is not None else ()) + ((mag,) if with_dq_magnitude else ())
     return res
+
+
+def attn_slot_prob(q_rows, kv, idx_rows, scale: float, Dv: int = 512, len_rows=None, sink=None):
+    """Head-averaged sparse-MLA softmax weight of every slot of the given rows -> prob [n, K] (fp64)."""
+    q = _f64(q_rows)
+    kvf = _f64(kv).reshape(kv.shape[0], -1)
+    idx = _i32(idx_rows)
+    ln = None if len_rows is None else _i32(len_rows)
+    n, H, Dqk = q.shape
+    K = idx.shape[1]
+    sk = None if sink is None else _f64(sink).reshape(H)
+    prob = np.zeros((n, K), np.float64)
+    _load().oracle_attn_slot_prob(_p(q), _p(kvf), _p(idx), _p(ln), n, kvf.shape[0], H, Dqk, Dv, K, float(scale),
+                                  _p(sk), _p(prob))
+    return prob
+
+
+def indexer_kl(q_idx_rows, k_idx, w_rows, idx_rows, prob_rows, coeff: float, len_rows=None, dk=None):
+    """Indexer KL loss of the given rows over their selected slots -> (kl [n], dq_idx [n,Hi,Di], dw [n,Hi],
+    dk [Tk,Di]) in fp64; prob_rows [n, K] is the attention's slot probability (normalised per row here).
+    dk accumulates the contributions of exactly these rows (pass an existing array to keep adding)."""
+    q = _f64(q_idx_rows)
+    k = _f64(k_idx)
+    w = _f64(w_rows)
+    idx = _i32(idx_rows)
+    pr = _f64(prob_rows)
+    ln = None if len_rows is None else _i32(len_rows)
+    n, Hi, Di = q.shape
+    K = idx.shape[1]
+    kl = np.zeros(n, np.float64)
+    dq = np.zeros((n, Hi, Di), np.float64)
+    dw = np.zeros((n, Hi), np.float64)
+    if dk is None:
+        dk = np.zeros((k.shape[0], Di), np.float64)
+    assert dk.dtype == np.float64 and dk.flags.c_contiguous
+    _load().oracle_indexer_kl(_p(q), _p(k), _p(w), _p(idx), _p(ln), _p(pr), n, k.shape[0], Hi, Di, K, float(coeff),
+                              _p(kl), _p(dq), _p(dw), _p(dk))
+    return kl, dq, dw, dk

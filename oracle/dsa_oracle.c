@@ -408,3 +408,129 @@ void oracle_sparse_mla_bwd(const double *q_rows, const double *kv, const int32_t
   free(P);
   free(dS);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Head-averaged attention probability per selected slot                      */
+/* [DSA-blog] "How DSA works": the indexer's KL loss aligns its score         */
+/* distribution with the main attention's, and "Why DSA needs fused kernels": */
+/* the attention-score tensor the KL loss consumes.  Reading: for row t and   */
+/* slot j, prob[t,j] = (1/H) sum_h P[t,h,j] with P the sparse-MLA softmax      */
+/* weights of the forward above (0 for an invalid slot).                      */
+/* ------------------------------------------------------------------------ */
+void oracle_attn_slot_prob(const double *q_rows, const double *kv, const int32_t *idx_rows,
+                           const int32_t *len_rows, int nrows, int Tk, int H, int Dqk, int Dv, int K,
+                           double scale, const double *sink, double *prob /*[nrows,K]*/) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < nrows; ++r) {
+    double *o_r = (double *)malloc(sizeof(double) * (size_t)H * Dv);
+    double *lse_r = (double *)malloc(sizeof(double) * (size_t)H);
+    double *p_r = (double *)malloc(sizeof(double) * (size_t)H * (K > 0 ? K : 1));
+    fwd_row(q_rows + (size_t)r * H * Dqk, kv, idx_rows + (size_t)r * K, len_rows, r, Tk, H, Dqk, Dv, K, scale,
+            sink, o_r, lse_r, p_r);
+    for (int j = 0; j < K; ++j) {
+      double s = 0.0;
+      for (int h = 0; h < H; ++h) s += p_r[(size_t)h * K + j];
+      prob[(size_t)r * K + j] = s / H;
+    }
+    free(o_r);
+    free(lse_r);
+    free(p_r);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Indexer KL auxiliary loss over the selected slots ("sparse formulation")   */
+/* [DSA-blog] "How DSA works" (the indexer emits an auxiliary KL loss that     */
+/* aligns its score distribution with the main attention's; its graph is      */
+/* independent of the main model's) and "Accelerating ... training results"   */
+/* (indexer loss, sparse formulation, coefficient 0.001).  The pages print no */
+/* formula.  Reading, per row t over its valid slot set J:                    */
+/*   I_j  = score(t, idx_j)            (the indexer score above)              */
+/*   q_j  = exp(I_j) / sum_J exp(I)    (the indexer's distribution)           */
+/*   p_j  = prob[t,j] / sum_J prob      (the attention's, a constant: no       */
+/*                                       gradient reaches the main model)     */
+/*   kl[t] = sum_{j in J, p_j > 0} p_j (log p_j - log q_j)                    */
+/* and with g_j = coeff (q_j - p_j) = d(coeff kl[t]) / dI_j:                  */
+/*   dw[t,h]      = sum_j g_j max(0, s_hj),      s_hj = <q_idx[t,h], k[idx_j]> */
+/*   dq_idx[t,h]  = sum_j g_j w[t,h] [s_hj > 0] k[idx_j]                      */
+/*   dk[idx_j]   += sum_h g_j w[t,h] [s_hj > 0] q_idx[t,h]                    */
+/* (the derivative of max(0, s) is taken as 0 at s = 0).  A row with no valid */
+/* slot, or whose probabilities sum to 0, has kl = 0 and no gradient.         */
+/* dk is added to (rows accumulate, as query chunks do).                      */
+/* ------------------------------------------------------------------------ */
+void oracle_indexer_kl(const double *q_rows /*[n,Hi,Di]*/, const double *k /*[Tk,Di]*/,
+                       const double *w_rows /*[n,Hi]*/, const int32_t *idx_rows /*[n,K]*/,
+                       const int32_t *len_rows, const double *prob_rows /*[n,K]*/, int nrows, int Tk, int Hi,
+                       int Di, int K, double coeff, double *kl /*[n]*/, double *dq /*[n,Hi,Di]*/,
+                       double *dw /*[n,Hi]*/, double *dk /*[Tk,Di], added to*/) {
+  double *gk = (double *)calloc((size_t)nrows * (K > 0 ? K : 1) * Hi, sizeof(double)); /* g_j w_h [s>0] */
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < nrows; ++r) {
+    const double *qt = q_rows + (size_t)r * Hi * Di, *wt = w_rows + (size_t)r * Hi;
+    const int32_t *ir = idx_rows + (size_t)r * K;
+    double *dqt = dq + (size_t)r * Hi * Di, *dwt = dw + (size_t)r * Hi;
+    for (int x = 0; x < Hi * Di; ++x) dqt[x] = 0.0;
+    for (int h = 0; h < Hi; ++h) dwt[h] = 0.0;
+    kl[r] = 0.0;
+    double *I = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    double imax = -INFINITY, psum = 0.0;
+    int nvalid = 0;
+    for (int j = 0; j < K; ++j) {
+      if (!slot_valid(ir, len_rows, r, j, Tk)) continue;
+      I[j] = indexer_score(qt, k + (size_t)ir[j] * Di, wt, Hi, Di, NULL);
+      if (I[j] > imax) imax = I[j];
+      psum += prob_rows[(size_t)r * K + j];
+      ++nvalid;
+    }
+    if (nvalid == 0 || !(psum > 0.0)) {
+      free(I);
+      continue;
+    }
+    double z = 0.0;
+    for (int j = 0; j < K; ++j)
+      if (slot_valid(ir, len_rows, r, j, Tk)) z += exp(I[j] - imax);
+    const double logz = imax + log(z);
+    double acc = 0.0;
+    for (int j = 0; j < K; ++j) {
+      if (!slot_valid(ir, len_rows, r, j, Tk)) continue;
+      const double logq = I[j] - logz, p = prob_rows[(size_t)r * K + j] / psum;
+      if (p > 0.0) acc += p * (log(p) - logq);
+      const double g = coeff * (exp(logq) - p);
+      const double *kj = k + (size_t)ir[j] * Di;
+      for (int h = 0; h < Hi; ++h) {
+        double s = 0.0;
+        for (int d = 0; d < Di; ++d) s += qt[(size_t)h * Di + d] * kj[d];
+        dwt[h] += g * (s > 0.0 ? s : 0.0);
+        const double m = (s > 0.0) ? g * wt[h] : 0.0;
+        gk[((size_t)r * K + j) * Hi + h] = m;
+        for (int d = 0; d < Di; ++d) dqt[(size_t)h * Di + d] += m * kj[d];
+      }
+    }
+    kl[r] = acc;
+    free(I);
+  }
+  /* key gradient: fixed order over (row, slot, head) per channel range, as the MLA backward */
+#pragma omp parallel
+  {
+    int nth = 1, id = 0;
+#ifdef _OPENMP
+    nth = omp_get_num_threads();
+    id = omp_get_thread_num();
+#endif
+    const int d0 = (int)((int64_t)Di * id / nth), d1 = (int)((int64_t)Di * (id + 1) / nth);
+    for (int r = 0; r < nrows; ++r) {
+      const int32_t *ir = idx_rows + (size_t)r * K;
+      for (int j = 0; j < K; ++j) {
+        if (!slot_valid(ir, len_rows, r, j, Tk)) continue;
+        double *dst = dk + (size_t)ir[j] * Di;
+        for (int h = 0; h < Hi; ++h) {
+          const double m = gk[((size_t)r * K + j) * Hi + h];
+          if (m == 0.0) continue;
+          const double *qh = q_rows + ((size_t)r * Hi + h) * Di;
+          for (int d = d0; d < d1; ++d) dst[d] += m * qh[d];
+        }
+      }
+    }
+  }
+  free(gk);
+}

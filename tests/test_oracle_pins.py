@@ -554,3 +554,92 @@ def test_sink_gradient_central_finite_differences():
         fa = np.sum(oracle.sparse_mla_fwd(q, kv, idx, 0.45, Dv=4, sink=a)[0] * dout)
         fb = np.sum(oracle.sparse_mla_fwd(q, kv, idx, 0.45, Dv=4, sink=b)[0] * dout)
         np.testing.assert_allclose(dsink[h], (fa - fb) / (2 * eps), rtol=1e-6, atol=1e-9)
+
+
+# --------------------------------------------------------------------------
+# attention slot probability and the indexer KL loss (reading: see the oracle)
+# --------------------------------------------------------------------------
+def test_attn_slot_prob_is_the_head_mean_of_the_dense_softmax():
+    q, kv, dout, idx = rand_case(seed=41)
+    prob = oracle.attn_slot_prob(q, kv, idx, 0.3, Dv=8)
+    qt, kt = torch.tensor(q), torch.tensor(kv)
+    s = 0.3 * torch.einsum("thd,sd->ths", qt, kt)
+    mask = torch.as_tensor(mask_from_idx(idx, kv.shape[0]))
+    p = torch.softmax(s.masked_fill(~mask[:, None, :], float("-inf")), dim=-1).nan_to_num(0.0).mean(dim=1)
+    ref = np.zeros_like(prob)
+    for t in range(idx.shape[0]):
+        for j in range(idx.shape[1]):
+            if idx[t, j] >= 0:
+                ref[t, j] = float(p[t, idx[t, j]])
+    np.testing.assert_allclose(prob, ref, rtol=1e-12, atol=1e-14)
+    rows = (idx >= 0).any(axis=1)
+    np.testing.assert_allclose(prob[rows].sum(axis=1), 1.0, rtol=1e-12)
+    # with a sink every row's probabilities sum to below 1 (the sink takes the rest)
+    ps = oracle.attn_slot_prob(q, kv, idx, 0.3, Dv=8, sink=np.array([0.5, 1.0, -0.5]))
+    assert np.all(ps[rows].sum(axis=1) < 1.0)
+
+
+def kl_case(seed, T=12, Hi=3, Di=10, Tk=30, K=7):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((T, Hi, Di))
+    k = rng.standard_normal((Tk, Di))
+    w = rng.uniform(-0.3, 1.0, (T, Hi))
+    idx = np.stack([np.sort(rng.choice(Tk, K, replace=False)) for _ in range(T)]).astype(np.int32)
+    idx[2, 4:] = -1  # fewer valid slots
+    idx[5, 0] = -1   # a hole
+    prob = rng.uniform(0.0, 1.0, (T, K)) * (idx >= 0)
+    return q, k, w, idx, prob
+
+
+def test_indexer_kl_matches_torch_autograd_of_the_dense_definition():
+    q, k, w, idx, prob = kl_case(51)
+    coeff = 0.37
+    kl, dq, dw, dk = oracle.indexer_kl(q, k, w, idx, prob, coeff)
+    qt = torch.tensor(q, requires_grad=True)
+    kt = torch.tensor(k, requires_grad=True)
+    wt = torch.tensor(w, requires_grad=True)
+    valid = torch.as_tensor(idx >= 0)
+    gidx = torch.as_tensor(np.where(idx >= 0, idx, 0)).long()
+    kg = kt[gidx]                                                      # [T, K, Di]
+    s = torch.einsum("thd,tjd->thj", qt, kg)
+    I = torch.einsum("th,thj->tj", wt, torch.relu(s))
+    logq = torch.log_softmax(I.masked_fill(~valid, float("-inf")), dim=1)
+    p = torch.tensor(prob) / torch.tensor(prob).sum(dim=1, keepdim=True)
+    terms = torch.where(p > 0, p * (torch.log(torch.where(p > 0, p, 1.0)) - logq), torch.zeros_like(p))
+    kl_t = terms.sum(dim=1)
+    (coeff * kl_t.sum()).backward()
+    np.testing.assert_allclose(kl, kl_t.detach().numpy(), rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(dq, qt.grad.numpy(), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(dw, wt.grad.numpy(), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), rtol=1e-10, atol=1e-13)
+
+
+def test_indexer_kl_closed_forms():
+    q, k, w, idx, _ = kl_case(52)
+    # the attention's distribution equal to the indexer's (softmax of the numpy scores): zero loss and gradient
+    I = np.einsum("th,thj->tj", w, np.maximum(np.einsum("thd,tjd->thj", q, k[np.where(idx >= 0, idx, 0)]), 0.0))
+    e = np.where(idx >= 0, np.exp(I - I.max(axis=1, keepdims=True)), 0.0)
+    kl, dq, dw, dk = oracle.indexer_kl(q, k, w, idx, e / e.sum(axis=1, keepdims=True), 1.0)
+    np.testing.assert_allclose(kl, 0.0, atol=1e-12)
+    for g in (dq, dw, dk):
+        np.testing.assert_allclose(g, 0.0, atol=1e-12)
+    # one valid slot: p = q = 1, nothing to learn; an empty row: zero
+    idx1 = np.full_like(idx, -1)
+    idx1[:, 3] = idx[:, 3].clip(min=0)
+    idx1[4, :] = -1
+    kl1, dq1, dw1, dk1 = oracle.indexer_kl(q, k, w, idx1, np.ones(idx.shape), 1.0)
+    assert np.all(kl1 == 0.0) and np.all(dq1 == 0.0) and np.all(dw1 == 0.0) and np.all(dk1 == 0.0)
+
+
+def test_indexer_kl_gradient_central_finite_differences_in_w():
+    q, k, w, idx, prob = kl_case(53, T=6)
+    _, _, dw, _ = oracle.indexer_kl(q, k, w, idx, prob, 0.5)
+    eps = 1e-6
+    for t in range(6):
+        for h in range(3):
+            a, b = w.copy(), w.copy()
+            a[t, h] += eps
+            b[t, h] -= eps
+            fa = 0.5 * oracle.indexer_kl(q, k, a, idx, prob, 1.0)[0].sum()
+            fb = 0.5 * oracle.indexer_kl(q, k, b, idx, prob, 1.0)[0].sum()
+            np.testing.assert_allclose(dw[t, h], (fa - fb) / (2 * eps), rtol=1e-6, atol=1e-9)
