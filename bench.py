@@ -329,6 +329,8 @@ def run_cuda(args, rank, world, local):
     if not args.no_e2e:
         e2e = run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, f_fwd + f_bwd, world)
     cp = None if args.no_cp else run_cp_indexer(args, dsa, torch, dev, stream, ind, topk_idx, topk_len)
+    kl_path = None if args.no_kl else run_kl_path(args, dsa, torch, dev, stream, ind, mla, topk_idx, topk_len, out,
+                                                   out_lo, lse, dq, dkv, ws_b, bwd_ms, n_valid)
     workloads = None
     if not args.no_workloads:
         del ws_b
@@ -355,6 +357,7 @@ def run_cuda(args, rank, world, local):
         "gpu_launches": 3 * args.steps,  # indexer, forward, backward per step
         "e2e": e2e,
         "cp_indexer": cp,
+        "kl_path": kl_path,
         "workloads": workloads,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -366,6 +369,47 @@ def run_cuda(args, rank, world, local):
                                           f"TFLOP/s; indexer {r['idx_tokens_per_s']:.2f} tokens/s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_kl_path(args, dsa, torch, dev, stream, ind, mla, topk_idx, topk_len, out, out_lo, lse, dq, dkv, ws_b,
+                bwd_ms, n_valid):
+    """The indexer KL auxiliary loss on the same selection: the backward with its slot-probability output
+    (the extra cost over the plain backward), then the KL kernel (loss and gradients).  CUDA events on the
+    launching stream, median over the timed steps."""
+    prob = torch.empty(S, K, dtype=torch.float32, device=dev)
+    ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
+    kl = torch.empty(S, dtype=torch.float32, device=dev)
+    dqi = torch.empty_like(ind["q_idx"])
+    dw = torch.empty_like(ind["w"])
+    dk = torch.empty(S, DI, dtype=torch.float32, device=dev)
+
+    def bwd():
+        dsa.dsa_sparse_mla_bwd(mla["q"], mla["kv"], topk_idx, SCALE, out, lse, mla["dout"], topk_len=topk_len, dq=dq,
+                               dkv_accum=dkv, workspace=ws_b, out_lo=out_lo, attn_prob=prob)
+
+    def klk():
+        dsa.dsa_indexer_kl(ind["q_idx"], ind["k_idx"], ind["w"], topk_idx, prob, 0.001, topk_len=topk_len, kl=kl,
+                           dq_idx=dqi, dw=dw, dk_idx_accum=dk, workspace=ws)
+
+    for _ in range(args.warmup):
+        bwd()
+        klk()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for e in ev:
+        e[0].record(stream)
+        bwd()
+        e[1].record(stream)
+        klk()
+        e[2].record(stream)
+    torch.cuda.synchronize(dev)
+    if dsa.dsa_read_device_status(ws) != 0 or dsa.dsa_read_device_status(ws_b) != 0:
+        raise RuntimeError("device status after the KL path")
+    b_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    k_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    f_alg = 3 * 2.0 * HI * DI * n_valid  # scores, dq_idx and dk_idx products; the kernel also recomputes the scores
+    return {"bwd_with_slot_prob_ms": round(b_ms, 3), "bwd_ms": round(bwd_ms, 3),
+            "indexer_kl_ms": round(k_ms, 3), "indexer_kl_tflops": round(f_alg / (k_ms * 1e-3) / 1e12, 2),
+            "note": "loss coefficient 0.001; kl per row, dq_idx, dw and the fp32 dk_idx accumulator"}
 
 
 def run_cp_indexer(args, dsa, torch, dev, stream, ind, topk_idx, topk_len, ranks=2):
@@ -627,6 +671,7 @@ def main():
     ap.add_argument("--no-cp", action="store_true", help="skip the context-parallel indexer line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the V3.2 and NoPE workload timings")
+    ap.add_argument("--no-kl", action="store_true", help="skip the indexer KL loss path")
     ap.add_argument("--workloads", default=None,
                     help="comma-separated workload names (tiny,v32,idx32k,nope,thd): one line per workload "
                          "instead of the benchmark line")

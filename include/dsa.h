@@ -172,6 +172,42 @@ dsa_status_t dsa_indexer_topk_with_scores(const dsa_bf16_t* q_idx, const dsa_bf1
                                           size_t workspace_bytes, dsa_stream_t stream);
 
 /*
+ * dsa_indexer_kl -- the indexer's KL auxiliary loss over each row's selected
+ * slots, and its gradient.
+ * Source: [DSA-blog] "How DSA works" (the indexer emits an auxiliary KL loss
+ * that aligns its score distribution with the main attention's; its graph is
+ * independent of the main model's) and the training-results section (indexer
+ * loss, sparse formulation, coefficient 0.001).  The pages print no formula;
+ * reading taken, per row t over its valid slots J (as in the sparse MLA calls):
+ *   I_j = score(t, topk_idx[t,j])  (the indexer score of dsa_indexer_topk)
+ *   q_j = softmax_J(I),  p_j = attn_prob[t,j] / sum_J attn_prob[t,:]
+ *   kl[t] = sum_{j: p_j > 0} p_j (log p_j - log q_j)
+ * with g_j = coeff (q_j - p_j), s_hj = <q_idx[t,h], k_idx[idx_j]> and
+ * m_hj = g_j w[t,h] [s_hj > 0]:
+ *   dw[t,h] = sum_j g_j max(0, s_hj),  dq_idx[t,h,:] = sum_j m_hj k_idx[idx_j,:],
+ *   dk_idx_accum[idx_j,:] += sum_h m_hj q_idx[t,h,:].
+ * A row with no valid slot, or whose attn_prob sums to 0, gets kl = 0 and no
+ * gradient.  The attention side is a constant (no gradient reaches it).
+ *  q_idx, k_idx, head_weights  as dsa_indexer_topk (Hi in [1, 64], Di = 128)
+ *  topk_idx     device int32 [T, K], K in [1, 4096];  topk_len device int32 [T] or NULL
+ *  attn_prob    device fp32 [T, K]: e.g. the attn_prob output of dsa_sparse_mla_bwd
+ *  coeff        the loss coefficient (the pages train with 0.001); the gradients
+ *               are those of coeff * sum_t kl[t]
+ *  kl           device fp32 [T] (out);  dq_idx device bf16 [T, Hi, Di] (out)
+ *  dw           device fp32 [T, Hi] (out)
+ *  dk_idx_accum device fp32 [T_k, Di]: zeroed first when accumulate == 0
+ *  workspace    >= dsa_indexer_kl_workspace_size() bytes
+ * Indices outside [-1, T_k) are masked and reported through the device error
+ * word.  Summation order of dk_idx_accum across rows is not deterministic.
+ */
+size_t dsa_indexer_kl_workspace_size(int32_t T, int32_t K);
+dsa_status_t dsa_indexer_kl(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
+                            const int32_t* topk_idx, const int32_t* topk_len, const float* attn_prob, int32_t T,
+                            int32_t T_k, int32_t Hi, int32_t Di, int32_t K, float coeff, float* kl,
+                            dsa_bf16_t* dq_idx, float* dw, float* dk_idx_accum, int32_t accumulate,
+                            void* workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+/*
  * dsa_sparse_mla_fwd -- absorbed sparse MLA forward (MQA over one latent KV).
  * Source: [DSA-blog] "How DSA works" and "Why DSA needs fused kernels";
  * [cudnn_dsa] cudnn_sparse_attention / _CudnnSparseAttention.forward (q
@@ -232,6 +268,10 @@ dsa_status_t dsa_sparse_mla_fwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const
  *                 added to when accumulate == 1 (query chunks)
  *  d_sink         device fp32 [H] or NULL (needs attn_sink): zeroed first when
  *                 accumulate == 0, added to when accumulate == 1
+ *  attn_prob      device fp32 [T, K] (out) or NULL: the head-averaged attention
+ *                 probability of every slot, (1/H) sum_h P[t,h,j] (0 for an
+ *                 invalid slot), the target distribution of dsa_indexer_kl;
+ *                 computed from the P the backward already forms
  *  dkv_bf16       device bf16 [T_k, Dqk] (out, rounded copy of dkv_accum) or NULL
  *  workspace      >= dsa_sparse_mla_bwd_workspace_size(T, H, K) bytes: the
  *                 error word, 256 scratch-slot flags, D (T*H fp32) and the
@@ -248,8 +288,8 @@ dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t* kv, const
                                 int32_t Dv, int32_t K, float softmax_scale, const float* attn_sink,
                                 const dsa_bf16_t* out, const dsa_bf16_t* out_lo, const float* lse,
                                 const dsa_bf16_t* dout, dsa_bf16_t* dq, float* dkv_accum, float* d_sink,
-                                int32_t accumulate, dsa_bf16_t* dkv_bf16, void* workspace, size_t workspace_bytes,
-                                dsa_stream_t stream);
+                                float* attn_prob, int32_t accumulate, dsa_bf16_t* dkv_bf16, void* workspace,
+                                size_t workspace_bytes, dsa_stream_t stream);
 
 /*
  * dsa_sparse_mla_bwd_noalloc -- dsa_sparse_mla_bwd without a caller workspace.
@@ -280,7 +320,8 @@ dsa_status_t dsa_sparse_mla_bwd_noalloc(const dsa_bf16_t* q, const dsa_bf16_t* k
                                         int32_t Dv, int32_t K, float softmax_scale, const float* attn_sink,
                                         const dsa_bf16_t* out, const dsa_bf16_t* out_lo, const float* lse,
                                         const dsa_bf16_t* dout, dsa_bf16_t* dq, float* dkv_accum, float* d_sink,
-                                        int32_t accumulate, dsa_bf16_t* dkv_bf16, dsa_stream_t stream);
+                                        float* attn_prob, int32_t accumulate, dsa_bf16_t* dkv_bf16,
+                                        dsa_stream_t stream);
 /*
  * dsa_sparse_mla_bwd_noalloc_read_status -- the no-alloc backward's device
  * error word: synchronise `stream`, read and clear the word in the built-in

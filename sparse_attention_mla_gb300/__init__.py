@@ -28,6 +28,7 @@ __all__ = [
     "dsa_indexer_topk",
     "dsa_indexer_topk_cp",
     "dsa_indexer_topk_with_scores",
+    "dsa_indexer_kl",
     "dsa_sparse_mla_fwd",
     "dsa_sparse_mla_bwd",
     "dsa_sparse_mla_bwd_noalloc",
@@ -105,14 +106,19 @@ def load_library(path: str | None = None):
         lib.dsa_sparse_mla_bwd_workspace_size.argtypes = [_I, _I, _I]
         lib.dsa_sparse_mla_bwd_workspace_size.restype = _SZ
         lib.dsa_sparse_mla_bwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P,
-                                           _P, _I, _P, _P, _SZ, _P]
+                                           _P, _P, _I, _P, _P, _SZ, _P]
         lib.dsa_read_device_status.argtypes = [_P, _P, _P]
+        lib.dsa_indexer_kl_workspace_size.argtypes = [_I, _I]
+        lib.dsa_indexer_kl_workspace_size.restype = _SZ
+        lib.dsa_indexer_kl.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _P, _SZ,
+                                       _P]
+        lib.dsa_indexer_kl.restype = ctypes.c_int
         lib.dsa_set_wait_limit_cycles.argtypes = [ctypes.c_int64]
         lib.dsa_set_wait_limit_cycles.restype = ctypes.c_int64
         lib.dsa_sparse_mla_bwd_noalloc_max_topk.restype = _I
         lib.dsa_sparse_mla_bwd_noalloc_max_topk.argtypes = []
         lib.dsa_sparse_mla_bwd_noalloc.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P,
-                                                   _P, _P, _P, _I, _P, _P]
+                                                   _P, _P, _P, _P, _I, _P, _P]
         lib.dsa_sparse_mla_bwd_noalloc.restype = ctypes.c_int
         lib.dsa_sparse_mla_bwd_noalloc_read_status.argtypes = [_P, _P]
         lib.dsa_sparse_mla_bwd_noalloc_read_status.restype = ctypes.c_int
@@ -291,6 +297,46 @@ def dsa_indexer_topk_with_scores(q_idx, k_idx, head_weights, seq_start, K: int, 
     return topk_idx, topk_len, scores
 
 
+def dsa_indexer_kl(q_idx, k_idx, head_weights, topk_idx, attn_prob, coeff: float, topk_len=None, kl=None,
+                   dq_idx=None, dw=None, dk_idx_accum=None, accumulate: bool = False, workspace=None):
+    """Indexer KL auxiliary loss over each row's selected slots and its gradient -> (kl fp32 [T],
+    dq_idx bf16 [T,Hi,Di], dw fp32 [T,Hi], dk_idx_accum fp32 [T_k,Di]); the gradients are those of
+    coeff * sum_t kl[t].  attn_prob: fp32 [T, K], e.g. from dsa_sparse_mla_bwd(attn_prob=True)."""
+    lib = load_library()
+    _need(q_idx, "q_idx", torch.bfloat16, 3)
+    dev = q_idx.device
+    _need(k_idx, "k_idx", torch.bfloat16, 2, dev)
+    _need(head_weights, "head_weights", torch.float32, 2, dev)
+    _need(topk_idx, "topk_idx", torch.int32, 2, dev)
+    _need(attn_prob, "attn_prob", torch.float32, 2, dev)
+    if topk_len is not None:
+        _need(topk_len, "topk_len", torch.int32, 1, dev)
+    T, Hi, Di = q_idx.shape
+    Tk = k_idx.shape[0]
+    K = topk_idx.shape[1]
+    if attn_prob.shape != topk_idx.shape:
+        raise ValueError("attn_prob must have the shape of topk_idx")
+    kl = torch.empty(T, dtype=torch.float32, device=dev) if kl is None else kl
+    dq_idx = torch.empty(T, Hi, Di, dtype=torch.bfloat16, device=dev) if dq_idx is None else dq_idx
+    dw = torch.empty(T, Hi, dtype=torch.float32, device=dev) if dw is None else dw
+    if dk_idx_accum is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs an existing dk_idx_accum")
+        dk_idx_accum = torch.empty(Tk, Di, dtype=torch.float32, device=dev)
+    for t_, n_, dt_ in ((kl, "kl", torch.float32), (dq_idx, "dq_idx", torch.bfloat16), (dw, "dw", torch.float32),
+                        (dk_idx_accum, "dk_idx_accum", torch.float32)):
+        _need(t_, n_, dt_, None, dev)
+    if workspace is None:
+        workspace = torch.empty(max(int(lib.dsa_indexer_kl_workspace_size(T, K)), 256), dtype=torch.uint8,
+                                device=dev)
+    _check(lib.dsa_indexer_kl(_ptr(q_idx), _ptr(k_idx), _ptr(head_weights), _ptr(topk_idx), _ptr(topk_len),
+                              _ptr(attn_prob), T, Tk, Hi, Di, K, float(coeff), _ptr(kl), _ptr(dq_idx), _ptr(dw),
+                              _ptr(dk_idx_accum), 1 if accumulate else 0, _ptr(workspace), workspace.numel(),
+                              _stream(dev)),
+           "dsa_indexer_kl")
+    return kl, dq_idx, dw, dk_idx_accum
+
+
 def dsa_sparse_mla_fwd(q, kv, topk_idx, softmax_scale: float, topk_len=None, out=None, lse=None,
                        workspace=None, Dv: int = 512, out_lo=None, attn_sink=None):
     """Sparse MLA forward -> (out bf16 [T,H,Dv], lse fp32 [T,H]), or (out, lse, out_lo) when
@@ -331,11 +377,13 @@ def dsa_sparse_mla_fwd(q, kv, topk_idx, softmax_scale: float, topk_len=None, out
 
 def dsa_sparse_mla_bwd(q, kv, topk_idx, softmax_scale: float, out, lse, dout, topk_len=None, dq=None,
                        dkv_accum=None, accumulate: bool = False, dkv_bf16=None, workspace=None, out_lo=None,
-                       attn_sink=None, d_sink=None):
+                       attn_sink=None, d_sink=None, attn_prob=None):
     """Sparse MLA backward -> (dq bf16 [T,H,Dqk], dkv_accum fp32 [T_k,Dqk], dkv_bf16 or None), and
     d_sink fp32 [H] as a fourth result when attn_sink is given (d_sink: an existing tensor to fill,
     or to add to with accumulate=True).
-    out_lo: the precise forward's residual (D then uses the fp32 output)."""
+    out_lo: the forward's residual of O (D then uses the fp32 output).
+    attn_prob: fp32 [T, K] tensor (or True to allocate one) that receives the head-averaged
+    attention probability of every slot; it is then returned as the last result."""
     lib = load_library()
     _need(q, "q", torch.bfloat16, 3)
     dev = q.device
@@ -370,13 +418,20 @@ def dsa_sparse_mla_bwd(q, kv, topk_idx, softmax_scale: float, out, lse, dout, to
                 raise ValueError("accumulate=True needs an existing d_sink")
             d_sink = torch.empty(H, dtype=torch.float32, device=dev)
         _need(d_sink, "d_sink", torch.float32, 1, dev)
+    want_prob = attn_prob is not None and attn_prob is not False
+    if attn_prob is True:
+        attn_prob = torch.empty(T, K, dtype=torch.float32, device=dev)
+    if want_prob:
+        _need(attn_prob, "attn_prob", torch.float32, 2, dev)
     ws, wsb = _workspace("bwd", T, H, dev, workspace, K)
     _check(lib.dsa_sparse_mla_bwd(_ptr(q), _ptr(kv), _ptr(topk_idx), _ptr(topk_len), T, Tk, H, Dqk, Dv, K,
                                   float(softmax_scale), _ptr(attn_sink), _ptr(out), _ptr(out_lo), _ptr(lse),
                                   _ptr(dout), _ptr(dq), _ptr(dkv_accum), _ptr(d_sink),
-                                  1 if accumulate else 0, _ptr(dkv_bf16), _ptr(ws), wsb, _stream(dev)),
+                                  _ptr(attn_prob if want_prob else None), 1 if accumulate else 0, _ptr(dkv_bf16),
+                                  _ptr(ws), wsb, _stream(dev)),
            "dsa_sparse_mla_bwd")
-    return (dq, dkv_accum, dkv_bf16) if attn_sink is None else (dq, dkv_accum, dkv_bf16, d_sink)
+    res = (dq, dkv_accum, dkv_bf16) if attn_sink is None else (dq, dkv_accum, dkv_bf16, d_sink)
+    return res + (attn_prob,) if want_prob else res
 
 
 def dsa_sparse_mla_bwd_noalloc(q, kv, topk_idx, softmax_scale: float, out, lse, dout, topk_len=None, dq=None,
@@ -409,7 +464,7 @@ def dsa_sparse_mla_bwd_noalloc(q, kv, topk_idx, softmax_scale: float, out, lse, 
     _need(dkv_accum, "dkv_accum", torch.float32, 2, dev)
     _check(lib.dsa_sparse_mla_bwd_noalloc(_ptr(q), _ptr(kv), _ptr(topk_idx), _ptr(topk_len), T, Tk, H, Dqk,
                                           out.shape[2], topk_idx.shape[1], float(softmax_scale), None, _ptr(out),
-                                          _ptr(out_lo), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dkv_accum), None,
+                                          _ptr(out_lo), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dkv_accum), None, None,
                                           1 if accumulate else 0, _ptr(dkv_bf16), _stream(dev)),
            "dsa_sparse_mla_bwd_noalloc")
     return dq, dkv_accum, dkv_bf16

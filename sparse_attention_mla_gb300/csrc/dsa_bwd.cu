@@ -251,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ topk_len,
                           const float* __restrict__ lse, const float* __restrict__ delta,
                           const __nv_bfloat16* __restrict__ dout, int T, int Tk, int H, int K, float scale,
-                          __nv_bfloat16* __restrict__ dq, float* __restrict__ dkv,
+                          __nv_bfloat16* __restrict__ dq, float* __restrict__ dkv, float* __restrict__ attn_prob,
+                          float inv_heads,
                           int* __restrict__ slot_flags, uint8_t* __restrict__ ds_scratch, int tiles_per_slot,
                           int* __restrict__ err, long long wait_limit) {
   using L = Smem<DQK>;
@@ -646,6 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       const bool valid = ix >= 0 && ix < Tk;
       uint32_t ph[16], pl[16], sh[16], sl[16];
+      float psum = 0.f;  // this half's sum of P over its 32 heads (the slot probability, on request)
 #pragma unroll
       for (int h = 0; h < 32; h += 2) {
         float p0 = 0.f, p1 = 0.f, s0 = 0.f, s1 = 0.f;
@@ -659,6 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           p1 = exp2f(__uint_as_float(sv[h + 1]) * sl2e - l1);
           s0 = scale * p0 * (__uint_as_float(dv[h]) - d0);
           s1 = scale * p1 * (__uint_as_float(dv[h + 1]) - d1);
+          psum += p0 + p1;
         }
         const __nv_bfloat162 phi = __floats2bfloat162_rn(p0, p1);
         const __nv_bfloat162 shi = __floats2bfloat162_rn(s0, s1);
@@ -682,6 +685,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DS + b));
+      // head-averaged attention probability of this slot (each half of each head group adds its part)
+      if (attn_prob != nullptr && valid) atomicAdd(attn_prob + (size_t)t * K + j, psum * inv_heads);
       // ---- this warp's share of the tile's staged dKV groups (role 1 + ch) ----
       const int kix = valid ? ix : -1;
       for (int g = 0; g < NG && !aborted; ++g)
@@ -743,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int DQK>
 dsa_status_t launch(const void* kv, const void* q, const int32_t* idx, const int32_t* len, const float* lse,
                     const float* delta, const void* dout, int T, int Tk, int H, int K, float scale, void* dq,
-                    float* dkv, int* slot_flags, uint8_t* ds_scratch, int* err, cudaStream_t s) {
+                    float* dkv, float* attn_prob, int* slot_flags, uint8_t* ds_scratch, int* err, cudaStream_t s) {
   using L = Smem<DQK>;
   dsa_status_t st = configure_kernel_smem(reinterpret_cast<const void*>(sparse_mla_bwd_kernel<DQK>), L::TOTAL,
                                           "configuring sparse_mla_bwd_kernel");
@@ -752,7 +757,7 @@ dsa_status_t launch(const void* kv, const void* q, const int32_t* idx, const int
   sparse_mla_bwd_kernel<DQK><<<grid, kThreads, L::TOTAL, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(kv), reinterpret_cast<const __nv_bfloat16*>(q), idx, len, lse, delta,
       reinterpret_cast<const __nv_bfloat16*>(dout), T, Tk, H, K, scale, reinterpret_cast<__nv_bfloat16*>(dq), dkv,
-      slot_flags, ds_scratch, (K + kTile - 1) / kTile, err, wait_limit_cycles());
+      attn_prob, 1.f / (float)H, slot_flags, ds_scratch, (K + kTile - 1) / kTile, err, wait_limit_cycles());
   return cuda_check(cudaGetLastError(), "launching sparse_mla_bwd_kernel");
 }
 
@@ -787,8 +792,9 @@ static dsa_status_t run(const char* who, const dsa_bf16_t* q, const dsa_bf16_t* 
                         const int32_t* topk_len, int32_t T, int32_t T_k, int32_t H, int32_t Dqk, int32_t Dv,
                         int32_t K, float softmax_scale, const float* attn_sink, const dsa_bf16_t* out,
                         const dsa_bf16_t* out_lo, const float* lse, const dsa_bf16_t* dout, dsa_bf16_t* dq,
-                        float* dkv_accum, float* d_sink, int32_t accumulate, dsa_bf16_t* dkv_bf16, void* workspace,
-                        size_t workspace_bytes, dsa_stream_t stream, bool first = true, bool last = true) {
+                        float* dkv_accum, float* d_sink, float* attn_prob, int32_t accumulate, dsa_bf16_t* dkv_bf16,
+                        void* workspace, size_t workspace_bytes, dsa_stream_t stream, bool first = true,
+                        bool last = true) {
   if (T < 0 || T_k < 1 || H < 1 || K < 1)
     return fail(DSA_ERR_INVALID_ARGUMENT, "%s: need T >= 0, T_k >= 1, H >= 1, K >= 1 (got %d, %d, %d, %d)", who, T,
                 T_k, H, K);
@@ -823,6 +829,9 @@ static dsa_status_t run(const char* who, const dsa_bf16_t* q, const dsa_bf16_t* 
   if (!accumulate && d_sink &&
       (st = cuda_check(cudaMemsetAsync(d_sink, 0, (size_t)H * sizeof(float), s), "zeroing d_sink")))
     return st;
+  if (attn_prob && T > 0 &&
+      (st = cuda_check(cudaMemsetAsync(attn_prob, 0, (size_t)T * K * sizeof(float), s), "zeroing attn_prob")))
+    return st;
   int* err = reinterpret_cast<int*>(workspace);
   int* flags = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(workspace) + kErrorWordBytes);
   float* delta = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + kHeadBytes);
@@ -834,9 +843,9 @@ static dsa_status_t run(const char* who, const dsa_bf16_t* q, const dsa_bf16_t* 
         reinterpret_cast<const __nv_bfloat16*>(dout), delta, rows, lse, attn_sink, d_sink, H);
     if ((st = cuda_check(cudaGetLastError(), "launching bwd_delta_kernel"))) return st;
     st = (Dqk == 576) ? launch<576>(kv, q, topk_idx, topk_len, lse, delta, dout, T, T_k, H, K, softmax_scale, dq,
-                                    dkv_accum, flags, ds_scratch, err, s)
+                                    dkv_accum, attn_prob, flags, ds_scratch, err, s)
                       : launch<512>(kv, q, topk_idx, topk_len, lse, delta, dout, T, T_k, H, K, softmax_scale, dq,
-                                    dkv_accum, flags, ds_scratch, err, s);
+                                    dkv_accum, attn_prob, flags, ds_scratch, err, s);
     if (st != DSA_OK) return st;
   }
   if (dkv_bf16 && last) {
@@ -854,11 +863,11 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd(const dsa_bf16_t* q, const dsa_bf16_t
                                            int32_t Dv, int32_t K, float softmax_scale, const float* attn_sink,
                                            const dsa_bf16_t* out, const dsa_bf16_t* out_lo, const float* lse,
                                            const dsa_bf16_t* dout, dsa_bf16_t* dq, float* dkv_accum, float* d_sink,
-                                           int32_t accumulate, dsa_bf16_t* dkv_bf16, void* workspace,
-                                           size_t workspace_bytes, dsa_stream_t stream) {
+                                           float* attn_prob, int32_t accumulate, dsa_bf16_t* dkv_bf16,
+                                           void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
   return bwd::run("dsa_sparse_mla_bwd", q, kv, topk_idx, topk_len, T, T_k, H, Dqk, Dv, K, softmax_scale, attn_sink,
-                  out, out_lo, lse, dout, dq, dkv_accum, d_sink, accumulate, dkv_bf16, workspace, workspace_bytes,
-                  stream);
+                  out, out_lo, lse, dout, dq, dkv_accum, d_sink, attn_prob, accumulate, dkv_bf16, workspace,
+                  workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -957,8 +966,8 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd_noalloc(const dsa_bf16_t* q, const ds
                                                    int32_t Dqk, int32_t Dv, int32_t K, float softmax_scale,
                                                    const float* attn_sink, const dsa_bf16_t* out,
                                                    const dsa_bf16_t* out_lo, const float* lse, const dsa_bf16_t* dout,
-                                                   dsa_bf16_t* dq, float* dkv_accum, float* d_sink, int32_t accumulate,
-                                                   dsa_bf16_t* dkv_bf16, dsa_stream_t stream) {
+                                                   dsa_bf16_t* dq, float* dkv_accum, float* d_sink, float* attn_prob,
+                                                   int32_t accumulate, dsa_bf16_t* dkv_bf16, dsa_stream_t stream) {
   if (K > bwd::kNoAllocMaxTopk)
     return fail(DSA_ERR_WORKSPACE,
                 "dsa_sparse_mla_bwd_noalloc: top-k K = %d exceeds the built-in scratch limit of %d (use "
@@ -976,7 +985,8 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd_noalloc(const dsa_bf16_t* q, const ds
   const int32_t per = (int32_t)std::min<size_t>(max_pairs / (size_t)H, (size_t)INT32_MAX);
   if (T <= 0)
     return bwd::run(who, q, kv, topk_idx, topk_len, T, T_k, H, Dqk, Dv, K, softmax_scale, attn_sink, out, out_lo, lse,
-                    dout, dq, dkv_accum, d_sink, accumulate, dkv_bf16, scratch, bwd::kNoAllocScratchBytes, stream);
+                    dout, dq, dkv_accum, d_sink, attn_prob, accumulate, dkv_bf16, scratch, bwd::kNoAllocScratchBytes,
+                    stream);
   for (int32_t r0 = 0; r0 < T; r0 += per) {
     const int32_t n = std::min(per, T - r0);
     const size_t rh = (size_t)r0 * H;
@@ -984,7 +994,7 @@ extern "C" dsa_status_t dsa_sparse_mla_bwd_noalloc(const dsa_bf16_t* q, const ds
                   topk_len ? topk_len + r0 : nullptr, n, T_k, H, Dqk, Dv, K, softmax_scale, attn_sink,
                   out ? out + rh * Dv : out, out_lo ? out_lo + rh * Dv : nullptr, lse ? lse + rh : lse,
                   dout ? dout + rh * Dv : dout, dq ? dq + rh * Dqk : dq, dkv_accum, d_sink,
-                  (r0 > 0) ? 1 : accumulate, dkv_bf16, scratch, bwd::kNoAllocScratchBytes, stream, r0 == 0,
+                  attn_prob ? attn_prob + (size_t)r0 * K : nullptr, (r0 > 0) ? 1 : accumulate, dkv_bf16, scratch, bwd::kNoAllocScratchBytes, stream, r0 == 0,
                   r0 + n >= T);
     if (st != DSA_OK) return st;
   }

@@ -1,0 +1,485 @@
+// dsa_indexer_kl.cu -- the indexer's KL auxiliary loss over the selected slots
+// and its gradient, on sm_103a (tcgen05 + TMEM).
+//
+// For one query row t over its valid selected slots J (reading of the pages:
+// "Accelerating GLM-5.2 Long-Context Training with cuDNN Fused DSA Kernels
+// ...", "How DSA works" -- the indexer emits an auxiliary KL loss aligning its
+// score distribution with the main attention's, its graph independent of the
+// main model's -- and the training-results section -- sparse formulation,
+// coefficient 0.001):
+//   I_j = sum_h w[t,h] max(0, s_hj),  s_hj = <q_idx[t,h,:], k_idx[idx_j,:]>
+//   q_j = softmax_J(I),  p_j = prob[t,j] / sum_J prob   (prob: the attention's
+//         head-averaged slot probability, a constant)
+//   kl[t] = sum_{j: p_j > 0} p_j (log p_j - log q_j)
+// and with g_j = coeff (q_j - p_j) and m_hj = g_j w[t,h] [s_hj > 0]:
+//   dw[t,h] = sum_j g_j max(0, s_hj),   dq_idx[t,h,:] = sum_j m_hj k_idx[idx_j,:],
+//   dk_idx[idx_j,:] += sum_h m_hj q_idx[t,h,:].
+//
+// Design (sm_103a): one CTA per query row, 4 worker warps (one TMEM lane
+// quadrant each, one slot row per thread) and one MMA warp.  The selected
+// k_idx rows of a 128-slot tile are gathered by cp.async into 128-byte-swizzled
+// shared memory, two tiles deep (the next tile is fetched while the current
+// one is multiplied).  Pass 1: S[slot, head] = K_tile . Q^T (M = 128 slots,
+// N = 64 heads) in TMEM, the head-weighted ReLU sum per slot into shared
+// memory; then the row's softmax, KL and p normalisation.  Pass 2 gathers and
+// multiplies again, forms m_hj (bf16 hi + lo parts, so the gradients carry it
+// to about fp32) and dw, and runs two more products per tile: dQ^T[dim, head]
+// += K_tile^T . M (accumulated in TMEM over the tiles) and dK[slot, dim] =
+// M . Q.  Every thread stages its dK row (512 bytes) in shared memory and
+// reduces it into the fp32 dk_idx accumulator with one bulk reduction
+// (cp.reduce.async.bulk .add.f32), which runs while the warps go on to the
+// next tile: a few warps issuing per-thread L2 reductions could not keep up
+// with 512 bytes per slot.
+#include <cmath>
+
+#include "dsa_device.cuh"
+#include "dsa_host.h"
+
+namespace dsa {
+namespace kl {
+
+constexpr int kWorkers = 128;             // warps 0-3
+constexpr int kThreads = kWorkers + 32;   // + the MMA warp (warp 4)
+constexpr int kHeads = 64;                // indexer heads (padded)
+constexpr int kDi = 128;                  // indexer head dim
+constexpr int kTile = 128;                // slots per tile (MMA M)
+constexpr int kMaxK = 4096;
+
+constexpr int Q_CHUNK = kHeads * 128;     // 8 KiB: 64 heads x 64 dims
+constexpr int K_CHUNK = kTile * 128;      // 16 KiB: 128 slots x 64 dims
+constexpr int K_BUF = 2 * K_CHUNK;        // one gathered tile
+constexpr int DK_PITCH = kDi * 4 + 16;    // staged dK row: 512 bytes + 16 (bank spread)
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + 2 * Q_CHUNK;          // two tile buffers
+constexpr int OFF_MHI = OFF_K + 2 * K_BUF;
+constexpr int OFF_MLO = OFF_MHI + kTile * 128;
+constexpr int OFF_DKS = OFF_MLO + kTile * 128;      // [128 rows][DK_PITCH] staged dK rows
+constexpr int OFF_I = OFF_DKS + kTile * DK_PITCH;   // float [kMaxK]: indexer scores (-inf: invalid slot)
+constexpr int OFF_P = OFF_I + kMaxK * 4;            // float [kMaxK]: attention slot probabilities
+constexpr int OFF_MISC = OFF_P + kMaxK * 4;
+constexpr int M_BAR_S = 0, M_BAR_MM = 8, M_BAR_FIN = 16, M_TMEM = 32, M_NEFF = 36, M_ABORT = 40, M_ACTIVE = 44;
+constexpr int M_STATS = 48;                         // float [3]: logZ, 1/psum, (spare)
+constexpr int M_W = 64;                             // float [64]
+constexpr int M_DW = M_W + 256;                     // float [64]
+constexpr int M_RED = M_DW + 256;                   // float [4]
+constexpr int MISC = 1024;
+constexpr int TOTAL = OFF_MISC + MISC + 1024;       // + alignment slack
+static_assert(TOTAL <= 232448, "shared memory budget");
+static_assert(M_RED + 16 <= MISC, "misc layout");
+
+// Reduction over the 128 worker threads (named barrier 2); every worker gets the result.
+template <bool MAX>
+__device__ __forceinline__ float worker_reduce(float v, float* red, int warp, int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float x = __shfl_xor_sync(0xffffffffu, v, o);
+    v = MAX ? fmaxf(v, x) : v + x;
+  }
+  if (lane == 0) red[warp] = v;
+  named_bar(2, kWorkers);
+  const float r = MAX ? fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])) : (red[0] + red[1]) + (red[2] + red[3]);
+  named_bar(2, kWorkers);  // red is reused by the next reduction
+  return r;
+}
+
+// Transposing butterfly: v[0..31] per lane (lane = slot row, index = head) -> lane l returns the sum
+// over the warp's 32 rows of head l.
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = upper ? v[i] : v[i + o];
+      const float keep = upper ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0];
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_kl_kernel(const __nv_bfloat16* __restrict__ k_idx, const __nv_bfloat16* __restrict__ q_idx,
+                      const float* __restrict__ w, const int32_t* __restrict__ topk_idx,
+                      const int32_t* __restrict__ topk_len, const float* __restrict__ prob, int Tk, int Hi, int K,
+                      float coeff, float* __restrict__ kl_out, __nv_bfloat16* __restrict__ dq_out,
+                      float* __restrict__ dw_out, float* __restrict__ dk, int* __restrict__ err,
+                      long long wait_limit) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sQ = smem_u32(smem + OFF_Q), sK = smem_u32(smem + OFF_K);
+  const uint32_t sMhi = smem_u32(smem + OFF_MHI), sMlo = smem_u32(smem + OFF_MLO);
+  float* s_I = reinterpret_cast<float*>(smem + OFF_I);
+  float* s_P = reinterpret_cast<float*>(smem + OFF_P);
+  uint8_t* misc = smem + OFF_MISC;
+  const uint32_t bar_s = smem_u32(misc + M_BAR_S), bar_mm = smem_u32(misc + M_BAR_MM);
+  const uint32_t bar_fin = smem_u32(misc + M_BAR_FIN);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + M_TMEM);
+  int* s_neff = reinterpret_cast<int*>(misc + M_NEFF);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(misc + M_ABORT);
+  int* s_active = reinterpret_cast<int*>(misc + M_ACTIVE);
+  float* s_stats = reinterpret_cast<float*>(misc + M_STATS);
+  float* s_w = reinterpret_cast<float*>(misc + M_W);
+  float* s_dw = reinterpret_cast<float*>(misc + M_DW);
+  float* s_red = reinterpret_cast<float*>(misc + M_RED);
+
+  const int t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;  // workers: 0..127, slot row / dim of this thread
+  const bool worker = warp < 4;
+  const int32_t* idx_row = topk_idx + (size_t)t * K;
+
+  if (tid == 0) {
+    mbar_init(bar_s, 1);
+    mbar_init(bar_mm, 1);
+    mbar_init(bar_fin, 1);
+    *s_neff = 0;
+    *s_abort = 0;
+    *s_active = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(smem_u32(s_tmem), 256);
+    tmem_relinquish();
+  }
+  __syncthreads();  // the counters are initialised before any worker adds to them
+  if (worker) {
+    if (topk_len != nullptr) {
+      if (tid == 0) {
+        const int n = topk_len[t];
+        *s_neff = n < 0 ? 0 : (n > K ? K : n);
+      }
+    } else {
+      int last = 0;
+      for (int j = tid; j < K; j += kWorkers)
+        if (idx_row[j] >= 0) last = j + 1;
+      if (last) atomicMax(s_neff, last);
+    }
+    // q_idx [64 heads x 128] -> 2 chunks of [64 rows x 128 B], 128B swizzle; padded heads are zero
+    const uint64_t pol = l2_evict_first_policy();
+    for (int u = tid; u < kHeads * 16; u += kWorkers) {
+      const int hh = u >> 4, c = (u >> 3) & 1, uc = u & 7;
+      const bool ok = hh < Hi;
+      cp_async16_hint(sQ + c * Q_CHUNK + sw128_off(hh, uc),
+                      q_idx + (ok ? ((size_t)t * Hi + hh) * kDi + c * 64 + uc * 8 : 0), ok ? 16u : 0u, pol);
+    }
+    if (tid < kHeads) {
+      s_w[tid] = (tid < Hi) ? __ldg(w + (size_t)t * Hi + tid) : 0.f;
+      s_dw[tid] = 0.f;
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  const int n_eff = *s_neff;
+  const int ntiles = (n_eff + kTile - 1) / kTile;
+  const uint32_t tmem = *s_tmem;
+  const uint32_t tS = tmem, tDQ = tmem + 64, tDK = tmem + 128;
+
+  // index of slot j (-1: invalid or beyond the prefix; out-of-range values are reported and masked)
+  auto slot_key = [&](int j) -> int {
+    if (j >= n_eff) return -1;
+    const int ix = __ldg(idx_row + j);
+    if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
+    return (ix >= 0 && ix < Tk) ? ix : -1;
+  };
+  // issue the gather of tile i's k_idx rows into buffer i & 1, one row per worker thread (zero-filled
+  // when invalid), as one cp.async group; returns this thread's key of the tile (-1: none)
+  auto gather = [&](int i) {
+    const int ix = slot_key(i * kTile + tid);
+    const __nv_bfloat16* src = k_idx + (ix >= 0 ? (size_t)ix * kDi : 0);
+    const uint32_t dst = sK + (uint32_t)(i & 1) * K_BUF;
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      cp_async16(dst + (u >> 3) * K_CHUNK + sw128_off(tid, u & 7), src + u * 8, ix >= 0 ? 16u : 0u);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    return ix;
+  };
+  // tile i (its group, and not the one issued after it) has landed and is visible to the tensor core
+  auto landed = [&](bool one_more_in_flight) {
+    if (one_more_in_flight)
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    fence_proxy_async_smem();
+  };
+  constexpr uint32_t kIdS = idesc_bf16(kTile, kHeads, false, false);   // S = K_tile . Q^T
+  constexpr uint32_t kIdDQ = idesc_bf16(kDi, kHeads, true, true);      // dQ^T += K_tile^T . M
+  constexpr uint32_t kIdDK = idesc_bf16(kTile, kDi, false, true);      // dK = M . Q
+  auto issue_s = [&](int i) {
+    tc_fence_after();
+    const uint32_t kb = sK + (uint32_t)(i & 1) * K_BUF;
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)  // + 16 dims = + 32 bytes per row
+        mma_ss(tS, sdesc_sw128(kb + c * K_CHUNK, 16, 1024) + (uint64_t)(k * 2),
+               sdesc_sw128(sQ + c * Q_CHUNK, 16, 1024) + (uint64_t)(k * 2), kIdS, (c | k) != 0);
+    mma_commit(bar_s);
+  };
+
+  bool aborted = false;
+  uint32_t ph_s = 0, ph_mm = 0;
+  // ---- pass 1: indexer scores of the selected slots ----
+  int ix_next = (worker && ntiles > 0) ? gather(0) : -1;
+  for (int i = 0; i < ntiles; ++i) {
+    const int ix = ix_next;
+    if (worker) {
+      const bool more = i + 1 < ntiles;
+      if (more) ix_next = gather(i + 1);  // buffer (i + 1) & 1 was last read by tile i - 1's finished MMAs
+      landed(more);
+    }
+    if (named_bar_or(1, kThreads, false)) { aborted = true; break; }  // the tile has landed
+    if (warp == 4 && lane == 0) issue_s(i);
+    bool ok = true;
+    if (worker) {
+      ok = mbar_wait(bar_s, ph_s, s_abort, err, wait_limit);
+      if (ok) {
+        tc_fence_after();
+        uint32_t v[64];
+        tmem_ld32(tmem_addr(tS, warp * 32, 0), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(tmem_addr(tS, warp * 32, 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_ld_wait();
+        float score = 0.f;
+#pragma unroll
+        for (int h = 0; h < kHeads; ++h) score = fmaf(s_w[h], fmaxf(__uint_as_float(v[h]), 0.f), score);
+        const int j = i * kTile + tid;
+        if (j < n_eff) s_I[j] = (ix >= 0) ? score : -INFINITY;
+      }
+      tc_fence_before();
+    }
+    ph_s ^= 1;
+    if (named_bar_or(1, kThreads, !ok)) { aborted = true; break; }  // S is read: TMEM and the tile are free
+  }
+
+  // ---- the row's distributions and its KL value (workers) ----
+  if (worker && !aborted) {
+    float imax = -INFINITY, psum = 0.f;
+    for (int j = tid; j < n_eff; j += kWorkers) {
+      const int ix = slot_key(j);
+      const float p = (ix >= 0) ? __ldg(prob + (size_t)t * K + j) : 0.f;
+      s_P[j] = p;
+      imax = fmaxf(imax, s_I[j]);
+      psum += p;
+    }
+    imax = worker_reduce<true>(imax, s_red, warp, lane);
+    psum = worker_reduce<false>(psum, s_red, warp, lane);
+    const bool active = imax > -INFINITY && psum > 0.f;
+    float klv = 0.f;
+    if (active) {
+      float z = 0.f;
+      for (int j = tid; j < n_eff; j += kWorkers) z += (s_I[j] > -INFINITY) ? expf(s_I[j] - imax) : 0.f;
+      z = worker_reduce<false>(z, s_red, warp, lane);
+      const float logz = imax + logf(z), inv_psum = 1.f / psum;
+      float acc = 0.f;
+      for (int j = tid; j < n_eff; j += kWorkers) {
+        const float p = s_P[j] * inv_psum;
+        if (s_I[j] > -INFINITY && p > 0.f) acc += p * (logf(p) - (s_I[j] - logz));
+      }
+      klv = worker_reduce<false>(acc, s_red, warp, lane);
+      if (tid == 0) {
+        s_stats[0] = logz;
+        s_stats[1] = inv_psum;
+      }
+    }
+    if (tid == 0) {
+      kl_out[t] = klv;
+      *s_active = active ? 1 : 0;
+    }
+  }
+  named_bar(1, kThreads);  // the statistics are in shared memory for every role
+  const bool active = !aborted && *s_active != 0;
+  const float logz = s_stats[0], inv_psum = s_stats[1];
+
+  // ---- pass 2: the gradient ----
+  ix_next = (worker && active && ntiles > 0) ? gather(0) : -1;
+  for (int i = 0; active && i < ntiles; ++i) {
+    const int ix = ix_next;
+    if (worker) {
+      const bool more = i + 1 < ntiles;
+      if (more) ix_next = gather(i + 1);
+      landed(more);
+    }
+    if (named_bar_or(1, kThreads, false)) { aborted = true; break; }
+    if (warp == 4 && lane == 0) issue_s(i);
+    bool ok = true;
+    if (worker) {
+      ok = mbar_wait(bar_s, ph_s, s_abort, err, wait_limit);
+      if (ok) {
+        tc_fence_after();
+        uint32_t v[64];
+        tmem_ld32(tmem_addr(tS, warp * 32, 0), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(tmem_addr(tS, warp * 32, 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_ld_wait();
+        const int j = i * kTile + tid;
+        float g = 0.f;
+        if (j < n_eff && ix >= 0) g = coeff * (expf(s_I[j] - logz) - s_P[j] * inv_psum);
+        // m_h = g w_h [s_h > 0] as bf16 hi + lo, row tid of the two M tiles; dw_h += g max(0, s_h)
+        uint32_t mh[32], ml[32];
+#pragma unroll
+        for (int h = 0; h < kHeads; h += 2) {
+          const float s0 = __uint_as_float(v[h]), s1 = __uint_as_float(v[h + 1]);
+          const float m0 = (s0 > 0.f) ? g * s_w[h] : 0.f, m1 = (s1 > 0.f) ? g * s_w[h + 1] : 0.f;
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(m0, m1);
+          const float2 hf = __bfloat1622float2(hi);
+          mh[h >> 1] = *reinterpret_cast<const uint32_t*>(&hi);
+          ml[h >> 1] = pack_bf16x2(m0 - hf.x, m1 - hf.y);
+          v[h] = __float_as_uint(g * fmaxf(s0, 0.f));
+          v[h + 1] = __float_as_uint(g * fmaxf(s1, 0.f));
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          st_shared_v4(sMhi + sw128_off(tid, u), mh[4 * u], mh[4 * u + 1], mh[4 * u + 2], mh[4 * u + 3]);
+          st_shared_v4(sMlo + sw128_off(tid, u), ml[4 * u], ml[4 * u + 1], ml[4 * u + 2], ml[4 * u + 3]);
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float d[32];
+#pragma unroll
+          for (int h = 0; h < 32; ++h) d[h] = __uint_as_float(v[32 * half + h]);
+          atomicAdd(s_dw + 32 * half + lane, warp_transpose_sum(d, lane));
+        }
+        fence_proxy_async_smem();  // M -> visible to the tensor core
+      }
+      tc_fence_before();
+    }
+    if (named_bar_or(1, kThreads, !ok)) { aborted = true; break; }  // M is in shared memory
+    if (warp == 4 && lane == 0) {
+      tc_fence_after();
+      const uint64_t ka = sdesc_sw128(sK + (uint32_t)(i & 1) * K_BUF, K_CHUNK, 1024);
+      const uint64_t mb_hi = sdesc_sw128(sMhi, K_CHUNK, 1024);
+      const uint64_t mb_lo = sdesc_sw128(sMlo, K_CHUNK, 1024);
+#pragma unroll
+      for (int k = 0; k < kTile / 16; ++k) {  // + 16 slots = + 2048 bytes
+        mma_ss(tDQ, ka + (uint64_t)(k * 128), mb_hi + (uint64_t)(k * 128), kIdDQ, (i > 0 || k > 0) ? 1u : 0u);
+        mma_ss(tDQ, ka + (uint64_t)(k * 128), mb_lo + (uint64_t)(k * 128), kIdDQ, 1u);
+      }
+      const uint64_t ma_hi = sdesc_sw128(sMhi, 16, 1024), ma_lo = sdesc_sw128(sMlo, 16, 1024);
+      const uint64_t qb = sdesc_sw128(sQ, Q_CHUNK, 1024);
+#pragma unroll
+      for (int k = 0; k < kHeads / 16; ++k) {  // + 16 heads: + 32 bytes along A's rows, + 16 rows of Q
+        mma_ss(tDK, ma_hi + (uint64_t)(k * 2), qb + (uint64_t)(k * 128), kIdDK, k > 0 ? 1u : 0u);
+        mma_ss(tDK, ma_lo + (uint64_t)(k * 2), qb + (uint64_t)(k * 128), kIdDK, 1u);
+      }
+      mma_commit(bar_mm);
+    }
+    ok = true;
+    if (worker) {
+      ok = mbar_wait(bar_mm, ph_mm, s_abort, err, wait_limit);
+      if (ok) {
+        tc_fence_after();
+        // dK row tid -> its staging row (the previous tile's bulk reduction has read it), then one bulk
+        // reduction of the 512-byte row into dk_idx[key], running while the warps go on
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        const uint32_t row = smem_u32(smem + OFF_DKS + tid * DK_PITCH);
+#pragma unroll 1
+        for (int b = 0; b < kDi / 32; ++b) {
+          uint32_t v[32];
+          tmem_ld32(tmem_addr(tDK, warp * 32, 32 * b), v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            st_shared_v4(row + 128 * b + 16 * u, v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        }
+        fence_proxy_async_smem();  // the row -> visible to the bulk copy
+        if (ix >= 0) {
+          asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                           dk + (size_t)ix * kDi),
+                       "r"(row), "n"(kDi * 4)
+                       : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+      }
+      tc_fence_before();
+    }
+    ph_s ^= 1;
+    ph_mm ^= 1;
+    if (named_bar_or(1, kThreads, !ok)) { aborted = true; break; }  // dK drained: TMEM, the tile and M are free
+  }
+
+  // ---- dq_idx (dQ^T in TMEM: lane = dim, column = head) and dw ----
+  if (worker) {
+    const bool have = active && !aborted && ntiles > 0;
+    uint32_t v[64];
+    if (have) {
+      tc_fence_after();
+      tmem_ld32(tmem_addr(tDQ, warp * 32, 0), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(tmem_addr(tDQ, warp * 32, 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int h = 0; h < kHeads; ++h) v[h] = 0u;
+    }
+    __nv_bfloat16* dq_row = dq_out + (size_t)t * Hi * kDi + tid;  // dim tid of every head
+#pragma unroll 8
+    for (int h = 0; h < kHeads; ++h)
+      if (h < Hi) dq_row[(size_t)h * kDi] = __float2bfloat16_rn(__uint_as_float(v[h]));
+    if (tid < Hi) dw_out[(size_t)t * Hi + tid] = have ? s_dw[tid] : 0.f;
+  }
+
+  // every bulk reduction of this thread is complete before the CTA exits
+  if (worker) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  if (warp == 4 && lane == 0) {
+    // every MMA of this CTA completes before the teardown frees TMEM
+    mma_commit(bar_fin);
+    volatile int dummy = 0;
+    mbar_wait(bar_fin, 0, &dummy, err);
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+}  // namespace kl
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" size_t dsa_indexer_kl_workspace_size(int32_t T, int32_t K) {
+  (void)T;
+  (void)K;
+  return kErrorWordBytes;
+}
+
+extern "C" dsa_status_t dsa_indexer_kl(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
+                                       const int32_t* topk_idx, const int32_t* topk_len, const float* attn_prob,
+                                       int32_t T, int32_t T_k, int32_t Hi, int32_t Di, int32_t K, float coeff,
+                                       float* kl, dsa_bf16_t* dq_idx, float* dw, float* dk_idx_accum,
+                                       int32_t accumulate, void* workspace, size_t workspace_bytes,
+                                       dsa_stream_t stream) {
+  const char* who = "dsa_indexer_kl";
+  if (T < 0 || T_k < 1) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: need T >= 0 and T_k >= 1", who);
+  if (Hi < 1 || Hi > kl::kHeads) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: Hi must be in [1, 64] (got %d)", who, Hi);
+  if (Di != kl::kDi) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: Di must be 128 (got %d)", who, Di);
+  if (K < 1 || K > kl::kMaxK)
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: K must be in [1, %d] (got %d)", who, kl::kMaxK, K);
+  if (accumulate != 0 && accumulate != 1) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: accumulate must be 0 or 1", who);
+  if (!std::isfinite(coeff)) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: coeff must be finite", who);
+  if (!k_idx || !dk_idx_accum) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: k_idx / dk_idx_accum is NULL", who);
+  if (T > 0 && (!q_idx || !head_weights || !topk_idx || !attn_prob || !kl || !dq_idx || !dw))
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: null tensor pointer", who);
+  if (!aligned16(k_idx) || !aligned16(dk_idx_accum) || (T > 0 && !aligned16(q_idx)))
+    return fail(DSA_ERR_INVALID_ARGUMENT, "%s: q_idx, k_idx and dk_idx_accum must be 16-byte aligned", who);
+  dsa_status_t st = check_workspace(workspace, workspace_bytes, dsa_indexer_kl_workspace_size(T, K), who);
+  if (st != DSA_OK) return st;
+  if ((st = check_device()) != DSA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = clear_error_word(workspace, s)) != DSA_OK) return st;
+  if (!accumulate && (st = cuda_check(cudaMemsetAsync(dk_idx_accum, 0, (size_t)T_k * Di * sizeof(float), s),
+                                      "zeroing dk_idx_accum")))
+    return st;
+  if (T == 0) return ok();
+  if ((st = configure_kernel_smem(reinterpret_cast<const void*>(kl::indexer_kl_kernel), kl::TOTAL,
+                                  "configuring indexer_kl_kernel")))
+    return st;
+  kl::indexer_kl_kernel<<<T, kl::kThreads, kl::TOTAL, s>>>(
+      reinterpret_cast<const __nv_bfloat16*>(k_idx), reinterpret_cast<const __nv_bfloat16*>(q_idx), head_weights,
+      topk_idx, topk_len, attn_prob, T_k, Hi, K, coeff, kl, reinterpret_cast<__nv_bfloat16*>(dq_idx), dw,
+      dk_idx_accum, reinterpret_cast<int*>(workspace), wait_limit_cycles());
+  if ((st = cuda_check(cudaGetLastError(), "launching indexer_kl_kernel"))) return st;
+  return ok();
+}

@@ -79,13 +79,13 @@ def test_metadata_cp_rejects_invalid_arguments(lib, bad):
 
 def bwd(lib, **kw):
     a = dict(q=FAKE, kv=FAKE, idx=FAKE, ln=None, T=4, Tk=8, H=16, Dqk=576, Dv=512, K=64, scale=0.1, sink=None,
-             out=FAKE, out_lo=None, lse=FAKE, dout=FAKE, dq=FAKE, dkv=FAKE, dsink=None, acc=0, dkv_bf16=None,
-             ws=P(0x100000), wsb=1 << 30, stream=None)
+             out=FAKE, out_lo=None, lse=FAKE, dout=FAKE, dq=FAKE, dkv=FAKE, dsink=None, prob=None, acc=0,
+             dkv_bf16=None, ws=P(0x100000), wsb=1 << 30, stream=None)
     a.update(kw)
     return lib.dsa_sparse_mla_bwd(a["q"], a["kv"], a["idx"], a["ln"], a["T"], a["Tk"], a["H"], a["Dqk"], a["Dv"],
                                   a["K"], ctypes.c_float(a["scale"]), a["sink"], a["out"], a["out_lo"], a["lse"],
-                                  a["dout"], a["dq"], a["dkv"], a["dsink"], a["acc"], a["dkv_bf16"], a["ws"], a["wsb"],
-                                  a["stream"])
+                                  a["dout"], a["dq"], a["dkv"], a["dsink"], a["prob"], a["acc"], a["dkv_bf16"], a["ws"],
+                                  a["wsb"], a["stream"])
 
 
 @pytest.mark.parametrize("bad", [dict(Dqk=500), dict(Dv=256), dict(K=0), dict(H=0), dict(Tk=0), dict(T=-1),

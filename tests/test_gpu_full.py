@@ -197,3 +197,41 @@ def test_full_thd_packed_indexshare_4_layers():
         del x
         torch.cuda.empty_cache()
     assert torch.equal(idx, idx_before)
+
+
+def test_full_indexer_kl_32k_after_the_backward():
+    # the indexer KL loss on the 32k workload: indexer -> sparse MLA fwd -> bwd (slot probabilities) -> KL.
+    # Sampled rows against the oracle (slot probability, kl, dq_idx, dw), and dk_idx of a chunk of rows
+    # exactly (a call on row-offset pointers)
+    c = synth.WORKLOADS["idx32k"]
+    T, K = c["T"], c["K"]
+    ind = synth.indexer_inputs(T, c["Hi"], c["Di"], seed=8, device=DEV)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=DEV)
+    start, _, _, _ = dsa.dsa_packed_metadata(cu, T)
+    idx, ln = dsa.dsa_indexer_topk(ind["q_idx"], ind["k_idx"], ind["w"], start, K)
+    x = synth.mla_inputs(T, c["H"], c["Dqk"], c["Dv"], seed=9, device=DEV)
+    out, lse, lo = dsa.dsa_sparse_mla_fwd(x["q"], x["kv"], idx, c["scale"], topk_len=ln, out_lo=True)
+    wb = torch.zeros(dsa.workspace_size("bwd", T, c["H"], K), dtype=torch.uint8, device=DEV)
+    *_, prob = dsa.dsa_sparse_mla_bwd(x["q"], x["kv"], idx, c["scale"], out, lse, x["dout"], topk_len=ln,
+                                      out_lo=lo, workspace=wb, attn_prob=True)
+    assert dsa.dsa_read_device_status(wb) == 0
+    del wb, out, lo
+    ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
+    kl, dq, dw, dk = dsa.dsa_indexer_kl(ind["q_idx"], ind["k_idx"], ind["w"], idx, prob, 1.0, topk_len=ln,
+                                        workspace=ws)
+    assert dsa.dsa_read_device_status(ws) == 0
+    rows = sample_rows(T, [0, 1, 2047, 2048, T - 1], n_random=43, seed=8)
+    r = torch.as_tensor(rows)
+    ref_p = oracle.attn_slot_prob(x["q"][r].cpu(), x["kv"].cpu(), idx[r].cpu(), c["scale"], len_rows=ln[r].cpu())
+    assert np.max(np.abs(prob[r].cpu().double().numpy() - ref_p)) <= 1e-5, "slot probability (sampled rows)"
+    rkl, rdq, rdw, _ = oracle.indexer_kl(ind["q_idx"][r].cpu(), ind["k_idx"].cpu(), ind["w"][r].cpu(), idx[r].cpu(),
+                                         prob[r].cpu(), 1.0, len_rows=ln[r].cpu())
+    assert np.max(np.abs(kl[r].cpu().double().numpy() - rkl) / np.maximum(1.0, np.abs(rkl))) <= 1e-4, "kl"
+    assert_close(dq[r].cpu(), rdq, "dq_idx (sampled rows)", max_abs=2e-3 * float(np.abs(rdq).max()))
+    assert_close(dw[r].cpu(), rdw, "dw (sampled rows)", max_abs=2e-3 * float(np.abs(rdw).max()), rel_fro=1e-4)
+    a, b = T - 40, T
+    _, _, _, dk_c = dsa.dsa_indexer_kl(ind["q_idx"][a:b], ind["k_idx"], ind["w"][a:b], idx[a:b], prob[a:b], 1.0,
+                                       topk_len=ln[a:b], workspace=ws)
+    _, _, _, ref_c = oracle.indexer_kl(ind["q_idx"][a:b].cpu(), ind["k_idx"].cpu(), ind["w"][a:b].cpu(),
+                                       idx[a:b].cpu(), prob[a:b].cpu(), 1.0, len_rows=ln[a:b].cpu())
+    assert_close(dk_c.cpu(), ref_c, f"dk_idx of rows {a}:{b}", max_abs=2e-3 * float(np.abs(ref_c).max()), rel_fro=1e-4)

@@ -48,7 +48,7 @@ def _noalloc_call(lib, q, kv, idx, scale, out, out_lo, lse, dout, ln=None):
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     st = lib.dsa_sparse_mla_bwd_noalloc(_p(q), _p(kv), _p(idx), _p(ln), T, kv.shape[0], H, Dqk, 512, idx.shape[1],
                                         ctypes.c_float(scale), None, _p(out), _p(out_lo), _p(lse), _p(dout), _p(dq),
-                                        _p(dkv), None, 0, None, stream)
+                                        _p(dkv), None, None, 0, None, stream)
     assert st == 0, lib.dsa_last_error_message().decode()
     dev_status = ctypes.c_int32(-1)
     assert lib.dsa_sparse_mla_bwd_noalloc_read_status(stream, ctypes.byref(dev_status)) == 0
@@ -106,7 +106,7 @@ def test_noalloc_bwd_rejects_topk_beyond_its_scratch():
     K = lib.dsa_sparse_mla_bwd_noalloc_max_topk() + 1
     fake = ctypes.c_void_p(0x10000)
     st = lib.dsa_sparse_mla_bwd_noalloc(fake, fake, fake, None, 4, 4, 64, 576, 512, K, ctypes.c_float(0.1), None,
-                                        fake, None, fake, fake, fake, fake, None, 0, None, None)
+                                        fake, None, fake, fake, fake, fake, None, None, 0, None, None)
     assert st == DSA_ERR_WORKSPACE
     assert "scratch limit" in lib.dsa_last_error_message().decode()
 
