@@ -49,7 +49,8 @@
 //  * The epilogue stages O (and, on request, the bf16 residual O - bf16(O))
 //    through shared memory for coalesced 16-byte stores.
 //
-// Warp roles: warp 0 issues MMAs (one thread) and owns TMEM; warps 1..8 run
+// Warp roles: warp 0 issues MMAs (the whole warp runs the issuing loop, one elected
+// lane issues each instruction) and owns TMEM; warps 1..8 run
 // the gather, the softmax and the epilogue.
 #include <cmath>
 
@@ -251,8 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tO = tmem + 64;   // O^T: 4 channel tiles x 64 columns
 
   if (warp == 0) {
-    // ======================= MMA issuer =======================
-    if (lane == 0) {
+    // ======================= MMA issuer (the whole warp, one elected lane issues) =======================
+    {
       constexpr uint32_t kIdS = idesc_bf16(128, kHeads, false, false);  // A = KV (K-major), B = Q (K-major)
       constexpr uint32_t kIdPV = idesc_bf16(128, kHeads, true, true);   // A = V^T (MN-major), B = P^T (MN-major)
       for (int i = 0; i < ntiles; ++i) {
@@ -261,23 +262,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         // later chunk that has landed too (fewer fences and waits between MMAs)
         const uint64_t a00 = sdesc_sw128(sKV, 16, 1024), b00 = sdesc_sw128(sQ, 16, 1024);
         for (int c = 0; c < NCH && !stop;) {
-          if (!mbar_wait(bar_kv + 8 * c, i & 1, s_abort, err, wait_limit)) { stop = true; break; }
+          if (!warp_all(mbar_wait(bar_kv + 8 * c, i & 1, s_abort, err, wait_limit))) { stop = true; break; }
           int ce = c + 1;
-          while (ce < NCH && mbar_test(bar_kv + 8 * ce, i & 1)) ++ce;
+          while (ce < NCH && warp_all(mbar_test(bar_kv + 8 * ce, i & 1))) ++ce;
           fence_proxy_async_smem();  // cp.async landings -> visible to the tensor core
           tc_fence_after();
           for (; c < ce; ++c) {
             const uint64_t a0 = a00 + (uint64_t)((c * L::KV_CHUNK) >> 4), b0 = b00 + (uint64_t)((c * L::Q_CHUNK) >> 4);
 #pragma unroll
             for (int k = 0; k < 4; ++k)  // + 16 channels = + 32 bytes per row
-              mma_ss(tS, a0 + (uint64_t)(k * 2), b0 + (uint64_t)(k * 2), kIdS, (c | k) != 0);
+              mma_ss_w(tS, a0 + (uint64_t)(k * 2), b0 + (uint64_t)(k * 2), kIdS, (c | k) != 0);
           }
         }
         if (stop) break;
-        mma_commit(bar_s);
+        mma_commit_w(bar_s);
         // O^T += V^T (P_hi + P_lo)^T, key rows 0..63 first (P_lo of those rows has its own slot),
         // so that rows 0..63 of every chunk slot are free while rows 64..127 are multiplied
-        if (!mbar_wait(bar_p, i & 1, s_abort, err, wait_limit)) break;
+        if (!warp_all(mbar_wait(bar_p, i & 1, s_abort, err, wait_limit))) break;
         tc_fence_after();
         const uint64_t pb0 = sdesc_sw128(sP, L::KV_CHUNK, 1024);
         const uint64_t lb0 = sdesc_sw128(sPlo, L::KV_CHUNK, 1024);
@@ -288,33 +289,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int m = 0; m < kDv / 128; ++m) {
 #pragma unroll
           for (int k = 0; k < kHalf; ++k)  // + 16 key rows = + 2048 bytes
-            mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV,
-                   (i > 0 || k > 0) ? 1u : 0u);
+            mma_ss_w(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV,
+                     (i > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
           for (int k = 0; k < kHalf; ++k)
-            mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), lb0 + (uint64_t)(k * 128), kIdPV, 1u);
+            mma_ss_w(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), lb0 + (uint64_t)(k * 128), kIdPV, 1u);
         }
-        mma_commit(bar_pvh);  // rows 0..63 of the chunk slots (and of the P slot) are read
+        mma_commit_w(bar_pvh);  // rows 0..63 of the chunk slots (and of the P slot) are read
 #pragma unroll
         for (int m = 0; m < kDv / 128; ++m) {
 #pragma unroll
           for (int k = kHalf; k < 2 * kHalf; ++k)
-            mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV, 1u);
+            mma_ss_w(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV, 1u);
         }
         // P_lo of rows 64..127, moved by the workers into the P slot's rows 0..63
-        if (!mbar_wait(bar_plo, i & 1, s_abort, err, wait_limit)) break;
+        if (!warp_all(mbar_wait(bar_plo, i & 1, s_abort, err, wait_limit))) break;
         tc_fence_after();
 #pragma unroll
         for (int m = 0; m < kDv / 128; ++m) {
 #pragma unroll
           for (int k = kHalf; k < 2 * kHalf; ++k)
-            mma_ss(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)((k - kHalf) * 128), kIdPV,
-                   1u);
+            mma_ss_w(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)((k - kHalf) * 128),
+                     kIdPV, 1u);
         }
-        mma_commit(bar_pv);  // P.V of this tile is complete
+        mma_commit_w(bar_pv);  // P.V of this tile is complete
       }
       // every MMA of this CTA completes before the teardown frees TMEM
-      mma_commit(bar_fin);
+      mma_commit_w(bar_fin);
       volatile int dummy = 0;
       mbar_wait(bar_fin, 0, &dummy, err);
     }
@@ -326,23 +327,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ch = wk >> 2;           // head half: heads ch*32 .. ch*32+31
     const int r = qd * 32 + lane;     // key row of the tile / channel row of an O^T tile
     const int bar_id = 1 + ch;        // named barrier of the 128 threads of this half
-    // row indices this thread gathers for tile i: -1 = zero-fill (invalid or beyond the prefix)
-    auto load_rows = [&](int i, int (&rix)[4]) {
+    // Row indices this thread gathers for tile i, in two steps: the raw loads (issued a tile
+    // ahead, so that their memory latency hides behind the softmax and P.V of the tile before)
+    // and the check that turns them into row numbers, -1 = zero-fill (invalid or beyond the prefix).
+    auto load_raw = [&](int i, int (&raw)[4]) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = i * kTile + (tid >> 3) + 32 * e;
-        int v = -1;
-        if (j < n_eff) {
-          const int ix = __ldg(idx_row + j);
-          v = (ix >= 0 && ix < Tk) ? ix : -1;
-          if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
-        }
-        rix[e] = v;
+        raw[e] = (j < n_eff) ? __ldg(idx_row + j) : -1;
       }
     };
+    auto check_rows = [&](const int (&raw)[4], int (&rix)[4]) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int ix = raw[e];
+        rix[e] = (ix >= 0 && ix < Tk) ? ix : -1;
+        if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
+      }
+    };
+    int nraw[4];  // raw indices of the next tile
     if (ntiles > 0) {
       int rix[4];
-      load_rows(0, rix);
+      load_raw(0, nraw);
+      check_rows(nraw, rix);
       for (int c = 0; c < NCH; ++c) gather_chunk<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, bar_kv + 8 * c);
     }
     // running max per head lives in s_stat (identical for all threads of a half)
@@ -352,9 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
     bool aborted = false;
     for (int i = 0; i < ntiles; ++i) {
-      // this key row's index does not depend on the MMA: its load overlaps the wait
+      // this key row's index and the next tile's gather rows do not depend on the MMA: their
+      // loads overlap the wait (and, for the gather rows, this whole tile)
       const int j = i * kTile + r;
       const int ixw = (j < n_eff) ? __ldg(idx_row + j) : -1;
+      const bool more = i + 1 < ntiles;
+      if (more) load_raw(i + 1, nraw);
       const bool got = mbar_wait(bar_s, i & 1, s_abort, err, wait_limit);
       // every thread of the half leaves together, or none does (named barriers follow)
       if (named_bar_or(bar_id, 128, !got)) { aborted = true; break; }
@@ -451,9 +461,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar_p);
       // rows 0..63 of every slot are free once bar_pvh completes: the lo part of key rows
       // 64..127 goes into the P slot's rows 0..63, and the next tile's rows 0..63 are gathered
-      const bool more = i + 1 < ntiles;
-      int rix[4];
-      if (more) load_rows(i + 1, rix);
       {
         const bool okh = mbar_wait(bar_pvh, i & 1, s_abort, err, wait_limit);
         if (qd >= 2) {
@@ -470,6 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (named_bar_or(bar_id, 128, !okh)) { aborted = true; break; }
       }
       if (more) {
+        int rix[4];
+        check_rows(nraw, rix);
         for (int c = 0; c < kDv / 64; ++c) gather_half<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, 0);
         // rows 64..127 (and the RoPE chunk, which holds P) once P.V is complete
         if (!mbar_wait(bar_pv, i & 1, s_abort, err, wait_limit)) {
