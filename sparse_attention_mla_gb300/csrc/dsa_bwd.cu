@@ -46,7 +46,8 @@
 //  * The gathered rows stream through shared memory in 64-channel chunks
 //    (128-byte swizzle) loaded by 16-byte cp.async (zero-fill for invalid or
 //    beyond-prefix rows).
-//  * One thread issues every MMA.  It polls its inputs (ring chunks landed,
+//  * One warp issues every MMA (one elected lane per instruction, the
+//    whole warp running the issuing loop).  It polls its inputs (ring chunks landed,
 //    dS ready, staging slot free, buffer free) and issues whichever unit of
 //    work is ready, dKV groups first, so that the tensor core follows the
 //    reductions instead of a fixed program order.
@@ -220,19 +221,26 @@ struct TileGather {
   const __nv_bfloat16* src[KU];
   uint32_t dst[KU];
   uint32_t okm;
-  __device__ __forceinline__ void rows(const __nv_bfloat16* __restrict__ kv, const int32_t* __restrict__ idx_row,
-                                       int i, int n_eff, int Tk, int et, int* err) {
-    okm = 0;
+  int raw[KU];  // indices of the tile loaded by load(), not yet checked
+  // Issue the index loads of tile i.  Nothing uses the values until resolve(), so a caller
+  // that loads the next tile before gathering the current one hides their memory latency.
+  __device__ __forceinline__ void load(const int32_t* __restrict__ idx_row, int i, int n_eff, int et) {
 #pragma unroll
     for (int k = 0; k < KU; ++k) {
       const int u = et + NT * k;
       const int j = i * kTile + (u >> 3);
-      int v = -1;
-      if (u < kUnits && j < n_eff) {
-        const int ix = __ldg(idx_row + j);
-        v = (ix >= 0 && ix < Tk) ? ix : -1;
-        if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
-      }
+      raw[k] = (u < kUnits && j < n_eff) ? __ldg(idx_row + j) : -1;
+    }
+  }
+  // Source rows and destinations of the loaded tile; bad indices are flagged and zero-filled.
+  __device__ __forceinline__ void resolve(const __nv_bfloat16* __restrict__ kv, int Tk, int et, int* err) {
+    okm = 0;
+#pragma unroll
+    for (int k = 0; k < KU; ++k) {
+      const int u = et + NT * k;
+      const int ix = raw[k];
+      const int v = (ix >= 0 && ix < Tk) ? ix : -1;
+      if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
       src[k] = kv + (v >= 0 ? (size_t)v * DQK : 0) + (u & 7) * 8;
       dst[k] = sw128_off((u >> 3) & (kTile - 1), u & 7);
       okm |= (v >= 0 ? 1u : 0u) << k;
@@ -395,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!mbar_wait(bar(B_ENDGO), 0, s_abort, err, wait_limit) || !mbar_wait(bar(B_DSDONE), 0, s_abort, err, wait_limit)) return;
     TileGather<DQK, NT> tg;
     int Le = 0;
+    tg.load(idx_row, 0, n_eff, et);
     for (int i = 0; i < ntiles; ++i) {
       int slot = Le % kERing;
       if (Le >= kERing && !mbar_wait(bar(B_EEMPTY + slot), ((Le / kERing) - 1) & 1, s_abort, err, wait_limit)) return;
@@ -402,7 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = et; u < kDsTileBytes / 16; u += NT) cp_async16(sERing + slot * L::ESLOT + 16 * u, src + 16 * u, 16u);
       cp_async_arrive(bar(B_EFULL + slot));
       ++Le;
-      tg.rows(kv, idx_row, i, n_eff, Tk, et, err);
+      tg.resolve(kv, Tk, et, err);
+      if (i + 1 < ntiles) tg.load(idx_row, i + 1, n_eff, et);  // the next tile's indices, a tile ahead
       for (int p = 0; p < NP; ++p, ++Le) {
         slot = Le % kERing;
         if (Le >= kERing && !mbar_wait(bar(B_EEMPTY + slot), ((Le / kERing) - 1) & 1, s_abort, err, wait_limit)) return;
@@ -442,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ======================= MMA issuer =======================
+    {
+      // ============ MMA issuer (the whole warp runs it; one elected lane issues each instruction) ============
       constexpr uint32_t kIdSP = idesc_bf16(128, 128, false, false);  // [S^T | dP^T] = KV [Q | dO]^T
       constexpr uint32_t kIdS = idesc_bf16(128, 64, false, false);    // S^T only (RoPE chunk)
       constexpr uint32_t kIdMM = idesc_bf16(128, 64, true, true);     // dQ^T
@@ -457,9 +467,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool progressed = false;
         // ---- dKV group gd of tile id: needs dS/P of tile id in TMEM and a free staging slot ----
         if (id < ia) {
-          if (!ds_seen) ds_seen = mbar_test(bar(B_DS + (id & 1)), (id >> 1) & 1);
+          if (!ds_seen) ds_seen = warp_all(mbar_test(bar(B_DS + (id & 1)), (id >> 1) & 1));
           const int s = G & (kStage - 1), n = G / kStage;
-          if (ds_seen && (n == 0 || mbar_test(bar(B_STE + s), (n - 1) & 1))) {
+          if (ds_seen && (n == 0 || warp_all(mbar_test(bar(B_STE + s), (n - 1) & 1)))) {
             tc_fence_after();
             const uint32_t bS = tmem + C_BUF * (id & 1), bP = bS + 64;
             const uint32_t d = tmem + C_STG + kGroup * s;
@@ -471,11 +481,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int k = 0; k < 4; ++k) {
                 const uint32_t acol = (k >> 1) * 32 + (k & 1) * 8;  // heads 16k..16k+15 in a thread-half region
                 const uint64_t bq = bq0 + (uint64_t)(k * 128), bo = bo0 + (uint64_t)(k * 128);  // + 16 head rows
-                mma_ts(d, bS + 16 + acol, bq, kIdKM, k > 0);  // dS hi
-                mma_ts(d, bS + acol, bq, kIdKM, 1u);          // dS lo
+                mma_ts_w(d, bS + 16 + acol, bq, kIdKM, k > 0);  // dS hi
+                mma_ts_w(d, bS + acol, bq, kIdKM, 1u);          // dS lo
                 if (with_p) {
-                  mma_ts(d, bP + acol, bo, kIdKM, 1u);        // P hi
-                  mma_ts(d, bP + 16 + acol, bo, kIdKM, 1u);   // P lo
+                  mma_ts_w(d, bP + acol, bo, kIdKM, 1u);        // P hi
+                  mma_ts_w(d, bP + 16 + acol, bo, kIdKM, 1u);   // P lo
                 }
               }
             } else {  // the RoPE channels 512..575: dS terms only
@@ -484,15 +494,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int k = 0; k < 4; ++k) {
                 const uint32_t acol = (k >> 1) * 32 + (k & 1) * 8;
                 const uint64_t bq = bq0 + (uint64_t)(k * 128);
-                mma_ts(d, bS + 16 + acol, bq, kIdKM64, k > 0);
-                mma_ts(d, bS + acol, bq, kIdKM64, 1u);
+                mma_ts_w(d, bS + 16 + acol, bq, kIdKM64, k > 0);
+                mma_ts_w(d, bS + acol, bq, kIdKM64, 1u);
               }
             }
-            mma_commit(bar(B_STF + s));
+            mma_commit_w(bar(B_STF + s));
             ++G;
             progressed = true;
             if (++gd == NG) {
-              mma_commit(bar(B_KVD + (id & 1)));  // buffer id & 1 may be overwritten once this lands
+              mma_commit_w(bar(B_KVD + (id & 1)));  // buffer id & 1 may be overwritten once this lands
               gd = 0;
               ++id;
               ds_seen = false;
@@ -501,9 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---- chunk ca of tile ia: S^T (+ dP^T) into buffer ia & 1 ----
         if (ia < ntiles) {
-          if (!buf_seen) buf_seen = (ia < 2) || mbar_test(bar(B_KVD + (ia & 1)), ((ia - 2) >> 1) & 1);
+          if (!buf_seen) buf_seen = (ia < 2) || warp_all(mbar_test(bar(B_KVD + (ia & 1)), ((ia - 2) >> 1) & 1));
           const int slot = La % kRing;
-          if (buf_seen && mbar_test(bar(B_FULL + slot), (La / kRing) & 1)) {
+          if (buf_seen && warp_all(mbar_test(bar(B_FULL + slot), (La / kRing) & 1))) {
             fence_proxy_async_smem();  // cp.async landings -> visible to the tensor core
             tc_fence_after();
             const uint32_t bS = tmem + C_BUF * (ia & 1);
@@ -512,12 +522,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idn = (ca < 8) ? kIdSP : kIdS;
 #pragma unroll
             for (int k = 0; k < 4; ++k)  // + 16 channels = + 32 bytes per row
-              mma_ss(bS, a0 + (uint64_t)(k * 2), b0 + (uint64_t)(k * 2), idn, (ca | k) != 0);
-            mma_commit(bar(B_EMPTY + slot));
+              mma_ss_w(bS, a0 + (uint64_t)(k * 2), b0 + (uint64_t)(k * 2), idn, (ca | k) != 0);
+            mma_commit_w(bar(B_EMPTY + slot));
             ++La;
             progressed = true;
             if (++ca == NCH) {
-              mma_commit(bar(B_SDP + (ia & 1)));
+              mma_commit_w(bar(B_SDP + (ia & 1)));
               ca = 0;
               ++ia;
               buf_seen = false;
@@ -532,10 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!idle) {
           idle = true;
           idle_t0 = clock64();
-        } else if (*s_abort) {
+        } else if (__any_sync(0xffffffffu, *s_abort != 0)) {
           stop = true;
           break;
-        } else if (clock64() - idle_t0 > wait_limit) {
+        } else if (__any_sync(0xffffffffu, clock64() - idle_t0 > wait_limit)) {
           *s_abort = 1;
           record_error(err, DSA_ERR_TIMEOUT);
           stop = true;
@@ -545,22 +555,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- end phase: dQ^T[pair p] += KV^T dS^T over every tile of the token ----
       if (!stop && ntiles > 0) {
         // every dKV MMA has landed: Q, dO, the main ring and the S/dP buffers are dead
-        stop = !mbar_wait(bar(B_KVD + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, s_abort, err, wait_limit);
-        if (!stop) mbar_arrive(bar(B_ENDGO));
+        stop = !warp_all(mbar_wait(bar(B_KVD + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, s_abort, err, wait_limit));
+        if (!stop && lane == 0) mbar_arrive(bar(B_ENDGO));
         // the rope tile of dQ^T overlaps staging slot 0: wait for its last drain
         bool rope_free = (NP * 64 <= (int)C_STG);
         const int uses0 = (G + kStage - 1) / kStage;
         int Le = 0;
         for (int i = 0; i < ntiles && !stop; ++i) {
           const int sds = Le % kERing;
-          if (!mbar_wait(bar(B_EFULL + sds), (Le / kERing) & 1, s_abort, err, wait_limit)) { stop = true; break; }
+          if (!warp_all(mbar_wait(bar(B_EFULL + sds), (Le / kERing) & 1, s_abort, err, wait_limit))) { stop = true; break; }
           const uint32_t dsb = sERing + sds * L::ESLOT;
           ++Le;
           for (int p = 0; p < NP; ++p, ++Le) {
             const int sl = Le % kERing;
-            if (!mbar_wait(bar(B_EFULL + sl), (Le / kERing) & 1, s_abort, err, wait_limit)) { stop = true; break; }
+            if (!warp_all(mbar_wait(bar(B_EFULL + sl), (Le / kERing) & 1, s_abort, err, wait_limit))) { stop = true; break; }
             if (p * 64 + 64 > (int)C_STG && !rope_free) {
-              if (uses0 > 0 && !mbar_wait(bar(B_STE), (uses0 - 1) & 1, s_abort, err, wait_limit)) { stop = true; break; }
+              if (uses0 > 0 && !warp_all(mbar_wait(bar(B_STE), (uses0 - 1) & 1, s_abort, err, wait_limit))) { stop = true; break; }
               rope_free = true;
             }
             fence_proxy_async_smem();
@@ -569,17 +579,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t b0 = sdesc_sw128(dsb, L::KV_CHUNK, 1024);
 #pragma unroll
             for (int k = 0; k < kTile / 16; ++k)  // + 16 key rows = + 2048 bytes
-              mma_ss(tmem + 64 * p, a0 + (uint64_t)(k * 128), b0 + (uint64_t)(k * 128), kIdMM, (i > 0 || k > 0) ? 1u : 0u);
-            mma_commit(bar(B_EEMPTY + sl));
+              mma_ss_w(tmem + 64 * p, a0 + (uint64_t)(k * 128), b0 + (uint64_t)(k * 128), kIdMM, (i > 0 || k > 0) ? 1u : 0u);
+            mma_commit_w(bar(B_EEMPTY + sl));
           }
           if (stop) break;
-          mma_commit(bar(B_EEMPTY + sds));
+          mma_commit_w(bar(B_EEMPTY + sds));
         }
       }
       if (stop) *s_abort = 1;
-      mma_commit(bar(B_DQ));
+      mma_commit_w(bar(B_DQ));
       // every MMA of this CTA completes before the teardown frees TMEM
-      mma_commit(bar(B_FIN));
+      mma_commit_w(bar(B_FIN));
       volatile int dummy = 0;
       mbar_wait(bar(B_FIN), 0, &dummy, err);
     }
@@ -590,8 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     TileGather<DQK, kGather> tg;
     bool aborted = false;
     int La = 0;
+    if (ntiles > 0) tg.load(idx_row, 0, n_eff, gt);
     for (int i = 0; i < ntiles && !aborted; ++i) {
-      tg.rows(kv, idx_row, i, n_eff, Tk, gt, err);
+      tg.resolve(kv, Tk, gt, err);
+      if (i + 1 < ntiles) tg.load(idx_row, i + 1, n_eff, gt);  // the next tile's indices, a tile ahead
       for (int c = 0; c < NCH; ++c, ++La) {
         const int slot = La % kRing;
         if (La >= kRing && !mbar_wait(bar(B_EMPTY + slot), ((La / kRing) - 1) & 1, s_abort, err, wait_limit)) {

@@ -213,9 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < 2; ++c)
 #pragma unroll
       for (int k = 0; k < 4; ++k)  // + 16 dims = + 32 bytes per row
-        mma_ss(tS, sdesc_sw128(kb + c * K_CHUNK, 16, 1024) + (uint64_t)(k * 2),
-               sdesc_sw128(sQ + c * Q_CHUNK, 16, 1024) + (uint64_t)(k * 2), kIdS, (c | k) != 0);
-    mma_commit(bar_s);
+        mma_ss_w(tS, sdesc_sw128(kb + c * K_CHUNK, 16, 1024) + (uint64_t)(k * 2),
+                 sdesc_sw128(sQ + c * Q_CHUNK, 16, 1024) + (uint64_t)(k * 2), kIdS, (c | k) != 0);
+    mma_commit_w(bar_s);
   };
 
   bool aborted = false;
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       landed(more);
     }
     if (named_bar_or(1, kThreads, false)) { aborted = true; break; }  // the tile has landed
-    if (warp == 4 && lane == 0) issue_s(i);
+    if (warp == 4) issue_s(i);  // the whole warp, one elected lane issues
     bool ok = true;
     if (worker) {
       ok = mbar_wait(bar_s, ph_s, s_abort, err, wait_limit);
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       landed(more);
     }
     if (named_bar_or(1, kThreads, false)) { aborted = true; break; }
-    if (warp == 4 && lane == 0) issue_s(i);
+    if (warp == 4) issue_s(i);  // the whole warp, one elected lane issues
     bool ok = true;
     if (worker) {
       ok = mbar_wait(bar_s, ph_s, s_abort, err, wait_limit);
@@ -344,24 +344,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
     }
     if (named_bar_or(1, kThreads, !ok)) { aborted = true; break; }  // M is in shared memory
-    if (warp == 4 && lane == 0) {
+    if (warp == 4) {
       tc_fence_after();
       const uint64_t ka = sdesc_sw128(sK + (uint32_t)(i & 1) * K_BUF, K_CHUNK, 1024);
       const uint64_t mb_hi = sdesc_sw128(sMhi, K_CHUNK, 1024);
       const uint64_t mb_lo = sdesc_sw128(sMlo, K_CHUNK, 1024);
 #pragma unroll
       for (int k = 0; k < kTile / 16; ++k) {  // + 16 slots = + 2048 bytes
-        mma_ss(tDQ, ka + (uint64_t)(k * 128), mb_hi + (uint64_t)(k * 128), kIdDQ, (i > 0 || k > 0) ? 1u : 0u);
-        mma_ss(tDQ, ka + (uint64_t)(k * 128), mb_lo + (uint64_t)(k * 128), kIdDQ, 1u);
+        mma_ss_w(tDQ, ka + (uint64_t)(k * 128), mb_hi + (uint64_t)(k * 128), kIdDQ, (i > 0 || k > 0) ? 1u : 0u);
+        mma_ss_w(tDQ, ka + (uint64_t)(k * 128), mb_lo + (uint64_t)(k * 128), kIdDQ, 1u);
       }
       const uint64_t ma_hi = sdesc_sw128(sMhi, 16, 1024), ma_lo = sdesc_sw128(sMlo, 16, 1024);
       const uint64_t qb = sdesc_sw128(sQ, Q_CHUNK, 1024);
 #pragma unroll
       for (int k = 0; k < kHeads / 16; ++k) {  // + 16 heads: + 32 bytes along A's rows, + 16 rows of Q
-        mma_ss(tDK, ma_hi + (uint64_t)(k * 2), qb + (uint64_t)(k * 128), kIdDK, k > 0 ? 1u : 0u);
-        mma_ss(tDK, ma_lo + (uint64_t)(k * 2), qb + (uint64_t)(k * 128), kIdDK, 1u);
+        mma_ss_w(tDK, ma_hi + (uint64_t)(k * 2), qb + (uint64_t)(k * 128), kIdDK, k > 0 ? 1u : 0u);
+        mma_ss_w(tDK, ma_lo + (uint64_t)(k * 2), qb + (uint64_t)(k * 128), kIdDK, 1u);
       }
-      mma_commit(bar_mm);
+      mma_commit_w(bar_mm);
     }
     ok = true;
     if (worker) {
@@ -419,9 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // every bulk reduction of this thread is complete before the CTA exits
   if (worker) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-  if (warp == 4 && lane == 0) {
+  if (warp == 4) {
     // every MMA of this CTA completes before the teardown frees TMEM
-    mma_commit(bar_fin);
+    mma_commit_w(bar_fin);
     volatile int dummy = 0;
     mbar_wait(bar_fin, 0, &dummy, err);
   }
