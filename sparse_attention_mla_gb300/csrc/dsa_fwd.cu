@@ -27,7 +27,9 @@
 //    would need M = 64 tiles that leave half of each TMEM lane quadrant idle.
 //  * P.V runs key rows 0..63 first, then rows 64..127, and signals after the
 //    first half: the next tile's rows 0..63 of every value chunk are
-//    gathered while the tensor core works on rows 64..127.
+//    gathered while the tensor core works on rows 64..127.  Rows 64..127 go
+//    channel pair by channel pair, each pair signalled once read, so the next
+//    tile's rows 64..127 of a pair are gathered while later pairs run.
 //  * Online softmax with the running max per head; a rescale of O^T happens
 //    only when some score exceeds the running max by more than 2^8 (lazy
 //    rescale), otherwise P uses the stale max.
@@ -88,6 +90,7 @@ struct Smem {
 constexpr int M_BAR_KV = 0;    // [9] chunk landed
 constexpr int M_BAR_PV = 80;   // P.V of the tile done
 constexpr int M_BAR_S = 112, M_BAR_P = 120, M_BAR_FIN = 128, M_BAR_PLO = 136, M_BAR_PVH = 144;
+constexpr int M_BAR_PVM = 152;  // [3]: key rows 64..127 of channel pair m (chunks 2m, 2m+1) read
 constexpr int M_TMEM = 192, M_NEFF = 196, M_ABORT = 200;
 constexpr int M_RED = 256;             // float [4][64]
 constexpr int M_STAT = M_RED + 1024;   // float [64]: running max per head
@@ -181,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_s = smem_u32(misc + M_BAR_S), bar_p = smem_u32(misc + M_BAR_P);
   const uint32_t bar_fin = smem_u32(misc + M_BAR_FIN);
   const uint32_t bar_plo = smem_u32(misc + M_BAR_PLO), bar_pvh = smem_u32(misc + M_BAR_PVH);
+  const uint32_t bar_pvm = smem_u32(misc + M_BAR_PVM);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + M_TMEM);
   int* s_neff = reinterpret_cast<int*>(misc + M_NEFF);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + M_ABORT);
@@ -199,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_s, 1);
     mbar_init(bar_p, 8);
     mbar_init(bar_pvh, 1);
+    for (int m = 0; m < 3; ++m) mbar_init(bar_pvm + 8 * m, 1);
     mbar_init(bar_plo, 4);  // the warps of key rows 64..127 (lane quadrants 2, 3)
     mbar_init(bar_fin, 1);
     *s_neff = 0;
@@ -296,21 +301,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss_w(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), lb0 + (uint64_t)(k * 128), kIdPV, 1u);
         }
         mma_commit_w(bar_pvh);  // rows 0..63 of the chunk slots (and of the P slot) are read
+        // Key rows 64..127 channel pair by channel pair, with a commit after each pair, so that
+        // the next tile's rows 64..127 of a pair are gathered while later pairs are multiplied.
+        // P_hi of pairs 0 and 1 first: the tensor core works on them while the workers move
+        // P_lo of rows 64..127 into the P slot's rows 0..63.
 #pragma unroll
-        for (int m = 0; m < kDv / 128; ++m) {
+        for (int m = 0; m < 2; ++m) {
 #pragma unroll
           for (int k = kHalf; k < 2 * kHalf; ++k)
             mma_ss_w(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV, 1u);
         }
-        // P_lo of rows 64..127, moved by the workers into the P slot's rows 0..63
         if (!warp_all(mbar_wait(bar_plo, i & 1, s_abort, err, wait_limit))) break;
         tc_fence_after();
 #pragma unroll
         for (int m = 0; m < kDv / 128; ++m) {
+          if (m >= 2) {
+#pragma unroll
+            for (int k = kHalf; k < 2 * kHalf; ++k)
+              mma_ss_w(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV, 1u);
+          }
 #pragma unroll
           for (int k = kHalf; k < 2 * kHalf; ++k)
             mma_ss_w(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)((k - kHalf) * 128),
                      kIdPV, 1u);
+          if (m < 3) mma_commit_w(bar_pvm + 8 * m);
         }
         mma_commit_w(bar_pv);  // P.V of this tile is complete
       }
@@ -480,16 +494,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         int rix[4];
         check_rows(nraw, rix);
         for (int c = 0; c < kDv / 64; ++c) gather_half<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, 0);
-        // rows 64..127 (and the RoPE chunk, which holds P) once P.V is complete
-        if (!mbar_wait(bar_pv, i & 1, s_abort, err, wait_limit)) {
-          aborted = true;
-        } else {
-          for (int c = 0; c < kDv / 64; ++c) {
+        // rows 64..127 of channel pair m once P.V has read them, and the RoPE chunk (which
+        // holds P) once P.V is complete
+        for (int m = 0; m < kDv / 128 && !aborted; ++m) {
+          if (!mbar_wait(m < 3 ? bar_pvm + 8 * m : bar_pv, i & 1, s_abort, err, wait_limit)) {
+            aborted = true;
+            break;
+          }
+#pragma unroll
+          for (int c = 2 * m; c < 2 * m + 2; ++c) {
             gather_half<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, 1);
             cp_async_arrive(bar_kv + 8 * c);  // covers this thread's copies of both halves
           }
-          if (NCH == 9) gather_chunk<DQK>(sKV + 8 * L::KV_CHUNK, kv, 8, tid, rix, bar_kv + 8 * 8);
         }
+        if (!aborted && NCH == 9) gather_chunk<DQK>(sKV + 8 * L::KV_CHUNK, kv, 8, tid, rix, bar_kv + 8 * 8);
         if (named_bar_or(bar_id, 128, aborted)) { aborted = true; break; }
       }
     }
