@@ -144,24 +144,52 @@ __device__ __forceinline__ int2 half_scan_count(const Half& hf, int n, int par) 
 
 // Exact (passes = 4): keep the best `target` of the cnt candidates (score
 // desc, index asc), stably, in place; returns v with "accept iff key > v".
-// Approximate (passes = 2): find the 16-bit key bucket that holds the
-// target-th best and keep every candidate at or above that bucket, stably: a
-// superset of the best `target` (so the final exact selection is unchanged)
-// in half the passes; returns the bucket floor minus one, again "accept iff
-// key > v".  *kept_out receives the number kept.
+// Approximate (passes = 2): find the key bucket that holds the target-th best
+// after two 8-bit digits and keep every candidate at or above that bucket,
+// stably: a superset of the best `target` (so the final exact selection is
+// unchanged) in half the passes; returns the bucket floor minus one, again
+// "accept iff key > v".  *kept_out receives the number kept.
+// The digits start just below the candidates' common key prefix (the bits
+// where the smallest and the largest key image agree): candidates near a
+// running threshold share sign and exponent, so digits taken from the top
+// would put nearly all of them into one histogram bin.
 __device__ uint32_t compact(const Half& hf, float* cs, int* ci, int cnt, int target, int& parity, int passes,
                             int* kept_out) {
-  // radix select: find the target-th largest key image (its top 8*passes bits)
-  uint32_t prefix = 0, pmask = 0;
+  // common prefix: min and max key image over the candidates
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  for (int e = hf.tid; e < cnt; e += 128) {
+    const uint32_t key = ordered(cs[e]);
+    kmin = min(kmin, key);
+    kmax = max(kmax, key);
+  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (hf.lane == 0) {
+    hf.hist[2 * hf.wq] = (int)kmin;
+    hf.hist[2 * hf.wq + 1] = (int)kmax;
+  }
+  named_bar(hf.bar, 128);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    kmin = min(kmin, (uint32_t)hf.hist[2 * w]);
+    kmax = max(kmax, (uint32_t)hf.hist[2 * w + 1]);
+  }
+  named_bar(hf.bar, 128);  // hist is cleared next
+  const uint32_t diff = kmin ^ kmax;
+  int top = diff ? 32 - __clz(diff) : 0;  // bits [top, 32) are common to every candidate
+  uint32_t pmask = top >= 32 ? 0u : ~((1u << top) - 1u);
+  uint32_t prefix = kmin & pmask;
+  // radix select of the target-th largest key image, 8 bits per pass below the resolved bits
   int kk = target;
-  for (int pass = 0; pass < passes; ++pass) {
-    const int shift = 24 - 8 * pass;
+  for (int pass = 0; pass < passes && top > 0; ++pass) {
+    const int shift = top > 8 ? top - 8 : 0;
+    const uint32_t dmask = (1u << (top - shift)) - 1u;  // 1..8 bits
     hf.hist[hf.tid] = 0;
     hf.hist[hf.tid + 128] = 0;
     named_bar(hf.bar, 128);
     for (int e = hf.tid; e < cnt; e += 128) {
       const uint32_t key = ordered(cs[e]);
-      if ((key & pmask) == prefix) atomicAdd(&hf.hist[(key >> shift) & 255], 1);
+      if ((key & pmask) == prefix) atomicAdd(&hf.hist[(key >> shift) & dmask], 1);
     }
     named_bar(hf.bar, 128);
     if (hf.wq == 0) {
@@ -194,7 +222,8 @@ __device__ uint32_t compact(const Half& hf, float* cs, int* ci, int cnt, int tar
     const int d = hf.sel[0];
     kk -= hf.sel[1];
     prefix |= (uint32_t)d << shift;
-    pmask |= 255u << shift;
+    pmask |= dmask << shift;
+    top = shift;
     named_bar(hf.bar, 128);  // sel is rewritten by the next pass
   }
   if (passes < 4) {
