@@ -44,9 +44,10 @@ def mla_flops(n_valid: int) -> tuple[float, float]:
 # L2 rates of this GPU for the two access patterns the MLA kernels live on, measured by
 # standalone microbenchmarks on a GB300 (all SMs, clocks at 2070 MHz): fp32 reductions of
 # 4-row x 128-byte segments at the selected rows (red.global.add.v4.f32, the backward's
-# pattern) and 16-byte cp.async gathers of selected 1152-byte rows.
+# pattern, replayed over the indexer's selection at 32k) and 16-byte cp.async gathers of
+# 128 random 1152-byte rows per tile by 256 threads, one tile in flight per SM.
 L2_RED_TBS = 6.9
-L2_GATHER_TBS = 8.9
+L2_GATHER_TBS = 17.5
 
 
 def l2_model(n_valid: int, n_tiles: int, fwd_ms: float, bwd_ms: float) -> dict:

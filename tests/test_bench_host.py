@@ -33,7 +33,9 @@ def test_l2_model_bytes_and_times():
     gat_f = 2 * 576 * n
     assert math.isclose(m["bwd"]["reduction_gb"], round(red / 1e9, 2))
     assert math.isclose(m["bwd"]["gather_gb"], round(gat_b / 1e9, 2))
-    t_b = (red / 6.9e12 + gat_b / 8.9e12) * 1e3
+    rr, rg = b.L2_RED_TBS * 1e12, b.L2_GATHER_TBS * 1e12  # the measured rates, bytes per second
+    assert m["rates_tbs"] == {"reduction": b.L2_RED_TBS, "gather": b.L2_GATHER_TBS}
+    t_b = (red / rr + gat_b / rg) * 1e3
     assert math.isclose(m["bwd"]["model_ms"], round(t_b, 3))
     assert math.isclose(m["bwd"]["frac"], round(t_b / 20.0, 4))
-    assert math.isclose(m["fwd"]["model_ms"], round(gat_f / 8.9e12 * 1e3, 3))
+    assert math.isclose(m["fwd"]["model_ms"], round(gat_f / rg * 1e3, 3))
