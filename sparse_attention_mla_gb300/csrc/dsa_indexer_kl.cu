@@ -177,16 +177,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tS = tmem, tDQ = tmem + 64, tDK = tmem + 128;
 
   // index of slot j (-1: invalid or beyond the prefix; out-of-range values are reported and masked)
-  auto slot_key = [&](int j) -> int {
-    if (j >= n_eff) return -1;
-    const int ix = __ldg(idx_row + j);
-    if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
-    return (ix >= 0 && ix < Tk) ? ix : -1;
+  // A slot's key in two steps: the load (issued a tile ahead of its gather, so that its memory
+  // latency hides behind the tile before) and the check (-1: none; bad indices are flagged).
+  auto raw_key = [&](int i) -> int {
+    const int j = i * kTile + tid;
+    return (j < n_eff) ? __ldg(idx_row + j) : -1;
+  };
+  auto check_key = [&](int raw) -> int {
+    if (raw < -1 || raw >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
+    return (raw >= 0 && raw < Tk) ? raw : -1;
   };
   // issue the gather of tile i's k_idx rows into buffer i & 1, one row per worker thread (zero-filled
-  // when invalid), as one cp.async group; returns this thread's key of the tile (-1: none)
-  auto gather = [&](int i) {
-    const int ix = slot_key(i * kTile + tid);
+  // when invalid), as one cp.async group; `raw` is this thread's loaded index of the tile; returns its
+  // key (-1: none)
+  auto gather = [&](int i, int raw) {
+    const int ix = check_key(raw);
     const __nv_bfloat16* src = k_idx + (ix >= 0 ? (size_t)ix * kDi : 0);
     const uint32_t dst = sK + (uint32_t)(i & 1) * K_BUF;
 #pragma unroll
@@ -221,12 +226,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool aborted = false;
   uint32_t ph_s = 0, ph_mm = 0;
   // ---- pass 1: indexer scores of the selected slots ----
-  int ix_next = (worker && ntiles > 0) ? gather(0) : -1;
+  int ix_next = (worker && ntiles > 0) ? gather(0, raw_key(0)) : -1;
+  int raw_next = (worker && ntiles > 1) ? raw_key(1) : -1;  // the next gather's indices, a tile ahead
   for (int i = 0; i < ntiles; ++i) {
     const int ix = ix_next;
     if (worker) {
       const bool more = i + 1 < ntiles;
-      if (more) ix_next = gather(i + 1);  // buffer (i + 1) & 1 was last read by tile i - 1's finished MMAs
+      if (more) {
+        ix_next = gather(i + 1, raw_next);  // buffer (i + 1) & 1 was last read by tile i - 1's finished MMAs
+        raw_next = (i + 2 < ntiles) ? raw_key(i + 2) : -1;
+      }
       landed(more);
     }
     if (named_bar_or(1, kThreads, false)) { aborted = true; break; }  // the tile has landed
@@ -256,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (worker && !aborted) {
     float imax = -INFINITY, psum = 0.f;
     for (int j = tid; j < n_eff; j += kWorkers) {
-      const int ix = slot_key(j);
+      const int ix = check_key(__ldg(idx_row + j));
       const float p = (ix >= 0) ? __ldg(prob + (size_t)t * K + j) : 0.f;
       s_P[j] = p;
       imax = fmaxf(imax, s_I[j]);
@@ -292,12 +301,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float logz = s_stats[0], inv_psum = s_stats[1];
 
   // ---- pass 2: the gradient ----
-  ix_next = (worker && active && ntiles > 0) ? gather(0) : -1;
+  ix_next = (worker && active && ntiles > 0) ? gather(0, raw_key(0)) : -1;
+  raw_next = (worker && active && ntiles > 1) ? raw_key(1) : -1;
   for (int i = 0; active && i < ntiles; ++i) {
     const int ix = ix_next;
     if (worker) {
       const bool more = i + 1 < ntiles;
-      if (more) ix_next = gather(i + 1);
+      if (more) {
+        ix_next = gather(i + 1, raw_next);
+        raw_next = (i + 2 < ntiles) ? raw_key(i + 2) : -1;
+      }
       landed(more);
     }
     if (named_bar_or(1, kThreads, false)) { aborted = true; break; }
