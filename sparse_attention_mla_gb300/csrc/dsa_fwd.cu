@@ -580,16 +580,458 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Few heads (H <= 16): the same computation with NH = 16 heads per CTA on the
+// MMA's N side instead of 64, so that a CTA for H = 8 does not multiply 56
+// zero heads.  P^T is split into bf16 hi + lo as above, but both halves sit side
+// by side in one K-major operand of 2 NH rows ([hi heads | lo heads], keys along
+// K), so one P.V MMA (N = 2 NH) forms O_hi and O_lo together; the epilogue adds
+// them.  P lives in a slot of its own: the tile's RoPE chunk is free once S^T is
+// done, and the next tile's RoPE rows are gathered during this tile's softmax.
+// Q is NH x Dqk (18 KiB at 576), so the tile buffer and P fit with room to spare.
+// ---------------------------------------------------------------------------
+template <int DQK, int NH>
+struct SmemFew {
+  static constexpr int NCH = DQK / 64;
+  static constexpr int Q_CHUNK = NH * 128;      // NH rows x 128 B (K-major B of S^T)
+  static constexpr int KV_CHUNK = kTile * 128;  // 128 keys x 128 B
+  static constexpr int P_BLOCK = 2 * NH * 128;  // one 64-key block of P: 2 NH rows x 128 B
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = (NCH * Q_CHUNK + 1023) / 1024 * 1024;
+  static constexpr int OFF_P = OFF_KV + NCH * KV_CHUNK;
+  static constexpr int OFF_MISC = OFF_P + 2 * P_BLOCK;
+  static constexpr int MISC = 2048;
+  static constexpr int TOTAL = OFF_MISC + MISC + 1024;  // + alignment slack
+  static_assert(TOTAL <= 232448, "shared memory budget");
+  static_assert(2 * NH * kDv * 2 <= NCH * KV_CHUNK, "output staging fits in the tile region");
+};
+
+// misc layout of the few-heads kernel (bytes): barriers as in the 64-head kernel, then
+constexpr int F_RED = 256;    // float [4 quadrants][NH]: per-quadrant maxima and sums
+constexpr int F_STAT = 768;   // float [NH]: running max per head (log2 units)
+constexpr int F_LSUM = 1024;  // float [NH]: softmax denominator per head
+
+// P element (row n of the [hi | lo] operand, key r) in the K-major 128B-swizzled layout: key block
+// r / 64 of P_BLOCK bytes, row n of 128 bytes, 16-byte unit (r % 64) / 8 swizzled with the row.
+template <int NH>
+__device__ __forceinline__ uint32_t p_off(int n, int r) {
+  const int kk = r & 63;
+  return (uint32_t)((r >> 6) * (2 * NH * 128) + n * 128 + ((((kk >> 3) ^ (n & 7))) << 4) + (kk & 7) * 2);
+}
+
+// Transposing butterfly over N values (N a power of two <= 32): v[0..N-1] per lane (lane = key,
+// index = head) -> lane l returns the reduction over the warp's 32 keys of head l % N.
+template <int N, bool MAX>
+__device__ __forceinline__ float warp_transpose_reduce_n(float (&v)[N], int lane) {
+#pragma unroll
+  for (int o = 16; o >= N; o >>= 1) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const float x = __shfl_xor_sync(0xffffffffu, v[i], o);
+      v[i] = MAX ? fmaxf(v[i], x) : v[i] + x;
+    }
+  }
+#pragma unroll
+  for (int o = N / 2; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      float send = upper ? v[i] : v[i + o];
+      float keep = upper ? v[i + o] : v[i];
+      float recv = __shfl_xor_sync(0xffffffffu, send, o);
+      v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  return v[0];
+}
+
+template <int DQK, int NH>
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_fwd_few_kernel(const __nv_bfloat16* __restrict__ kv, const __nv_bfloat16* __restrict__ q,
+                              const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ topk_len, int T,
+                              int Tk, int H, int K, float sl2e, const float* __restrict__ sink,
+                              __nv_bfloat16* __restrict__ out, __nv_bfloat16* __restrict__ out_lo,
+                              float* __restrict__ lse, int* __restrict__ err, long long wait_limit) {
+  using L = SmemFew<DQK, NH>;
+  constexpr int NCH = L::NCH;
+  constexpr int NHH = NH / 2;  // heads per softmax thread
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sQ = smem_u32(smem + L::OFF_Q);
+  const uint32_t sKV = smem_u32(smem + L::OFF_KV);
+  const uint32_t sP = smem_u32(smem + L::OFF_P);
+  uint8_t* misc = smem + L::OFF_MISC;
+  const uint32_t bar_kv = smem_u32(misc + M_BAR_KV), bar_pv = smem_u32(misc + M_BAR_PV);
+  const uint32_t bar_s = smem_u32(misc + M_BAR_S), bar_p = smem_u32(misc + M_BAR_P);
+  const uint32_t bar_fin = smem_u32(misc + M_BAR_FIN), bar_pvh = smem_u32(misc + M_BAR_PVH);
+  const uint32_t bar_pvm = smem_u32(misc + M_BAR_PVM);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + M_TMEM);
+  int* s_neff = reinterpret_cast<int*>(misc + M_NEFF);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(misc + M_ABORT);
+  float* s_red = reinterpret_cast<float*>(misc + F_RED);
+  float* s_stat = reinterpret_cast<float*>(misc + F_STAT);
+  float* s_lsum = reinterpret_cast<float*>(misc + F_LSUM);
+
+  const int t = blockIdx.x;
+  const int hg = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t* idx_row = topk_idx + (size_t)t * K;
+
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < NCH; ++c) mbar_init(bar_kv + 8 * c, kWorkers);
+    mbar_init(bar_pv, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_p, 8);
+    mbar_init(bar_pvh, 1);
+    for (int m = 0; m < 3; ++m) mbar_init(bar_pvm + 8 * m, 1);
+    mbar_init(bar_fin, 1);
+    *s_neff = 0;
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(s_tmem), 256);
+    tmem_relinquish();
+  }
+  __syncthreads();
+
+  const int tid = threadIdx.x - 32;  // worker id 0..255 (negative for warp 0)
+  // ---- valid prefix length and Q staging (workers) ----
+  if (warp >= 1) {
+    if (topk_len != nullptr) {
+      if (tid == 0) {
+        int n = topk_len[t];
+        *s_neff = n < 0 ? 0 : (n > K ? K : n);
+      }
+    } else {
+      int last = 0;
+      for (int j = tid; j < K; j += kWorkers)
+        if (idx_row[j] >= 0) last = j + 1;
+      if (last) atomicMax(s_neff, last);
+    }
+    if (tid < NH) {  // running max per head (log2 units), from the sink logit when there is one
+      const int h = hg * NH + tid;
+      s_stat[tid] = (sink != nullptr && h < H) ? __ldg(sink + h) * 1.4426950408889634f : -INFINITY;
+    }
+    // Q [NH heads, DQK] -> NCH chunks of [NH rows x 128 B], 128B swizzle; heads >= H are zero.
+    constexpr int UNITS = NH * NCH * 8;
+    const uint64_t pol = l2_evict_first_policy();
+    for (int u = tid; u < UNITS; u += kWorkers) {
+      const int hh = u / (NCH * 8);
+      const int rem = u - hh * (NCH * 8);
+      const int c = rem >> 3, uc = rem & 7;
+      const int h = hg * NH + hh;
+      const bool ok = h < H;
+      cp_async16_hint(sQ + c * L::Q_CHUNK + sw128_off(hh, uc),
+                      q + (ok ? ((size_t)t * H + h) * DQK + c * 64 + uc * 8 : 0), ok ? 16u : 0u, pol);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  const int n_eff = *s_neff;
+  const int ntiles = (n_eff + kTile - 1) / kTile;
+  const uint32_t tmem = *s_tmem;
+  const uint32_t tS = tmem;       // S^T: 128 lanes x NH columns
+  const uint32_t tO = tmem + 32;  // [O_hi^T | O_lo^T]: 4 channel tiles x 2 NH columns
+
+  if (warp == 0) {
+    // ======================= MMA issuer (the whole warp, one elected lane issues) =======================
+    {
+      constexpr uint32_t kIdS = idesc_bf16(128, NH, false, false);       // A = KV (K-major), B = Q (K-major)
+      constexpr uint32_t kIdPV = idesc_bf16(128, 2 * NH, true, false);   // A = V^T (MN-major), B = [P_hi|P_lo] (K-major)
+      for (int i = 0; i < ntiles; ++i) {
+        bool stop = false;
+        const uint64_t a00 = sdesc_sw128(sKV, 16, 1024), b00 = sdesc_sw128(sQ, 16, 1024);
+        for (int c = 0; c < NCH && !stop;) {
+          if (!warp_all(mbar_wait(bar_kv + 8 * c, i & 1, s_abort, err, wait_limit))) { stop = true; break; }
+          int ce = c + 1;
+          while (ce < NCH && warp_all(mbar_test(bar_kv + 8 * ce, i & 1))) ++ce;
+          fence_proxy_async_smem();
+          tc_fence_after();
+          for (; c < ce; ++c) {
+            const uint64_t a0 = a00 + (uint64_t)((c * L::KV_CHUNK) >> 4), b0 = b00 + (uint64_t)((c * L::Q_CHUNK) >> 4);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ss_w(tS, a0 + (uint64_t)(k * 2), b0 + (uint64_t)(k * 2), kIdS, (c | k) != 0);
+          }
+        }
+        if (stop) break;
+        mma_commit_w(bar_s);
+        if (!warp_all(mbar_wait(bar_p, i & 1, s_abort, err, wait_limit))) break;
+        tc_fence_after();
+        const uint64_t va0 = sdesc_sw128(sKV, L::KV_CHUNK, 1024);
+        const uint64_t pb0 = sdesc_sw128(sP, 16, 1024);
+        constexpr uint64_t kPair = (2 * L::KV_CHUNK) >> 4;  // descriptor step between channel pairs
+        constexpr uint64_t kPBlk = L::P_BLOCK >> 4;         // descriptor step between 64-key blocks of P
+        // key rows 0..63 for every channel pair, then rows 64..127 pair by pair with a commit after each
+#pragma unroll
+        for (int m = 0; m < kDv / 128; ++m) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)  // + 16 key rows: + 2048 B in V^T, + 32 B along P's rows
+            mma_ss_w(tO + m * 2 * NH, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 2), kIdPV,
+                     (i > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit_w(bar_pvh);
+#pragma unroll
+        for (int m = 0; m < kDv / 128; ++m) {
+#pragma unroll
+          for (int k = 4; k < 8; ++k)
+            mma_ss_w(tO + m * 2 * NH, va0 + m * kPair + (uint64_t)(k * 128), pb0 + kPBlk + (uint64_t)((k - 4) * 2),
+                     kIdPV, 1u);
+          if (m < 3) mma_commit_w(bar_pvm + 8 * m);
+        }
+        mma_commit_w(bar_pv);
+      }
+      mma_commit_w(bar_fin);
+      volatile int dummy = 0;
+      mbar_wait(bar_fin, 0, &dummy, err);
+    }
+    __syncwarp();
+  } else {
+    // ======================= gather + softmax + epilogue =======================
+    const int wk = warp - 1;       // 0..7
+    const int qd = warp & 3;       // TMEM lane quadrant this warp may access
+    const int ch = wk >> 2;        // head half: heads ch*NHH .. ch*NHH+NHH-1
+    const int r = qd * 32 + lane;  // key row of the tile / channel row of an O^T tile
+    const int bar_id = 1 + ch;     // named barrier of the 128 threads of this half
+    auto load_raw = [&](int i, int (&raw)[4]) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = i * kTile + (tid >> 3) + 32 * e;
+        raw[e] = (j < n_eff) ? __ldg(idx_row + j) : -1;
+      }
+    };
+    auto check_rows = [&](const int (&raw)[4], int (&rix)[4]) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int ix = raw[e];
+        rix[e] = (ix >= 0 && ix < Tk) ? ix : -1;
+        if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
+      }
+    };
+    int nraw[4];
+    if (ntiles > 0) {
+      int rix[4];
+      load_raw(0, nraw);
+      check_rows(nraw, rix);
+      for (int c = 0; c < NCH; ++c) gather_chunk<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, bar_kv + 8 * c);
+    }
+    const float* m_run = s_stat + ch * NHH;
+    float l_part[NHH];
+#pragma unroll
+    for (int h = 0; h < NHH; ++h) l_part[h] = 0.f;
+    bool aborted = false;
+    for (int i = 0; i < ntiles; ++i) {
+      const int j = i * kTile + r;
+      const int ixw = (j < n_eff) ? __ldg(idx_row + j) : -1;
+      const bool more = i + 1 < ntiles;
+      if (more) load_raw(i + 1, nraw);
+      const bool got = mbar_wait(bar_s, i & 1, s_abort, err, wait_limit);
+      if (named_bar_or(bar_id, 128, !got)) { aborted = true; break; }
+      tc_fence_after();
+      // S^T of the tile is read: the next tile's RoPE rows may be gathered now (P has its own slot)
+      int rix[4];
+      if (more) {
+        check_rows(nraw, rix);
+        if (NCH == 9) gather_chunk<DQK>(sKV + 8 * L::KV_CHUNK, kv, 8, tid, rix, bar_kv + 8 * 8);
+      }
+      uint32_t sv[NHH];
+      if constexpr (NHH == 8) tmem_ld8(tmem_addr(tS + ch * NHH, qd * 32, 0), sv);
+      else tmem_ld16(tmem_addr(tS + ch * NHH, qd * 32, 0), sv);
+      tmem_ld_wait();
+      const bool valid = ixw >= 0 && ixw < Tk;
+      float z[NHH];
+#pragma unroll
+      for (int h = 0; h < NHH; ++h) z[h] = valid ? __uint_as_float(sv[h]) * sl2e : -INFINITY;
+      bool need = (i == 0);
+      if (!need) {
+        bool mine = false;
+#pragma unroll
+        for (int h = 0; h < NHH; ++h) mine |= z[h] > m_run[h] + kRescaleThreshold;
+        need = named_bar_or(bar_id, 128, mine);
+      }
+      if (need) {
+        float v[NHH];
+#pragma unroll
+        for (int h = 0; h < NHH; ++h) v[h] = z[h];
+        const float wmax = warp_transpose_reduce_n<NHH, true>(v, lane);  // head lane % NHH of this warp's keys
+        if (lane < NHH) s_red[qd * NH + ch * NHH + lane] = wmax;
+        named_bar(bar_id, 128);
+        const int hl = lane % NHH;
+        const float bm = fmaxf(fmaxf(s_red[ch * NHH + hl], s_red[NH + ch * NHH + hl]),
+                               fmaxf(s_red[2 * NH + ch * NHH + hl], s_red[3 * NH + ch * NHH + hl]));
+        const float mo_lane = s_stat[ch * NHH + hl];
+        const float mn = fmaxf(mo_lane, bm);
+        named_bar(bar_id, 128);
+        if (qd == 0 && lane < NHH) s_stat[ch * NHH + lane] = mn;
+        named_bar(bar_id, 128);
+        float alpha[NHH];
+        bool any = false;
+#pragma unroll
+        for (int h = 0; h < NHH; ++h) {
+          const float mo = __shfl_sync(0xffffffffu, mo_lane, h);
+          const float mnew = m_run[h];
+          alpha[h] = (mo == -INFINITY) ? 0.f : exp2f(mo - mnew);
+          any |= (i > 0) && (alpha[h] != 1.f);
+          l_part[h] *= alpha[h];
+        }
+        if (any) {
+          // [O_hi^T | O_lo^T] is complete for the previous tile (bar_s of this tile follows those MMAs)
+#pragma unroll 1
+          for (int mt = 0; mt < kDv / 128; ++mt) {
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+              const uint32_t ta = tmem_addr(tO + mt * 2 * NH + part * NH + ch * NHH, qd * 32, 0);
+              uint32_t ov[NHH];
+              if constexpr (NHH == 8) tmem_ld8(ta, ov);
+              else tmem_ld16(ta, ov);
+              tmem_ld_wait();
+#pragma unroll
+              for (int h = 0; h < NHH; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+              if constexpr (NHH == 8) tmem_st8(ta, ov);
+              else tmem_st16(ta, ov);
+            }
+          }
+          tmem_st_wait();
+        }
+      }
+      // P_hi into rows ch*NHH.., P_lo into rows NH + ch*NHH.. of the [hi | lo] operand, key r along K
+#pragma unroll
+      for (int h = 0; h < NHH; ++h) {
+        const float mh = m_run[h];
+        const float mu = (mh == -INFINITY) ? 0.f : mh;
+        const float p = exp2f(z[h] - mu);
+        l_part[h] += p;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(p);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
+        const int n = ch * NHH + h;
+        st_shared_u16(sP + p_off<NH>(n, r), __bfloat16_as_ushort(hi));
+        st_shared_u16(sP + p_off<NH>(NH + n, r), __bfloat16_as_ushort(lo));
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p);
+      // rows 0..63 of every value chunk once the first key half of P.V has read them, rows 64..127
+      // of channel pair m once pair m is read
+      {
+        const bool okh = mbar_wait(bar_pvh, i & 1, s_abort, err, wait_limit);
+        if (named_bar_or(bar_id, 128, !okh)) { aborted = true; break; }
+      }
+      if (more) {
+        for (int c = 0; c < kDv / 64; ++c) gather_half<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, 0);
+        for (int m = 0; m < kDv / 128 && !aborted; ++m) {
+          if (!mbar_wait(m < 3 ? bar_pvm + 8 * m : bar_pv, i & 1, s_abort, err, wait_limit)) {
+            aborted = true;
+            break;
+          }
+#pragma unroll
+          for (int c = 2 * m; c < 2 * m + 2; ++c) {
+            gather_half<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, 1);
+            cp_async_arrive(bar_kv + 8 * c);
+          }
+        }
+        if (named_bar_or(bar_id, 128, aborted)) { aborted = true; break; }
+      }
+    }
+    if (!aborted && ntiles > 0) {
+      const bool got = mbar_wait(bar_pv, (ntiles - 1) & 1, s_abort, err, wait_limit);
+      aborted = named_bar_or(bar_id, 128, !got);
+      tc_fence_after();
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    // ---- epilogue: l per head, lse, out = (O_hi + O_lo)^T / l ----
+    const float lsum = warp_transpose_reduce_n<NHH, false>(l_part, lane);
+    named_bar(bar_id, 128);
+    if (lane < NHH) s_red[qd * NH + ch * NHH + lane] = lsum;
+    named_bar(bar_id, 128);
+    if (qd == 0 && lane < NHH) {
+      const int hh = ch * NHH + lane;
+      const float mh = s_stat[hh];
+      const int hl = hg * NH + hh;
+      const float s2 = (sink != nullptr && hl < H) ? __ldg(sink + hl) * 1.4426950408889634f : -INFINITY;
+      const float lsink = (s2 > -INFINITY) ? exp2f(s2 - mh) : 0.f;
+      const float lt = s_red[hh] + s_red[NH + hh] + s_red[2 * NH + hh] + s_red[3 * NH + hh] + lsink;
+      if (hl < H) lse[(size_t)t * H + hl] = (lt > 0.f) ? (mh * 0.69314718055994531f + logf(lt)) : -INFINITY;
+      s_lsum[hh] = lt;
+    }
+    named_bar(bar_id, 128);
+    float inv[NHH];
+#pragma unroll
+    for (int h = 0; h < NHH; ++h) {
+      const float l = s_lsum[ch * NHH + h];
+      inv[h] = (l > 0.f) ? 1.f / l : 0.f;
+    }
+    uint8_t* stage = smem + L::OFF_KV;
+    uint8_t* stage_lo = stage + NH * kDv * 2;
+#pragma unroll 1
+    for (int mt = 0; mt < kDv / 128; ++mt) {
+      uint32_t oh[NHH], ol[NHH];
+      if (ntiles > 0 && !aborted) {
+        const uint32_t ta = tmem_addr(tO + mt * 2 * NH + ch * NHH, qd * 32, 0);
+        if constexpr (NHH == 8) {
+          tmem_ld8(ta, oh);
+          tmem_ld8(ta + NH, ol);
+        } else {
+          tmem_ld16(ta, oh);
+          tmem_ld16(ta + NH, ol);
+        }
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int h = 0; h < NHH; ++h) oh[h] = ol[h] = 0u;
+      }
+      const int c = mt * 128 + qd * 32 + lane;
+#pragma unroll
+      for (int h = 0; h < NHH; ++h) {
+        const float o = (__uint_as_float(oh[h]) + __uint_as_float(ol[h])) * inv[h];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(o);
+        reinterpret_cast<__nv_bfloat16*>(stage)[(ch * NHH + h) * kDv + c] = hi;
+        if (out_lo) reinterpret_cast<__nv_bfloat16*>(stage_lo)[(ch * NHH + h) * kDv + c] =
+            __float2bfloat16_rn(o - __bfloat162float(hi));
+      }
+    }
+    named_bar(3, kWorkers);
+    const int hcount = min(NH, H - hg * NH);
+    const size_t gbase = ((size_t)t * H + hg * NH) * kDv;
+    const uint64_t pol = l2_evict_first_policy();
+    for (int u = tid; u < hcount * (kDv / 8); u += kWorkers) {
+      stg16_hint(reinterpret_cast<uint4*>(out + gbase) + u, reinterpret_cast<const uint4*>(stage)[u], pol);
+      if (out_lo) stg16_hint(reinterpret_cast<uint4*>(out_lo + gbase) + u, reinterpret_cast<const uint4*>(stage_lo)[u], pol);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
 template <int DQK>
 dsa_status_t launch(const void* kv, const void* q, const int32_t* idx, const int32_t* len, int T, int Tk, int H,
                     int K, float scale, const float* sink, void* out, void* out_lo, float* lse, int* err,
                     cudaStream_t s) {
+  const float sl2e = scale * 1.4426950408889634f;
+  if (H <= 16) {  // few heads: 16 per CTA on the MMA's N side
+    constexpr int NH = 16;
+    using F = SmemFew<DQK, NH>;
+    dsa_status_t st = configure_kernel_smem(reinterpret_cast<const void*>(sparse_mla_fwd_few_kernel<DQK, NH>),
+                                            F::TOTAL, "configuring sparse_mla_fwd_few_kernel");
+    if (st != DSA_OK) return st;
+    sparse_mla_fwd_few_kernel<DQK, NH><<<dim3(T, 1), kThreads, F::TOTAL, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(kv), reinterpret_cast<const __nv_bfloat16*>(q), idx, len, T, Tk, H,
+        K, sl2e, sink, reinterpret_cast<__nv_bfloat16*>(out), reinterpret_cast<__nv_bfloat16*>(out_lo), lse, err,
+        wait_limit_cycles());
+    return cuda_check(cudaGetLastError(), "launching sparse_mla_fwd_few_kernel");
+  }
   using L = Smem<DQK>;
   dsa_status_t st = configure_kernel_smem(reinterpret_cast<const void*>(sparse_mla_fwd_kernel<DQK>), L::TOTAL,
                                           "configuring sparse_mla_fwd_kernel");
   if (st != DSA_OK) return st;
   dim3 grid(T, (H + kHeads - 1) / kHeads);
-  const float sl2e = scale * 1.4426950408889634f;
   sparse_mla_fwd_kernel<DQK><<<grid, kThreads, L::TOTAL, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(kv), reinterpret_cast<const __nv_bfloat16*>(q), idx, len, T, Tk, H, K,
       sl2e, sink, reinterpret_cast<__nv_bfloat16*>(out), reinterpret_cast<__nv_bfloat16*>(out_lo), lse, err,

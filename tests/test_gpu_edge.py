@@ -49,16 +49,18 @@ def fwd_bwd_vs_oracle(q, kv, dout, idx, scale, ln=None, stress=False):
         assert rf <= REL_FRO, f"dq: rel_fro={rf:.3e}"
 
 
-def test_topk_one():
+@pytest.mark.parametrize("H", [64, 16])  # the 64-head forward and the few-heads one (H <= 16)
+def test_topk_one(H):
     # K = 1: each row attends to exactly one key (P = 1, dS = 0, dkv = dO on that row)
-    q, kv, dout, idx = make_case(40, 100, 64, 576, 1, 11)
+    q, kv, dout, idx = make_case(40, 100, H, 576, 1, 11)
     fwd_bwd_vs_oracle(q, kv, dout, idx, 192 ** -0.5)
 
 
-def test_growing_scores_rescale_running_max():
+@pytest.mark.parametrize("H", [64, 8])  # the 64-head forward and the few-heads one (H <= 16)
+def test_growing_scores_rescale_running_max(H):
     # kv rows scaled up with the key index, slots ascending: every new 128-slot tile raises the
     # running max by far more than the lazy-rescale threshold, so O is rescaled tile after tile
-    q, kv, dout, idx = make_case(24, 700, 64, 576, 600, 12)
+    q, kv, dout, idx = make_case(24, 700, H, 576, 600, 12)
     ramp = (1.0 + torch.arange(kv.shape[0], dtype=torch.float32) / 120.0)[:, None]
     kv = (kv.float() * ramp).to(torch.bfloat16)
     fwd_bwd_vs_oracle(q, kv, dout, idx, 0.25, stress=True)
