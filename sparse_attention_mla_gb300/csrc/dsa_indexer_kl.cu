@@ -62,10 +62,11 @@ constexpr int M_STATS = 48;                         // float [3]: logZ, 1/psum, 
 constexpr int M_W = 64;                             // float [64]
 constexpr int M_DW = M_W + 256;                     // float [64]
 constexpr int M_RED = M_DW + 256;                   // float [4]
-constexpr int MISC = 1024;
+constexpr int M_KEY = 1024;                         // int [2][128]: the keys of the next two tiles
+constexpr int MISC = 2048;
 constexpr int TOTAL = OFF_MISC + MISC + 1024;       // + alignment slack
 static_assert(TOTAL <= 232448, "shared memory budget");
-static_assert(M_RED + 16 <= MISC, "misc layout");
+static_assert(M_RED + 16 <= M_KEY && M_KEY + 2 * kTile * 4 <= MISC, "misc layout");
 
 // Reduction over the 128 worker threads (named barrier 2); every worker gets the result.
 template <bool MAX>
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* s_w = reinterpret_cast<float*>(misc + M_W);
   float* s_dw = reinterpret_cast<float*>(misc + M_DW);
   float* s_red = reinterpret_cast<float*>(misc + M_RED);
+  int* s_key = reinterpret_cast<int*>(misc + M_KEY);
 
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -187,18 +189,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (raw < -1 || raw >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
     return (raw >= 0 && raw < Tk) ? raw : -1;
   };
-  // issue the gather of tile i's k_idx rows into buffer i & 1, one row per worker thread (zero-filled
-  // when invalid), as one cp.async group; `raw` is this thread's loaded index of the tile; returns its
-  // key (-1: none)
-  auto gather = [&](int i, int raw) {
-    const int ix = check_key(raw);
-    const __nv_bfloat16* src = k_idx + (ix >= 0 ? (size_t)ix * kDi : 0);
+  // Issue the gather of tile i's k_idx rows into buffer i & 1 as one cp.async group: 16 lanes per
+  // 256-byte row, so that each instruction covers two contiguous rows; the rows' keys come from the
+  // table s_key[i & 1] (written a tile ahead by the thread that owns each row; -1 zero-fills).
+  auto gather_rows = [&](int i) {
+    const int* keys = s_key + (i & 1) * kTile;
     const uint32_t dst = sK + (uint32_t)(i & 1) * K_BUF;
+    const int u = tid & 15;
 #pragma unroll
-    for (int u = 0; u < 16; ++u)
-      cp_async16(dst + (u >> 3) * K_CHUNK + sw128_off(tid, u & 7), src + u * 8, ix >= 0 ? 16u : 0u);
+    for (int e = 0; e < kTile / 8; ++e) {
+      const int row = (tid >> 4) + 8 * e;
+      const int ix = keys[row];
+      cp_async16(dst + (u >> 3) * K_CHUNK + sw128_off(row, u & 7), k_idx + (ix >= 0 ? (size_t)ix * kDi : 0) + u * 8,
+                 ix >= 0 ? 16u : 0u);
+    }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    return ix;
+  };
+  // This thread's keys of tiles i and i + 1 (its own row), the raw index of tile i + 2, and the table
+  // entries: the keys of tiles 0 and 1 before the first gather, then that of tile i + 2 at the end of
+  // tile i (gather i + 2 follows the tile's last barrier; the table half it reuses was read by gather i).
+  int ixa = -1, ixb = -1, rawc = -1;
+  auto start_pass = [&]() {
+    ixa = check_key(raw_key(0));
+    s_key[tid] = ixa;
+    ixb = (ntiles > 1) ? check_key(raw_key(1)) : -1;
+    s_key[kTile + tid] = ixb;
+    rawc = (ntiles > 2) ? raw_key(2) : -1;
+    named_bar(2, kWorkers);
+    gather_rows(0);
+  };
+  auto end_tile = [&](int i) {
+    const int kc = (i + 2 < ntiles) ? check_key(rawc) : -1;
+    if (i + 2 < ntiles) s_key[((i + 2) & 1) * kTile + tid] = kc;
+    ixa = ixb;
+    ixb = kc;
+    rawc = (i + 3 < ntiles) ? raw_key(i + 3) : -1;
   };
   // tile i (its group, and not the one issued after it) has landed and is visible to the tensor core
   auto landed = [&](bool one_more_in_flight) {
@@ -226,16 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool aborted = false;
   uint32_t ph_s = 0, ph_mm = 0;
   // ---- pass 1: indexer scores of the selected slots ----
-  int ix_next = (worker && ntiles > 0) ? gather(0, raw_key(0)) : -1;
-  int raw_next = (worker && ntiles > 1) ? raw_key(1) : -1;  // the next gather's indices, a tile ahead
+  if (worker && ntiles > 0) start_pass();
   for (int i = 0; i < ntiles; ++i) {
-    const int ix = ix_next;
+    const int ix = ixa;
     if (worker) {
       const bool more = i + 1 < ntiles;
-      if (more) {
-        ix_next = gather(i + 1, raw_next);  // buffer (i + 1) & 1 was last read by tile i - 1's finished MMAs
-        raw_next = (i + 2 < ntiles) ? raw_key(i + 2) : -1;
-      }
+      if (more) gather_rows(i + 1);  // buffer (i + 1) & 1 was last read by tile i - 1's finished MMAs
       landed(more);
     }
     if (named_bar_or(1, kThreads, false)) { aborted = true; break; }  // the tile has landed
@@ -256,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j < n_eff) s_I[j] = (ix >= 0) ? score : -INFINITY;
       }
       tc_fence_before();
+      end_tile(i);
     }
     ph_s ^= 1;
     if (named_bar_or(1, kThreads, !ok)) { aborted = true; break; }  // S is read: TMEM and the tile are free
@@ -301,16 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float logz = s_stats[0], inv_psum = s_stats[1];
 
   // ---- pass 2: the gradient ----
-  ix_next = (worker && active && ntiles > 0) ? gather(0, raw_key(0)) : -1;
-  raw_next = (worker && active && ntiles > 1) ? raw_key(1) : -1;
+  if (worker && active && ntiles > 0) start_pass();
   for (int i = 0; active && i < ntiles; ++i) {
-    const int ix = ix_next;
+    const int ix = ixa;
     if (worker) {
       const bool more = i + 1 < ntiles;
-      if (more) {
-        ix_next = gather(i + 1, raw_next);
-        raw_next = (i + 2 < ntiles) ? raw_key(i + 2) : -1;
-      }
+      if (more) gather_rows(i + 1);
       landed(more);
     }
     if (named_bar_or(1, kThreads, false)) { aborted = true; break; }
@@ -404,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
+      end_tile(i);
     }
     ph_s ^= 1;
     ph_mm ^= 1;
