@@ -39,7 +39,8 @@ namespace dsa {
 namespace kl {
 
 constexpr int kWorkers = 128;             // warps 0-3
-constexpr int kThreads = kWorkers + 32;   // + the MMA warp (warp 4)
+constexpr int kPass1 = kWorkers + 32;     // + the MMA warp (warp 4): the threads of the first pass
+constexpr int kThreads = kPass1 + 128;    // + the dK drain warps (warps 5-8)
 constexpr int kHeads = 64;                // indexer heads (padded)
 constexpr int kDi = 128;                  // indexer head dim
 constexpr int kTile = 128;                // slots per tile (MMA M)
@@ -58,6 +59,9 @@ constexpr int OFF_I = OFF_DKS + kTile * DK_PITCH;   // float [kMaxK]: indexer sc
 constexpr int OFF_P = OFF_I + kMaxK * 4;            // float [kMaxK]: attention slot probabilities
 constexpr int OFF_MISC = OFF_P + kMaxK * 4;
 constexpr int M_BAR_S = 0, M_BAR_MM = 8, M_BAR_FIN = 16, M_TMEM = 32, M_NEFF = 36, M_ABORT = 40, M_ACTIVE = 44;
+// second pass: tile landed, S read, M written, dK buffer b read (two), products into dK buffer b done (two;
+// the drain warps wait on these, so that a phase of the buffer they drain cannot be overtaken)
+constexpr int M_BAR_LAND = 600, M_BAR_SFREE = 608, M_BAR_M = 616, M_BAR_DKF = 624, M_BAR_MMD = 640;
 constexpr int M_STATS = 48;                         // float [3]: logZ, 1/psum, (spare)
 constexpr int M_W = 64;                             // float [64]
 constexpr int M_DW = M_W + 256;                     // float [64]
@@ -66,7 +70,7 @@ constexpr int M_KEY = 1024;                         // int [2][128]: the keys of
 constexpr int MISC = 2048;
 constexpr int TOTAL = OFF_MISC + MISC + 1024;       // + alignment slack
 static_assert(TOTAL <= 232448, "shared memory budget");
-static_assert(M_RED + 16 <= M_KEY && M_KEY + 2 * kTile * 4 <= MISC, "misc layout");
+static_assert(M_RED + 16 <= M_BAR_LAND && M_BAR_MMD + 16 <= M_KEY && M_KEY + 2 * kTile * 4 <= MISC, "misc layout");
 
 // Reduction over the 128 worker threads (named barrier 2); every worker gets the result.
 template <bool MAX>
@@ -115,6 +119,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* misc = smem + OFF_MISC;
   const uint32_t bar_s = smem_u32(misc + M_BAR_S), bar_mm = smem_u32(misc + M_BAR_MM);
   const uint32_t bar_fin = smem_u32(misc + M_BAR_FIN);
+  const uint32_t bar_land = smem_u32(misc + M_BAR_LAND), bar_sfree = smem_u32(misc + M_BAR_SFREE);
+  const uint32_t bar_m = smem_u32(misc + M_BAR_M), bar_dkf = smem_u32(misc + M_BAR_DKF);
+  const uint32_t bar_mmd = smem_u32(misc + M_BAR_MMD);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + M_TMEM);
   int* s_neff = reinterpret_cast<int*>(misc + M_NEFF);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + M_ABORT);
@@ -135,13 +142,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_s, 1);
     mbar_init(bar_mm, 1);
     mbar_init(bar_fin, 1);
+    mbar_init(bar_land, kWorkers / 32);
+    mbar_init(bar_sfree, kWorkers / 32);
+    mbar_init(bar_m, kWorkers / 32);
+    mbar_init(bar_dkf, 4);
+    mbar_init(bar_dkf + 8, 4);
+    mbar_init(bar_mmd, 1);
+    mbar_init(bar_mmd + 8, 1);
     *s_neff = 0;
     *s_abort = 0;
     *s_active = 0;
     fence_mbar_init();
   }
   if (warp == 4) {
-    tmem_alloc(smem_u32(s_tmem), 256);
+    tmem_alloc(smem_u32(s_tmem), 512);
     tmem_relinquish();
   }
   __syncthreads();  // the counters are initialised before any worker adds to them
@@ -176,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_eff = *s_neff;
   const int ntiles = (n_eff + kTile - 1) / kTile;
   const uint32_t tmem = *s_tmem;
-  const uint32_t tS = tmem, tDQ = tmem + 64, tDK = tmem + 128;
+  const uint32_t tS = tmem, tDQ = tmem + 64, tDK = tmem + 128;  // dK: two buffers of 128 columns
 
   // index of slot j (-1: invalid or beyond the prefix; out-of-range values are reported and masked)
   // A slot's key in two steps: the load (issued a tile ahead of its gather, so that its memory
@@ -249,17 +263,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   bool aborted = false;
-  uint32_t ph_s = 0, ph_mm = 0;
+  uint32_t ph_s = 0;  // phase parity of bar_s, which counts the S products of both passes
   // ---- pass 1: indexer scores of the selected slots ----
   if (worker && ntiles > 0) start_pass();
-  for (int i = 0; i < ntiles; ++i) {
+  for (int i = 0; warp <= 4 && i < ntiles; ++i) {  // workers and the MMA warp; the drain warps wait below
     const int ix = ixa;
     if (worker) {
       const bool more = i + 1 < ntiles;
       if (more) gather_rows(i + 1);  // buffer (i + 1) & 1 was last read by tile i - 1's finished MMAs
       landed(more);
     }
-    if (named_bar_or(1, kThreads, false)) { aborted = true; break; }  // the tile has landed
+    if (named_bar_or(1, kPass1, false)) { aborted = true; break; }  // the tile has landed
     if (warp == 4) issue_s(i);  // the whole warp, one elected lane issues
     bool ok = true;
     if (worker) {
@@ -280,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       end_tile(i);
     }
     ph_s ^= 1;
-    if (named_bar_or(1, kThreads, !ok)) { aborted = true; break; }  // S is read: TMEM and the tile are free
+    if (named_bar_or(1, kPass1, !ok)) { aborted = true; break; }  // S is read: TMEM and the tile are free
   }
 
   // ---- the row's distributions and its KL value (workers) ----
@@ -318,30 +332,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       *s_active = active ? 1 : 0;
     }
   }
-  named_bar(1, kThreads);  // the statistics are in shared memory for every role
+  __syncthreads();  // the statistics are in shared memory for every role, the drain warps included
   const bool active = !aborted && *s_active != 0;
   const float logz = s_stats[0], inv_psum = s_stats[1];
 
-  // ---- pass 2: the gradient ----
-  if (worker && active && ntiles > 0) start_pass();
-  for (int i = 0; active && i < ntiles; ++i) {
-    const int ix = ixa;
-    if (worker) {
+  // ---- pass 2: the gradient, three roles ----
+  // workers: gather, S read, m_hj and dw; MMA warp: S, then dQ^T += K_tile^T.M and dK = M.Q into one of
+  // two dK buffers; drain warps: dK of the previous product into dk_idx while the workers go on.
+  if (worker && active) {
+    bool bad = false;  // a wait of this thread gave up (made uniform by the next workers' barrier)
+    if (ntiles > 0) start_pass();
+    for (int i = 0; i < ntiles; ++i) {
+      const int ix = ixa;
       const bool more = i + 1 < ntiles;
+      // the products of tile i - 1 are done: K buffer (i + 1) & 1 and the M tiles are free
+      if (i >= 1 && !bad) bad = !mbar_wait(bar_mm, (i - 1) & 1, s_abort, err, wait_limit);
+      // every worker's key table entry for tile i + 1 is written (end of tile i - 1)
+      if (named_bar_or(2, kWorkers, bad)) { aborted = true; break; }
       if (more) gather_rows(i + 1);
       landed(more);
-    }
-    if (named_bar_or(1, kThreads, false)) { aborted = true; break; }
-    if (warp == 4) issue_s(i);  // the whole warp, one elected lane issues
-    bool ok = true;
-    if (worker) {
-      ok = mbar_wait(bar_s, ph_s, s_abort, err, wait_limit);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_land);
+      const bool ok = mbar_wait(bar_s, ph_s ^ (uint32_t)(i & 1), s_abort, err, wait_limit);
       if (ok) {
         tc_fence_after();
         uint32_t v[64];
         tmem_ld32(tmem_addr(tS, warp * 32, 0), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
         tmem_ld32(tmem_addr(tS, warp * 32, 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
         tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sfree);  // S is read: the next tile's S may be formed
         const int j = i * kTile + tid;
         float g = 0.f;
         if (j < n_eff && ix >= 0) g = coeff * (expf(s_I[j] - logz) - s_P[j] * inv_psum);
@@ -373,10 +394,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();  // M -> visible to the tensor core
       }
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_m);
+      end_tile(i);
+      bad |= !ok;
     }
-    if (named_bar_or(1, kThreads, !ok)) { aborted = true; break; }  // M is in shared memory
-    if (warp == 4) {
+    // the last tile's products are done before dQ^T is read
+    if (!aborted && !bad && ntiles > 0) bad = !mbar_wait(bar_mm, (ntiles - 1) & 1, s_abort, err, wait_limit);
+    aborted = named_bar_or(2, kWorkers, aborted || bad);
+  } else if (warp == 4 && active) {
+    for (int i = 0; i < ntiles; ++i) {
+      if (!warp_all(mbar_wait(bar_land, i & 1, s_abort, err, wait_limit))) { aborted = true; break; }
+      if (i >= 1 && !warp_all(mbar_wait(bar_sfree, (i - 1) & 1, s_abort, err, wait_limit))) { aborted = true; break; }
+      issue_s(i);
+      if (!warp_all(mbar_wait(bar_m, i & 1, s_abort, err, wait_limit))) { aborted = true; break; }
+      // dK buffer i & 1 was read by the drain of tile i - 2
+      if (i >= 2 && !warp_all(mbar_wait(bar_dkf + 8 * (i & 1), ((i - 2) >> 1) & 1, s_abort, err, wait_limit))) {
+        aborted = true;
+        break;
+      }
       tc_fence_after();
+      const uint32_t tdk = tDK + 128 * (uint32_t)(i & 1);
       const uint64_t ka = sdesc_sw128(sK + (uint32_t)(i & 1) * K_BUF, K_CHUNK, 1024);
       const uint64_t mb_hi = sdesc_sw128(sMhi, K_CHUNK, 1024);
       const uint64_t mb_lo = sdesc_sw128(sMlo, K_CHUNK, 1024);
@@ -389,44 +427,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qb = sdesc_sw128(sQ, Q_CHUNK, 1024);
 #pragma unroll
       for (int k = 0; k < kHeads / 16; ++k) {  // + 16 heads: + 32 bytes along A's rows, + 16 rows of Q
-        mma_ss_w(tDK, ma_hi + (uint64_t)(k * 2), qb + (uint64_t)(k * 128), kIdDK, k > 0 ? 1u : 0u);
-        mma_ss_w(tDK, ma_lo + (uint64_t)(k * 2), qb + (uint64_t)(k * 128), kIdDK, 1u);
+        mma_ss_w(tdk, ma_hi + (uint64_t)(k * 2), qb + (uint64_t)(k * 128), kIdDK, k > 0 ? 1u : 0u);
+        mma_ss_w(tdk, ma_lo + (uint64_t)(k * 2), qb + (uint64_t)(k * 128), kIdDK, 1u);
       }
       mma_commit_w(bar_mm);
+      mma_commit_w(bar_mmd + 8 * (i & 1));
     }
-    ok = true;
-    if (worker) {
-      ok = mbar_wait(bar_mm, ph_mm, s_abort, err, wait_limit);
-      if (ok) {
-        tc_fence_after();
-        // dK row tid -> its staging row (the previous tile's bulk reduction has read it), then one bulk
-        // reduction of the 512-byte row into dk_idx[key], running while the warps go on
-        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-        const uint32_t row = smem_u32(smem + OFF_DKS + tid * DK_PITCH);
+  } else if (warp >= 5 && active) {
+    // ======================= dK drain: one staged row per slot, one bulk reduction each =======================
+    const int qd = warp & 3;          // TMEM lane quadrant of this warp
+    const int r = qd * 32 + lane;     // slot row of the tile
+    const uint32_t row = smem_u32(smem + OFF_DKS + r * DK_PITCH);
+    auto key_of = [&](int i) -> int {  // the row's key (the workers report bad indices)
+      const int j = i * kTile + r;
+      const int raw = (j < n_eff) ? __ldg(idx_row + j) : -1;
+      return (raw >= 0 && raw < Tk) ? raw : -1;
+    };
+    int key_next = (ntiles > 0) ? key_of(0) : -1;
+    for (int i = 0; i < ntiles; ++i) {
+      const int key = key_next;
+      if (i + 1 < ntiles) key_next = key_of(i + 1);
+      if (!mbar_wait(bar_mmd + 8 * (i & 1), (i >> 1) & 1, s_abort, err, wait_limit)) { aborted = true; break; }
+      tc_fence_after();
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // the previous reduction read the row
+      const uint32_t tdk = tDK + 128 * (uint32_t)(i & 1);
 #pragma unroll 1
-        for (int b = 0; b < kDi / 32; ++b) {
-          uint32_t v[32];
-          tmem_ld32(tmem_addr(tDK, warp * 32, 32 * b), v);
-          tmem_ld_wait();
+      for (int b = 0; b < kDi / 32; ++b) {
+        uint32_t v[32];
+        tmem_ld32(tmem_addr(tdk, qd * 32, 32 * b), v);
+        tmem_ld_wait();
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            st_shared_v4(row + 128 * b + 16 * u, v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-        }
-        fence_proxy_async_smem();  // the row -> visible to the bulk copy
-        if (ix >= 0) {
-          asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
-                           dk + (size_t)ix * kDi),
-                       "r"(row), "n"(kDi * 4)
-                       : "memory");
-          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        }
+        for (int u = 0; u < 8; ++u)
+          st_shared_v4(row + 128 * b + 16 * u, v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
       }
       tc_fence_before();
-      end_tile(i);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dkf + 8 * (i & 1));  // dK buffer i & 1 is read
+      fence_proxy_async_smem();  // the row -> visible to the bulk copy
+      if (key >= 0) {
+        asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                         dk + (size_t)key * kDi),
+                     "r"(row), "n"(kDi * 4)
+                     : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
     }
-    ph_s ^= 1;
-    ph_mm ^= 1;
-    if (named_bar_or(1, kThreads, !ok)) { aborted = true; break; }  // dK drained: TMEM, the tile and M are free
+    // every bulk reduction of this thread is complete before the CTA exits
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 
   // ---- dq_idx (dQ^T in TMEM: lane = dim, column = head) and dw ----
@@ -449,8 +496,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid < Hi) dw_out[(size_t)t * Hi + tid] = have ? s_dw[tid] : 0.f;
   }
 
-  // every bulk reduction of this thread is complete before the CTA exits
-  if (worker) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   if (warp == 4) {
     // every MMA of this CTA completes before the teardown frees TMEM
     mma_commit_w(bar_fin);
@@ -462,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 4) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
