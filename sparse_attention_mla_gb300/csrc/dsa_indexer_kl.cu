@@ -15,21 +15,24 @@
 //   dw[t,h] = sum_j g_j max(0, s_hj),   dq_idx[t,h,:] = sum_j m_hj k_idx[idx_j,:],
 //   dk_idx[idx_j,:] += sum_h m_hj q_idx[t,h,:].
 //
-// Design (sm_103a): one CTA per query row, 4 worker warps (one TMEM lane
-// quadrant each, one slot row per thread) and one MMA warp.  The selected
-// k_idx rows of a 128-slot tile are gathered by cp.async into 128-byte-swizzled
-// shared memory, two tiles deep (the next tile is fetched while the current
-// one is multiplied).  Pass 1: S[slot, head] = K_tile . Q^T (M = 128 slots,
-// N = 64 heads) in TMEM, the head-weighted ReLU sum per slot into shared
-// memory; then the row's softmax, KL and p normalisation.  Pass 2 gathers and
-// multiplies again, forms m_hj (bf16 hi + lo parts, so the gradients carry it
-// to about fp32) and dw, and runs two more products per tile: dQ^T[dim, head]
-// += K_tile^T . M (accumulated in TMEM over the tiles) and dK[slot, dim] =
-// M . Q.  Every thread stages its dK row (512 bytes) in shared memory and
-// reduces it into the fp32 dk_idx accumulator with one bulk reduction
-// (cp.reduce.async.bulk .add.f32), which runs while the warps go on to the
-// next tile: a few warps issuing per-thread L2 reductions could not keep up
-// with 512 bytes per slot.
+// Design (sm_103a): one CTA per query row; 4 worker warps (one TMEM lane
+// quadrant each, one slot row per thread), an MMA warp and, in the second
+// pass, 4 drain warps.  The selected k_idx rows of a 128-slot tile are
+// gathered by cp.async into 128-byte-swizzled shared memory (16 lanes per
+// 256-byte row), two tiles deep.  Pass 1: S[slot, head] = K_tile . Q^T
+// (M = 128 slots, N = 64 heads) in TMEM, the head-weighted ReLU sum per slot
+// and the slot's probability into shared memory; then the row's softmax, KL
+// and p normalisation.  Pass 2 gathers and multiplies again and writes
+// m'_hj = g_j [s_hj > 0] (bf16 hi + lo parts: two values selected by the ReLU
+// mask), with which
+//   U^T[dim, head] += K_tile^T . M'   (in TMEM over the tiles), and
+//   dK[slot, dim] = M' . Q',  Q' = w_h q_idx[h,:] (bf16 hi + lo, made once),
+// and at the end dq_h = w_h U_h and dw_h = <q_h, U_h> (the same sums as
+// above, regrouped; the gradients carry about fp32 accuracy).  dK has two
+// TMEM buffers: the drain warps reduce one into the fp32 dk_idx accumulator
+// (red.global.add.v4.f32, 4 rows x 128 bytes per instruction after a
+// transpose through shared memory) while the workers build the next tile's
+// M'.  The roles hand over through mbarriers.
 #include <cmath>
 
 #include "dsa_device.cuh"
@@ -49,13 +52,13 @@ constexpr int kMaxK = 4096;
 constexpr int Q_CHUNK = kHeads * 128;     // 8 KiB: 64 heads x 64 dims
 constexpr int K_CHUNK = kTile * 128;      // 16 KiB: 128 slots x 64 dims
 constexpr int K_BUF = 2 * K_CHUNK;        // one gathered tile
-constexpr int DK_PITCH = kDi * 4 + 16;    // staged dK row: 512 bytes + 16 (bank spread)
 constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + 2 * Q_CHUNK;          // two tile buffers
+constexpr int OFF_QW = OFF_Q + 2 * Q_CHUNK;         // w_h q_idx[h,:] as bf16 hi (2 chunks), then lo (2 chunks)
+constexpr int OFF_K = OFF_QW + 4 * Q_CHUNK;         // two tile buffers
 constexpr int OFF_MHI = OFF_K + 2 * K_BUF;
 constexpr int OFF_MLO = OFF_MHI + kTile * 128;
-constexpr int OFF_DKS = OFF_MLO + kTile * 128;      // [128 rows][DK_PITCH] staged dK rows
-constexpr int OFF_I = OFF_DKS + kTile * DK_PITCH;   // float [kMaxK]: indexer scores (-inf: invalid slot)
+constexpr int OFF_FST = OFF_MLO + kTile * 128;      // [4 drain warps][16 rows x 128 B]: dK transposes
+constexpr int OFF_I = OFF_FST + 4 * 2048;           // float [kMaxK]: indexer scores (-inf: invalid slot)
 constexpr int OFF_P = OFF_I + kMaxK * 4;            // float [kMaxK]: attention slot probabilities
 constexpr int OFF_MISC = OFF_P + kMaxK * 4;
 constexpr int M_BAR_S = 0, M_BAR_MM = 8, M_BAR_FIN = 16, M_TMEM = 32, M_NEFF = 36, M_ABORT = 40, M_ACTIVE = 44;
@@ -191,6 +194,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = (n_eff + kTile - 1) / kTile;
   const uint32_t tmem = *s_tmem;
   const uint32_t tS = tmem, tDQ = tmem + 64, tDK = tmem + 128;  // dK: two buffers of 128 columns
+  const uint32_t sQW = smem_u32(smem + OFF_QW);
+  if (worker) {
+    // Q' = w_h q_idx[h,:] as bf16 hi + lo in Q's layout: the B operand of dK = M'.Q' (M' = g [s > 0])
+#pragma unroll
+    for (int k = 0; k < kHeads * 16 / kWorkers; ++k) {
+      const int u = tid + kWorkers * k;  // 16-byte unit: head u >> 4, chunk (u >> 3) & 1, unit u & 7
+      const int hh = u >> 4;
+      const uint32_t off = ((u >> 3) & 1) * Q_CHUNK + sw128_off(hh, u & 7);
+      const uint4 qv = *reinterpret_cast<const uint4*>(smem + OFF_Q + off);
+      const float wh = s_w[hh];
+      const uint32_t* qe = reinterpret_cast<const uint32_t*>(&qv);
+      uint32_t hv[4], lv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qe[e]));
+        const float a = wh * qf.x, b = wh * qf.y;
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(a, b);
+        const float2 hf = __bfloat1622float2(hi);
+        hv[e] = *reinterpret_cast<const uint32_t*>(&hi);
+        lv[e] = pack_bf16x2(a - hf.x, b - hf.y);
+      }
+      st_shared_v4(sQW + off, hv[0], hv[1], hv[2], hv[3]);
+      st_shared_v4(sQW + 2 * Q_CHUNK + off, lv[0], lv[1], lv[2], lv[3]);
+    }
+    fence_proxy_async_smem();  // Q' -> visible to the tensor core (first used in the second pass)
+  }
 
   // index of slot j (-1: invalid or beyond the prefix; out-of-range values are reported and masked)
   // A slot's key in two steps: the load (issued a tile ahead of its gather, so that its memory
@@ -264,7 +293,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   bool aborted = false;
   uint32_t ph_s = 0;  // phase parity of bar_s, which counts the S products of both passes
-  // ---- pass 1: indexer scores of the selected slots ----
+  // ---- pass 1: indexer scores of the selected slots, and their attention probabilities ----
+  // (each worker loads its slot's probability a tile ahead, stores it for the second pass and keeps
+  // running partials of the row's score maximum and probability sum)
+  float imax_part = -INFINITY, psum_part = 0.f;
+  auto prob_of = [&](int i) -> float {
+    const int j = i * kTile + tid;
+    return (j < n_eff) ? __ldg(prob + (size_t)t * K + j) : 0.f;
+  };
+  float p_next = (worker && ntiles > 0) ? prob_of(0) : 0.f;
   if (worker && ntiles > 0) start_pass();
   for (int i = 0; warp <= 4 && i < ntiles; ++i) {  // workers and the MMA warp; the drain warps wait below
     const int ix = ixa;
@@ -288,10 +325,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < kHeads; ++h) score = fmaf(s_w[h], fmaxf(__uint_as_float(v[h]), 0.f), score);
         const int j = i * kTile + tid;
-        if (j < n_eff) s_I[j] = (ix >= 0) ? score : -INFINITY;
+        if (j < n_eff) {
+          const float sc = (ix >= 0) ? score : -INFINITY;
+          const float p = (ix >= 0) ? p_next : 0.f;
+          s_I[j] = sc;
+          s_P[j] = p;
+          imax_part = fmaxf(imax_part, sc);
+          psum_part += p;
+        }
       }
       tc_fence_before();
       end_tile(i);
+      p_next = (i + 1 < ntiles) ? prob_of(i + 1) : 0.f;
     }
     ph_s ^= 1;
     if (named_bar_or(1, kPass1, !ok)) { aborted = true; break; }  // S is read: TMEM and the tile are free
@@ -299,16 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- the row's distributions and its KL value (workers) ----
   if (worker && !aborted) {
-    float imax = -INFINITY, psum = 0.f;
-    for (int j = tid; j < n_eff; j += kWorkers) {
-      const int ix = check_key(__ldg(idx_row + j));
-      const float p = (ix >= 0) ? __ldg(prob + (size_t)t * K + j) : 0.f;
-      s_P[j] = p;
-      imax = fmaxf(imax, s_I[j]);
-      psum += p;
-    }
-    imax = worker_reduce<true>(imax, s_red, warp, lane);
-    psum = worker_reduce<false>(psum, s_red, warp, lane);
+    const float imax = worker_reduce<true>(imax_part, s_red, warp, lane);
+    const float psum = worker_reduce<false>(psum_part, s_red, warp, lane);
     const bool active = imax > -INFINITY && psum > 0.f;
     float klv = 0.f;
     if (active) {
@@ -366,32 +403,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = i * kTile + tid;
         float g = 0.f;
         if (j < n_eff && ix >= 0) g = coeff * (expf(s_I[j] - logz) - s_P[j] * inv_psum);
-        // m_h = g w_h [s_h > 0] as bf16 hi + lo, row tid of the two M tiles; dw_h += g max(0, s_h)
+        // m'_h = g [s_h > 0] as bf16 hi + lo, row tid of the two M tiles: two values selected per head by
+        // the ReLU mask (w_h enters through Q' for dK and at the end for dq; dw = <q_h, U_h> at the end)
+        const __nv_bfloat16 ghi = __float2bfloat16_rn(g);
+        const uint32_t gh = __bfloat16_as_ushort(ghi);
+        const uint32_t gl = __bfloat16_as_ushort(__float2bfloat16_rn(g - __bfloat162float(ghi)));
         uint32_t mh[32], ml[32];
 #pragma unroll
         for (int h = 0; h < kHeads; h += 2) {
-          const float s0 = __uint_as_float(v[h]), s1 = __uint_as_float(v[h + 1]);
-          const float m0 = (s0 > 0.f) ? g * s_w[h] : 0.f, m1 = (s1 > 0.f) ? g * s_w[h + 1] : 0.f;
-          const __nv_bfloat162 hi = __floats2bfloat162_rn(m0, m1);
-          const float2 hf = __bfloat1622float2(hi);
-          mh[h >> 1] = *reinterpret_cast<const uint32_t*>(&hi);
-          ml[h >> 1] = pack_bf16x2(m0 - hf.x, m1 - hf.y);
-          v[h] = __float_as_uint(g * fmaxf(s0, 0.f));
-          v[h + 1] = __float_as_uint(g * fmaxf(s1, 0.f));
+          const bool p0 = __uint_as_float(v[h]) > 0.f, p1 = __uint_as_float(v[h + 1]) > 0.f;
+          mh[h >> 1] = (p0 ? gh : 0u) | ((p1 ? gh : 0u) << 16);
+          ml[h >> 1] = (p0 ? gl : 0u) | ((p1 ? gl : 0u) << 16);
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           st_shared_v4(sMhi + sw128_off(tid, u), mh[4 * u], mh[4 * u + 1], mh[4 * u + 2], mh[4 * u + 3]);
           st_shared_v4(sMlo + sw128_off(tid, u), ml[4 * u], ml[4 * u + 1], ml[4 * u + 2], ml[4 * u + 3]);
         }
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float d[32];
-#pragma unroll
-          for (int h = 0; h < 32; ++h) d[h] = __uint_as_float(v[32 * half + h]);
-          atomicAdd(s_dw + 32 * half + lane, warp_transpose_sum(d, lane));
-        }
-        fence_proxy_async_smem();  // M -> visible to the tensor core
+        fence_proxy_async_smem();  // M' -> visible to the tensor core
       }
       tc_fence_before();
       __syncwarp();
@@ -424,20 +453,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_ss_w(tDQ, ka + (uint64_t)(k * 128), mb_lo + (uint64_t)(k * 128), kIdDQ, 1u);
       }
       const uint64_t ma_hi = sdesc_sw128(sMhi, 16, 1024), ma_lo = sdesc_sw128(sMlo, 16, 1024);
-      const uint64_t qb = sdesc_sw128(sQ, Q_CHUNK, 1024);
+      const uint64_t qwh = sdesc_sw128(sQW, Q_CHUNK, 1024), qwl = sdesc_sw128(sQW + 2 * Q_CHUNK, Q_CHUNK, 1024);
 #pragma unroll
-      for (int k = 0; k < kHeads / 16; ++k) {  // + 16 heads: + 32 bytes along A's rows, + 16 rows of Q
-        mma_ss_w(tdk, ma_hi + (uint64_t)(k * 2), qb + (uint64_t)(k * 128), kIdDK, k > 0 ? 1u : 0u);
-        mma_ss_w(tdk, ma_lo + (uint64_t)(k * 2), qb + (uint64_t)(k * 128), kIdDK, 1u);
+      for (int k = 0; k < kHeads / 16; ++k) {  // + 16 heads: + 32 bytes along A's rows, + 16 rows of Q'
+        // dK = M'_hi Q'_hi + M'_hi Q'_lo + M'_lo Q'_hi (the lo x lo term is below fp32 rounding)
+        mma_ss_w(tdk, ma_hi + (uint64_t)(k * 2), qwh + (uint64_t)(k * 128), kIdDK, k > 0 ? 1u : 0u);
+        mma_ss_w(tdk, ma_hi + (uint64_t)(k * 2), qwl + (uint64_t)(k * 128), kIdDK, 1u);
+        mma_ss_w(tdk, ma_lo + (uint64_t)(k * 2), qwh + (uint64_t)(k * 128), kIdDK, 1u);
       }
       mma_commit_w(bar_mm);
       mma_commit_w(bar_mmd + 8 * (i & 1));
     }
   } else if (warp >= 5 && active) {
-    // ======================= dK drain: one staged row per slot, one bulk reduction each =======================
-    const int qd = warp & 3;          // TMEM lane quadrant of this warp
-    const int r = qd * 32 + lane;     // slot row of the tile
-    const uint32_t row = smem_u32(smem + OFF_DKS + r * DK_PITCH);
+    // ======================= dK drain: rows into dk_idx by L2 reductions =======================
+    // 32 rows x 32 dims at a time per warp, transposed through the warp's 2 KiB buffer 16 rows at a
+    // time, so that each red.global.add.v4.f32 covers 4 rows x 128 bytes
+    const int qd = warp & 3;       // TMEM lane quadrant of this warp
+    const int r = qd * 32 + lane;  // slot row of the tile
+    const uint32_t fst = smem_u32(smem + OFF_FST + (warp - 5) * 2048);
     auto key_of = [&](int i) -> int {  // the row's key (the workers report bad indices)
       const int j = i * kTile + r;
       const int raw = (j < n_eff) ? __ldg(idx_row + j) : -1;
@@ -449,31 +482,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (i + 1 < ntiles) key_next = key_of(i + 1);
       if (!mbar_wait(bar_mmd + 8 * (i & 1), (i >> 1) & 1, s_abort, err, wait_limit)) { aborted = true; break; }
       tc_fence_after();
-      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // the previous reduction read the row
       const uint32_t tdk = tDK + 128 * (uint32_t)(i & 1);
 #pragma unroll 1
       for (int b = 0; b < kDi / 32; ++b) {
         uint32_t v[32];
         tmem_ld32(tmem_addr(tdk, qd * 32, 32 * b), v);
         tmem_ld_wait();
+        if (b == kDi / 32 - 1) {  // the last load of the buffer: it may be refilled
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_dkf + 8 * (i & 1));
+        }
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          st_shared_v4(row + 128 * b + 16 * u, v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_dkf + 8 * (i & 1));  // dK buffer i & 1 is read
-      fence_proxy_async_smem();  // the row -> visible to the bulk copy
-      if (key >= 0) {
-        asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
-                         dk + (size_t)key * kDi),
-                     "r"(row), "n"(kDi * 4)
-                     : "memory");
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        for (int hh = 0; hh < 2; ++hh) {
+          if ((lane >> 4) == hh) {
+            const int rl = lane & 15;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              st_shared_v4(fst + rl * 128 + ((u ^ (rl & 7)) << 4), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int st = 0; st < 4; ++st) {
+            const int rl = 4 * st + (lane >> 3), u = lane & 7;
+            const int kr = __shfl_sync(0xffffffffu, key, 16 * hh + rl);
+            float4 f;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+                         : "r"(fst + rl * 128 + ((u ^ (rl & 7)) << 4))
+                         : "memory");
+            if (kr >= 0) red_add_v4(dk + (size_t)kr * kDi + 32 * b + 4 * u, f.x, f.y, f.z, f.w);
+          }
+          __syncwarp();
+        }
       }
     }
-    // every bulk reduction of this thread is complete before the CTA exits
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 
   // ---- dq_idx (dQ^T in TMEM: lane = dim, column = head) and dw ----
@@ -489,10 +532,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int h = 0; h < kHeads; ++h) v[h] = 0u;
     }
+    // TMEM holds U^T (U_h = sum_j g_j [s_jh > 0] k_j): dq_h = w_h U_h, dw_h = <q_h, U_h>
     __nv_bfloat16* dq_row = dq_out + (size_t)t * Hi * kDi + tid;  // dim tid of every head
 #pragma unroll 8
     for (int h = 0; h < kHeads; ++h)
-      if (h < Hi) dq_row[(size_t)h * kDi] = __float2bfloat16_rn(__uint_as_float(v[h]));
+      if (h < Hi) dq_row[(size_t)h * kDi] = __float2bfloat16_rn(s_w[h] * __uint_as_float(v[h]));
+    const uint8_t* qcol = smem + OFF_Q + (tid >> 6) * Q_CHUNK + (tid & 7) * 2;  // q_idx[., tid]: chunk, lane in unit
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float d[32];
+#pragma unroll
+      for (int hh = 0; hh < 32; ++hh) {
+        const int h = 32 * half + hh;
+        const __nv_bfloat16 qv = *reinterpret_cast<const __nv_bfloat16*>(qcol + sw128_off(h, (tid & 63) >> 3));
+        d[hh] = __bfloat162float(qv) * __uint_as_float(v[h]);
+      }
+      atomicAdd(s_dw + 32 * half + lane, warp_transpose_sum(d, lane));
+    }
+    named_bar(2, kWorkers);
     if (tid < Hi) dw_out[(size_t)t * Hi + tid] = have ? s_dw[tid] : 0.f;
   }
 
