@@ -22,9 +22,17 @@
 //    tensor-core M axis is the 128 keys of the tile and N = 64 heads
 //    (M = 128 is the full-rate tcgen05 shape; the heads are the shared
 //    operand).  Output is accumulated transposed too, O^T[ch, head] +=
-//    V^T . P^T, as four M = 128 channel tiles.  TMEM holds S^T (64 columns)
-//    and O^T (256 columns); 64 x 512 fp32 O in the heads-on-M orientation
-//    would need M = 64 tiles that leave half of each TMEM lane quadrant idle.
+//    V^T . P^T, as four M = 128 channel tiles.
+//  * P is split into bf16 hi + lo parts and P.V runs on both, so O is accurate
+//    to about fp32 and the backward's D = <dO, O> matches the exact softmax:
+//    with P in bf16 alone (the operand precision of the pages' kernels) D is
+//    off by about 2^-8 of its terms, and dq / dkv miss the 2e-2 max-abs target
+//    on unit-scale inputs.  For channel tiles 0..2 the two parts sit side by
+//    side on the MMA's N axis (N = 128, hi and lo accumulated in separate TMEM
+//    columns and added at the end): one MMA reads each V^T tile once, and N =
+//    128 runs at the full rate where N = 64 runs at two thirds of it.  TMEM
+//    (512 columns: S^T 64, O^T 3 x 128 + 64) leaves tile 3 at N = 64, hi and lo
+//    one after the other into the same columns.
 //  * P.V runs key rows 0..63 first, then rows 64..127, and signals after the
 //    first half: the next tile's rows 0..63 of every value chunk are
 //    gathered while the tensor core works on rows 64..127.  Rows 64..127 go
@@ -34,16 +42,13 @@
 //    only when some score exceeds the running max by more than 2^8 (lazy
 //    rescale), otherwise P uses the stale max.
 //  * P^T is written into the shared-memory slot of the tile's RoPE channels
-//    (no longer needed once S^T is done), which keeps the working set
-//    (Q 72 KiB + tile 144 KiB) inside one SM's shared memory.  P is split
-//    into bf16 hi + lo parts and P.V runs on both, so O is accurate to about
-//    fp32 and the backward's D = <dO, O> matches the exact softmax: with P in
-//    bf16 alone (the operand precision of the pages' kernels) D is off by
-//    about 2^-8 of its terms, and dq / dkv miss the 2e-2 max-abs target on
-//    unit-scale inputs.  The lo part of key rows 0..63 has an 8 KiB slot of
-//    its own; the lo part of rows 64..127 goes into the P slot's rows 0..63
-//    once the first key half of P.V has read them, while the tensor core runs
-//    P_hi of rows 64..127.
+//    (no longer needed once S^T is done) and an 8 KiB slot before it, which
+//    keeps the working set (Q 72 KiB + tile 144 KiB + 8 KiB) inside one SM's
+//    shared memory.  For each 64-key half the hi and lo blocks of the N = 128
+//    operand are 8 KiB apart: keys 0..63 hold hi in rows 0..63 of the P slot
+//    and lo in rows 64..127; keys 64..127 hold hi in the slot before, and their
+//    lo goes into the P slot's rows 0..63 once the first key half of P.V has
+//    read them, while the tensor core runs P_hi of rows 64..127 of tile 3.
 //  * An attention sink (optional, one logit per head: NeMo AutoModel
 //    glm_moe_dsa.kernels.cudnn_dsa, _pad_attention_heads) starts the running
 //    max of its head and adds its own term to the denominator at the end; it
@@ -75,14 +80,17 @@ struct Smem {
   static constexpr int Q_CHUNK = kHeads * 128;  // one chunk of Q: 64 heads x 128 B
   static constexpr int KV_CHUNK = kTile * 128;  // one chunk of the tile: 128 keys x 128 B
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + NCH * Q_CHUNK;
-  // P^T lives in the RoPE chunk when there is one, else in its own slot.
-  static constexpr int OFF_P = (DQK == 576) ? OFF_KV + 8 * KV_CHUNK : OFF_KV + NCH * KV_CHUNK;
-  static constexpr int OFF_MISC = (DQK == 576) ? OFF_KV + NCH * KV_CHUNK : OFF_P + KV_CHUNK;
+  static constexpr int OFF_KV = OFF_Q + NCH * Q_CHUNK;  // value chunks 0..7
+  // P^T, one 64-key half at a time, as an MN-major operand of N = 128 ([hi | lo] column blocks
+  // 8 KiB apart).  The P slot is the RoPE chunk when there is one (free once S^T is done), else a
+  // slot of its own; its rows 0..63 hold P_hi and rows 64..127 P_lo of keys 0..63.  The 8 KiB
+  // slot just before it holds P_hi of keys 64..127, whose P_lo goes into the P slot's rows 0..63
+  // once keys 0..63 have been multiplied.
+  static constexpr int OFF_PHI2 = OFF_KV + 8 * KV_CHUNK;
+  static constexpr int OFF_P = OFF_PHI2 + KV_CHUNK / 2;
+  static constexpr int OFF_MISC = OFF_P + KV_CHUNK;
   static constexpr int MISC = 2048;
-  // P_lo^T of key rows 0..63 (8 KiB, the layout of the first half of the P slot)
-  static constexpr int OFF_PLO = OFF_MISC + MISC;
-  static constexpr int TOTAL = OFF_PLO + KV_CHUNK / 2 + 1024;  // + alignment slack
+  static constexpr int TOTAL = OFF_MISC + MISC + 1024;  // + alignment slack
   static_assert(TOTAL <= 232448, "shared memory budget");
 };
 
@@ -178,7 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + L::OFF_Q);
   const uint32_t sKV = smem_u32(smem + L::OFF_KV);
   const uint32_t sP = smem_u32(smem + L::OFF_P);
-  const uint32_t sPlo = smem_u32(smem + L::OFF_PLO);
+  const uint32_t sPhi2 = smem_u32(smem + L::OFF_PHI2);
+  // chunk slot c of the tile: value chunks 0..7, the RoPE chunk in the P slot
+  auto chunk_addr = [&](int c) -> uint32_t { return c < 8 ? sKV + c * L::KV_CHUNK : sP; };
   uint8_t* misc = smem + L::OFF_MISC;
   const uint32_t bar_kv = smem_u32(misc + M_BAR_KV), bar_pv = smem_u32(misc + M_BAR_PV);
   const uint32_t bar_s = smem_u32(misc + M_BAR_S), bar_p = smem_u32(misc + M_BAR_P);
@@ -254,18 +264,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = (n_eff + kTile - 1) / kTile;
   const uint32_t tmem = *s_tmem;
   const uint32_t tS = tmem;        // S^T: 128 lanes x 64 columns
-  const uint32_t tO = tmem + 64;   // O^T: 4 channel tiles x 64 columns
+  // O^T: channel tiles 0..2 as [hi | lo] (128 columns each), channel tile 3 with hi and lo
+  // accumulated together (64 columns): 64 + 3 x 128 + 64 = 512 columns
+  const uint32_t tO = tmem + 64;
+  const uint32_t tO3 = tO + 3 * 128;
 
   if (warp == 0) {
     // ======================= MMA issuer (the whole warp, one elected lane issues) =======================
     {
       constexpr uint32_t kIdS = idesc_bf16(128, kHeads, false, false);  // A = KV (K-major), B = Q (K-major)
       constexpr uint32_t kIdPV = idesc_bf16(128, kHeads, true, true);   // A = V^T (MN-major), B = P^T (MN-major)
+      constexpr uint32_t kIdPV2 = idesc_bf16(128, 2 * kHeads, true, true);  // B = [P_hi | P_lo]^T, N = 128
       for (int i = 0; i < ntiles; ++i) {
         bool stop = false;
         // one burst per group of landed chunks: wait for the next chunk, then take every
         // later chunk that has landed too (fewer fences and waits between MMAs)
-        const uint64_t a00 = sdesc_sw128(sKV, 16, 1024), b00 = sdesc_sw128(sQ, 16, 1024);
+        const uint64_t b00 = sdesc_sw128(sQ, 16, 1024);
         for (int c = 0; c < NCH && !stop;) {
           if (!warp_all(mbar_wait(bar_kv + 8 * c, i & 1, s_abort, err, wait_limit))) { stop = true; break; }
           int ce = c + 1;
@@ -273,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();  // cp.async landings -> visible to the tensor core
           tc_fence_after();
           for (; c < ce; ++c) {
-            const uint64_t a0 = a00 + (uint64_t)((c * L::KV_CHUNK) >> 4), b0 = b00 + (uint64_t)((c * L::Q_CHUNK) >> 4);
+            const uint64_t a0 = sdesc_sw128(chunk_addr(c), 16, 1024), b0 = b00 + (uint64_t)((c * L::Q_CHUNK) >> 4);
 #pragma unroll
             for (int k = 0; k < 4; ++k)  // + 16 channels = + 32 bytes per row
               mma_ss_w(tS, a0 + (uint64_t)(k * 2), b0 + (uint64_t)(k * 2), kIdS, (c | k) != 0);
@@ -281,51 +295,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (stop) break;
         mma_commit_w(bar_s);
-        // O^T += V^T (P_hi + P_lo)^T, key rows 0..63 first (P_lo of those rows has its own slot),
-        // so that rows 0..63 of every chunk slot are free while rows 64..127 are multiplied
+        // O^T += V^T [P_hi | P_lo]^T, key rows 0..63 first, so that rows 0..63 of every chunk slot
+        // are free while rows 64..127 are multiplied.  Channel tiles 0..2 take hi and lo in one MMA
+        // (N = 128, separate accumulators); tile 3 takes them one after the other (N = 64 each).
         if (!warp_all(mbar_wait(bar_p, i & 1, s_abort, err, wait_limit))) break;
         tc_fence_after();
-        const uint64_t pb0 = sdesc_sw128(sP, L::KV_CHUNK, 1024);
-        const uint64_t lb0 = sdesc_sw128(sPlo, L::KV_CHUNK, 1024);
+        constexpr uint64_t kLo = (L::KV_CHUNK / 2) >> 4;    // descriptor step from the hi to the lo block
+        const uint64_t pa = sdesc_sw128(sP, L::KV_CHUNK / 2, 1024);     // keys 0..63
+        const uint64_t pb = sdesc_sw128(sPhi2, L::KV_CHUNK / 2, 1024);  // keys 64..127
         const uint64_t va0 = sdesc_sw128(sKV, L::KV_CHUNK, 1024);
         constexpr uint64_t kPair = (2 * L::KV_CHUNK) >> 4;  // descriptor step between channel pairs
         constexpr int kHalf = kTile / 32;                   // 16-key steps per 64-key half
 #pragma unroll
-        for (int m = 0; m < kDv / 128; ++m) {
+        for (int m = 0; m < 3; ++m) {
 #pragma unroll
           for (int k = 0; k < kHalf; ++k)  // + 16 key rows = + 2048 bytes
-            mma_ss_w(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV,
+            mma_ss_w(tO + m * 128, va0 + m * kPair + (uint64_t)(k * 128), pa + (uint64_t)(k * 128), kIdPV2,
                      (i > 0 || k > 0) ? 1u : 0u);
-#pragma unroll
-          for (int k = 0; k < kHalf; ++k)
-            mma_ss_w(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), lb0 + (uint64_t)(k * 128), kIdPV, 1u);
         }
-        mma_commit_w(bar_pvh);  // rows 0..63 of the chunk slots (and of the P slot) are read
-        // Key rows 64..127 channel pair by channel pair, with a commit after each pair, so that
-        // the next tile's rows 64..127 of a pair are gathered while later pairs are multiplied.
-        // P_hi of pairs 0 and 1 first: the tensor core works on them while the workers move
-        // P_lo of rows 64..127 into the P slot's rows 0..63.
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
+        for (int k = 0; k < kHalf; ++k)
+          mma_ss_w(tO3, va0 + 3 * kPair + (uint64_t)(k * 128), pa + (uint64_t)(k * 128), kIdPV,
+                   (i > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
-          for (int k = kHalf; k < 2 * kHalf; ++k)
-            mma_ss_w(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV, 1u);
-        }
+        for (int k = 0; k < kHalf; ++k)
+          mma_ss_w(tO3, va0 + 3 * kPair + (uint64_t)(k * 128), pa + kLo + (uint64_t)(k * 128), kIdPV, 1u);
+        mma_commit_w(bar_pvh);  // rows 0..63 of the chunk slots (and the P slot) are read
+        // Key rows 64..127 channel pair by channel pair, with a commit after each pair, so that the
+        // next tile's rows 64..127 of a pair are gathered while later pairs are multiplied.  P_hi of
+        // tile 3 first: the tensor core works on it while the workers move P_lo of rows 64..127 into
+        // the P slot's rows 0..63.
+#pragma unroll
+        for (int k = 0; k < kHalf; ++k)
+          mma_ss_w(tO3, va0 + 3 * kPair + (uint64_t)((kHalf + k) * 128), pb + (uint64_t)(k * 128), kIdPV, 1u);
         if (!warp_all(mbar_wait(bar_plo, i & 1, s_abort, err, wait_limit))) break;
         tc_fence_after();
 #pragma unroll
-        for (int m = 0; m < kDv / 128; ++m) {
-          if (m >= 2) {
+        for (int m = 0; m < 3; ++m) {
 #pragma unroll
-            for (int k = kHalf; k < 2 * kHalf; ++k)
-              mma_ss_w(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 128), kIdPV, 1u);
-          }
-#pragma unroll
-          for (int k = kHalf; k < 2 * kHalf; ++k)
-            mma_ss_w(tO + m * kHeads, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)((k - kHalf) * 128),
-                     kIdPV, 1u);
-          if (m < 3) mma_commit_w(bar_pvm + 8 * m);
+          for (int k = 0; k < kHalf; ++k)
+            mma_ss_w(tO + m * 128, va0 + m * kPair + (uint64_t)((kHalf + k) * 128), pb + (uint64_t)(k * 128), kIdPV2,
+                     1u);
+          mma_commit_w(bar_pvm + 8 * m);
         }
+#pragma unroll
+        for (int k = 0; k < kHalf; ++k)
+          mma_ss_w(tO3, va0 + 3 * kPair + (uint64_t)((kHalf + k) * 128), pb + kLo + (uint64_t)(k * 128), kIdPV, 1u);
         mma_commit_w(bar_pv);  // P.V of this tile is complete
       }
       // every MMA of this CTA completes before the teardown frees TMEM
@@ -364,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int rix[4];
       load_raw(0, nraw);
       check_rows(nraw, rix);
-      for (int c = 0; c < NCH; ++c) gather_chunk<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, bar_kv + 8 * c);
+      for (int c = 0; c < NCH; ++c) gather_chunk<DQK>(chunk_addr(c), kv, c, tid, rix, bar_kv + 8 * c);
     }
     // running max per head lives in s_stat (identical for all threads of a half)
     const float* m_run = s_stat + ch * 32;
@@ -430,9 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // O^T is complete for the previous tile: bar_s of this tile was
           // committed after those MMAs by the same thread.
 #pragma unroll 1
-          for (int mt = 0; mt < kDv / 128; ++mt) {
+          for (int g = 0; g < 7; ++g) {  // hi and lo of channel tiles 0..2, then tile 3
             uint32_t ov[32];
-            const uint32_t ta = tmem_addr(tO + mt * kHeads, qd * 32, ch * 32);
+            const uint32_t ta = tmem_addr(g < 6 ? tO + (g >> 1) * 128 + (g & 1) * 64 : tO3, qd * 32, ch * 32);
             tmem_ld32(ta, ov);
             tmem_ld_wait();
 #pragma unroll
@@ -460,14 +475,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk[h >> 1] = *reinterpret_cast<const uint32_t*>(&hi);
         pl[h >> 1] = pack_bf16x2(lo.x, lo.y);
       }
-      // P^T row r: 64 heads x bf16 = 128 B; this half owns units ch*4 .. ch*4+3.
+      // P^T row: 64 heads x bf16 = 128 B; this half owns units ch*4 .. ch*4+3.  Keys 0..63: hi in
+      // the P slot's row r, lo in row r + 64; keys 64..127: hi in row r - 64 of the slot before it.
+      const uint32_t hi_row = (qd < 2) ? sP + (uint32_t)r * 128u : sPhi2 + (uint32_t)(r - 64) * 128u;
 #pragma unroll
       for (int uu = 0; uu < 4; ++uu)
-        st_shared_v4(sP + sw128_off(r, ch * 4 + uu), pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2], pk[4 * uu + 3]);
-      if (qd < 2) {  // key rows 0..63: the lo part has its own slot
+        st_shared_v4(hi_row + (((ch * 4 + uu) ^ (r & 7)) << 4), pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2],
+                     pk[4 * uu + 3]);
+      if (qd < 2) {
 #pragma unroll
         for (int uu = 0; uu < 4; ++uu)
-          st_shared_v4(sPlo + sw128_off(r, ch * 4 + uu), pl[4 * uu], pl[4 * uu + 1], pl[4 * uu + 2], pl[4 * uu + 3]);
+          st_shared_v4(sP + sw128_off(r + 64, ch * 4 + uu), pl[4 * uu], pl[4 * uu + 1], pl[4 * uu + 2], pl[4 * uu + 3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -507,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             cp_async_arrive(bar_kv + 8 * c);  // covers this thread's copies of both halves
           }
         }
-        if (!aborted && NCH == 9) gather_chunk<DQK>(sKV + 8 * L::KV_CHUNK, kv, 8, tid, rix, bar_kv + 8 * 8);
+        if (!aborted && NCH == 9) gather_chunk<DQK>(sP, kv, 8, tid, rix, bar_kv + 8 * 8);
         if (named_bar_or(bar_id, 128, aborted)) { aborted = true; break; }
       }
     }
@@ -546,8 +564,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int mt = 0; mt < kDv / 128; ++mt) {
       uint32_t ov[32];
       if (ntiles > 0 && !aborted) {
-        tmem_ld32(tmem_addr(tO + mt * kHeads, qd * 32, ch * 32), ov);
-        tmem_ld_wait();
+        if (mt < 3) {  // O = hi + lo
+          uint32_t ol[32];
+          tmem_ld32(tmem_addr(tO + mt * 128, qd * 32, ch * 32), ov);
+          tmem_ld32(tmem_addr(tO + mt * 128 + 64, qd * 32, ch * 32), ol);
+          tmem_ld_wait();
+#pragma unroll
+          for (int h = 0; h < 32; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) + __uint_as_float(ol[h]));
+        } else {
+          tmem_ld32(tmem_addr(tO3, qd * 32, ch * 32), ov);
+          tmem_ld_wait();
+        }
       } else {
 #pragma unroll
         for (int h = 0; h < 32; ++h) ov[h] = 0u;
