@@ -103,14 +103,24 @@ constexpr int M_TMEM = 192, M_NEFF = 196, M_ABORT = 200;
 constexpr int M_RED = 256;             // float [4][64]
 constexpr int M_STAT = M_RED + 1024;   // float [64]: running max per head
 constexpr int M_LSUM = M_STAT + 256;   // float [64]: softmax denominator per head
+constexpr int M_MMIN = M_LSUM + 256;   // float [2]: smallest running max of each head half
 
-// Element-wise fp32 on two lanes at once (add.f32x2 / sub.f32x2, round to nearest as the scalar ops).
+// Element-wise fp32 on two lanes at once (add / fma / sub .f32x2, round to nearest as the scalar ops).
 __device__ __forceinline__ float2 f32x2_add(float2 a, float2 b) {
   uint64_t r;
   asm("add.rn.f32x2 %0, %1, %2;"
       : "=l"(r)
       : "l"((uint64_t)__float_as_uint(a.x) | ((uint64_t)__float_as_uint(a.y) << 32)),
         "l"((uint64_t)__float_as_uint(b.x) | ((uint64_t)__float_as_uint(b.y) << 32)));
+  return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
+}
+__device__ __forceinline__ float2 f32x2_fma(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(r)
+      : "l"((uint64_t)__float_as_uint(a.x) | ((uint64_t)__float_as_uint(a.y) << 32)),
+        "l"((uint64_t)__float_as_uint(b.x) | ((uint64_t)__float_as_uint(b.y) << 32)),
+        "l"((uint64_t)__float_as_uint(c.x) | ((uint64_t)__float_as_uint(c.y) << 32)));
   return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
 }
 __device__ __forceinline__ float2 f32x2_sub(float2 a, float2 b) {
@@ -201,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* s_red = reinterpret_cast<float*>(misc + M_RED);
   float* s_stat = reinterpret_cast<float*>(misc + M_STAT);
   float* s_lsum = reinterpret_cast<float*>(misc + M_LSUM);
+  float* s_mmin = reinterpret_cast<float*>(misc + M_MMIN);
 
   const int t = blockIdx.x;
   const int hg = blockIdx.y;
@@ -402,24 +413,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem_addr(tS, qd * 32, ch * 32), sv);
       tmem_ld_wait();
       const bool valid = ixw >= 0 && ixw < Tk;
-      float z[32];
-#pragma unroll
-      for (int h = 0; h < 32; ++h) z[h] = valid ? __uint_as_float(sv[h]) * sl2e : -INFINITY;
       bool need = (i == 0);
       if (!need) {
-        bool mine = false;
+        // Does any score of this key exceed its head's running max by the threshold?  First against
+        // the smallest running max of the half (this key's largest score, one compare), per head only
+        // when that test fails.
+        float smax = __uint_as_float(sv[0]);
 #pragma unroll
-        for (int h4 = 0; h4 < 8; ++h4) {  // running max as 16-byte loads (4 heads)
-          const float4 m4 = reinterpret_cast<const float4*>(m_run)[h4];
-          mine |= (z[4 * h4] > m4.x + kRescaleThreshold) | (z[4 * h4 + 1] > m4.y + kRescaleThreshold) |
-                  (z[4 * h4 + 2] > m4.z + kRescaleThreshold) | (z[4 * h4 + 3] > m4.w + kRescaleThreshold);
+        for (int h = 1; h < 32; ++h) smax = fmaxf(smax, __uint_as_float(sv[h]));
+        bool mine = valid && smax * sl2e > s_mmin[ch] + kRescaleThreshold;
+        if (mine) {
+          mine = false;
+#pragma unroll
+          for (int h4 = 0; h4 < 8; ++h4) {  // running max as 16-byte loads (4 heads)
+            const float4 m4 = reinterpret_cast<const float4*>(m_run)[h4];
+            mine |= (__uint_as_float(sv[4 * h4]) * sl2e > m4.x + kRescaleThreshold) |
+                    (__uint_as_float(sv[4 * h4 + 1]) * sl2e > m4.y + kRescaleThreshold) |
+                    (__uint_as_float(sv[4 * h4 + 2]) * sl2e > m4.z + kRescaleThreshold) |
+                    (__uint_as_float(sv[4 * h4 + 3]) * sl2e > m4.w + kRescaleThreshold);
+          }
         }
         need = named_bar_or(bar_id, 128, mine);
       }
       if (need) {
         float v[32];
 #pragma unroll
-        for (int h = 0; h < 32; ++h) v[h] = z[h];
+        for (int h = 0; h < 32; ++h) v[h] = valid ? __uint_as_float(sv[h]) * sl2e : -INFINITY;
         const float wmax = warp_transpose_reduce<true>(v, lane);
         s_red[qd * 64 + ch * 32 + lane] = wmax;
         named_bar(bar_id, 128);
@@ -431,7 +450,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool any = false;
         const float mo_lane = s_stat[ch * 32 + lane];
         named_bar(bar_id, 128);
-        if (qd == 0) s_stat[ch * 32 + lane] = mn;
+        if (qd == 0) {
+          s_stat[ch * 32 + lane] = mn;
+          float mm = mn;
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) mm = fminf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+          if (lane == 0) s_mmin[ch] = mm;
+        }
         named_bar(bar_id, 128);
 #pragma unroll
         for (int h = 0; h < 32; ++h) {
@@ -458,14 +483,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       uint32_t pk[16], pl[16];
+      // exponent argument s * scale * log2(e) - m in one rounding; an invalid slot gets -inf (P = +0)
+      const float shift = valid ? 0.f : -INFINITY;
 #pragma unroll
       for (int h = 0; h < 32; h += 2) {
         const float4 m4 = reinterpret_cast<const float4*>(m_run)[h >> 2];
         const float ma = (h & 2) ? m4.z : m4.x, mb = (h & 2) ? m4.w : m4.y;
-        const float mu0 = (ma == -INFINITY) ? 0.f : ma;  // a head with no valid slot yet: keep z - mu = -inf
+        const float mu0 = (ma == -INFINITY) ? 0.f : ma;  // a head with no valid slot yet (all its slots masked)
         const float mu1 = (mb == -INFINITY) ? 0.f : mb;
-        // masked slots have z = -inf, so exp2 gives +0 without a test; pairs of lanes in packed fp32
-        const float2 e = f32x2_sub(make_float2(z[h], z[h + 1]), make_float2(mu0, mu1));
+        const float2 nmu = f32x2_sub(make_float2(shift, shift), make_float2(mu0, mu1));
+        const float2 e = f32x2_fma(make_float2(__uint_as_float(sv[h]), __uint_as_float(sv[h + 1])),
+                                   make_float2(sl2e, sl2e), nmu);
         const float2 pp = make_float2(exp2f(e.x), exp2f(e.y));
         const float2 ls = f32x2_add(make_float2(l_part[h], l_part[h + 1]), pp);
         l_part[h] = ls.x;
