@@ -97,6 +97,7 @@ struct Smem {
 // misc layout (bytes)
 constexpr int M_BAR_KV = 0;    // [9] chunk landed
 constexpr int M_BAR_PV = 80;   // P.V of the tile done
+constexpr int M_BAR_PVP = 88;  // [3]: key rows 0..63 of channel pair m read (pair 3: M_BAR_PVH)
 constexpr int M_BAR_S = 112, M_BAR_P = 120, M_BAR_FIN = 128, M_BAR_PLO = 136, M_BAR_PVH = 144;
 constexpr int M_BAR_PVM = 152;  // [3]: key rows 64..127 of channel pair m (chunks 2m, 2m+1) read
 constexpr int M_TMEM = 192, M_NEFF = 196, M_ABORT = 200;
@@ -205,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_fin = smem_u32(misc + M_BAR_FIN);
   const uint32_t bar_plo = smem_u32(misc + M_BAR_PLO), bar_pvh = smem_u32(misc + M_BAR_PVH);
   const uint32_t bar_pvm = smem_u32(misc + M_BAR_PVM);
+  const uint32_t bar_pvp = smem_u32(misc + M_BAR_PVP);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + M_TMEM);
   int* s_neff = reinterpret_cast<int*>(misc + M_NEFF);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + M_ABORT);
@@ -225,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_p, 8);
     mbar_init(bar_pvh, 1);
     for (int m = 0; m < 3; ++m) mbar_init(bar_pvm + 8 * m, 1);
+    for (int m = 0; m < 3; ++m) mbar_init(bar_pvp + 8 * m, 1);
     mbar_init(bar_plo, 4);  // the warps of key rows 64..127 (lane quadrants 2, 3)
     mbar_init(bar_fin, 1);
     *s_neff = 0;
@@ -323,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kHalf; ++k)  // + 16 key rows = + 2048 bytes
             mma_ss_w(tO + m * 128, va0 + m * kPair + (uint64_t)(k * 128), pa + (uint64_t)(k * 128), kIdPV2,
                      (i > 0 || k > 0) ? 1u : 0u);
+          mma_commit_w(bar_pvp + 8 * m);  // rows 0..63 of channel pair m are read
         }
 #pragma unroll
         for (int k = 0; k < kHalf; ++k)
@@ -519,27 +523,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p);
-      // rows 0..63 of every slot are free once bar_pvh completes: the lo part of key rows
-      // 64..127 goes into the P slot's rows 0..63, and the next tile's rows 0..63 are gathered
+      // Rows 0..63 of channel pair m are free once the first key half of the pair is multiplied: the
+      // next tile's rows 0..63 of the pair are gathered then.  Once the last pair's are (bar_pvh), the
+      // lo part of key rows 64..127 goes into the P slot's rows 0..63.
+      int rix[4];
+      if (more) check_rows(nraw, rix);
       {
-        const bool okh = mbar_wait(bar_pvh, i & 1, s_abort, err, wait_limit);
-        if (qd >= 2) {
-          if (okh) {
+        bool okh = true;
+#pragma unroll 1
+        for (int m = 0; m < kDv / 128; ++m) {
+          okh = okh && mbar_wait(m < 3 ? bar_pvp + 8 * m : bar_pvh, i & 1, s_abort, err, wait_limit);
+          if (m == 3 && qd >= 2) {
+            if (okh) {
 #pragma unroll
-            for (int uu = 0; uu < 4; ++uu)
-              st_shared_v4(sP + sw128_off(r - 64, ch * 4 + uu), pl[4 * uu], pl[4 * uu + 1], pl[4 * uu + 2],
-                           pl[4 * uu + 3]);
-            fence_proxy_async_smem();
+              for (int uu = 0; uu < 4; ++uu)
+                st_shared_v4(sP + sw128_off(r - 64, ch * 4 + uu), pl[4 * uu], pl[4 * uu + 1], pl[4 * uu + 2],
+                             pl[4 * uu + 3]);
+              fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_plo);
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_plo);
+          if (more && okh) {
+            gather_half<DQK>(sKV + (2 * m) * L::KV_CHUNK, kv, 2 * m, tid, rix, 0);
+            gather_half<DQK>(sKV + (2 * m + 1) * L::KV_CHUNK, kv, 2 * m + 1, tid, rix, 0);
+          }
         }
         if (named_bar_or(bar_id, 128, !okh)) { aborted = true; break; }
       }
       if (more) {
-        int rix[4];
-        check_rows(nraw, rix);
-        for (int c = 0; c < kDv / 64; ++c) gather_half<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, 0);
         // rows 64..127 of channel pair m once P.V has read them, and the RoPE chunk (which
         // holds P) once P.V is complete
         for (int m = 0; m < kDv / 128 && !aborted; ++m) {
