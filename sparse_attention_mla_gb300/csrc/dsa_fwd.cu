@@ -529,11 +529,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int rix[4];
       if (more) check_rows(nraw, rix);
       {
-        bool okh = true;
+        bool okh = true, plo_done = false;
 #pragma unroll 1
         for (int m = 0; m < kDv / 128; ++m) {
           okh = okh && mbar_wait(m < 3 ? bar_pvp + 8 * m : bar_pvh, i & 1, s_abort, err, wait_limit);
-          if (m == 3 && qd >= 2) {
+          // the P_lo move is on the tensor core's path: done as soon as the whole first half is read,
+          // tested between the gathers of the pairs (the gathers run behind the MMAs)
+          if (qd >= 2 && !plo_done && (m == 3 || (okh && warp_all(mbar_test(bar_pvh, i & 1))))) {
             if (okh) {
 #pragma unroll
               for (int uu = 0; uu < 4; ++uu)
@@ -543,6 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_plo);
+            plo_done = true;
           }
           if (more && okh) {
             gather_half<DQK>(sKV + (2 * m) * L::KV_CHUNK, kv, 2 * m, tid, rix, 0);
