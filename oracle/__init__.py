@@ -66,6 +66,14 @@ def _load():
             lib.oracle_attn_slot_prob.restype = None
             lib.oracle_indexer_kl.argtypes = [P, P, P, P, P, P, I, I, I, I, I, ctypes.c_double, P, P, P, P]
             lib.oracle_indexer_kl.restype = None
+            lib.oracle_kpool_metadata.argtypes = [P, I, I, I, P, P, P, P]
+            lib.oracle_kpool_metadata.restype = I
+            lib.oracle_kpool_pool.argtypes = [P, I, P, I, I, I, P]
+            lib.oracle_kpool_pool.restype = None
+            lib.oracle_kpool_compose_row.argtypes = [P, I, I, I, I, I, P]
+            lib.oracle_kpool_compose_row.restype = I
+            lib.oracle_kpool_unpool_grad.argtypes = [P, I, P, I, I, I, P]
+            lib.oracle_kpool_unpool_grad.restype = None
             _lib = lib
     return _lib
 
@@ -264,3 +272,66 @@ def indexer_kl(q_idx_rows, k_idx, w_rows, idx_rows, prob_rows, coeff: float, len
     _load().oracle_indexer_kl(_p(q), _p(k), _p(w), _p(idx), _p(ln), _p(pr), n, k.shape[0], Hi, Di, K, float(coeff),
                               _p(kl), _p(dq), _p(dw), _p(dk))
     return kl, dq, dw, dk
+
+
+# ---------------------------------------------------------------------------
+# k-pool selection (GLM-5.3-Flash): pools of P consecutive tokens of a packed
+# sequence, the query's top-K complete pools by the indexer score against the
+# pooled keys, then the tokens of its incomplete pool; attention over
+# [pooled rows; token rows].  The readings are written in dsa_oracle.c.
+# ---------------------------------------------------------------------------
+def kpool_metadata(cu_seqlens, total_tokens: int, P: int):
+    """Returns (pool_cu [nseq+1], pool_start [T], n_pools [T], tail_start [T], total_pools)."""
+    cu = _i32(cu_seqlens)
+    T, nseq = int(total_tokens), len(cu) - 1
+    pool_cu = np.zeros(nseq + 1, np.int32)
+    ps = np.zeros(max(T, 1), np.int32)
+    npl = np.zeros(max(T, 1), np.int32)
+    ts = np.zeros(max(T, 1), np.int32)
+    total = _load().oracle_kpool_metadata(_p(cu), nseq, T, int(P), _p(pool_cu), _p(ps), _p(npl), _p(ts))
+    if total < 0:
+        raise ValueError("cu_seqlens must be a non-decreasing cover of [0, T] and P >= 1")
+    return pool_cu, ps[:T], npl[:T], ts[:T], int(total)
+
+
+def kpool_pool(x, cu_seqlens, P: int, round_to_bf16: bool = True):
+    """Pooled rows [total_pools, D] (fp64 values; bf16-rounded means unless round_to_bf16 is False)."""
+    xv = _f64(x)
+    cu = _i32(cu_seqlens)
+    nseq = len(cu) - 1
+    total = sum((int(cu[i + 1]) - int(cu[i])) // int(P) for i in range(nseq))
+    D = xv.shape[1]
+    out = np.zeros((max(total, 1), D), np.float64)
+    _load().oracle_kpool_pool(_p(xv), D, _p(cu), nseq, int(P), 1 if round_to_bf16 else 0, _p(out))
+    return out[:total]
+
+
+def kpool_topk(q_idx_rows, k_pool, w_rows, row_t, pool_start_rows, n_pools_rows, tail_start_rows,
+               total_pools: int, K: int, P: int):
+    """Selection of the given rows: the K best complete pools (window [pool_start, pool_start + n_pools - 1]
+    of the pooled keys), then the tail tokens as rows total_pools + s.  Returns (idx [n, K + P - 1]
+    ascending with -1 suffix, len [n], the K-th best pool score [n])."""
+    pidx, plen, kth = indexer_topk_window(q_idx_rows, k_pool, w_rows, pool_start_rows, n_pools_rows, K)
+    lib = _load()
+    n = pidx.shape[0]
+    W = int(K) + int(P) - 1
+    out = np.zeros((n, W), np.int32)
+    ln = np.zeros(n, np.int32)
+    rt, ts = _i64(row_t), _i32(tail_start_rows)
+    for r in range(n):
+        row = np.ascontiguousarray(pidx[r])
+        o = np.zeros(W, np.int32)
+        ln[r] = lib.oracle_kpool_compose_row(_p(row), int(plen[r]), int(ts[r]), int(rt[r]), int(total_pools), W, _p(o))
+        out[r] = o
+    return out, ln, kth
+
+
+def kpool_unpool_grad(dcat, cu_seqlens, P: int, total_pools: int):
+    """Token key gradient [T, D] from the gradient of the attended rows [total_pools + T, D]."""
+    d = _f64(dcat)
+    cu = _i32(cu_seqlens)
+    T = int(cu[-1])
+    D = d.shape[1]
+    out = np.zeros((max(T, 1), D), np.float64)
+    _load().oracle_kpool_unpool_grad(_p(d), D, _p(cu), len(cu) - 1, int(P), int(total_pools), _p(out))
+    return out[:T]

@@ -534,3 +534,112 @@ void oracle_indexer_kl(const double *q_rows /*[n,Hi,Di]*/, const double *k /*[Tk
   }
   free(gk);
 }
+
+/* ------------------------------------------------------------------------ */
+/* k-pool selection (GLM-5.3-Flash).  [NoPE-PR] "Why": the k-pool selection   */
+/* appends the query's incomplete tail pool, so the top-k width is            */
+/* 2048 + 3 = 2051.  The pages define nothing else; the readings taken:       */
+/*  - a pool is P consecutive tokens of one packed sequence, counted from the */
+/*    sequence start (P = 4: an incomplete pool holds at most 3 tokens);      */
+/*  - a pooled row (index key or kv latent) is the mean of its P token rows,  */
+/*    stored in the rows' dtype (bf16, round to nearest even);                */
+/*  - query t ranks, by the indexer score against the pooled keys, the        */
+/*    complete pools of its sequence that end at or before t, keeps the K     */
+/*    best (ties to the lower pool), and appends the tokens of its own        */
+/*    incomplete pool (0 .. P-1 of them);                                     */
+/*  - attention runs over the rows [pooled rows of every sequence; token      */
+/*    rows], pool p at row p and token s at row total_pools + s, so the       */
+/*    selection is one ascending index list of width K + P - 1 (-1 suffix);   */
+/*  - the key gradient of a token is its own row's plus 1/P of its pool's.    */
+/* ------------------------------------------------------------------------ */
+
+/* Per sequence i: pool_cu[i] = complete pools of the sequences before it.    */
+/* Per token t of sequence i: pool_start[t] = pool_cu[i] (the sequence's first */
+/* pool), n_pools[t] = complete pools ending at or before t, tail_start[t] =   */
+/* the first token of t's incomplete pool (t + 1 when there is none).         */
+/* Returns the total number of pools, or -1 if cu_seqlens is not a            */
+/* non-decreasing cover of [0, T] or P < 1.                                   */
+int oracle_kpool_metadata(const int32_t *cu_seqlens, int num_seqs, int T, int P, int32_t *pool_cu,
+                          int32_t *pool_start, int32_t *n_pools, int32_t *tail_start) {
+  if (P < 1 || num_seqs < 0 || cu_seqlens[0] != 0 || cu_seqlens[num_seqs] != T) return -1;
+  int total = 0;
+  for (int i = 0; i < num_seqs; ++i) {
+    const int a = cu_seqlens[i], b = cu_seqlens[i + 1];
+    if (b < a) return -1;
+    pool_cu[i] = total;
+    for (int t = a; t < b; ++t) {
+      const int pos = t - a;             /* position of t in its sequence */
+      const int np = (pos + 1) / P;      /* pools whose last token is <= t */
+      pool_start[t] = total;
+      n_pools[t] = np;
+      tail_start[t] = a + np * P;        /* == t + 1 when t closes a pool */
+    }
+    total += (b - a) / P;
+  }
+  pool_cu[num_seqs] = total;
+  return total;
+}
+
+/* bf16 with round to nearest even of a double that a float holds exactly or
+   nearly (the mean of P bf16 values): through float, then the 16-bit round. */
+static double round_bf16(double x) {
+  float f = (float)x;
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u) return x; /* inf / nan: out of contract */
+  const uint32_t lsb = (u >> 16) & 1u;
+  u = (u + 0x7fffu + lsb) & 0xffff0000u;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* Pooled rows: out[pool_cu[i] + p, :] = mean of x[a + P p .. a + P p + P - 1, :] for
+   every complete pool p of sequence i (a = cu_seqlens[i]); rounded to bf16 unless
+   round_to_bf16 is 0. */
+void oracle_kpool_pool(const double *x, int D, const int32_t *cu_seqlens, int num_seqs, int P,
+                       int round_to_bf16, double *out) {
+  int row = 0;
+  for (int i = 0; i < num_seqs; ++i) {
+    const int a = cu_seqlens[i], n = (cu_seqlens[i + 1] - a) / P;
+    for (int p = 0; p < n; ++p, ++row) {
+      for (int d = 0; d < D; ++d) {
+        double s = 0.0;
+        for (int r = 0; r < P; ++r) s += x[(int64_t)(a + p * P + r) * D + d];
+        const double m = s / (double)P;
+        out[(int64_t)row * D + d] = round_to_bf16 ? round_bf16(m) : m;
+      }
+    }
+  }
+}
+
+/* One query row: the pooled selection (pool_idx[0 .. pool_len-1], pools in
+   global numbering, ascending) followed by the tail tokens tail_start .. t as
+   rows total_pools + s; -1 up to width.  Returns the valid count. */
+int oracle_kpool_compose_row(const int32_t *pool_idx, int pool_len, int tail_start, int t, int total_pools,
+                             int width, int32_t *out) {
+  int n = 0;
+  for (int j = 0; j < pool_len; ++j) out[n++] = pool_idx[j];
+  for (int s = tail_start; s <= t; ++s) out[n++] = total_pools + s;
+  for (int j = n; j < width; ++j) out[j] = -1;
+  return n;
+}
+
+/* Key gradient of the tokens from the gradient of the attended rows:
+   dx[t] = dcat[total_pools + t] + dcat[pool(t)] / P when t lies in a complete
+   pool (pool(t) = pool_cu[i] + (t - a) / P), else dcat[total_pools + t]. */
+void oracle_kpool_unpool_grad(const double *dcat, int D, const int32_t *cu_seqlens, int num_seqs, int P,
+                              int total_pools, double *dx) {
+  int pool0 = 0;
+  for (int i = 0; i < num_seqs; ++i) {
+    const int a = cu_seqlens[i], b = cu_seqlens[i + 1], n = (b - a) / P;
+    for (int t = a; t < b; ++t) {
+      const int p = (t - a) / P;
+      for (int d = 0; d < D; ++d) {
+        double g = dcat[(int64_t)(total_pools + t) * D + d];
+        if (p < n) g += dcat[(int64_t)(pool0 + p) * D + d] / (double)P;
+        dx[(int64_t)t * D + d] = g;
+      }
+    }
+    pool0 += n;
+  }
+}

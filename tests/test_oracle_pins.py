@@ -643,3 +643,133 @@ def test_indexer_kl_gradient_central_finite_differences_in_w():
             fa = 0.5 * oracle.indexer_kl(q, k, a, idx, prob, 1.0)[0].sum()
             fb = 0.5 * oracle.indexer_kl(q, k, b, idx, prob, 1.0)[0].sum()
             np.testing.assert_allclose(dw[t, h], (fa - fb) / (2 * eps), rtol=1e-6, atol=1e-9)
+
+
+# ---------------------------------------------------------------------------
+# k-pool selection (GLM-5.3-Flash; readings in the oracle source)
+# ---------------------------------------------------------------------------
+def enumerate_pools(cu, P):
+    """Independent route: list every complete pool (sequence, first token) in order."""
+    pools = []
+    for i in range(len(cu) - 1):
+        a, b = int(cu[i]), int(cu[i + 1])
+        for f in range(a, b - P + 1, P):
+            pools.append((i, f))
+    return pools
+
+
+@pytest.mark.parametrize("P", [1, 3, 4])
+def test_kpool_metadata_by_enumeration(P):
+    cu = np.array([0, 9, 9, 11, 30, 34], np.int32)  # an empty sequence, one shorter than a pool
+    T = int(cu[-1])
+    pool_cu, ps, npl, ts, total = oracle.kpool_metadata(cu, T, P)
+    pools = enumerate_pools(cu, P)
+    assert total == len(pools)
+    for i in range(len(cu) - 1):
+        assert pool_cu[i] == sum(1 for (j, _) in pools if j < i)
+    for t in range(T):
+        i = int(np.searchsorted(cu, t, side="right")) - 1
+        mine = [g for g, (j, f) in enumerate(pools) if j == i and f + P - 1 <= t]
+        assert npl[t] == len(mine)
+        assert ps[t] == sum(1 for (j, _) in pools if j < i)
+        if mine:
+            assert mine == list(range(ps[t], ps[t] + npl[t]))
+        # the tail: tokens of t's sequence after its last complete pool, up to t
+        last_end = pools[mine[-1]][1] + P if mine else int(cu[i])
+        assert ts[t] == last_end and 0 <= t + 1 - ts[t] <= P - 1
+
+
+def test_kpool_metadata_rejects_bad_input():
+    with pytest.raises(ValueError):
+        oracle.kpool_metadata(np.array([0, 5, 4], np.int32), 4, 4)
+    with pytest.raises(ValueError):
+        oracle.kpool_metadata(np.array([0, 4], np.int32), 4, 0)
+
+
+def test_kpool_pool_is_the_numpy_mean_and_the_bf16_rounding_of_torch():
+    cu = np.array([0, 10, 10, 23], np.int32)
+    P, D = 4, 6
+    x = torch.randn(23, D, generator=torch.Generator().manual_seed(41)).to(torch.bfloat16)
+    xf = x.double().numpy()
+    ref = []
+    for i in range(len(cu) - 1):
+        a, b = int(cu[i]), int(cu[i + 1])
+        n = (b - a) // P
+        if n:
+            ref.append(xf[a:a + n * P].reshape(n, P, D).mean(axis=1))
+    ref = np.concatenate(ref)
+    exact = oracle.kpool_pool(x, cu, P, round_to_bf16=False)
+    assert np.array_equal(exact, ref)
+    rounded = oracle.kpool_pool(x, cu, P)
+    assert np.array_equal(rounded, torch.from_numpy(ref).float().to(torch.bfloat16).double().numpy())
+    # a pool of identical rows is that row
+    same = np.repeat(xf[:1], 8, axis=0)
+    assert np.array_equal(oracle.kpool_pool(same, np.array([0, 8], np.int32), 4), same[:2])
+
+
+def test_kpool_unpool_grad_is_the_adjoint_of_pooling():
+    # x -> [pool(x); x] is linear; the key gradient must be its transpose: <A x, y> = <x, A^T y>
+    rng = np.random.default_rng(42)
+    cu = np.array([0, 13, 13, 30, 33], np.int32)
+    T, D, P = 33, 5, 4
+    x = rng.standard_normal((T, D))
+    pooled = oracle.kpool_pool(x, cu, P, round_to_bf16=False)
+    total = pooled.shape[0]
+    y = rng.standard_normal((total + T, D))
+    lhs = float(np.sum(np.concatenate([pooled, x]) * y))
+    rhs = float(np.sum(x * oracle.kpool_unpool_grad(y, cu, P, total)))
+    assert lhs == pytest.approx(rhs, rel=1e-13, abs=1e-13)
+
+
+def test_kpool_topk_with_pools_of_one_token_is_the_token_indexer():
+    rng = np.random.default_rng(43)
+    cu = np.array([0, 19, 40], np.int32)
+    T, K = 40, 6
+    q = torch.randn(T, 3, 8, generator=torch.Generator().manual_seed(44)).to(torch.bfloat16)
+    k = torch.randn(T, 8, generator=torch.Generator().manual_seed(45)).to(torch.bfloat16)
+    w = rng.uniform(0, 1, (T, 3))
+    _, ps, npl, ts, total = oracle.kpool_metadata(cu, T, 1)
+    kp = oracle.kpool_pool(k, cu, 1)
+    assert total == T and np.array_equal(kp, k.double().numpy())
+    idx, ln, _ = oracle.kpool_topk(q, kp, w, np.arange(T), ps, npl, ts, total, K, 1)
+    st, _, _, _ = oracle.packed_metadata(cu, T)
+    ref, rln, _ = oracle.indexer_topk(q, k, w, st, np.arange(T), K)
+    assert np.array_equal(idx, ref) and np.array_equal(ln, rln)
+
+
+def test_kpool_topk_increasing_pool_scores_pick_the_latest_pools_and_the_tail():
+    cu = np.array([0, 23, 41], np.int32)
+    T, Di, K, P = 41, 4, 3, 4
+    k = np.zeros((T, Di))
+    for i in range(len(cu) - 1):  # every token of pool p (in its sequence) = alpha (p+1) e0
+        for t in range(int(cu[i]), int(cu[i + 1])):
+            k[t, 0] = 0.5 * ((t - int(cu[i])) // P + 1)
+    q = np.abs(np.random.default_rng(46).standard_normal((T, 2, Di))) + 0.1
+    w = np.full((T, 2), 0.25)
+    _, ps, npl, ts, total = oracle.kpool_metadata(cu, T, P)
+    kp = oracle.kpool_pool(k, cu, P)
+    idx, ln, _ = oracle.kpool_topk(q, kp, w, np.arange(T), ps, npl, ts, total, K, P)
+    for t in range(T):
+        n = min(K, int(npl[t]))
+        pools = list(range(ps[t] + npl[t] - n, ps[t] + npl[t]))
+        tail = [total + s for s in range(ts[t], t + 1)]
+        want = pools + tail
+        assert idx[t].tolist() == want + [-1] * (K + P - 1 - len(want)), t
+        assert ln[t] == len(want)
+
+
+def test_kpool_topk_brute_force():
+    rng = np.random.default_rng(47)
+    cu = np.array([0, 30, 37, 64], np.int32)
+    T, Hi, Di, K, P = 64, 3, 6, 4, 4
+    q = rng.standard_normal((T, Hi, Di))
+    k = rng.standard_normal((T, Di))
+    w = rng.uniform(-0.1, 1, (T, Hi))
+    _, ps, npl, ts, total = oracle.kpool_metadata(cu, T, P)
+    kp = oracle.kpool_pool(k, cu, P, round_to_bf16=False)
+    idx, ln, _ = oracle.kpool_topk(q, kp, w, np.arange(T), ps, npl, ts, total, K, P)
+    S = numpy_indexer_scores(q, kp, w)
+    for t in range(T):
+        cand = sorted(range(ps[t], ps[t] + npl[t]), key=lambda p: (-S[t, p], p))
+        sel = sorted(cand[:K]) + [total + s for s in range(ts[t], t + 1)]
+        assert idx[t].tolist() == sel + [-1] * (K + P - 1 - len(sel)), t
