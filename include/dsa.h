@@ -208,6 +208,88 @@ dsa_status_t dsa_indexer_kl(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, co
                             void* workspace, size_t workspace_bytes, dsa_stream_t stream);
 
 /*
+ * k-pool selection (GLM-5.3-Flash).  Source: [NoPE-PR] "Why" (the k-pool
+ * selection appends the query's incomplete tail pool, so the top-k width is
+ * 2048 + 3 = 2051) and "Comparing against cuDNN" (the k-pool path makes its own
+ * selection instead of the token-level top-k).  The pages define nothing more;
+ * readings taken: a pool is P consecutive tokens of one packed sequence counted
+ * from its start (P = 4: an incomplete pool holds at most 3 tokens), numbered
+ * across the sequences in order; a pooled row is the bf16 mean of its P token
+ * rows; query t keeps the K complete pools of its sequence that end at or
+ * before t with the best indexer score against the pooled keys, then the tokens
+ * of its incomplete pool; attention runs over [pooled kv; token kv] (pool p at
+ * row p, token s at row total_pools + s) with the sparse MLA entries unchanged,
+ * and a token's key gradient is its row's plus 1/P of its pool's.
+ */
+
+/*
+ * dsa_kpool_metadata -- pool coordinates of a packed batch.  For sequence i
+ * (L_i tokens) and token t of it at position u = t - cu_seqlens[i]:
+ *   pool_cu[i] = sum_{j<i} floor(L_j / P),  pool_cu[num_seqs] = total pools,
+ *   pool_start[t] = pool_cu[i],  n_pools[t] = floor((u + 1) / P) (complete pools
+ *   ending at or before t),  tail_start[t] = cu_seqlens[i] + P n_pools[t] (the
+ *   first token of t's incomplete pool; t + 1 when t closes a pool).
+ *  cu_seqlens   device int32 [num_seqs + 1], from 0, non-decreasing, ending at total_tokens
+ *  pool         P >= 1
+ *  pool_cu      device int32 [num_seqs + 1] (out)
+ *  pool_start, n_pools, tail_start  device int32 [total_tokens] (out)
+ *  total_pools_host  host int32 (out), may be NULL
+ * Performs one device-to-host synchronisation to validate cu_seqlens
+ * (DSA_ERR_INVALID_ARGUMENT when a rule above is broken; outputs untouched).
+ */
+dsa_status_t dsa_kpool_metadata(const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens, int32_t pool,
+                                int32_t* pool_cu, int32_t* pool_start, int32_t* n_pools, int32_t* tail_start,
+                                int32_t* total_pools_host, dsa_stream_t stream);
+
+/*
+ * dsa_kpool_pool -- pooled rows: out[pool_cu[i] + p, :] = bf16(sum_{r<P}
+ * x[cu_seqlens[i] + P p + r, :] / P) (fp32 sum, round to nearest even) for every
+ * complete pool p of every sequence i.  For the index keys (D = 128) and the kv
+ * latents (D = 576 or 512).
+ *  x            device bf16 [total_tokens, D], D a multiple of 8, 16-byte aligned
+ *  cu_seqlens, pool_cu, num_seqs, pool, total_pools  as dsa_kpool_metadata
+ *  out          device bf16 [total_pools, D] (out), 16-byte aligned
+ */
+dsa_status_t dsa_kpool_pool(const dsa_bf16_t* x, int32_t total_tokens, int32_t D, const int32_t* cu_seqlens,
+                            const int32_t* pool_cu, int32_t num_seqs, int32_t pool, int32_t total_pools,
+                            dsa_bf16_t* out, dsa_stream_t stream);
+
+/*
+ * dsa_kpool_topk -- per query row t: the K pools of [pool_start[t],
+ * pool_start[t] + n_pools[t] - 1] with the highest indexer score (the score and
+ * ranking of dsa_indexer_topk, ties to the lower pool) against the pooled keys,
+ * ascending, then the rows total_pools + s for s = tail_start[t] .. t, then -1,
+ * in rows of width K + pool - 1; topk_len[t] = the valid count.
+ *  q_idx, head_weights  as dsa_indexer_topk (T query rows, Hi in [1, 64], Di = 128)
+ *  k_pool       device bf16 [total_pools, Di] (dsa_kpool_pool of the index keys)
+ *  pool_start, n_pools, tail_start  device int32 [T] (dsa_kpool_metadata)
+ *  K            in [1, 2048] (2048 for GLM-5.3-Flash)
+ *  topk_idx     device int32 [T, K + pool - 1] (out);  topk_len device int32 [T] (out) or NULL
+ *  workspace    >= dsa_kpool_topk_workspace_size(T, K) bytes; its first word is
+ *               the device error word (dsa_read_device_status)
+ */
+size_t dsa_kpool_topk_workspace_size(int32_t T, int32_t K);
+dsa_status_t dsa_kpool_topk(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_pool, const float* head_weights,
+                            const int32_t* pool_start, const int32_t* n_pools, const int32_t* tail_start, int32_t T,
+                            int32_t total_pools, int32_t Hi, int32_t Di, int32_t K, int32_t pool, int32_t* topk_idx,
+                            int32_t* topk_len, void* workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+/*
+ * dsa_kpool_unpool_grad -- token key gradient from the gradient of the attended
+ * rows (the adjoint of x -> [pooled rows; x], without the bf16 rounding):
+ *   dx[t, :] = dcat[total_pools + t, :] + dcat[pool(t), :] / P if t lies in a
+ *   complete pool (pool(t) = pool_cu[i] + floor((t - cu_seqlens[i]) / P)),
+ *   else dcat[total_pools + t, :].
+ *  dcat         device fp32 [total_pools + total_tokens, D] (e.g. the dkv
+ *               accumulator of dsa_sparse_mla_bwd over [pooled kv; kv]), D a
+ *               multiple of 4, 16-byte aligned
+ *  dx           device fp32 [total_tokens, D] (out), 16-byte aligned, not overlapping dcat
+ */
+dsa_status_t dsa_kpool_unpool_grad(const float* dcat, int32_t total_tokens, int32_t D, const int32_t* cu_seqlens,
+                                   const int32_t* pool_cu, int32_t num_seqs, int32_t pool, int32_t total_pools,
+                                   float* dx, dsa_stream_t stream);
+
+/*
  * dsa_sparse_mla_fwd -- absorbed sparse MLA forward (MQA over one latent KV).
  * Source: [DSA-blog] "How DSA works" and "Why DSA needs fused kernels";
  * [cudnn_dsa] cudnn_sparse_attention / _CudnnSparseAttention.forward (q

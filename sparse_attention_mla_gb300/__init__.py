@@ -29,6 +29,10 @@ __all__ = [
     "dsa_indexer_topk_cp",
     "dsa_indexer_topk_with_scores",
     "dsa_indexer_kl",
+    "dsa_kpool_metadata",
+    "dsa_kpool_pool",
+    "dsa_kpool_topk",
+    "dsa_kpool_unpool_grad",
     "dsa_sparse_mla_fwd",
     "dsa_sparse_mla_bwd",
     "dsa_sparse_mla_bwd_noalloc",
@@ -122,6 +126,14 @@ def load_library(path: str | None = None):
         lib.dsa_sparse_mla_bwd_noalloc.restype = ctypes.c_int
         lib.dsa_sparse_mla_bwd_noalloc_read_status.argtypes = [_P, _P]
         lib.dsa_sparse_mla_bwd_noalloc_read_status.restype = ctypes.c_int
+        lib.dsa_kpool_metadata.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
+        lib.dsa_kpool_pool.argtypes = [_P, _I, _I, _P, _P, _I, _I, _I, _P, _P]
+        lib.dsa_kpool_topk_workspace_size.argtypes = [_I, _I]
+        lib.dsa_kpool_topk_workspace_size.restype = _SZ
+        lib.dsa_kpool_topk.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]
+        lib.dsa_kpool_unpool_grad.argtypes = [_P, _I, _I, _P, _P, _I, _I, _I, _P, _P]
+        for name in ("dsa_kpool_metadata", "dsa_kpool_pool", "dsa_kpool_topk", "dsa_kpool_unpool_grad"):
+            getattr(lib, name).restype = ctypes.c_int
         for name in ("dsa_packed_metadata", "dsa_indexer_topk", "dsa_indexer_topk_with_scores",
                      "dsa_sparse_mla_fwd", "dsa_sparse_mla_bwd", "dsa_read_device_status"):
             getattr(lib, name).restype = ctypes.c_int
@@ -335,6 +347,95 @@ def dsa_indexer_kl(q_idx, k_idx, head_weights, topk_idx, attn_prob, coeff: float
                               _stream(dev)),
            "dsa_indexer_kl")
     return kl, dq_idx, dw, dk_idx_accum
+
+
+class KPoolMeta:
+    """Pool coordinates of a packed batch (dsa_kpool_metadata): pool size, per-sequence pool
+    offsets (device int32 [nseq+1]), per-token pool_start / n_pools / tail_start (device int32 [T])
+    and the total number of pools."""
+
+    def __init__(self, cu_seqlens, pool, pool_cu, pool_start, n_pools, tail_start, total_pools):
+        self.cu_seqlens, self.pool, self.pool_cu = cu_seqlens, pool, pool_cu
+        self.pool_start, self.n_pools, self.tail_start, self.total_pools = pool_start, n_pools, tail_start, total_pools
+
+    @property
+    def num_seqs(self) -> int:
+        return self.cu_seqlens.numel() - 1
+
+    @property
+    def total_tokens(self) -> int:
+        return self.pool_start.numel()
+
+
+def dsa_kpool_metadata(cu_seqlens: torch.Tensor, total_tokens: int, pool: int = 4) -> KPoolMeta:
+    """k-pool coordinates: pools of `pool` consecutive tokens of each packed sequence (GLM-5.3-Flash)."""
+    lib = load_library()
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    dev = cu_seqlens.device
+    T = int(total_tokens)
+    pool_cu = torch.empty(cu_seqlens.numel(), dtype=torch.int32, device=dev)
+    ps = torch.empty(T, dtype=torch.int32, device=dev)
+    npl = torch.empty(T, dtype=torch.int32, device=dev)
+    ts = torch.empty(T, dtype=torch.int32, device=dev)
+    total = ctypes.c_int32(0)
+    _check(lib.dsa_kpool_metadata(_ptr(cu_seqlens), cu_seqlens.numel() - 1, T, int(pool), _ptr(pool_cu), _ptr(ps),
+                                  _ptr(npl), _ptr(ts), ctypes.byref(total), _stream(dev)), "dsa_kpool_metadata")
+    return KPoolMeta(cu_seqlens, int(pool), pool_cu, ps, npl, ts, total.value)
+
+
+def dsa_kpool_pool(x: torch.Tensor, meta: KPoolMeta, out=None):
+    """Pooled rows of x (bf16 [T, D]) -> bf16 [total_pools, D]: the mean of each pool's token rows."""
+    lib = load_library()
+    _need(x, "x", torch.bfloat16, 2)
+    dev = x.device
+    T, D = x.shape
+    if out is None:
+        out = torch.empty(meta.total_pools, D, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, 2, dev)
+    _check(lib.dsa_kpool_pool(_ptr(x), T, D, _ptr(meta.cu_seqlens), _ptr(meta.pool_cu), meta.num_seqs, meta.pool,
+                              meta.total_pools, _ptr(out), _stream(dev)), "dsa_kpool_pool")
+    return out
+
+
+def dsa_kpool_topk(q_idx, k_pool, head_weights, meta: KPoolMeta, K: int = 2048, topk_idx=None, topk_len=None,
+                   workspace=None):
+    """k-pool selection -> (topk_idx int32 [T, K + pool - 1], topk_len int32 [T]): the K best complete pools
+    of each row's sequence (rows 0 .. total_pools - 1), then its incomplete pool's tokens (rows
+    total_pools + s), ascending, -1 suffix."""
+    lib = load_library()
+    _need(q_idx, "q_idx", torch.bfloat16, 3)
+    dev = q_idx.device
+    _need(k_pool, "k_pool", torch.bfloat16, 2, dev)
+    _need(head_weights, "head_weights", torch.float32, 2, dev)
+    T, Hi, Di = q_idx.shape
+    W = int(K) + meta.pool - 1
+    if topk_idx is None:
+        topk_idx = torch.empty(T, W, dtype=torch.int32, device=dev)
+    if topk_len is None:
+        topk_len = torch.empty(T, dtype=torch.int32, device=dev)
+    need = int(lib.dsa_kpool_topk_workspace_size(T, int(K)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check(lib.dsa_kpool_topk(_ptr(q_idx), _ptr(k_pool), _ptr(head_weights), _ptr(meta.pool_start),
+                              _ptr(meta.n_pools), _ptr(meta.tail_start), T, meta.total_pools, Hi, Di, int(K),
+                              meta.pool, _ptr(topk_idx), _ptr(topk_len), _ptr(workspace), workspace.numel(),
+                              _stream(dev)), "dsa_kpool_topk")
+    return topk_idx, topk_len
+
+
+def dsa_kpool_unpool_grad(dcat: torch.Tensor, meta: KPoolMeta, dx=None):
+    """Token key gradient fp32 [T, D] from the gradient of the attended rows fp32 [total_pools + T, D]."""
+    lib = load_library()
+    _need(dcat, "dcat", torch.float32, 2)
+    dev = dcat.device
+    D = dcat.shape[1]
+    T = meta.total_tokens
+    if dx is None:
+        dx = torch.empty(T, D, dtype=torch.float32, device=dev)
+    _need(dx, "dx", torch.float32, 2, dev)
+    _check(lib.dsa_kpool_unpool_grad(_ptr(dcat), T, D, _ptr(meta.cu_seqlens), _ptr(meta.pool_cu), meta.num_seqs,
+                                     meta.pool, meta.total_pools, _ptr(dx), _stream(dev)), "dsa_kpool_unpool_grad")
+    return dx
 
 
 def dsa_sparse_mla_fwd(q, kv, topk_idx, softmax_scale: float, topk_len=None, out=None, lse=None,

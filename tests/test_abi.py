@@ -151,3 +151,35 @@ def test_wait_limit_setter_returns_the_previous_value(lib):
         assert lib.dsa_set_wait_limit_cycles(-1) == 1 << 31  # negative: the default
     finally:
         lib.dsa_set_wait_limit_cycles(prev)
+
+
+def test_kpool_entries_reject_invalid_arguments(lib):
+    I = ctypes.c_int32
+    m = lib.dsa_kpool_metadata
+    assert m(FAKE, 2, 16, 0, FAKE, FAKE, FAKE, FAKE, None, None) == 3      # pool < 1
+    assert m(None, 2, 16, 4, FAKE, FAKE, FAKE, FAKE, None, None) == 3      # no cu_seqlens
+    assert m(FAKE, 0, 16, 4, FAKE, FAKE, FAKE, FAKE, None, None) == 3      # no sequence
+    assert m(FAKE, 2, 16, 4, FAKE, None, FAKE, FAKE, None, None) == 3      # no output
+    assert lib.dsa_last_error_message().decode().startswith("dsa_kpool_metadata")
+    pl = lib.dsa_kpool_pool
+    assert pl(FAKE, 16, 12, FAKE, FAKE, 2, 4, 4, FAKE, None) == 3           # D not a multiple of 8
+    assert pl(FAKE, 16, 128, FAKE, FAKE, 2, 4, 5, FAKE, None) == 3          # more pools than tokens / P
+    assert pl(P(0x10002), 16, 128, FAKE, FAKE, 2, 4, 4, FAKE, None) == 3    # misaligned rows
+    assert lib.dsa_last_error_message().decode().startswith("dsa_kpool_pool")
+    tk = lib.dsa_kpool_topk
+    tk.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, ctypes.c_size_t, P]
+
+    def topk(**kw):
+        a = dict(T=8, pools=2, Hi=64, Di=128, K=2048, pool=4, ws=P(0x100000), wsb=1 << 20)
+        a.update(kw)
+        return tk(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["T"], a["pools"], a["Hi"], a["Di"], a["K"], a["pool"], FAKE,
+                  FAKE, a["ws"], a["wsb"], None)
+
+    for bad in [dict(K=0), dict(K=2049), dict(Hi=65), dict(Di=64), dict(pool=0), dict(T=-1)]:
+        assert topk(**bad) == 3, bad
+    assert topk(ws=None) == 4 and topk(wsb=64) == 4
+    assert lib.dsa_kpool_topk_workspace_size(8, 2048) >= 8 * 2048 * 4 + 8 * 4
+    ug = lib.dsa_kpool_unpool_grad
+    assert ug(FAKE, 16, 6, FAKE, FAKE, 2, 4, 4, FAKE, None) == 3            # D not a multiple of 4
+    assert ug(P(0x100000), 16, 8, FAKE, FAKE, 2, 4, 4, P(0x100040), None) == 3  # dx overlaps dcat
+    assert lib.dsa_last_error_message().decode().startswith("dsa_kpool_unpool_grad")
