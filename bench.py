@@ -336,7 +336,7 @@ def run_cuda(args, rank, world, local):
     if not args.no_workloads:
         del ws_b
         torch.cuda.empty_cache()
-        workloads = {name: time_workload(name, args, dev, stream) for name in ("v32", "nope")}
+        workloads = {name: time_workload(name, args, dev, stream) for name in ("v32", "nope", "kpool")}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -582,7 +582,28 @@ def time_workload(name, args, dev, stream) -> dict:
         cu = torch.tensor([0, T], dtype=torch.int32)
     st, _, _, _ = dsa.dsa_packed_metadata(cu.to(dev), T)
     idx_ms = None
-    if "Hi" in c:
+    P = c.get("pool")
+    meta = None
+    if P:  # k-pool selection: the K - P + 1 best pools of 4 tokens, then the tail tokens
+        meta = dsa.dsa_kpool_metadata(cu.to(dev), T, P)
+        ind = synth.indexer_inputs(T, c["Hi"], c["Di"], seed=0, device=dev)
+        k_pool = dsa.dsa_kpool_pool(ind["k_idx"], meta)
+        wi = torch.zeros(int(dsa.load_library().dsa_kpool_topk_workspace_size(T, Kw - P + 1)), dtype=torch.uint8,
+                         device=dev)
+        run_idx = lambda: dsa.dsa_kpool_topk(ind["q_idx"], k_pool, ind["w"], meta, Kw - P + 1, workspace=wi)
+        for _ in range(args.warmup):
+            idx, ln = run_idx()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in ev:
+            a.record(stream)
+            idx, ln = run_idx()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        idx_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        if dsa.dsa_read_device_status(wi) != 0:
+            raise RuntimeError("device status after the k-pool selection")
+        del ind, k_pool
+    elif "Hi" in c:
         ind = synth.indexer_inputs(T, c["Hi"], c["Di"], seed=0, device=dev)
         wi = torch.zeros(dsa.workspace_size("indexer", T, Kw), dtype=torch.uint8, device=dev)
         run_idx = lambda: dsa.dsa_indexer_topk(ind["q_idx"], ind["k_idx"], ind["w"], st, Kw, workspace=wi)
@@ -600,25 +621,37 @@ def time_workload(name, args, dev, stream) -> dict:
         idx = synth.random_causal_topk(st.cpu(), Kw, g).to(dev)
         ln = (idx >= 0).sum(1).to(torch.int32)
     x = synth.mla_inputs(T, Hh, Dqk, Dv, seed=1000, device=dev)
+    kv_rows, extra = x["kv"], 0
+    if meta is not None:  # attention over [pooled kv; kv]
+        extra = meta.total_pools
+        kv_rows = torch.empty(extra + T, Dqk, dtype=torch.bfloat16, device=dev)
+        kv_rows[extra:] = x["kv"]
     wf = torch.zeros(dsa.workspace_size("fwd", T, Hh), dtype=torch.uint8, device=dev)
     wb = torch.zeros(dsa.workspace_size("bwd", T, Hh, Kw), dtype=torch.uint8, device=dev)
     out = torch.empty(T, Hh, Dv, dtype=torch.bfloat16, device=dev)
     lo = torch.empty_like(out)
     lse = torch.empty(T, Hh, dtype=torch.float32, device=dev)
     dq = torch.empty(T, Hh, Dqk, dtype=torch.bfloat16, device=dev)
-    dkv = torch.empty(T, Dqk, dtype=torch.float32, device=dev)
+    dkv = torch.empty(extra + T, Dqk, dtype=torch.float32, device=dev)
+    dkv_tok = torch.empty(T, Dqk, dtype=torch.float32, device=dev) if meta is not None else None
     evs = []
 
     def step(rec):
         for _ in range(layers):  # IndexShare: every layer reuses the one selection
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)] if rec else None
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(5)] if rec else None
+            if e: e[3].record(stream)
+            if meta is not None:  # this layer's pooled kv rows
+                dsa.dsa_kpool_pool(x["kv"], meta, out=kv_rows[:extra])
             if e: e[0].record(stream)
-            dsa.dsa_sparse_mla_fwd(x["q"], x["kv"], idx, scale, topk_len=ln, out=out, lse=lse, workspace=wf,
+            dsa.dsa_sparse_mla_fwd(x["q"], kv_rows, idx, scale, topk_len=ln, out=out, lse=lse, workspace=wf,
                                    out_lo=lo, Dv=Dv)
             if e: e[1].record(stream)
-            dsa.dsa_sparse_mla_bwd(x["q"], x["kv"], idx, scale, out, lse, x["dout"], topk_len=ln, dq=dq,
+            dsa.dsa_sparse_mla_bwd(x["q"], kv_rows, idx, scale, out, lse, x["dout"], topk_len=ln, dq=dq,
                                    dkv_accum=dkv, workspace=wb, out_lo=lo)
             if e: e[2].record(stream)
+            if meta is not None:  # the key gradient back to the tokens
+                dsa.dsa_kpool_unpool_grad(dkv, meta, dx=dkv_tok)
+            if e: e[4].record(stream)
             if e: evs.append(e)
 
     for _ in range(args.warmup):
@@ -642,7 +675,11 @@ def time_workload(name, args, dev, stream) -> dict:
             "timing": f"CUDA events, {args.warmup} warm-up and {args.steps} timed steps, median"}
     if idx_ms is not None:
         line.update({"indexer_ms": round(idx_ms, 3), "indexer_tokens_per_s": round(T / (idx_ms * 1e-3), 1)})
-    del x, out, lo, dq, dkv, idx, ln, wf, wb
+    if meta is not None:
+        line.update({"pool": P, "total_pools": meta.total_pools, "selection": "k-pool (indexer over pooled keys + tail)",
+                     "kv_pool_ms": round(statistics.median(e[3].elapsed_time(e[0]) for e in evs), 3),
+                     "unpool_grad_ms": round(statistics.median(e[2].elapsed_time(e[4]) for e in evs), 3)})
+    del x, out, lo, dq, dkv, idx, ln, wf, wb, kv_rows, dkv_tok
     torch.cuda.empty_cache()
     return line
 
@@ -693,10 +730,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cp", action="store_true", help="skip the context-parallel indexer line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-workloads", action="store_true", help="skip the V3.2 and NoPE workload timings")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the V3.2, NoPE and k-pool workload timings")
     ap.add_argument("--no-kl", action="store_true", help="skip the indexer KL loss path")
     ap.add_argument("--workloads", default=None,
-                    help="comma-separated workload names (tiny,v32,idx32k,nope,thd): one line per workload "
+                    help="comma-separated workload names (tiny,v32,idx32k,nope,thd,kpool): one line per workload "
                          "instead of the benchmark line")
     ap.add_argument("--seq", type=int, default=32768,
                     help="sequence length; only for small-case profiler captures (the benchmark is 32768)")

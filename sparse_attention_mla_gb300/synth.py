@@ -105,4 +105,6 @@ WORKLOADS = {
     "nope": dict(T=16384, H=8, Dqk=512, Dv=512, K=2051, scale=512 ** -0.5),
     "thd": dict(T=131072, H=64, Dqk=576, Dv=512, K=2048, scale=192 ** -0.5, Hi=64, Di=128,
                 nseq=8, lo=4096, hi=32768, layers=4),
+    # GLM-5.3-Flash k-pool selection: pools of 4 tokens, 2048 pools + the 3-token tail = 2051
+    "kpool": dict(T=16384, H=8, Dqk=512, Dv=512, K=2051, scale=512 ** -0.5, Hi=64, Di=128, pool=4),
 }
