@@ -235,3 +235,85 @@ def test_full_indexer_kl_32k_after_the_backward():
     _, _, _, ref_c = oracle.indexer_kl(ind["q_idx"][a:b].cpu(), ind["k_idx"].cpu(), ind["w"][a:b].cpu(),
                                        idx[a:b].cpu(), prob[a:b].cpu(), 1.0, len_rows=ln[a:b].cpu())
     assert_close(dk_c.cpu(), ref_c, f"dk_idx of rows {a}:{b}", max_abs=2e-3 * float(np.abs(ref_c).max()), rel_fro=1e-4)
+
+
+def test_full_kpool_glm_flash_S16384_H8_K2048_plus_tail():
+    """GLM-5.3-Flash k-pool selection at full size (the kpool workload of the benchmark): NoPE
+    width 512, H = 8, 4096 pools of 4 tokens, K = 2048 pools + the 3-token tail.  The oracle makes
+    its own pooling and selection for the rows it checks (sampled rows and a chunk of 64 rows);
+    rows whose selection equals the GPU's are compared element by element with the oracle's own
+    indices (out, lse, dq, and the chunk's dkv over [pooled rows; token rows]), and every checked
+    row's pool set must match within the indexer's fp32 tie band."""
+    c = synth.WORKLOADS["kpool"]
+    T, H, D, P = c["T"], c["H"], c["Dqk"], c["pool"]
+    Kp = c["K"] - P + 1
+    scale = c["scale"]
+    cu = torch.tensor([0, T], dtype=torch.int32)
+    ind = synth.indexer_inputs(T, c["Hi"], c["Di"], seed=0, device=DEV)
+    x = synth.mla_inputs(T, H, D, c["Dv"], seed=1000, device=DEV)
+    meta = dsa.dsa_kpool_metadata(cu.to(DEV), T, P)
+    k_pool = dsa.dsa_kpool_pool(ind["k_idx"], meta)
+    kv_cat = torch.empty(meta.total_pools + T, D, dtype=torch.bfloat16, device=DEV)
+    dsa.dsa_kpool_pool(x["kv"], meta, out=kv_cat[:meta.total_pools])
+    kv_cat[meta.total_pools:] = x["kv"]
+    idx, ln = dsa.dsa_kpool_topk(ind["q_idx"], k_pool, ind["w"], meta, Kp)
+    W = idx.shape[1]
+    wf = torch.zeros(dsa.workspace_size("fwd", T, H), dtype=torch.uint8, device=DEV)
+    wb = torch.zeros(dsa.workspace_size("bwd", T, H, W), dtype=torch.uint8, device=DEV)
+    out, lse, lo = dsa.dsa_sparse_mla_fwd(x["q"], kv_cat, idx, scale, topk_len=ln, out_lo=True, workspace=wf)
+    dq, dcat, _ = dsa.dsa_sparse_mla_bwd(x["q"], kv_cat, idx, scale, out, lse, x["dout"], topk_len=ln, out_lo=lo,
+                                          workspace=wb)
+    dkv = dsa.dsa_kpool_unpool_grad(dcat, meta)
+    assert dsa.dsa_read_device_status(wf) == 0 and dsa.dsa_read_device_status(wb) == 0
+    # the oracle's own pooling and selection for the checked rows
+    _, ps, npl, ts, total = oracle.kpool_metadata(cu, T, P)
+    assert total == meta.total_pools
+    kp = oracle.kpool_pool(ind["k_idx"].cpu(), cu, P)
+    kv_cat_ref = np.concatenate([oracle.kpool_pool(x["kv"].cpu(), cu, P), x["kv"].cpu().double().numpy()])
+    a = T - 64
+    rows = np.unique(np.concatenate([sample_rows(T, [0, 2, 3, 4, 7, 8190, 8191, T - 1], n_random=16, seed=11),
+                                     np.arange(a, T)]))
+    qi, wr = ind["q_idx"][torch.as_tensor(rows)].cpu(), ind["w"][torch.as_tensor(rows)].cpu()
+    ref_idx, ref_len, kth = oracle.kpool_topk(qi, kp, wr, rows, ps[rows], npl[rows], ts[rows], total, Kp, P)
+    gidx, glen = idx[torch.as_tensor(rows)].cpu().numpy(), ln[torch.as_tensor(rows)].cpu().numpy()
+    same = np.zeros(len(rows), bool)
+    for k, t in enumerate(rows):
+        n = int(ref_len[k])
+        assert glen[k] == n and np.all(gidx[k, n:] == -1), t
+        ntail = t + 1 - int(ts[t])
+        assert np.array_equal(gidx[k, n - ntail:n], ref_idx[k, n - ntail:n]), f"row {t}: tail"
+        npool = n - ntail
+        diff = sorted(set(gidx[k, :npool].tolist()) ^ set(ref_idx[k, :npool].tolist()))
+        same[k] = not diff
+        if diff:
+            sc, mag = oracle.indexer_scores(qi[[k]], kp, wr[[k]], np.zeros(len(diff), np.int64), np.array(diff),
+                                            with_magnitude=True)
+            ksc, kmag = oracle.indexer_scores(qi[[k]], kp, wr[[k]], np.zeros(npool, np.int64), ref_idx[k, :npool],
+                                              with_magnitude=True)
+            j = int(np.argmin(ksc))
+            for d in range(len(diff)):
+                assert abs(sc[d] - kth[k]) <= 200 * 2.0 ** -24 * (mag[d] + kmag[j]), f"row {t}: pool {diff[d]}"
+    assert same.mean() >= 0.9
+    ok = rows[same]
+    r = torch.as_tensor(ok)
+    ref_o, ref_l = oracle.sparse_mla_fwd(x["q"][r].cpu(), kv_cat_ref, ref_idx[same], scale, Dv=512,
+                                         len_rows=ref_len[same])
+    assert_close(out[r].cpu(), ref_o, "out (checked rows)")
+    assert_lse(lse[r].cpu(), ref_l)
+    ref_dq, _ = oracle.sparse_mla_bwd(x["q"][r].cpu(), kv_cat_ref, ref_idx[same], x["dout"][r].cpu(), scale,
+                                      Dv=512, len_rows=ref_len[same])
+    assert_close(dq[r].cpu(), ref_dq, "dq (checked rows)")
+    # dkv over [pooled rows; token rows] from the chunk's rows whose selection matched, and the
+    # token gradient through the pooling
+    cr = torch.as_tensor(ok[ok >= a])
+    _, dcat_c, _ = dsa.dsa_sparse_mla_bwd(x["q"][cr].contiguous(), kv_cat, idx[cr].contiguous(), scale,
+                                          out[cr].contiguous(), lse[cr].contiguous(), x["dout"][cr].contiguous(),
+                                          topk_len=ln[cr].contiguous(), out_lo=lo[cr].contiguous(), workspace=wb)
+    assert dsa.dsa_read_device_status(wb) == 0
+    sel = np.isin(rows, ok[ok >= a])
+    _, ref_dcat = oracle.sparse_mla_bwd(x["q"][cr].cpu(), kv_cat_ref, ref_idx[sel], x["dout"][cr].cpu(), scale,
+                                        Dv=512, len_rows=ref_len[sel])
+    assert_close(dcat_c.cpu(), ref_dcat, "dkv of the chunk's rows over [pooled; token] rows")
+    assert_close(dsa.dsa_kpool_unpool_grad(dcat_c, meta).cpu(), oracle.kpool_unpool_grad(ref_dcat, cu, P, total),
+                 "token dkv of the chunk's rows")
+    assert dkv.shape == (T, D)
