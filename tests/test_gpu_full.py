@@ -8,11 +8,13 @@ backward), against the fp64 oracle.
   * the 32k indexer -> MLA path and the THD IndexShare layers, where the
     oracle cannot run every row: out / lse / dq on sampled rows the oracle
     computes one by one (query rows are independent), dkv restricted to a
-    chunk of rows (a call on row-offset pointers) against the oracle's dkv of
-    exactly those rows at full T_k and K, and the dkv column sums
+    chunk of rows (a call on those rows) against the oracle's dkv of exactly
+    those rows at full T_k and K, and the dkv column sums
     sum_k dkv[k,c] = sum_{t,h nonempty} dO[t,h,c] (c < 512), 0 for RoPE;
   * query chunks give the same outputs as one shot.
-Inputs are drawn on the GPU with the seeded recipe (sparse_attention_mla_gb300.synth).
+Inputs are drawn on the GPU with the seeded recipe (sparse_attention_mla_gb300.synth).  Where the
+index sets come from the GPU indexer, the oracle computes its own selection of the rows it checks
+and runs the attention on its own indices, on the rows whose selection equals the GPU's.
 """
 import numpy as np
 import pytest
@@ -58,10 +60,24 @@ def sample_rows(T, starts_of_interest, n_random=12, seed=0):
     return np.array(sorted(rows))
 
 
-def mla_full_check(q, kv, dout, idx, scale, ln=None, rows=None, chunk=(0, 64), Dv=512, every_row=False):
+def matching_rows(idx, ln, rows, sel):
+    """Rows whose GPU selection equals the oracle's own (sel = (idx, len) of `rows`), with the
+    oracle's indices of those rows."""
+    ridx, rlen = sel
+    g = idx[torch.as_tensor(rows)].cpu().numpy()
+    gl = ln[torch.as_tensor(rows)].cpu().numpy()
+    same = np.all(g == ridx, axis=1) & (gl == rlen)
+    assert same.mean() >= 0.9, f"only {same.sum()} of {len(rows)} rows select as the oracle does"
+    return np.asarray(rows)[same], torch.as_tensor(ridx[same]), torch.as_tensor(rlen[same])
+
+
+def mla_full_check(q, kv, dout, idx, scale, ln=None, rows=None, chunk=(0, 64), Dv=512, every_row=False,
+                   ref_sel=None, chunk_sel=None):
     """fwd+bwd of the whole problem as the benchmark runs it, then out/lse on the sampled rows and
     either (every_row) dq of every row and the whole dkv element by element, or dq on the sampled
-    rows, the dkv column sums and the exact dkv of one chunk of rows."""
+    rows, the dkv column sums and the exact dkv of one chunk of rows.  When the index sets come
+    from the GPU indexer, ref_sel / chunk_sel carry the oracle's own selection of `rows` / of the
+    chunk's rows: the oracle then runs on its own indices, on the rows where they equal the GPU's."""
     T, H = q.shape[0], q.shape[1]
     K = idx.shape[1]
     wf = torch.zeros(dsa.workspace_size("fwd", T, H), dtype=torch.uint8, device=DEV)
@@ -70,9 +86,13 @@ def mla_full_check(q, kv, dout, idx, scale, ln=None, rows=None, chunk=(0, 64), D
     dq, dkv, _ = dsa.dsa_sparse_mla_bwd(q, kv, idx, scale, out, lse, dout, topk_len=ln, out_lo=lo, workspace=wb)
     assert dsa.dsa_read_device_status(wf) == 0 and dsa.dsa_read_device_status(wb) == 0
     kvc = kv.cpu()
+    if ref_sel is not None:
+        rows, ridx, rlen = matching_rows(idx, ln, rows, ref_sel)
     r = torch.as_tensor(rows)
-    ln_r = None if ln is None else ln[r].cpu()
-    ref_o, ref_l = oracle.sparse_mla_fwd(q[r].cpu(), kvc, idx[r].cpu(), scale, len_rows=ln_r)
+    if ref_sel is None:  # seeded index sets: the same input on both sides
+        ridx, rlen = idx[r].cpu(), None if ln is None else ln[r].cpu()
+    ln_r = rlen
+    ref_o, ref_l = oracle.sparse_mla_fwd(q[r].cpu(), kvc, ridx, scale, len_rows=ln_r)
     assert_close(out[r].cpu(), ref_o, "out (sampled rows)")
     assert_lse(lse[r].cpu(), ref_l)
     if every_row:
@@ -85,7 +105,7 @@ def mla_full_check(q, kv, dout, idx, scale, ln=None, rows=None, chunk=(0, 64), D
             assert_close(dq[a:b].cpu(), ref_dq, f"dq rows {a}:{b}")
         assert_close(dkv.cpu(), ref_dkv, "dkv (every key row)")
         return out, lse, lo, dq, dkv
-    ref_dq, _ = oracle.sparse_mla_bwd(q[r].cpu(), kvc, idx[r].cpu(), dout[r].cpu(), scale, len_rows=ln_r)
+    ref_dq, _ = oracle.sparse_mla_bwd(q[r].cpu(), kvc, ridx, dout[r].cpu(), scale, len_rows=ln_r)
     assert_close(dq[r].cpu(), ref_dq, "dq (sampled rows)")
     # column sums of the full dkv
     valid = (idx >= 0) if ln is None else ((idx >= 0) & (torch.arange(K, device=DEV)[None, :] < ln[:, None]))
@@ -100,11 +120,17 @@ def mla_full_check(q, kv, dout, idx, scale, ln=None, rows=None, chunk=(0, 64), D
     assert np.max(np.abs(col[Dv:])) <= 2e-2 * scale_ref if col.shape[0] > Dv else True
     # exact dkv of a chunk of rows, at full T_k and K
     a, b = chunk
-    _, dkv_c, _ = dsa.dsa_sparse_mla_bwd(q[a:b], kv, idx[a:b], scale, out[a:b], lse[a:b], dout[a:b],
-                                         topk_len=None if ln is None else ln[a:b], out_lo=lo[a:b], workspace=wb)
+    if chunk_sel is None:
+        cr, cidx, clen = torch.arange(a, b), idx[a:b].cpu(), None if ln is None else ln[a:b].cpu()
+    else:
+        crows, cidx, clen = matching_rows(idx, ln, np.arange(a, b), chunk_sel)
+        cr = torch.as_tensor(crows)
+    g = lambda x: x[cr.to(x.device)].contiguous()
+    _, dkv_c, _ = dsa.dsa_sparse_mla_bwd(g(q), kv, g(idx), scale, g(out), g(lse), g(dout),
+                                         topk_len=None if ln is None else g(ln), out_lo=g(lo), workspace=wb)
     assert dsa.dsa_read_device_status(wb) == 0
-    _, ref_c = oracle.sparse_mla_bwd(q[a:b].cpu(), kvc, idx[a:b].cpu(), dout[a:b].cpu(), scale,
-                                     len_rows=None if ln is None else ln[a:b].cpu())
+    _, ref_c = oracle.sparse_mla_bwd(q[cr.to(q.device)].cpu(), kvc, cidx, dout[cr.to(q.device)].cpu(), scale,
+                                     len_rows=clen)
     assert_close(dkv_c.cpu(), ref_c, f"dkv of rows {a}:{b}")
     return out, lse, lo, dq, dkv
 
@@ -130,16 +156,20 @@ def test_full_indexer_32k_then_sparse_mla_H64():
     ws = torch.zeros(dsa.workspace_size("indexer", T, K), dtype=torch.uint8, device=DEV)
     idx, ln = dsa.dsa_indexer_topk(ind["q_idx"], ind["k_idx"], ind["w"], start, K, workspace=ws)
     assert dsa.dsa_read_device_status(ws) == 0
-    # >= 2048 distinct rows of the indexer against the oracle's full-window top-k
-    rows = np.union1d(sample_rows(T, [0, 1, 2047, 2048, 2049, 16383, T - 2, T - 1], n_random=0, seed=3),
-                      np.random.default_rng(3).choice(T, 2048, replace=False))
-    qi = ind["q_idx"].cpu()
-    check_rows(idx.cpu().numpy(), ln.cpu().numpy(), qi, ind["k_idx"].cpu(), ind["w"].cpu(),
-               start.cpu().numpy(), rows, K)
+    # >= 2048 distinct rows of the indexer against the oracle's full-window top-k; the MLA checks run
+    # on a subset of them with the oracle's own selection
     rows = sample_rows(T, [0, 1, 2047, 2048, 2049, 16383, T - 2, T - 1], n_random=24, seed=3)
-    x = synth.mla_inputs(T, c["H"], c["Dqk"], c["Dv"], seed=4, device=DEV)
     mla_rows = np.union1d(rows, np.random.default_rng(33).choice(T, 512, replace=False))  # oracle time bounds this
-    mla_full_check(x["q"], x["kv"], x["dout"], idx, c["scale"], ln=ln, rows=mla_rows, chunk=(T - 32, T))
+    chunk_rows = np.arange(T - 32, T)
+    all_rows = np.union1d(np.union1d(mla_rows, chunk_rows), np.random.default_rng(3).choice(T, 2048, replace=False))
+    qi = ind["q_idx"].cpu()
+    ref = {}
+    check_rows(idx.cpu().numpy(), ln.cpu().numpy(), qi, ind["k_idx"].cpu(), ind["w"].cpu(),
+               start.cpu().numpy(), all_rows, K, ref_out=ref)
+    pick = lambda rr: (ref["idx"][np.searchsorted(all_rows, rr)], ref["len"][np.searchsorted(all_rows, rr)])
+    x = synth.mla_inputs(T, c["H"], c["Dqk"], c["Dv"], seed=4, device=DEV)
+    mla_full_check(x["q"], x["kv"], x["dout"], idx, c["scale"], ln=ln, rows=mla_rows, chunk=(T - 32, T),
+                   ref_sel=pick(mla_rows), chunk_sel=pick(chunk_rows))
 
 
 def test_full_nope_S16384_H8_K2051_and_query_chunks():
@@ -179,8 +209,12 @@ def test_full_thd_packed_indexshare_4_layers():
     cuts = cu.tolist()
     rows = sample_rows(T, [cuts[1] - 1, cuts[1], cuts[1] + 1, cuts[4] + 2047, cuts[4] + 2048, T - 1], n_random=6,
                        seed=6)
+    chunk_rows = np.arange(cuts[5] - 16, cuts[5] + 16)
+    all_rows = np.union1d(rows, chunk_rows)
+    ref = {}
     check_rows(idx.cpu().numpy(), ln.cpu().numpy(), ind["q_idx"].cpu(), ind["k_idx"].cpu(), ind["w"].cpu(),
-               st_ref, rows, K)
+               st_ref, all_rows, K, ref_out=ref)
+    pick = lambda rr: (ref["idx"][np.searchsorted(all_rows, rr)], ref["len"][np.searchsorted(all_rows, rr)])
     # packing is exact: one sequence run alone gives the same indices (shifted by its offset)
     a, b = cuts[2], cuts[3]
     cu1 = torch.tensor([0, b - a], dtype=torch.int32, device=DEV)
@@ -193,7 +227,7 @@ def test_full_thd_packed_indexshare_4_layers():
     for layer in range(c["layers"]):
         x = synth.mla_inputs(T, c["H"], c["Dqk"], 512, seed=100 + layer, device=DEV)
         mla_full_check(x["q"], x["kv"], x["dout"], idx, c["scale"], ln=ln, rows=rows[::3],
-                       chunk=(cuts[5] - 16, cuts[5] + 16))
+                       chunk=(cuts[5] - 16, cuts[5] + 16), ref_sel=pick(rows[::3]), chunk_sel=pick(chunk_rows))
         del x
         torch.cuda.empty_cache()
     assert torch.equal(idx, idx_before)
@@ -202,7 +236,7 @@ def test_full_thd_packed_indexshare_4_layers():
 def test_full_indexer_kl_32k_after_the_backward():
     # the indexer KL loss on the 32k workload: indexer -> sparse MLA fwd -> bwd (slot probabilities) -> KL.
     # Sampled rows against the oracle (slot probability, kl, dq_idx, dw), and dk_idx of a chunk of rows
-    # exactly (a call on row-offset pointers)
+    # exactly (a call on those rows)
     c = synth.WORKLOADS["idx32k"]
     T, K = c["T"], c["K"]
     ind = synth.indexer_inputs(T, c["Hi"], c["Di"], seed=8, device=DEV)
@@ -220,21 +254,35 @@ def test_full_indexer_kl_32k_after_the_backward():
     kl, dq, dw, dk = dsa.dsa_indexer_kl(ind["q_idx"], ind["k_idx"], ind["w"], idx, prob, 1.0, topk_len=ln,
                                         workspace=ws)
     assert dsa.dsa_read_device_status(ws) == 0
+    # the oracle's own chain for the checked rows: its selection, its slot probabilities, its loss
     rows = sample_rows(T, [0, 1, 2047, 2048, T - 1], n_random=43, seed=8)
+    chunk_rows = np.arange(T - 40, T)
+    all_rows = np.union1d(rows, chunk_rows)
+    ref = {}
+    check_rows(idx.cpu().numpy(), ln.cpu().numpy(), ind["q_idx"].cpu(), ind["k_idx"].cpu(), ind["w"].cpu(),
+               start.cpu().numpy(), all_rows, K, ref_out=ref)
+    pick = lambda rr: (ref["idx"][np.searchsorted(all_rows, rr)], ref["len"][np.searchsorted(all_rows, rr)])
+    rows, ridx, rlen = matching_rows(idx, ln, rows, pick(rows))
     r = torch.as_tensor(rows)
-    ref_p = oracle.attn_slot_prob(x["q"][r].cpu(), x["kv"].cpu(), idx[r].cpu(), c["scale"], len_rows=ln[r].cpu())
+    ref_p = oracle.attn_slot_prob(x["q"][r].cpu(), x["kv"].cpu(), ridx, c["scale"], len_rows=rlen)
     assert np.max(np.abs(prob[r].cpu().double().numpy() - ref_p)) <= 1e-5, "slot probability (sampled rows)"
-    rkl, rdq, rdw, _ = oracle.indexer_kl(ind["q_idx"][r].cpu(), ind["k_idx"].cpu(), ind["w"][r].cpu(), idx[r].cpu(),
-                                         prob[r].cpu(), 1.0, len_rows=ln[r].cpu())
+    rkl, rdq, rdw, _ = oracle.indexer_kl(ind["q_idx"][r].cpu(), ind["k_idx"].cpu(), ind["w"][r].cpu(), ridx,
+                                         ref_p, 1.0, len_rows=rlen)
     assert np.max(np.abs(kl[r].cpu().double().numpy() - rkl) / np.maximum(1.0, np.abs(rkl))) <= 1e-4, "kl"
     assert_close(dq[r].cpu(), rdq, "dq_idx (sampled rows)", max_abs=2e-3 * float(np.abs(rdq).max()))
     assert_close(dw[r].cpu(), rdw, "dw (sampled rows)", max_abs=2e-3 * float(np.abs(rdw).max()), rel_fro=1e-4)
-    a, b = T - 40, T
-    _, _, _, dk_c = dsa.dsa_indexer_kl(ind["q_idx"][a:b], ind["k_idx"], ind["w"][a:b], idx[a:b], prob[a:b], 1.0,
-                                       topk_len=ln[a:b], workspace=ws)
-    _, _, _, ref_c = oracle.indexer_kl(ind["q_idx"][a:b].cpu(), ind["k_idx"].cpu(), ind["w"][a:b].cpu(),
-                                       idx[a:b].cpu(), prob[a:b].cpu(), 1.0, len_rows=ln[a:b].cpu())
-    assert_close(dk_c.cpu(), ref_c, f"dk_idx of rows {a}:{b}", max_abs=2e-3 * float(np.abs(ref_c).max()), rel_fro=1e-4)
+    # dk_idx of the chunk's rows whose selection matches, each side from its own probabilities
+    crows, cidx, clen = matching_rows(idx, ln, chunk_rows, pick(chunk_rows))
+    cr = torch.as_tensor(crows)
+    g = lambda t_: t_[cr.to(t_.device)].contiguous()
+    _, _, _, dk_c = dsa.dsa_indexer_kl(g(ind["q_idx"]), ind["k_idx"], g(ind["w"]), g(idx), g(prob), 1.0,
+                                       topk_len=g(ln), workspace=ws)
+    assert dsa.dsa_read_device_status(ws) == 0
+    cp_ref = oracle.attn_slot_prob(g(x["q"]).cpu(), x["kv"].cpu(), cidx, c["scale"], len_rows=clen)
+    _, _, _, ref_c = oracle.indexer_kl(g(ind["q_idx"]).cpu(), ind["k_idx"].cpu(), g(ind["w"]).cpu(), cidx, cp_ref,
+                                       1.0, len_rows=clen)
+    assert_close(dk_c.cpu(), ref_c, f"dk_idx of rows {chunk_rows[0]}:{chunk_rows[-1] + 1}",
+                 max_abs=2e-3 * float(np.abs(ref_c).max()), rel_fro=1e-4)
 
 
 def test_full_kpool_glm_flash_S16384_H8_K2048_plus_tail():

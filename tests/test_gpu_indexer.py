@@ -29,8 +29,13 @@ def run_gpu(q_idx, k_idx, w, cu, K):
     return idx.cpu().numpy(), ln.cpu().numpy(), start.cpu().numpy()
 
 
-def check_rows(gidx, glen, q_idx, k_idx, w, start, rows, K):
+def check_rows(gidx, glen, q_idx, k_idx, w, start, rows, K, ref_out=None):
+    """The GPU rows against the oracle's own top-k of the same rows (lengths, order and -1 suffix
+    exact; sets equal but for keys inside the fp32 tie band).  Returns the number of swapped pairs;
+    with a dict ref_out, also hands back the oracle's selection of the rows (keys "idx", "len")."""
     ref_idx, ref_len, kth = oracle.indexer_topk(q_idx[rows], k_idx, w[rows], start, rows, K)
+    if ref_out is not None:
+        ref_out["idx"], ref_out["len"] = ref_idx, ref_len
     swaps = 0
     for r, t in enumerate(rows):
         n = int(ref_len[r])
