@@ -113,6 +113,12 @@ dsa_status_t configure_kernel_smem(const void* func, int bytes, const char* what
   if (st != DSA_OK) return st;
   table.run(func, dev, [&] {
     st = cuda_check(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes), what);
+    // all of the SM's unified L1 / shared memory as shared memory, so that kernels sized for two
+    // CTAs per SM get them
+    if (st == DSA_OK)
+      st = cuda_check(cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           (int)cudaSharedmemCarveoutMaxShared),
+                      what);
     return st == DSA_OK;
   });
   return st;

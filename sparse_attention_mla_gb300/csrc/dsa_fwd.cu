@@ -653,26 +653,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // Few heads (H <= 16): the same computation with NH = 16 heads per CTA on the
 // MMA's N side instead of 64, so that a CTA for H = 8 does not multiply 56
-// zero heads.  P^T is split into bf16 hi + lo as above, but both halves sit side
-// by side in one K-major operand of 2 NH rows ([hi heads | lo heads], keys along
-// K), so one P.V MMA (N = 2 NH) forms O_hi and O_lo together; the epilogue adds
-// them.  P lives in a slot of its own: the tile's RoPE chunk is free once S^T is
-// done, and the next tile's RoPE rows are gathered during this tile's softmax.
-// Q is NH x Dqk (18 KiB at 576), so the tile buffer and P fit with room to spare.
+// zero heads, and with 64-key tiles, so that two CTAs share an SM.  With so few
+// heads the tensor core has little to do per key; what bounds a tile is the
+// chain gather -> S^T -> softmax -> P.V -> release of the rows for the next
+// tile's gather, and a second CTA on the SM runs its own chain in the gaps of
+// the first (shared memory per CTA: Q 18 KiB + one tile 72 KiB + P 4 KiB).
+//  * S^T of a tile is an M = 64 MMA: key row 16q + i lands in TMEM lane 32q + i
+//    (i < 16) of lane quadrant q; the softmax threads of lanes 16..31 hold no key.
+//  * P^T is split into bf16 hi + lo as above, both halves side by side in one
+//    K-major operand of 2 NH rows ([hi heads | lo heads], 64 keys along K), so
+//    one P.V MMA (N = 2 NH, M = 128 channels) forms O_hi and O_lo together; the
+//    epilogue adds them.  P has a slot of its own: the tile's RoPE chunk is
+//    free once S^T is done, and the next tile's RoPE rows are gathered during
+//    this tile's softmax; its value chunks channel pair by channel pair as P.V
+//    releases them.
 // ---------------------------------------------------------------------------
+constexpr int kTileF = 64;  // top-k slots per tile of the few-heads kernel (S^T's MMA M)
+
 template <int DQK, int NH>
 struct SmemFew {
   static constexpr int NCH = DQK / 64;
-  static constexpr int Q_CHUNK = NH * 128;      // NH rows x 128 B (K-major B of S^T)
-  static constexpr int KV_CHUNK = kTile * 128;  // 128 keys x 128 B
-  static constexpr int P_BLOCK = 2 * NH * 128;  // one 64-key block of P: 2 NH rows x 128 B
+  static constexpr int Q_CHUNK = NH * 128;       // NH rows x 128 B (K-major B of S^T)
+  static constexpr int KV_CHUNK = kTileF * 128;  // 64 keys x 128 B
+  static constexpr int P_BLOCK = 2 * NH * 128;   // P: 2 NH rows ([hi | lo] heads) x 64 keys (128 B)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = (NCH * Q_CHUNK + 1023) / 1024 * 1024;
   static constexpr int OFF_P = OFF_KV + NCH * KV_CHUNK;
-  static constexpr int OFF_MISC = OFF_P + 2 * P_BLOCK;
+  static constexpr int OFF_MISC = OFF_P + P_BLOCK;
   static constexpr int MISC = 2048;
   static constexpr int TOTAL = OFF_MISC + MISC + 1024;  // + alignment slack
-  static_assert(TOTAL <= 232448, "shared memory budget");
+  // two CTAs per SM (228 KiB of shared memory per SM, 1 KiB of it reserved per CTA)
+  static_assert(2 * (TOTAL + 1024) <= 228 * 1024, "two CTAs per SM");
   static_assert(2 * NH * kDv * 2 <= NCH * KV_CHUNK, "output staging fits in the tile region");
 };
 
@@ -681,12 +692,11 @@ constexpr int F_RED = 256;    // float [4 quadrants][NH]: per-quadrant maxima an
 constexpr int F_STAT = 768;   // float [NH]: running max per head (log2 units)
 constexpr int F_LSUM = 1024;  // float [NH]: softmax denominator per head
 
-// P element (row n of the [hi | lo] operand, key r) in the K-major 128B-swizzled layout: key block
-// r / 64 of P_BLOCK bytes, row n of 128 bytes, 16-byte unit (r % 64) / 8 swizzled with the row.
+// P element (row n of the [hi | lo] operand, key r < 64) in the K-major 128B-swizzled layout:
+// row n of 128 bytes, 16-byte unit r / 8 swizzled with the row.
 template <int NH>
 __device__ __forceinline__ uint32_t p_off(int n, int r) {
-  const int kk = r & 63;
-  return (uint32_t)((r >> 6) * (2 * NH * 128) + n * 128 + ((((kk >> 3) ^ (n & 7))) << 4) + (kk & 7) * 2);
+  return (uint32_t)(n * 128 + ((((r >> 3) ^ (n & 7))) << 4) + (r & 7) * 2);
 }
 
 // Transposing butterfly over N values (N a power of two <= 32): v[0..N-1] per lane (lane = key,
@@ -715,8 +725,25 @@ __device__ __forceinline__ float warp_transpose_reduce_n(float (&v)[N], int lane
   return v[0];
 }
 
+// Rows of chunk c of a 64-key tile into a chunk slot: thread `tid` (of 256) copies 16-byte unit
+// (tid & 7) of rows (tid >> 3) and (tid >> 3) + 32, then arrives on bar (the arrival covers every
+// copy this thread issued before it).  Invalid rows are zero-filled without a global read.
+template <int DQK>
+__device__ __forceinline__ void gather_chunk64(uint32_t dst_chunk, const __nv_bfloat16* __restrict__ kv, int c,
+                                               int tid, const int (&rix)[2], uint32_t bar) {
+  const int uc = tid & 7;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int r = (tid >> 3) + 32 * e;
+    const bool ok = rix[e] >= 0;
+    const __nv_bfloat16* src = kv + (ok ? (size_t)rix[e] * DQK + c * 64 + uc * 8 : 0);
+    cp_async16(dst_chunk + sw128_off(r, uc), src, ok ? 16u : 0u);
+  }
+  cp_async_arrive(bar);
+}
+
 template <int DQK, int NH>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     sparse_mla_fwd_few_kernel(const __nv_bfloat16* __restrict__ kv, const __nv_bfloat16* __restrict__ q,
                               const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ topk_len, int T,
                               int Tk, int H, int K, float sl2e, const float* __restrict__ sink,
@@ -733,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* misc = smem + L::OFF_MISC;
   const uint32_t bar_kv = smem_u32(misc + M_BAR_KV), bar_pv = smem_u32(misc + M_BAR_PV);
   const uint32_t bar_s = smem_u32(misc + M_BAR_S), bar_p = smem_u32(misc + M_BAR_P);
-  const uint32_t bar_fin = smem_u32(misc + M_BAR_FIN), bar_pvh = smem_u32(misc + M_BAR_PVH);
+  const uint32_t bar_fin = smem_u32(misc + M_BAR_FIN);
   const uint32_t bar_pvm = smem_u32(misc + M_BAR_PVM);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + M_TMEM);
   int* s_neff = reinterpret_cast<int*>(misc + M_NEFF);
@@ -752,7 +779,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_pv, 1);
     mbar_init(bar_s, 1);
     mbar_init(bar_p, 8);
-    mbar_init(bar_pvh, 1);
     for (int m = 0; m < 3; ++m) mbar_init(bar_pvm + 8 * m, 1);
     mbar_init(bar_fin, 1);
     *s_neff = 0;
@@ -760,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(s_tmem), 256);
+    tmem_alloc(smem_u32(s_tmem), 256);  // two CTAs per SM: half the columns each
     tmem_relinquish();
   }
   __syncthreads();
@@ -800,19 +826,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   const int n_eff = *s_neff;
-  const int ntiles = (n_eff + kTile - 1) / kTile;
+  const int ntiles = (n_eff + kTileF - 1) / kTileF;
   const uint32_t tmem = *s_tmem;
-  const uint32_t tS = tmem;       // S^T: 128 lanes x NH columns
+  const uint32_t tS = tmem;       // S^T: 64 keys in lanes 32q + i (i < 16) x NH columns
   const uint32_t tO = tmem + 32;  // [O_hi^T | O_lo^T]: 4 channel tiles x 2 NH columns
 
   if (warp == 0) {
     // ======================= MMA issuer (the whole warp, one elected lane issues) =======================
     {
-      constexpr uint32_t kIdS = idesc_bf16(128, NH, false, false);       // A = KV (K-major), B = Q (K-major)
+      constexpr uint32_t kIdS = idesc_bf16(kTileF, NH, false, false);    // A = KV (K-major), B = Q (K-major)
       constexpr uint32_t kIdPV = idesc_bf16(128, 2 * NH, true, false);   // A = V^T (MN-major), B = [P_hi|P_lo] (K-major)
       for (int i = 0; i < ntiles; ++i) {
         bool stop = false;
-        const uint64_t a00 = sdesc_sw128(sKV, 16, 1024), b00 = sdesc_sw128(sQ, 16, 1024);
+        const uint64_t b00 = sdesc_sw128(sQ, 16, 1024);
         for (int c = 0; c < NCH && !stop;) {
           if (!warp_all(mbar_wait(bar_kv + 8 * c, i & 1, s_abort, err, wait_limit))) { stop = true; break; }
           int ce = c + 1;
@@ -820,7 +846,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           tc_fence_after();
           for (; c < ce; ++c) {
-            const uint64_t a0 = a00 + (uint64_t)((c * L::KV_CHUNK) >> 4), b0 = b00 + (uint64_t)((c * L::Q_CHUNK) >> 4);
+            const uint64_t a0 = sdesc_sw128(sKV + c * L::KV_CHUNK, 16, 1024);
+            const uint64_t b0 = b00 + (uint64_t)((c * L::Q_CHUNK) >> 4);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma_ss_w(tS, a0 + (uint64_t)(k * 2), b0 + (uint64_t)(k * 2), kIdS, (c | k) != 0);
@@ -833,22 +860,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t va0 = sdesc_sw128(sKV, L::KV_CHUNK, 1024);
         const uint64_t pb0 = sdesc_sw128(sP, 16, 1024);
         constexpr uint64_t kPair = (2 * L::KV_CHUNK) >> 4;  // descriptor step between channel pairs
-        constexpr uint64_t kPBlk = L::P_BLOCK >> 4;         // descriptor step between 64-key blocks of P
-        // key rows 0..63 for every channel pair, then rows 64..127 pair by pair with a commit after each
+        // channel pair by channel pair, with a commit after each, so that the next tile's rows of a
+        // pair are gathered while later pairs are multiplied
 #pragma unroll
         for (int m = 0; m < kDv / 128; ++m) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)  // + 16 key rows: + 2048 B in V^T, + 32 B along P's rows
+          for (int k = 0; k < kTileF / 16; ++k)  // + 16 key rows: + 2048 B in V^T, + 32 B along P's rows
             mma_ss_w(tO + m * 2 * NH, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 2), kIdPV,
                      (i > 0 || k > 0) ? 1u : 0u);
-        }
-        mma_commit_w(bar_pvh);
-#pragma unroll
-        for (int m = 0; m < kDv / 128; ++m) {
-#pragma unroll
-          for (int k = 4; k < 8; ++k)
-            mma_ss_w(tO + m * 2 * NH, va0 + m * kPair + (uint64_t)(k * 128), pb0 + kPBlk + (uint64_t)((k - 4) * 2),
-                     kIdPV, 1u);
           if (m < 3) mma_commit_w(bar_pvm + 8 * m);
         }
         mma_commit_w(bar_pv);
@@ -863,29 +882,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wk = warp - 1;       // 0..7
     const int qd = warp & 3;       // TMEM lane quadrant this warp may access
     const int ch = wk >> 2;        // head half: heads ch*NHH .. ch*NHH+NHH-1
-    const int r = qd * 32 + lane;  // key row of the tile / channel row of an O^T tile
+    const bool has_key = lane < 16;
+    const int r = qd * 16 + lane;  // key row of the tile (lanes 0..15)
     const int bar_id = 1 + ch;     // named barrier of the 128 threads of this half
-    auto load_raw = [&](int i, int (&raw)[4]) {
+    auto load_raw = [&](int i, int (&raw)[2]) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = i * kTile + (tid >> 3) + 32 * e;
+      for (int e = 0; e < 2; ++e) {
+        const int j = i * kTileF + (tid >> 3) + 32 * e;
         raw[e] = (j < n_eff) ? __ldg(idx_row + j) : -1;
       }
     };
-    auto check_rows = [&](const int (&raw)[4], int (&rix)[4]) {
+    auto check_rows = [&](const int (&raw)[2], int (&rix)[2]) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int e = 0; e < 2; ++e) {
         const int ix = raw[e];
         rix[e] = (ix >= 0 && ix < Tk) ? ix : -1;
         if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
       }
     };
-    int nraw[4];
+    int nraw[2];
     if (ntiles > 0) {
-      int rix[4];
+      int rix[2];
       load_raw(0, nraw);
       check_rows(nraw, rix);
-      for (int c = 0; c < NCH; ++c) gather_chunk<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, bar_kv + 8 * c);
+      for (int c = 0; c < NCH; ++c) gather_chunk64<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, bar_kv + 8 * c);
     }
     const float* m_run = s_stat + ch * NHH;
     float l_part[NHH];
@@ -893,24 +913,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int h = 0; h < NHH; ++h) l_part[h] = 0.f;
     bool aborted = false;
     for (int i = 0; i < ntiles; ++i) {
-      const int j = i * kTile + r;
-      const int ixw = (j < n_eff) ? __ldg(idx_row + j) : -1;
+      const int j = i * kTileF + r;
+      const int ixw = (has_key && j < n_eff) ? __ldg(idx_row + j) : -1;
       const bool more = i + 1 < ntiles;
       if (more) load_raw(i + 1, nraw);
       const bool got = mbar_wait(bar_s, i & 1, s_abort, err, wait_limit);
       if (named_bar_or(bar_id, 128, !got)) { aborted = true; break; }
       tc_fence_after();
       // S^T of the tile is read: the next tile's RoPE rows may be gathered now (P has its own slot)
-      int rix[4];
+      int rix[2];
       if (more) {
         check_rows(nraw, rix);
-        if (NCH == 9) gather_chunk<DQK>(sKV + 8 * L::KV_CHUNK, kv, 8, tid, rix, bar_kv + 8 * 8);
+        if (NCH == 9) gather_chunk64<DQK>(sKV + 8 * L::KV_CHUNK, kv, 8, tid, rix, bar_kv + 8 * 8);
       }
       uint32_t sv[NHH];
       if constexpr (NHH == 8) tmem_ld8(tmem_addr(tS + ch * NHH, qd * 32, 0), sv);
       else tmem_ld16(tmem_addr(tS + ch * NHH, qd * 32, 0), sv);
       tmem_ld_wait();
-      const bool valid = ixw >= 0 && ixw < Tk;
+      const bool valid = has_key && ixw >= 0 && ixw < Tk;  // lanes 16..31 hold no key
       float z[NHH];
 #pragma unroll
       for (int h = 0; h < NHH; ++h) z[h] = valid ? __uint_as_float(sv[h]) * sl2e : -INFINITY;
@@ -973,34 +993,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mu = (mh == -INFINITY) ? 0.f : mh;
         const float p = exp2f(z[h] - mu);
         l_part[h] += p;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(p);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
-        const int n = ch * NHH + h;
-        st_shared_u16(sP + p_off<NH>(n, r), __bfloat16_as_ushort(hi));
-        st_shared_u16(sP + p_off<NH>(NH + n, r), __bfloat16_as_ushort(lo));
+        if (has_key) {
+          const __nv_bfloat16 hi = __float2bfloat16_rn(p);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
+          const int n = ch * NHH + h;
+          st_shared_u16(sP + p_off<NH>(n, r), __bfloat16_as_ushort(hi));
+          st_shared_u16(sP + p_off<NH>(NH + n, r), __bfloat16_as_ushort(lo));
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p);
-      // rows 0..63 of every value chunk once the first key half of P.V has read them, rows 64..127
-      // of channel pair m once pair m is read
-      {
-        const bool okh = mbar_wait(bar_pvh, i & 1, s_abort, err, wait_limit);
-        if (named_bar_or(bar_id, 128, !okh)) { aborted = true; break; }
-      }
+      // the next tile's value chunks, channel pair m as soon as P.V has read it
       if (more) {
-        for (int c = 0; c < kDv / 64; ++c) gather_half<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, 0);
         for (int m = 0; m < kDv / 128 && !aborted; ++m) {
           if (!mbar_wait(m < 3 ? bar_pvm + 8 * m : bar_pv, i & 1, s_abort, err, wait_limit)) {
             aborted = true;
             break;
           }
 #pragma unroll
-          for (int c = 2 * m; c < 2 * m + 2; ++c) {
-            gather_half<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, 1);
-            cp_async_arrive(bar_kv + 8 * c);
-          }
+          for (int c = 2 * m; c < 2 * m + 2; ++c)
+            gather_chunk64<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, bar_kv + 8 * c);
         }
         if (named_bar_or(bar_id, 128, aborted)) { aborted = true; break; }
       }
