@@ -330,8 +330,8 @@ def run_cuda(args, rank, world, local):
     if not args.no_e2e:
         e2e = run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, f_fwd + f_bwd, world)
     cp = None if args.no_cp else run_cp_indexer(args, dsa, torch, dev, stream, ind, topk_idx, topk_len)
-    kl_path = None if args.no_kl else run_kl_path(args, dsa, torch, dev, stream, ind, mla, topk_idx, topk_len, out,
-                                                   out_lo, lse, dq, dkv, ws_b, bwd_ms, n_valid)
+    kl_path = None if args.no_kl else run_kl_path(args, dsa, torch, dev, stream, ind, mla, seq_start, topk_idx,
+                                                   topk_len, out, out_lo, lse, dq, dkv, ws_b, bwd_ms, n_valid)
     workloads = None
     if not args.no_workloads:
         del ws_b
@@ -372,11 +372,12 @@ def run_cuda(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-def run_kl_path(args, dsa, torch, dev, stream, ind, mla, topk_idx, topk_len, out, out_lo, lse, dq, dkv, ws_b,
-                bwd_ms, n_valid):
+def run_kl_path(args, dsa, torch, dev, stream, ind, mla, seq_start, topk_idx, topk_len, out, out_lo, lse, dq, dkv,
+                ws_b, bwd_ms, n_valid):
     """The indexer KL auxiliary loss on the same selection: the backward with its slot-probability output
-    (the extra cost over the plain backward), then the KL kernel (loss and gradients).  CUDA events on the
-    launching stream, median over the timed steps."""
+    (the extra cost over the plain backward), then the KL kernel (loss and gradients) forming the slots'
+    indexer scores itself; and the other order of work: the indexer returning its selection's scores, and
+    the KL kernel reading them.  CUDA events on the launching stream, median over the timed steps."""
     prob = torch.empty(S, K, dtype=torch.float32, device=dev)
     ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
     kl = torch.empty(S, dtype=torch.float32, device=dev)
@@ -388,29 +389,42 @@ def run_kl_path(args, dsa, torch, dev, stream, ind, mla, topk_idx, topk_len, out
         dsa.dsa_sparse_mla_bwd(mla["q"], mla["kv"], topk_idx, SCALE, out, lse, mla["dout"], topk_len=topk_len, dq=dq,
                                dkv_accum=dkv, workspace=ws_b, out_lo=out_lo, attn_prob=prob)
 
-    def klk():
+    def klk(score=None):
         dsa.dsa_indexer_kl(ind["q_idx"], ind["k_idx"], ind["w"], topk_idx, prob, 0.001, topk_len=topk_len, kl=kl,
-                           dq_idx=dqi, dw=dw, dk_idx_accum=dk, workspace=ws)
+                           dq_idx=dqi, dw=dw, dk_idx_accum=dk, workspace=ws, topk_score=score)
 
+    isc = torch.empty(S, K, dtype=torch.float32, device=dev)
+    idx_s, len_s = torch.empty_like(topk_idx), torch.empty_like(topk_len)
+    wi = torch.zeros(dsa.workspace_size("indexer", S, K), dtype=torch.uint8, device=dev)
+
+    def idx_scored():
+        dsa.dsa_indexer_topk_scored(ind["q_idx"], ind["k_idx"], ind["w"], seq_start, K, topk_idx=idx_s,
+                                    topk_len=len_s, topk_score=isc, workspace=wi)
+
+    steps = (bwd, klk, idx_scored, lambda: klk(isc))
     for _ in range(args.warmup):
-        bwd()
-        klk()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        for f in steps:
+            f()
+    torch.cuda.synchronize(dev)
+    if not (torch.equal(idx_s, topk_idx) and torch.equal(len_s, topk_len)):
+        raise RuntimeError("the indexer with scores selected differently")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(steps) + 1)] for _ in range(args.steps)]
     for e in ev:
         e[0].record(stream)
-        bwd()
-        e[1].record(stream)
-        klk()
-        e[2].record(stream)
+        for i, f in enumerate(steps):
+            f()
+            e[i + 1].record(stream)
     torch.cuda.synchronize(dev)
-    if dsa.dsa_read_device_status(ws) != 0 or dsa.dsa_read_device_status(ws_b) != 0:
+    if any(dsa.dsa_read_device_status(w_) != 0 for w_ in (ws, ws_b, wi)):
         raise RuntimeError("device status after the KL path")
-    b_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
-    k_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
-    f_alg = 3 * 2.0 * HI * DI * n_valid  # scores, dq_idx and dk_idx products; the kernel also recomputes the scores
+    b_ms, k_ms, i_ms, kr_ms = (statistics.median(e[i].elapsed_time(e[i + 1]) for e in ev) for i in range(len(steps)))
+    f_alg = 3 * 2.0 * HI * DI * n_valid  # scores, dq_idx and dk_idx products
     return {"bwd_with_slot_prob_ms": round(b_ms, 3), "bwd_ms": round(bwd_ms, 3),
             "indexer_kl_ms": round(k_ms, 3), "indexer_kl_tflops": round(f_alg / (k_ms * 1e-3) / 1e12, 2),
-            "note": "loss coefficient 0.001; kl per row, dq_idx, dw and the fp32 dk_idx accumulator"}
+            "indexer_topk_scored_ms": round(i_ms, 3), "indexer_kl_reading_scores_ms": round(kr_ms, 3),
+            "note": "loss coefficient 0.001; kl per row, dq_idx, dw and the fp32 dk_idx accumulator; "
+                    "indexer_kl_ms forms the slots' scores again, indexer_kl_reading_scores_ms reads those of "
+                    "dsa_indexer_topk_scored (same selection)"}
 
 
 def run_cp_indexer(args, dsa, torch, dev, stream, ind, topk_idx, topk_len, ranks=2):

@@ -172,6 +172,25 @@ dsa_status_t dsa_indexer_topk_with_scores(const dsa_bf16_t* q_idx, const dsa_bf1
                                           size_t workspace_bytes, dsa_stream_t stream);
 
 /*
+ * dsa_indexer_topk_scored -- dsa_indexer_topk (causal_len NULL) or
+ * dsa_indexer_topk_cp (causal_len given) that also returns, slot for slot, the
+ * fp32 score the selection ranked: topk_score[t, j] = score(t, topk_idx[t, j])
+ * for j < topk_len[t], -inf after.  Same kernel and same topk_idx / topk_len as
+ * those calls; the scores are the ones the kernel kept with each candidate.
+ * Their consumer is dsa_indexer_kl, whose loss needs exactly these values
+ * (the KL term of [DSA-blog] "How DSA works" compares the indexer's score
+ * distribution over the selected slots with the attention's).
+ *  topk_score   device fp32 [T, K] (out; required when T > 0)
+ *  the rest     as dsa_indexer_topk / dsa_indexer_topk_cp
+ * Errors as those calls, plus DSA_ERR_INVALID_ARGUMENT when topk_score is NULL.
+ */
+dsa_status_t dsa_indexer_topk_scored(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
+                                     const int32_t* seq_start, const int32_t* causal_len, int32_t T, int32_t T_k,
+                                     int32_t Hi, int32_t Di, int32_t K, int32_t* topk_idx, int32_t* topk_len,
+                                     float* topk_score, void* workspace, size_t workspace_bytes,
+                                     dsa_stream_t stream);
+
+/*
  * dsa_indexer_kl -- the indexer's KL auxiliary loss over each row's selected
  * slots, and its gradient.
  * Source: [DSA-blog] "How DSA works" (the indexer emits an auxiliary KL loss
@@ -191,6 +210,11 @@ dsa_status_t dsa_indexer_topk_with_scores(const dsa_bf16_t* q_idx, const dsa_bf1
  *  q_idx, k_idx, head_weights  as dsa_indexer_topk (Hi in [1, 64], Di = 128)
  *  topk_idx     device int32 [T, K], K in [1, 4096];  topk_len device int32 [T] or NULL
  *  attn_prob    device fp32 [T, K]: e.g. the attn_prob output of dsa_sparse_mla_bwd
+ *  topk_score   device fp32 [T, K] or NULL: the scores I_j of the slots, e.g. the
+ *               topk_score output of dsa_indexer_topk_scored for this topk_idx.
+ *               Given, they are read instead of formed again (one pass over the
+ *               selected keys instead of two); the ReLU masks of the gradient are
+ *               formed from the keys as always.  NULL: I_j is formed here.
  *  coeff        the loss coefficient (the pages train with 0.001); the gradients
  *               are those of coeff * sum_t kl[t]
  *  kl           device fp32 [T] (out);  dq_idx device bf16 [T, Hi, Di] (out)
@@ -202,8 +226,9 @@ dsa_status_t dsa_indexer_topk_with_scores(const dsa_bf16_t* q_idx, const dsa_bf1
  */
 size_t dsa_indexer_kl_workspace_size(int32_t T, int32_t K);
 dsa_status_t dsa_indexer_kl(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
-                            const int32_t* topk_idx, const int32_t* topk_len, const float* attn_prob, int32_t T,
-                            int32_t T_k, int32_t Hi, int32_t Di, int32_t K, float coeff, float* kl,
+                            const int32_t* topk_idx, const int32_t* topk_len, const float* attn_prob,
+                            const float* topk_score, int32_t T, int32_t T_k, int32_t Hi, int32_t Di, int32_t K,
+                            float coeff, float* kl,
                             dsa_bf16_t* dq_idx, float* dw, float* dk_idx_accum, int32_t accumulate,
                             void* workspace, size_t workspace_bytes, dsa_stream_t stream);
 

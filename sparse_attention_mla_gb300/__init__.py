@@ -28,6 +28,7 @@ __all__ = [
     "dsa_indexer_topk",
     "dsa_indexer_topk_cp",
     "dsa_indexer_topk_with_scores",
+    "dsa_indexer_topk_scored",
     "dsa_indexer_kl",
     "dsa_kpool_metadata",
     "dsa_kpool_pool",
@@ -102,6 +103,7 @@ def load_library(path: str | None = None):
         lib.dsa_indexer_topk_workspace_size.restype = _SZ
         lib.dsa_indexer_topk.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]
         lib.dsa_indexer_topk_cp.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]
+        lib.dsa_indexer_topk_scored.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]
         lib.dsa_indexer_topk_with_scores.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _I, _I, _P,
                                                      _SZ, _P]
         lib.dsa_sparse_mla_fwd_workspace_size.argtypes = [_I, _I]
@@ -114,8 +116,8 @@ def load_library(path: str | None = None):
         lib.dsa_read_device_status.argtypes = [_P, _P, _P]
         lib.dsa_indexer_kl_workspace_size.argtypes = [_I, _I]
         lib.dsa_indexer_kl_workspace_size.restype = _SZ
-        lib.dsa_indexer_kl.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _P, _SZ,
-                                       _P]
+        lib.dsa_indexer_kl.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _P,
+                                       _SZ, _P]
         lib.dsa_indexer_kl.restype = ctypes.c_int
         lib.dsa_set_wait_limit_cycles.argtypes = [ctypes.c_int64]
         lib.dsa_set_wait_limit_cycles.restype = ctypes.c_int64
@@ -134,7 +136,8 @@ def load_library(path: str | None = None):
         lib.dsa_kpool_unpool_grad.argtypes = [_P, _I, _I, _P, _P, _I, _I, _I, _P, _P]
         for name in ("dsa_kpool_metadata", "dsa_kpool_pool", "dsa_kpool_topk", "dsa_kpool_unpool_grad"):
             getattr(lib, name).restype = ctypes.c_int
-        for name in ("dsa_packed_metadata", "dsa_indexer_topk", "dsa_indexer_topk_with_scores",
+        for name in ("dsa_packed_metadata", "dsa_indexer_topk", "dsa_indexer_topk_with_scores", "dsa_indexer_topk_scored",
+                     "dsa_indexer_topk_cp",
                      "dsa_sparse_mla_fwd", "dsa_sparse_mla_bwd", "dsa_read_device_status"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -286,6 +289,35 @@ def dsa_indexer_topk(q_idx, k_idx, head_weights, seq_start, K: int, topk_idx=Non
     return topk_idx, topk_len
 
 
+def dsa_indexer_topk_scored(q_idx, k_idx, head_weights, seq_start, K: int, causal_len=None, topk_idx=None,
+                            topk_len=None, topk_score=None, workspace=None):
+    """dsa_indexer_topk (causal_len None) or dsa_indexer_topk_cp that also returns each selected slot's fp32
+    score -> (topk_idx int32 [T,K], topk_len int32 [T], topk_score fp32 [T,K], -inf after the prefix)."""
+    lib = load_library()
+    _need(q_idx, "q_idx", torch.bfloat16, 3)
+    dev = q_idx.device
+    _need(k_idx, "k_idx", torch.bfloat16, 2, dev)
+    _need(head_weights, "head_weights", torch.float32, 2, dev)
+    _need(seq_start, "seq_start", torch.int32, 1, dev)
+    if causal_len is not None:
+        _need(causal_len, "causal_len", torch.int32, 1, dev)
+    T, Hi, Di = q_idx.shape
+    Tk = k_idx.shape[0]
+    if topk_idx is None:
+        topk_idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+    if topk_len is None:
+        topk_len = torch.empty(T, dtype=torch.int32, device=dev)
+    if topk_score is None:
+        topk_score = torch.empty(T, K, dtype=torch.float32, device=dev)
+    _need(topk_score, "topk_score", torch.float32, 2, dev)
+    ws, wsb = _workspace("indexer", T, K, dev, workspace)
+    _check(lib.dsa_indexer_topk_scored(_ptr(q_idx), _ptr(k_idx), _ptr(head_weights), _ptr(seq_start),
+                                       _ptr(causal_len), T, Tk, Hi, Di, int(K), _ptr(topk_idx), _ptr(topk_len),
+                                       _ptr(topk_score), _ptr(ws), wsb, _stream(dev)),
+           "dsa_indexer_topk_scored")
+    return topk_idx, topk_len, topk_score
+
+
 def dsa_indexer_topk_with_scores(q_idx, k_idx, head_weights, seq_start, K: int, score_row0: int,
                                  score_rows: int, workspace=None):
     """Diagnostic form of dsa_indexer_topk -> (topk_idx, topk_len, scores fp32 [score_rows, T_k]): the
@@ -310,10 +342,13 @@ def dsa_indexer_topk_with_scores(q_idx, k_idx, head_weights, seq_start, K: int, 
 
 
 def dsa_indexer_kl(q_idx, k_idx, head_weights, topk_idx, attn_prob, coeff: float, topk_len=None, kl=None,
-                   dq_idx=None, dw=None, dk_idx_accum=None, accumulate: bool = False, workspace=None):
+                   dq_idx=None, dw=None, dk_idx_accum=None, accumulate: bool = False, workspace=None,
+                   topk_score=None):
     """Indexer KL auxiliary loss over each row's selected slots and its gradient -> (kl fp32 [T],
     dq_idx bf16 [T,Hi,Di], dw fp32 [T,Hi], dk_idx_accum fp32 [T_k,Di]); the gradients are those of
-    coeff * sum_t kl[t].  attn_prob: fp32 [T, K], e.g. from dsa_sparse_mla_bwd(attn_prob=True)."""
+    coeff * sum_t kl[t].  attn_prob: fp32 [T, K], e.g. from dsa_sparse_mla_bwd(attn_prob=True).
+    topk_score: fp32 [T, K] or None, the slots' indexer scores (dsa_indexer_topk_scored), read instead
+    of formed again."""
     lib = load_library()
     _need(q_idx, "q_idx", torch.bfloat16, 3)
     dev = q_idx.device
@@ -328,6 +363,10 @@ def dsa_indexer_kl(q_idx, k_idx, head_weights, topk_idx, attn_prob, coeff: float
     K = topk_idx.shape[1]
     if attn_prob.shape != topk_idx.shape:
         raise ValueError("attn_prob must have the shape of topk_idx")
+    if topk_score is not None:
+        _need(topk_score, "topk_score", torch.float32, 2, dev)
+        if topk_score.shape != topk_idx.shape:
+            raise ValueError("topk_score must have the shape of topk_idx")
     kl = torch.empty(T, dtype=torch.float32, device=dev) if kl is None else kl
     dq_idx = torch.empty(T, Hi, Di, dtype=torch.bfloat16, device=dev) if dq_idx is None else dq_idx
     dw = torch.empty(T, Hi, dtype=torch.float32, device=dev) if dw is None else dw
@@ -342,7 +381,7 @@ def dsa_indexer_kl(q_idx, k_idx, head_weights, topk_idx, attn_prob, coeff: float
         workspace = torch.empty(max(int(lib.dsa_indexer_kl_workspace_size(T, K)), 256), dtype=torch.uint8,
                                 device=dev)
     _check(lib.dsa_indexer_kl(_ptr(q_idx), _ptr(k_idx), _ptr(head_weights), _ptr(topk_idx), _ptr(topk_len),
-                              _ptr(attn_prob), T, Tk, Hi, Di, K, float(coeff), _ptr(kl), _ptr(dq_idx), _ptr(dw),
+                              _ptr(attn_prob), _ptr(topk_score), T, Tk, Hi, Di, K, float(coeff), _ptr(kl), _ptr(dq_idx), _ptr(dw),
                               _ptr(dk_idx_accum), 1 if accumulate else 0, _ptr(workspace), workspace.numel(),
                               _stream(dev)),
            "dsa_indexer_kl")

@@ -188,7 +188,7 @@ const char* dsa_status_string(dsa_status_t s) {
 
 const char* dsa_last_error_message(void) { return g_msg; }
 
-int32_t dsa_abi_version(void) { return 2; }
+int32_t dsa_abi_version(void) { return 3; }
 
 int64_t dsa_set_wait_limit_cycles(int64_t cycles) {
   return g_wait_limit.exchange(cycles < 0 ? (1ll << 31) : cycles);

@@ -334,8 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float* __restrict__ w, const int32_t* __restrict__ seq_start,
                         const int32_t* __restrict__ causal_len, int T, int Tk, int Hi,
                         int K, int32_t* __restrict__ topk_idx, int32_t* __restrict__ topk_len,
-                        int* __restrict__ err, float* __restrict__ scores, int score_row0, int score_rows,
-                        long long wait_limit) {
+                        float* __restrict__ topk_score, int* __restrict__ err, float* __restrict__ scores,
+                        int score_row0, int score_rows, long long wait_limit) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(smem + OFF_Q);
@@ -543,6 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int have = aborted ? 0 : min(cnt, n);
       int32_t* row = topk_idx + (size_t)t * K;
       for (int j = hf.tid; j < K; j += 128) row[j] = (j < have) ? ci[j] : -1;
+      if (topk_score != nullptr) {  // the fp32 scores the selection ranked, slot for slot (-inf after the prefix)
+        float* srow = topk_score + (size_t)t * K;
+        for (int j = hf.tid; j < K; j += 128) srow[j] = (j < have) ? cs[j] : -INFINITY;
+      }
       if (topk_len != nullptr && hf.tid == 0) topk_len[t] = have;
     }
   }
@@ -572,7 +576,8 @@ template <bool kScores>
 static dsa_status_t run(const char* who, const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
                         const int32_t* seq_start, const int32_t* causal_len, int32_t T, int32_t T_k, int32_t Hi,
                         int32_t Di, int32_t K,
-                        int32_t* topk_idx, int32_t* topk_len, float* scores, int32_t score_row0, int32_t score_rows,
+                        int32_t* topk_idx, int32_t* topk_len, float* topk_score, float* scores, int32_t score_row0,
+                        int32_t score_rows,
                         void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
   if (T < 0 || T_k < 1) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: need T >= 0 and T_k >= 1", who);
   if (!causal_len && T_k < T) return fail(DSA_ERR_INVALID_ARGUMENT, "%s: T_k (%d) must be >= T (%d)", who, T_k, T);
@@ -600,7 +605,7 @@ static dsa_status_t run(const char* who, const dsa_bf16_t* q_idx, const dsa_bf16
   const int nblk = (T + kTokens - 1) / kTokens;
   indexer_topk_kernel<kScores><<<nblk, kThreads, TOTAL, s>>>(
       map, reinterpret_cast<const __nv_bfloat16*>(q_idx), head_weights, seq_start, causal_len, T, T_k, Hi, K, topk_idx,
-      topk_len, reinterpret_cast<int*>(workspace), scores, score_row0, score_rows, wait_limit_cycles());
+      topk_len, topk_score, reinterpret_cast<int*>(workspace), scores, score_row0, score_rows, wait_limit_cycles());
   if ((st = cuda_check(cudaGetLastError(), "launching indexer_topk_kernel"))) return st;
   return ok();
 }
@@ -612,7 +617,18 @@ extern "C" dsa_status_t dsa_indexer_topk(const dsa_bf16_t* q_idx, const dsa_bf16
                                          int32_t K, int32_t* topk_idx, int32_t* topk_len, void* workspace,
                                          size_t workspace_bytes, dsa_stream_t stream) {
   return idx::run<false>("dsa_indexer_topk", q_idx, k_idx, head_weights, seq_start, nullptr, T, T_k, Hi, Di, K,
-                         topk_idx, topk_len, nullptr, 0, 0, workspace, workspace_bytes, stream);
+                         topk_idx, topk_len, nullptr, nullptr, 0, 0, workspace, workspace_bytes, stream);
+}
+
+extern "C" dsa_status_t dsa_indexer_topk_scored(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx,
+                                                const float* head_weights, const int32_t* seq_start,
+                                                const int32_t* causal_len, int32_t T, int32_t T_k, int32_t Hi,
+                                                int32_t Di, int32_t K, int32_t* topk_idx, int32_t* topk_len,
+                                                float* topk_score, void* workspace, size_t workspace_bytes,
+                                                dsa_stream_t stream) {
+  if (T > 0 && !topk_score) return fail(DSA_ERR_INVALID_ARGUMENT, "dsa_indexer_topk_scored: topk_score is NULL");
+  return idx::run<false>("dsa_indexer_topk_scored", q_idx, k_idx, head_weights, seq_start, causal_len, T, T_k, Hi,
+                         Di, K, topk_idx, topk_len, topk_score, nullptr, 0, 0, workspace, workspace_bytes, stream);
 }
 
 extern "C" dsa_status_t dsa_indexer_topk_cp(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
@@ -622,7 +638,7 @@ extern "C" dsa_status_t dsa_indexer_topk_cp(const dsa_bf16_t* q_idx, const dsa_b
                                             dsa_stream_t stream) {
   if (T_q > 0 && !causal_len) return fail(DSA_ERR_INVALID_ARGUMENT, "dsa_indexer_topk_cp: causal_len is NULL");
   return idx::run<false>("dsa_indexer_topk_cp", q_idx, k_idx, head_weights, seq_start, causal_len, T_q, T_k, Hi, Di,
-                         K, topk_idx, topk_len, nullptr, 0, 0, workspace, workspace_bytes, stream);
+                         K, topk_idx, topk_len, nullptr, nullptr, 0, 0, workspace, workspace_bytes, stream);
 }
 
 extern "C" dsa_status_t dsa_indexer_topk_with_scores(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx,
@@ -632,5 +648,5 @@ extern "C" dsa_status_t dsa_indexer_topk_with_scores(const dsa_bf16_t* q_idx, co
                                                      int32_t score_rows, void* workspace, size_t workspace_bytes,
                                                      dsa_stream_t stream) {
   return idx::run<true>("dsa_indexer_topk_with_scores", q_idx, k_idx, head_weights, seq_start, nullptr, T, T_k, Hi, Di,
-                        K, topk_idx, topk_len, scores, score_row0, score_rows, workspace, workspace_bytes, stream);
+                        K, topk_idx, topk_len, nullptr, scores, score_row0, score_rows, workspace, workspace_bytes, stream);
 }

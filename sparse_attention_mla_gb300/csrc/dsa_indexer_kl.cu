@@ -109,7 +109,8 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[32], int lane) {
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kl_kernel(const __nv_bfloat16* __restrict__ k_idx, const __nv_bfloat16* __restrict__ q_idx,
                       const float* __restrict__ w, const int32_t* __restrict__ topk_idx,
-                      const int32_t* __restrict__ topk_len, const float* __restrict__ prob, int Tk, int Hi, int K,
+                      const int32_t* __restrict__ topk_len, const float* __restrict__ prob,
+                      const float* __restrict__ topk_score, int Tk, int Hi, int K,
                       float coeff, float* __restrict__ kl_out, __nv_bfloat16* __restrict__ dq_out,
                       float* __restrict__ dw_out, float* __restrict__ dk, int* __restrict__ err,
                       long long wait_limit) {
@@ -295,15 +296,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t ph_s = 0;  // phase parity of bar_s, which counts the S products of both passes
   // ---- pass 1: indexer scores of the selected slots, and their attention probabilities ----
   // (each worker loads its slot's probability a tile ahead, stores it for the second pass and keeps
-  // running partials of the row's score maximum and probability sum)
+  // running partials of the row's score maximum and probability sum; the drain warps wait below.
+  // When the selection's scores are given, they are read instead of formed again.)
   float imax_part = -INFINITY, psum_part = 0.f;
   auto prob_of = [&](int i) -> float {
     const int j = i * kTile + tid;
     return (j < n_eff) ? __ldg(prob + (size_t)t * K + j) : 0.f;
   };
-  float p_next = (worker && ntiles > 0) ? prob_of(0) : 0.f;
-  if (worker && ntiles > 0) start_pass();
-  for (int i = 0; warp <= 4 && i < ntiles; ++i) {  // workers and the MMA warp; the drain warps wait below
+  if (topk_score != nullptr) {
+    // the selection's own fp32 scores, slot for slot: no gather and no S product in this pass
+    if (worker) {
+      const float* srow = topk_score + (size_t)t * K;
+      const float* prow = prob + (size_t)t * K;
+#pragma unroll 4
+      for (int j = tid; j < n_eff; j += kWorkers) {
+        const int ix = check_key(__ldg(idx_row + j));
+        const float sc = (ix >= 0) ? __ldg(srow + j) : -INFINITY;
+        const float p = (ix >= 0) ? __ldg(prow + j) : 0.f;
+        s_I[j] = sc;
+        s_P[j] = p;
+        imax_part = fmaxf(imax_part, sc);
+        psum_part += p;
+      }
+    }
+  }
+  float p_next = (worker && ntiles > 0 && topk_score == nullptr) ? prob_of(0) : 0.f;
+  if (worker && ntiles > 0 && topk_score == nullptr) start_pass();
+  for (int i = 0; warp <= 4 && i < ntiles && topk_score == nullptr; ++i) {  // workers and the MMA warp
     const int ix = ixa;
     if (worker) {
       const bool more = i + 1 < ntiles;
@@ -581,7 +600,7 @@ extern "C" size_t dsa_indexer_kl_workspace_size(int32_t T, int32_t K) {
 
 extern "C" dsa_status_t dsa_indexer_kl(const dsa_bf16_t* q_idx, const dsa_bf16_t* k_idx, const float* head_weights,
                                        const int32_t* topk_idx, const int32_t* topk_len, const float* attn_prob,
-                                       int32_t T, int32_t T_k, int32_t Hi, int32_t Di, int32_t K, float coeff,
+                                       const float* topk_score, int32_t T, int32_t T_k, int32_t Hi, int32_t Di, int32_t K, float coeff,
                                        float* kl, dsa_bf16_t* dq_idx, float* dw, float* dk_idx_accum,
                                        int32_t accumulate, void* workspace, size_t workspace_bytes,
                                        dsa_stream_t stream) {
@@ -612,7 +631,7 @@ extern "C" dsa_status_t dsa_indexer_kl(const dsa_bf16_t* q_idx, const dsa_bf16_t
     return st;
   kl::indexer_kl_kernel<<<T, kl::kThreads, kl::TOTAL, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(k_idx), reinterpret_cast<const __nv_bfloat16*>(q_idx), head_weights,
-      topk_idx, topk_len, attn_prob, T_k, Hi, K, coeff, kl, reinterpret_cast<__nv_bfloat16*>(dq_idx), dw,
+      topk_idx, topk_len, attn_prob, topk_score, T_k, Hi, K, coeff, kl, reinterpret_cast<__nv_bfloat16*>(dq_idx), dw,
       dk_idx_accum, reinterpret_cast<int*>(workspace), wait_limit_cycles());
   if ((st = cuda_check(cudaGetLastError(), "launching indexer_kl_kernel"))) return st;
   return ok();

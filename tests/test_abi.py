@@ -26,7 +26,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dsa_abi_version() == 2
+    assert lib.dsa_abi_version() == 3
     for code in range(8):
         s = lib.dsa_status_string(code).decode()
         assert s.startswith(dsa.STATUS_NAMES[code])
@@ -135,6 +135,20 @@ def idxr_cp(lib, **kw):
 def test_indexer_cp_rejects_invalid_arguments(lib, bad):
     assert idxr_cp(lib, **bad) == 3
     assert lib.dsa_last_error_message().decode().startswith("dsa_indexer_topk_cp")
+
+
+def test_indexer_scored_rejects_invalid_arguments(lib):
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, w=FAKE, st=FAKE, cl=None, T=4, Tk=8, Hi=64, Di=128, K=64, idx=FAKE, ln=None,
+                 sc=FAKE, ws=P(0x100000), wsb=1 << 20, stream=None)
+        a.update(kw)
+        return lib.dsa_indexer_topk_scored(a["q"], a["k"], a["w"], a["st"], a["cl"], a["T"], a["Tk"], a["Hi"],
+                                           a["Di"], a["K"], a["idx"], a["ln"], a["sc"], a["ws"], a["wsb"],
+                                           a["stream"])
+    for bad in (dict(sc=None), dict(Tk=3), dict(K=2049), dict(Hi=65), dict(q=P(0x10002))):
+        assert call(**bad) == 3, bad
+        assert lib.dsa_last_error_message().decode().startswith("dsa_indexer_topk_scored")
+    assert call(ws=None) == 4
 
 
 def test_indexer_rejects_bad_workspace(lib):

@@ -130,7 +130,11 @@ def test_indexer_cp_ranks_equal_cp1_and_oracle():
         qi64 = qi.astype(np.int64)
         idx, ln = dsa.dsa_indexer_topk_cp(q_all[qi64].to(DEV), k_dev, w_all[qi64].to(DEV), st, cl, K, workspace=ws)
         assert dsa.dsa_read_device_status(ws) == 0
-        idx, ln, st, cl = idx.cpu().numpy(), ln.cpu().numpy(), st.cpu().numpy(), cl.cpu().numpy()
+        # the oracle's own window metadata for these rows; the GPU's must equal it
+        st_ref, cl_ref, _, _ = oracle.packed_metadata_cp(cu, total, query_indices=qi, cu_seqlens_padded=P,
+                                                         padding_mask=pm)
+        assert np.array_equal(st.cpu().numpy(), st_ref) and np.array_equal(cl.cpu().numpy(), cl_ref)
+        idx, ln, st, cl = idx.cpu().numpy(), ln.cpu().numpy(), st_ref, cl_ref
         for j, g in enumerate(qi.tolist()):
             c = compact_of.get(g)
             if c is None or pm[j]:  # a padding row: empty window, empty selection

@@ -20,7 +20,7 @@ from sparse_attention_mla_gb300 import synth
 
 from _cmp import MAX_ABS, REL_FRO, assert_close, assert_lse, errors, storage_half_ulp, to64
 from test_gpu_fwd import make_case
-from test_gpu_indexer import check_rows
+from test_gpu_indexer import check_rows, oracle_start
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -115,4 +115,5 @@ def test_indexer_k_one_and_k_2048_boundaries():
         ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
         idx, ln = dsa.dsa_indexer_topk(x["q_idx"].to(DEV), x["k_idx"].to(DEV), x["w"].to(DEV), start, K, workspace=ws)
         assert dsa.dsa_read_device_status(ws) == 0
-        check_rows(idx.cpu().numpy(), ln.cpu().numpy(), x["q_idx"], x["k_idx"], x["w"], start.cpu().numpy(), rows, K)
+        check_rows(idx.cpu().numpy(), ln.cpu().numpy(), x["q_idx"], x["k_idx"], x["w"], oracle_start(cu, T, start),
+                   rows, K)

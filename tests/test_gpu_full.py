@@ -25,7 +25,7 @@ import sparse_attention_mla_gb300 as dsa
 from sparse_attention_mla_gb300 import synth
 
 from _cmp import assert_close, assert_lse
-from test_gpu_indexer import check_rows
+from test_gpu_indexer import check_rows, oracle_start
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -165,7 +165,7 @@ def test_full_indexer_32k_then_sparse_mla_H64():
     qi = ind["q_idx"].cpu()
     ref = {}
     check_rows(idx.cpu().numpy(), ln.cpu().numpy(), qi, ind["k_idx"].cpu(), ind["w"].cpu(),
-               start.cpu().numpy(), all_rows, K, ref_out=ref)
+               oracle_start(cu, T, start), all_rows, K, ref_out=ref)
     pick = lambda rr: (ref["idx"][np.searchsorted(all_rows, rr)], ref["len"][np.searchsorted(all_rows, rr)])
     x = synth.mla_inputs(T, c["H"], c["Dqk"], c["Dv"], seed=4, device=DEV)
     mla_full_check(x["q"], x["kv"], x["dout"], idx, c["scale"], ln=ln, rows=mla_rows, chunk=(T - 32, T),
@@ -242,7 +242,7 @@ def test_full_indexer_kl_32k_after_the_backward():
     ind = synth.indexer_inputs(T, c["Hi"], c["Di"], seed=8, device=DEV)
     cu = torch.tensor([0, T], dtype=torch.int32, device=DEV)
     start, _, _, _ = dsa.dsa_packed_metadata(cu, T)
-    idx, ln = dsa.dsa_indexer_topk(ind["q_idx"], ind["k_idx"], ind["w"], start, K)
+    idx, ln, isc = dsa.dsa_indexer_topk_scored(ind["q_idx"], ind["k_idx"], ind["w"], start, K)
     x = synth.mla_inputs(T, c["H"], c["Dqk"], c["Dv"], seed=9, device=DEV)
     out, lse, lo = dsa.dsa_sparse_mla_fwd(x["q"], x["kv"], idx, c["scale"], topk_len=ln, out_lo=True)
     wb = torch.zeros(dsa.workspace_size("bwd", T, c["H"], K), dtype=torch.uint8, device=DEV)
@@ -251,16 +251,18 @@ def test_full_indexer_kl_32k_after_the_backward():
     assert dsa.dsa_read_device_status(wb) == 0
     del wb, out, lo
     ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
-    kl, dq, dw, dk = dsa.dsa_indexer_kl(ind["q_idx"], ind["k_idx"], ind["w"], idx, prob, 1.0, topk_len=ln,
-                                        workspace=ws)
+    # the KL twice: forming the slots' indexer scores itself, and reading the selection's own scores
+    runs = [dsa.dsa_indexer_kl(ind["q_idx"], ind["k_idx"], ind["w"], idx, prob, 1.0, topk_len=ln, workspace=ws,
+                               topk_score=s_) for s_ in (None, isc)]
     assert dsa.dsa_read_device_status(ws) == 0
+    del isc
     # the oracle's own chain for the checked rows: its selection, its slot probabilities, its loss
     rows = sample_rows(T, [0, 1, 2047, 2048, T - 1], n_random=43, seed=8)
     chunk_rows = np.arange(T - 40, T)
     all_rows = np.union1d(rows, chunk_rows)
     ref = {}
     check_rows(idx.cpu().numpy(), ln.cpu().numpy(), ind["q_idx"].cpu(), ind["k_idx"].cpu(), ind["w"].cpu(),
-               start.cpu().numpy(), all_rows, K, ref_out=ref)
+               oracle_start(cu, T, start), all_rows, K, ref_out=ref)
     pick = lambda rr: (ref["idx"][np.searchsorted(all_rows, rr)], ref["len"][np.searchsorted(all_rows, rr)])
     rows, ridx, rlen = matching_rows(idx, ln, rows, pick(rows))
     r = torch.as_tensor(rows)
@@ -268,9 +270,12 @@ def test_full_indexer_kl_32k_after_the_backward():
     assert np.max(np.abs(prob[r].cpu().double().numpy() - ref_p)) <= 1e-5, "slot probability (sampled rows)"
     rkl, rdq, rdw, _ = oracle.indexer_kl(ind["q_idx"][r].cpu(), ind["k_idx"].cpu(), ind["w"][r].cpu(), ridx,
                                          ref_p, 1.0, len_rows=rlen)
-    assert np.max(np.abs(kl[r].cpu().double().numpy() - rkl) / np.maximum(1.0, np.abs(rkl))) <= 1e-4, "kl"
-    assert_close(dq[r].cpu(), rdq, "dq_idx (sampled rows)", max_abs=2e-3 * float(np.abs(rdq).max()))
-    assert_close(dw[r].cpu(), rdw, "dw (sampled rows)", max_abs=2e-3 * float(np.abs(rdw).max()), rel_fro=1e-4)
+    for how, (kl, dq, dw, _) in zip(("formed scores", "read scores"), runs):
+        assert np.max(np.abs(kl[r].cpu().double().numpy() - rkl) / np.maximum(1.0, np.abs(rkl))) <= 1e-4, how
+        assert_close(dq[r].cpu(), rdq, f"dq_idx (sampled rows, {how})", max_abs=2e-3 * float(np.abs(rdq).max()))
+        assert_close(dw[r].cpu(), rdw, f"dw (sampled rows, {how})", max_abs=2e-3 * float(np.abs(rdw).max()),
+                     rel_fro=1e-4)
+    del runs
     # dk_idx of the chunk's rows whose selection matches, each side from its own probabilities
     crows, cidx, clen = matching_rows(idx, ln, chunk_rows, pick(chunk_rows))
     cr = torch.as_tensor(crows)

@@ -20,13 +20,22 @@ DEV = "cuda:0"
 GAMMA = 200 * 2.0 ** -24
 
 
+def oracle_start(cu, T, gpu_start=None):
+    """The oracle's own window starts for cu_seqlens; the GPU's metadata, when given, must equal them
+    exactly (it is checked here, never handed to the oracle)."""
+    st = oracle.packed_metadata(np.asarray(cu.cpu() if torch.is_tensor(cu) else cu, np.int32), T)[0]
+    if gpu_start is not None:
+        assert np.array_equal(gpu_start.cpu().numpy(), st[:T]), "seq_start differs from the oracle's"
+    return st
+
+
 def run_gpu(q_idx, k_idx, w, cu, K):
     T = q_idx.shape[0]
     start, _, _, _ = dsa.dsa_packed_metadata(cu.to(DEV), T)
     ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
     idx, ln = dsa.dsa_indexer_topk(q_idx.to(DEV), k_idx.to(DEV), w.to(DEV), start, K, workspace=ws)
     assert dsa.dsa_read_device_status(ws) == 0
-    return idx.cpu().numpy(), ln.cpu().numpy(), start.cpu().numpy()
+    return idx.cpu().numpy(), ln.cpu().numpy(), oracle_start(cu, T, start)
 
 
 def check_rows(gidx, glen, q_idx, k_idx, w, start, rows, K, ref_out=None):
@@ -148,7 +157,7 @@ def test_indexer_selection_is_exact_on_its_own_scores(T, K, cut, row0, nrows):
     assert dsa.dsa_read_device_status(ws) == 0
     idx0, ln0 = dsa.dsa_indexer_topk(q, k, w, start, K)  # the production kernel selects the same
     assert torch.equal(idx0, idx) and torch.equal(ln0, ln)
-    idx, ln, sc, st = idx.cpu().numpy(), ln.cpu().numpy(), sc.cpu().numpy(), start.cpu().numpy()
+    idx, ln, sc, st = idx.cpu().numpy(), ln.cpu().numpy(), sc.cpu().numpy(), oracle_start(cu, T, start)
     for r in range(nrows):
         t = row0 + r
         want = _exact_topk(sc[r], st[t], t, K)

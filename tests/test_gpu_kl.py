@@ -63,12 +63,17 @@ def kl_inputs(T, Tk, K, Hi, seed, ln_frac=None):
     return q_idx, x["k_idx"], w, idx, prob, ln
 
 
-def check_kl(q_idx, k_idx, w, idx, prob, coeff=1.0, ln=None):
+def check_kl(q_idx, k_idx, w, idx, prob, coeff=1.0, ln=None, topk_score=None, ref=None):
+    """The GPU's KL on (idx, prob, ln[, topk_score]) against the oracle's on ref = (idx, prob, ln): the
+    same seeded inputs by default, or the oracle's own selection and target where the GPU's come from
+    GPU kernels (they must then name the same slots)."""
     ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
-    kl, dq, dw, dk = dsa.dsa_indexer_kl(q_idx.to(DEV), k_idx.to(DEV), w.to(DEV), idx.to(DEV), prob.to(DEV), coeff,
-                                        topk_len=None if ln is None else ln.to(DEV), workspace=ws)
+    dev = lambda t_: None if t_ is None else t_.to(DEV)
+    kl, dq, dw, dk = dsa.dsa_indexer_kl(dev(q_idx), dev(k_idx), dev(w), dev(idx), dev(prob), coeff, topk_len=dev(ln),
+                                        workspace=ws, topk_score=dev(topk_score))
     assert dsa.dsa_read_device_status(ws) == 0
-    rkl, rdq, rdw, rdk = oracle.indexer_kl(q_idx, k_idx, w, idx, prob, coeff, len_rows=ln)
+    r_idx, r_prob, r_ln = (idx, prob, ln) if ref is None else ref
+    rkl, rdq, rdw, rdk = oracle.indexer_kl(q_idx, k_idx, w, r_idx, r_prob, coeff, len_rows=r_ln)
     gkl = to64(kl)
     assert np.max(np.abs(gkl - rkl) / np.maximum(1.0, np.abs(rkl))) <= 1e-4, "kl"
     for got, ref, name in ((dq, rdq, "dq_idx"), (dw, rdw, "dw"), (dk, rdk, "dk_idx")):
@@ -117,9 +122,49 @@ def test_kl_target_equal_to_indexer_distribution_gives_zero():
 
 
 def test_kl_chained_after_the_sparse_mla_backward():
-    # the backward's attn_prob feeds the KL kernel directly (the training order)
+    # the backward's attn_prob feeds the KL kernel directly (the training order); the oracle chains its
+    # own slot probabilities into its own loss
     T, Tk, K = 64, 700, 200
     q, kv, dout, idx = make_case(T, Tk - T, 64, 576, K, 74)
     x = synth.indexer_inputs(Tk, 64, 128, seed=74)
     prob = gpu_prob(q, kv, dout, idx, 192 ** -0.5)
-    check_kl(x["q_idx"][Tk - T:].contiguous(), x["k_idx"], x["w"][Tk - T:].contiguous(), idx, prob.cpu())
+    ref_prob = torch.as_tensor(oracle.attn_slot_prob(q, kv, idx, 192 ** -0.5, Dv=512))
+    check_kl(x["q_idx"][Tk - T:].contiguous(), x["k_idx"], x["w"][Tk - T:].contiguous(), idx, prob,
+             ref=(idx, ref_prob, None))
+
+
+@pytest.mark.parametrize("T,K,cut,nrows", [(900, 256, [0, 300, 303, 900], 900), (2300, 2048, [0, 2300], 160)])
+def test_kl_reading_the_selection_scores(T, K, cut, nrows):
+    # indexer with its scores -> KL reading them (no second gather or S product for the scores).  The
+    # scores against the oracle's fp64 scores of its own selection; the loss and gradients against the
+    # oracle on the rows whose selection equals the oracle's, with the oracle's own indices
+    from test_gpu_indexer import GAMMA, check_rows, oracle_start
+    x = synth.indexer_inputs(T, 64, 128, seed=79)
+    cu = torch.tensor(cut, dtype=torch.int32)
+    start, _, _, _ = dsa.dsa_packed_metadata(cu.to(DEV), T)
+    q, k, w = x["q_idx"].to(DEV), x["k_idx"].to(DEV), x["w"].to(DEV)
+    idx, ln, sc = dsa.dsa_indexer_topk_scored(q, k, w, start, K)
+    idx0, ln0 = dsa.dsa_indexer_topk(q, k, w, start, K)
+    assert torch.equal(idx, idx0) and torch.equal(ln, ln0)  # the same kernel selects the same
+    # checked rows: all, or a sample with the first and last rows and those around K
+    chk = np.arange(T) if nrows >= T else np.union1d([0, 1, K - 1, K, K + 1, T - 1],
+                                                     np.random.default_rng(81).choice(T, nrows, replace=False))
+    ref = {}
+    check_rows(idx.cpu().numpy(), ln.cpu().numpy(), x["q_idx"], x["k_idx"], x["w"], oracle_start(cu, T, start),
+               chk, K, ref_out=ref)
+    gi, gl, gs = idx.cpu().numpy()[chk], ln.cpu().numpy()[chk], sc.cpu().double().numpy()[chk]
+    same = np.all(gi == ref["idx"], axis=1) & (gl == ref["len"])
+    assert same.mean() >= 0.95
+    for i in np.nonzero(same)[0][:: max(1, int(same.sum()) // 200)]:
+        t, n = int(chk[i]), int(ref["len"][i])
+        assert np.all(gs[i, n:] == -np.inf), t
+        rs, mag = oracle.indexer_scores(x["q_idx"][[t]], x["k_idx"], x["w"][[t]], np.zeros(n, np.int64),
+                                        ref["idx"][i, :n], with_magnitude=True)
+        assert np.all(np.abs(gs[i, :n] - rs) <= GAMMA * mag), f"row {t}: scores"
+    prob = (torch.rand(T, K, generator=synth.generator(80), dtype=torch.float64) ** 4).float()
+    rows = chk[same]
+    r = torch.as_tensor(rows)
+    ref_idx, ref_ln = torch.as_tensor(ref["idx"][same]), torch.as_tensor(ref["len"][same])
+    g = lambda t_: t_[r.to(t_.device)].contiguous()
+    check_kl(g(x["q_idx"]), x["k_idx"], g(x["w"]), g(idx), g(prob), ln=g(ln), topk_score=g(sc),
+             ref=(ref_idx, g(prob), ref_ln))

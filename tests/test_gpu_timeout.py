@@ -18,7 +18,7 @@ from sparse_attention_mla_gb300 import synth
 
 from _cmp import assert_close, assert_lse
 from test_gpu_fwd import make_case
-from test_gpu_indexer import check_rows
+from test_gpu_indexer import check_rows, oracle_start
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -57,7 +57,7 @@ def test_wait_limit_expiry_is_reported_and_the_next_call_is_clean(zero_wait_limi
     dsa.dsa_set_wait_limit_cycles(-1)
     status, (ti, tl), (out, lse), (dq, dkv) = run_all(q, kv, dout, idx, 0.1, ind, start, K)
     assert status == (0, 0, 0), status
-    check_rows(ti.cpu().numpy(), tl.cpu().numpy(), ind["q_idx"], ind["k_idx"], ind["w"], start.cpu().numpy(),
+    check_rows(ti.cpu().numpy(), tl.cpu().numpy(), ind["q_idx"], ind["k_idx"], ind["w"], oracle_start([0, T], T, start),
                np.array([0, 1, 63, 64, 350, T - 1]), K)
     ref_o, ref_l = oracle.sparse_mla_fwd(q, kv, idx, 0.1)
     ref_dq, ref_dkv = oracle.sparse_mla_bwd(q, kv, idx, dout, 0.1)
