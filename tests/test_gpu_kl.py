@@ -97,6 +97,36 @@ def test_kl_several_tiles_ragged_holes_and_special_rows():
         assert torch.all(dw[r] == 0)
 
 
+def _slot_scores_fp32(q_idx, k_idx, w, idx):
+    # the slots' indexer scores in fp64 by torch (not the oracle), stored as fp32 like the indexer's output;
+    # holes and slots past a row's prefix get NaN, which the kernel must never read
+    qd, kd, wd = q_idx.double(), k_idx.double(), w.double()
+    safe = idx.clamp(min=0).long()
+    I = torch.einsum("th,thj->tj", wd, torch.relu(torch.einsum("thd,tjd->thj", qd, kd[safe])))
+    return torch.where(idx >= 0, I, torch.full_like(I, float("nan"))).float()
+
+
+@pytest.mark.parametrize("T,K,use_len", [(24, 300, False), (400, 300, True), (400, 301, False)])
+def test_kl_reading_scores_special_rows_and_many_rows_per_cta(T, K, use_len):
+    # the score-reading kernel walks several rows per CTA (T = 400 over at most one CTA per SM): rows
+    # without tiles (empty, zero target) between rows with tiles, holes, one valid slot, prefixes; rows
+    # of K = 300 slots start on 16-byte boundaries (vector loads), rows of K = 301 do not
+    q_idx, k_idx, w, idx, prob, ln = kl_inputs(T, 900, K, 64, 76, ln_frac=1.0 if use_len else None)
+    idx[2, 10] = -1
+    idx[4, :] = -1
+    idx[6, 1:] = -1
+    prob[8] = 0.0
+    idx[T - 1, :] = -1
+    if ln is not None:
+        ln[11] = 0
+        idx = torch.where(torch.arange(idx.shape[1])[None, :] < ln[:, None].long(), idx, torch.full_like(idx, -1))
+    sc = _slot_scores_fp32(q_idx, k_idx, w, idx)
+    kl, dq, dw, _ = check_kl(q_idx, k_idx, w, idx, prob, ln=ln, topk_score=sc)
+    for r in (4, 6, 8, T - 1):
+        assert abs(float(kl[r])) < 1e-6
+        assert torch.all(dw[r] == 0)
+
+
 def test_kl_fewer_heads_topk_len_and_coefficient():
     q_idx, k_idx, w, idx, prob, ln = kl_inputs(20, 700, 261, 16, 72, ln_frac=1.0)
     check_kl(q_idx, k_idx, w, idx, prob, coeff=0.001, ln=ln)
