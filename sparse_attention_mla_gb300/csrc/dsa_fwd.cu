@@ -650,44 +650,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ---------------------------------------------------------------------------
-// Few heads (H <= 16): the same computation with NH = 16 heads per CTA on the
-// MMA's N side instead of 64, so that a CTA for H = 8 does not multiply 56
-// zero heads, and with 64-key tiles, so that two CTAs share an SM.  With so few
-// heads the tensor core has little to do per key; what bounds a tile is the
-// chain gather -> S^T -> softmax -> P.V -> release of the rows for the next
-// tile's gather, and a second CTA on the SM runs its own chain in the gaps of
-// the first (shared memory per CTA: Q 18 KiB + one tile 72 KiB + P 4 KiB).
-//  * S^T of a tile is an M = 64 MMA: key row 16q + i lands in TMEM lane 32q + i
-//    (i < 16) of lane quadrant q; the softmax threads of lanes 16..31 hold no key.
-//  * P^T is split into bf16 hi + lo as above, both halves side by side in one
-//    K-major operand of 2 NH rows ([hi heads | lo heads], 64 keys along K), so
-//    one P.V MMA (N = 2 NH, M = 128 channels) forms O_hi and O_lo together; the
-//    epilogue adds them.  P has a slot of its own: the tile's RoPE chunk is
-//    free once S^T is done, and the next tile's RoPE rows are gathered during
-//    this tile's softmax; its value chunks channel pair by channel pair as P.V
-//    releases them.
-// ---------------------------------------------------------------------------
 constexpr int kTileF = 64;  // top-k slots per tile of the few-heads kernel (S^T's MMA M)
 
-template <int DQK, int NH>
-struct SmemFew {
-  static constexpr int NCH = DQK / 64;
-  static constexpr int Q_CHUNK = NH * 128;       // NH rows x 128 B (K-major B of S^T)
-  static constexpr int KV_CHUNK = kTileF * 128;  // 64 keys x 128 B
-  static constexpr int P_BLOCK = 2 * NH * 128;   // P: 2 NH rows ([hi | lo] heads) x 64 keys (128 B)
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = (NCH * Q_CHUNK + 1023) / 1024 * 1024;
-  static constexpr int OFF_P = OFF_KV + NCH * KV_CHUNK;
-  static constexpr int OFF_MISC = OFF_P + P_BLOCK;
-  static constexpr int MISC = 2048;
-  static constexpr int TOTAL = OFF_MISC + MISC + 1024;  // + alignment slack
-  // two CTAs per SM (228 KiB of shared memory per SM, 1 KiB of it reserved per CTA)
-  static_assert(2 * (TOTAL + 1024) <= 228 * 1024, "two CTAs per SM");
-  static_assert(2 * NH * kDv * 2 <= NCH * KV_CHUNK, "output staging fits in the tile region");
-};
-
-// misc layout of the few-heads kernel (bytes): barriers as in the 64-head kernel, then
+// misc offsets of the few-heads kernel (bytes), after its barriers:
 constexpr int F_RED = 256;    // float [4 quadrants][NH]: per-quadrant maxima and sums
 constexpr int F_STAT = 768;   // float [NH]: running max per head (log2 units)
 constexpr int F_LSUM = 1024;  // float [NH]: softmax denominator per head
@@ -725,32 +690,64 @@ __device__ __forceinline__ float warp_transpose_reduce_n(float (&v)[N], int lane
   return v[0];
 }
 
-// Rows of chunk c of a 64-key tile into a chunk slot: thread `tid` (of 256) copies 16-byte unit
-// (tid & 7) of rows (tid >> 3) and (tid >> 3) + 32, then arrives on bar (the arrival covers every
-// copy this thread issued before it).  Invalid rows are zero-filled without a global read.
-template <int DQK>
-__device__ __forceinline__ void gather_chunk64(uint32_t dst_chunk, const __nv_bfloat16* __restrict__ kv, int c,
-                                               int tid, const int (&rix)[2], uint32_t bar) {
-  const int uc = tid & 7;
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int r = (tid >> 3) + 32 * e;
-    const bool ok = rix[e] >= 0;
-    const __nv_bfloat16* src = kv + (ok ? (size_t)rix[e] * DQK + c * 64 + uc * 8 : 0);
-    cp_async16(dst_chunk + sw128_off(r, uc), src, ok ? 16u : 0u);
-  }
-  cp_async_arrive(bar);
-}
+// ---------------------------------------------------------------------------
+// Few heads (H <= 16): the same computation with NH = 16 heads per CTA on the
+// MMA's N side instead of 64 (so that H = 8 does not multiply 56 zero heads)
+// and 64-key tiles.  With so few heads the tensor core has little to do per
+// key, and the tile is bound by its MMA instructions (48 small ones per 64
+// keys), by shared-memory traffic and by the gathers, not by the arithmetic.
+// So one CTA per SM holds a ring of R tiles (R = 3 at width 512, 2 at 576),
+// filled by four gather warps (a slot is refilled once P.V of the tile it held
+// is done), and three warps issue the MMAs: two form S^T of a tile from half
+// the channel chunks each, into two TMEM partials that the softmax adds, and
+// one forms P.V.  S^T is double-buffered in TMEM and runs up to two tiles
+// ahead of the softmax; P is double-buffered in shared memory.  A rescale of O
+// at tile i waits for P.V(i - 1) explicitly.
+//  * S^T of a tile is an M = 64 MMA: key row 16q + i lands in TMEM lane 32q + i
+//    (i < 16) of lane quadrant q; the softmax threads of lanes 16..31 hold no key.
+//  * P^T is split into bf16 hi + lo, both halves side by side in one K-major
+//    operand of 2 NH rows ([hi heads | lo heads], 64 keys along K), so one P.V
+//    MMA (N = 2 NH, M = 128 channels) forms O_hi and O_lo together; the
+//    epilogue adds them.
+// Warps: 0 and 14 issue S^T, 1-8 run the softmax and the epilogue, 9-12 gather,
+// 13 issues P.V.
+// ---------------------------------------------------------------------------
+constexpr int kRingGather = 128;                       // gather threads (warps 9-12)
+constexpr int kRingRows = kTileF / (kRingGather / 8); // rows of a tile per gather thread
+constexpr int kRingThreads = 32 + kWorkers + kRingGather + 64;  // + the P.V issuer (warp 13), S^T issuer 2 (14)
 
 template <int DQK, int NH>
-__global__ void __launch_bounds__(kThreads, 2)
-    sparse_mla_fwd_few_kernel(const __nv_bfloat16* __restrict__ kv, const __nv_bfloat16* __restrict__ q,
-                              const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ topk_len, int T,
-                              int Tk, int H, int K, float sl2e, const float* __restrict__ sink,
-                              __nv_bfloat16* __restrict__ out, __nv_bfloat16* __restrict__ out_lo,
-                              float* __restrict__ lse, int* __restrict__ err, long long wait_limit) {
-  using L = SmemFew<DQK, NH>;
-  constexpr int NCH = L::NCH;
+struct SmemRing {
+  static constexpr int NCH = DQK / 64;
+  static constexpr int R = (DQK == 512) ? 3 : 2;        // tiles in the ring
+  static constexpr int Q_CHUNK = NH * 128;
+  static constexpr int KV_CHUNK = kTileF * 128;
+  static constexpr int SLOT = NCH * KV_CHUNK;
+  static constexpr int P_BLOCK = 2 * NH * 128;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = (NCH * Q_CHUNK + 1023) / 1024 * 1024;
+  static constexpr int OFF_P = OFF_KV + R * SLOT;        // two P buffers
+  static constexpr int OFF_MISC = OFF_P + 2 * P_BLOCK;
+  static constexpr int MISC = 2048;
+  static constexpr int TOTAL = OFF_MISC + MISC + 1024;  // + alignment slack
+  static_assert(TOTAL <= 232448, "shared memory budget");
+  static_assert(2 * NH * kDv * 2 <= SLOT, "output staging fits in slot 0");
+  static_assert(NH <= 16, "TMEM layout: S^T partials of 16 columns");
+};
+// misc layout (bytes): barriers, then the statistics at the offsets above
+constexpr int RB_KV = 0, RB_PV = 32, RB_S = 64, RB_P = 80, RB_FIN = 96;  // [R], [R], [2], [2], [3]
+constexpr int RM_TMEM = 128, RM_NEFF = 132, RM_ABORT = 136;
+static_assert(RB_FIN + 24 <= RM_TMEM && RM_ABORT + 4 <= F_RED, "ring misc layout");
+
+template <int DQK, int NH>
+__global__ void __launch_bounds__(kRingThreads, 1)
+    sparse_mla_fwd_ring_kernel(const __nv_bfloat16* __restrict__ kv, const __nv_bfloat16* __restrict__ q,
+                               const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ topk_len, int T,
+                               int Tk, int H, int K, float sl2e, const float* __restrict__ sink,
+                               __nv_bfloat16* __restrict__ out, __nv_bfloat16* __restrict__ out_lo,
+                               float* __restrict__ lse, int* __restrict__ err, long long wait_limit) {
+  using L = SmemRing<DQK, NH>;
+  constexpr int NCH = L::NCH, R = L::R;
   constexpr int NHH = NH / 2;  // heads per softmax thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -758,42 +755,44 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t sKV = smem_u32(smem + L::OFF_KV);
   const uint32_t sP = smem_u32(smem + L::OFF_P);
   uint8_t* misc = smem + L::OFF_MISC;
-  const uint32_t bar_kv = smem_u32(misc + M_BAR_KV), bar_pv = smem_u32(misc + M_BAR_PV);
-  const uint32_t bar_s = smem_u32(misc + M_BAR_S), bar_p = smem_u32(misc + M_BAR_P);
-  const uint32_t bar_fin = smem_u32(misc + M_BAR_FIN);
-  const uint32_t bar_pvm = smem_u32(misc + M_BAR_PVM);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + M_TMEM);
-  int* s_neff = reinterpret_cast<int*>(misc + M_NEFF);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(misc + M_ABORT);
+  const uint32_t bar_kv = smem_u32(misc + RB_KV), bar_pv = smem_u32(misc + RB_PV);
+  const uint32_t bar_s = smem_u32(misc + RB_S), bar_p = smem_u32(misc + RB_P);
+  const uint32_t bar_fin = smem_u32(misc + RB_FIN);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + RM_TMEM);
+  int* s_neff = reinterpret_cast<int*>(misc + RM_NEFF);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(misc + RM_ABORT);
   float* s_red = reinterpret_cast<float*>(misc + F_RED);
   float* s_stat = reinterpret_cast<float*>(misc + F_STAT);
   float* s_lsum = reinterpret_cast<float*>(misc + F_LSUM);
 
   const int t = blockIdx.x;
-  const int hg = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool worker = warp >= 1 && warp <= 8;
   const int32_t* idx_row = topk_idx + (size_t)t * K;
 
   if (threadIdx.x == 0) {
-    for (int c = 0; c < NCH; ++c) mbar_init(bar_kv + 8 * c, kWorkers);
-    mbar_init(bar_pv, 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_p, 8);
-    for (int m = 0; m < 3; ++m) mbar_init(bar_pvm + 8 * m, 1);
-    mbar_init(bar_fin, 1);
+    for (int s = 0; s < R; ++s) {
+      mbar_init(bar_kv + 8 * s, kRingGather);
+      mbar_init(bar_pv + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_s + 8 * b, 2);  // both S^T partials
+      mbar_init(bar_p + 8 * b, 8);
+    }
+    for (int f = 0; f < 3; ++f) mbar_init(bar_fin + 8 * f, 1);
     *s_neff = 0;
     *s_abort = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(s_tmem), 256);  // two CTAs per SM: half the columns each
+    tmem_alloc(smem_u32(s_tmem), 256);
     tmem_relinquish();
   }
   __syncthreads();
 
-  const int tid = threadIdx.x - 32;  // worker id 0..255 (negative for warp 0)
+  const int tid = threadIdx.x - 32;  // worker id 0..255
   // ---- valid prefix length and Q staging (workers) ----
-  if (warp >= 1) {
+  if (worker) {
     if (topk_len != nullptr) {
       if (tid == 0) {
         int n = topk_len[t];
@@ -806,20 +805,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (last) atomicMax(s_neff, last);
     }
     if (tid < NH) {  // running max per head (log2 units), from the sink logit when there is one
-      const int h = hg * NH + tid;
-      s_stat[tid] = (sink != nullptr && h < H) ? __ldg(sink + h) * 1.4426950408889634f : -INFINITY;
+      s_stat[tid] = (sink != nullptr && tid < H) ? __ldg(sink + tid) * 1.4426950408889634f : -INFINITY;
     }
-    // Q [NH heads, DQK] -> NCH chunks of [NH rows x 128 B], 128B swizzle; heads >= H are zero.
     constexpr int UNITS = NH * NCH * 8;
     const uint64_t pol = l2_evict_first_policy();
     for (int u = tid; u < UNITS; u += kWorkers) {
       const int hh = u / (NCH * 8);
       const int rem = u - hh * (NCH * 8);
       const int c = rem >> 3, uc = rem & 7;
-      const int h = hg * NH + hh;
-      const bool ok = h < H;
+      const bool ok = hh < H;
       cp_async16_hint(sQ + c * L::Q_CHUNK + sw128_off(hh, uc),
-                      q + (ok ? ((size_t)t * H + h) * DQK + c * 64 + uc * 8 : 0), ok ? 16u : 0u, pol);
+                      q + (ok ? ((size_t)t * H + hh) * DQK + c * 64 + uc * 8 : 0), ok ? 16u : 0u, pol);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     fence_proxy_async_smem();
@@ -828,112 +824,135 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int n_eff = *s_neff;
   const int ntiles = (n_eff + kTileF - 1) / kTileF;
   const uint32_t tmem = *s_tmem;
-  const uint32_t tS = tmem;       // S^T: 64 keys in lanes 32q + i (i < 16) x NH columns
-  const uint32_t tO = tmem + 32;  // [O_hi^T | O_lo^T]: 4 channel tiles x 2 NH columns
+  const uint32_t tS = tmem;       // S^T buffer b, partial p (channel chunks) at column 32 b + 16 p
+  const uint32_t tO = tmem + 64;  // [O_hi^T | O_lo^T]: 4 channel tiles x 2 NH columns
 
-  if (warp == 0) {
-    // ======================= MMA issuer (the whole warp, one elected lane issues) =======================
-    {
-      constexpr uint32_t kIdS = idesc_bf16(kTileF, NH, false, false);    // A = KV (K-major), B = Q (K-major)
-      constexpr uint32_t kIdPV = idesc_bf16(128, 2 * NH, true, false);   // A = V^T (MN-major), B = [P_hi|P_lo] (K-major)
-      for (int i = 0; i < ntiles; ++i) {
-        bool stop = false;
-        const uint64_t b00 = sdesc_sw128(sQ, 16, 1024);
-        for (int c = 0; c < NCH && !stop;) {
-          if (!warp_all(mbar_wait(bar_kv + 8 * c, i & 1, s_abort, err, wait_limit))) { stop = true; break; }
-          int ce = c + 1;
-          while (ce < NCH && warp_all(mbar_test(bar_kv + 8 * ce, i & 1))) ++ce;
-          fence_proxy_async_smem();
-          tc_fence_after();
-          for (; c < ce; ++c) {
-            const uint64_t a0 = sdesc_sw128(sKV + c * L::KV_CHUNK, 16, 1024);
-            const uint64_t b0 = b00 + (uint64_t)((c * L::Q_CHUNK) >> 4);
+  if (warp == 0 || warp == 14) {
+    // ============ S^T issuers (the whole warp, one elected lane issues), half the channel chunks each ============
+    constexpr uint32_t kIdS = idesc_bf16(kTileF, NH, false, false);  // A = KV (K-major), B = Q (K-major)
+    constexpr int NCH_A = (NCH + 1) / 2;
+    const int part = (warp == 0) ? 0 : 1;
+    const int c0 = part ? NCH_A : 0, c1 = part ? NCH : NCH_A;
+    for (int i = 0; i < ntiles; ++i) {
+      const int sl = i % R;
+      // S^T buffer i & 1 was last read by the softmax of tile i - 2, which then published P(i - 2)
+      if (i >= 2 && !warp_all(mbar_wait(bar_p + 8 * (i & 1), ((i - 2) >> 1) & 1, s_abort, err, wait_limit))) break;
+      if (!warp_all(mbar_wait(bar_kv + 8 * sl, (i / R) & 1, s_abort, err, wait_limit))) break;
+      fence_proxy_async_smem();
+      tc_fence_after();
+      const uint32_t tSb = tS + 32 * (i & 1) + 16 * part;
+      const uint64_t b00 = sdesc_sw128(sQ, 16, 1024);
+#pragma unroll 1
+      for (int c = c0; c < c1; ++c) {
+        const uint64_t a0 = sdesc_sw128(sKV + sl * L::SLOT + c * L::KV_CHUNK, 16, 1024);
+        const uint64_t b0 = b00 + (uint64_t)((c * L::Q_CHUNK) >> 4);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ss_w(tS, a0 + (uint64_t)(k * 2), b0 + (uint64_t)(k * 2), kIdS, (c | k) != 0);
-          }
-        }
-        if (stop) break;
-        mma_commit_w(bar_s);
-        if (!warp_all(mbar_wait(bar_p, i & 1, s_abort, err, wait_limit))) break;
-        tc_fence_after();
-        const uint64_t va0 = sdesc_sw128(sKV, L::KV_CHUNK, 1024);
-        const uint64_t pb0 = sdesc_sw128(sP, 16, 1024);
-        constexpr uint64_t kPair = (2 * L::KV_CHUNK) >> 4;  // descriptor step between channel pairs
-        // channel pair by channel pair, with a commit after each, so that the next tile's rows of a
-        // pair are gathered while later pairs are multiplied
-#pragma unroll
-        for (int m = 0; m < kDv / 128; ++m) {
-#pragma unroll
-          for (int k = 0; k < kTileF / 16; ++k)  // + 16 key rows: + 2048 B in V^T, + 32 B along P's rows
-            mma_ss_w(tO + m * 2 * NH, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 2), kIdPV,
-                     (i > 0 || k > 0) ? 1u : 0u);
-          if (m < 3) mma_commit_w(bar_pvm + 8 * m);
-        }
-        mma_commit_w(bar_pv);
+        for (int k = 0; k < 4; ++k)
+          mma_ss_w(tSb, a0 + (uint64_t)(k * 2), b0 + (uint64_t)(k * 2), kIdS, (c != c0 || k != 0) ? 1u : 0u);
       }
-      mma_commit_w(bar_fin);
-      volatile int dummy = 0;
-      mbar_wait(bar_fin, 0, &dummy, err);
+      mma_commit_w(bar_s + 8 * (i & 1));
     }
+    mma_commit_w(bar_fin + 8 * (1 + part));
+    volatile int dummy = 0;
+    mbar_wait(bar_fin + 8 * (1 + part), 0, &dummy, err);
     __syncwarp();
+  } else if (warp == 13) {
+    // ======================= P.V issuer: O^T += V^T [P_hi | P_lo] per tile =======================
+    constexpr uint32_t kIdPV = idesc_bf16(128, 2 * NH, true, false);  // A = V^T (MN-major), B = [P_hi|P_lo]
+    for (int i = 0; i < ntiles; ++i) {
+      if (!warp_all(mbar_wait(bar_p + 8 * (i & 1), (i >> 1) & 1, s_abort, err, wait_limit))) break;
+      tc_fence_after();
+      const uint64_t va0 = sdesc_sw128(sKV + (i % R) * L::SLOT, L::KV_CHUNK, 1024);
+      const uint64_t pb0 = sdesc_sw128(sP + (i & 1) * L::P_BLOCK, 16, 1024);
+      constexpr uint64_t kPair = (2 * L::KV_CHUNK) >> 4;  // descriptor step between channel pairs
+#pragma unroll
+      for (int m = 0; m < kDv / 128; ++m)
+#pragma unroll
+        for (int k = 0; k < kTileF / 16; ++k)
+          mma_ss_w(tO + m * 2 * NH, va0 + m * kPair + (uint64_t)(k * 128), pb0 + (uint64_t)(k * 2), kIdPV,
+                   (i > 0 || k > 0) ? 1u : 0u);
+      mma_commit_w(bar_pv + 8 * (i % R));  // the slot and P buffer i & 1 are free
+    }
+    mma_commit_w(bar_fin);
+    volatile int dummy = 0;
+    mbar_wait(bar_fin, 0, &dummy, err);
+    __syncwarp();
+  } else if (!worker) {
+    // ======================= gather warps (9-12): the ring's slots, a tile at a time =======================
+    const int gt = threadIdx.x - 32 - kWorkers;  // 0..kRingGather-1
+    const int uc = gt & 7;
+    constexpr int kRowStep = kRingGather / 8;
+    auto load_raw = [&](int i, int (&raw)[kRingRows]) {
+#pragma unroll
+      for (int e = 0; e < kRingRows; ++e) {
+        const int j = i * kTileF + (gt >> 3) + kRowStep * e;
+        raw[e] = (j < n_eff) ? __ldg(idx_row + j) : -1;
+      }
+    };
+    int raw[kRingRows];
+#pragma unroll
+    for (int e = 0; e < kRingRows; ++e) raw[e] = -1;
+    if (ntiles > 0) load_raw(0, raw);
+    for (int i = 0; i < ntiles; ++i) {
+      const int sl = i % R;
+      int rix[kRingRows];
+#pragma unroll
+      for (int e = 0; e < kRingRows; ++e) {
+        rix[e] = (raw[e] >= 0 && raw[e] < Tk) ? raw[e] : -1;
+        if (raw[e] < -1 || raw[e] >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
+      }
+      if (i + 1 < ntiles) load_raw(i + 1, raw);
+      // the slot's previous tile (i - R) has been multiplied: P.V done (its S^T came before)
+      if (i >= R && !mbar_wait(bar_pv + 8 * sl, ((i - R) / R) & 1, s_abort, err, wait_limit)) break;
+      const uint32_t dst = sKV + sl * L::SLOT;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c)
+#pragma unroll
+        for (int e = 0; e < kRingRows; ++e) {
+          const int r = (gt >> 3) + kRowStep * e;
+          const bool ok = rix[e] >= 0;
+          cp_async16(dst + c * L::KV_CHUNK + sw128_off(r, uc), kv + (ok ? (size_t)rix[e] * DQK + c * 64 + uc * 8 : 0),
+                     ok ? 16u : 0u);
+        }
+      cp_async_arrive(bar_kv + 8 * sl);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
   } else {
-    // ======================= gather + softmax + epilogue =======================
+    // ======================= softmax + epilogue =======================
     const int wk = warp - 1;       // 0..7
     const int qd = warp & 3;       // TMEM lane quadrant this warp may access
     const int ch = wk >> 2;        // head half: heads ch*NHH .. ch*NHH+NHH-1
     const bool has_key = lane < 16;
     const int r = qd * 16 + lane;  // key row of the tile (lanes 0..15)
     const int bar_id = 1 + ch;     // named barrier of the 128 threads of this half
-    auto load_raw = [&](int i, int (&raw)[2]) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int j = i * kTileF + (tid >> 3) + 32 * e;
-        raw[e] = (j < n_eff) ? __ldg(idx_row + j) : -1;
-      }
-    };
-    auto check_rows = [&](const int (&raw)[2], int (&rix)[2]) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int ix = raw[e];
-        rix[e] = (ix >= 0 && ix < Tk) ? ix : -1;
-        if (ix < -1 || ix >= Tk) record_error(err, DSA_ERR_DEVICE_INDEX);
-      }
-    };
-    int nraw[2];
-    if (ntiles > 0) {
-      int rix[2];
-      load_raw(0, nraw);
-      check_rows(nraw, rix);
-      for (int c = 0; c < NCH; ++c) gather_chunk64<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, bar_kv + 8 * c);
-    }
     const float* m_run = s_stat + ch * NHH;
     float l_part[NHH];
 #pragma unroll
     for (int h = 0; h < NHH; ++h) l_part[h] = 0.f;
     bool aborted = false;
+    int ixw_next = (ntiles > 0 && has_key && r < n_eff) ? __ldg(idx_row + r) : -1;
     for (int i = 0; i < ntiles; ++i) {
-      const int j = i * kTileF + r;
-      const int ixw = (has_key && j < n_eff) ? __ldg(idx_row + j) : -1;
-      const bool more = i + 1 < ntiles;
-      if (more) load_raw(i + 1, nraw);
-      const bool got = mbar_wait(bar_s, i & 1, s_abort, err, wait_limit);
+      const int ixw = ixw_next;
+      {
+        const int jn = (i + 1) * kTileF + r;
+        ixw_next = (i + 1 < ntiles && has_key && jn < n_eff) ? __ldg(idx_row + jn) : -1;
+      }
+      const bool got = mbar_wait(bar_s + 8 * (i & 1), (i >> 1) & 1, s_abort, err, wait_limit);
       if (named_bar_or(bar_id, 128, !got)) { aborted = true; break; }
       tc_fence_after();
-      // S^T of the tile is read: the next tile's RoPE rows may be gathered now (P has its own slot)
-      int rix[2];
-      if (more) {
-        check_rows(nraw, rix);
-        if (NCH == 9) gather_chunk64<DQK>(sKV + 8 * L::KV_CHUNK, kv, 8, tid, rix, bar_kv + 8 * 8);
+      uint32_t sv[NHH], sw[NHH];  // the two partial sums of S^T
+      if constexpr (NHH == 8) {
+        tmem_ld8(tmem_addr(tS + 32 * (i & 1) + ch * NHH, qd * 32, 0), sv);
+        tmem_ld8(tmem_addr(tS + 32 * (i & 1) + 16 + ch * NHH, qd * 32, 0), sw);
+      } else {
+        tmem_ld16(tmem_addr(tS + 32 * (i & 1) + ch * NHH, qd * 32, 0), sv);
+        tmem_ld16(tmem_addr(tS + 32 * (i & 1) + 16 + ch * NHH, qd * 32, 0), sw);
       }
-      uint32_t sv[NHH];
-      if constexpr (NHH == 8) tmem_ld8(tmem_addr(tS + ch * NHH, qd * 32, 0), sv);
-      else tmem_ld16(tmem_addr(tS + ch * NHH, qd * 32, 0), sv);
       tmem_ld_wait();
       const bool valid = has_key && ixw >= 0 && ixw < Tk;  // lanes 16..31 hold no key
       float z[NHH];
 #pragma unroll
-      for (int h = 0; h < NHH; ++h) z[h] = valid ? __uint_as_float(sv[h]) * sl2e : -INFINITY;
+      for (int h = 0; h < NHH; ++h) z[h] = valid ? (__uint_as_float(sv[h]) + __uint_as_float(sw[h])) * sl2e : -INFINITY;
       bool need = (i == 0);
       if (!need) {
         bool mine = false;
@@ -945,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         float v[NHH];
 #pragma unroll
         for (int h = 0; h < NHH; ++h) v[h] = z[h];
-        const float wmax = warp_transpose_reduce_n<NHH, true>(v, lane);  // head lane % NHH of this warp's keys
+        const float wmax = warp_transpose_reduce_n<NHH, true>(v, lane);
         if (lane < NHH) s_red[qd * NH + ch * NHH + lane] = wmax;
         named_bar(bar_id, 128);
         const int hl = lane % NHH;
@@ -966,27 +985,36 @@ __global__ void __launch_bounds__(kThreads, 2)
           any |= (i > 0) && (alpha[h] != 1.f);
           l_part[h] *= alpha[h];
         }
+        bool okw = true;
         if (any) {
-          // [O_hi^T | O_lo^T] is complete for the previous tile (bar_s of this tile follows those MMAs)
+          // O holds the products through tile i - 1 once P.V(i - 1) is done
+          okw = mbar_wait(bar_pv + 8 * ((i - 1) % R), ((i - 1) / R) & 1, s_abort, err, wait_limit);
+          if (okw) {
+            tc_fence_after();
 #pragma unroll 1
-          for (int mt = 0; mt < kDv / 128; ++mt) {
+            for (int mt = 0; mt < kDv / 128; ++mt) {
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-              const uint32_t ta = tmem_addr(tO + mt * 2 * NH + part * NH + ch * NHH, qd * 32, 0);
-              uint32_t ov[NHH];
-              if constexpr (NHH == 8) tmem_ld8(ta, ov);
-              else tmem_ld16(ta, ov);
-              tmem_ld_wait();
+              for (int part = 0; part < 2; ++part) {
+                const uint32_t ta = tmem_addr(tO + mt * 2 * NH + part * NH + ch * NHH, qd * 32, 0);
+                uint32_t ov[NHH];
+                if constexpr (NHH == 8) tmem_ld8(ta, ov);
+                else tmem_ld16(ta, ov);
+                tmem_ld_wait();
 #pragma unroll
-              for (int h = 0; h < NHH; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
-              if constexpr (NHH == 8) tmem_st8(ta, ov);
-              else tmem_st16(ta, ov);
+                for (int h = 0; h < NHH; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+                if constexpr (NHH == 8) tmem_st8(ta, ov);
+                else tmem_st16(ta, ov);
+              }
             }
+            tmem_st_wait();
           }
-          tmem_st_wait();
         }
+        if (named_bar_or(bar_id, 128, !okw)) { aborted = true; break; }
       }
-      // P_hi into rows ch*NHH.., P_lo into rows NH + ch*NHH.. of the [hi | lo] operand, key r along K
+      // P buffer i & 1 was last read by P.V(i - 2)
+      const bool okp = (i < 2) || mbar_wait(bar_pv + 8 * ((i - 2) % R), ((i - 2) / R) & 1, s_abort, err, wait_limit);
+      if (named_bar_or(bar_id, 128, !okp)) { aborted = true; break; }
+      const uint32_t sPb = sP + (i & 1) * L::P_BLOCK;
 #pragma unroll
       for (int h = 0; h < NHH; ++h) {
         const float mh = m_run[h];
@@ -997,34 +1025,20 @@ __global__ void __launch_bounds__(kThreads, 2)
           const __nv_bfloat16 hi = __float2bfloat16_rn(p);
           const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
           const int n = ch * NHH + h;
-          st_shared_u16(sP + p_off<NH>(n, r), __bfloat16_as_ushort(hi));
-          st_shared_u16(sP + p_off<NH>(NH + n, r), __bfloat16_as_ushort(lo));
+          st_shared_u16(sPb + p_off<NH>(n, r), __bfloat16_as_ushort(hi));
+          st_shared_u16(sPb + p_off<NH>(NH + n, r), __bfloat16_as_ushort(lo));
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p);
-      // the next tile's value chunks, channel pair m as soon as P.V has read it
-      if (more) {
-        for (int m = 0; m < kDv / 128 && !aborted; ++m) {
-          if (!mbar_wait(m < 3 ? bar_pvm + 8 * m : bar_pv, i & 1, s_abort, err, wait_limit)) {
-            aborted = true;
-            break;
-          }
-#pragma unroll
-          for (int c = 2 * m; c < 2 * m + 2; ++c)
-            gather_chunk64<DQK>(sKV + c * L::KV_CHUNK, kv, c, tid, rix, bar_kv + 8 * c);
-        }
-        if (named_bar_or(bar_id, 128, aborted)) { aborted = true; break; }
-      }
+      if (lane == 0) mbar_arrive(bar_p + 8 * (i & 1));
     }
     if (!aborted && ntiles > 0) {
-      const bool got = mbar_wait(bar_pv, (ntiles - 1) & 1, s_abort, err, wait_limit);
+      const bool got = mbar_wait(bar_pv + 8 * ((ntiles - 1) % R), ((ntiles - 1) / R) & 1, s_abort, err, wait_limit);
       aborted = named_bar_or(bar_id, 128, !got);
       tc_fence_after();
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
     // ---- epilogue: l per head, lse, out = (O_hi + O_lo)^T / l ----
     const float lsum = warp_transpose_reduce_n<NHH, false>(l_part, lane);
     named_bar(bar_id, 128);
@@ -1033,11 +1047,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (qd == 0 && lane < NHH) {
       const int hh = ch * NHH + lane;
       const float mh = s_stat[hh];
-      const int hl = hg * NH + hh;
-      const float s2 = (sink != nullptr && hl < H) ? __ldg(sink + hl) * 1.4426950408889634f : -INFINITY;
+      const float s2 = (sink != nullptr && hh < H) ? __ldg(sink + hh) * 1.4426950408889634f : -INFINITY;
       const float lsink = (s2 > -INFINITY) ? exp2f(s2 - mh) : 0.f;
       const float lt = s_red[hh] + s_red[NH + hh] + s_red[2 * NH + hh] + s_red[3 * NH + hh] + lsink;
-      if (hl < H) lse[(size_t)t * H + hl] = (lt > 0.f) ? (mh * 0.69314718055994531f + logf(lt)) : -INFINITY;
+      if (hh < H) lse[(size_t)t * H + hh] = (lt > 0.f) ? (mh * 0.69314718055994531f + logf(lt)) : -INFINITY;
       s_lsum[hh] = lt;
     }
     named_bar(bar_id, 128);
@@ -1047,6 +1060,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float l = s_lsum[ch * NHH + h];
       inv[h] = (l > 0.f) ? 1.f / l : 0.f;
     }
+    // staging in slot 0 of the ring: every product is done, and no gather is in flight (every tile's
+    // copies landed before its S^T)
     uint8_t* stage = smem + L::OFF_KV;
     uint8_t* stage_lo = stage + NH * kDv * 2;
 #pragma unroll 1
@@ -1077,8 +1092,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
     named_bar(3, kWorkers);
-    const int hcount = min(NH, H - hg * NH);
-    const size_t gbase = ((size_t)t * H + hg * NH) * kDv;
+    const int hcount = min(NH, H);
+    const size_t gbase = (size_t)t * H * kDv;
     const uint64_t pol = l2_evict_first_policy();
     for (int u = tid; u < hcount * (kDv / 8); u += kWorkers) {
       stg16_hint(reinterpret_cast<uint4*>(out + gbase) + u, reinterpret_cast<const uint4*>(stage)[u], pol);
@@ -1099,17 +1114,17 @@ dsa_status_t launch(const void* kv, const void* q, const int32_t* idx, const int
                     int K, float scale, const float* sink, void* out, void* out_lo, float* lse, int* err,
                     cudaStream_t s) {
   const float sl2e = scale * 1.4426950408889634f;
-  if (H <= 16) {  // few heads: 16 per CTA on the MMA's N side
+  if (H <= 16) {  // few heads: 16 per CTA on the MMA's N side, one CTA per SM
     constexpr int NH = 16;
-    using F = SmemFew<DQK, NH>;
-    dsa_status_t st = configure_kernel_smem(reinterpret_cast<const void*>(sparse_mla_fwd_few_kernel<DQK, NH>),
-                                            F::TOTAL, "configuring sparse_mla_fwd_few_kernel");
+    using F = SmemRing<DQK, NH>;
+    dsa_status_t st = configure_kernel_smem(reinterpret_cast<const void*>(sparse_mla_fwd_ring_kernel<DQK, NH>),
+                                            F::TOTAL, "configuring sparse_mla_fwd_ring_kernel");
     if (st != DSA_OK) return st;
-    sparse_mla_fwd_few_kernel<DQK, NH><<<dim3(T, 1), kThreads, F::TOTAL, s>>>(
+    sparse_mla_fwd_ring_kernel<DQK, NH><<<dim3(T, 1), kRingThreads, F::TOTAL, s>>>(
         reinterpret_cast<const __nv_bfloat16*>(kv), reinterpret_cast<const __nv_bfloat16*>(q), idx, len, T, Tk, H,
         K, sl2e, sink, reinterpret_cast<__nv_bfloat16*>(out), reinterpret_cast<__nv_bfloat16*>(out_lo), lse, err,
         wait_limit_cycles());
-    return cuda_check(cudaGetLastError(), "launching sparse_mla_fwd_few_kernel");
+    return cuda_check(cudaGetLastError(), "launching sparse_mla_fwd_ring_kernel");
   }
   using L = Smem<DQK>;
   dsa_status_t st = configure_kernel_smem(reinterpret_cast<const void*>(sparse_mla_fwd_kernel<DQK>), L::TOTAL,
