@@ -305,15 +305,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (worker && ntiles > 0) start_pass();
   for (int i = 0; warp <= 4 && i < ntiles; ++i) {  // workers and the MMA warp; the drain warps wait below
     const int ix = ixa;
-    if (worker) {
-      const bool more = i + 1 < ntiles;
-      if (more) gather_rows(i + 1);  // buffer (i + 1) & 1 was last read by tile i - 1's finished MMAs
-      landed(more);
-    }
+    if (worker) landed(false);  // tile i, gathered a tile ago (the only copies in flight)
     if (named_bar_or(1, kPass1, false)) { aborted = true; break; }  // the tile has landed
     if (warp == 4) issue_s(i);  // the whole warp, one elected lane issues
     bool ok = true;
     if (worker) {
+      // the next tile's rows while S of this one is formed: buffer (i + 1) & 1 was last read by the S
+      // product of tile i - 1, which was read before the end-of-tile barrier of tile i - 1
+      if (i + 1 < ntiles) gather_rows(i + 1);
       ok = mbar_wait(bar_s, ph_s, s_abort, err, wait_limit);
       if (ok) {
         tc_fence_after();
@@ -382,14 +381,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < ntiles; ++i) {
       const int ix = ixa;
       const bool more = i + 1 < ntiles;
+      // tile i (gathered a tile ago, the only copies in flight) has landed: S of it may be formed
+      // right after the products of tile i - 1, while this warp issues the next gather
+      landed(false);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_land);
       // the products of tile i - 1 are done: K buffer (i + 1) & 1 and the M tiles are free
       if (i >= 1 && !bad) bad = !mbar_wait(bar_mm, (i - 1) & 1, s_abort, err, wait_limit);
       // every worker's key table entry for tile i + 1 is written (end of tile i - 1)
       if (named_bar_or(2, kWorkers, bad)) { aborted = true; break; }
       if (more) gather_rows(i + 1);
-      landed(more);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_land);
       const bool ok = mbar_wait(bar_s, ph_s ^ (uint32_t)(i & 1), s_abort, err, wait_limit);
       if (ok) {
         tc_fence_after();
@@ -820,18 +821,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t g = g0 + i;
           const int ix = ixa;
           const bool more = i + 1 < nt;
+          // tile g (gathered a tile ago, the only copies in flight) has landed: S of it may be formed
+          // right after the products of tile g - 1, while this warp issues the next gather
+          asm volatile("cp.async.wait_group 0;" ::: "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_land);
           // the products of tile g - 1 are done: K buffer (g + 1) & 1 and the M tiles are free (at a
           // row's first tile the previous row's end already waited for them)
           if (i >= 1 && !bad) bad = !mbar_wait(bar_mm, (g - 1) & 1, s_abort, err, wait_limit);
           if (named_bar_or(2, kWorkers, bad)) { aborted = true; break; }
           if (more) gather_rows(g + 1);
-          if (more)
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-          else
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_land);
           const bool ok = mbar_wait(bar_s, g & 1, s_abort, err, wait_limit);
           if (ok) {
             tc_fence_after();
