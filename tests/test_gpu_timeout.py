@@ -66,3 +66,36 @@ def test_wait_limit_expiry_is_reported_and_the_next_call_is_clean(zero_wait_limi
     assert_close(dq.cpu(), ref_dq, "dq")
     assert_close(dkv.cpu(), ref_dkv, "dkv")
 
+
+
+def test_wait_limit_expiry_in_the_few_heads_forward_and_the_kl_kernels(zero_wait_limit):
+    # The few-heads forward (its gather, S^T and P.V warps) and both KL kernels (forming the slots'
+    # scores, and reading them with one CTA per SM walking the rows): each reports DSA_ERR_TIMEOUT with
+    # a zero limit, and the same calls with the default limit match the oracle.
+    from test_gpu_kl import _slot_scores_fp32, check_kl, kl_inputs
+    q, kv, dout, idx = make_case(12, 600, 8, 512, 400, 53)  # 7 tiles of 64 keys: the ring turns over
+    q_idx, k_idx, w, kidx, prob, _ = kl_inputs(200, 900, 300, 64, 78)  # 200 rows: several per CTA
+    sc = _slot_scores_fp32(q_idx, k_idx, w, kidx)
+
+    def fwd():
+        ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
+        out, lse = dsa.dsa_sparse_mla_fwd(q.to(DEV), kv.to(DEV), idx.to(DEV), 0.1, workspace=ws)
+        return dsa.dsa_read_device_status(ws), out, lse
+
+    def kl(score):
+        ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
+        dsa.dsa_indexer_kl(q_idx.to(DEV), k_idx.to(DEV), w.to(DEV), kidx.to(DEV), prob.to(DEV), 1.0, workspace=ws,
+                           topk_score=None if score is None else score.to(DEV))
+        return dsa.dsa_read_device_status(ws)
+
+    assert fwd()[0] == DSA_ERR_TIMEOUT
+    assert kl(None) == DSA_ERR_TIMEOUT
+    assert kl(sc) == DSA_ERR_TIMEOUT
+    dsa.dsa_set_wait_limit_cycles(-1)
+    status, out, lse = fwd()
+    assert status == 0
+    ref_o, ref_l = oracle.sparse_mla_fwd(q, kv, idx, 0.1)
+    assert_close(out.cpu(), ref_o, "out")
+    assert_lse(lse.cpu(), ref_l)
+    check_kl(q_idx, k_idx, w, kidx, prob)
+    check_kl(q_idx, k_idx, w, kidx, prob, topk_score=sc)
