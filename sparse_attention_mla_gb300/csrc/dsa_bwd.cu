@@ -207,7 +207,9 @@ __device__ __forceinline__ void reduce_rows64(const uint32_t (&v)[4][16], uint32
 // Drain warps of a quadrant: the flush warp (role 0) and the two math warps
 // (roles 1, 2 = head halves).  The flush warp drains the first half (64
 // channels) of every dKV group; the second halves alternate between the math
-// warps, which also run the softmax on the critical path.
+// warps, which also run the softmax on the critical path.  (When the upper
+// head half is all padding its math warp runs no softmax; giving it more of
+// the second halves was measured slower than the alternation.)
 __device__ __forceinline__ int drain_role(int g, int hf) { return hf == 0 ? 0 : 1 + (g & 1); }
 
 // One thread's share of gathering a tile's rows, 64 channels at a time, with
@@ -426,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // A drain warp's part of staged dKV group G (group g of its tile): wait for it (every drain warp
   // waits for every group, in order, so that each slot barrier is read phase by phase), load the
   // half this warp owns if any, release the slot, then reduce it into dkv.
+  const bool pad_hi = hg * kHeads + 32 >= H;  // heads 32..63 of this CTA are all padding
   auto drain_group = [&](int G, int g, int role, int ix, uint32_t fst) -> bool {
     const int s = G & (kStage - 1);
     if (!mbar_wait(bar(B_STF + s), (G / kStage) & 1, s_abort, err, wait_limit)) return false;
@@ -643,6 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* lse2 = s_lse2 + ch * 32;
     const float* dl = s_dl + ch * 32;
     const uint32_t fst_m = smem_u32(smem + L::OFF_FST + (4 + mw) * 2048);  // this warp's transpose buffer
+    const bool pad_half = ch == 1 && pad_hi;  // every head of this half is padding
     bool aborted = false;
     for (int i = 0; i < ntiles; ++i) {
       const int b = i & 1;
@@ -653,11 +657,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tS = tmem_addr(tmem + C_BUF * b + ch * 32, qd * 32, 0);
       const uint32_t tP = tS + 64;
+      const bool valid = ix >= 0 && ix < Tk;
+      if (pad_half) {
+        // heads of zero q and dO rows only: S^T and dP^T are exact zeros, whose fp32 bits are also the
+        // bf16 hi + lo zeros the dKV products read, and dq of these heads is not stored
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_DS + b));
+        const int kix = valid ? ix : -1;
+        for (int g = 0; g < NG && !aborted; ++g)
+          if (!drain_group(i * NG + g, g, 1 + ch, kix, fst_m)) aborted = true;
+        if (aborted) break;
+        continue;
+      }
       uint32_t sv[32], dv[32];
       tmem_ld32(tS, sv);
       tmem_ld32(tP, dv);
       tmem_ld_wait();
-      const bool valid = ix >= 0 && ix < Tk;
       uint32_t ph[16], pl[16], sh[16], sl[16];
       float psum = 0.f;  // this half's sum of P over its 32 heads (the slot probability, on request)
 #pragma unroll
