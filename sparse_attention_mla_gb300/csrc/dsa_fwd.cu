@@ -938,7 +938,10 @@ __global__ void __launch_bounds__(kRingThreads, 1)
         ixw_next = (i + 1 < ntiles && has_key && jn < n_eff) ? __ldg(idx_row + jn) : -1;
       }
       const bool got = mbar_wait(bar_s + 8 * (i & 1), (i >> 1) & 1, s_abort, err, wait_limit);
-      if (named_bar_or(bar_id, 128, !got)) { aborted = true; break; }
+      // P buffer i & 1 was last read by P.V(i - 2), long done: waited here, so that the one barrier below
+      // also covers it
+      const bool okp = (i < 2) || mbar_wait(bar_pv + 8 * ((i - 2) % R), ((i - 2) / R) & 1, s_abort, err, wait_limit);
+      const bool bad = !got || !okp;  // (TMEM is still read below: a stale value is harmless, the tile is dropped)
       tc_fence_after();
       uint32_t sv[NHH], sw[NHH];  // the two partial sums of S^T
       if constexpr (NHH == 8) {
@@ -953,12 +956,17 @@ __global__ void __launch_bounds__(kRingThreads, 1)
       float z[NHH];
 #pragma unroll
       for (int h = 0; h < NHH; ++h) z[h] = valid ? (__uint_as_float(sv[h]) + __uint_as_float(sw[h])) * sl2e : -INFINITY;
-      bool need = (i == 0);
-      if (!need) {
-        bool mine = false;
+      bool mine = (i == 0);  // the first tile always sets the running max
+      if (!mine) {
 #pragma unroll
         for (int h = 0; h < NHH; ++h) mine |= z[h] > m_run[h] + kRescaleThreshold;
-        need = named_bar_or(bar_id, 128, mine);
+      }
+      // one barrier of the half per tile in the common case; a rescale, the first tile or an abort takes a
+      // second one to tell them apart (every thread of the half leaves together, or none does)
+      bool need = false;
+      if (named_bar_or(bar_id, 128, mine || bad)) {
+        if (named_bar_or(bar_id, 128, bad)) { aborted = true; break; }
+        need = true;
       }
       if (need) {
         float v[NHH];
@@ -1011,9 +1019,6 @@ __global__ void __launch_bounds__(kRingThreads, 1)
         }
         if (named_bar_or(bar_id, 128, !okw)) { aborted = true; break; }
       }
-      // P buffer i & 1 was last read by P.V(i - 2)
-      const bool okp = (i < 2) || mbar_wait(bar_pv + 8 * ((i - 2) % R), ((i - 2) / R) & 1, s_abort, err, wait_limit);
-      if (named_bar_or(bar_id, 128, !okp)) { aborted = true; break; }
       const uint32_t sPb = sP + (i & 1) * L::P_BLOCK;
 #pragma unroll
       for (int h = 0; h < NHH; ++h) {
