@@ -410,22 +410,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool more = i + 1 < ntiles;
       if (more) load_raw(i + 1, nraw);
       const bool got = mbar_wait(bar_s, i & 1, s_abort, err, wait_limit);
-      // every thread of the half leaves together, or none does (named barriers follow)
-      if (named_bar_or(bar_id, 128, !got)) { aborted = true; break; }
       tc_fence_after();
       uint32_t sv[32];
-      tmem_ld32(tmem_addr(tS, qd * 32, ch * 32), sv);
+      tmem_ld32(tmem_addr(tS, qd * 32, ch * 32), sv);  // (after a failed wait a stale value is harmless)
       tmem_ld_wait();
       const bool valid = ixw >= 0 && ixw < Tk;
-      bool need = (i == 0);
-      if (!need) {
+      bool mine = (i == 0);  // the first tile always sets the running max
+      if (!mine) {
         // Does any score of this key exceed its head's running max by the threshold?  First against
         // the smallest running max of the half (this key's largest score, one compare), per head only
         // when that test fails.
         float smax = __uint_as_float(sv[0]);
 #pragma unroll
         for (int h = 1; h < 32; ++h) smax = fmaxf(smax, __uint_as_float(sv[h]));
-        bool mine = valid && smax * sl2e > s_mmin[ch] + kRescaleThreshold;
+        mine = valid && smax * sl2e > s_mmin[ch] + kRescaleThreshold;
         if (mine) {
           mine = false;
 #pragma unroll
@@ -437,7 +435,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     (__uint_as_float(sv[4 * h4 + 3]) * sl2e > m4.w + kRescaleThreshold);
           }
         }
-        need = named_bar_or(bar_id, 128, mine);
+      }
+      // one barrier of the half per tile in the common case; a rescale, the first tile or an abort takes a
+      // second one to tell them apart (every thread of the half leaves together, or none does)
+      bool need = false;
+      if (named_bar_or(bar_id, 128, mine || !got)) {
+        if (named_bar_or(bar_id, 128, !got)) { aborted = true; break; }
+        need = true;
       }
       if (need) {
         float v[32];
