@@ -694,6 +694,14 @@ __device__ __forceinline__ float warp_transpose_reduce_n(float (&v)[N], int lane
   return v[0];
 }
 
+// 16 TMEM lanes x 64 bits, 4 times (the 16x64b shape): thread t of the warp gets lane base + (t >> 2) +
+// 8 (t & 1) and the columns c + 2j + ((t >> 1) & 1), j = 0..3, of the address (lane base, c).
+__device__ __forceinline__ void tmem_ld16x64b_x4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x64b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+
 // ---------------------------------------------------------------------------
 // Few heads (H <= 16): the same computation with NH = 16 heads per CTA on the
 // MMA's N side instead of 64 (so that H = 8 does not multiply 56 zero heads)
@@ -708,7 +716,9 @@ __device__ __forceinline__ float warp_transpose_reduce_n(float (&v)[N], int lane
 // ahead of the softmax; P is double-buffered in shared memory.  A rescale of O
 // at tile i waits for P.V(i - 1) explicitly.
 //  * S^T of a tile is an M = 64 MMA: key row 16q + i lands in TMEM lane 32q + i
-//    (i < 16) of lane quadrant q; the softmax threads of lanes 16..31 hold no key.
+//    (i < 16) of lane quadrant q.  The softmax reads it with the 16x64b shape,
+//    which spreads those 16 lanes over all 32 threads of the warp (two threads
+//    per key, alternate columns): each thread takes one key and 4 heads.
 //  * P^T is split into bf16 hi + lo, both halves side by side in one K-major
 //    operand of 2 NH rows ([hi heads | lo heads], 64 keys along K), so one P.V
 //    MMA (N = 2 NH, M = 128 channels) forms O_hi and O_lo together; the
@@ -926,20 +936,32 @@ __global__ void __launch_bounds__(kRingThreads, 1)
     const int wk = warp - 1;       // 0..7
     const int qd = warp & 3;       // TMEM lane quadrant this warp may access
     const int ch = wk >> 2;        // head half: heads ch*NHH .. ch*NHH+NHH-1
-    const bool has_key = lane < 16;
-    const int r = qd * 16 + lane;  // key row of the tile (lanes 0..15)
+    // S^T's 16 keys of the quadrant over all 32 threads (16x64b loads): this thread's key row and its
+    // NQ heads ch*NHH + par + 2j
+    constexpr int NQ = NHH / 2;
+    const int par = (lane >> 1) & 1;
+    const int r = qd * 16 + (lane >> 2) + 8 * (lane & 1);  // key row of the tile
     const int bar_id = 1 + ch;     // named barrier of the 128 threads of this half
-    const float* m_run = s_stat + ch * NHH;
-    float l_part[NHH];
+    float l_part[NQ];
 #pragma unroll
-    for (int h = 0; h < NHH; ++h) l_part[h] = 0.f;
+    for (int j = 0; j < NQ; ++j) l_part[j] = 0.f;
+    // per-head reduction over the warp's 16 keys: the lanes of one column parity hold the same heads
+    auto reduce_keys = [&](float v, bool is_max) -> float {
+#pragma unroll
+      for (int o = 1; o <= 16; o <<= 1) {
+        if (o == 2) continue;
+        const float x = __shfl_xor_sync(0xffffffffu, v, o);
+        v = is_max ? fmaxf(v, x) : v + x;
+      }
+      return v;
+    };
     bool aborted = false;
-    int ixw_next = (ntiles > 0 && has_key && r < n_eff) ? __ldg(idx_row + r) : -1;
+    int ixw_next = (ntiles > 0 && r < n_eff) ? __ldg(idx_row + r) : -1;
     for (int i = 0; i < ntiles; ++i) {
       const int ixw = ixw_next;
       {
         const int jn = (i + 1) * kTileF + r;
-        ixw_next = (i + 1 < ntiles && has_key && jn < n_eff) ? __ldg(idx_row + jn) : -1;
+        ixw_next = (i + 1 < ntiles && jn < n_eff) ? __ldg(idx_row + jn) : -1;
       }
       const bool got = mbar_wait(bar_s + 8 * (i & 1), (i >> 1) & 1, s_abort, err, wait_limit);
       // P buffer i & 1 was last read by P.V(i - 2), long done: waited here, so that the one barrier below
@@ -947,23 +969,18 @@ __global__ void __launch_bounds__(kRingThreads, 1)
       const bool okp = (i < 2) || mbar_wait(bar_pv + 8 * ((i - 2) % R), ((i - 2) / R) & 1, s_abort, err, wait_limit);
       const bool bad = !got || !okp;  // (TMEM is still read below: a stale value is harmless, the tile is dropped)
       tc_fence_after();
-      uint32_t sv[NHH], sw[NHH];  // the two partial sums of S^T
-      if constexpr (NHH == 8) {
-        tmem_ld8(tmem_addr(tS + 32 * (i & 1) + ch * NHH, qd * 32, 0), sv);
-        tmem_ld8(tmem_addr(tS + 32 * (i & 1) + 16 + ch * NHH, qd * 32, 0), sw);
-      } else {
-        tmem_ld16(tmem_addr(tS + 32 * (i & 1) + ch * NHH, qd * 32, 0), sv);
-        tmem_ld16(tmem_addr(tS + 32 * (i & 1) + 16 + ch * NHH, qd * 32, 0), sw);
-      }
+      uint32_t sv[NQ], sw[NQ];  // the two partial sums of S^T
+      tmem_ld16x64b_x4(tmem_addr(tS + 32 * (i & 1) + ch * NHH, qd * 32, 0), sv);
+      tmem_ld16x64b_x4(tmem_addr(tS + 32 * (i & 1) + 16 + ch * NHH, qd * 32, 0), sw);
       tmem_ld_wait();
-      const bool valid = has_key && ixw >= 0 && ixw < Tk;  // lanes 16..31 hold no key
-      float z[NHH];
+      const bool valid = ixw >= 0 && ixw < Tk;
+      float z[NQ];
 #pragma unroll
-      for (int h = 0; h < NHH; ++h) z[h] = valid ? (__uint_as_float(sv[h]) + __uint_as_float(sw[h])) * sl2e : -INFINITY;
+      for (int j = 0; j < NQ; ++j) z[j] = valid ? (__uint_as_float(sv[j]) + __uint_as_float(sw[j])) * sl2e : -INFINITY;
       bool mine = (i == 0);  // the first tile always sets the running max
       if (!mine) {
 #pragma unroll
-        for (int h = 0; h < NHH; ++h) mine |= z[h] > m_run[h] + kRescaleThreshold;
+        for (int j = 0; j < NQ; ++j) mine |= z[j] > s_stat[ch * NHH + par + 2 * j] + kRescaleThreshold;
       }
       // one barrier of the half per tile in the common case; a rescale, the first tile or an abort takes a
       // second one to tell them apart (every thread of the half leaves together, or none does)
@@ -973,30 +990,31 @@ __global__ void __launch_bounds__(kRingThreads, 1)
         need = true;
       }
       if (need) {
-        float v[NHH];
 #pragma unroll
-        for (int h = 0; h < NHH; ++h) v[h] = z[h];
-        const float wmax = warp_transpose_reduce_n<NHH, true>(v, lane);
-        if (lane < NHH) s_red[qd * NH + ch * NHH + lane] = wmax;
+        for (int j = 0; j < NQ; ++j) {
+          const float wmax = reduce_keys(z[j], true);
+          if ((lane & ~2) == 0) s_red[qd * NH + ch * NHH + par + 2 * j] = wmax;
+        }
         named_bar(bar_id, 128);
-        const int hl = lane % NHH;
-        const float bm = fmaxf(fmaxf(s_red[ch * NHH + hl], s_red[NH + ch * NHH + hl]),
-                               fmaxf(s_red[2 * NH + ch * NHH + hl], s_red[3 * NH + ch * NHH + hl]));
-        const float mo_lane = s_stat[ch * NHH + hl];
-        const float mn = fmaxf(mo_lane, bm);
-        named_bar(bar_id, 128);
-        if (qd == 0 && lane < NHH) s_stat[ch * NHH + lane] = mn;
-        named_bar(bar_id, 128);
-        float alpha[NHH];
+        // old and new running max of every head of the half (all of them: O is rescaled per head below)
+        float mo[NHH], mn[NHH], alpha[NHH];
         bool any = false;
 #pragma unroll
         for (int h = 0; h < NHH; ++h) {
-          const float mo = __shfl_sync(0xffffffffu, mo_lane, h);
-          const float mnew = m_run[h];
-          alpha[h] = (mo == -INFINITY) ? 0.f : exp2f(mo - mnew);
+          const int hh = ch * NHH + h;
+          const float bm = fmaxf(fmaxf(s_red[hh], s_red[NH + hh]), fmaxf(s_red[2 * NH + hh], s_red[3 * NH + hh]));
+          mo[h] = s_stat[hh];
+          mn[h] = fmaxf(mo[h], bm);
+          alpha[h] = (mo[h] == -INFINITY) ? 0.f : exp2f(mo[h] - mn[h]);
           any |= (i > 0) && (alpha[h] != 1.f);
-          l_part[h] *= alpha[h];
         }
+        named_bar(bar_id, 128);
+        if (qd == 0 && lane == 0) {
+#pragma unroll
+          for (int h = 0; h < NHH; ++h) s_stat[ch * NHH + h] = mn[h];
+        }
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) l_part[j] *= par ? alpha[2 * j + 1] : alpha[2 * j];
         bool okw = true;
         if (any) {
           // O holds the products through tile i - 1 once P.V(i - 1) is done
@@ -1021,22 +1039,21 @@ __global__ void __launch_bounds__(kRingThreads, 1)
             tmem_st_wait();
           }
         }
+        // (also orders the s_stat update before every thread's reads below)
         if (named_bar_or(bar_id, 128, !okw)) { aborted = true; break; }
       }
       const uint32_t sPb = sP + (i & 1) * L::P_BLOCK;
 #pragma unroll
-      for (int h = 0; h < NHH; ++h) {
-        const float mh = m_run[h];
+      for (int j = 0; j < NQ; ++j) {
+        const int n = ch * NHH + par + 2 * j;
+        const float mh = s_stat[n];
         const float mu = (mh == -INFINITY) ? 0.f : mh;
-        const float p = exp2f(z[h] - mu);
-        l_part[h] += p;
-        if (has_key) {
-          const __nv_bfloat16 hi = __float2bfloat16_rn(p);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
-          const int n = ch * NHH + h;
-          st_shared_u16(sPb + p_off<NH>(n, r), __bfloat16_as_ushort(hi));
-          st_shared_u16(sPb + p_off<NH>(NH + n, r), __bfloat16_as_ushort(lo));
-        }
+        const float pv = exp2f(z[j] - mu);
+        l_part[j] += pv;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(pv - __bfloat162float(hi));
+        st_shared_u16(sPb + p_off<NH>(n, r), __bfloat16_as_ushort(hi));
+        st_shared_u16(sPb + p_off<NH>(NH + n, r), __bfloat16_as_ushort(lo));
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -1049,9 +1066,12 @@ __global__ void __launch_bounds__(kRingThreads, 1)
       tc_fence_after();
     }
     // ---- epilogue: l per head, lse, out = (O_hi + O_lo)^T / l ----
-    const float lsum = warp_transpose_reduce_n<NHH, false>(l_part, lane);
-    named_bar(bar_id, 128);
-    if (lane < NHH) s_red[qd * NH + ch * NHH + lane] = lsum;
+    named_bar(bar_id, 128);  // everyone is done reading s_red / s_stat of the loop
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+      const float lsum = reduce_keys(l_part[j], false);
+      if ((lane & ~2) == 0) s_red[qd * NH + ch * NHH + par + 2 * j] = lsum;
+    }
     named_bar(bar_id, 128);
     if (qd == 0 && lane < NHH) {
       const int hh = ch * NHH + lane;

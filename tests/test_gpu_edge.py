@@ -56,11 +56,11 @@ def test_topk_one(H):
     fwd_bwd_vs_oracle(q, kv, dout, idx, 192 ** -0.5)
 
 
-@pytest.mark.parametrize("H", [64, 8])  # the 64-head forward and the few-heads one (H <= 16)
-def test_growing_scores_rescale_running_max(H):
-    # kv rows scaled up with the key index, slots ascending: every new 128-slot tile raises the
-    # running max by far more than the lazy-rescale threshold, so O is rescaled tile after tile
-    q, kv, dout, idx = make_case(24, 700, H, 576, 600, 12)
+@pytest.mark.parametrize("H,D", [(64, 576), (8, 576), (8, 512)])  # 64-head forward; few heads, ring of 2 / 3 tiles
+def test_growing_scores_rescale_running_max(H, D):
+    # kv rows scaled up with the key index, slots ascending: every new tile raises the running max by
+    # far more than the lazy-rescale threshold, so O is rescaled tile after tile
+    q, kv, dout, idx = make_case(24, 700, H, D, 600, 12)
     ramp = (1.0 + torch.arange(kv.shape[0], dtype=torch.float32) / 120.0)[:, None]
     kv = (kv.float() * ramp).to(torch.bfloat16)
     fwd_bwd_vs_oracle(q, kv, dout, idx, 0.25, stress=True)
