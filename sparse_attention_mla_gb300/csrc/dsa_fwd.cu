@@ -60,6 +60,7 @@
 // lane issues each instruction) and owns TMEM; warps 1..8 run
 // the gather, the softmax and the epilogue.
 #include <cmath>
+#include <type_traits>
 
 #include "dsa_device.cuh"
 #include "dsa_host.h"
@@ -701,6 +702,38 @@ __device__ __forceinline__ void tmem_ld16x64b_x4(uint32_t taddr, uint32_t (&r)[4
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld16x64b_x2(uint32_t taddr, uint32_t (&r)[2]) {  // columns c + (t >> 1) & 1, + 2
+  asm volatile("tcgen05.ld.sync.aligned.16x64b.x2.b32 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
+}
+template <int N>
+__device__ __forceinline__ void tmem_ld16x64b(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 4) tmem_ld16x64b_x4(taddr, r);
+  else tmem_ld16x64b_x2(taddr, r);
+}
+// 32 lanes x 32 bits, 4 columns (32x32b.x4): thread i gets lane base + i, columns c .. c + 3
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+// NHH consecutive columns of the warp's 32 lanes (NHH = 4, 8 or 16)
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 4) tmem_ld4(taddr, r);
+  else if constexpr (N == 8) tmem_ld8(taddr, r);
+  else tmem_ld16(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]) {
+  if constexpr (N == 4) tmem_st4(taddr, r);
+  else if constexpr (N == 8) tmem_st8(taddr, r);
+  else tmem_st16(taddr, r);
+}
 
 // ---------------------------------------------------------------------------
 // Few heads (H <= 16): the same computation with NH = 16 heads per CTA on the
@@ -970,8 +1003,8 @@ __global__ void __launch_bounds__(kRingThreads, 1)
       const bool bad = !got || !okp;  // (TMEM is still read below: a stale value is harmless, the tile is dropped)
       tc_fence_after();
       uint32_t sv[NQ], sw[NQ];  // the two partial sums of S^T
-      tmem_ld16x64b_x4(tmem_addr(tS + 32 * (i & 1) + ch * NHH, qd * 32, 0), sv);
-      tmem_ld16x64b_x4(tmem_addr(tS + 32 * (i & 1) + 16 + ch * NHH, qd * 32, 0), sw);
+      tmem_ld16x64b<NQ>(tmem_addr(tS + 32 * (i & 1) + ch * NHH, qd * 32, 0), sv);
+      tmem_ld16x64b<NQ>(tmem_addr(tS + 32 * (i & 1) + 16 + ch * NHH, qd * 32, 0), sw);
       tmem_ld_wait();
       const bool valid = ixw >= 0 && ixw < Tk;
       float z[NQ];
@@ -1027,13 +1060,11 @@ __global__ void __launch_bounds__(kRingThreads, 1)
               for (int part = 0; part < 2; ++part) {
                 const uint32_t ta = tmem_addr(tO + mt * 2 * NH + part * NH + ch * NHH, qd * 32, 0);
                 uint32_t ov[NHH];
-                if constexpr (NHH == 8) tmem_ld8(ta, ov);
-                else tmem_ld16(ta, ov);
+                tmem_ld_n<NHH>(ta, ov);
                 tmem_ld_wait();
 #pragma unroll
                 for (int h = 0; h < NHH; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
-                if constexpr (NHH == 8) tmem_st8(ta, ov);
-                else tmem_st16(ta, ov);
+                tmem_st_n<NHH>(ta, ov);
               }
             }
             tmem_st_wait();
@@ -1098,13 +1129,8 @@ __global__ void __launch_bounds__(kRingThreads, 1)
       uint32_t oh[NHH], ol[NHH];
       if (ntiles > 0 && !aborted) {
         const uint32_t ta = tmem_addr(tO + mt * 2 * NH + ch * NHH, qd * 32, 0);
-        if constexpr (NHH == 8) {
-          tmem_ld8(ta, oh);
-          tmem_ld8(ta + NH, ol);
-        } else {
-          tmem_ld16(ta, oh);
-          tmem_ld16(ta + NH, ol);
-        }
+        tmem_ld_n<NHH>(ta, oh);
+        tmem_ld_n<NHH>(ta + NH, ol);
         tmem_ld_wait();
       } else {
 #pragma unroll
@@ -1143,17 +1169,20 @@ dsa_status_t launch(const void* kv, const void* q, const int32_t* idx, const int
                     int K, float scale, const float* sink, void* out, void* out_lo, float* lse, int* err,
                     cudaStream_t s) {
   const float sl2e = scale * 1.4426950408889634f;
-  if (H <= 16) {  // few heads: 16 per CTA on the MMA's N side, one CTA per SM
-    constexpr int NH = 16;
-    using F = SmemRing<DQK, NH>;
-    dsa_status_t st = configure_kernel_smem(reinterpret_cast<const void*>(sparse_mla_fwd_ring_kernel<DQK, NH>),
-                                            F::TOTAL, "configuring sparse_mla_fwd_ring_kernel");
-    if (st != DSA_OK) return st;
-    sparse_mla_fwd_ring_kernel<DQK, NH><<<dim3(T, 1), kRingThreads, F::TOTAL, s>>>(
-        reinterpret_cast<const __nv_bfloat16*>(kv), reinterpret_cast<const __nv_bfloat16*>(q), idx, len, T, Tk, H,
-        K, sl2e, sink, reinterpret_cast<__nv_bfloat16*>(out), reinterpret_cast<__nv_bfloat16*>(out_lo), lse, err,
-        wait_limit_cycles());
-    return cuda_check(cudaGetLastError(), "launching sparse_mla_fwd_ring_kernel");
+  if (H <= 16) {  // few heads: 8 or 16 per CTA on the MMA's N side, one CTA per SM
+    auto ring = [&](auto nh) -> dsa_status_t {
+      constexpr int NH = decltype(nh)::value;
+      using F = SmemRing<DQK, NH>;
+      dsa_status_t st = configure_kernel_smem(reinterpret_cast<const void*>(sparse_mla_fwd_ring_kernel<DQK, NH>),
+                                              F::TOTAL, "configuring sparse_mla_fwd_ring_kernel");
+      if (st != DSA_OK) return st;
+      sparse_mla_fwd_ring_kernel<DQK, NH><<<dim3(T, 1), kRingThreads, F::TOTAL, s>>>(
+          reinterpret_cast<const __nv_bfloat16*>(kv), reinterpret_cast<const __nv_bfloat16*>(q), idx, len, T, Tk, H,
+          K, sl2e, sink, reinterpret_cast<__nv_bfloat16*>(out), reinterpret_cast<__nv_bfloat16*>(out_lo), lse, err,
+          wait_limit_cycles());
+      return cuda_check(cudaGetLastError(), "launching sparse_mla_fwd_ring_kernel");
+    };
+    return H <= 8 ? ring(std::integral_constant<int, 8>{}) : ring(std::integral_constant<int, 16>{});
   }
   using L = Smem<DQK>;
   dsa_status_t st = configure_kernel_smem(reinterpret_cast<const void*>(sparse_mla_fwd_kernel<DQK>), L::TOTAL,

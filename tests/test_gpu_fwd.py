@@ -79,9 +79,10 @@ def test_fwd_two_head_groups_nope_topk_len_holes():
     check(q, kv, idx, 512 ** -0.5, ln=ln)
 
 
-def test_fwd_few_heads_padded_in_smem():
-    q, kv, _, idx = make_case(50, 300, 8, 512, 259, 4)
-    check(q, kv, idx, 512 ** -0.5)
+@pytest.mark.parametrize("H,D", [(8, 512), (3, 576), (12, 512)])  # 8 and 16 heads per CTA, padded in smem
+def test_fwd_few_heads_padded_in_smem(H, D):
+    q, kv, _, idx = make_case(50, 300, H, D, 259, 4)
+    check(q, kv, idx, D ** -0.5)
 
 
 def test_fwd_empty_rows_and_single_slot():
