@@ -190,3 +190,35 @@ def test_cp_ranks_through_fwd_bwd_equal_one_shot():
     pad = np.setdiff1d(np.arange(total), np.concatenate([np.arange(P[i], P[i] + lens[i]) for i in range(2)]))
     assert torch.all(one[1][torch.as_tensor(pad).to(DEV)] == 0)
     assert torch.all(one[2][torch.as_tensor(pad).to(DEV)] == 0)
+
+
+def test_indexer_cp_with_scores():
+    # the context-parallel indexer through the scored entry: the same selection as dsa_indexer_topk_cp,
+    # and each selected slot's score against the oracle's fp64 score of its own selection (rows whose
+    # selection equals the oracle's), -inf past the prefix
+    lens, pads, K = [1500, 400], [10, 3], 256
+    cu, P, total = layout(lens, pads, 6)
+    x = synth.indexer_inputs(total, 64, 128, seed=48)
+    qi = cp_split(total, 2, 1)
+    st, cl, _, _ = dsa.dsa_packed_metadata_cp(t32(cu), total, query_indices=t32(qi), cu_seqlens_padded=t32(P))
+    st_ref, cl_ref, _, _ = oracle.packed_metadata_cp(cu, total, query_indices=qi, cu_seqlens_padded=P)
+    assert np.array_equal(st.cpu().numpy(), st_ref) and np.array_equal(cl.cpu().numpy(), cl_ref)
+    qi64 = qi.astype(np.int64)
+    q, k, w = x["q_idx"][qi64].to(DEV), x["k_idx"].to(DEV), x["w"][qi64].to(DEV)
+    idx, ln, sc = dsa.dsa_indexer_topk_scored(q, k, w, st, K, causal_len=cl)
+    idx0, ln0 = dsa.dsa_indexer_topk_cp(q, k, w, st, cl, K)
+    assert torch.equal(idx, idx0) and torch.equal(ln, ln0)
+    rows = np.unique(np.concatenate([[0, 1, len(qi) // 2, len(qi) - 1],
+                                     np.random.default_rng(49).choice(len(qi), 60, replace=False)]))
+    ref_idx, ref_len, _ = oracle.indexer_topk_window(x["q_idx"][qi64[rows]], x["k_idx"], x["w"][qi64[rows]],
+                                                      st_ref[rows], cl_ref[rows], K)
+    gi, gl, gs = idx.cpu().numpy()[rows], ln.cpu().numpy()[rows], sc.cpu().double().numpy()[rows]
+    same = np.all(gi == ref_idx, axis=1) & (gl == ref_len)
+    assert same.mean() >= 0.9
+    for i in np.nonzero(same)[0]:
+        n = int(ref_len[i])
+        assert np.all(gs[i, n:] == -np.inf)
+        if n:
+            rs, mag = oracle.indexer_scores(x["q_idx"][[int(qi64[rows[i]])]], x["k_idx"], x["w"][[int(qi64[rows[i]])]],
+                                            np.zeros(n, np.int64), ref_idx[i, :n], with_magnitude=True)
+            assert np.all(np.abs(gs[i, :n] - rs) <= GAMMA * mag), f"row {rows[i]}: scores"
