@@ -75,6 +75,19 @@ def test_sink_two_head_groups_nope_topk_len():
     check(q, kv, dout, idx, 512 ** -0.5, sink_values(128, 42), ln=ln)
 
 
+def test_sink_few_heads_nope_empty_rows_and_topk_len():
+    # the few-heads forward at 8 heads per CTA (NoPE width): the sink starts the running max, an empty
+    # row has lse = sink and out = 0, prefixes of random length
+    q, kv, dout, idx = make_case(30, 500, 8, 512, 259, 45)
+    idx[3, :] = -1
+    ln = torch.randint(0, 260, (30,), generator=torch.Generator().manual_seed(45), dtype=torch.int32)
+    s = sink_values(8, 45)
+    out, lse = check(q, kv, dout, idx, 512 ** -0.5, s, ln=ln)
+    fin = torch.isfinite(s)
+    assert torch.all(out[3] == 0)
+    assert torch.allclose(lse[3].cpu()[fin], s[fin], atol=1e-6, rtol=0)
+
+
 def test_sink_dominant_and_query_chunks_accumulate():
     # sinks far above the scores take most of the mass; d_sink and dkv accumulate over query chunks
     q, kv, dout, idx = make_case(48, 500, 16, 576, 200, 43)
