@@ -106,12 +106,13 @@ def _slot_scores_fp32(q_idx, k_idx, w, idx):
     return torch.where(idx >= 0, I, torch.full_like(I, float("nan"))).float()
 
 
-@pytest.mark.parametrize("T,K,use_len", [(24, 300, False), (400, 300, True), (400, 301, False)])
-def test_kl_reading_scores_special_rows_and_many_rows_per_cta(T, K, use_len):
+@pytest.mark.parametrize("T,K,use_len,Hi", [(24, 300, False, 64), (400, 300, True, 64), (400, 301, False, 64),
+                                              (300, 300, True, 16)])
+def test_kl_reading_scores_special_rows_and_many_rows_per_cta(T, K, use_len, Hi):
     # the score-reading kernel walks several rows per CTA (T = 400 over at most one CTA per SM): rows
     # without tiles (empty, zero target) between rows with tiles, holes, one valid slot, prefixes; rows
     # of K = 300 slots start on 16-byte boundaries (vector loads), rows of K = 301 do not
-    q_idx, k_idx, w, idx, prob, ln = kl_inputs(T, 900, K, 64, 76, ln_frac=1.0 if use_len else None)
+    q_idx, k_idx, w, idx, prob, ln = kl_inputs(T, 900, K, Hi, 76, ln_frac=1.0 if use_len else None)
     idx[2, 10] = -1
     idx[4, :] = -1
     idx[6, 1:] = -1
