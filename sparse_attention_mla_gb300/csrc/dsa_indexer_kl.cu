@@ -32,7 +32,13 @@
 // TMEM buffers: the drain warps reduce one into the fp32 dk_idx accumulator
 // (red.global.add.v4.f32, 4 rows x 128 bytes per instruction after a
 // transpose through shared memory) while the workers build the next tile's
-// M'.  The roles hand over through mbarriers.
+// M'.  The roles hand over through mbarriers.  A tile's rows are gathered a
+// tile ahead, so the workers signal its landing first and issue the next
+// tile's gather while S of this one is formed.
+//
+// When the selection's own scores are given (the indexer keeps each
+// candidate's fp32 score), indexer_kl_rows_kernel reads them instead of the
+// first pass, with one CTA per SM walking the rows (see there).
 #include <cmath>
 
 #include "dsa_device.cuh"
