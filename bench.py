@@ -552,7 +552,10 @@ def run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, flops_per_step, 
             state["dkv_out"].record(cout)
 
     steps = max(1, min(args.steps, 3))
-    step()
+    # one untimed step per device input set, so that every buffer the timed steps use (both input sets,
+    # the pinned host buffers, the results) has been through a copy before the timed region
+    for _ in range(2):
+        step()
     torch.cuda.synchronize(dev)
     barrier(world)
     t0 = torch.cuda.Event(enable_timing=True)
