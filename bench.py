@@ -328,6 +328,9 @@ def run_cuda(args, rank, world, local):
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
+        # one untimed pass of the whole leg first: its 12 GB of pinned host buffers are allocated and used
+        # once (right after other large jobs on the host, the first pass's copies ran at about 2/3 speed)
+        run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, f_fwd + f_bwd, world)
         e2e = run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, f_fwd + f_bwd, world)
     cp = None if args.no_cp else run_cp_indexer(args, dsa, torch, dev, stream, ind, topk_idx, topk_len)
     kl_path = None if args.no_kl else run_kl_path(args, dsa, torch, dev, stream, ind, mla, seq_start, topk_idx,
@@ -574,7 +577,8 @@ def run_e2e(args, dsa, torch, dev, stream, ind, mla, seq_start, flops_per_step, 
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "note": "MLA fwd+bwd FLOPs over the whole step incl. indexer and host copies; query chunks of 4096 "
                     "with copies overlapping compute on two copy streams; each step copies all its inputs in "
-                    "(two device input sets used by alternate steps) and all its results out"}
+                    "(two device input sets used by alternate steps) and all its results out; measured after "
+                    "one untimed pass of the whole leg"}
 
 
 def time_workload(name, args, dev, stream) -> dict:
